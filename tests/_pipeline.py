@@ -1,0 +1,68 @@
+"""Oracle-side assembly of a decode step for a synthetic workload.
+
+Test infrastructure: drives the float64 oracle over a workload from the
+seeded generators. For a subset of sequences it builds a compact page pool
+(the sequences' pages renumbered 0..n-1), which holds the same logical
+contents as the full pool, so a sample of a large workload can be checked
+without materialising all of it on the host."""
+import numpy as np
+
+import oracle
+from paged_kv_gqa_04_gb300 import synth
+
+
+def oracle_step(w: synth.Workload, seqs=None, num_splits: int = 1):
+    """Run the oracle's cache write (context tokens, then the new token with
+    q) and decode + merge for the given sequences.
+
+    Returns dict(q_rot [n,Hq,D] uint16, k_cache, v_cache (compact pool),
+    block_tables [n, maxp], seq_lens [n], out_partial, lse_partial, out, lse)."""
+    seqs = list(range(w.B)) if seqs is None else list(seqs)
+    n = len(seqs)
+    P = w.page_size
+    npg = [int((int(w.seq_lens[b]) + P - 1) // P) for b in seqs]
+    width = max(1, max(npg) if npg else 1)
+    bt = np.full((n, width), -1, np.int32)
+    base = 0
+    for i, c in enumerate(npg):
+        bt[i, :c] = np.arange(base, base + c, dtype=np.int32)
+        base += c
+    pool = max(base, 1)
+    shape = (pool, w.Hkv, P, w.D) if w.layout == "HND" else (pool, P, w.Hkv, w.D)
+    kc = oracle.empty_cache(shape, w.cache_dtype)
+    vc = np.zeros_like(kc)
+    cs = w.cos_sin()
+    q_rot = np.zeros((n, w.Hq, w.D), np.uint16)
+    sl = np.array([int(w.seq_lens[b]) for b in seqs], np.int32)
+    for i, b in enumerate(seqs):
+        L = int(w.seq_lens[b])
+        if L == 0:
+            continue
+        k, v = w.seq_kv(b)
+        pos = np.arange(L, dtype=np.int32)
+        slots = (bt[i, pos // P].astype(np.int64) * P + pos % P).astype(np.int32)
+        # context tokens (no q) ...
+        if L > 1:
+            oracle.rope_kv_write(None, k[:L - 1], v[:L - 1], pos[:L - 1], cs, kc, vc, slots[:L - 1],
+                                 w.layout, w.style, w.k_scale, w.v_scale)
+        # ... then the new token with its q
+        q = w.seq_q(b).reshape(1, w.Hq, w.D).copy()
+        oracle.rope_kv_write(q, k[L - 1:], v[L - 1:], pos[L - 1:], cs, kc, vc, slots[L - 1:],
+                             w.layout, w.style, w.k_scale, w.v_scale)
+        q_rot[i] = q[0]
+    op, lp = oracle.paged_decode(q_rot, kc, vc, bt, sl, w.softmax_scale, num_splits, w.layout,
+                                 w.k_scale, w.v_scale)
+    out, lse = oracle.lse_merge(op, lp)
+    return dict(q_rot=q_rot, k_cache=kc, v_cache=vc, block_tables=bt, seq_lens=sl,
+                out_partial=op, lse_partial=lp, out=out, lse=lse)
+
+
+def cache_values_f64(cache: np.ndarray, cache_dtype: str) -> np.ndarray:
+    """Cache bytes as float64 through torch's own dtype views (independent of
+    the oracle's decoders)."""
+    import torch
+    if cache_dtype == "fp8":
+        t = torch.from_numpy(cache.view(np.uint8)).view(torch.float8_e4m3fn)
+    else:
+        t = torch.from_numpy(cache.view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
