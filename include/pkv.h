@@ -1,0 +1,239 @@
+/*
+ * pkv.h -- C ABI of the paged-KV GQA decode step for NVIDIA GB300 (sm_103a).
+ *
+ * One decode step of transformer attention over a paged KV cache is three
+ * calls on one CUDA stream:
+ *
+ *   pkv_rope_kv_write     rotate q and k of the new token(s) (NeoX or
+ *                         interleaved RoPE) and write k and v into the paged
+ *                         cache as bf16 or static-scale FP8 E4M3 bytes.
+ *   pkv_paged_gqa_decode  attention of each query head over the pages its
+ *                         sequence's block table names, split-K over the
+ *                         context, one partial output and LSE per split.
+ *   pkv_lse_merge         log-sum-exp merge of the split partials into the
+ *                         bf16 output.
+ *
+ * Sources of the operation (page title, section):
+ *   - Loom Kernels, "Supported operator paths" table: row "Position and KV"
+ *     (NeoX/interleaved RoPE + native/static-FP8 paged-KV write, packed QKV,
+ *     NHD/HND cache views, static per-tensor/per-head FP8 E4M3 scales) and
+ *     row "Attention" (paged MQA/GQA decode, local split-K/LSE merge).
+ *   - mainarch, decode-attention section: split-KV online softmax with a
+ *     combine of the partials, paged KV in the vLLM/SGLang sense (a block
+ *     table maps logical blocks to physical pages), GQA reading each KV head
+ *     once per group, OCP e4m3fn FP8.
+ *
+ * Conventions for every call:
+ *   - Memory. All tensor pointers are DEVICE addresses of caller-owned memory
+ *     (borrowed for the duration of the call's GPU work). The library
+ *     allocates nothing and keeps no pointer after the call returns.
+ *   - Streams. Every call only enqueues GPU work on `stream` (NULL = the
+ *     legacy default stream) and returns; results are ready when that
+ *     stream's work completes. Calls contain no host synchronisation.
+ *   - Status. The return value reports argument validation and launch
+ *     errors only: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED are returned
+ *     before anything is launched; PKV_ERR_CUDA reports a launch failure
+ *     (cudaGetLastError). Device-side problems with index VALUES (a slot,
+ *     position, page id or sequence length out of range) are not visible to
+ *     the host at call time: the kernels skip the offending element and OR a
+ *     PKV_FLAG_* bit into *err_flag (a device int32 the caller zeroes; may be
+ *     NULL). No kernel traps, asserts or faults on bad index values.
+ *   - Tensors. A pkv_tensor is a strided view: shape and strides in ELEMENTS,
+ *     outermost first. Innermost strides must be 1 where stated.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,  /* shapes, strides, dtypes or enums inconsistent   */
+    PKV_ERR_UNSUPPORTED = 2,  /* consistent but outside what the kernels handle  */
+    PKV_ERR_CUDA = 3          /* a CUDA runtime/driver call or launch failed     */
+} pkv_status;
+
+typedef enum { PKV_NHD = 0, PKV_HND = 1 } pkv_layout;
+typedef enum { PKV_ROPE_NEOX = 0, PKV_ROPE_INTERLEAVED = 1 } pkv_rope_style;
+typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1, PKV_F32 = 2, PKV_I32 = 3 } pkv_dtype;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define PKV_FLAG_SLOT_RANGE     0x01  /* slot_mapping entry >= num_pages * page_size        */
+#define PKV_FLAG_POSITION_RANGE 0x02  /* positions entry outside [0, cos_sin rows)          */
+#define PKV_FLAG_PAGE_RANGE     0x04  /* a needed block-table entry outside [0, num_pages)   */
+#define PKV_FLAG_SEQ_LEN_RANGE  0x08  /* seq_lens entry < 0 or > block-table width * 16      */
+#define PKV_FLAG_DUPLICATE_SLOT 0x10  /* two tokens of one call map to the same slot         */
+#define PKV_FLAG_WAIT_TIMEOUT   0x20  /* an in-kernel wait gave up after its time limit      */
+
+typedef struct {
+    void*   ptr;        /* device address (NULL allowed only where stated) */
+    int32_t dtype;      /* pkv_dtype                                        */
+    int32_t ndim;       /* 1..4                                             */
+    int64_t shape[4];   /* extents, outermost first                         */
+    int64_t stride[4];  /* in elements                                      */
+} pkv_tensor;
+
+/*
+ * pkv_rope_kv_write -- fused RoPE + paged-KV cache write.
+ * (Loom Kernels, "Supported operator paths", row "Position and KV";
+ *  "Evidence" table, rows "RoPE + paged-KV write" and "Static FP8 KV-cache
+ *  write"; microLLM-rocm, optimisation checkpoints: split-half RoPE and
+ *  positions-aware RoPE with a mapped KV store.)
+ *
+ * For every token t with slot_mapping[t] >= 0, with (c_i, s_i) =
+ * cos_sin[positions[t], i] and cos_sin[positions[t], D/2 + i]:
+ *   pairs (i, i + D/2) for NeoX or (2i, 2i+1) for interleaved, i < D/2:
+ *     y1 = x1*c - x2*s,  y2 = x2*c + x1*s
+ *   each product and the sum/difference rounded to float32, no fused
+ *   multiply-add. Then:
+ *   q[t]   <- bf16 round-to-nearest-even of the rotated q   (in place)
+ *   k_cache[slot] <- rotated k, v_cache[slot] <- v, each as
+ *     bf16 RNE (bf16 cache), or
+ *     E4M3(y / scale): the correctly rounded float32 quotient, then
+ *     saturating (to +-448) round-to-nearest-even OCP E4M3 (FP8 cache).
+ *   slot = page * page_size + offset.
+ *
+ * q            [T, Hq, D]  bf16, innermost stride 1, rows 16-byte aligned;
+ *              rotated IN PLACE. ptr may be NULL (cache fill without q).
+ * k, v         [T, Hkv, D] bf16, read only, same alignment rule. Strided
+ *              views of a packed QKV buffer are accepted.
+ * positions    [T] int32, contiguous.
+ * cos_sin      [max_pos, D] float32, innermost stride 1, 16-byte aligned rows:
+ *              columns [0, D/2) cos, [D/2, D) sin of frequency index i.
+ * k_cache,
+ * v_cache      NHD: [num_pages, page_size, Hkv, D]; HND: [num_pages, Hkv,
+ *              page_size, D]; dtype PKV_BF16 or PKV_FP8_E4M3 (both the same);
+ *              innermost stride 1, other strides multiples of 16 bytes.
+ * slot_mapping [T] int32; < 0 skips the token (q, k and v untouched).
+ * k_scale,
+ * v_scale      FP8 cache only: [1] (per tensor) or [Hkv] (per head) float32,
+ *              positive; ignored (ptr may be NULL) for a bf16 cache.
+ * layout       pkv_layout; rope_style pkv_rope_style.
+ * Supported: D in {64, 128}; Hq a multiple of Hkv (or q NULL).
+ * Errors: a slot >= num_pages*page_size sets PKV_FLAG_SLOT_RANGE, a position
+ * outside [0, max_pos) sets PKV_FLAG_POSITION_RANGE; that token is skipped
+ * entirely. Two tokens with the same slot: the surviving write is unspecified.
+ * q must not alias k, v or the caches; the caches must not alias k or v.
+ */
+pkv_status pkv_rope_kv_write(pkv_tensor q, pkv_tensor k, pkv_tensor v, pkv_tensor positions,
+                             pkv_tensor cos_sin, pkv_tensor k_cache, pkv_tensor v_cache,
+                             pkv_tensor slot_mapping, pkv_tensor k_scale, pkv_tensor v_scale,
+                             int32_t layout, int32_t rope_style, int32_t* err_flag,
+                             pkv_stream_t stream);
+
+/*
+ * pkv_paged_gqa_decode -- paged MQA/GQA split-K decode attention.
+ * (mainarch, decode-attention section: split-KV online softmax, paged KV
+ *  with a block table and a shuffled page layout, GQA sharing each KV head
+ *  load, FP8 KV dequantised in-kernel; Loom Kernels, "Attention" row.)
+ *
+ * For sequence b with L = seq_lens[b] (counting the new token) and
+ * npages = ceil(L / 16), split s in [0, num_splits) covers logical pages
+ * [s*pps, min((s+1)*pps, npages)), pps = ceil(npages / num_splits).
+ * Query head h reads kv head h / (Hq/Hkv). Over the tokens of the split:
+ *   score_t = softmax_scale * sum_d q[b,h,d] * K_t[d]
+ *   out_partial[b,s,h,:] = sum_t exp(score_t - m) V_t / sum_t exp(score_t - m)
+ *   lse_partial[b,s,h]   = m + ln sum_t exp(score_t - m)   (natural log)
+ * with m = max_t score_t; an empty split gives 0 and -inf. K_t, V_t are the
+ * cache values (FP8: byte * k_scale / v_scale of the kv head).
+ *
+ * q            [B, Hq, D] bf16 (already rotated), innermost stride 1.
+ * k_cache,
+ * v_cache      as for pkv_rope_kv_write; page_size must be 16; the base
+ *              address 16-byte aligned.
+ * block_tables [B, max_pages] int32, innermost stride 1; entries past a
+ *              sequence's npages are never read.
+ * seq_lens     [B] int32.
+ * softmax_scale  multiplies q.k (natural-log units).
+ * num_splits   >= 1, <= 4096 (see pkv_choose_num_splits).
+ * out_partial  [B, num_splits, Hq, D] float32, innermost stride 1.
+ * lse_partial  [B, num_splits, Hq] float32, innermost stride 1.
+ * k_scale,
+ * v_scale      as for pkv_rope_kv_write.
+ * Supported: D in {64, 128}; 1 <= Hq/Hkv <= 16.
+ * Errors: a block-table entry outside [0, num_pages) sets
+ * PKV_FLAG_PAGE_RANGE and that page is left out; seq_lens[b] < 0 or
+ * > 16*max_pages sets PKV_FLAG_SEQ_LEN_RANGE and L is clamped to [0,
+ * 16*max_pages]. Outputs must not alias inputs.
+ */
+pkv_status pkv_paged_gqa_decode(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
+                                pkv_tensor block_tables, pkv_tensor seq_lens, float softmax_scale,
+                                int32_t num_splits, pkv_tensor out_partial, pkv_tensor lse_partial,
+                                pkv_tensor k_scale, pkv_tensor v_scale, int32_t layout,
+                                int32_t* err_flag, pkv_stream_t stream);
+
+/*
+ * pkv_lse_merge -- merge of the split partials.
+ * (mainarch, decode-attention section: the combine of split-KV partials;
+ *  Loom Kernels, "Attention" row: local split-K/LSE merge.)
+ *
+ *   M = max_s lse_partial[b,s,h];  w_s = exp(lse_partial[b,s,h] - M)
+ *   out[b,h,:] = bf16_rne( sum_s w_s out_partial[b,s,h,:] / sum_s w_s )
+ *   lse_out[b,h] = M + ln sum_s w_s
+ * A row whose every split is empty gives out = 0 and lse_out = -inf.
+ *
+ * out_partial  [B, S, Hq, D] float32, innermost stride 1.
+ * lse_partial  [B, S, Hq] float32, innermost stride 1.
+ * out          [B, Hq, D] bf16, innermost stride 1.
+ * lse_out      [B, Hq] float32; ptr may be NULL.
+ * Supported: D in {64, 128}.
+ */
+pkv_status pkv_lse_merge(pkv_tensor out_partial, pkv_tensor lse_partial, pkv_tensor out,
+                         pkv_tensor lse_out, pkv_stream_t stream);
+
+/*
+ * pkv_choose_num_splits -- split count for pkv_paged_gqa_decode (host only,
+ * no GPU work). (mainarch, MLA decode section: split-K of 64 vs 8 changes the
+ * per-token time about threefold; Loom Kernels, "Evidence" table, row
+ * "Local split-K paged decode".)
+ *
+ * B, Hkv: batch and kv heads; total_pages = sum over the batch of
+ * ceil(seq_len/16); max_pages = the largest ceil(seq_len/16); cache_dtype a
+ * pkv_dtype; sm_count the device's SM count. Models each split as one CTA
+ * and returns the S in [1, 64] with the lowest estimated time for streaming
+ * the pages over the GPU's CTA slots plus the merge's extra traffic.
+ * Returns 1 for empty or invalid input.
+ */
+int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int64_t total_pages,
+                              int32_t max_pages, int32_t cache_dtype, int32_t sm_count);
+
+/*
+ * pkv_validate_indices -- device check of index values before a step.
+ * (The pages' test practice of checking every span before the GPU uses it:
+ *  mainarch, kernel ABI layer; Loom Kernels, "What Loom owns": invalid-input
+ *  behaviour is part of the contract.)
+ *
+ * Sets PKV_FLAG_SEQ_LEN_RANGE for seq_lens entries < 0 or > 16*max_pages,
+ * PKV_FLAG_PAGE_RANGE for block-table entries a sequence needs that are
+ * outside [0, num_pages), PKV_FLAG_SLOT_RANGE for slot_mapping entries >=
+ * num_pages*16 and, when slot_bitmap is given, PKV_FLAG_DUPLICATE_SLOT if
+ * two non-negative slot_mapping entries are equal.
+ * block_tables [B, max_pages] int32; seq_lens [B] int32; slot_mapping [T]
+ * int32 (ptr may be NULL to skip slot checks); slot_bitmap: caller-provided
+ * device scratch of ceil(num_pages*16/32) int32 words, which this call
+ * zeroes and then uses (ptr may be NULL to skip the duplicate check).
+ * err_flag must be non-NULL.
+ */
+pkv_status pkv_validate_indices(pkv_tensor block_tables, pkv_tensor seq_lens,
+                                pkv_tensor slot_mapping, int64_t num_pages,
+                                pkv_tensor slot_bitmap, int32_t* err_flag, pkv_stream_t stream);
+
+/* Static description of a status code. */
+const char* pkv_status_string(int32_t status);
+
+/* ABI version of this header (bumped on any signature change). */
+int32_t pkv_abi_version(void);
+#define PKV_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

@@ -1,0 +1,158 @@
+"""Thin ctypes binding of the C ABI in include/pkv.h (libpkv.so).
+
+Argument marshalling only: each function turns torch tensors into pkv_tensor
+descriptors (pointer, dtype, shape, strides) and calls the library on the
+current CUDA stream. Every step of the computation runs in the library's CUDA
+kernels; there is no Python or CPU implementation behind these names, and a
+missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA = 0, 1, 2, 3
+LAYOUTS = {"NHD": 0, "HND": 1}
+STYLES = {"neox": 0, "interleaved": 1}
+FLAG_SLOT_RANGE = 0x01
+FLAG_POSITION_RANGE = 0x02
+FLAG_PAGE_RANGE = 0x04
+FLAG_SEQ_LEN_RANGE = 0x08
+FLAG_DUPLICATE_SLOT = 0x10
+FLAG_WAIT_TIMEOUT = 0x20
+
+_DTYPES = {
+    torch.bfloat16: 0,
+    torch.float8_e4m3fn: 1,
+    torch.uint8: 1,
+    torch.float32: 2,
+    torch.int32: 3,
+}
+
+EXPORTED = ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_choose_num_splits",
+            "pkv_validate_indices", "pkv_status_string", "pkv_abi_version")
+
+
+class PkvTensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library {LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        T = PkvTensor
+        P = ctypes.c_void_p
+        i32 = ctypes.c_int32
+        L.pkv_rope_kv_write.argtypes = [T, T, T, T, T, T, T, T, T, T, i32, i32, P, P]
+        L.pkv_paged_gqa_decode.argtypes = [T, T, T, T, T, ctypes.c_float, i32, T, T, T, T, i32, P, P]
+        L.pkv_lse_merge.argtypes = [T, T, T, T, P]
+        L.pkv_choose_num_splits.argtypes = [i32, i32, i32, i32, ctypes.c_int64, i32, i32, i32]
+        L.pkv_validate_indices.argtypes = [T, T, T, ctypes.c_int64, T, P, P]
+        L.pkv_status_string.argtypes = [i32]
+        L.pkv_status_string.restype = ctypes.c_char_p
+        for name in ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_validate_indices",
+                     "pkv_choose_num_splits", "pkv_abi_version"):
+            getattr(L, name).restype = ctypes.c_int32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pkv_status_string(int(status)).decode()
+
+
+def _desc(t: Optional[torch.Tensor]) -> PkvTensor:
+    d = PkvTensor()
+    if t is None:
+        return d
+    if t.dim() > 4:
+        raise ValueError("tensors of more than 4 dims are not part of the ABI")
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"dtype {t.dtype} is not part of the ABI")
+    if t.numel() and not t.is_cuda:
+        raise ValueError("the C ABI takes device tensors; copy host data to the GPU first")
+    d.ptr = t.data_ptr() if t.numel() else None
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i, (n, s) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = n
+        d.stride[i] = s
+    return d
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != PKV_OK:
+        raise PkvError(fn, status)
+
+
+def rope_kv_write(q, k, v, positions, cos_sin, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,
+                  layout: str = "HND", rope_style: str = "neox", err_flag=None, stream=None) -> None:
+    """Fused RoPE + paged-KV write (pkv_rope_kv_write): q (or None) rotated
+    in place, rotated k and v written into the caches at slot_mapping."""
+    _check("pkv_rope_kv_write", lib().pkv_rope_kv_write(
+        _desc(q), _desc(k), _desc(v), _desc(positions), _desc(cos_sin), _desc(k_cache), _desc(v_cache),
+        _desc(slot_mapping), _desc(k_scale), _desc(v_scale), LAYOUTS[layout], STYLES[rope_style],
+        _ptr(err_flag), _stream(stream)))
+
+
+def paged_gqa_decode(q, k_cache, v_cache, block_tables, seq_lens, softmax_scale: float, num_splits: int,
+                     out_partial, lse_partial, k_scale=None, v_scale=None, layout: str = "HND", err_flag=None,
+                     stream=None) -> None:
+    """Paged GQA split-K decode (pkv_paged_gqa_decode) into out_partial
+    [B,S,Hq,D] and lse_partial [B,S,Hq]."""
+    _check("pkv_paged_gqa_decode", lib().pkv_paged_gqa_decode(
+        _desc(q), _desc(k_cache), _desc(v_cache), _desc(block_tables), _desc(seq_lens), float(softmax_scale),
+        int(num_splits), _desc(out_partial), _desc(lse_partial), _desc(k_scale), _desc(v_scale), LAYOUTS[layout],
+        _ptr(err_flag), _stream(stream)))
+
+
+def lse_merge(out_partial, lse_partial, out, lse_out=None, stream=None) -> None:
+    """LSE merge of the split partials into out [B,Hq,D] bf16 (pkv_lse_merge)."""
+    _check("pkv_lse_merge", lib().pkv_lse_merge(_desc(out_partial), _desc(lse_partial), _desc(out),
+                                                 _desc(lse_out), _stream(stream)))
+
+
+def choose_num_splits(B: int, Hkv: int, Hq: int, D: int, total_pages: int, max_pages: int, cache_dtype: str,
+                      sm_count: int) -> int:
+    """Split count from the library's heuristic (host only)."""
+    return int(lib().pkv_choose_num_splits(B, Hkv, Hq, D, int(total_pages), max_pages,
+                                           1 if cache_dtype == "fp8" else 0, sm_count))
+
+
+def validate_indices(block_tables, seq_lens, slot_mapping, num_pages: int, err_flag, slot_bitmap=None,
+                     stream=None) -> None:
+    """Device check of seq_lens, block tables and slots (pkv_validate_indices)."""
+    _check("pkv_validate_indices", lib().pkv_validate_indices(
+        _desc(block_tables), _desc(seq_lens), _desc(slot_mapping), int(num_pages), _desc(slot_bitmap),
+        _ptr(err_flag), _stream(stream)))

@@ -1,0 +1,94 @@
+// lse_merge.cu -- log-sum-exp merge of split-K decode partials.
+//
+// mainarch, decode-attention section: the split-KV partials are combined by
+// their log-sum-exp weights; Loom Kernels, "Attention" row: local
+// split-K/LSE merge.
+//
+// One warp per (sequence, query head) row. The warp reads the row's S LSE
+// values, forms M = max and the weights w_s = exp(lse_s - M), then each lane
+// accumulates D/32 consecutive output columns over the S partial rows with
+// 8- or 16-byte loads (a partial row of D floats is one fully coalesced
+// 256/512-byte read), divides by sum w_s and writes bf16 (round to nearest
+// even) plus lse = M + ln sum w_s.
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarps = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs a) {
+    constexpr int V = D / 32;  // columns per lane
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    if (row >= static_cast<int64_t>(a.B) * a.Hq) return;
+    const int b = static_cast<int>(row / a.Hq);
+    const int h = static_cast<int>(row % a.Hq);
+    const float* lse = a.lse_partial + b * a.lp_s0 + h;
+
+    float m = -INFINITY;
+    for (int s = lane; s < a.S; s += 32) m = fmaxf(m, __ldg(lse + s * a.lp_s1));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+        const float* op = a.out_partial + b * a.op_s0 + h * a.op_s2 + lane * V;
+        for (int s0 = 0; s0 < a.S; s0 += 32) {
+            const int s = s0 + lane;
+            const float w_mine = (s < a.S) ? __expf(__ldg(lse + s * a.lp_s1) - m) : 0.f;
+            wsum += w_mine;
+            const int n = min(32, a.S - s0);
+            for (int j = 0; j < n; ++j) {
+                const float w = __shfl_sync(0xffffffffu, w_mine, j);
+                const float* src = op + (s0 + j) * a.op_s1;
+                if constexpr (V == 4) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+                    acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+                } else {
+                    const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+                    acc[0] += w * x.x; acc[1] += w * x.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+        const float inv = 1.f / wsum;
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] *= inv;
+    }
+    uint16_t* dst = a.out + b * a.o_s0 + h * a.o_s1 + lane * V;
+    if constexpr (V == 4) {
+        uint2 w;
+        w.x = pack_bf16(acc[0], acc[1]);
+        w.y = pack_bf16(acc[2], acc[3]);
+        *reinterpret_cast<uint2*>(dst) = w;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
+    }
+    if (a.lse_out && lane == 0)
+        a.lse_out[b * a.lo_s0 + h * a.lo_s1] = (m == -INFINITY) ? -INFINITY : m + __logf(wsum);
+}
+
+}  // namespace
+
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(a.B) * a.Hq;
+    if (rows == 0) return cudaSuccess;
+    const int64_t blocks = (rows + kWarps - 1) / kWarps;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    if (a.D == 128)
+        lse_merge_kernel<128><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(a);
+    else if (a.D == 64)
+        lse_merge_kernel<64><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(a);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,401 @@
+// pkv_abi.cu -- the C ABI: argument validation, TMA descriptors, launches.
+//
+// Loom Kernels, "Architecture": every operator checks the exact contract
+// (dtypes, shapes, layouts, aliasing) at the boundary and either accepts it
+// or returns an error; there is no fallback path. Nothing here allocates
+// device memory or synchronises the host.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+using pkv::kPageSize;
+
+namespace {
+
+int elem_bytes(int32_t dtype) {
+    switch (dtype) {
+        case PKV_BF16: return 2;
+        case PKV_FP8_E4M3: return 1;
+        case PKV_F32: return 4;
+        case PKV_I32: return 4;
+        default: return 0;
+    }
+}
+
+bool shape_ok(const pkv_tensor& t, int ndim, int32_t dtype) {
+    if (t.ndim != ndim || t.dtype != dtype) return false;
+    for (int i = 0; i < ndim; ++i)
+        if (t.shape[i] < 0) return false;
+    return true;
+}
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+// Strides of the given dims, in bytes, multiples of `n`.
+bool strides_multiple(const pkv_tensor& t, int upto, int64_t n) {
+    const int e = elem_bytes(t.dtype);
+    for (int i = 0; i < upto; ++i)
+        if ((t.stride[i] * e) % n != 0) return false;
+    return true;
+}
+
+pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Tile map over a cache tensor [pages, a, b, D] (NHD: a = P, b = Hkv; HND:
+// a = Hkv, b = P). One box = 16 token rows of one kv head x (128 or 64
+// bytes of the head dim), swizzled to the same span.
+bool make_cache_map(CUtensorMap* m, const pkv_tensor& c, int32_t layout) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const int e = elem_bytes(c.dtype);
+    const int D = static_cast<int>(c.shape[3]);
+    const int row = D * e;
+    const int boxb = row >= 128 ? 128 : row;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(c.shape[2]),
+                          static_cast<cuuint64_t>(c.shape[1]), static_cast<cuuint64_t>(c.shape[0])};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(c.stride[2] * e), static_cast<cuuint64_t>(c.stride[1] * e),
+                             static_cast<cuuint64_t>(c.stride[0] * e)};
+    cuuint32_t box[4];
+    box[0] = static_cast<cuuint32_t>(boxb / e);
+    box[1] = layout == PKV_HND ? kPageSize : 1;
+    box[2] = layout == PKV_HND ? 1 : kPageSize;
+    box[3] = 1;
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                     c.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     boxb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Common checks of a cache pair. Returns PKV_OK and fills the dims.
+pkv_status check_caches(const pkv_tensor& kc, const pkv_tensor& vc, int32_t layout, int64_t* num_pages,
+                        int* P, int* Hkv, int* D) {
+    if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
+    if (kc.ndim != 4 || vc.ndim != 4 || kc.dtype != vc.dtype) return PKV_ERR_INVALID_ARG;
+    if (kc.dtype != PKV_BF16 && kc.dtype != PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i)
+        if (kc.shape[i] != vc.shape[i] || kc.shape[i] < 0) return PKV_ERR_INVALID_ARG;
+    if (!kc.ptr || !vc.ptr) return PKV_ERR_INVALID_ARG;
+    *num_pages = kc.shape[0];
+    *P = static_cast<int>(layout == PKV_HND ? kc.shape[2] : kc.shape[1]);
+    *Hkv = static_cast<int>(layout == PKV_HND ? kc.shape[1] : kc.shape[2]);
+    *D = static_cast<int>(kc.shape[3]);
+    if (*num_pages < 1 || *P < 1 || *Hkv < 1) return PKV_ERR_INVALID_ARG;
+    if (kc.stride[3] != 1 || vc.stride[3] != 1) return PKV_ERR_UNSUPPORTED;
+    if (*D != 64 && *D != 128) return PKV_ERR_UNSUPPORTED;
+    if (!strides_multiple(kc, 3, 16) || !strides_multiple(vc, 3, 16)) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(kc.ptr, 16) || !aligned(vc.ptr, 16)) return PKV_ERR_UNSUPPORTED;
+    if (*num_pages > 0x7FFFFFFF / 16) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+pkv_status check_scales(const pkv_tensor& ks, const pkv_tensor& vs, int Hkv, int* n_scale) {
+    if (!ks.ptr || !vs.ptr) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(ks, 1, PKV_F32) || !shape_ok(vs, 1, PKV_F32)) return PKV_ERR_INVALID_ARG;
+    if (ks.shape[0] != vs.shape[0]) return PKV_ERR_INVALID_ARG;
+    if (ks.shape[0] != 1 && ks.shape[0] != Hkv) return PKV_ERR_INVALID_ARG;
+    if (ks.stride[0] != 1 || vs.stride[0] != 1) return PKV_ERR_INVALID_ARG;
+    *n_scale = static_cast<int>(ks.shape[0]);
+    return PKV_OK;
+}
+
+// bf16 rows read with 16-byte vectors: innermost stride 1, other strides and
+// the base 16-byte aligned.
+bool row16(const pkv_tensor& t, int outer) {
+    return t.stride[outer] == 1 && aligned(t.ptr, 16) && strides_multiple(t, outer, 16);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+const char* pkv_status_string(int32_t status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument (shape, stride, dtype or enum)";
+        case PKV_ERR_UNSUPPORTED: return "unsupported configuration (head dim, group size, page size or alignment)";
+        case PKV_ERR_CUDA: return "CUDA launch or driver call failed";
+        default: return "unknown status";
+    }
+}
+
+pkv_status pkv_rope_kv_write(pkv_tensor q, pkv_tensor k, pkv_tensor v, pkv_tensor positions, pkv_tensor cos_sin,
+                             pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor slot_mapping, pkv_tensor k_scale,
+                             pkv_tensor v_scale, int32_t layout, int32_t rope_style, int32_t* err_flag,
+                             pkv_stream_t stream) {
+    if (rope_style != PKV_ROPE_NEOX && rope_style != PKV_ROPE_INTERLEAVED) return PKV_ERR_INVALID_ARG;
+    int64_t num_pages;
+    int P, Hkv, D;
+    pkv_status st = check_caches(k_cache, v_cache, layout, &num_pages, &P, &Hkv, &D);
+    if (st != PKV_OK) return st;
+    if (!shape_ok(k, 3, PKV_BF16) || !shape_ok(v, 3, PKV_BF16)) return PKV_ERR_INVALID_ARG;
+    const int64_t T = k.shape[0];
+    if (k.shape[1] != Hkv || k.shape[2] != D || v.shape[0] != T || v.shape[1] != Hkv || v.shape[2] != D)
+        return PKV_ERR_INVALID_ARG;
+    int Hq = 0;
+    if (q.ptr) {
+        if (!shape_ok(q, 3, PKV_BF16) || q.shape[0] != T || q.shape[2] != D) return PKV_ERR_INVALID_ARG;
+        Hq = static_cast<int>(q.shape[1]);
+        if (Hq < 1 || Hq % Hkv != 0) return PKV_ERR_INVALID_ARG;
+    }
+    if (!shape_ok(positions, 1, PKV_I32) || !shape_ok(slot_mapping, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;
+    if (positions.shape[0] != T || slot_mapping.shape[0] != T) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(cos_sin, 2, PKV_F32) || cos_sin.shape[1] != D || cos_sin.shape[0] < 1) return PKV_ERR_INVALID_ARG;
+    const bool fp8 = k_cache.dtype == PKV_FP8_E4M3;
+    int n_scale = 0;
+    if (fp8) {
+        st = check_scales(k_scale, v_scale, Hkv, &n_scale);
+        if (st != PKV_OK) return st;
+    }
+    if (T == 0) return PKV_OK;
+    if (!k.ptr || !v.ptr || !positions.ptr || !slot_mapping.ptr || !cos_sin.ptr) return PKV_ERR_INVALID_ARG;
+    if (positions.stride[0] != 1 || slot_mapping.stride[0] != 1) return PKV_ERR_UNSUPPORTED;
+    if (!row16(k, 2) || !row16(v, 2) || (q.ptr && !row16(q, 2))) return PKV_ERR_UNSUPPORTED;
+    if (!row16(cos_sin, 1)) return PKV_ERR_UNSUPPORTED;
+
+    pkv::RopeArgs a{};
+    a.q = static_cast<uint16_t*>(q.ptr);
+    a.q_s0 = q.ptr ? q.stride[0] : 0;
+    a.q_s1 = q.ptr ? q.stride[1] : 0;
+    a.k = static_cast<const uint16_t*>(k.ptr);
+    a.k_s0 = k.stride[0];
+    a.k_s1 = k.stride[1];
+    a.v = static_cast<const uint16_t*>(v.ptr);
+    a.v_s0 = v.stride[0];
+    a.v_s1 = v.stride[1];
+    a.positions = static_cast<const int32_t*>(positions.ptr);
+    a.slots = static_cast<const int32_t*>(slot_mapping.ptr);
+    a.cos_sin = static_cast<const float*>(cos_sin.ptr);
+    a.cs_s0 = cos_sin.stride[0];
+    a.max_pos = cos_sin.shape[0];
+    a.k_cache = k_cache.ptr;
+    a.v_cache = v_cache.ptr;
+    for (int i = 0; i < 4; ++i) {
+        a.kc_s[i] = k_cache.stride[i];
+        a.vc_s[i] = v_cache.stride[i];
+    }
+    a.num_pages = num_pages;
+    a.page_size = P;
+    a.layout = layout;
+    a.k_scale = fp8 ? static_cast<const float*>(k_scale.ptr) : nullptr;
+    a.v_scale = fp8 ? static_cast<const float*>(v_scale.ptr) : nullptr;
+    a.n_scale = n_scale;
+    a.T = T;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.interleaved = rope_style == PKV_ROPE_INTERLEAVED;
+    a.fp8 = fp8;
+    a.err = err_flag;
+    return cuda_status(pkv::launch_rope_kv_write(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_gqa_decode(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor block_tables,
+                                pkv_tensor seq_lens, float softmax_scale, int32_t num_splits, pkv_tensor out_partial,
+                                pkv_tensor lse_partial, pkv_tensor k_scale, pkv_tensor v_scale, int32_t layout,
+                                int32_t* err_flag, pkv_stream_t stream) {
+    int64_t num_pages;
+    int P, Hkv, D;
+    pkv_status st = check_caches(k_cache, v_cache, layout, &num_pages, &P, &Hkv, &D);
+    if (st != PKV_OK) return st;
+    if (!shape_ok(q, 3, PKV_BF16) || q.shape[2] != D) return PKV_ERR_INVALID_ARG;
+    const int64_t B = q.shape[0];
+    const int64_t Hq = q.shape[1];
+    if (Hq < 1 || Hq % Hkv != 0) return PKV_ERR_INVALID_ARG;
+    if (num_splits < 1) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(block_tables, 2, PKV_I32) || block_tables.shape[0] != B) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(seq_lens, 1, PKV_I32) || seq_lens.shape[0] != B) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(out_partial, 4, PKV_F32) || out_partial.shape[0] != B || out_partial.shape[1] != num_splits ||
+        out_partial.shape[2] != Hq || out_partial.shape[3] != D)
+        return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(lse_partial, 3, PKV_F32) || lse_partial.shape[0] != B || lse_partial.shape[1] != num_splits ||
+        lse_partial.shape[2] != Hq)
+        return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARG;
+    const bool fp8 = k_cache.dtype == PKV_FP8_E4M3;
+    int n_scale = 0;
+    if (fp8) {
+        st = check_scales(k_scale, v_scale, Hkv, &n_scale);
+        if (st != PKV_OK) return st;
+    }
+    const int64_t G = Hq / Hkv;
+    if (P != kPageSize) return PKV_ERR_UNSUPPORTED;
+    if (G > 16) return PKV_ERR_UNSUPPORTED;
+    if (num_splits > 4096 || B > 65535 || Hkv > 65535) return PKV_ERR_UNSUPPORTED;
+    if (B == 0) return PKV_OK;
+    if (!q.ptr || !block_tables.ptr || !seq_lens.ptr || !out_partial.ptr || !lse_partial.ptr)
+        return PKV_ERR_INVALID_ARG;
+    const int64_t max_pages = block_tables.shape[1];
+    if (max_pages < 1) return PKV_ERR_INVALID_ARG;
+    if (max_pages > (int64_t{1} << 26)) return PKV_ERR_UNSUPPORTED;
+    if (q.stride[2] != 1 || !aligned(q.ptr, 4) || (q.stride[0] % 2) || (q.stride[1] % 2)) return PKV_ERR_UNSUPPORTED;
+    if (block_tables.stride[1] != 1 || seq_lens.stride[0] != 1) return PKV_ERR_UNSUPPORTED;
+    if (out_partial.stride[3] != 1 || lse_partial.stride[2] != 1) return PKV_ERR_UNSUPPORTED;
+
+    CUtensorMap tk, tv;
+    if (!make_cache_map(&tk, k_cache, layout) || !make_cache_map(&tv, v_cache, layout)) return PKV_ERR_CUDA;
+
+    pkv::DecodeArgs a{};
+    a.q = static_cast<const uint16_t*>(q.ptr);
+    a.q_s0 = q.stride[0];
+    a.q_s1 = q.stride[1];
+    a.block_tables = static_cast<const int32_t*>(block_tables.ptr);
+    a.bt_s0 = block_tables.stride[0];
+    a.max_pages = static_cast<int32_t>(max_pages);
+    a.seq_lens = static_cast<const int32_t*>(seq_lens.ptr);
+    a.num_pages = num_pages;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.k_scale = fp8 ? static_cast<const float*>(k_scale.ptr) : nullptr;
+    a.v_scale = fp8 ? static_cast<const float*>(v_scale.ptr) : nullptr;
+    a.n_scale = n_scale;
+    a.num_splits = num_splits;
+    a.out_partial = static_cast<float*>(out_partial.ptr);
+    a.op_s0 = out_partial.stride[0];
+    a.op_s1 = out_partial.stride[1];
+    a.op_s2 = out_partial.stride[2];
+    a.lse_partial = static_cast<float*>(lse_partial.ptr);
+    a.lp_s0 = lse_partial.stride[0];
+    a.lp_s1 = lse_partial.stride[1];
+    a.B = static_cast<int32_t>(B);
+    a.Hq = static_cast<int32_t>(Hq);
+    a.Hkv = Hkv;
+    a.D = D;
+    a.G = static_cast<int32_t>(G);
+    a.fp8 = fp8;
+    a.layout = layout;
+    a.err = err_flag;
+    return cuda_status(pkv::launch_paged_decode(a, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_lse_merge(pkv_tensor out_partial, pkv_tensor lse_partial, pkv_tensor out, pkv_tensor lse_out,
+                         pkv_stream_t stream) {
+    if (!shape_ok(out_partial, 4, PKV_F32)) return PKV_ERR_INVALID_ARG;
+    const int64_t B = out_partial.shape[0], S = out_partial.shape[1], Hq = out_partial.shape[2],
+                  D = out_partial.shape[3];
+    if (!shape_ok(lse_partial, 3, PKV_F32) || lse_partial.shape[0] != B || lse_partial.shape[1] != S ||
+        lse_partial.shape[2] != Hq)
+        return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(out, 3, PKV_BF16) || out.shape[0] != B || out.shape[1] != Hq || out.shape[2] != D)
+        return PKV_ERR_INVALID_ARG;
+    if (lse_out.ptr && (!shape_ok(lse_out, 2, PKV_F32) || lse_out.shape[0] != B || lse_out.shape[1] != Hq))
+        return PKV_ERR_INVALID_ARG;
+    if (S < 1) return PKV_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
+    if (B * Hq == 0) return PKV_OK;
+    if (!out_partial.ptr || !lse_partial.ptr || !out.ptr) return PKV_ERR_INVALID_ARG;
+    if (out_partial.stride[3] != 1 || lse_partial.stride[2] != 1 || out.stride[2] != 1) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(out_partial.ptr, 16) || !strides_multiple(out_partial, 3, 16)) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(out.ptr, 8) || !strides_multiple(out, 2, 8)) return PKV_ERR_UNSUPPORTED;
+    if (S > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+
+    pkv::MergeArgs a{};
+    a.out_partial = static_cast<const float*>(out_partial.ptr);
+    a.op_s0 = out_partial.stride[0];
+    a.op_s1 = out_partial.stride[1];
+    a.op_s2 = out_partial.stride[2];
+    a.lse_partial = static_cast<const float*>(lse_partial.ptr);
+    a.lp_s0 = lse_partial.stride[0];
+    a.lp_s1 = lse_partial.stride[1];
+    a.out = static_cast<uint16_t*>(out.ptr);
+    a.o_s0 = out.stride[0];
+    a.o_s1 = out.stride[1];
+    a.lse_out = static_cast<float*>(lse_out.ptr);
+    a.lo_s0 = lse_out.ptr ? lse_out.stride[0] : 0;
+    a.lo_s1 = lse_out.ptr ? lse_out.stride[1] : 0;
+    a.B = static_cast<int32_t>(B);
+    a.S = static_cast<int32_t>(S);
+    a.Hq = static_cast<int32_t>(Hq);
+    a.D = static_cast<int32_t>(D);
+    return cuda_status(pkv::launch_lse_merge(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int64_t total_pages,
+                              int32_t max_pages, int32_t cache_dtype, int32_t sm_count) {
+    if (B <= 0 || Hkv <= 0 || Hq <= 0 || D <= 0 || total_pages <= 0 || max_pages <= 0 || sm_count <= 0) return 1;
+    const int e = cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
+    const double page_bytes = 2.0 * kPageSize * D * e;              // K + V of one page, one kv head
+    const double slots = static_cast<double>(sm_count) * pkv::decode_ctas_per_sm(D, cache_dtype == PKV_FP8_E4M3);
+    const double c0 = 32768.0 / page_bytes;                          // per-CTA start-up, in pages
+    const double units = static_cast<double>(B) * Hkv;
+    const double work = static_cast<double>(Hkv) * static_cast<double>(total_pages);
+    int best = 1;
+    double best_cost = 1e300;
+    for (int S = 1; S <= 64; ++S) {
+        if (S > max_pages) break;
+        const double ncta = units * S;
+        const double longest = std::ceil(static_cast<double>(max_pages) / S) + c0;
+        const double total = work + ncta * c0;
+        double est = std::fmax(total / slots, longest);
+        if (ncta > slots) est = std::fmax(est, std::ceil(ncta / slots) * (total / ncta));
+        // partial records written by the decode and read by the merge
+        const double merge_bytes = 2.0 * B * S * static_cast<double>(Hq) * (D + 1) * 4.0;
+        const double cost = est + merge_bytes / (page_bytes * slots);
+        if (cost < best_cost * (1.0 - 1e-9)) {
+            best_cost = cost;
+            best = S;
+        }
+    }
+    return best;
+}
+
+pkv_status pkv_validate_indices(pkv_tensor block_tables, pkv_tensor seq_lens, pkv_tensor slot_mapping,
+                                int64_t num_pages, pkv_tensor slot_bitmap, int32_t* err_flag, pkv_stream_t stream) {
+    if (!err_flag) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(block_tables, 2, PKV_I32) || !shape_ok(seq_lens, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;
+    if (seq_lens.shape[0] != block_tables.shape[0]) return PKV_ERR_INVALID_ARG;
+    if (num_pages < 0) return PKV_ERR_INVALID_ARG;
+    if (num_pages > 0x7FFFFFFF / kPageSize) return PKV_ERR_UNSUPPORTED;
+    pkv::ValidateArgs a{};
+    if (slot_mapping.ptr) {
+        if (!shape_ok(slot_mapping, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;
+        a.slots = static_cast<const int32_t*>(slot_mapping.ptr);
+        a.sm_s0 = slot_mapping.stride[0];
+        a.T = slot_mapping.shape[0];
+    }
+    if (slot_bitmap.ptr) {
+        if (!shape_ok(slot_bitmap, 1, PKV_I32) || slot_bitmap.stride[0] != 1) return PKV_ERR_INVALID_ARG;
+        const int64_t words = (num_pages * kPageSize + 31) / 32;
+        if (slot_bitmap.shape[0] < words) return PKV_ERR_INVALID_ARG;
+        a.bitmap = static_cast<uint32_t*>(slot_bitmap.ptr);
+        a.bitmap_words = words;
+    }
+    if (block_tables.shape[0] > 0x7FFFFFFF / 32 || block_tables.shape[1] > (int64_t{1} << 26))
+        return PKV_ERR_UNSUPPORTED;
+    if (block_tables.shape[0] > 0 && (!block_tables.ptr || !seq_lens.ptr)) return PKV_ERR_INVALID_ARG;
+    a.block_tables = static_cast<const int32_t*>(block_tables.ptr);
+    a.bt_s0 = block_tables.stride[0];
+    a.bt_s1 = block_tables.stride[1];
+    a.max_pages = static_cast<int32_t>(block_tables.shape[1]);
+    a.seq_lens = static_cast<const int32_t*>(seq_lens.ptr);
+    a.sl_s0 = seq_lens.stride[0];
+    a.B = static_cast<int32_t>(block_tables.shape[0]);
+    a.num_pages = num_pages;
+    a.err = err_flag;
+    return cuda_status(pkv::launch_validate(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

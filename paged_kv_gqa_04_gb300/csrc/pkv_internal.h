@@ -1,0 +1,106 @@
+// pkv_internal.h -- argument blocks passed from the C-ABI layer (pkv_abi.cu)
+// to the kernel launchers. Host and device code both include this header.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr int kPageSize = 16;  // tokens per page for the decode kernel
+
+struct RopeArgs {
+    uint16_t* q;               // bf16 bits, may be null
+    int64_t q_s0, q_s1;        // element strides (token, head)
+    const uint16_t* k;
+    int64_t k_s0, k_s1;
+    const uint16_t* v;
+    int64_t v_s0, v_s1;
+    const int32_t* positions;
+    const int32_t* slots;
+    const float* cos_sin;
+    int64_t cs_s0;             // row stride (elements)
+    int64_t max_pos;
+    void* k_cache;
+    void* v_cache;
+    int64_t kc_s[4];           // element strides of the 4 cache dims, tensor order
+    int64_t vc_s[4];
+    int64_t num_pages;
+    int32_t page_size;
+    int32_t layout;            // pkv_layout
+    const float* k_scale;      // fp8 only
+    const float* v_scale;
+    int32_t n_scale;           // 1 or Hkv
+    int64_t T;
+    int32_t Hq;                // 0 when q is null
+    int32_t Hkv;
+    int32_t D;
+    int32_t interleaved;
+    int32_t fp8;
+    int32_t* err;
+};
+
+struct DecodeArgs {
+    const uint16_t* q;         // [B, Hq, D] bf16 bits
+    int64_t q_s0, q_s1;
+    const int32_t* block_tables;
+    int64_t bt_s0;
+    int32_t max_pages;
+    const int32_t* seq_lens;
+    int64_t num_pages;
+    float scale_log2;          // softmax_scale * log2(e)
+    const float* k_scale;      // fp8 only
+    const float* v_scale;
+    int32_t n_scale;
+    int32_t num_splits;
+    float* out_partial;
+    int64_t op_s0, op_s1, op_s2;
+    float* lse_partial;
+    int64_t lp_s0, lp_s1;
+    int32_t B, Hq, Hkv, D, G;
+    int32_t fp8;
+    int32_t layout;            // pkv_layout (selects the TMA coordinate order)
+    int32_t* err;
+};
+
+struct MergeArgs {
+    const float* out_partial;
+    int64_t op_s0, op_s1, op_s2;
+    const float* lse_partial;
+    int64_t lp_s0, lp_s1;
+    uint16_t* out;             // bf16 bits
+    int64_t o_s0, o_s1;
+    float* lse_out;            // may be null
+    int64_t lo_s0, lo_s1;
+    int32_t B, S, Hq, D;
+};
+
+struct ValidateArgs {
+    const int32_t* block_tables;
+    int64_t bt_s0, bt_s1;
+    int32_t max_pages;
+    const int32_t* seq_lens;
+    int64_t sl_s0;
+    int32_t B;
+    const int32_t* slots;      // may be null
+    int64_t sm_s0;
+    int64_t T;
+    int64_t num_pages;
+    uint32_t* bitmap;          // may be null
+    int64_t bitmap_words;
+    int32_t* err;
+};
+
+cudaError_t launch_rope_kv_write(const RopeArgs& a, cudaStream_t s);
+cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                cudaStream_t s);
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s);
+cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s);
+
+// Occupancy-related constants of the decode kernel, shared with the split
+// heuristic on the host.
+int decode_ctas_per_sm(int D, int fp8);
+
+}  // namespace pkv

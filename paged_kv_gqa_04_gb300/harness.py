@@ -1,0 +1,133 @@
+"""Device-side setup and execution of a synthetic decode workload.
+
+Allocates the paged caches and the step's buffers on the GPU, uploads the
+seeded inputs from ``synth``, fills the cache with the context tokens through
+the library's own cache-write call, and runs one decode step (cache write of
+the new token, paged GQA decode, LSE merge) through the C ABI. Used by the
+GPU tests, the smoke check and the benchmark; it computes nothing itself.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _abi, synth
+
+
+def _u16_to_bf16(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+class DeviceWorkload:
+    """Caches, metadata and step buffers of one workload on one GPU."""
+
+    def __init__(self, w: synth.Workload, device: str = "cuda", num_splits: Optional[int] = None):
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        cache_dtype = torch.uint8 if w.cache_dtype == "fp8" else torch.bfloat16
+        self.k_cache = torch.zeros(w.cache_shape(), dtype=cache_dtype, device=dev)
+        self.v_cache = torch.zeros(w.cache_shape(), dtype=cache_dtype, device=dev)
+        self.cos_sin = torch.from_numpy(w.cos_sin()).to(dev)
+        self.block_tables = torch.from_numpy(w.block_tables).to(dev)
+        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+        self.k_scale = None if w.k_scale is None else torch.from_numpy(w.k_scale).to(dev)
+        self.v_scale = None if w.v_scale is None else torch.from_numpy(w.v_scale).to(dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        if num_splits is None:
+            props = torch.cuda.get_device_properties(dev)
+            num_splits = _abi.choose_num_splits(w.B, w.Hkv, w.Hq, w.D, int(w.pages_per_seq.sum()),
+                                                max(1, int(w.pages_per_seq.max()) if w.B else 1), w.cache_dtype,
+                                                props.multi_processor_count)
+        self.set_splits(num_splits)
+        self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+        self.decode_inputs = None
+
+    def set_splits(self, num_splits: int) -> None:
+        w = self.w
+        self.num_splits = int(num_splits)
+        self.out_partial = torch.empty((w.B, self.num_splits, w.Hq, w.D), dtype=torch.float32, device=self.device)
+        self.lse_partial = torch.empty((w.B, self.num_splits, w.Hq), dtype=torch.float32, device=self.device)
+
+    # ---- cache fill ----------------------------------------------------------
+    def fill(self, max_tokens: int = 1 << 18) -> int:
+        """Write context tokens 0..L-2 of every sequence with the library's
+        cache-write call (no q), in chunks of whole sequences. Returns the
+        number of tokens written."""
+        w = self.w
+        written = 0
+        b = 0
+        while b < w.B:
+            seqs = []
+            n = 0
+            while b < w.B and (not seqs or n + max(0, int(w.seq_lens[b]) - 1) <= max_tokens):
+                seqs.append(b)
+                n += max(0, int(w.seq_lens[b]) - 1)
+                b += 1
+            fb = w.fill_batch(seqs)
+            if len(fb["positions"]) == 0:
+                continue
+            k = _u16_to_bf16(fb["k"], self.device)
+            v = _u16_to_bf16(fb["v"], self.device)
+            pos = torch.from_numpy(fb["positions"]).to(self.device)
+            slot = torch.from_numpy(fb["slot_mapping"]).to(self.device)
+            self.write(None, k, v, pos, slot)
+            written += len(fb["positions"])
+        return written
+
+    def fill_inputs(self, seqs=None):
+        """Device tensors of one fill call (for timing the cache write)."""
+        fb = self.w.fill_batch(seqs)
+        return dict(k=_u16_to_bf16(fb["k"], self.device), v=_u16_to_bf16(fb["v"], self.device),
+                    positions=torch.from_numpy(fb["positions"]).to(self.device),
+                    slot_mapping=torch.from_numpy(fb["slot_mapping"]).to(self.device))
+
+    # ---- the three calls -------------------------------------------------------
+    def write(self, q, k, v, positions, slot_mapping, stream=None) -> None:
+        w = self.w
+        _abi.rope_kv_write(q, k, v, positions, self.cos_sin, self.k_cache, self.v_cache, slot_mapping,
+                           self.k_scale, self.v_scale, w.layout, w.style, self.err, stream)
+
+    def decode(self, q, stream=None) -> None:
+        w = self.w
+        _abi.paged_gqa_decode(q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens, w.softmax_scale,
+                              self.num_splits, self.out_partial, self.lse_partial, self.k_scale, self.v_scale,
+                              w.layout, self.err, stream)
+
+    def merge(self, stream=None) -> None:
+        _abi.lse_merge(self.out_partial, self.lse_partial, self.out, self.lse, stream)
+
+    def upload_decode(self) -> dict:
+        """Device copies of the new token's q, k, v, position and slot. q0 is
+        kept unrotated; `q` is the working copy the step rotates in place."""
+        db = self.w.decode_batch()
+        d = dict(q0=_u16_to_bf16(db["q"], self.device), k=_u16_to_bf16(db["k"], self.device),
+                 v=_u16_to_bf16(db["v"], self.device), positions=torch.from_numpy(db["positions"]).to(self.device),
+                 slot_mapping=torch.from_numpy(db["slot_mapping"]).to(self.device))
+        d["q"] = d["q0"].clone()
+        self.decode_inputs = d
+        return d
+
+    def step(self, stream=None) -> None:
+        """One decode step on the current inputs: cache write of the new
+        token (q rotated in place), decode, merge."""
+        d = self.decode_inputs
+        self.write(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"], stream)
+        self.decode(d["q"], stream)
+        self.merge(stream)
+
+    # ---- host views -------------------------------------------------------------
+    def cache_pages_u(self, cache: torch.Tensor, pages) -> np.ndarray:
+        """Raw bytes (uint16 for bf16, uint8 for fp8) of the given pages."""
+        idx = torch.as_tensor(np.asarray(pages, np.int64), device=self.device)
+        sel = cache.index_select(0, idx).cpu()
+        if sel.dtype == torch.bfloat16:
+            return sel.view(torch.int16).numpy().view(np.uint16)
+        return sel.numpy()
+
+    @staticmethod
+    def bf16_u16(t: torch.Tensor) -> np.ndarray:
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

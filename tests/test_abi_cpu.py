@@ -1,0 +1,156 @@
+"""CPU tests of the C ABI: the library loads, exports every function that
+include/pkv.h declares, rejects inconsistent arguments before touching the
+GPU, and its split heuristic behaves as specified. No GPU work is launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import paged_kv_gqa_04_gb300 as pkv
+from paged_kv_gqa_04_gb300 import _abi, _build, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pkv.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert set(names) == set(_abi.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", _abi.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (pkv_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.pkv_abi_version() == 1
+    for s in range(4):
+        assert pkv.status_string(s)
+    assert "invalid" in pkv.status_string(1)
+
+
+def _t(shape, dtype, ptr=0x1000, strides=None):
+    d = _abi.PkvTensor()
+    d.ptr = ptr
+    d.dtype = {"bf16": 0, "fp8": 1, "f32": 2, "i32": 3}[dtype]
+    d.ndim = len(shape)
+    if strides is None:
+        strides, acc = [], 1
+        for n in reversed(shape):
+            strides.insert(0, acc)
+            acc *= n
+    for i, (n, s) in enumerate(zip(shape, strides)):
+        d.shape[i] = n
+        d.stride[i] = s
+    return d
+
+
+NULL = _abi.PkvTensor()
+
+
+def test_write_rejects_inconsistent_arguments(lib):
+    """Host validation only: fake (never dereferenced) pointers; every call
+    must return before any CUDA work."""
+    T, Hq, Hkv, D = 4, 8, 2, 128
+    kc = _t((10, Hkv, 16, D), "bf16")
+    args = dict(q=_t((T, Hq, D), "bf16"), k=_t((T, Hkv, D), "bf16"), v=_t((T, Hkv, D), "bf16"),
+                pos=_t((T,), "i32"), cs=_t((100, D), "f32"), kc=kc, vc=_t((10, Hkv, 16, D), "bf16"),
+                slot=_t((T,), "i32"), ks=NULL, vs=NULL)
+
+    def call(layout=1, style=0, **over):
+        a = dict(args, **over)
+        return lib.pkv_rope_kv_write(a["q"], a["k"], a["v"], a["pos"], a["cs"], a["kc"], a["vc"], a["slot"],
+                                     a["ks"], a["vs"], layout, style, None, None)
+
+    assert call(layout=2) == _abi.PKV_ERR_INVALID_ARG
+    assert call(style=5) == _abi.PKV_ERR_INVALID_ARG
+    assert call(k=_t((T, Hkv, D), "f32")) == _abi.PKV_ERR_INVALID_ARG
+    assert call(v=_t((T + 1, Hkv, D), "bf16")) == _abi.PKV_ERR_INVALID_ARG
+    assert call(q=_t((T, 7, D), "bf16")) == _abi.PKV_ERR_INVALID_ARG           # 7 % 2 != 0
+    assert call(pos=_t((T - 1,), "i32")) == _abi.PKV_ERR_INVALID_ARG
+    assert call(cs=_t((100, D // 2), "f32")) == _abi.PKV_ERR_INVALID_ARG
+    assert call(vc=_t((10, Hkv, 16, D), "fp8")) == _abi.PKV_ERR_INVALID_ARG   # cache dtypes differ
+    fp8c = _t((10, Hkv, 16, D), "fp8")
+    assert call(kc=fp8c, vc=fp8c) == _abi.PKV_ERR_INVALID_ARG                # fp8 without scales
+    assert call(kc=fp8c, vc=fp8c, ks=_t((3,), "f32"), vs=_t((3,), "f32")) == _abi.PKV_ERR_INVALID_ARG
+    d96 = dict(q=_t((T, Hq, 96), "bf16"), k=_t((T, Hkv, 96), "bf16"), v=_t((T, Hkv, 96), "bf16"),
+               cs=_t((100, 96), "f32"), kc=_t((10, Hkv, 16, 96), "bf16"), vc=_t((10, Hkv, 16, 96), "bf16"))
+    assert call(**d96) == _abi.PKV_ERR_UNSUPPORTED
+    assert call(k=_t((T, Hkv, D), "bf16", ptr=0x1002)) == _abi.PKV_ERR_UNSUPPORTED  # not 16-byte aligned
+    # an empty call is valid and launches nothing
+    e = dict(q=_t((0, Hq, D), "bf16"), k=_t((0, Hkv, D), "bf16"), v=_t((0, Hkv, D), "bf16"),
+             pos=_t((0,), "i32"), slot=_t((0,), "i32"))
+    assert call(**e) == _abi.PKV_OK
+
+
+def test_decode_and_merge_reject_inconsistent_arguments(lib):
+    B, Hq, Hkv, D, S = 3, 12, 2, 128, 4
+    q = _t((B, Hq, D), "bf16")
+    kc = _t((50, Hkv, 16, D), "bf16")
+    bt = _t((B, 10), "i32")
+    sl = _t((B,), "i32")
+    op = _t((B, S, Hq, D), "f32")
+    lp = _t((B, S, Hq), "f32")
+
+    def dec(**o):
+        a = dict(q=q, kc=kc, vc=kc, bt=bt, sl=sl, scale=0.1, S=S, op=op, lp=lp, ks=NULL, vs=NULL, layout=1)
+        a.update(o)
+        return lib.pkv_paged_gqa_decode(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["scale"], a["S"], a["op"],
+                                        a["lp"], a["ks"], a["vs"], a["layout"], None, None)
+
+    assert dec(S=0) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(S=5) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(bt=_t((B + 1, 10), "i32")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(lp=_t((B, S, Hq + 1), "f32")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(scale=float("nan")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(kc=_t((50, Hkv, 8, D), "bf16"), vc=_t((50, Hkv, 8, D), "bf16")) == _abi.PKV_ERR_UNSUPPORTED
+    q64 = _t((B, 64, D), "bf16")
+    assert dec(q=q64, op=_t((B, S, 64, D), "f32"), lp=_t((B, S, 64), "f32"),
+               kc=_t((50, 2, 16, D), "bf16"), vc=_t((50, 2, 16, D), "bf16")) == _abi.PKV_ERR_UNSUPPORTED
+    assert dec(q=_t((0, Hq, D), "bf16"), bt=_t((0, 10), "i32"), sl=_t((0,), "i32"), op=_t((0, S, Hq, D), "f32"),
+               lp=_t((0, S, Hq), "f32")) == _abi.PKV_OK
+
+    out = _t((B, Hq, D), "bf16")
+    m = lib.pkv_lse_merge
+    assert m(op, lp, _t((B, Hq + 1, D), "bf16"), NULL, None) == _abi.PKV_ERR_INVALID_ARG
+    assert m(op, _t((B, S + 1, Hq), "f32"), out, NULL, None) == _abi.PKV_ERR_INVALID_ARG
+    assert m(_t((B, S, Hq, 96), "f32"), lp, _t((B, Hq, 96), "bf16"), NULL, None) == _abi.PKV_ERR_UNSUPPORTED
+    assert m(op, lp, out, _t((B, Hq + 2), "f32"), None) == _abi.PKV_ERR_INVALID_ARG
+    assert lib.pkv_validate_indices(bt, sl, NULL, 50, NULL, None, None) == _abi.PKV_ERR_INVALID_ARG
+
+
+def test_split_heuristic(lib):
+    sms = 152
+
+    def choose(name):
+        w = synth.make_workload(name)
+        return pkv.choose_num_splits(w.B, w.Hkv, w.Hq, w.D, int(w.pages_per_seq.sum()), int(w.pages_per_seq.max()),
+                                     w.cache_dtype, sms)
+
+    # long context, 8 (sequence, kv head) units: enough splits to cover every SM
+    s3 = choose("longctx")
+    assert 16 <= s3 <= 64 and 2 * 4 * s3 >= sms
+    # large ragged batch already has 2048 units: few splits
+    assert choose("ragged") <= 4
+    for name in synth.WORKLOADS:
+        assert 1 <= choose(name) <= 64
+    # degenerate inputs
+    assert pkv.choose_num_splits(0, 1, 1, 128, 0, 0, "bf16", sms) == 1
+    assert pkv.choose_num_splits(1, 1, 1, 128, 1, 1, "bf16", sms) == 1
+    # never more splits than pages
+    assert pkv.choose_num_splits(1, 1, 8, 128, 3, 3, "bf16", sms) <= 3

@@ -1,0 +1,190 @@
+"""GPU parity of the decode step against the float64 oracle (small sizes).
+
+Every case runs the CUDA path through the C ABI (cache fill, new-token RoPE
++ cache write, paged GQA decode, LSE merge) and the oracle on the same seeded
+inputs, and compares: rotated q and every cache byte bit for bit; partial
+outputs, merged output and LSE within the tolerance of tests/_compare.py.
+Sizes span several pages per warp, ragged last pages, empty splits, block
+tables longer than one 32-entry batch per warp, both layouts, both RoPE
+styles, bf16 and FP8 caches, head dims 64 and 128 and groups of 1 to 16."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_gqa_04_gb300 import _abi, harness, synth
+from tests._compare import assert_close_lse, assert_close_out, bf16_u16_to_f64
+from tests._pipeline import oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(name, S_list, **kw):
+    return pytest.param(name, S_list, kw, id=name)
+
+
+CASES = [
+    _case("tiny", (1, 2)),
+    _case("hnd_d128_g6_tails", (1, 3, 8), seq_lens=[1, 16, 17, 31, 32, 33, 100, 257], Hq=12, Hkv=2, D=128,
+          rope_base=1e6, k_mult=0.5),
+    _case("nhd_d128_g4_interleaved", (1, 2), seq_lens=[5, 48, 130], Hq=16, Hkv=4, D=128, layout="NHD",
+          style="interleaved", rope_base=5e5, outlier_p=0.05),
+    _case("fp8_hnd_d128_g6_head_scales", (1, 4), seq_lens=[15, 16, 17, 200], Hq=12, Hkv=2, D=128,
+          cache_dtype="fp8", rope_base=1e6),
+    _case("fp8_nhd_d64_g2_tensor_scale", (1, 2), seq_lens=[3, 70], Hq=4, Hkv=2, D=64, layout="NHD",
+          cache_dtype="fp8", per_head_scale=False),
+    _case("bf16_hnd_d64_g16", (1, 3), seq_lens=[40, 9], Hq=16, Hkv=1, D=64),
+    _case("fp8_hnd_d128_g12", (2,), seq_lens=[33, 64], Hq=24, Hkv=2, D=128, cache_dtype="fp8"),
+    _case("mha_nhd_d128", (1,), seq_lens=[50], Hq=3, Hkv=3, D=128, layout="NHD"),
+    _case("empty_and_short", (5,), seq_lens=[0, 1, 20], Hq=8, Hkv=2, D=128),
+    _case("long_blocktable_batches", (1, 2), seq_lens=[4800, 4799], Hq=7, Hkv=1, D=128, rope_base=1e6),
+]
+
+
+def _workload(name, kw):
+    return synth.make_workload("tiny") if name == "tiny" else synth.custom_workload(name, 101, **kw)
+
+
+def run_and_compare(w, S, dw=None):
+    if dw is None:
+        dw = harness.DeviceWorkload(w, num_splits=S)
+        dw.fill()
+        dw.upload_decode()
+    else:
+        dw.set_splits(S)
+    dw.err.zero_()
+    dw.step()
+    torch.cuda.synchronize()
+    st = oracle_step(w, num_splits=S)
+    d = dw.decode_inputs
+    assert np.array_equal(dw.bf16_u16(d["q"]), st["q_rot"]), "rotated q bytes"
+    for b in range(w.B):
+        n = int(w.pages_per_seq[b])
+        if n == 0:
+            continue
+        for gc, oc in ((dw.k_cache, st["k_cache"]), (dw.v_cache, st["v_cache"])):
+            got = dw.cache_pages_u(gc, w.block_tables[b, :n])
+            assert np.array_equal(got, oc[st["block_tables"][b, :n]]), f"cache bytes of sequence {b}"
+    assert_close_out(dw.out_partial.cpu().numpy(), st["out_partial"], "out_partial")
+    assert_close_lse(dw.lse_partial.cpu().numpy(), st["lse_partial"], "lse_partial")
+    assert_close_out(bf16_u16_to_f64(dw.bf16_u16(dw.out)), st["out"], "out")
+    assert_close_lse(dw.lse.cpu().numpy(), st["lse"], "lse")
+    assert int(dw.err.item()) == 0
+    return dw
+
+
+@pytest.mark.parametrize("name,S_list,kw", CASES)
+def test_decode_step_parity(name, S_list, kw):
+    w = _workload(name, kw)
+    dw = None
+    for S in S_list:
+        if dw is not None:  # re-run the step on unrotated q with another split count
+            dw.decode_inputs["q"].copy_(dw.decode_inputs["q0"])
+        dw = run_and_compare(w, S, dw)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.0137, 3.5])
+def test_e4m3_write_exhaustive_over_bf16(scale):
+    """Every finite bf16 pattern, written as v (no rotation) and as k at
+    position 0 (identity rotation), to an FP8 cache with the given scale:
+    the bytes equal the oracle's encoder of f32(x / scale). Also the bf16
+    cache path for the same values."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    fin = np.isfinite(bf16_u16_to_f64(pats))
+    pats = np.where(fin, pats, 0).astype(np.uint16)
+    D, T = 128, 512
+    vals = pats.reshape(T, 1, D)
+    for cache_dtype in ("fp8", "bf16"):
+        w = synth.custom_workload("exh", 5, [T], 1, 1, D, cache_dtype=cache_dtype)
+        kc_ref = oracle.empty_cache(w.cache_shape(), cache_dtype)
+        vc_ref = np.zeros_like(kc_ref)
+        sc = np.array([scale], np.float32)
+        cs = np.zeros((1, D), np.float32)
+        cs[0, :D // 2] = 1.0
+        pos = np.zeros(T, np.int32)
+        slots = np.arange(T, dtype=np.int32)
+        oracle.rope_kv_write(None, vals, vals, pos, cs, kc_ref, vc_ref, slots, "HND", "neox",
+                             sc if cache_dtype == "fp8" else None, sc if cache_dtype == "fp8" else None)
+        dw = harness.DeviceWorkload(w, num_splits=1)
+        dw.cos_sin = torch.from_numpy(cs).cuda()
+        if cache_dtype == "fp8":
+            dw.k_scale = torch.from_numpy(sc).cuda()
+            dw.v_scale = torch.from_numpy(sc).cuda()
+        kv = harness._u16_to_bf16(vals, "cuda")
+        dw.write(None, kv, kv, torch.from_numpy(pos).cuda(), torch.from_numpy(slots).cuda())
+        torch.cuda.synchronize()
+        pages = np.arange(T // 16)
+        assert np.array_equal(dw.cache_pages_u(dw.k_cache, pages), kc_ref)
+        assert np.array_equal(dw.cache_pages_u(dw.v_cache, pages), vc_ref)
+
+
+@pytest.mark.parametrize("style", synth.STYLES)
+@pytest.mark.parametrize("layout", synth.LAYOUTS)
+@pytest.mark.parametrize("cache_dtype", synth.CACHE_DTYPES)
+def test_rope_write_random_positions(style, layout, cache_dtype):
+    """4096 tokens at random positions of a 8192-row table, written to a
+    shuffled set of slots: q, k and v bytes bit-exact."""
+    T, Hq, Hkv, D = 4096, 8, 2, 128
+    key = synth.stream_key(17, style + layout + cache_dtype)
+    q = synth.f32_to_bf16_trunc(synth.normal_f32(key, T * Hq * D) * 3).reshape(T, Hq, D)
+    k = synth.f32_to_bf16_trunc(synth.normal_f32(synth.stream_key(18, "k"), T * Hkv * D) * 3).reshape(T, Hkv, D)
+    v = synth.f32_to_bf16_trunc(synth.normal_f32(synth.stream_key(18, "v"), T * Hkv * D) * 3).reshape(T, Hkv, D)
+    cs = synth.cos_sin_table(8192, D, 1e6)
+    pos = (synth.uniform(synth.stream_key(19, "p"), T) * 8192).astype(np.int32)
+    pool = 512
+    slots = np.argsort(synth.uniform(synth.stream_key(19, "s"), pool * 16))[:T].astype(np.int32)
+    w = synth.custom_workload("rw", 20, [16], Hq, Hkv, D, layout=layout, style=style, cache_dtype=cache_dtype,
+                              num_pages=pool)
+    kc = oracle.empty_cache(w.cache_shape(), cache_dtype); vc = np.zeros_like(kc)
+    q_ref = q.copy()
+    oracle.rope_kv_write(q_ref, k, v, pos, cs, kc, vc, slots, layout, style, w.k_scale, w.v_scale)
+    dw = harness.DeviceWorkload(w, num_splits=1)
+    dw.cos_sin = torch.from_numpy(cs).cuda()
+    qg = harness._u16_to_bf16(q, "cuda")
+    dw.write(qg, harness._u16_to_bf16(k, "cuda"), harness._u16_to_bf16(v, "cuda"), torch.from_numpy(pos).cuda(),
+             torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(dw.bf16_u16(qg), q_ref)
+    assert np.array_equal(dw.cache_pages_u(dw.k_cache, np.arange(pool)), kc)
+    assert np.array_equal(dw.cache_pages_u(dw.v_cache, np.arange(pool)), vc)
+    assert int(dw.err.item()) == 0
+
+
+def test_page_permutation_gives_identical_output():
+    """The same logical cache in a differently shuffled pool gives a
+    bit-identical GPU output (pages are read in logical order)."""
+    kw = dict(seq_lens=[37, 300, 16], Hq=12, Hkv=2, D=128)
+    w1 = synth.custom_workload("perm", 30, num_pages=64, **kw)
+    outs = []
+    for seed_off in (0, 1):
+        w = synth.custom_workload("perm", 30, num_pages=64, **kw)
+        if seed_off:
+            perm = np.argsort(synth.uniform(synth.stream_key(31, "perm"), 64)).astype(np.int32)
+            w.block_tables = np.where(w1.block_tables >= 0, perm[np.maximum(w1.block_tables, 0)], -1).astype(np.int32)
+        dw = harness.DeviceWorkload(w, num_splits=3)
+        dw.fill()
+        dw.upload_decode()
+        dw.step()
+        torch.cuda.synchronize()
+        outs.append((dw.bf16_u16(dw.out), dw.lse.cpu().numpy(), dw.out_partial.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
+    assert np.array_equal(outs[0][2], outs[1][2])
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_lse_merge_random_partials(D):
+    B, S, Hq = 5, 37, 6
+    op = synth.normal_f32(synth.stream_key(40, "o"), B * S * Hq * D).reshape(B, S, Hq, D)
+    lp = (synth.normal_f32(synth.stream_key(40, "l"), B * S * Hq) * 4).reshape(B, S, Hq)
+    lp[0, :, 0] = -np.inf                       # an all-empty row
+    lp[1, 3:, :] = -np.inf                      # empty tail splits
+    op[1, 3:, :, :] = 0.0
+    out_ref, lse_ref = oracle.lse_merge(op.astype(np.float64), lp.astype(np.float64))
+    opg = torch.from_numpy(op).cuda(); lpg = torch.from_numpy(lp).cuda()
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    _abi.lse_merge(opg, lpg, out, lse)
+    torch.cuda.synchronize()
+    assert_close_out(bf16_u16_to_f64(harness.DeviceWorkload.bf16_u16(out)), out_ref)
+    assert_close_lse(lse.cpu().numpy(), lse_ref)
