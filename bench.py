@@ -1,0 +1,523 @@
+"""Benchmark of the paged-KV GQA decode step on GB300.
+
+One step = the whole hot path over one batch: fused RoPE + paged-KV write of
+the new token (q rotated in place), paged GQA split-K decode, LSE merge --
+three launches of the library's kernels through the C ABI.
+
+Default workload: the Qwen2.5-1.5B-shaped decode (batch 32, seq_lens uniform
+in [512, 4096], 12 query / 2 kv heads, head dim 128, page size 16, HND, bf16
+cache, NeoX RoPE base 1e6, 12000-page shuffled pool). The cache holds every
+context token (written by the library's cache-write call before timing).
+
+Timing: W warm-up steps, then exactly K steps between a barrier and a device
+synchronise on each side. Before every timed step the L2 is flushed (a 512 MiB
+device write) and q is restored from its unrotated copy, both outside the
+step's CUDA events; per step, events on the launching stream bracket each of
+the three launches. Reported:
+  value       tokens/s = B*K / sum of step times (inputs resident in HBM)
+  e2e         the same through the Python binding with host buffers: every
+              step copies its inputs from pinned host memory to the device and
+              its output (out, lse) back, inside the step's events
+  roofline    of the decode kernel: algorithmic bytes (Q + K/V pages + block-
+              table entries + output) / its mean event time, against the
+              measured HBM copy bandwidth
+  cache_write GB/s of one cache-fill call over all context tokens
+  cpu_baseline the float64 oracle on the host, single thread
+`--impl reference` times that oracle alone as the reference arm.
+Under torchrun with N > 1 every rank runs an independent replica (weak
+scaling, no collective on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "decode-attn KV-read GB/s & % of HBM peak; tokens/s/step; RoPE+KV-write GB/s"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20
+
+WORKLOAD_TEXT = {
+    "qwen": "Qwen2.5-1.5B-shaped paged GQA decode: B32, seq_lens ~U[512,4096], 12 q / 2 kv heads (GQA 6), "
+            "D128, page 16, HND, bf16 cache, NeoX RoPE base 1e6, 12000-page shuffled pool",
+    "longctx": "long-context decode: B2, seq_len 32768, 28 q / 4 kv heads (GQA 7), D128, page 16, HND, bf16, "
+               "8192-page fragmented pool",
+    "ragged": "ragged large-batch decode: B256, lognormal seq_lens (median 1024, sigma 1, [1,8192]), 32 q / 8 kv "
+              "heads (GQA 4), D128, NHD, interleaved RoPE 5e5, 1% outlier K rows x8",
+    "fp8": "FP8 E4M3 paged cache decode: B64, seq_lens ~U[2048,16384], 12 q / 2 kv heads, D128, HND, per-head "
+           "static K/V scales ~U[0.01,0.1]",
+    "tiny": "tiny paged GQA decode: B2, seq_lens {37,100}, 4 q / 2 kv heads, D64, HND",
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--workload", default="qwen", choices=sorted(WORKLOAD_TEXT))
+    p.add_argument("--splits", type=int, default=0, help="num_splits (0 = the library's heuristic)")
+    p.add_argument("--also", default="longctx,ragged,fp8",
+                   help="extra workloads whose decode roofline is reported under 'other_workloads' ('' = none)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--clock-window", type=float, default=1.0,
+                   help="seconds of untimed steps run under the clock sampler before the timed steps")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ---- distributed plumbing (replicas only) -----------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- clocks --------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_kernel_source_hash() -> str:
+    src = open(os.path.join(ROOT, "paged_kv_gqa_04_gb300", "csrc", "paged_decode.cu"), "rb").read()
+    return hashlib.sha256(src).hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    workload, if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", f"paged_gqa_decode_{workload}.md")
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None
+    h = t = None
+    for line in txt.splitlines():
+        if line.startswith("kernel_source_sha256_16:"):
+            h = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            try:
+                t = float(line.split(":", 1)[1].strip())
+            except ValueError:
+                t = None
+    return t if (h == decode_kernel_source_hash() and t) else None
+
+
+# ---- byte counts ---------------------------------------------------------------------
+def decode_alg_bytes(w) -> float:
+    """Q + K/V pages of every sequence + block-table entries read + bf16 out."""
+    e = w.elem_bytes
+    q = w.B * w.Hq * w.D * 2
+    kv = float(w.seq_lens.astype(np.int64).sum()) * w.Hkv * w.D * 2 * e
+    bt = float(w.pages_per_seq.sum()) * 4
+    out = w.B * w.Hq * w.D * 2
+    return q + kv + bt + out
+
+
+def partial_bytes(w, S) -> float:
+    return 2.0 * w.B * S * w.Hq * (w.D + 1) * 4
+
+
+def write_alg_bytes(w, T: int, with_q: bool) -> float:
+    e = w.elem_bytes
+    per = 2 * w.Hkv * w.D * 2 + 2 * w.Hkv * w.D * e + 8 + w.D * 4
+    if with_q:
+        per += 2 * w.Hq * w.D * 2
+    return float(T) * per
+
+
+# ---- GPU measurements ----------------------------------------------------------------
+def flush_buffer():
+    return torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+
+def time_steps(dw, steps: int, warmup: int, world: int, flush) -> dict:
+    """Device-resident steps: per step flush, restore q, then events around
+    each of the three launches."""
+    d = dw.decode_inputs
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        d["q"].copy_(d["q0"])
+        dw.step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        d["q"].copy_(d["q0"])
+        e = ev[i]
+        e[0].record(stream)
+        dw.write(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"])
+        e[1].record(stream)
+        dw.decode(d["q"])
+        e[2].record(stream)
+        dw.merge()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    write = [e[0].elapsed_time(e[1]) for e in ev]
+    dec = [e[1].elapsed_time(e[2]) for e in ev]
+    mer = [e[2].elapsed_time(e[3]) for e in ev]
+    tot = [e[0].elapsed_time(e[3]) for e in ev]
+    return dict(step_ms=tot, write_ms=write, decode_ms=dec, merge_ms=mer, wall_s=wall)
+
+
+def time_e2e(dw, steps: int, warmup: int, world: int, flush) -> dict:
+    """Through the binding with host buffers: per step, pinned-host -> device
+    copies of the step's inputs, the three calls, device -> pinned-host copy
+    of out and lse; CUDA events around all of it."""
+    w = dw.w
+    d = dw.decode_inputs
+    host = {k: d[k if k != "q" else "q0"].cpu().pin_memory() for k in ("q", "k", "v", "positions", "slot_mapping")}
+    host["block_tables"] = dw.block_tables.cpu().pin_memory()
+    host["seq_lens"] = dw.seq_lens.cpu().pin_memory()
+    out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    lse_h = torch.empty(dw.lse.shape, dtype=dw.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one(e0=None, e1=None):
+        if e0 is not None:
+            e0.record(stream)
+        d["q"].copy_(host["q"], non_blocking=True)
+        for key in ("k", "v", "positions", "slot_mapping"):
+            d[key].copy_(host[key], non_blocking=True)
+        dw.block_tables.copy_(host["block_tables"], non_blocking=True)
+        dw.seq_lens.copy_(host["seq_lens"], non_blocking=True)
+        dw.step()
+        out_h.copy_(dw.out, non_blocking=True)
+        lse_h.copy_(dw.lse, non_blocking=True)
+        if e1 is not None:
+            e1.record(stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        one()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        one(*ev[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return dict(step_ms=ms, h2d=h2d, d2h=d2h, B=w.B)
+
+
+def time_fill(dw, reps: int, flush) -> dict:
+    """One cache-fill call (all context tokens, no q), timed alone."""
+    fi = dw.fill_inputs()
+    T = int(fi["positions"].numel())
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        flush.zero_()
+        dw.write(None, fi["k"], fi["v"], fi["positions"], fi["slot_mapping"])
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        dw.write(None, fi["k"], fi["v"], fi["positions"], fi["slot_mapping"])
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    del fi
+    return dict(T=T, ms=statistics.median(ms), ms_all=ms)
+
+
+def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -> dict:
+    """Decode-kernel roofline of another workload (filled, then `reps`
+    flushed launches)."""
+    from paged_kv_gqa_04_gb300 import harness, synth
+    w = synth.make_workload(name)
+    dw = harness.DeviceWorkload(w, num_splits=splits or None)
+    dw.fill()
+    d = dw.upload_decode()
+    dw.step()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        dw.decode(d["q"])
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    fill = time_fill(dw, 5, flush)
+    wb = write_alg_bytes(w, fill["T"], False)
+    alg = decode_alg_bytes(w)
+    r = dict(workload=WORKLOAD_TEXT[name], num_splits=dw.num_splits, decode_us=ms * 1e3,
+             decode_gbs=alg / (ms * 1e-3) / 1e9, decode_frac=alg / (ms * 1e-3) / 1e9 / peak,
+             cache_write_gbs=wb / (fill["ms"] * 1e-3) / 1e9,
+             cache_write_frac=wb / (fill["ms"] * 1e-3) / 1e9 / peak, err_flag=int(dw.err.item()))
+    del dw
+    torch.cuda.empty_cache()
+    return r
+
+
+# ---- CPU oracle -------------------------------------------------------------------------
+def oracle_step_timer(w, seqs, num_splits):
+    """Prepare the oracle's cache for `seqs` (untimed) and return a function
+    that runs one oracle decode step over them (new-token write with q,
+    decode, merge) and returns its seconds."""
+    import oracle
+    from tests._pipeline import oracle_step
+    st = oracle_step(w, seqs=seqs, num_splits=num_splits)
+    db = w.decode_batch()
+    q0 = db["q"][seqs].copy()
+    k = db["k"][seqs]
+    v = db["v"][seqs]
+    pos = db["positions"][seqs]
+    P = w.page_size
+    bt = st["block_tables"]
+    slots = np.array([bt[i, p // P] * P + p % P if w.seq_lens[b] > 0 else -1
+                      for i, (b, p) in enumerate(zip(seqs, pos))], np.int32)
+    cs = w.cos_sin()
+
+    def run() -> float:
+        q = q0.copy()
+        t0 = time.perf_counter()
+        oracle.rope_kv_write(q, k, v, pos, cs, st["k_cache"], st["v_cache"], slots, w.layout, w.style,
+                             w.k_scale, w.v_scale)
+        op, lp = oracle.paged_decode(q, st["k_cache"], st["v_cache"], bt, st["seq_lens"], w.softmax_scale,
+                                     num_splits, w.layout, w.k_scale, w.v_scale)
+        oracle.lse_merge(op, lp)
+        return time.perf_counter() - t0
+    return run
+
+
+def cpu_baseline(w, num_splits, seconds: float) -> dict:
+    run = oracle_step_timer(w, list(range(w.B)), num_splits)
+    total, n = 0.0, 0
+    while total < seconds or n == 0:
+        total += run()
+        n += 1
+    return {"value": w.B * n / total, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} oracle decode steps over the whole batch ({w.B} sequences, {num_splits} splits): "
+                      f"new-token cache write, decode, merge; float64, single thread; cache prepared untimed"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the float64 oracle timed on the host cores."""
+    if rank != 0:
+        return
+    from paged_kv_gqa_04_gb300 import synth
+    w = synth.make_workload(args.workload)
+    S = args.splits or 1
+    import oracle
+    oracle.build()
+    # size the per-step sample so that warm-up + timed steps take about a minute
+    probe = oracle_step_timer(w, [0], S)
+    t1 = probe()
+    n = int(max(1, min(w.B, round(60.0 / max(1, args.steps + args.warmup) / max(t1, 1e-6)))))
+    seqs = list(range(n))
+    run = oracle_step_timer(w, seqs, S)
+    for _ in range(args.warmup):
+        run()
+    ts = [run() for _ in range(args.steps)]
+    total = sum(ts)
+    value = n * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "batch_sample": n, "num_splits": S},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1,
+                         "sample": f"each step: the first {n} of {w.B} sequences (new-token write, decode, merge)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- main -------------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    world, rank = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_gqa_04_gb300 import harness, synth
+
+    peak, peak_kind = hbm_peak()
+    w = synth.make_workload(args.workload)
+    dw = harness.DeviceWorkload(w, num_splits=args.splits or None)
+    dw.fill()
+    dw.upload_decode()
+    flush = flush_buffer()
+    gpu_index = torch.cuda.current_device()
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(gpu_index)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else gpu_index)
+    clocks.start()
+    time.sleep(0.4)
+    # keep the GPU under this load for about a second before the timed steps so
+    # the clock samples describe it
+    t_end = time.perf_counter() + args.clock_window
+    while time.perf_counter() < t_end:
+        time_steps(dw, 20, 0, 1, flush)
+    r = time_steps(dw, args.steps, args.warmup, world, flush)
+    clk = clocks.stop()
+    err = int(dw.err.item())
+
+    step_s = sum(r["step_ms"]) * 1e-3
+    step_s = max_over_ranks(step_s, world)
+    value = world * w.B * args.steps / step_s
+    dec_ms = statistics.mean(r["decode_ms"])
+    alg = decode_alg_bytes(w)
+    achieved = alg / (dec_ms * 1e-3) / 1e9
+
+    e2e = None if args.no_e2e else time_e2e(dw, args.steps, max(3, args.warmup // 2), world, flush)
+    e2e_s = max_over_ranks(sum(e2e["step_ms"]) * 1e-3, world) if e2e else None
+    fill = time_fill(dw, 10, flush)
+    wb = write_alg_bytes(w, fill["T"], False)
+    write_gbs = wb / (fill["ms"] * 1e-3) / 1e9
+
+    others = {}
+    if args.also:
+        for name in [x for x in args.also.split(",") if x]:
+            others[name] = measure_decode_only(name, 0, 20, flush, peak)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, dw.num_splits, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * step_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "batch": w.B, "num_splits": dw.num_splits,
+                   "context_tokens": int(w.seq_lens.sum()),
+                   "l2": "flushed before every timed step (512 MiB device write, outside the step's events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "step_us": {"rope_kv_write": 1e3 * statistics.mean(r["write_ms"]), "paged_gqa_decode": 1e3 * dec_ms,
+                    "lse_merge": 1e3 * statistics.mean(r["merge_ms"]),
+                    "step": 1e3 * statistics.mean(r["step_ms"])},
+        "decode_kv_read_gbs": achieved,
+        "decode_hbm_frac": achieved / peak,
+        "rope_kv_write_gbs": write_gbs,
+        "rope_kv_write_hbm_frac": write_gbs / peak,
+        "cache_fill": {"tokens": fill["T"], "us": fill["ms"] * 1e3, "bytes": wb},
+        "roofline": {"kernel": "paged_gqa_decode", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload),
+                     "alg_bytes_per_launch": alg, "partial_record_bytes": partial_bytes(w, dw.num_splits)},
+        "e2e": None if e2e is None else {"value": world * w.B * args.steps / e2e_s, "unit": UNIT,
+                                         "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "err_flag": err,
+    }
+    if others:
+        line["other_workloads"] = others
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -39,7 +39,10 @@
  *     PKV_FLAG_* bit into *err_flag (a device int32 the caller zeroes; may be
  *     NULL). No kernel traps, asserts or faults on bad index values.
  *   - Tensors. A pkv_tensor is a strided view: shape and strides in ELEMENTS,
- *     outermost first. Innermost strides must be 1 where stated.
+ *     outermost first. Innermost strides must be 1 where stated. Tensors are
+ *     passed by pointer to their descriptor; the descriptor is read during
+ *     the call only. Where a tensor is optional, a NULL descriptor pointer
+ *     or a descriptor whose ptr is NULL both mean "absent".
  */
 #ifndef PKV_H
 #define PKV_H
@@ -123,9 +126,9 @@ typedef struct {
  * entirely. Two tokens with the same slot: the surviving write is unspecified.
  * q must not alias k, v or the caches; the caches must not alias k or v.
  */
-pkv_status pkv_rope_kv_write(pkv_tensor q, pkv_tensor k, pkv_tensor v, pkv_tensor positions,
-                             pkv_tensor cos_sin, pkv_tensor k_cache, pkv_tensor v_cache,
-                             pkv_tensor slot_mapping, pkv_tensor k_scale, pkv_tensor v_scale,
+pkv_status pkv_rope_kv_write(const pkv_tensor* q, const pkv_tensor* k, const pkv_tensor* v, const pkv_tensor* positions,
+                             const pkv_tensor* cos_sin, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                             const pkv_tensor* slot_mapping, const pkv_tensor* k_scale, const pkv_tensor* v_scale,
                              int32_t layout, int32_t rope_style, int32_t* err_flag,
                              pkv_stream_t stream);
 
@@ -164,10 +167,10 @@ pkv_status pkv_rope_kv_write(pkv_tensor q, pkv_tensor k, pkv_tensor v, pkv_tenso
  * > 16*max_pages sets PKV_FLAG_SEQ_LEN_RANGE and L is clamped to [0,
  * 16*max_pages]. Outputs must not alias inputs.
  */
-pkv_status pkv_paged_gqa_decode(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
-                                pkv_tensor block_tables, pkv_tensor seq_lens, float softmax_scale,
-                                int32_t num_splits, pkv_tensor out_partial, pkv_tensor lse_partial,
-                                pkv_tensor k_scale, pkv_tensor v_scale, int32_t layout,
+pkv_status pkv_paged_gqa_decode(const pkv_tensor* q, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                                const pkv_tensor* block_tables, const pkv_tensor* seq_lens, float softmax_scale,
+                                int32_t num_splits, const pkv_tensor* out_partial, const pkv_tensor* lse_partial,
+                                const pkv_tensor* k_scale, const pkv_tensor* v_scale, int32_t layout,
                                 int32_t* err_flag, pkv_stream_t stream);
 
 /*
@@ -186,8 +189,8 @@ pkv_status pkv_paged_gqa_decode(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_c
  * lse_out      [B, Hq] float32; ptr may be NULL.
  * Supported: D in {64, 128}.
  */
-pkv_status pkv_lse_merge(pkv_tensor out_partial, pkv_tensor lse_partial, pkv_tensor out,
-                         pkv_tensor lse_out, pkv_stream_t stream);
+pkv_status pkv_lse_merge(const pkv_tensor* out_partial, const pkv_tensor* lse_partial, const pkv_tensor* out,
+                         const pkv_tensor* lse_out, pkv_stream_t stream);
 
 /*
  * pkv_choose_num_splits -- split count for pkv_paged_gqa_decode (host only,
@@ -222,9 +225,9 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
  * zeroes and then uses (ptr may be NULL to skip the duplicate check).
  * err_flag must be non-NULL.
  */
-pkv_status pkv_validate_indices(pkv_tensor block_tables, pkv_tensor seq_lens,
-                                pkv_tensor slot_mapping, int64_t num_pages,
-                                pkv_tensor slot_bitmap, int32_t* err_flag, pkv_stream_t stream);
+pkv_status pkv_validate_indices(const pkv_tensor* block_tables, const pkv_tensor* seq_lens,
+                                const pkv_tensor* slot_mapping, int64_t num_pages,
+                                const pkv_tensor* slot_bitmap, int32_t* err_flag, pkv_stream_t stream);
 
 /* Static description of a status code. */
 const char* pkv_status_string(int32_t status);

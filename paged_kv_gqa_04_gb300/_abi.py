@@ -61,7 +61,7 @@ def lib() -> ctypes.CDLL:
             raise RuntimeError(f"CUDA library {LIB_PATH} is missing: build it with "
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
         L = ctypes.CDLL(LIB_PATH)
-        T = PkvTensor
+        T = ctypes.POINTER(PkvTensor)
         P = ctypes.c_void_p
         i32 = ctypes.c_int32
         L.pkv_rope_kv_write.argtypes = [T, T, T, T, T, T, T, T, T, T, i32, i32, P, P]
@@ -82,10 +82,11 @@ def status_string(status: int) -> str:
     return lib().pkv_status_string(int(status)).decode()
 
 
-def _desc(t: Optional[torch.Tensor]) -> PkvTensor:
-    d = PkvTensor()
+def _desc(t: Optional[torch.Tensor]):
+    """Pointer to a descriptor of t (NULL for None)."""
     if t is None:
-        return d
+        return None
+    d = PkvTensor()
     if t.dim() > 4:
         raise ValueError("tensors of more than 4 dims are not part of the ABI")
     if t.dtype not in _DTYPES:
@@ -98,7 +99,7 @@ def _desc(t: Optional[torch.Tensor]) -> PkvTensor:
     for i, (n, s) in enumerate(zip(t.shape, t.stride())):
         d.shape[i] = n
         d.stride[i] = s
-    return d
+    return ctypes.pointer(d)
 
 
 def _stream(stream) -> Optional[int]:

@@ -46,6 +46,10 @@ bool strides_multiple(const pkv_tensor& t, int upto, int64_t n) {
     return true;
 }
 
+const pkv_tensor kAbsent{};
+// An absent optional tensor may be given as a NULL descriptor pointer.
+const pkv_tensor& arg(const pkv_tensor* p) { return p ? *p : kAbsent; }
+
 pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -143,10 +147,20 @@ const char* pkv_status_string(int32_t status) {
     }
 }
 
-pkv_status pkv_rope_kv_write(pkv_tensor q, pkv_tensor k, pkv_tensor v, pkv_tensor positions, pkv_tensor cos_sin,
-                             pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor slot_mapping, pkv_tensor k_scale,
-                             pkv_tensor v_scale, int32_t layout, int32_t rope_style, int32_t* err_flag,
+pkv_status pkv_rope_kv_write(const pkv_tensor* q_p, const pkv_tensor* k_p, const pkv_tensor* v_p, const pkv_tensor* positions_p, const pkv_tensor* cos_sin_p,
+                             const pkv_tensor* k_cache_p, const pkv_tensor* v_cache_p, const pkv_tensor* slot_mapping_p, const pkv_tensor* k_scale_p,
+                             const pkv_tensor* v_scale_p, int32_t layout, int32_t rope_style, int32_t* err_flag,
                              pkv_stream_t stream) {
+    const pkv_tensor& q = arg(q_p);
+    const pkv_tensor& k = arg(k_p);
+    const pkv_tensor& v = arg(v_p);
+    const pkv_tensor& positions = arg(positions_p);
+    const pkv_tensor& cos_sin = arg(cos_sin_p);
+    const pkv_tensor& k_cache = arg(k_cache_p);
+    const pkv_tensor& v_cache = arg(v_cache_p);
+    const pkv_tensor& slot_mapping = arg(slot_mapping_p);
+    const pkv_tensor& k_scale = arg(k_scale_p);
+    const pkv_tensor& v_scale = arg(v_scale_p);
     if (rope_style != PKV_ROPE_NEOX && rope_style != PKV_ROPE_INTERLEAVED) return PKV_ERR_INVALID_ARG;
     int64_t num_pages;
     int P, Hkv, D;
@@ -214,10 +228,19 @@ pkv_status pkv_rope_kv_write(pkv_tensor q, pkv_tensor k, pkv_tensor v, pkv_tenso
     return cuda_status(pkv::launch_rope_kv_write(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-pkv_status pkv_paged_gqa_decode(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor block_tables,
-                                pkv_tensor seq_lens, float softmax_scale, int32_t num_splits, pkv_tensor out_partial,
-                                pkv_tensor lse_partial, pkv_tensor k_scale, pkv_tensor v_scale, int32_t layout,
+pkv_status pkv_paged_gqa_decode(const pkv_tensor* q_p, const pkv_tensor* k_cache_p, const pkv_tensor* v_cache_p, const pkv_tensor* block_tables_p,
+                                const pkv_tensor* seq_lens_p, float softmax_scale, int32_t num_splits, const pkv_tensor* out_partial_p,
+                                const pkv_tensor* lse_partial_p, const pkv_tensor* k_scale_p, const pkv_tensor* v_scale_p, int32_t layout,
                                 int32_t* err_flag, pkv_stream_t stream) {
+    const pkv_tensor& q = arg(q_p);
+    const pkv_tensor& k_cache = arg(k_cache_p);
+    const pkv_tensor& v_cache = arg(v_cache_p);
+    const pkv_tensor& block_tables = arg(block_tables_p);
+    const pkv_tensor& seq_lens = arg(seq_lens_p);
+    const pkv_tensor& out_partial = arg(out_partial_p);
+    const pkv_tensor& lse_partial = arg(lse_partial_p);
+    const pkv_tensor& k_scale = arg(k_scale_p);
+    const pkv_tensor& v_scale = arg(v_scale_p);
     int64_t num_pages;
     int P, Hkv, D;
     pkv_status st = check_caches(k_cache, v_cache, layout, &num_pages, &P, &Hkv, &D);
@@ -291,8 +314,12 @@ pkv_status pkv_paged_gqa_decode(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_c
     return cuda_status(pkv::launch_paged_decode(a, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-pkv_status pkv_lse_merge(pkv_tensor out_partial, pkv_tensor lse_partial, pkv_tensor out, pkv_tensor lse_out,
+pkv_status pkv_lse_merge(const pkv_tensor* out_partial_p, const pkv_tensor* lse_partial_p, const pkv_tensor* out_p, const pkv_tensor* lse_out_p,
                          pkv_stream_t stream) {
+    const pkv_tensor& out_partial = arg(out_partial_p);
+    const pkv_tensor& lse_partial = arg(lse_partial_p);
+    const pkv_tensor& out = arg(out_p);
+    const pkv_tensor& lse_out = arg(lse_out_p);
     if (!shape_ok(out_partial, 4, PKV_F32)) return PKV_ERR_INVALID_ARG;
     const int64_t B = out_partial.shape[0], S = out_partial.shape[1], Hq = out_partial.shape[2],
                   D = out_partial.shape[3];
@@ -362,8 +389,12 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
     return best;
 }
 
-pkv_status pkv_validate_indices(pkv_tensor block_tables, pkv_tensor seq_lens, pkv_tensor slot_mapping,
-                                int64_t num_pages, pkv_tensor slot_bitmap, int32_t* err_flag, pkv_stream_t stream) {
+pkv_status pkv_validate_indices(const pkv_tensor* block_tables_p, const pkv_tensor* seq_lens_p, const pkv_tensor* slot_mapping_p,
+                                int64_t num_pages, const pkv_tensor* slot_bitmap_p, int32_t* err_flag, pkv_stream_t stream) {
+    const pkv_tensor& block_tables = arg(block_tables_p);
+    const pkv_tensor& seq_lens = arg(seq_lens_p);
+    const pkv_tensor& slot_mapping = arg(slot_mapping_p);
+    const pkv_tensor& slot_bitmap = arg(slot_bitmap_p);
     if (!err_flag) return PKV_ERR_INVALID_ARG;
     if (!shape_ok(block_tables, 2, PKV_I32) || !shape_ok(seq_lens, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;
     if (seq_lens.shape[0] != block_tables.shape[0]) return PKV_ERR_INVALID_ARG;

@@ -13,7 +13,9 @@ their inputs from here; this module imports neither of them.
 Random numbers come from a counter-based generator: output i of stream
 (seed, name, index) is the splitmix64 finaliser applied to
 key + (i + 1) * 0x9E3779B97F4A7C15, so any sequence's values can be drawn on
-their own, in any order, with the same result on every machine.
+their own, in any order. (Normals go through float32 transcendental
+functions, whose last bits may differ between CPUs; both sides of a parity
+check always draw their inputs in the same process.)
 
 Workload shapes follow the decode regimes the pages describe:
   * Loom Kernels, "Supported operator paths" table, rows "Position and KV"
@@ -64,12 +66,23 @@ def stream_key(seed: int, name: str, index: int = 0) -> np.uint64:
 def raw_u64(key: np.uint64, start: int, n: int) -> np.ndarray:
     """Outputs start .. start+n-1 of the stream with this key."""
     out = np.empty(n, dtype=np.uint64)
-    with np.errstate(over="ignore"):
-        for c0 in range(0, n, _CHUNK):
-            c1 = min(n, c0 + _CHUNK)
-            ctr = np.arange(start + c0 + 1, start + c1 + 1, dtype=np.uint64)
-            out[c0:c1] = _mix64(np.uint64(key) + ctr * _GAMMA)
+    for c0 in range(0, n, _CHUNK):
+        c1 = min(n, c0 + _CHUNK)
+        out[c0:c1] = _raw_chunk(key, start + c0, c1 - c0)
     return out
+
+
+def _raw_chunk(key: np.uint64, start: int, n: int) -> np.ndarray:
+    # splitmix64 of key + (i + 1) * gamma, computed in place
+    x = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+    t = np.empty_like(x)
+    with np.errstate(over="ignore"):
+        np.multiply(x, _GAMMA, out=x)
+        np.add(x, np.uint64(key), out=x)
+        np.right_shift(x, np.uint64(30), out=t); np.bitwise_xor(x, t, out=x); np.multiply(x, _M1, out=x)
+        np.right_shift(x, np.uint64(27), out=t); np.bitwise_xor(x, t, out=x); np.multiply(x, _M2, out=x)
+        np.right_shift(x, np.uint64(31), out=t); np.bitwise_xor(x, t, out=x)
+    return x
 
 
 def uniform(key: np.uint64, n: int, start: int = 0) -> np.ndarray:
@@ -79,21 +92,22 @@ def uniform(key: np.uint64, n: int, start: int = 0) -> np.ndarray:
 
 
 def normal_f32(key: np.uint64, n: int) -> np.ndarray:
-    """n standard normals (float32), Box-Muller on pairs of uniforms.
-
-    Each 64-bit output gives two 26-bit uniforms; each uniform pair gives two
-    normals (cos and sin branch)."""
+    """n standard normals (float32), Box-Muller in float32 on pairs of
+    uniforms: each 64-bit output gives two 24-bit uniforms, each uniform
+    pair gives two normals (cos and sin branch)."""
     npair = (n + 1) // 2
     out = np.empty(2 * npair, dtype=np.float32)
+    inv = np.float32(1.0 / 16777216.0)
+    half = np.float32(0.5)
     for c0 in range(0, npair, _CHUNK):
         c1 = min(npair, c0 + _CHUNK)
-        u = raw_u64(key, c0, c1 - c0)
-        u1 = ((u >> np.uint64(38)).astype(np.float64) + 0.5) * (1.0 / 67108864.0)
-        u2 = (((u >> np.uint64(6)) & np.uint64(0x3FFFFFF)).astype(np.float64) + 0.5) * (1.0 / 67108864.0)
-        r = np.sqrt(-2.0 * np.log(u1))
-        th = (2.0 * math.pi) * u2
-        out[2 * c0:2 * c1:2] = (r * np.cos(th)).astype(np.float32)
-        out[2 * c0 + 1:2 * c1:2] = (r * np.sin(th)).astype(np.float32)
+        u = _raw_chunk(key, c0, c1 - c0)
+        u1 = ((u >> np.uint64(40)).astype(np.float32) + half) * inv
+        u2 = (((u >> np.uint64(8)) & np.uint64(0xFFFFFF)).astype(np.float32) + half) * inv
+        r = np.sqrt(np.float32(-2.0) * np.log(u1))
+        th = np.float32(2.0 * math.pi) * u2
+        out[2 * c0:2 * c1:2] = r * np.cos(th)
+        out[2 * c0 + 1:2 * c1:2] = r * np.sin(th)
     return out[:n]
 
 

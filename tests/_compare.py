@@ -32,7 +32,8 @@ def assert_close_lse(got: np.ndarray, ref: np.ndarray, what: str = "lse") -> Non
     ninf = ref == -np.inf
     if not np.array_equal(got == -np.inf, ninf):
         raise AssertionError(f"{what}: -inf pattern differs ({int((got == -np.inf).sum())} vs {int(ninf.sum())})")
-    err = np.abs(np.where(ninf, 0.0, got - ref))
+    with np.errstate(invalid="ignore"):
+        err = np.abs(np.where(ninf, 0.0, got - ref))
     if not (err <= LSE_ATOL).all():
         i = np.unravel_index(np.argmax(err), err.shape)
         raise AssertionError(f"{what}: max |err| {err[i]} at {i}: gpu {got[i]} oracle {ref[i]}")

@@ -37,6 +37,8 @@ def oracle_step(w: synth.Workload, seqs=None, num_splits: int = 1):
     for i, b in enumerate(seqs):
         L = int(w.seq_lens[b])
         if L == 0:
+            # no token to write (its slot is -1): q stays as it came
+            q_rot[i] = w.seq_q(b)
             continue
         k, v = w.seq_kv(b)
         pos = np.arange(L, dtype=np.int32)

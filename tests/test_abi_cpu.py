@@ -57,10 +57,10 @@ def _t(shape, dtype, ptr=0x1000, strides=None):
     for i, (n, s) in enumerate(zip(shape, strides)):
         d.shape[i] = n
         d.stride[i] = s
-    return d
+    return ctypes.pointer(d)
 
 
-NULL = _abi.PkvTensor()
+NULL = None
 
 
 def test_write_rejects_inconsistent_arguments(lib):

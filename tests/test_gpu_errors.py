@@ -105,7 +105,9 @@ def test_validate_indices_finds_each_problem():
     bt2 = bt.clone(); bt2[1, 2] = 20; checks.append((bt2, sl, slots, _abi.FLAG_PAGE_RANGE))
     bt3 = bt.clone(); bt3[2, 0] = -1; checks.append((bt3, sl, slots, _abi.FLAG_PAGE_RANGE))
     sl2 = sl.clone(); sl2[0] = -3; checks.append((bt, sl2, slots, _abi.FLAG_SEQ_LEN_RANGE))
-    sl3 = sl.clone(); sl3[2] = 16 * bt.shape[1] + 1; checks.append((bt, sl3, slots, _abi.FLAG_SEQ_LEN_RANGE))
+    # clamped to the block-table width, the sequence then also reaches its -1 padding entries
+    sl3 = sl.clone(); sl3[2] = 16 * bt.shape[1] + 1
+    checks.append((bt, sl3, slots, _abi.FLAG_SEQ_LEN_RANGE | _abi.FLAG_PAGE_RANGE))
     s2 = slots.clone(); s2[3] = 320; checks.append((bt, sl, s2, _abi.FLAG_SLOT_RANGE))
     s3 = slots.clone(); s3[3] = 5; checks.append((bt, sl, s3, _abi.FLAG_DUPLICATE_SLOT))
     for b_, l_, s_, flag in checks:
