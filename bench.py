@@ -224,9 +224,12 @@ def flush_buffer():
     return torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
 
-def time_steps(dw, steps: int, warmup: int, world: int, flush) -> dict:
-    """Device-resident steps: per step flush, restore q, then events around
-    each of the three launches."""
+def time_steps(dw, steps: int, warmup: int, world: int, flush, per_kernel: bool) -> dict:
+    """Device-resident steps: per step flush L2 and restore q (both outside
+    the events), then the three launches. With per_kernel, events also
+    separate the launches (which stops the decode and merge kernels from
+    starting early behind their predecessors); without, events bracket the
+    step only."""
     d = dw.decode_inputs
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -243,63 +246,45 @@ def time_steps(dw, steps: int, warmup: int, world: int, flush) -> dict:
         e = ev[i]
         e[0].record(stream)
         dw.write(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"])
-        e[1].record(stream)
+        if per_kernel:
+            e[1].record(stream)
         dw.decode(d["q"])
-        e[2].record(stream)
+        if per_kernel:
+            e[2].record(stream)
         dw.merge()
         e[3].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
-    write = [e[0].elapsed_time(e[1]) for e in ev]
-    dec = [e[1].elapsed_time(e[2]) for e in ev]
-    mer = [e[2].elapsed_time(e[3]) for e in ev]
-    tot = [e[0].elapsed_time(e[3]) for e in ev]
-    return dict(step_ms=tot, write_ms=write, decode_ms=dec, merge_ms=mer, wall_s=wall)
+    r = dict(step_ms=[e[0].elapsed_time(e[3]) for e in ev], wall_s=wall)
+    if per_kernel:
+        r.update(write_ms=[e[0].elapsed_time(e[1]) for e in ev], decode_ms=[e[1].elapsed_time(e[2]) for e in ev],
+                 merge_ms=[e[2].elapsed_time(e[3]) for e in ev])
+    return r
 
 
 def time_e2e(dw, steps: int, warmup: int, world: int, flush) -> dict:
-    """Through the binding with host buffers: per step, pinned-host -> device
-    copies of the step's inputs, the three calls, device -> pinned-host copy
-    of out and lse; CUDA events around all of it."""
-    w = dw.w
-    d = dw.decode_inputs
-    host = {k: d[k if k != "q" else "q0"].cpu().pin_memory() for k in ("q", "k", "v", "positions", "slot_mapping")}
-    host["block_tables"] = dw.block_tables.cpu().pin_memory()
-    host["seq_lens"] = dw.seq_lens.cpu().pin_memory()
-    out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
-    lse_h = torch.empty(dw.lse.shape, dtype=dw.lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    """Through the binding with host buffers, one CUDA-graph submission per
+    step (harness.StepGraph): pinned-host -> device copies of the step's
+    inputs, the three C-ABI launches, device -> pinned-host copies of out and
+    lse; CUDA events around each replay."""
+    from paged_kv_gqa_04_gb300 import harness
+    g = harness.StepGraph(dw, host_io=True)
     stream = torch.cuda.current_stream()
-
-    def one(e0=None, e1=None):
-        if e0 is not None:
-            e0.record(stream)
-        d["q"].copy_(host["q"], non_blocking=True)
-        for key in ("k", "v", "positions", "slot_mapping"):
-            d[key].copy_(host[key], non_blocking=True)
-        dw.block_tables.copy_(host["block_tables"], non_blocking=True)
-        dw.seq_lens.copy_(host["seq_lens"], non_blocking=True)
-        dw.step()
-        out_h.copy_(dw.out, non_blocking=True)
-        lse_h.copy_(dw.lse, non_blocking=True)
-        if e1 is not None:
-            e1.record(stream)
-
     for _ in range(warmup):
         flush.zero_()
-        one()
+        g.replay()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
-    for i in range(steps):
+    for a, b in ev:
         flush.zero_()
-        one(*ev[i])
+        a.record(stream)
+        g.replay()
+        b.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    ms = [a.elapsed_time(b) for a, b in ev]
-    return dict(step_ms=ms, h2d=h2d, d2h=d2h, B=w.B)
+    return dict(step_ms=[a.elapsed_time(b) for a, b in ev], h2d=g.h2d_bytes, d2h=g.d2h_bytes, B=dw.w.B)
 
 
 def time_fill(dw, reps: int, flush) -> dict:
@@ -320,6 +305,28 @@ def time_fill(dw, reps: int, flush) -> dict:
     ms = [a.elapsed_time(b) for a, b in ev]
     del fi
     return dict(T=T, ms=statistics.median(ms), ms_all=ms)
+
+
+def stream_ceiling(nbytes: int, flush, reps: int = 20) -> float:
+    """GB/s of one streaming-read launch (the library's pkv_stream_read) over
+    the given number of bytes, L2 flushed before each launch."""
+    from paged_kv_gqa_04_gb300 import _abi
+    n = max(16, int(nbytes) // 16 * 16)
+    buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    sink = torch.empty(4 * sms, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    _abi.stream_read(buf, sink)
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        _abi.stream_read(buf, sink)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    del buf
+    return n / (ms * 1e-3) / 1e9
 
 
 def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -> dict:
@@ -346,7 +353,8 @@ def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -
     r = dict(workload=WORKLOAD_TEXT[name], num_splits=dw.num_splits, decode_us=ms * 1e3,
              decode_gbs=alg / (ms * 1e-3) / 1e9, decode_frac=alg / (ms * 1e-3) / 1e9 / peak,
              cache_write_gbs=wb / (fill["ms"] * 1e-3) / 1e9,
-             cache_write_frac=wb / (fill["ms"] * 1e-3) / 1e9 / peak, err_flag=int(dw.err.item()))
+             cache_write_frac=wb / (fill["ms"] * 1e-3) / 1e9 / peak, err_flag=int(dw.err.item()),
+             stream_read_frac_same_bytes=stream_ceiling(alg, flush) / peak)
     del dw
     torch.cuda.empty_cache()
     return r
@@ -454,15 +462,16 @@ def main():
     # the clock samples describe it
     t_end = time.perf_counter() + args.clock_window
     while time.perf_counter() < t_end:
-        time_steps(dw, 20, 0, 1, flush)
-    r = time_steps(dw, args.steps, args.warmup, world, flush)
+        time_steps(dw, 20, 0, 1, flush, False)
+    r = time_steps(dw, args.steps, args.warmup, world, flush, False)
     clk = clocks.stop()
+    rk = time_steps(dw, args.steps, args.warmup, world, flush, True)
     err = int(dw.err.item())
 
     step_s = sum(r["step_ms"]) * 1e-3
     step_s = max_over_ranks(step_s, world)
     value = world * w.B * args.steps / step_s
-    dec_ms = statistics.mean(r["decode_ms"])
+    dec_ms = statistics.mean(rk["decode_ms"])
     alg = decode_alg_bytes(w)
     achieved = alg / (dec_ms * 1e-3) / 1e9
 
@@ -472,6 +481,7 @@ def main():
     wb = write_alg_bytes(w, fill["T"], False)
     write_gbs = wb / (fill["ms"] * 1e-3) / 1e9
 
+    ceiling = stream_ceiling(alg, flush)
     others = {}
     if args.also:
         for name in [x for x in args.also.split(",") if x]:
@@ -489,9 +499,13 @@ def main():
                    "context_tokens": int(w.seq_lens.sum()),
                    "l2": "flushed before every timed step (512 MiB device write, outside the step's events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "step_us": {"rope_kv_write": 1e3 * statistics.mean(r["write_ms"]), "paged_gqa_decode": 1e3 * dec_ms,
-                    "lse_merge": 1e3 * statistics.mean(r["merge_ms"]),
-                    "step": 1e3 * statistics.mean(r["step_ms"])},
+        "step_us": {"step": 1e3 * statistics.mean(r["step_ms"]),
+                    "separated": {"rope_kv_write": 1e3 * statistics.mean(rk["write_ms"]),
+                                  "paged_gqa_decode": 1e3 * dec_ms,
+                                  "lse_merge": 1e3 * statistics.mean(rk["merge_ms"]),
+                                  "step": 1e3 * statistics.mean(rk["step_ms"]),
+                                  "note": "second K-step pass with an event between launches (no early "
+                                          "start of decode/merge); the roofline uses its decode time"}},
         "decode_kv_read_gbs": achieved,
         "decode_hbm_frac": achieved / peak,
         "rope_kv_write_gbs": write_gbs,
@@ -501,7 +515,9 @@ def main():
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload),
-                     "alg_bytes_per_launch": alg, "partial_record_bytes": partial_bytes(w, dw.num_splits)},
+                     "alg_bytes_per_launch": alg, "partial_record_bytes": partial_bytes(w, dw.num_splits),
+                     "stream_read_same_bytes_gbs": ceiling,
+                     "stream_read_same_bytes_frac": ceiling / peak},
         "e2e": None if e2e is None else {"value": world * w.B * args.steps / e2e_s, "unit": UNIT,
                                          "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": 3 * args.steps,

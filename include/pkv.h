@@ -229,6 +229,20 @@ pkv_status pkv_validate_indices(const pkv_tensor* block_tables, const pkv_tensor
                                 const pkv_tensor* slot_mapping, int64_t num_pages,
                                 const pkv_tensor* slot_bitmap, int32_t* err_flag, pkv_stream_t stream);
 
+/*
+ * pkv_stream_read -- streaming-read ceiling (a measurement helper; not one of
+ * the decode step's calls). (mainarch, decode-attention section: a pure
+ * device-memory streaming read is measured first and is the ceiling each
+ * decode kernel is held to.)
+ *
+ * Reads `bytes` bytes at `buf` once, in one launch of `ctas` CTAs, with
+ * 16-byte non-caching loads, and writes one folded word per CTA to sink[0,
+ * ctas). buf: device memory, 16-byte aligned; bytes: a multiple of 16;
+ * sink: device memory of at least `ctas` uint32 words; 1 <= ctas <= 65535.
+ */
+pkv_status pkv_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int32_t ctas,
+                           pkv_stream_t stream);
+
 /* Static description of a status code. */
 const char* pkv_status_string(int32_t status);
 

@@ -36,7 +36,7 @@ _DTYPES = {
 }
 
 EXPORTED = ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_choose_num_splits",
-            "pkv_validate_indices", "pkv_status_string", "pkv_abi_version")
+            "pkv_validate_indices", "pkv_status_string", "pkv_abi_version", "pkv_stream_read")
 
 
 class PkvTensor(ctypes.Structure):
@@ -69,10 +69,11 @@ def lib() -> ctypes.CDLL:
         L.pkv_lse_merge.argtypes = [T, T, T, T, P]
         L.pkv_choose_num_splits.argtypes = [i32, i32, i32, i32, ctypes.c_int64, i32, i32, i32]
         L.pkv_validate_indices.argtypes = [T, T, T, ctypes.c_int64, T, P, P]
+        L.pkv_stream_read.argtypes = [P, ctypes.c_int64, P, i32, P]
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         for name in ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_validate_indices",
-                     "pkv_choose_num_splits", "pkv_abi_version"):
+                     "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read"):
             getattr(L, name).restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -157,3 +158,12 @@ def validate_indices(block_tables, seq_lens, slot_mapping, num_pages: int, err_f
     _check("pkv_validate_indices", lib().pkv_validate_indices(
         _desc(block_tables), _desc(seq_lens), _desc(slot_mapping), int(num_pages), _desc(slot_bitmap),
         _ptr(err_flag), _stream(stream)))
+
+
+def stream_read(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """Streaming-read ceiling (pkv_stream_read): read all of `buf` once in
+    one launch of sink.numel() CTAs."""
+    if not (buf.is_cuda and sink.is_cuda and sink.dtype == torch.int32):
+        raise ValueError("device buffer and int32 device sink expected")
+    _check("pkv_stream_read", lib().pkv_stream_read(buf.data_ptr(), buf.numel() * buf.element_size(),
+                                                     sink.data_ptr(), sink.numel(), _stream(stream)))

@@ -9,7 +9,9 @@
 // accumulates D/32 consecutive output columns over the S partial rows with
 // 8- or 16-byte loads (a partial row of D floats is one fully coalesced
 // 256/512-byte read), divides by sum w_s and writes bf16 (round to nearest
-// even) plus lse = M + ln sum w_s.
+// even) plus lse = M + ln sum w_s. The kernel is latency-bound (the partials
+// are a few MB): partial rows are loaded in batches of eight, the first batch
+// together with the LSE values, before any value is used.
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
@@ -18,18 +20,48 @@ namespace {
 
 constexpr int kWarps = 4;
 
+template <int V>
+struct Vec;
+template <>
+struct Vec<4> {
+    using T = float4;
+    static __device__ __forceinline__ void fma(float* acc, float w, const T& x) {
+        acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+    }
+};
+template <>
+struct Vec<2> {
+    using T = float2;
+    static __device__ __forceinline__ void fma(float* acc, float w, const T& x) {
+        acc[0] += w * x.x; acc[1] += w * x.y;
+    }
+};
+
+constexpr int kBatch = 8;  // partial rows loaded before any of them is used
+
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs a) {
     constexpr int V = D / 32;  // columns per lane
+    using VT = typename Vec<V>::T;
+    grid_dep_wait();  // the partials come from the preceding decode grid
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
     if (row >= static_cast<int64_t>(a.B) * a.Hq) return;
     const int b = static_cast<int>(row / a.Hq);
     const int h = static_cast<int>(row % a.Hq);
     const float* lse = a.lse_partial + b * a.lp_s0 + h;
+    const float* op = a.out_partial + b * a.op_s0 + h * a.op_s2 + lane * V;
 
-    float m = -INFINITY;
-    for (int s = lane; s < a.S; s += 32) m = fmaxf(m, __ldg(lse + s * a.lp_s1));
+    // The LSE values and the first batch of partial rows are loaded together
+    // (none depends on another), so the row costs one memory round trip when
+    // S <= 8.
+    float lv = (lane < a.S) ? __ldg(lse + lane * a.lp_s1) : -INFINITY;
+    VT x[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+        if (j < a.S) x[j] = __ldg(reinterpret_cast<const VT*>(op + j * a.op_s1));
+    float m = lv;
+    for (int s = 32 + lane; s < a.S; s += 32) m = fmaxf(m, __ldg(lse + s * a.lp_s1));
 #pragma unroll
     for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
 
@@ -38,22 +70,23 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs 
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
     float wsum = 0.f;
     if (m != -INFINITY) {
-        const float* op = a.out_partial + b * a.op_s0 + h * a.op_s2 + lane * V;
-        for (int s0 = 0; s0 < a.S; s0 += 32) {
-            const int s = s0 + lane;
-            const float w_mine = (s < a.S) ? __expf(__ldg(lse + s * a.lp_s1) - m) : 0.f;
-            wsum += w_mine;
-            const int n = min(32, a.S - s0);
-            for (int j = 0; j < n; ++j) {
-                const float w = __shfl_sync(0xffffffffu, w_mine, j);
-                const float* src = op + (s0 + j) * a.op_s1;
-                if constexpr (V == 4) {
-                    const float4 x = __ldg(reinterpret_cast<const float4*>(src));
-                    acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
-                } else {
-                    const float2 x = __ldg(reinterpret_cast<const float2*>(src));
-                    acc[0] += w * x.x; acc[1] += w * x.y;
-                }
+        float w_mine = (lane < a.S) ? __expf(lv - m) : 0.f;
+        wsum = w_mine;
+        for (int s0 = 0; s0 < a.S; s0 += kBatch) {
+            if (s0 > 0) {
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j)
+                    if (s0 + j < a.S) x[j] = __ldg(reinterpret_cast<const VT*>(op + (s0 + j) * a.op_s1));
+            }
+            if ((s0 & 31) == 0 && s0 > 0) {  // weights of splits s0 .. s0+31
+                const int s = s0 + lane;
+                w_mine = (s < a.S) ? __expf(__ldg(lse + s * a.lp_s1) - m) : 0.f;
+                wsum += w_mine;
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const float w = __shfl_sync(0xffffffffu, w_mine, (s0 + j) & 31);
+                if (s0 + j < a.S) Vec<V>::fma(acc, w, x[j]);
             }
         }
 #pragma unroll
@@ -82,13 +115,10 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
     const int64_t blocks = (rows + kWarps - 1) / kWarps;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-    if (a.D == 128)
-        lse_merge_kernel<128><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(a);
-    else if (a.D == 64)
-        lse_merge_kernel<64><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(a);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    const dim3 grid(static_cast<unsigned>(blocks)), block(kWarps * 32);
+    if (a.D == 128) return launch_dependent(lse_merge_kernel<128>, grid, block, 0, s, a);
+    if (a.D == 64) return launch_dependent(lse_merge_kernel<64>, grid, block, 0, s, a);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

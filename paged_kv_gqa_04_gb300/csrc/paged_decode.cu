@@ -47,7 +47,20 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 4;
+// Launch shape: warps per CTA, shared-memory ring bytes per warp and the
+// CTAs per SM the register budget is sized for (tuned on GB300; see the
+// measurements recorded with the profiles).
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+#ifndef PKV_DECODE_RING_BYTES
+#define PKV_DECODE_RING_BYTES 16384
+#endif
+#ifndef PKV_DECODE_MIN_CTAS
+#define PKV_DECODE_MIN_CTAS 3
+#endif
+constexpr int kWarps = PKV_DECODE_WARPS;
+constexpr int kRingBytes = PKV_DECODE_RING_BYTES;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 template <int D, bool FP8>
@@ -58,13 +71,13 @@ struct Cfg {
     static constexpr int NBOX = ROW / BOXB;                // boxes per page per tensor
     static constexpr int PAGE = kPageSize * ROW;           // bytes of one page of one head, K or V
     static constexpr int SLOT = 2 * PAGE;                  // K + V
-    static constexpr int NSLOT = (24 * 1024) / SLOT < 2 ? 2 : ((24 * 1024) / SLOT > 8 ? 8 : (24 * 1024) / SLOT);
+    static constexpr int NSLOT = kRingBytes / SLOT < 2 ? 2 : (kRingBytes / SLOT > 8 ? 8 : kRingBytes / SLOT);
     static constexpr int RING = NSLOT * SLOT;              // per warp
     static constexpr int KS = D / 16;                      // k-steps of QK
     static constexpr int NT = D / 8;                       // n-tiles of PV
     static constexpr int SMEM = kWarps * RING + kWarps * NSLOT * 8 + 1024;  // + barriers + alignment
     static_assert(BOXB == 128 || BOXB == 64, "swizzle span");
-    static_assert(RING >= (16 * D + 64) * 4, "combine area must fit in a warp's ring");
+    static_assert(RING >= (16 * (D + 8) + 32) * 4, "combine area must fit in a warp's ring");
 };
 
 // Byte offset of (row r, byte column col) in one page slice laid out by TMA
@@ -86,7 +99,7 @@ __device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16
 __device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
 
 template <int D, bool FP8, bool TWO>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         const DecodeArgs a, const int hnd) {
     using C = Cfg<D, FP8>;
@@ -105,6 +118,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int h0 = kvh * G;
 
     // ---- sequence bounds and this split's page range -----------------------
+    // The block-table entries this warp needs first depend on the split's
+    // first page, which depends on seq_len. They are read at the same time as
+    // seq_len from the position a sequence of the full block-table width
+    // would start at; the guess is kept when it turns out right (always, for
+    // equal lengths) and re-read otherwise.
+    const int pps_guess = (a.max_pages + a.num_splits - 1) / a.num_splits;
+    const int p0_guess = s * pps_guess;
+    const int32_t* bt_row = a.block_tables + b * a.bt_s0;
+    auto guess_at = [&](int k) -> int {
+        const int p = p0_guess + warp + kWarps * (k * 32 + lane);
+        return p < a.max_pages ? __ldg(bt_row + p) : -1;
+    };
+    const int cur_guess = guess_at(0);
+    const int nxt_guess = guess_at(1);
     int L = __ldg(a.seq_lens + b);
     const int cap = a.max_pages * kPageSize;
     if (L < 0 || L > cap) {
@@ -118,6 +145,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     float* outp = a.out_partial + b * a.op_s0 + s * a.op_s1 + h0 * a.op_s2;
     float* lsep = a.lse_partial + b * a.lp_s0 + s * a.lp_s1 + h0;
     if (p0 >= p1) {  // empty split: (0, -inf)
+        grid_dep_wait();
+        grid_dep_launch();
         for (int i = threadIdx.x; i < G * D; i += blockDim.x) outp[(i / D) * a.op_s2 + (i % D)] = 0.f;
         for (int i = threadIdx.x; i < G; i += blockDim.x) lsep[i] = -INFINITY;
         return;
@@ -138,15 +167,27 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     __syncwarp();
 
     // ---- block-table batches (32 entries, one batch ahead) -----------------
-    const int32_t* bt = a.block_tables + b * a.bt_s0 + p0 + warp;
+    const int32_t* bt = bt_row + p0 + warp;
     auto load_batch = [&](int k) -> int {
         const int i = k * 32 + lane;
         return i < nw ? __ldg(bt + kWarps * i) : -1;
     };
-    int cur = load_batch(0);
-    int nxt = load_batch(1);
+    const bool guessed = p0 == p0_guess;
+    int cur = guessed ? cur_guess : load_batch(0);
+    int nxt = guessed ? nxt_guess : load_batch(1);
     const uint64_t policy = l2_policy_evict_first();
     const int64_t num_pages = a.num_pages;
+    float ks = 1.f, vs = 1.f;
+    if constexpr (FP8) {
+        ks = __ldg(a.k_scale + (a.n_scale == 1 ? 0 : kvh));
+        vs = __ldg(a.v_scale + (a.n_scale == 1 ? 0 : kvh));
+    }
+
+    // Everything above reads only this call's index inputs. q and the cache
+    // may still be being written by the preceding cache-write grid (launched
+    // as our programmatic predecessor): wait for it before touching them.
+    grid_dep_wait();
+    grid_dep_launch();
 
     auto page_id = [&](int i, int cur_batch) -> int {
         const int src = ((i >> 5) == cur_batch) ? cur : nxt;
@@ -216,11 +257,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         }
     }
 
-    float ks = 1.f, vs = 1.f;
-    if constexpr (FP8) {
-        ks = __ldg(a.k_scale + (a.n_scale == 1 ? 0 : kvh));
-        vs = __ldg(a.v_scale + (a.n_scale == 1 ? 0 : kvh));
-    }
     const float sl = a.scale_log2 * ks;
 
     float acc[C::NT][4];
@@ -439,8 +475,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         lB += __shfl_xor_sync(0xffffffffu, lB, 2);
     }
     __syncwarp();
-    float* cw = reinterpret_cast<float*>(ring);  // [16][D] partial sums, then m[16], l[16]
-    float* cm = cw + 16 * D;
+    // [16][D + 8] partial sums (the 8-float pad makes the float2 stores of
+    // the eight row groups fall on distinct banks), then m[16], l[16]
+    constexpr int CWS = D + 8;
+    float* cw = reinterpret_cast<float*>(ring);
+    float* cm = cw + 16 * CWS;
     float* cl = cm + 16;
     if (t == 0) {
         cm[g] = mA;
@@ -450,15 +489,17 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     }
 #pragma unroll
     for (int n = 0; n < C::NT; ++n) {
+        if constexpr (FP8) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            int d;
-            if constexpr (FP8)
-                d = (D / 8) * (2 * t + e) + n;
-            else
-                d = 8 * n + 2 * t + e;
-            cw[g * D + d] = acc[n][e];
-            if constexpr (TWO) cw[(g + 8) * D + d] = acc[n][2 + e];
+            for (int e = 0; e < 2; ++e) {
+                const int d = (D / 8) * (2 * t + e) + n;
+                cw[g * CWS + d] = acc[n][e];
+                if constexpr (TWO) cw[(g + 8) * CWS + d] = acc[n][2 + e];
+            }
+        } else {
+            const int d = 8 * n + 2 * t;
+            *reinterpret_cast<float2*>(cw + g * CWS + d) = make_float2(acc[n][0], acc[n][1]);
+            if constexpr (TWO) *reinterpret_cast<float2*>(cw + (g + 8) * CWS + d) = make_float2(acc[n][2], acc[n][3]);
         }
     }
     __syncthreads();
@@ -470,12 +511,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         const int r = threadIdx.x;
         float M = -INFINITY;
         for (int w = 0; w < kWarps; ++w) {
-            const float* cmw = reinterpret_cast<const float*>(smem + w * C::RING) + 16 * D;
+            const float* cmw = reinterpret_cast<const float*>(smem + w * C::RING) + 16 * CWS;
             M = fmaxf(M, cmw[r]);
         }
         float Lsum = 0.f;
         for (int w = 0; w < kWarps; ++w) {
-            const float* cmw = reinterpret_cast<const float*>(smem + w * C::RING) + 16 * D;
+            const float* cmw = reinterpret_cast<const float*>(smem + w * C::RING) + 16 * CWS;
             const float ww = (M == -INFINITY || cmw[r] == -INFINITY) ? 0.f : exp2f(cmw[r] - M);
             wgt[w][r] = ww;
             Lsum += ww * cmw[16 + r];
@@ -490,7 +531,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         const int d = idx - r * D;
         float o = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) o += wgt[w][r] * reinterpret_cast<const float*>(smem + w * C::RING)[r * D + d];
+        for (int w = 0; w < kWarps; ++w) o += wgt[w][r] * reinterpret_cast<const float*>(smem + w * C::RING)[r * CWS + d];
         outp[r * a.op_s2 + d] = o * inv_l[r];
     }
 }
@@ -501,9 +542,8 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
     auto kern = paged_decode_kernel<D, FP8, TWO>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.num_splits, a.Hkv, a.B);
-    kern<<<grid, kWarps * 32, C::SMEM, s>>>(tk, tv, a, hnd);
-    return cudaGetLastError();
+    const dim3 grid(a.num_splits, a.Hkv, a.B);
+    return launch_dependent(kern, grid, dim3(kWarps * 32), C::SMEM, s, tk, tv, a, hnd);
 }
 
 template <int D, bool FP8>
@@ -516,7 +556,7 @@ cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
 int decode_ctas_per_sm(int D, int fp8) {
     (void)D;
     (void)fp8;
-    return 2;
+    return PKV_DECODE_MIN_CTAS;
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -429,4 +429,11 @@ pkv_status pkv_validate_indices(const pkv_tensor* block_tables_p, const pkv_tens
     return cuda_status(pkv::launch_validate(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int32_t ctas, pkv_stream_t stream) {
+    if (bytes < 0 || bytes % 16 != 0 || ctas < 1 || ctas > 65535) return PKV_ERR_INVALID_ARG;
+    if (bytes == 0) return PKV_OK;
+    if (!buf || !sink || !aligned(buf, 16)) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_stream_read(buf, bytes, sink, ctas, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -93,11 +93,31 @@ struct ValidateArgs {
     int32_t* err;
 };
 
+// Launch as a programmatic dependent of the preceding work in the stream:
+// the kernel may start while the preceding kernel finishes, and orders its
+// reads and writes of data that kernel touches after griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_rope_kv_write(const RopeArgs& a, cudaStream_t s);
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t s);
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s);
 cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s);
+cudaError_t launch_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int ctas, cudaStream_t s);
 
 // Occupancy-related constants of the decode kernel, shared with the split
 // heuristic on the host.

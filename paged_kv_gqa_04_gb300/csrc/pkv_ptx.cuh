@@ -59,6 +59,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Programmatic dependent launch: wait until the preceding grid in the
+// stream has completed and its writes are visible (a no-op when the kernel
+// was not launched as a programmatic dependent), and let the following grid
+// be scheduled once every CTA of this grid has passed this point.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

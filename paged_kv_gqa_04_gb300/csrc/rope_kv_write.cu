@@ -115,6 +115,9 @@ __device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float* 
 template <int D, bool INTER, bool FP8>
 __global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a, const int64_t total) {
     constexpr int TPR = D / 16;  // threads per row
+    // The decode kernel that usually follows may start its prologue now; it
+    // waits for this grid's writes before it reads q or the cache.
+    grid_dep_launch();
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= total) return;
     const int rows = a.Hq + 2 * a.Hkv;
@@ -124,9 +127,19 @@ __global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a, co
     const int row = r / TPR;
     const int c = r % TPR;
 
+    // slot, position and the row's two chunks do not depend on one another:
+    // all four loads are issued before any of them is checked (reading the
+    // row of a skipped token stays inside the [T, heads, D] input).
+    const bool is_q = row < a.Hq;
+    const bool is_k = !is_q && row < a.Hq + a.Hkv;
+    const int h = is_q ? row : (is_k ? row - a.Hq : row - a.Hq - a.Hkv);
+    const uint16_t* src = is_q ? a.q + t * a.q_s0 + h * a.q_s1
+                               : (is_k ? a.k + t * a.k_s0 + h * a.k_s1 : a.v + t * a.v_s0 + h * a.v_s1);
     const int32_t slot = __ldg(a.slots + t);
-    if (slot < 0) return;
     const int32_t pos = __ldg(a.positions + t);
+    const uint4 wlo = *reinterpret_cast<const uint4*>(src + 8 * c);
+    const uint4 whi = *reinterpret_cast<const uint4*>(src + D / 2 + 8 * c);
+    if (slot < 0) return;
     const int64_t num_slots = a.num_pages * a.page_size;
     if (slot >= num_slots) {
         if (r == 0) flag_error(a.err, PKV_FLAG_SLOT_RANGE);
@@ -137,21 +150,16 @@ __global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a, co
         return;
     }
     const float* cs = a.cos_sin + pos * a.cs_s0;
+    Chunk8 lo = unpack_bf16x8(wlo);
+    Chunk8 hi = unpack_bf16x8(whi);
 
-    if (row < a.Hq) {  // q head: rotate in place
-        uint16_t* p = a.q + t * a.q_s0 + row * a.q_s1;
-        Chunk8 lo = unpack_bf16x8(*reinterpret_cast<const uint4*>(p + 8 * c));
-        Chunk8 hi = unpack_bf16x8(*reinterpret_cast<const uint4*>(p + D / 2 + 8 * c));
+    if (is_q) {  // q head: rotate in place
         rotate_row<D, INTER>(lo, hi, cs, c);
+        uint16_t* p = a.q + t * a.q_s0 + h * a.q_s1;
         *reinterpret_cast<uint4*>(p + 8 * c) = pack_bf16x8(lo);
         *reinterpret_cast<uint4*>(p + D / 2 + 8 * c) = pack_bf16x8(hi);
         return;
     }
-    const bool is_k = row < a.Hq + a.Hkv;
-    const int h = is_k ? row - a.Hq : row - a.Hq - a.Hkv;
-    const uint16_t* src = is_k ? a.k + t * a.k_s0 + h * a.k_s1 : a.v + t * a.v_s0 + h * a.v_s1;
-    Chunk8 lo = unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(src + 8 * c)));
-    Chunk8 hi = unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(src + D / 2 + 8 * c)));
     if (is_k) rotate_row<D, INTER>(lo, hi, cs, c);
 
     const int64_t page = slot / a.page_size;

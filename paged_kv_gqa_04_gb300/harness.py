@@ -131,3 +131,61 @@ class DeviceWorkload:
     @staticmethod
     def bf16_u16(t: torch.Tensor) -> np.ndarray:
         return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+class StepGraph:
+    """One decode step captured as a CUDA graph: one submission per step.
+
+    The graph holds the three C-ABI launches (the cache write; the decode and
+    the merge as programmatic dependents, so each starts its prologue while
+    its predecessor finishes). With ``host_io`` it also holds the step's
+    input copies from pinned host buffers (q, k, v, positions, slot_mapping,
+    block_tables, seq_lens) and the copies of out and lse back to pinned host
+    buffers; otherwise it starts by restoring the unrotated q on the device.
+    """
+
+    def __init__(self, dw: DeviceWorkload, host_io: bool = False):
+        self.dw = dw
+        d = dw.decode_inputs
+        self.host = None
+        if host_io:
+            self.host = {k: d[k if k != "q" else "q0"].cpu().pin_memory()
+                         for k in ("q", "k", "v", "positions", "slot_mapping")}
+            self.host["block_tables"] = dw.block_tables.cpu().pin_memory()
+            self.host["seq_lens"] = dw.seq_lens.cpu().pin_memory()
+            self.out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+            self.lse_h = torch.empty(dw.lse.shape, dtype=dw.lse.dtype).pin_memory()
+        self._body()  # run once outside the capture (first-call set-up)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._body()
+        torch.cuda.synchronize()
+
+    def _body(self) -> None:
+        dw, d, h = self.dw, self.dw.decode_inputs, self.host
+        if h is None:
+            d["q"].copy_(d["q0"])
+        else:
+            d["q"].copy_(h["q"], non_blocking=True)
+            for key in ("k", "v", "positions", "slot_mapping"):
+                d[key].copy_(h[key], non_blocking=True)
+            dw.block_tables.copy_(h["block_tables"], non_blocking=True)
+            dw.seq_lens.copy_(h["seq_lens"], non_blocking=True)
+        dw.step()
+        if h is not None:
+            self.out_h.copy_(dw.out, non_blocking=True)
+            self.lse_h.copy_(dw.lse, non_blocking=True)
+
+    @property
+    def h2d_bytes(self) -> int:
+        return 0 if self.host is None else sum(t.numel() * t.element_size() for t in self.host.values())
+
+    @property
+    def d2h_bytes(self) -> int:
+        if self.host is None:
+            return 0
+        return self.out_h.numel() * self.out_h.element_size() + self.lse_h.numel() * self.lse_h.element_size()
+
+    def replay(self) -> None:
+        self.graph.replay()
