@@ -230,6 +230,36 @@ pkv_status pkv_validate_indices(const pkv_tensor* block_tables, const pkv_tensor
                                 const pkv_tensor* slot_bitmap, int32_t* err_flag, pkv_stream_t stream);
 
 /*
+ * pkv_validate_indices_static -- the same check as pkv_validate_indices,
+ * including the duplicate-slot check, for callers that cannot allocate
+ * device memory. (No counterpart on the pages: this entry point exists for
+ * callers of this library, not for the method.)
+ *
+ * Who needs it: an engine whose allocator has already taken all free device
+ * memory for its KV-cache pool cannot hand out a fresh scratch buffer for
+ * the slot bitmap, and a latency-critical path may not call cudaMalloc or
+ * cudaFree at all, because both can synchronise the whole device. This entry
+ * point therefore takes no scratch argument and allocates nothing: the
+ * bitmap lives in a fixed device array inside the library, of
+ * PKV_STATIC_VALIDATE_MAX_SLOTS bits (1 MiB), which every GPU that loads the
+ * library keeps until the process exits.
+ *
+ * Arguments are those of pkv_validate_indices without slot_bitmap.
+ * num_pages * 16 must not exceed PKV_STATIC_VALIDATE_MAX_SLOTS, else the call
+ * returns PKV_ERR_UNSUPPORTED and launches nothing. The first call on a
+ * device looks up the array's device address (once per device, with that
+ * device current); make that first call before any stream capture. Every
+ * call clears the bitmap on `stream` before using it, and all calls share
+ * the one array: calls whose GPU work overlaps (on different streams, or
+ * different host threads on one device) race on it and may report false or
+ * missed duplicates. Calls ordered on one stream are safe.
+ */
+#define PKV_STATIC_VALIDATE_MAX_SLOTS (1 << 23)
+pkv_status pkv_validate_indices_static(const pkv_tensor* block_tables, const pkv_tensor* seq_lens,
+                                       const pkv_tensor* slot_mapping, int64_t num_pages, int32_t* err_flag,
+                                       pkv_stream_t stream);
+
+/*
  * pkv_stream_read -- streaming-read ceiling (a measurement helper; not one of
  * the decode step's calls). (mainarch, decode-attention section: a pure
  * device-memory streaming read is measured first and is the ceiling each

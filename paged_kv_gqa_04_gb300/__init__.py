@@ -9,8 +9,10 @@ use; without it every call raises.
 """
 from ._abi import (EXPORTED, FLAG_DUPLICATE_SLOT, FLAG_PAGE_RANGE, FLAG_POSITION_RANGE, FLAG_SEQ_LEN_RANGE,
                    FLAG_SLOT_RANGE, FLAG_WAIT_TIMEOUT, PkvError, choose_num_splits, lib, lse_merge,
-                   paged_gqa_decode, rope_kv_write, status_string, stream_read, validate_indices)
+                   paged_gqa_decode, rope_kv_write, status_string, stream_read, validate_indices,
+                   validate_indices_static)
 
 __all__ = ["rope_kv_write", "paged_gqa_decode", "lse_merge", "choose_num_splits", "validate_indices",
+           "validate_indices_static",
            "status_string", "stream_read", "PkvError", "lib", "EXPORTED", "FLAG_SLOT_RANGE", "FLAG_POSITION_RANGE",
            "FLAG_PAGE_RANGE", "FLAG_SEQ_LEN_RANGE", "FLAG_DUPLICATE_SLOT", "FLAG_WAIT_TIMEOUT"]

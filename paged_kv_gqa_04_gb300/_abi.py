@@ -36,7 +36,8 @@ _DTYPES = {
 }
 
 EXPORTED = ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_choose_num_splits",
-            "pkv_validate_indices", "pkv_status_string", "pkv_abi_version", "pkv_stream_read")
+            "pkv_validate_indices", "pkv_status_string", "pkv_abi_version", "pkv_stream_read",
+            "pkv_validate_indices_static")
 
 
 class PkvTensor(ctypes.Structure):
@@ -70,10 +71,11 @@ def lib() -> ctypes.CDLL:
         L.pkv_choose_num_splits.argtypes = [i32, i32, i32, i32, ctypes.c_int64, i32, i32, i32]
         L.pkv_validate_indices.argtypes = [T, T, T, ctypes.c_int64, T, P, P]
         L.pkv_stream_read.argtypes = [P, ctypes.c_int64, P, i32, P]
+        L.pkv_validate_indices_static.argtypes = [T, T, T, ctypes.c_int64, P, P]
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         for name in ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_validate_indices",
-                     "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read"):
+                     "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read", "pkv_validate_indices_static"):
             getattr(L, name).restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -158,6 +160,20 @@ def validate_indices(block_tables, seq_lens, slot_mapping, num_pages: int, err_f
     _check("pkv_validate_indices", lib().pkv_validate_indices(
         _desc(block_tables), _desc(seq_lens), _desc(slot_mapping), int(num_pages), _desc(slot_bitmap),
         _ptr(err_flag), _stream(stream)))
+
+
+def validate_indices_static(block_tables, seq_lens, slot_mapping, num_pages: int, err_flag, stream=None) -> None:
+    """pkv_validate_indices_static: the same check as validate_indices
+    (duplicates included) for callers that cannot allocate device memory --
+    e.g. an engine whose allocator already holds all free memory for its KV
+    pool, or a path that must not call cudaMalloc/cudaFree because they can
+    synchronise the device. The bitmap is a fixed 1 MiB device array in the
+    library (at most 2**23 cache slots); calls overlapping on the GPU race on
+    it, and the first call on a device should come before any stream
+    capture."""
+    _check("pkv_validate_indices_static", lib().pkv_validate_indices_static(
+        _desc(block_tables), _desc(seq_lens), _desc(slot_mapping), int(num_pages), _ptr(err_flag),
+        _stream(stream)))
 
 
 def stream_read(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:

@@ -429,6 +429,47 @@ pkv_status pkv_validate_indices(const pkv_tensor* block_tables_p, const pkv_tens
     return cuda_status(pkv::launch_validate(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Same checks as pkv_validate_indices; the bitmap is the library's static
+// device array instead of a caller buffer, so nothing is allocated.
+pkv_status pkv_validate_indices_static(const pkv_tensor* block_tables_p, const pkv_tensor* seq_lens_p,
+                                       const pkv_tensor* slot_mapping_p, int64_t num_pages, int32_t* err_flag,
+                                       pkv_stream_t stream) {
+    const pkv_tensor& block_tables = arg(block_tables_p);
+    const pkv_tensor& seq_lens = arg(seq_lens_p);
+    const pkv_tensor& slot_mapping = arg(slot_mapping_p);
+    if (!err_flag) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(block_tables, 2, PKV_I32) || !shape_ok(seq_lens, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;
+    if (seq_lens.shape[0] != block_tables.shape[0]) return PKV_ERR_INVALID_ARG;
+    if (num_pages < 0) return PKV_ERR_INVALID_ARG;
+    if (num_pages * kPageSize > PKV_STATIC_VALIDATE_MAX_SLOTS) return PKV_ERR_UNSUPPORTED;
+    pkv::ValidateArgs a{};
+    if (slot_mapping.ptr) {
+        if (!shape_ok(slot_mapping, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;
+        a.slots = static_cast<const int32_t*>(slot_mapping.ptr);
+        a.sm_s0 = slot_mapping.stride[0];
+        a.T = slot_mapping.shape[0];
+    }
+    if (block_tables.shape[0] > 0x7FFFFFFF / 32 || block_tables.shape[1] > (int64_t{1} << 26))
+        return PKV_ERR_UNSUPPORTED;
+    if (block_tables.shape[0] > 0 && (!block_tables.ptr || !seq_lens.ptr)) return PKV_ERR_INVALID_ARG;
+    uint32_t* bitmap = nullptr;
+    int64_t words = 0;
+    cudaError_t e = pkv::static_slot_bitmap(&bitmap, &words);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    a.bitmap = bitmap;
+    a.bitmap_words = (num_pages * kPageSize + 31) / 32;  // only the part this call uses is cleared
+    a.block_tables = static_cast<const int32_t*>(block_tables.ptr);
+    a.bt_s0 = block_tables.stride[0];
+    a.bt_s1 = block_tables.stride[1];
+    a.max_pages = static_cast<int32_t>(block_tables.shape[1]);
+    a.seq_lens = static_cast<const int32_t*>(seq_lens.ptr);
+    a.sl_s0 = seq_lens.stride[0];
+    a.B = static_cast<int32_t>(block_tables.shape[0]);
+    a.num_pages = num_pages;
+    a.err = err_flag;
+    return cuda_status(pkv::launch_validate(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int32_t ctas, pkv_stream_t stream) {
     if (bytes < 0 || bytes % 16 != 0 || ctas < 1 || ctas > 65535) return PKV_ERR_INVALID_ARG;
     if (bytes == 0) return PKV_OK;

@@ -117,6 +117,7 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, cons
                                 cudaStream_t s);
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s);
 cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s);
+cudaError_t static_slot_bitmap(uint32_t** ptr, int64_t* words);
 cudaError_t launch_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int ctas, cudaStream_t s);
 
 // Occupancy-related constants of the decode kernel, shared with the split

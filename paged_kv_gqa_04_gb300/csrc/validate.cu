@@ -12,6 +12,8 @@
 // [32*B, 32*B + T) check one slot_mapping entry each and, given a bitmap of
 // one bit per cache slot, set the slot's bit with atomicOr: a bit that was
 // already set marks a duplicate.
+#include <mutex>
+
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
@@ -54,7 +56,35 @@ __global__ void __launch_bounds__(256) validate_kernel(const ValidateArgs a) {
     }
 }
 
+// Bitmap for pkv_validate_indices_static: a fixed device array so that the
+// entry point needs no allocation. Host code must not pass the symbol itself
+// to a kernel (on the host it names a host-side stand-in, not device
+// memory): static_slot_bitmap() looks up its device address.
+static __device__ __align__(256) uint32_t g_static_slot_bitmap[PKV_STATIC_VALIDATE_MAX_SLOTS / 32];
+
 }  // namespace
+
+// Device address of this device's copy of the static bitmap: looked up once
+// per device (with that device current) and then reused.
+cudaError_t static_slot_bitmap(uint32_t** ptr, int64_t* words) {
+    constexpr int kMaxDevices = 64;
+    static uint32_t* addr[kMaxDevices] = {};
+    static cudaError_t status[kMaxDevices] = {};
+    static std::once_flag once[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        void* p = nullptr;
+        status[dev] = cudaGetSymbolAddress(&p, g_static_slot_bitmap);
+        addr[dev] = static_cast<uint32_t*>(p);
+    });
+    if (status[dev] != cudaSuccess) return status[dev];
+    *ptr = addr[dev];
+    *words = PKV_STATIC_VALIDATE_MAX_SLOTS / 32;
+    return cudaSuccess;
+}
 
 cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s) {
     if (a.bitmap) {
