@@ -211,12 +211,17 @@ def partial_bytes(w, S) -> float:
     return 2.0 * w.B * S * w.Hq * (w.D + 1) * 4
 
 
-def write_alg_bytes(w, T: int, with_q: bool) -> float:
+def write_alg_bytes(w, T: int, with_q: bool, table_rows=None) -> float:
+    """q read+write (if given) + k, v read + cache write + position and slot
+    + one cos_sin row per token; with table_rows, the cos_sin rows are
+    counted once per distinct position instead (rows shared by tokens at the
+    same position are read from L2, not HBM)."""
     e = w.elem_bytes
-    per = 2 * w.Hkv * w.D * 2 + 2 * w.Hkv * w.D * e + 8 + w.D * 4
+    per = 2 * w.Hkv * w.D * 2 + 2 * w.Hkv * w.D * e + 8
     if with_q:
         per += 2 * w.Hq * w.D * 2
-    return float(T) * per
+    rows = T if table_rows is None else table_rows
+    return float(T) * per + float(rows) * w.D * 4
 
 
 # ---- GPU measurements ----------------------------------------------------------------
@@ -291,6 +296,7 @@ def time_fill(dw, reps: int, flush) -> dict:
     """One cache-fill call (all context tokens, no q), timed alone."""
     fi = dw.fill_inputs()
     T = int(fi["positions"].numel())
+    rows = int(torch.unique(fi["positions"]).numel())
     stream = torch.cuda.current_stream()
     for _ in range(2):
         flush.zero_()
@@ -304,7 +310,7 @@ def time_fill(dw, reps: int, flush) -> dict:
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
     del fi
-    return dict(T=T, ms=statistics.median(ms), ms_all=ms)
+    return dict(T=T, rows=rows, ms=statistics.median(ms), ms_all=ms)
 
 
 def stream_ceiling(nbytes: int, flush, reps: int = 20) -> float:
@@ -329,6 +335,39 @@ def stream_ceiling(nbytes: int, flush, reps: int = 20) -> float:
     return n / (ms * 1e-3) / 1e9
 
 
+def measure_layered(dw, layers: int, reps: int, flush, peak: float) -> dict:
+    """Decode as a model's layers run it: `layers` decode launches back to
+    back, each over its own cache (distinct memory, so nothing one layer
+    reads is in L2 for the next), each launch free to start behind the
+    previous one; L2 flushed before each group. Bytes / time of the group."""
+    from paged_kv_gqa_04_gb300 import _abi
+    w = dw.w
+    caches = [(dw.k_cache, dw.v_cache)]
+    for _ in range(layers - 1):
+        caches.append((dw.k_cache.clone(), dw.v_cache.clone()))
+    d = dw.decode_inputs
+    outs = [(torch.empty_like(dw.out_partial), torch.empty_like(dw.lse_partial)) for _ in range(layers)]
+
+    def group():
+        for (kc, vc), (op, lp) in zip(caches, outs):
+            _abi.paged_gqa_decode(d["q"], kc, vc, dw.block_tables, dw.seq_lens, w.softmax_scale, dw.num_splits,
+                                  op, lp, dw.k_scale, dw.v_scale, w.layout, dw.err)
+    stream = torch.cuda.current_stream()
+    group()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        group()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    gbs = layers * decode_alg_bytes(w) / (ms * 1e-3) / 1e9
+    ok = all(torch.equal(op, outs[0][0]) for op, _ in outs[1:])
+    del caches, outs
+    return dict(layers=layers, us_per_layer=1e3 * ms / layers, gbs=gbs, frac=gbs / peak, layers_agree=ok)
+
+
 def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -> dict:
     """Decode-kernel roofline of another workload (filled, then `reps`
     flushed launches)."""
@@ -347,14 +386,17 @@ def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -
         b.record(stream)
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    layered = measure_layered(dw, 4 if decode_alg_bytes(w) < 1e9 else 2, 5, flush, peak)
     fill = time_fill(dw, 5, flush)
     wb = write_alg_bytes(w, fill["T"], False)
+    wbu = write_alg_bytes(w, fill["T"], False, fill["rows"])
     alg = decode_alg_bytes(w)
     r = dict(workload=WORKLOAD_TEXT[name], num_splits=dw.num_splits, decode_us=ms * 1e3,
              decode_gbs=alg / (ms * 1e-3) / 1e9, decode_frac=alg / (ms * 1e-3) / 1e9 / peak,
              cache_write_gbs=wb / (fill["ms"] * 1e-3) / 1e9,
-             cache_write_frac=wb / (fill["ms"] * 1e-3) / 1e9 / peak, err_flag=int(dw.err.item()),
-             stream_read_frac_same_bytes=stream_ceiling(alg, flush) / peak)
+             cache_write_frac=wb / (fill["ms"] * 1e-3) / 1e9 / peak,
+             cache_write_frac_table_rows_once=wbu / (fill["ms"] * 1e-3) / 1e9 / peak, err_flag=int(dw.err.item()),
+             stream_read_frac_same_bytes=stream_ceiling(alg, flush) / peak, layered=layered)
     del dw
     torch.cuda.empty_cache()
     return r
@@ -479,9 +521,11 @@ def main():
     e2e_s = max_over_ranks(sum(e2e["step_ms"]) * 1e-3, world) if e2e else None
     fill = time_fill(dw, 10, flush)
     wb = write_alg_bytes(w, fill["T"], False)
+    wbu = write_alg_bytes(w, fill["T"], False, fill["rows"])
     write_gbs = wb / (fill["ms"] * 1e-3) / 1e9
 
     ceiling = stream_ceiling(alg, flush)
+    layered = measure_layered(dw, 4, 10, flush, peak)
     others = {}
     if args.also:
         for name in [x for x in args.also.split(",") if x]:
@@ -510,14 +554,18 @@ def main():
         "decode_hbm_frac": achieved / peak,
         "rope_kv_write_gbs": write_gbs,
         "rope_kv_write_hbm_frac": write_gbs / peak,
-        "cache_fill": {"tokens": fill["T"], "us": fill["ms"] * 1e3, "bytes": wb},
+        "cache_fill": {"tokens": fill["T"], "us": fill["ms"] * 1e3, "bytes": wb,
+                       "hbm_frac_table_rows_once": wbu / (fill["ms"] * 1e-3) / 1e9 / peak,
+                       "note": "rope_kv_write_gbs counts one cos_sin row per token; hbm_frac_table_rows_once counts "
+                               "each distinct position's row once"},
         "roofline": {"kernel": "paged_gqa_decode", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload),
                      "alg_bytes_per_launch": alg, "partial_record_bytes": partial_bytes(w, dw.num_splits),
                      "stream_read_same_bytes_gbs": ceiling,
-                     "stream_read_same_bytes_frac": ceiling / peak},
+                     "stream_read_same_bytes_frac": ceiling / peak,
+                     "layered": layered},
         "e2e": None if e2e is None else {"value": world * w.B * args.steps / e2e_s, "unit": UNIT,
                                          "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": 3 * args.steps,

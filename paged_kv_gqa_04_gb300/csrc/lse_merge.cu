@@ -10,15 +10,16 @@
 // 8- or 16-byte loads (a partial row of D floats is one fully coalesced
 // 256/512-byte read), divides by sum w_s and writes bf16 (round to nearest
 // even) plus lse = M + ln sum w_s. The kernel is latency-bound (the partials
-// are a few MB): partial rows are loaded in batches of eight, the first batch
-// together with the LSE values, before any value is used.
+// are a few MB): partial rows are loaded in batches of sixteen, the first
+// together with the LSE values and each next one while the previous batch is
+// summed, and the CTAs are two warps so the rows spread over many SMs.
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 2;  // small CTAs: the rows spread over more SMs
 
 template <int V>
 struct Vec;
@@ -37,7 +38,7 @@ struct Vec<2> {
     }
 };
 
-constexpr int kBatch = 8;  // partial rows loaded before any of them is used
+constexpr int kBatch = 16;  // partial rows in flight per lane
 
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs a) {
@@ -51,17 +52,18 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs 
     const int h = static_cast<int>(row % a.Hq);
     const float* lse = a.lse_partial + b * a.lp_s0 + h;
     const float* op = a.out_partial + b * a.op_s0 + h * a.op_s2 + lane * V;
+    const int S = a.S;
 
-    // The LSE values and the first batch of partial rows are loaded together
-    // (none depends on another), so the row costs one memory round trip when
-    // S <= 8.
-    float lv = (lane < a.S) ? __ldg(lse + lane * a.lp_s1) : -INFINITY;
+    // All loads of a batch are issued before any is used: the first batch of
+    // up to 16 partial rows goes out together with the LSE values, and each
+    // later batch is requested before the previous one is accumulated.
+    float lv = (lane < S) ? __ldg(lse + lane * a.lp_s1) : -INFINITY;
     VT x[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j)
-        if (j < a.S) x[j] = __ldg(reinterpret_cast<const VT*>(op + j * a.op_s1));
+        if (j < S) x[j] = __ldg(reinterpret_cast<const VT*>(op + j * a.op_s1));
     float m = lv;
-    for (int s = 32 + lane; s < a.S; s += 32) m = fmaxf(m, __ldg(lse + s * a.lp_s1));
+    for (int s = 32 + lane; s < S; s += 32) m = fmaxf(m, __ldg(lse + s * a.lp_s1));
 #pragma unroll
     for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
 
@@ -70,23 +72,29 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs 
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
     float wsum = 0.f;
     if (m != -INFINITY) {
-        float w_mine = (lane < a.S) ? __expf(lv - m) : 0.f;
+        float w_mine = (lane < S) ? __expf(lv - m) : 0.f;
         wsum = w_mine;
-        for (int s0 = 0; s0 < a.S; s0 += kBatch) {
-            if (s0 > 0) {
+        for (int s0 = 0; s0 < S; s0 += kBatch) {
+            VT y[kBatch];
+            const int s1 = s0 + kBatch;
+            if (s1 < S) {  // next batch in flight while this one is summed
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j)
-                    if (s0 + j < a.S) x[j] = __ldg(reinterpret_cast<const VT*>(op + (s0 + j) * a.op_s1));
-            }
-            if ((s0 & 31) == 0 && s0 > 0) {  // weights of splits s0 .. s0+31
-                const int s = s0 + lane;
-                w_mine = (s < a.S) ? __expf(__ldg(lse + s * a.lp_s1) - m) : 0.f;
-                wsum += w_mine;
+                    if (s1 + j < S) y[j] = __ldg(reinterpret_cast<const VT*>(op + (s1 + j) * a.op_s1));
             }
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
-                const float w = __shfl_sync(0xffffffffu, w_mine, (s0 + j) & 31);
-                if (s0 + j < a.S) Vec<V>::fma(acc, w, x[j]);
+                const int s = s0 + j;
+                if ((s & 31) == 0 && s > 0) {  // weights of splits s .. s+31
+                    w_mine = (s + lane < S) ? __expf(__ldg(lse + (s + lane) * a.lp_s1) - m) : 0.f;
+                    wsum += w_mine;
+                }
+                const float w = __shfl_sync(0xffffffffu, w_mine, s & 31);
+                if (s < S) Vec<V>::fma(acc, w, x[j]);
+            }
+            if (s1 < S) {
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) x[j] = y[j];
             }
         }
 #pragma unroll

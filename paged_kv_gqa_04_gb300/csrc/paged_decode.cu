@@ -73,6 +73,10 @@ struct Cfg {
     static constexpr int SLOT = 2 * PAGE;                  // K + V
     static constexpr int NSLOT = kRingBytes / SLOT < 2 ? 2 : (kRingBytes / SLOT > 8 ? 8 : kRingBytes / SLOT);
     static constexpr int RING = NSLOT * SLOT;              // per warp
+    // Pages consumed per iteration. Two (one softmax update per 32 tokens)
+    // measured slower on GB300 for every ring size that fits: it halves the
+    // pages a warp keeps in flight while it computes.
+    static constexpr int PG = 1;
     static constexpr int KS = D / 16;                      // k-steps of QK
     static constexpr int NT = D / 8;                       // n-tiles of PV
     static constexpr int SMEM = kWarps * RING + kWarps * NSLOT * 8 + 1024;  // + barriers + alignment
@@ -267,74 +271,152 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     int bad_pages = 0;
     int i = 0;
 
-    for (; i < nw; ++i) {
+    // S = Q K^T for the 16 tokens of the page at kb: sc[nt] holds tokens
+    // 8nt + 2t, 8nt + 2t + 1 of rows g and g + 8.
+    auto qk_page = [&](uint32_t kb, float (*sc)[4]) {
+        if constexpr (!FP8) {
+#pragma unroll
+            for (int jj = 0; jj < C::KS / 2; ++jj) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int r = 8 * nt + (lane & 7);
+                    const int col = 2 * (32 * jj + 8 * (lane >> 3));
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + swz<C::BOXB>(r, col), b0, b1, b2, b3);
+                    mma16816<false>(sc[nt], qa[2 * jj][0], qa[2 * jj][1], qa[2 * jj][2], qa[2 * jj][3], b0, b1);
+                    mma16816<false>(sc[nt], qa[2 * jj + 1][0], qa[2 * jj + 1][1], qa[2 * jj + 1][2],
+                                    qa[2 * jj + 1][3], b2, b3);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int r = 8 * nt + g;
+                uint32_t w[C::KS];
+                if constexpr (D == 128) {
+                    const uint4 x0 = lds128(kb + swz<C::BOXB>(r, 32 * t));
+                    const uint4 x1 = lds128(kb + swz<C::BOXB>(r, 32 * t + 16));
+                    w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
+                    w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
+                } else {
+                    const uint4 x0 = lds128(kb + swz<C::BOXB>(r, 16 * t));
+                    w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
+                }
+#pragma unroll
+                for (int j = 0; j < C::KS; ++j)
+                    mma16816<true>(sc[nt], qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(lo16(w[j])),
+                                   e4m3x2_to_f16x2(hi16(w[j])));
+            }
+        }
+    };
+    // O += P V for the page at vb; tokens at or past `valid` contribute zero
+    // (their V bytes may be anything, so they are zeroed, not only weighted 0).
+    auto pv_page = [&](uint32_t vb, int valid, uint32_t pa0, uint32_t pa1, uint32_t pa2, uint32_t pa3) {
+        if constexpr (!FP8) {
+            uint32_t mk0 = 0xFFFFFFFFu, mk1 = 0xFFFFFFFFu;
+            if (valid < kPageSize) {
+                mk0 = (2 * t < valid ? 0x0000FFFFu : 0u) | (2 * t + 1 < valid ? 0xFFFF0000u : 0u);
+                mk1 = (2 * t + 8 < valid ? 0x0000FFFFu : 0u) | (2 * t + 9 < valid ? 0xFFFF0000u : 0u);
+            }
+#pragma unroll
+            for (int dp = 0; dp < C::NT / 2; ++dp) {
+                const int mi = lane >> 3;
+                const int r = 8 * (mi & 1) + (lane & 7);
+                const int col = 16 * (2 * dp + (mi >> 1));
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vb + swz<C::BOXB>(r, col), b0, b1, b2, b3);
+                mma16816<false>(acc[2 * dp], pa0, pa1, pa2, pa3, b0 & mk0, b1 & mk1);
+                mma16816<false>(acc[2 * dp + 1], pa0, pa1, pa2, pa3, b2 & mk0, b3 & mk1);
+            }
+        } else {
+            constexpr int NWD = D / 32;  // words of V bytes per token row per thread
+            uint32_t va[4][NWD];
+            const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if constexpr (D == 128) {
+                    const uint4 xv = lds128(vb + swz<C::BOXB>(rows[q], 16 * g));
+                    va[q][0] = xv.x; va[q][1] = xv.y; va[q][2] = xv.z; va[q][3] = xv.w;
+                } else {
+                    const uint2 xv = lds64(vb + swz<C::BOXB>(rows[q], 8 * g));
+                    va[q][0] = xv.x; va[q][1] = xv.y;
+                }
+                if (rows[q] >= valid) {
+#pragma unroll
+                    for (int wd = 0; wd < NWD; ++wd) va[q][wd] = 0u;
+                }
+            }
+#pragma unroll
+            for (int wd = 0; wd < NWD; ++wd) {
+                const uint32_t pl = prmt(va[0][wd], va[1][wd], 0x5140u);
+                const uint32_t ph = prmt(va[0][wd], va[1][wd], 0x7362u);
+                const uint32_t ql = prmt(va[2][wd], va[3][wd], 0x5140u);
+                const uint32_t qh = prmt(va[2][wd], va[3][wd], 0x7362u);
+                mma16816<true>(acc[4 * wd + 0], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(lo16(pl)),
+                               e4m3x2_to_f16x2(lo16(ql)));
+                mma16816<true>(acc[4 * wd + 1], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(hi16(pl)),
+                               e4m3x2_to_f16x2(hi16(ql)));
+                mma16816<true>(acc[4 * wd + 2], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(lo16(ph)),
+                               e4m3x2_to_f16x2(lo16(qh)));
+                mma16816<true>(acc[4 * wd + 3], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(hi16(ph)),
+                               e4m3x2_to_f16x2(hi16(qh)));
+            }
+        }
+    };
+
+    // Pages are consumed PG at a time; one softmax update covers all their
+    // tokens.
+    constexpr int PG = C::PG;
+    for (; i < nw; i += PG) {
         if (i > 0 && (i & 31) == 0) {
             cur = nxt;
             nxt = load_batch((i >> 5) + 1);
         }
-        const int slot = i % C::NSLOT;
-        const uint32_t bar = bar0 + 8 * slot;
-        const bool landed = mbar_wait_bounded(bar, (i / C::NSLOT) & 1, kWaitLimitNs);
+        bool landed = true;
+#pragma unroll
+        for (int j = 0; j < PG; ++j) {
+            const int ij = i + j;
+            if (ij < nw) landed &= mbar_wait_bounded(bar0 + 8 * (ij % C::NSLOT), (ij / C::NSLOT) & 1, kWaitLimitNs);
+        }
         if (!__all_sync(0xffffffffu, landed)) {
             ok = false;
             break;
         }
-        const int pid = page_id(i, i >> 5);
-        const int p = p0 + warp + kWarps * i;
-        if (pid >= 0 && pid < num_pages) {
-            const int valid = min(kPageSize, L - p * kPageSize);
-            const uint32_t kb = ring0 + slot * C::SLOT;
-            const uint32_t vb = kb + C::PAGE;
-
-            // ---- S = Q K^T ---------------------------------------------------
-            float sc[2][4];
+        int valid[PG];
+        bool any = false;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-            if constexpr (!FP8) {
+        for (int j = 0; j < PG; ++j) {
+            const int ij = i + j;
+            const int pid = page_id(ij, i >> 5);
+            const bool pid_ok = pid >= 0 && pid < num_pages;
+            if (ij < nw && !pid_ok) ++bad_pages;
+            const int p = p0 + warp + kWarps * ij;
+            valid[j] = (ij < nw && pid_ok) ? min(kPageSize, L - p * kPageSize) : 0;
+            any |= valid[j] > 0;
+        }
+        if (any) {
+            float sc[2 * PG][4];
 #pragma unroll
-                for (int jj = 0; jj < C::KS / 2; ++jj) {
+            for (int n = 0; n < 2 * PG; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int r = 8 * nt + (lane & 7);
-                        const int col = 2 * (32 * jj + 8 * (lane >> 3));
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(kb + swz<C::BOXB>(r, col), b0, b1, b2, b3);
-                        mma16816<false>(sc[nt], qa[2 * jj][0], qa[2 * jj][1], qa[2 * jj][2], qa[2 * jj][3], b0, b1);
-                        mma16816<false>(sc[nt], qa[2 * jj + 1][0], qa[2 * jj + 1][1], qa[2 * jj + 1][2],
-                                        qa[2 * jj + 1][3], b2, b3);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int r = 8 * nt + g;
-                    uint32_t w[C::KS];
-                    if constexpr (D == 128) {
-                        const uint4 x0 = lds128(kb + swz<C::BOXB>(r, 32 * t));
-                        const uint4 x1 = lds128(kb + swz<C::BOXB>(r, 32 * t + 16));
-                        w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
-                        w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
-                    } else {
-                        const uint4 x0 = lds128(kb + swz<C::BOXB>(r, 16 * t));
-                        w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
-                    }
-#pragma unroll
-                    for (int j = 0; j < C::KS; ++j)
-                        mma16816<true>(sc[nt], qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(lo16(w[j])),
-                                       e4m3x2_to_f16x2(hi16(w[j])));
-                }
-            }
+            for (int j = 0; j < PG; ++j)
+                if (valid[j] > 0) qk_page(ring0 + ((i + j) % C::NSLOT) * C::SLOT, &sc[2 * j]);
 
             // ---- online softmax (log2 domain) -------------------------------
-            float x[2][4];
+            float x[2 * PG][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int n = 0; n < 2 * PG; ++n)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int tok = 8 * nt + 2 * t + (e & 1);
-                    x[nt][e] = tok < valid ? sc[nt][e] * sl : -INFINITY;
+                    const int tok = 8 * (n & 1) + 2 * t + (e & 1);
+                    x[n][e] = tok < valid[n >> 1] ? sc[n][e] * sl : -INFINITY;
                 }
-            float pmA = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+            float pmA = -INFINITY, pmB = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < 2 * PG; ++n) {
+                pmA = fmaxf(pmA, fmaxf(x[n][0], x[n][1]));
+                if constexpr (TWO) pmB = fmaxf(pmB, fmaxf(x[n][2], x[n][3]));
+            }
             pmA = fmaxf(pmA, __shfl_xor_sync(0xffffffffu, pmA, 1));
             pmA = fmaxf(pmA, __shfl_xor_sync(0xffffffffu, pmA, 2));
             const float nA = fmaxf(mA, pmA);
@@ -342,117 +424,80 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
             mA = nA;
             float nB = 0.f, alB = 1.f;
             if constexpr (TWO) {
-                float pmB = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
                 pmB = fmaxf(pmB, __shfl_xor_sync(0xffffffffu, pmB, 1));
                 pmB = fmaxf(pmB, __shfl_xor_sync(0xffffffffu, pmB, 2));
                 nB = fmaxf(mB, pmB);
                 alB = fast_exp2(mB - nB);
                 mB = nB;
             }
-            float pr[2][4];
+            float pr[2 * PG][4];
+            float sA = 0.f, sB = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                pr[nt][0] = fast_exp2(x[nt][0] - nA);
-                pr[nt][1] = fast_exp2(x[nt][1] - nA);
+            for (int n = 0; n < 2 * PG; ++n) {
+                pr[n][0] = fast_exp2(x[n][0] - nA);
+                pr[n][1] = fast_exp2(x[n][1] - nA);
+                sA += pr[n][0] + pr[n][1];
                 if constexpr (TWO) {
-                    pr[nt][2] = fast_exp2(x[nt][2] - nB);
-                    pr[nt][3] = fast_exp2(x[nt][3] - nB);
+                    pr[n][2] = fast_exp2(x[n][2] - nB);
+                    pr[n][3] = fast_exp2(x[n][3] - nB);
+                    sB += pr[n][2] + pr[n][3];
                 } else {
-                    pr[nt][2] = pr[nt][3] = 0.f;
+                    pr[n][2] = pr[n][3] = 0.f;
                 }
             }
-            lA = lA * alA + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
-            if constexpr (TWO) lB = lB * alB + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+            lA = lA * alA + sA;
+            if constexpr (TWO) lB = lB * alB + sB;
+            // rescale the accumulators only when some row's max moved (after
+            // the first pages it rarely does)
+            if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
 #pragma unroll
-            for (int n = 0; n < C::NT; ++n) {
-                acc[n][0] *= alA;
-                acc[n][1] *= alA;
-                if constexpr (TWO) {
-                    acc[n][2] *= alB;
-                    acc[n][3] *= alB;
-                }
-            }
-            // P as the A operand (rows g / g+8, tokens 2t.. and 8+2t..)
-            uint32_t pa0, pa1 = 0u, pa2, pa3 = 0u;
-            if constexpr (FP8) {
-                pa0 = pack_f16(pr[0][0], pr[0][1]);
-                pa2 = pack_f16(pr[1][0], pr[1][1]);
-                if constexpr (TWO) {
-                    pa1 = pack_f16(pr[0][2], pr[0][3]);
-                    pa3 = pack_f16(pr[1][2], pr[1][3]);
-                }
-            } else {
-                pa0 = pack_bf16(pr[0][0], pr[0][1]);
-                pa2 = pack_bf16(pr[1][0], pr[1][1]);
-                if constexpr (TWO) {
-                    pa1 = pack_bf16(pr[0][2], pr[0][3]);
-                    pa3 = pack_bf16(pr[1][2], pr[1][3]);
-                }
-            }
-
-            // ---- O += P V ----------------------------------------------------
-            if constexpr (!FP8) {
-                uint32_t mk0 = 0xFFFFFFFFu, mk1 = 0xFFFFFFFFu;
-                if (valid < kPageSize) {  // zero V of tokens past the end (their bytes may be anything)
-                    mk0 = (2 * t < valid ? 0x0000FFFFu : 0u) | (2 * t + 1 < valid ? 0xFFFF0000u : 0u);
-                    mk1 = (2 * t + 8 < valid ? 0x0000FFFFu : 0u) | (2 * t + 9 < valid ? 0xFFFF0000u : 0u);
-                }
-#pragma unroll
-                for (int dp = 0; dp < C::NT / 2; ++dp) {
-                    const int mi = lane >> 3;
-                    const int r = 8 * (mi & 1) + (lane & 7);
-                    const int col = 16 * (2 * dp + (mi >> 1));
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vb + swz<C::BOXB>(r, col), b0, b1, b2, b3);
-                    mma16816<false>(acc[2 * dp], pa0, pa1, pa2, pa3, b0 & mk0, b1 & mk1);
-                    mma16816<false>(acc[2 * dp + 1], pa0, pa1, pa2, pa3, b2 & mk0, b3 & mk1);
-                }
-            } else {
-                constexpr int NWD = D / 32;  // words of V bytes per token row per thread
-                uint32_t va[4][NWD];
-                const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if constexpr (D == 128) {
-                        const uint4 xv = lds128(vb + swz<C::BOXB>(rows[q], 16 * g));
-                        va[q][0] = xv.x; va[q][1] = xv.y; va[q][2] = xv.z; va[q][3] = xv.w;
-                    } else {
-                        const uint2 xv = lds64(vb + swz<C::BOXB>(rows[q], 8 * g));
-                        va[q][0] = xv.x; va[q][1] = xv.y;
-                    }
-                    if (rows[q] >= valid) {
-#pragma unroll
-                        for (int wd = 0; wd < NWD; ++wd) va[q][wd] = 0u;
+                for (int n = 0; n < C::NT; ++n) {
+                    acc[n][0] *= alA;
+                    acc[n][1] *= alA;
+                    if constexpr (TWO) {
+                        acc[n][2] *= alB;
+                        acc[n][3] *= alB;
                     }
                 }
-#pragma unroll
-                for (int wd = 0; wd < NWD; ++wd) {
-                    const uint32_t pl = prmt(va[0][wd], va[1][wd], 0x5140u);
-                    const uint32_t ph = prmt(va[0][wd], va[1][wd], 0x7362u);
-                    const uint32_t ql = prmt(va[2][wd], va[3][wd], 0x5140u);
-                    const uint32_t qh = prmt(va[2][wd], va[3][wd], 0x7362u);
-                    mma16816<true>(acc[4 * wd + 0], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(lo16(pl)),
-                                   e4m3x2_to_f16x2(lo16(ql)));
-                    mma16816<true>(acc[4 * wd + 1], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(hi16(pl)),
-                                   e4m3x2_to_f16x2(hi16(ql)));
-                    mma16816<true>(acc[4 * wd + 2], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(lo16(ph)),
-                                   e4m3x2_to_f16x2(lo16(qh)));
-                    mma16816<true>(acc[4 * wd + 3], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(hi16(ph)),
-                                   e4m3x2_to_f16x2(hi16(qh)));
-                }
             }
-        } else {
-            ++bad_pages;
+            // ---- O += P V, page by page (P as the A operand: rows g / g+8,
+            // tokens 2t.. and 8+2t.. of the page) -----------------------------
+#pragma unroll
+            for (int j = 0; j < PG; ++j) {
+                if (valid[j] <= 0) continue;
+                const float* p0r = pr[2 * j];
+                const float* p1r = pr[2 * j + 1];
+                uint32_t pa0, pa1 = 0u, pa2, pa3 = 0u;
+                if constexpr (FP8) {
+                    pa0 = pack_f16(p0r[0], p0r[1]);
+                    pa2 = pack_f16(p1r[0], p1r[1]);
+                    if constexpr (TWO) {
+                        pa1 = pack_f16(p0r[2], p0r[3]);
+                        pa3 = pack_f16(p1r[2], p1r[3]);
+                    }
+                } else {
+                    pa0 = pack_bf16(p0r[0], p0r[1]);
+                    pa2 = pack_bf16(p1r[0], p1r[1]);
+                    if constexpr (TWO) {
+                        pa1 = pack_bf16(p0r[2], p0r[3]);
+                        pa3 = pack_bf16(p1r[2], p1r[3]);
+                    }
+                }
+                pv_page(ring0 + ((i + j) % C::NSLOT) * C::SLOT + C::PAGE, valid[j], pa0, pa1, pa2, pa3);
+            }
         }
 
-        // ---- refill this slot with page i + NSLOT ------------------------------
+        // ---- refill the consumed slots with pages i + NSLOT .. ----------------
         __syncwarp();
-        const int nx = i + C::NSLOT;
-        if (nx < nw) {
-            const int pid2 = page_id(nx, i >> 5);
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                issue(nx, pid2);
+#pragma unroll
+        for (int j = 0; j < PG; ++j) {
+            const int nx = i + j + C::NSLOT;
+            if (nx < nw) {
+                const int pid2 = page_id(nx, i >> 5);
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    issue(nx, pid2);
+                }
             }
         }
     }

@@ -190,6 +190,7 @@ pkv_status pkv_rope_kv_write(const pkv_tensor* q_p, const pkv_tensor* k_p, const
     if (positions.stride[0] != 1 || slot_mapping.stride[0] != 1) return PKV_ERR_UNSUPPORTED;
     if (!row16(k, 2) || !row16(v, 2) || (q.ptr && !row16(q, 2))) return PKV_ERR_UNSUPPORTED;
     if (!row16(cos_sin, 1)) return PKV_ERR_UNSUPPORTED;
+    if ((Hq + 2 * Hkv) * (D / 16) > 1024) return PKV_ERR_UNSUPPORTED;  // one token's rows per CTA
 
     pkv::RopeArgs a{};
     a.q = static_cast<uint16_t*>(q.ptr);

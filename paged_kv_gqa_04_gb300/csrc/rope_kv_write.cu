@@ -6,8 +6,9 @@
 // separate q/k/v. microLLM-rocm, optimisation checkpoints: split-half RoPE
 // reading the projection layout and writing the attention layout directly.
 //
-// Mapping: every (token, row) -- a q head, a k head or a v head -- is handled
-// by D/16 threads; thread c of a row owns the 8-element chunk starting at 8c
+// Mapping: a CTA is a 2-D block, x = the (row, chunk) items of one token and
+// y = tokens. Every (token, row) -- a q head, a k head or a v head -- is
+// handled by D/16 threads; thread c of a row owns the 8-element chunk starting at 8c
 // and the chunk starting at D/2 + 8c. Under NeoX these two chunks are exactly
 // the partners of one another's rotation pairs (i, i + D/2); under the
 // interleaved style each chunk holds four whole pairs (2i, 2i+1). Every
@@ -18,8 +19,10 @@
 // Arithmetic: y1 = x1*c - x2*s and y2 = x2*c + x1*s with every product and
 // the sum/difference rounded separately (__fmul_rn/__fsub_rn/__fadd_rn are
 // never contracted into FMA), then bf16 round-to-nearest-even, or for FP8
-// the correctly rounded quotient y / scale (__fdiv_rn) followed by the
-// hardware's saturating round-to-nearest-even E4M3 conversion.
+// the E4M3 byte of the correctly rounded quotient y / scale (from a
+// reciprocal product when that provably gives the same byte, else from the
+// IEEE division), with the hardware's saturating round-to-nearest-even
+// E4M3 conversion.
 #include <cuda_fp8.h>
 
 #include "pkv_internal.h"
@@ -52,18 +55,43 @@ __device__ __forceinline__ uint4 pack_bf16x8(const Chunk8& c) {
     return w;
 }
 
-__device__ __forceinline__ uint2 pack_e4m3x8(const Chunk8& c, float scale) {
+// True when some float within six representable steps of z may round to a
+// different E4M3 byte than z: z is below the normal E4M3 range (|z| < 2^-6,
+// including zero), or the 20 bits below E4M3's mantissa are within 6 of the
+// midpoint pattern 0x80000, i.e. ((m + 0x80006) mod 2^20) <= 12. Anything
+// else (the E4M3 values themselves and the powers of two where binades
+// change lie far from midpoints; magnitudes of 448 and above all saturate
+// to 448, and the test only errs on the safe side there) keeps its byte.
+__device__ __forceinline__ bool e4m3_byte_may_change(float z) {
+    const uint32_t b = __float_as_uint(z);
+    return (b & 0x7FFFFFFFu) < 0x3C800000u || ((b + 0x80006u) & 0xFFFFFu) <= 12u;
+}
+
+// E4M3 bytes (low byte first) of the correctly rounded float32 quotients
+// y / scale, saturating, for the 8 values of a chunk. z = RN(y * r) with
+// r = RN(1 / scale) is within two units in the last place of y / scale, so
+// the correctly rounded quotient lies within five representable steps of z.
+// When no value of the chunk is near an E4M3 rounding boundary, the bytes of
+// the products are the bytes of the quotients and no division is needed;
+// otherwise (rare) the chunk is quantised from IEEE divisions.
+__device__ __forceinline__ uint2 pack_e4m3x8(const Chunk8& c, float scale, float rcp) {
+    float z[8];
+    bool near = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        z[j] = __fmul_rn(c.v[j], rcp);
+        near |= e4m3_byte_may_change(z[j]);
+    }
+    if (near) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) z[j] = __fdiv_rn(c.v[j], scale);
+    }
     uint32_t w[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        uint32_t b = 0;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            float2 z = make_float2(__fdiv_rn(c.v[4 * h + 2 * i], scale), __fdiv_rn(c.v[4 * h + 2 * i + 1], scale));
-            __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(z, __NV_SATFINITE, __NV_E4M3);
-            b |= static_cast<uint32_t>(p) << (16 * i);
-        }
-        w[h] = b;
+        const uint32_t b0 = __nv_cvt_float2_to_fp8x2(make_float2(z[4 * h], z[4 * h + 1]), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t b1 = __nv_cvt_float2_to_fp8x2(make_float2(z[4 * h + 2], z[4 * h + 3]), __NV_SATFINITE, __NV_E4M3);
+        w[h] = b0 | (b1 << 16);
     }
     return make_uint2(w[0], w[1]);
 }
@@ -73,16 +101,33 @@ __device__ __forceinline__ void rot(float x1, float x2, float c, float s, float&
     y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
 }
 
+// The cos and sin a thread needs for its two chunks, loaded as four 16-byte
+// vectors. NeoX: chunk 8c pairs with chunk D/2 + 8c at frequencies 8c..8c+7.
+// Interleaved: chunk 8c holds the pairs of frequencies 4c..4c+3, chunk
+// D/2 + 8c those of D/4 + 4c .. D/4 + 4c + 3.
 template <int D, bool INTER>
-__device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float* cs, int c) {
+__device__ __forceinline__ void load_cos_sin(const float* cs, int c, float (&cv)[8], float (&sv)[8]) {
+    float4 a0, a1, b0, b1;
     if constexpr (!INTER) {
-        // pairs (8c + j, D/2 + 8c + j), frequency index 8c + j
-        const float4 c0 = *reinterpret_cast<const float4*>(cs + 8 * c);
-        const float4 c1 = *reinterpret_cast<const float4*>(cs + 8 * c + 4);
-        const float4 s0 = *reinterpret_cast<const float4*>(cs + D / 2 + 8 * c);
-        const float4 s1 = *reinterpret_cast<const float4*>(cs + D / 2 + 8 * c + 4);
-        const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        a0 = *reinterpret_cast<const float4*>(cs + 8 * c);
+        a1 = *reinterpret_cast<const float4*>(cs + 8 * c + 4);
+        b0 = *reinterpret_cast<const float4*>(cs + D / 2 + 8 * c);
+        b1 = *reinterpret_cast<const float4*>(cs + D / 2 + 8 * c + 4);
+    } else {
+        a0 = *reinterpret_cast<const float4*>(cs + 4 * c);
+        a1 = *reinterpret_cast<const float4*>(cs + D / 4 + 4 * c);
+        b0 = *reinterpret_cast<const float4*>(cs + D / 2 + 4 * c);
+        b1 = *reinterpret_cast<const float4*>(cs + D / 2 + D / 4 + 4 * c);
+    }
+    cv[0] = a0.x; cv[1] = a0.y; cv[2] = a0.z; cv[3] = a0.w;
+    cv[4] = a1.x; cv[5] = a1.y; cv[6] = a1.z; cv[7] = a1.w;
+    sv[0] = b0.x; sv[1] = b0.y; sv[2] = b0.z; sv[3] = b0.w;
+    sv[4] = b1.x; sv[5] = b1.y; sv[6] = b1.z; sv[7] = b1.w;
+}
+
+template <bool INTER>
+__device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float (&cv)[8], const float (&sv)[8]) {
+    if constexpr (!INTER) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             float y1, y2;
@@ -91,103 +136,138 @@ __device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float* 
             hi.v[j] = y2;
         }
     } else {
-        // chunk 8c holds pairs of frequency 4c..4c+3; chunk D/2 + 8c holds
-        // pairs of frequency D/4 + 4c .. D/4 + 4c + 3
-        const float4 cl = *reinterpret_cast<const float4*>(cs + 4 * c);
-        const float4 sl = *reinterpret_cast<const float4*>(cs + D / 2 + 4 * c);
-        const float4 ch = *reinterpret_cast<const float4*>(cs + D / 4 + 4 * c);
-        const float4 sh = *reinterpret_cast<const float4*>(cs + D / 2 + D / 4 + 4 * c);
-        const float clv[4] = {cl.x, cl.y, cl.z, cl.w}, slv[4] = {sl.x, sl.y, sl.z, sl.w};
-        const float chv[4] = {ch.x, ch.y, ch.z, ch.w}, shv[4] = {sh.x, sh.y, sh.z, sh.w};
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             float y1, y2;
-            rot(lo.v[2 * m], lo.v[2 * m + 1], clv[m], slv[m], y1, y2);
+            rot(lo.v[2 * m], lo.v[2 * m + 1], cv[m], sv[m], y1, y2);
             lo.v[2 * m] = y1;
             lo.v[2 * m + 1] = y2;
-            rot(hi.v[2 * m], hi.v[2 * m + 1], chv[m], shv[m], y1, y2);
+            rot(hi.v[2 * m], hi.v[2 * m + 1], cv[4 + m], sv[4 + m], y1, y2);
             hi.v[2 * m] = y1;
             hi.v[2 * m + 1] = y2;
         }
     }
 }
 
-template <int D, bool INTER, bool FP8>
-__global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a, const int64_t total) {
+// U tokens per thread: all of their loads (slot, position, the row's two
+// chunks, then the cos/sin rows) are issued before any token is processed,
+// so a thread keeps U times as many bytes in flight.
+template <int D, bool INTER, bool FP8, int U>
+__global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(const RopeArgs a) {
     constexpr int TPR = D / 16;  // threads per row
     // The decode kernel that usually follows may start its prologue now; it
     // waits for this grid's writes before it reads q or the cache.
     grid_dep_launch();
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= total) return;
-    const int rows = a.Hq + 2 * a.Hkv;
-    const int64_t per_tok = static_cast<int64_t>(rows) * TPR;
-    const int64_t t = idx / per_tok;
-    const int r = static_cast<int>(idx - t * per_tok);
+    // threadIdx.x: the (row, chunk) work items of one token; threadIdx.y, u
+    // and blockIdx.x: tokens. No division is needed to find either.
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.y * U + threadIdx.y;
+    const int r = threadIdx.x;
     const int row = r / TPR;
     const int c = r % TPR;
-
-    // slot, position and the row's two chunks do not depend on one another:
-    // all four loads are issued before any of them is checked (reading the
-    // row of a skipped token stays inside the [T, heads, D] input).
     const bool is_q = row < a.Hq;
     const bool is_k = !is_q && row < a.Hq + a.Hkv;
     const int h = is_q ? row : (is_k ? row - a.Hq : row - a.Hq - a.Hkv);
-    const uint16_t* src = is_q ? a.q + t * a.q_s0 + h * a.q_s1
-                               : (is_k ? a.k + t * a.k_s0 + h * a.k_s1 : a.v + t * a.v_s0 + h * a.v_s1);
-    const int32_t slot = __ldg(a.slots + t);
-    const int32_t pos = __ldg(a.positions + t);
-    const uint4 wlo = *reinterpret_cast<const uint4*>(src + 8 * c);
-    const uint4 whi = *reinterpret_cast<const uint4*>(src + D / 2 + 8 * c);
-    if (slot < 0) return;
     const int64_t num_slots = a.num_pages * a.page_size;
-    if (slot >= num_slots) {
-        if (r == 0) flag_error(a.err, PKV_FLAG_SLOT_RANGE);
-        return;
-    }
-    if (pos < 0 || pos >= a.max_pos) {
-        if (r == 0) flag_error(a.err, PKV_FLAG_POSITION_RANGE);
-        return;
-    }
-    const float* cs = a.cos_sin + pos * a.cs_s0;
-    Chunk8 lo = unpack_bf16x8(wlo);
-    Chunk8 hi = unpack_bf16x8(whi);
 
-    if (is_q) {  // q head: rotate in place
-        rotate_row<D, INTER>(lo, hi, cs, c);
-        uint16_t* p = a.q + t * a.q_s0 + h * a.q_s1;
-        *reinterpret_cast<uint4*>(p + 8 * c) = pack_bf16x8(lo);
-        *reinterpret_cast<uint4*>(p + D / 2 + 8 * c) = pack_bf16x8(hi);
-        return;
+    // Reading the row of a skipped token stays inside the [T, heads, D] input.
+    int32_t slot[U], pos[U];
+    uint4 wlo[U], whi[U];
+    bool live[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t t = t0 + static_cast<int64_t>(u) * blockDim.y;
+        live[u] = t < a.T;
+        if (!live[u]) continue;
+        const uint16_t* src = is_q ? a.q + t * a.q_s0 + h * a.q_s1
+                                   : (is_k ? a.k + t * a.k_s0 + h * a.k_s1 : a.v + t * a.v_s0 + h * a.v_s1);
+        slot[u] = __ldg(a.slots + t);
+        pos[u] = __ldg(a.positions + t);
+        wlo[u] = *reinterpret_cast<const uint4*>(src + 8 * c);
+        whi[u] = *reinterpret_cast<const uint4*>(src + D / 2 + 8 * c);
     }
-    if (is_k) rotate_row<D, INTER>(lo, hi, cs, c);
+    float cv[U][8], sv[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (!live[u] || slot[u] < 0) {
+            live[u] = false;
+            continue;
+        }
+        if (slot[u] >= num_slots) {
+            if (r == 0) flag_error(a.err, PKV_FLAG_SLOT_RANGE);
+            live[u] = false;
+            continue;
+        }
+        if (pos[u] < 0 || pos[u] >= a.max_pos) {
+            if (r == 0) flag_error(a.err, PKV_FLAG_POSITION_RANGE);
+            live[u] = false;
+            continue;
+        }
+        if (is_q || is_k) load_cos_sin<D, INTER>(a.cos_sin + pos[u] * a.cs_s0, c, cv[u], sv[u]);
+    }
 
-    const int64_t page = slot / a.page_size;
-    const int off = static_cast<int>(slot - page * a.page_size);
-    const int64_t* st = is_k ? a.kc_s : a.vc_s;
-    const int64_t e = (a.layout == PKV_HND) ? page * st[0] + h * st[1] + off * st[2]
-                                            : page * st[0] + off * st[1] + h * st[2];
+    float scale = 1.f, rcp = 1.f;
     if constexpr (FP8) {
-        const float* sp = is_k ? a.k_scale : a.v_scale;
-        const float scale = __ldg(sp + (a.n_scale == 1 ? 0 : h));
-        uint8_t* dst = static_cast<uint8_t*>(is_k ? a.k_cache : a.v_cache) + e;
-        *reinterpret_cast<uint2*>(dst + 8 * c) = pack_e4m3x8(lo, scale);
-        *reinterpret_cast<uint2*>(dst + D / 2 + 8 * c) = pack_e4m3x8(hi, scale);
-    } else {
-        uint16_t* dst = static_cast<uint16_t*>(is_k ? a.k_cache : a.v_cache) + e;
-        *reinterpret_cast<uint4*>(dst + 8 * c) = pack_bf16x8(lo);
-        *reinterpret_cast<uint4*>(dst + D / 2 + 8 * c) = pack_bf16x8(hi);
+        if (!is_q) {
+            scale = __ldg((is_k ? a.k_scale : a.v_scale) + (a.n_scale == 1 ? 0 : h));
+            rcp = __frcp_rn(scale);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (!live[u]) continue;
+        const int64_t t = t0 + static_cast<int64_t>(u) * blockDim.y;
+        Chunk8 lo = unpack_bf16x8(wlo[u]);
+        Chunk8 hi = unpack_bf16x8(whi[u]);
+        if (is_q) {  // q head: rotate in place
+            rotate_row<INTER>(lo, hi, cv[u], sv[u]);
+            uint16_t* p = a.q + t * a.q_s0 + h * a.q_s1;
+            *reinterpret_cast<uint4*>(p + 8 * c) = pack_bf16x8(lo);
+            *reinterpret_cast<uint4*>(p + D / 2 + 8 * c) = pack_bf16x8(hi);
+            continue;
+        }
+        if (is_k) rotate_row<INTER>(lo, hi, cv[u], sv[u]);
+        int64_t page;
+        int off;
+        if (a.page_size == 16) {  // the decode kernel's page size: no division
+            page = slot[u] >> 4;
+            off = slot[u] & 15;
+        } else {
+            page = slot[u] / a.page_size;
+            off = static_cast<int>(slot[u] - page * a.page_size);
+        }
+        const int64_t* st = is_k ? a.kc_s : a.vc_s;
+        const int64_t e = (a.layout == PKV_HND) ? page * st[0] + h * st[1] + off * st[2]
+                                                : page * st[0] + off * st[1] + h * st[2];
+        if constexpr (FP8) {
+            uint8_t* dst = static_cast<uint8_t*>(is_k ? a.k_cache : a.v_cache) + e;
+            *reinterpret_cast<uint2*>(dst + 8 * c) = pack_e4m3x8(lo, scale, rcp);
+            *reinterpret_cast<uint2*>(dst + D / 2 + 8 * c) = pack_e4m3x8(hi, scale, rcp);
+        } else {
+            uint16_t* dst = static_cast<uint16_t*>(is_k ? a.k_cache : a.v_cache) + e;
+            *reinterpret_cast<uint4*>(dst + 8 * c) = pack_bf16x8(lo);
+            *reinterpret_cast<uint4*>(dst + D / 2 + 8 * c) = pack_bf16x8(hi);
+        }
     }
 }
 
 template <int D, bool INTER, bool FP8>
 cudaError_t launch_t(const RopeArgs& a, cudaStream_t s) {
-    const int64_t total = a.T * static_cast<int64_t>(a.Hq + 2 * a.Hkv) * (D / 16);
-    if (total == 0) return cudaSuccess;
-    const int threads = 256;
-    const int64_t blocks = (total + threads - 1) / threads;
+    if (a.T == 0) return cudaSuccess;
+    const int per_tok = (a.Hq + 2 * a.Hkv) * (D / 16);  // work items of one token
+    if (per_tok > 1024) return cudaErrorInvalidConfiguration;
+    const int toks = per_tok >= 256 ? 1 : 256 / per_tok;  // tokens per CTA row of threads
+    // Two tokens per thread when there are enough tokens to keep every SM
+    // busy (cache fills of a bf16 cache); one for a decode step's few tokens
+    // and for FP8 caches (measured slower there: the quantiser's registers
+    // cost more occupancy than the second token's loads gain).
+    const bool two = !FP8 && a.T >= 8192 && per_tok * toks <= 512;
+    const int64_t per_cta = static_cast<int64_t>(toks) * (two ? 2 : 1);
+    const int64_t blocks = (a.T + per_cta - 1) / per_cta;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-    rope_kv_write_kernel<D, INTER, FP8><<<static_cast<unsigned>(blocks), threads, 0, s>>>(a, total);
+    if (two)
+        rope_kv_write_kernel<D, INTER, FP8, 2><<<static_cast<unsigned>(blocks), dim3(per_tok, toks), 0, s>>>(a);
+    else
+        rope_kv_write_kernel<D, INTER, FP8, 1><<<static_cast<unsigned>(blocks), dim3(per_tok, toks), 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -227,3 +227,100 @@ def test_back_to_back_steps_and_step_graphs_match_a_single_step():
     assert np.array_equal(g2.out_h.view(torch.int16).numpy().view(np.uint16), ref[0])
     assert np.array_equal(dw.cache_pages_u(dw.k_cache, np.arange(w.num_pages)), ref_k)
     assert int(dw.err.item()) == 0
+
+
+@pytest.mark.parametrize("cache_dtype", synth.CACHE_DTYPES)
+def test_packed_qkv_views(cache_dtype):
+    """q, k and v given as strided views of one packed [T, Hq + 2 Hkv, D]
+    projection output (no copies): same bytes as contiguous inputs; the
+    decode then reads q from the same packed buffer."""
+    w = synth.custom_workload("packed", 80, [23, 64, 130], 12, 2, 128, cache_dtype=cache_dtype, rope_base=1e6)
+    ref = harness.DeviceWorkload(w, num_splits=2)
+    ref.fill()
+    d = ref.upload_decode()
+    ref.step()
+    torch.cuda.synchronize()
+    B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
+    packed = torch.empty((B, Hq + 2 * Hkv, D), dtype=torch.bfloat16, device="cuda")
+    packed[:, :Hq] = d["q0"]
+    packed[:, Hq:Hq + Hkv] = d["k"]
+    packed[:, Hq + Hkv:] = d["v"]
+    q, k, v = packed[:, :Hq], packed[:, Hq:Hq + Hkv], packed[:, Hq + Hkv:]
+    assert not q.is_contiguous()
+    dw = harness.DeviceWorkload(w, num_splits=2)
+    dw.fill()
+    dw.write(q, k, v, d["positions"], d["slot_mapping"])
+    dw.decode(q)
+    dw.merge()
+    torch.cuda.synchronize()
+    assert np.array_equal(dw.bf16_u16(q), ref.bf16_u16(d["q"]))
+    for cache in ("k_cache", "v_cache"):
+        assert torch.equal(getattr(dw, cache), getattr(ref, cache))
+    assert np.array_equal(dw.bf16_u16(dw.out), ref.bf16_u16(ref.out))
+    assert torch.equal(dw.lse, ref.lse)
+
+
+def test_validate_without_slots_and_strided_tables():
+    """Block tables given as a column slice of a wider buffer, and no slot
+    mapping: only the sequence checks run."""
+    w = synth.custom_workload("val2", 81, [40, 3, 100], 4, 2, 128, num_pages=30)
+    wide = np.full((w.B, w.max_pages + 5), 7, np.int32)
+    wide[:, 2:2 + w.max_pages] = w.block_tables
+    bt = torch.from_numpy(wide).cuda()[:, 2:2 + w.max_pages]
+    assert not bt.is_contiguous()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _abi.validate_indices(bt, sl, None, w.num_pages, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    bt[1, 0] = -5
+    _abi.validate_indices(bt, sl, None, w.num_pages, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == _abi.FLAG_PAGE_RANGE
+
+
+def _e4m3_midpoints():
+    """Positive midpoints between consecutive E4M3 magnitudes, normal range
+    and below (from the oracle's decode table), plus the saturation edge."""
+    mags = np.array(sorted(v for v in oracle.e4m3_table()[:127]), np.float64)
+    mids = (mags[1:] + mags[:-1]) / 2
+    return np.concatenate([mids, [448.0, 464.0, 2.0 ** -6, 2.0 ** -9]])
+
+
+@pytest.mark.parametrize("scale", [0.0137, 0.05, 1.0 / 3.0, 0.1, 3.5])
+def test_fp8_write_near_every_rounding_boundary(scale):
+    """Arbitrary float32 values reach the quantiser through the table:
+    with k = [1 .. 1 | 0 .. 0] (NeoX halves), the rotated row is exactly
+    (cos_i, sin_i). Values are placed at scale * (each E4M3 midpoint) and up
+    to 8 float steps either side, both signs: the E4M3 bytes must equal the
+    oracle's f32(y / scale) encoding."""
+    D = 128
+    sc = np.float32(scale)
+    base = (_e4m3_midpoints() * np.float64(sc)).astype(np.float32)
+    vals = []
+    for k in range(-8, 9):
+        vals.append((base.view(np.int32) + k).view(np.float32))
+    vals = np.concatenate(vals)
+    vals = np.concatenate([vals, -vals])
+    T = (len(vals) + D - 1) // D
+    vals = np.resize(vals, T * D).astype(np.float32)
+    cs = vals.reshape(T, D).copy()                    # row t: cos half, sin half
+    k = np.zeros((T, 1, D), np.uint16)
+    k[:, 0, :D // 2] = 0x3F80                         # 1.0 in bf16; second half 0
+    v = np.zeros_like(k)
+    pos = np.arange(T, dtype=np.int32)
+    slots = np.arange(T, dtype=np.int32)
+    w = synth.custom_workload("mid", 6, [max(T, 1)], 1, 1, D, cache_dtype="fp8", num_pages=(T + 15) // 16)
+    sca = np.array([sc], np.float32)
+    kc = oracle.empty_cache(w.cache_shape(), "fp8"); vc = np.zeros_like(kc)
+    oracle.rope_kv_write(None, k, v, pos, cs, kc, vc, slots, "HND", "neox", sca, sca)
+    dw = harness.DeviceWorkload(w, num_splits=1)
+    dw.cos_sin = torch.from_numpy(cs).cuda()
+    dw.k_scale = torch.from_numpy(sca).cuda()
+    dw.v_scale = torch.from_numpy(sca).cuda()
+    dw.write(None, harness._u16_to_bf16(k, "cuda"), harness._u16_to_bf16(v, "cuda"), torch.from_numpy(pos).cuda(),
+             torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    got = dw.cache_pages_u(dw.k_cache, np.arange(w.num_pages))
+    assert np.array_equal(got, kc)
+    assert int(dw.err.item()) == 0
