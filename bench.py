@@ -61,6 +61,8 @@ WORKLOAD_TEXT = {
     "fp8": "FP8 E4M3 paged cache decode: B64, seq_lens ~U[2048,16384], 12 q / 2 kv heads, D128, HND, per-head "
            "static K/V scales ~U[0.01,0.1]",
     "tiny": "tiny paged GQA decode: B2, seq_lens {37,100}, 4 q / 2 kv heads, D64, HND",
+    "million": "1M-token decode: B1, seq_len 1048576, 8 q / 1 kv heads (GQA 8), D128, page 16, HND, bf16, "
+               "65536-page shuffled pool",
 }
 
 
@@ -72,7 +74,7 @@ def parse_args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="qwen", choices=sorted(WORKLOAD_TEXT))
     p.add_argument("--splits", type=int, default=0, help="num_splits (0 = the library's heuristic)")
-    p.add_argument("--also", default="longctx,ragged,fp8",
+    p.add_argument("--also", default="longctx,ragged,fp8,million",
                    help="extra workloads whose decode roofline is reported under 'other_workloads' ('' = none)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -386,6 +388,13 @@ def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -
         b.record(stream)
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    rs = time_steps(dw, 20, 3, 1, flush, True)
+    rc = time_steps(dw, 20, 3, 1, flush, False)
+    step = dict(chained_us=1e3 * statistics.mean(rc["step_ms"]),
+                tokens_per_s=w.B / (statistics.mean(rc["step_ms"]) * 1e-3),
+                separated_us={"rope_kv_write": 1e3 * statistics.mean(rs["write_ms"]),
+                              "paged_gqa_decode": 1e3 * statistics.mean(rs["decode_ms"]),
+                              "lse_merge": 1e3 * statistics.mean(rs["merge_ms"])})
     layered = measure_layered(dw, 4 if decode_alg_bytes(w) < 1e9 else 2, 5, flush, peak)
     fill = time_fill(dw, 5, flush)
     wb = write_alg_bytes(w, fill["T"], False)
@@ -396,7 +405,7 @@ def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -
              cache_write_gbs=wb / (fill["ms"] * 1e-3) / 1e9,
              cache_write_frac=wb / (fill["ms"] * 1e-3) / 1e9 / peak,
              cache_write_frac_table_rows_once=wbu / (fill["ms"] * 1e-3) / 1e9 / peak, err_flag=int(dw.err.item()),
-             stream_read_frac_same_bytes=stream_ceiling(alg, flush) / peak, layered=layered)
+             stream_read_frac_same_bytes=stream_ceiling(alg, flush) / peak, layered=layered, step=step)
     del dw
     torch.cuda.empty_cache()
     return r

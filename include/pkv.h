@@ -201,8 +201,9 @@ pkv_status pkv_lse_merge(const pkv_tensor* out_partial, const pkv_tensor* lse_pa
  * B, Hkv: batch and kv heads; total_pages = sum over the batch of
  * ceil(seq_len/16); max_pages = the largest ceil(seq_len/16); cache_dtype a
  * pkv_dtype; sm_count the device's SM count. Models each split as one CTA
- * and returns the S in [1, 64] with the lowest estimated time for streaming
- * the pages over the GPU's CTA slots plus the merge's extra traffic.
+ * and returns the S in [1, 1024] with the lowest estimated time for
+ * streaming the pages over the GPU's CTA slots plus the merge's extra
+ * traffic and round trips.
  * Returns 1 for empty or invalid input.
  */
 int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int64_t total_pages,

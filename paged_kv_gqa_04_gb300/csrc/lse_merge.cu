@@ -4,15 +4,20 @@
 // their log-sum-exp weights; Loom Kernels, "Attention" row: local
 // split-K/LSE merge.
 //
-// One warp per (sequence, query head) row. The warp reads the row's S LSE
-// values, forms M = max and the weights w_s = exp(lse_s - M), then each lane
-// accumulates D/32 consecutive output columns over the S partial rows with
-// 8- or 16-byte loads (a partial row of D floats is one fully coalesced
-// 256/512-byte read), divides by sum w_s and writes bf16 (round to nearest
-// even) plus lse = M + ln sum w_s. The kernel is latency-bound (the partials
+// A warp merges a run of splits of one (sequence, query head) row: it reads
+// their LSE values, forms their max M and the weights w_s = exp(lse_s - M),
+// and each lane accumulates D/32 consecutive output columns over the partial
+// rows with 8- or 16-byte loads (a partial row of D floats is one coalesced
+// 256/512-byte read). With up to 32 splits one warp does the whole row and
+// writes bf16 (round to nearest even) out = sum w_s o_s / sum w_s and
+// lse = M + ln sum w_s. With more, the row is a two-level tree (mainarch,
+// decode-attention section: a parallel tree combine rather than one
+// workgroup grinding through the partials): up to 16 warps of one CTA each
+// merge a contiguous run of splits in parallel and their results are merged
+// again by their own LSE weights. The kernel is latency-bound (the partials
 // are a few MB): partial rows are loaded in batches of sixteen, the first
 // together with the LSE values and each next one while the previous batch is
-// summed, and the CTAs are two warps so the rows spread over many SMs.
+// summed.
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
@@ -38,82 +43,144 @@ struct Vec<2> {
     }
 };
 
-constexpr int kBatch = 16;  // partial rows in flight per lane
+// One warp's share of a row: splits [s_lo, s_hi). Returns the warp's LSE
+// maximum m (-inf when every split in the range is empty), the weight sum
+// l = sum_s exp(lse_s - m) (warp-reduced, every lane holds it) and, per
+// lane, acc = sum_s exp(lse_s - m) * out_partial_s over the lane's V columns.
+// All loads of a batch of 16 partial rows are issued before any is used: the
+// first batch goes out with the first 32 LSE values, each later batch while
+// the previous one is summed. (16 rows per batch for a warp that merges a
+// whole row, 8 in the tree kernel, whose 16 warps share the register file.)
+template <int V, int kBatch>
+__device__ __forceinline__ void warp_merge(const float* lse, int64_t lp_s1, const float* op, int64_t op_s1, int s_lo,
+                                           int s_hi, float& m, float& l, float (&acc)[V]) {
+    using VT = typename Vec<V>::T;
+    const int lane = threadIdx.x & 31;
+    const int n = s_hi - s_lo;
+    lse += s_lo * lp_s1;
+    op += s_lo * op_s1;
+    float lv = (lane < n) ? __ldg(lse + lane * lp_s1) : -INFINITY;
+    VT x[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+        if (j < n) x[j] = __ldg(reinterpret_cast<const VT*>(op + j * op_s1));
+    m = lv;
+    for (int s = 32 + lane; s < n; s += 32) m = fmaxf(m, __ldg(lse + s * lp_s1));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    l = 0.f;
+    if (m == -INFINITY) return;
+    float w_mine = (lane < n) ? __expf(lv - m) : 0.f;
+    float wsum = w_mine;
+    for (int s0 = 0; s0 < n; s0 += kBatch) {
+        VT y[kBatch];
+        const int s1 = s0 + kBatch;
+        if (s1 < n) {  // next batch in flight while this one is summed
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (s1 + j < n) y[j] = __ldg(reinterpret_cast<const VT*>(op + (s1 + j) * op_s1));
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int s = s0 + j;
+            if ((s & 31) == 0 && s > 0) {  // weights of splits s .. s+31
+                w_mine = (s + lane < n) ? __expf(__ldg(lse + (s + lane) * lp_s1) - m) : 0.f;
+                wsum += w_mine;
+            }
+            const float w = __shfl_sync(0xffffffffu, w_mine, s & 31);
+            if (s < n) Vec<V>::fma(acc, w, x[j]);
+        }
+        if (s1 < n) {
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) x[j] = y[j];
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    l = wsum;
+}
 
+template <int V>
+__device__ __forceinline__ void store_row(uint16_t* dst, const float (&o)[V]) {
+    if constexpr (V == 4) {
+        uint2 w;
+        w.x = pack_bf16(o[0], o[1]);
+        w.y = pack_bf16(o[2], o[3]);
+        *reinterpret_cast<uint2*>(dst) = w;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16(o[0], o[1]);
+    }
+}
+
+// Few splits (S <= 32): one warp per row, two rows per CTA.
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs a) {
     constexpr int V = D / 32;  // columns per lane
-    using VT = typename Vec<V>::T;
-    grid_dep_wait();  // the partials come from the preceding decode grid
+    grid_dep_wait();           // the partials come from the preceding decode grid
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
     if (row >= static_cast<int64_t>(a.B) * a.Hq) return;
     const int b = static_cast<int>(row / a.Hq);
     const int h = static_cast<int>(row % a.Hq);
-    const float* lse = a.lse_partial + b * a.lp_s0 + h;
-    const float* op = a.out_partial + b * a.op_s0 + h * a.op_s2 + lane * V;
-    const int S = a.S;
-
-    // All loads of a batch are issued before any is used: the first batch of
-    // up to 16 partial rows goes out together with the LSE values, and each
-    // later batch is requested before the previous one is accumulated.
-    float lv = (lane < S) ? __ldg(lse + lane * a.lp_s1) : -INFINITY;
-    VT x[kBatch];
+    float m, l, acc[V];
+    warp_merge<V, 16>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1, a.out_partial + b * a.op_s0 + h * a.op_s2 + lane * V,
+                      a.op_s1, 0, a.S, m, l, acc);
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j)
-        if (j < S) x[j] = __ldg(reinterpret_cast<const VT*>(op + j * a.op_s1));
-    float m = lv;
-    for (int s = 32 + lane; s < S; s += 32) m = fmaxf(m, __ldg(lse + s * a.lp_s1));
-#pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-
-    float acc[V];
-#pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] = 0.f;
-    float wsum = 0.f;
-    if (m != -INFINITY) {
-        float w_mine = (lane < S) ? __expf(lv - m) : 0.f;
-        wsum = w_mine;
-        for (int s0 = 0; s0 < S; s0 += kBatch) {
-            VT y[kBatch];
-            const int s1 = s0 + kBatch;
-            if (s1 < S) {  // next batch in flight while this one is summed
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j)
-                    if (s1 + j < S) y[j] = __ldg(reinterpret_cast<const VT*>(op + (s1 + j) * a.op_s1));
-            }
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int s = s0 + j;
-                if ((s & 31) == 0 && s > 0) {  // weights of splits s .. s+31
-                    w_mine = (s + lane < S) ? __expf(__ldg(lse + (s + lane) * a.lp_s1) - m) : 0.f;
-                    wsum += w_mine;
-                }
-                const float w = __shfl_sync(0xffffffffu, w_mine, s & 31);
-                if (s < S) Vec<V>::fma(acc, w, x[j]);
-            }
-            if (s1 < S) {
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) x[j] = y[j];
-            }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-        const float inv = 1.f / wsum;
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] *= inv;
-    }
-    uint16_t* dst = a.out + b * a.o_s0 + h * a.o_s1 + lane * V;
-    if constexpr (V == 4) {
-        uint2 w;
-        w.x = pack_bf16(acc[0], acc[1]);
-        w.y = pack_bf16(acc[2], acc[3]);
-        *reinterpret_cast<uint2*>(dst) = w;
-    } else {
-        *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
-    }
+    for (int i = 0; i < V; ++i) acc[i] *= inv;
+    store_row<V>(a.out + b * a.o_s0 + h * a.o_s1 + lane * V, acc);
     if (a.lse_out && lane == 0)
-        a.lse_out[b * a.lo_s0 + h * a.lo_s1] = (m == -INFINITY) ? -INFINITY : m + __logf(wsum);
+        a.lse_out[b * a.lo_s0 + h * a.lo_s1] = (m == -INFINITY) ? -INFINITY : m + __logf(l);
+}
+
+// Many splits: a two-level tree. One CTA per row; each of its W warps
+// merges a contiguous chunk of the splits (all chunks in parallel), then the
+// W warp results are combined through shared memory by their own LSE weights.
+template <int D>
+__global__ void __launch_bounds__(512) lse_merge_tree_kernel(const MergeArgs a) {
+    constexpr int V = D / 32;
+    extern __shared__ float tree_smem[];  // W * D partial sums, then W maxima, W weight sums
+    grid_dep_wait();
+    const int W = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = blockIdx.x;
+    const int b = static_cast<int>(row / a.Hq);
+    const int h = static_cast<int>(row % a.Hq);
+    const int chunk = (a.S + W - 1) / W;
+    const int s_lo = min(a.S, warp * chunk), s_hi = min(a.S, s_lo + chunk);
+    float m, l, acc[V];
+    warp_merge<V, 8>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1, a.out_partial + b * a.op_s0 + h * a.op_s2 + lane * V,
+                     a.op_s1, s_lo, s_hi, m, l, acc);
+    float* sacc = tree_smem;
+    float* sm = tree_smem + W * D;
+    float* sl = sm + W;
+#pragma unroll
+    for (int i = 0; i < V; ++i) sacc[warp * D + lane * V + i] = acc[i];
+    if (lane == 0) {
+        sm[warp] = m;
+        sl[warp] = l;
+    }
+    __syncthreads();
+    float M = -INFINITY;
+    for (int w = 0; w < W; ++w) M = fmaxf(M, sm[w]);
+    float L = 0.f;
+    for (int w = 0; w < W; ++w) L += (sm[w] == -INFINITY) ? 0.f : __expf(sm[w] - M) * sl[w];
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    for (int d2 = threadIdx.x; d2 < D / 2; d2 += blockDim.x) {
+        float o0 = 0.f, o1 = 0.f;
+        for (int w = 0; w < W; ++w) {
+            if (sm[w] == -INFINITY) continue;
+            const float e = __expf(sm[w] - M);
+            o0 += e * sacc[w * D + 2 * d2];
+            o1 += e * sacc[w * D + 2 * d2 + 1];
+        }
+        *reinterpret_cast<uint32_t*>(a.out + b * a.o_s0 + h * a.o_s1 + 2 * d2) = pack_bf16(o0 * inv, o1 * inv);
+    }
+    if (a.lse_out && threadIdx.x == 0)
+        a.lse_out[b * a.lo_s0 + h * a.lo_s1] = (M == -INFINITY) ? -INFINITY : M + __logf(L);
 }
 
 }  // namespace
@@ -121,11 +188,21 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs 
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s) {
     const int64_t rows = static_cast<int64_t>(a.B) * a.Hq;
     if (rows == 0) return cudaSuccess;
-    const int64_t blocks = (rows + kWarps - 1) / kWarps;
-    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-    const dim3 grid(static_cast<unsigned>(blocks)), block(kWarps * 32);
-    if (a.D == 128) return launch_dependent(lse_merge_kernel<128>, grid, block, 0, s, a);
-    if (a.D == 64) return launch_dependent(lse_merge_kernel<64>, grid, block, 0, s, a);
+    if (a.S <= 32) {
+        const int64_t blocks = (rows + kWarps - 1) / kWarps;
+        if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+        const dim3 grid(static_cast<unsigned>(blocks)), block(kWarps * 32);
+        if (a.D == 128) return launch_dependent(lse_merge_kernel<128>, grid, block, 0, s, a);
+        if (a.D == 64) return launch_dependent(lse_merge_kernel<64>, grid, block, 0, s, a);
+        return cudaErrorInvalidValue;
+    }
+    if (rows > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    // one warp per 32 splits, 2..16 warps per row
+    const int W = a.S >= 16 * 32 ? 16 : (a.S + 31) / 32 < 2 ? 2 : (a.S + 31) / 32;
+    const size_t smem = static_cast<size_t>(W) * (a.D + 2) * sizeof(float);
+    const dim3 grid(static_cast<unsigned>(rows)), block(W * 32);
+    if (a.D == 128) return launch_dependent(lse_merge_tree_kernel<128>, grid, block, smem, s, a);
+    if (a.D == 64) return launch_dependent(lse_merge_tree_kernel<64>, grid, block, smem, s, a);
     return cudaErrorInvalidValue;
 }
 

@@ -372,7 +372,7 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
     const double work = static_cast<double>(Hkv) * static_cast<double>(total_pages);
     int best = 1;
     double best_cost = 1e300;
-    for (int S = 1; S <= 64; ++S) {
+    for (int S = 1; S <= 1024; ++S) {
         if (S > max_pages) break;
         const double ncta = units * S;
         const double longest = std::ceil(static_cast<double>(max_pages) / S) + c0;
@@ -381,7 +381,11 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
         if (ncta > slots) est = std::fmax(est, std::ceil(ncta / slots) * (total / ncta));
         // partial records written by the decode and read by the merge
         const double merge_bytes = 2.0 * B * S * static_cast<double>(Hq) * (D + 1) * 4.0;
-        const double cost = est + merge_bytes / (page_bytes * slots);
+        // the merge also pays about one memory round trip (~2 page times) per
+        // 16 partial rows one of its warps reads in sequence (up to 16 warps
+        // share a row beyond 32 splits)
+        const double rounds = S <= 32 ? std::ceil(S / 16.0) : std::ceil(std::ceil(S / 16.0) / 16.0);
+        const double cost = est + merge_bytes / (page_bytes * slots) + 2.0 * rounds;
         if (cost < best_cost * (1.0 - 1e-9)) {
             best_cost = cost;
             best = S;

@@ -304,8 +304,11 @@ def make_workload(name: str, seed: Optional[int] = None) -> Workload:
                 32/8, D128, NHD, interleaved base 5e5, 1% K rows x8
     fp8         B64, L ~ U[2048,16384], 12/2, D128, HND, E4M3 cache,
                 per-head K/V scales ~ U[0.01, 0.1]
+    million     B1, L = 2^20, 8/1 (GQA 8), D128, HND, NeoX base 1e6,
+                a 65536-page shuffled pool (the 1M-token regime of the
+                mainarch decode-attention tables)
     """
-    idx = {"tiny": 0, "qwen": 1, "longctx": 2, "ragged": 3, "fp8": 4}[name]
+    idx = {"tiny": 0, "qwen": 1, "longctx": 2, "ragged": 3, "fp8": 4, "million": 5}[name]
     seed = 1000 + idx if seed is None else seed
     if name == "tiny":
         L = np.array([37, 100], np.int32)
@@ -326,6 +329,10 @@ def make_workload(name: str, seed: Optional[int] = None) -> Workload:
         pool = int(((L.astype(np.int64) + 15) // 16).sum())
         return Workload(name, seed, 256, 32, 8, 128, "NHD", "interleaved", "bf16", 5e5, L, pool,
                         _pool_tables(seed, L, pool), None, None, outlier_p=0.01)
+    if name == "million":
+        L = np.full(1, 1 << 20, np.int32)
+        return Workload(name, seed, 1, 8, 1, 128, "HND", "neox", "bf16", 1e6, L, 1 << 16,
+                        _pool_tables(seed, L, 1 << 16), None, None)
     # fp8
     L = _uniform_int(seed, "lens", 64, 2048, 16384)
     pool = int(((L.astype(np.int64) + 15) // 16).sum())
@@ -335,7 +342,7 @@ def make_workload(name: str, seed: Optional[int] = None) -> Workload:
                     _pool_tables(seed, L, pool), ks, vs)
 
 
-WORKLOADS = ("tiny", "qwen", "longctx", "ragged", "fp8")
+WORKLOADS = ("tiny", "qwen", "longctx", "ragged", "fp8", "million")
 
 
 def custom_workload(name: str, seed: int, seq_lens, Hq: int, Hkv: int, D: int, layout: str = "HND",

@@ -69,7 +69,7 @@ def filled():
     cache.clear()
 
 
-@pytest.mark.parametrize("name", ["qwen", "longctx", "ragged", "fp8"])
+@pytest.mark.parametrize("name", ["qwen", "longctx", "ragged", "fp8", "million"])
 def test_full_size_sampled(filled, name):
     w, dw = filled(name)
     dw.decode_inputs["q"].copy_(dw.decode_inputs["q0"])

@@ -172,14 +172,20 @@ def test_page_permutation_gives_identical_output():
     assert np.array_equal(outs[0][2], outs[1][2])
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_lse_merge_random_partials(D):
-    B, S, Hq = 5, 37, 6
+@pytest.mark.parametrize("D,S", [(64, 37), (128, 37), (128, 1), (128, 32), (128, 33), (64, 100), (128, 1000),
+                                 (128, 4096)])
+def test_lse_merge_random_partials(D, S):
+    """Both merge forms: one warp per row (S <= 32) and the two-level tree
+    (S > 32, up to 16 warps per row)."""
+    B, Hq = (5, 6) if S <= 1000 else (2, 3)
     op = synth.normal_f32(synth.stream_key(40, "o"), B * S * Hq * D).reshape(B, S, Hq, D)
     lp = (synth.normal_f32(synth.stream_key(40, "l"), B * S * Hq) * 4).reshape(B, S, Hq)
     lp[0, :, 0] = -np.inf                       # an all-empty row
     lp[1, 3:, :] = -np.inf                      # empty tail splits
     op[1, 3:, :, :] = 0.0
+    if S > 40:
+        lp[0, : S // 2, 1] = -np.inf            # a row whose first half is empty (whole warps' chunks)
+        op[0, : S // 2, 1, :] = 0.0
     out_ref, lse_ref = oracle.lse_merge(op.astype(np.float64), lp.astype(np.float64))
     opg = torch.from_numpy(op).cuda(); lpg = torch.from_numpy(lp).cuda()
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
