@@ -71,6 +71,15 @@ def _L():
         lib.orc_paged_decode.argtypes = [i32, i32, i32, i32, i32, P, P, P, i64, i32, i32, P, P, i32, P,
                                          i32, P, dbl, i32, P, P]
         lib.orc_lse_merge.argtypes = [i32, i32, i32, i32, P, P, P, P]
+        lib.orc_e2m1_sat_rne_n.argtypes = [P, P, i64]
+        lib.orc_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.orc_e2m1_to_f64.restype = dbl
+        lib.orc_nvfp4_block.argtypes = [P, ctypes.c_float, P, P]
+        lib.orc_rope_kv_write_nvfp4.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, i64, P, P, P, P, i64,
+                                                i32, i32, P, P, i32, P]
+        lib.orc_rope_kv_write_nvfp4.restype = i64
+        lib.orc_paged_decode_nvfp4.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, i64, i32, P, P, i32, P,
+                                               i32, P, dbl, i32, P, P]
         _lib = lib
     return _lib
 
@@ -217,4 +226,66 @@ def lse_merge(out_partial, lse_partial):
 
 
 def empty_cache(shape, cache_dtype: str) -> np.ndarray:
-    return np.zeros(shape, np.uint8 if cache_dtype == "fp8" else np.uint16)
+    return np.zeros(shape, np.uint8 if cache_dtype in ("fp8", "nvfp4") else np.uint16)
+
+
+# ---- NVFP4 (E2M1 values + an E4M3 scale per 16 elements) --------------------
+def e2m1_sat_rne(x) -> np.ndarray:
+    """float32 -> 4-bit E2M1 codes (uint8, 0..15), saturating to +-6, ties to even."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _L().orc_e2m1_sat_rne_n(_p(x), _p(out), x.size)
+    return out
+
+
+def e2m1_table() -> np.ndarray:
+    """float64 value of each of the 16 E2M1 codes."""
+    f = _L().orc_e2m1_to_f64
+    return np.array([f(c) for c in range(16)], np.float64)
+
+
+def nvfp4_block(y, g: float):
+    """One block of 16 float32 values -> (8 packed bytes, scale byte)."""
+    y = _c(y, np.float32)
+    assert y.size == 16
+    packed = np.empty(8, np.uint8)
+    sb = np.empty(1, np.uint8)
+    _L().orc_nvfp4_block(_p(y), float(g), _p(packed), _p(sb))
+    return packed, int(sb[0])
+
+
+def rope_kv_write_nvfp4(q, k, v, positions, cos_sin, k_cache, v_cache, k_block_scale, v_block_scale,
+                        slot_mapping, layout: str, style: str, k_scale, v_scale, page_size: int = 16) -> int:
+    """In place on numpy arrays: value caches uint8 [.., D/2] (packed E2M1
+    pairs), scale caches uint8 [.., D/16] (E4M3), both in the given layout."""
+    k = _c(k, np.uint16); v = _c(v, np.uint16)
+    T, Hkv, D = k.shape
+    Hq = 0 if q is None else q.shape[1]
+    for a in (k_cache, v_cache, k_block_scale, v_block_scale):
+        assert a.dtype == np.uint8 and a.flags.c_contiguous
+    pos = _c(positions, np.int32); slot = _c(slot_mapping, np.int32)
+    cs = _c(cos_sin, np.float32)
+    ks = _c(k_scale, np.float32); vs = _c(v_scale, np.float32)
+    return int(_L().orc_rope_kv_write_nvfp4(T, Hq, Hkv, D, page_size, _p(q), _p(k), _p(v), _p(pos), _p(cs),
+                                            cs.shape[0], _p(k_cache), _p(v_cache), _p(k_block_scale),
+                                            _p(v_block_scale), k_cache.shape[0], LAYOUT[layout],
+                                            int(style == "interleaved"), _p(ks), _p(vs), ks.size, _p(slot)))
+
+
+def paged_decode_nvfp4(q, k_cache, v_cache, k_block_scale, v_block_scale, block_tables, seq_lens,
+                       softmax_scale: float, num_splits: int, layout: str, k_scale, v_scale):
+    """As paged_decode, for NVFP4 caches (value caches [.., D/2] bytes)."""
+    q = _c(q, np.uint16)
+    B, Hq, D = q.shape
+    if layout == "HND":
+        num_pages, Hkv, P, _ = k_cache.shape
+    else:
+        num_pages, P, Hkv, _ = k_cache.shape
+    ks = _c(k_scale, np.float32); vs = _c(v_scale, np.float32)
+    bt = _c(block_tables, np.int32); sl = _c(seq_lens, np.int32)
+    o = np.empty((B, num_splits, Hq, D), np.float64)
+    l = np.empty((B, num_splits, Hq), np.float64)
+    _L().orc_paged_decode_nvfp4(B, Hq, Hkv, D, P, _p(q), _p(k_cache), _p(v_cache), _p(k_block_scale),
+                                _p(v_block_scale), num_pages, LAYOUT[layout], _p(ks), _p(vs), ks.size, _p(bt),
+                                bt.shape[1], _p(sl), float(softmax_scale), num_splits, _p(o), _p(l))
+    return o, l

@@ -121,6 +121,73 @@ void orc_e4m3_sat_rne_n(const float* x, uint8_t* out, int64_t n) {
 }
 
 /* ---------------------------------------------------------------------- */
+/* E2M1 ("e2m1fn", the 4-bit element of NVFP4 and MXFP4): 1 sign bit, 2     */
+/* exponent bits (bias 1), 1 mantissa bit; no infinities or NaN. Exponent   */
+/* field 0 is the subnormal m * 0.5. Magnitudes of codes 0..7:              */
+/* 0, 0.5, 1, 1.5, 2, 3, 4, 6. (mainarch, decode-attention section: FP4 is   */
+/* E2M1 with block scales.)                                                 */
+/* ---------------------------------------------------------------------- */
+double orc_e2m1_to_f64(uint8_t code) {
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Saturating round-to-nearest-even: magnitudes >= 6 give 6; below, the
+ * nearer of the two neighbouring codes, ties to the even code; the sign bit
+ * is kept (tiny negatives give 0x8). NaN is not an input of this path. */
+uint8_t orc_e2m1_sat_rne(float x) {
+    double dx = (double)x;
+    uint8_t sign = (f32_bits(x) >> 31) ? 0x8 : 0x0;
+    double ax = fabs(dx);
+    if (ax >= 6.0) return (uint8_t)(sign | 7);
+    int c = 0;
+    while (c < 7 && orc_e2m1_to_f64((uint8_t)(c + 1)) <= ax) ++c;
+    if (orc_e2m1_to_f64((uint8_t)c) != ax) {
+        double dlo = ax - orc_e2m1_to_f64((uint8_t)c), dhi = orc_e2m1_to_f64((uint8_t)(c + 1)) - ax;
+        if (dhi < dlo || (dhi == dlo && (c & 1))) c = c + 1;
+    }
+    return (uint8_t)(sign | c);
+}
+
+void orc_e2m1_sat_rne_n(const float* x, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_sat_rne(x[i]);
+}
+
+/*
+ * NVFP4 block of 16 values y (float32) under the static scale g:
+ *   s = E4M3(f32(amax / f32(6 g)))        (saturating RNE, positive)
+ *   nibble_i = E2M1(f32(y_i / f32(g * s)))  (0 for every value when s = 0)
+ * packed[i] holds value 2i in its low nibble and value 2i+1 in its high
+ * nibble. Dequantisation: y_i ~ g * s * E2M1(nibble_i). (The 16-element
+ * block with an E4M3 scale is Blackwell's NVFP4 form of mainarch's "E2M1
+ * KV with block scales"; the scale choice maps the block's largest
+ * magnitude to E2M1's largest value, 6.)
+ */
+void orc_nvfp4_block(const float* y, float g, uint8_t* packed, uint8_t* scale_byte) {
+    double amax = 0.0;
+    for (int i = 0; i < 16; ++i) {
+        double a = fabs((double)y[i]);
+        if (a > amax) amax = a;
+    }
+    float six_g = orc_f32(6.0 * (double)g);
+    uint8_t sb = orc_e4m3_sat_rne(orc_f32(amax / (double)six_g));
+    double s = orc_e4m3_to_f64(sb);
+    *scale_byte = sb;
+    float denom = orc_f32((double)g * s);
+    for (int i = 0; i < 8; ++i) {
+        uint8_t lo = 0, hi = 0;
+        if (s != 0.0) {
+            lo = orc_e2m1_sat_rne(orc_f32((double)y[2 * i] / (double)denom));
+            hi = orc_e2m1_sat_rne(orc_f32((double)y[2 * i + 1] / (double)denom));
+        }
+        packed[i] = (uint8_t)(lo | (hi << 4));
+    }
+}
+
+/* ---------------------------------------------------------------------- */
 /* RoPE                                                                    */
 /* Pairs: NeoX rotates (i, i + D/2); interleaved rotates (2i, 2i+1); both   */
 /* use frequency index i in [0, D/2). With (c, s) the cos and sin of the    */
@@ -227,12 +294,83 @@ int64_t orc_rope_kv_write(int64_t T, int Hq, int Hkv, int D, int page_size,
     return bad;
 }
 
+/*
+ * NVFP4 cache write: as orc_rope_kv_write, but each (token, kv head) row of
+ * rotated k / plain v is quantised in blocks of 16 (orc_nvfp4_block) with
+ * the static scale of its head. Value caches hold packed E2M1 pairs,
+ * NHD [pages, P, Hkv, D/2] or HND [pages, Hkv, P, D/2]; scale caches hold
+ * one E4M3 byte per block, [pages, P, Hkv, D/16] or [pages, Hkv, P, D/16].
+ */
+int64_t orc_rope_kv_write_nvfp4(int64_t T, int Hq, int Hkv, int D, int page_size,
+                                uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                                uint8_t* k_cache, uint8_t* v_cache, uint8_t* k_block_scale,
+                                uint8_t* v_block_scale, int64_t num_pages, int layout, int interleaved,
+                                const float* k_scale, const float* v_scale, int n_scale,
+                                const int32_t* slot_mapping) {
+    int64_t bad = 0;
+    float* y = (float*)malloc(sizeof(float) * (size_t)D);
+    int64_t num_slots = num_pages * page_size;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        int64_t pos = positions[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots || pos < 0 || pos >= max_pos) { ++bad; continue; }
+        const float* cs = cos_sin + pos * D;
+        int64_t page = slot / page_size;
+        int off = (int)(slot % page_size);
+        if (q) {
+            for (int h = 0; h < Hq; ++h) {
+                uint16_t* row = q + (t * Hq + h) * D;
+                orc_rope_row_f32(row, cs, y, D, interleaved);
+                for (int d = 0; d < D; ++d) row[d] = orc_bf16_rne(y[d]);
+            }
+        }
+        for (int h = 0; h < Hkv; ++h) {
+            for (int which = 0; which < 2; ++which) {
+                const uint16_t* src = (which == 0 ? k : v) + (t * Hkv + h) * D;
+                float g = scale_of(which == 0 ? k_scale : v_scale, n_scale, h);
+                if (which == 0) orc_rope_row_f32(src, cs, y, D, interleaved);
+                else for (int d = 0; d < D; ++d) y[d] = (float)orc_bf16_to_f64(src[d]);
+                uint8_t* vals = which == 0 ? k_cache : v_cache;
+                uint8_t* scales = which == 0 ? k_block_scale : v_block_scale;
+                for (int blk = 0; blk < D / 16; ++blk) {
+                    uint8_t packed[8], sb;
+                    orc_nvfp4_block(y + 16 * blk, g, packed, &sb);
+                    int64_t vrow = cache_index(layout, page, off, h, 0, Hkv, page_size, D / 2);
+                    for (int i = 0; i < 8; ++i) vals[vrow + 8 * blk + i] = packed[i];
+                    scales[cache_index(layout, page, off, h, blk, Hkv, page_size, D / 16)] = sb;
+                }
+            }
+        }
+    }
+    free(y);
+    return bad;
+}
+
 /* ---------------------------------------------------------------------- */
 /* Decode attention                                                        */
 /* ---------------------------------------------------------------------- */
-static double load_elem(const void* cache, int64_t idx, int fp8) {
-    if (fp8) return orc_e4m3_to_f64(((const uint8_t*)cache)[idx]);
-    return orc_bf16_to_f64(((const uint16_t*)cache)[idx]);
+/* A cache as the decode reads it: bf16 bits (fmt 0), E4M3 bytes (fmt 1) or
+ * NVFP4 packed E2M1 pairs with one E4M3 scale byte per 16 elements (fmt 2). */
+typedef struct {
+    const void* data;
+    const uint8_t* block_scale;
+    int fmt;
+} cache_view;
+
+static double cache_value(const cache_view* c, int layout, int64_t page, int off, int h, int d, int Hkv, int P,
+                          int D) {
+    if (c->fmt == 2) {
+        int64_t e = cache_index(layout, page, off, h, d, Hkv, P, D);
+        uint8_t byte = ((const uint8_t*)c->data)[e / 2];
+        uint8_t nib = (e & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+        uint8_t sb = c->block_scale[cache_index(layout, page, off, h, d / 16, Hkv, P, D / 16)];
+        return orc_e2m1_to_f64(nib) * orc_e4m3_to_f64(sb);
+    }
+    int64_t idx = cache_index(layout, page, off, h, d, Hkv, P, D);
+    if (c->fmt == 1) return orc_e4m3_to_f64(((const uint8_t*)c->data)[idx]);
+    return orc_bf16_to_f64(((const uint16_t*)c->data)[idx]);
 }
 
 /*
@@ -247,12 +385,12 @@ static double load_elem(const void* cache, int64_t idx, int fp8) {
  * v likewise with v_scale. Pages whose block-table entry is outside
  * [0, num_pages) are left out of the sum.
  */
-void orc_decode_head(int b, int h, int Hq, int Hkv, int D, int page_size,
-                     const uint16_t* q_row, const void* k_cache, const void* v_cache,
-                     int64_t num_pages, int layout, int fp8, const float* k_scale,
-                     const float* v_scale, int n_scale, const int32_t* block_tables,
-                     int max_pages, const int32_t* seq_lens, double softmax_scale,
-                     int num_splits, double* out_partial, double* lse_partial) {
+static void decode_head_impl(int b, int h, int Hq, int Hkv, int D, int page_size, const uint16_t* q_row,
+                             const cache_view* kc, const cache_view* vc, int64_t num_pages, int layout,
+                             const float* k_scale, const float* v_scale, int n_scale,
+                             const int32_t* block_tables, int max_pages, const int32_t* seq_lens,
+                             double softmax_scale, int num_splits, double* out_partial, double* lse_partial) {
+    int fp8 = kc->fmt != 0;  /* the static per-tensor / per-head scales apply */
     int G = Hq / Hkv;
     int kvh = h / G;
     int64_t L = seq_lens[b];
@@ -282,7 +420,7 @@ void orc_decode_head(int b, int h, int Hq, int Hkv, int D, int page_size,
                 if (t >= L) break;
                 double dot = 0.0;
                 for (int d = 0; d < D; ++d)
-                    dot += qd[d] * (load_elem(k_cache, cache_index(layout, page, off, kvh, d, Hkv, page_size, D), fp8) * ks);
+                    dot += qd[d] * (cache_value(kc, layout, page, off, kvh, d, Hkv, page_size, D) * ks);
                 sc[n] = softmax_scale * dot;
                 where[n] = page * page_size + off;
                 ++n;
@@ -299,13 +437,60 @@ void orc_decode_head(int b, int h, int Hq, int Hkv, int D, int page_size,
             int64_t page = where[i] / page_size;
             int off = (int)(where[i] % page_size);
             for (int d = 0; d < D; ++d)
-                o[d] += p * (load_elem(v_cache, cache_index(layout, page, off, kvh, d, Hkv, page_size, D), fp8) * vs);
+                o[d] += p * (cache_value(vc, layout, page, off, kvh, d, Hkv, page_size, D) * vs);
         }
         lse_partial[s] = m + log(l);
     }
     free(where);
     free(sc);
     free(qd);
+}
+
+void orc_decode_head(int b, int h, int Hq, int Hkv, int D, int page_size,
+                     const uint16_t* q_row, const void* k_cache, const void* v_cache,
+                     int64_t num_pages, int layout, int fp8, const float* k_scale,
+                     const float* v_scale, int n_scale, const int32_t* block_tables,
+                     int max_pages, const int32_t* seq_lens, double softmax_scale,
+                     int num_splits, double* out_partial, double* lse_partial) {
+    cache_view kc = {k_cache, NULL, fp8 ? 1 : 0}, vc = {v_cache, NULL, fp8 ? 1 : 0};
+    decode_head_impl(b, h, Hq, Hkv, D, page_size, q_row, &kc, &vc, num_pages, layout, k_scale, v_scale, n_scale,
+                     block_tables, max_pages, seq_lens, softmax_scale, num_splits, out_partial, lse_partial);
+}
+
+/* NVFP4 caches: value k = g_k * s_block * E2M1 (and likewise v). */
+void orc_decode_head_nvfp4(int b, int h, int Hq, int Hkv, int D, int page_size,
+                           const uint16_t* q_row, const uint8_t* k_cache, const uint8_t* v_cache,
+                           const uint8_t* k_block_scale, const uint8_t* v_block_scale, int64_t num_pages,
+                           int layout, const float* k_scale, const float* v_scale, int n_scale,
+                           const int32_t* block_tables, int max_pages, const int32_t* seq_lens,
+                           double softmax_scale, int num_splits, double* out_partial, double* lse_partial) {
+    cache_view kc = {k_cache, k_block_scale, 2}, vc = {v_cache, v_block_scale, 2};
+    decode_head_impl(b, h, Hq, Hkv, D, page_size, q_row, &kc, &vc, num_pages, layout, k_scale, v_scale, n_scale,
+                     block_tables, max_pages, seq_lens, softmax_scale, num_splits, out_partial, lse_partial);
+}
+
+void orc_paged_decode_nvfp4(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
+                            const uint8_t* k_cache, const uint8_t* v_cache, const uint8_t* k_block_scale,
+                            const uint8_t* v_block_scale, int64_t num_pages, int layout, const float* k_scale,
+                            const float* v_scale, int n_scale, const int32_t* block_tables, int max_pages,
+                            const int32_t* seq_lens, double softmax_scale, int num_splits,
+                            double* out_partial, double* lse_partial) {
+    double* o = (double*)malloc(sizeof(double) * (size_t)num_splits * D);
+    double* l = (double*)malloc(sizeof(double) * (size_t)num_splits);
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < Hq; ++h) {
+            orc_decode_head_nvfp4(b, h, Hq, Hkv, D, page_size, q + ((int64_t)b * Hq + h) * D, k_cache, v_cache,
+                                  k_block_scale, v_block_scale, num_pages, layout, k_scale, v_scale, n_scale,
+                                  block_tables, max_pages, seq_lens, softmax_scale, num_splits, o, l);
+            for (int s = 0; s < num_splits; ++s) {
+                int64_t r = ((int64_t)b * num_splits + s) * Hq + h;
+                lse_partial[r] = l[s];
+                for (int d = 0; d < D; ++d) out_partial[r * D + d] = o[(int64_t)s * D + d];
+            }
+        }
+    }
+    free(l);
+    free(o);
 }
 
 void orc_paged_decode(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,

@@ -40,7 +40,13 @@ uint8_t  orc_e4m3_sat_rne(float x);
 double   orc_e4m3_to_f64(uint8_t b);
 float    orc_f32(double x);
 
+/* E2M1 (4-bit, e2m1fn) codes and the NVFP4 block quantiser. */
+uint8_t  orc_e2m1_sat_rne(float x);
+double   orc_e2m1_to_f64(uint8_t code);
+void     orc_nvfp4_block(const float* y, float g, uint8_t* packed, uint8_t* scale_byte);
+
 /* Vector forms of the encoders, for exhaustive tests. */
+void orc_e2m1_sat_rne_n(const float* x, uint8_t* out, int64_t n);
 void orc_bf16_rne_n(const float* x, uint16_t* out, int64_t n);
 void orc_e4m3_sat_rne_n(const float* x, uint8_t* out, int64_t n);
 
@@ -87,6 +93,28 @@ void orc_paged_decode(int B, int Hq, int Hkv, int D, int page_size, const uint16
                       const int32_t* block_tables, int max_pages, const int32_t* seq_lens,
                       double softmax_scale, int num_splits, double* out_partial,
                       double* lse_partial);
+
+/* NVFP4 caches (packed E2M1 values + one E4M3 scale byte per 16 elements,
+ * static scales g per tensor or per head); see oracle.c. */
+int64_t orc_rope_kv_write_nvfp4(int64_t T, int Hq, int Hkv, int D, int page_size,
+                                uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                                uint8_t* k_cache, uint8_t* v_cache, uint8_t* k_block_scale,
+                                uint8_t* v_block_scale, int64_t num_pages, int layout, int interleaved,
+                                const float* k_scale, const float* v_scale, int n_scale,
+                                const int32_t* slot_mapping);
+void orc_decode_head_nvfp4(int b, int h, int Hq, int Hkv, int D, int page_size,
+                           const uint16_t* q_row, const uint8_t* k_cache, const uint8_t* v_cache,
+                           const uint8_t* k_block_scale, const uint8_t* v_block_scale, int64_t num_pages,
+                           int layout, const float* k_scale, const float* v_scale, int n_scale,
+                           const int32_t* block_tables, int max_pages, const int32_t* seq_lens,
+                           double softmax_scale, int num_splits, double* out_partial, double* lse_partial);
+void orc_paged_decode_nvfp4(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
+                            const uint8_t* k_cache, const uint8_t* v_cache, const uint8_t* k_block_scale,
+                            const uint8_t* v_block_scale, int64_t num_pages, int layout, const float* k_scale,
+                            const float* v_scale, int n_scale, const int32_t* block_tables, int max_pages,
+                            const int32_t* seq_lens, double softmax_scale, int num_splits,
+                            double* out_partial, double* lse_partial);
 
 /* Merge: out_partial [B,S,Hq,D], lse_partial [B,S,Hq] -> out [B,Hq,D],
  * lse [B,Hq]. */

@@ -141,6 +141,7 @@ def cos_sin_table(max_pos: int, head_dim: int, base: float) -> np.ndarray:
 LAYOUTS = ("NHD", "HND")
 STYLES = ("neox", "interleaved")
 CACHE_DTYPES = ("bf16", "fp8")
+ALL_CACHE_DTYPES = ("bf16", "fp8", "nvfp4")
 
 
 @dataclasses.dataclass
@@ -186,18 +187,30 @@ class Workload:
         return int(self.seq_lens.max()) if self.B else 1
 
     @property
-    def elem_bytes(self) -> int:
-        return 1 if self.cache_dtype == "fp8" else 2
+    def elem_bytes(self) -> float:
+        """Bytes per cached value (NVFP4: half a byte, plus one scale byte
+        per 16 values, counted by scale_shape)."""
+        return {"fp8": 1, "nvfp4": 0.5}.get(self.cache_dtype, 2)
 
     @property
     def pages_per_seq(self) -> np.ndarray:
         return (self.seq_lens.astype(np.int64) + self.page_size - 1) // self.page_size
 
     def cache_shape(self) -> tuple:
+        """Shape of the value cache in storage units (bf16 / E4M3 values, or
+        bytes of packed E2M1 pairs for NVFP4)."""
+        P = self.page_size
+        last = self.D // 2 if self.cache_dtype == "nvfp4" else self.D
+        if self.layout == "HND":
+            return (self.num_pages, self.Hkv, P, last)
+        return (self.num_pages, P, self.Hkv, last)
+
+    def scale_shape(self) -> tuple:
+        """NVFP4 block-scale cache: one E4M3 byte per 16 values."""
         P = self.page_size
         if self.layout == "HND":
-            return (self.num_pages, self.Hkv, P, self.D)
-        return (self.num_pages, P, self.Hkv, self.D)
+            return (self.num_pages, self.Hkv, P, self.D // 16)
+        return (self.num_pages, P, self.Hkv, self.D // 16)
 
     def cos_sin(self) -> np.ndarray:
         return cos_sin_table(max(self.max_pos, 1), self.D, self.rope_base)
@@ -295,7 +308,7 @@ def _uniform_int(seed: int, name: str, n: int, lo: int, hi: int) -> np.ndarray:
 
 
 def make_workload(name: str, seed: Optional[int] = None) -> Workload:
-    """The five decode workloads:
+    """The decode workloads:
 
     tiny        B2, L {37,100}, 4/2 heads, D64, HND, NeoX base 1e4, 16 pages
     qwen        B32, L ~ U[512,4096], 12/2, D128, HND, K x0.5, 12000-page pool
@@ -304,11 +317,14 @@ def make_workload(name: str, seed: Optional[int] = None) -> Workload:
                 32/8, D128, NHD, interleaved base 5e5, 1% K rows x8
     fp8         B64, L ~ U[2048,16384], 12/2, D128, HND, E4M3 cache,
                 per-head K/V scales ~ U[0.01, 0.1]
+    fp4         the fp8 workload's shapes with an NVFP4 cache: packed E2M1
+                values, an E4M3 scale per 16 values, static per-head scales
+                ~ U[0.5, 1.5]
     million     B1, L = 2^20, 8/1 (GQA 8), D128, HND, NeoX base 1e6,
                 a 65536-page shuffled pool (the 1M-token regime of the
                 mainarch decode-attention tables)
     """
-    idx = {"tiny": 0, "qwen": 1, "longctx": 2, "ragged": 3, "fp8": 4, "million": 5}[name]
+    idx = {"tiny": 0, "qwen": 1, "longctx": 2, "ragged": 3, "fp8": 4, "million": 5, "fp4": 6}[name]
     seed = 1000 + idx if seed is None else seed
     if name == "tiny":
         L = np.array([37, 100], np.int32)
@@ -329,6 +345,13 @@ def make_workload(name: str, seed: Optional[int] = None) -> Workload:
         pool = int(((L.astype(np.int64) + 15) // 16).sum())
         return Workload(name, seed, 256, 32, 8, 128, "NHD", "interleaved", "bf16", 5e5, L, pool,
                         _pool_tables(seed, L, pool), None, None, outlier_p=0.01)
+    if name == "fp4":
+        L = _uniform_int(seed, "lens", 64, 2048, 16384)
+        pool = int(((L.astype(np.int64) + 15) // 16).sum())
+        ks = (0.5 + uniform(stream_key(seed, "kscale"), 2)).astype(np.float32)
+        vs = (0.5 + uniform(stream_key(seed, "vscale"), 2)).astype(np.float32)
+        return Workload(name, seed, 64, 12, 2, 128, "HND", "neox", "nvfp4", 1e6, L, pool,
+                        _pool_tables(seed, L, pool), ks, vs)
     if name == "million":
         L = np.full(1, 1 << 20, np.int32)
         return Workload(name, seed, 1, 8, 1, 128, "HND", "neox", "bf16", 1e6, L, 1 << 16,
@@ -342,7 +365,7 @@ def make_workload(name: str, seed: Optional[int] = None) -> Workload:
                     _pool_tables(seed, L, pool), ks, vs)
 
 
-WORKLOADS = ("tiny", "qwen", "longctx", "ragged", "fp8", "million")
+WORKLOADS = ("tiny", "qwen", "longctx", "ragged", "fp8", "million", "fp4")
 
 
 def custom_workload(name: str, seed: int, seq_lens, Hq: int, Hkv: int, D: int, layout: str = "HND",
@@ -362,5 +385,9 @@ def custom_workload(name: str, seed: int, seq_lens, Hq: int, Hkv: int, D: int, l
         n = Hkv if per_head_scale else 1
         ks = (0.01 + 0.09 * uniform(stream_key(seed, "kscale"), n)).astype(np.float32)
         vs = (0.01 + 0.09 * uniform(stream_key(seed, "vscale"), n)).astype(np.float32)
+    elif cache_dtype == "nvfp4":
+        n = Hkv if per_head_scale else 1
+        ks = (0.5 + uniform(stream_key(seed, "kscale"), n)).astype(np.float32)
+        vs = (0.5 + uniform(stream_key(seed, "vscale"), n)).astype(np.float32)
     return Workload(name, seed, len(L), Hq, Hkv, D, layout, style, cache_dtype, rope_base, L, pool, bt,
                     ks, vs, k_mult=k_mult, outlier_p=outlier_p)

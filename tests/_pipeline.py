@@ -28,9 +28,22 @@ def oracle_step(w: synth.Workload, seqs=None, num_splits: int = 1):
         bt[i, :c] = np.arange(base, base + c, dtype=np.int32)
         base += c
     pool = max(base, 1)
-    shape = (pool, w.Hkv, P, w.D) if w.layout == "HND" else (pool, P, w.Hkv, w.D)
+    nv = w.cache_dtype == "nvfp4"
+    last = w.D // 2 if nv else w.D
+    shape = (pool, w.Hkv, P, last) if w.layout == "HND" else (pool, P, w.Hkv, last)
     kc = oracle.empty_cache(shape, w.cache_dtype)
     vc = np.zeros_like(kc)
+    if nv:
+        sshape = shape[:3] + (w.D // 16,)
+        ksc = np.zeros(sshape, np.uint8)
+        vsc = np.zeros(sshape, np.uint8)
+
+    def write(q, k, v, pos, slots):
+        if nv:
+            oracle.rope_kv_write_nvfp4(q, k, v, pos, cs, kc, vc, ksc, vsc, slots, w.layout, w.style,
+                                       w.k_scale, w.v_scale)
+        else:
+            oracle.rope_kv_write(q, k, v, pos, cs, kc, vc, slots, w.layout, w.style, w.k_scale, w.v_scale)
     cs = w.cos_sin()
     q_rot = np.zeros((n, w.Hq, w.D), np.uint16)
     sl = np.array([int(w.seq_lens[b]) for b in seqs], np.int32)
@@ -45,18 +58,23 @@ def oracle_step(w: synth.Workload, seqs=None, num_splits: int = 1):
         slots = (bt[i, pos // P].astype(np.int64) * P + pos % P).astype(np.int32)
         # context tokens (no q) ...
         if L > 1:
-            oracle.rope_kv_write(None, k[:L - 1], v[:L - 1], pos[:L - 1], cs, kc, vc, slots[:L - 1],
-                                 w.layout, w.style, w.k_scale, w.v_scale)
+            write(None, k[:L - 1], v[:L - 1], pos[:L - 1], slots[:L - 1])
         # ... then the new token with its q
         q = w.seq_q(b).reshape(1, w.Hq, w.D).copy()
-        oracle.rope_kv_write(q, k[L - 1:], v[L - 1:], pos[L - 1:], cs, kc, vc, slots[L - 1:],
-                             w.layout, w.style, w.k_scale, w.v_scale)
+        write(q, k[L - 1:], v[L - 1:], pos[L - 1:], slots[L - 1:])
         q_rot[i] = q[0]
-    op, lp = oracle.paged_decode(q_rot, kc, vc, bt, sl, w.softmax_scale, num_splits, w.layout,
-                                 w.k_scale, w.v_scale)
+    if nv:
+        op, lp = oracle.paged_decode_nvfp4(q_rot, kc, vc, ksc, vsc, bt, sl, w.softmax_scale, num_splits, w.layout,
+                                           w.k_scale, w.v_scale)
+    else:
+        op, lp = oracle.paged_decode(q_rot, kc, vc, bt, sl, w.softmax_scale, num_splits, w.layout,
+                                     w.k_scale, w.v_scale)
     out, lse = oracle.lse_merge(op, lp)
-    return dict(q_rot=q_rot, k_cache=kc, v_cache=vc, block_tables=bt, seq_lens=sl,
-                out_partial=op, lse_partial=lp, out=out, lse=lse)
+    r = dict(q_rot=q_rot, k_cache=kc, v_cache=vc, block_tables=bt, seq_lens=sl,
+             out_partial=op, lse_partial=lp, out=out, lse=lse)
+    if nv:
+        r.update(k_block_scale=ksc, v_block_scale=vsc)
+    return r
 
 
 def cache_values_f64(cache: np.ndarray, cache_dtype: str) -> np.ndarray:
@@ -68,3 +86,22 @@ def cache_values_f64(cache: np.ndarray, cache_dtype: str) -> np.ndarray:
     else:
         t = torch.from_numpy(cache.view(np.int16)).view(torch.bfloat16)
     return t.to(torch.float64).numpy()
+
+
+# The 16 E2M1 code values, written out from the OCP Microscaling Formats
+# definition of the FP4 (e2m1) element: codes 0-7 positive, 8-15 negative.
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+                        -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0], np.float64)
+
+
+def nvfp4_values_f64(cache: np.ndarray, block_scale: np.ndarray) -> np.ndarray:
+    """NVFP4 cache [.., D/2] packed bytes + [.., D/16] E4M3 scale bytes ->
+    float64 values [.., D] (without the static per-head scale), decoded with
+    the literal E2M1 table and torch's float8_e4m3fn view for the scales
+    (independent of the oracle's decoders)."""
+    import torch
+    lo = E2M1_VALUES[cache & 0xF]
+    hi = E2M1_VALUES[cache >> 4]
+    vals = np.stack([lo, hi], axis=-1).reshape(cache.shape[:-1] + (2 * cache.shape[-1],))
+    s = torch.from_numpy(np.ascontiguousarray(block_scale)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return vals * np.repeat(s, 16, axis=-1)
