@@ -63,6 +63,8 @@ WORKLOAD_TEXT = {
     "tiny": "tiny paged GQA decode: B2, seq_lens {37,100}, 4 q / 2 kv heads, D64, HND",
     "million": "1M-token decode: B1, seq_len 1048576, 8 q / 1 kv heads (GQA 8), D128, page 16, HND, bf16, "
                "65536-page shuffled pool",
+    "fp4": "NVFP4 paged cache decode (E2M1 values + E4M3 scale per 16 + per-head static scale ~U[0.5,1.5]): "
+           "B64, seq_lens ~U[2048,16384], 12 q / 2 kv heads, D128, HND",
 }
 
 
@@ -74,7 +76,7 @@ def parse_args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="qwen", choices=sorted(WORKLOAD_TEXT))
     p.add_argument("--splits", type=int, default=0, help="num_splits (0 = the library's heuristic)")
-    p.add_argument("--also", default="longctx,ragged,fp8,million",
+    p.add_argument("--also", default="longctx,ragged,fp8,million,fp4",
                    help="extra workloads whose decode roofline is reported under 'other_workloads' ('' = none)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -200,8 +202,9 @@ def ncu_traffic(workload: str):
 
 # ---- byte counts ---------------------------------------------------------------------
 def decode_alg_bytes(w) -> float:
-    """Q + K/V pages of every sequence + block-table entries read + bf16 out."""
-    e = w.elem_bytes
+    """Q + K/V pages of every sequence (values and any block scales) +
+    block-table entries read + bf16 out."""
+    e = w.cache_bytes_per_value
     q = w.B * w.Hq * w.D * 2
     kv = float(w.seq_lens.astype(np.int64).sum()) * w.Hkv * w.D * 2 * e
     bt = float(w.pages_per_seq.sum()) * 4
@@ -218,7 +221,7 @@ def write_alg_bytes(w, T: int, with_q: bool, table_rows=None) -> float:
     + one cos_sin row per token; with table_rows, the cos_sin rows are
     counted once per distinct position instead (rows shared by tokens at the
     same position are read from L2, not HBM)."""
-    e = w.elem_bytes
+    e = w.cache_bytes_per_value
     per = 2 * w.Hkv * w.D * 2 + 2 * w.Hkv * w.D * e + 8
     if with_q:
         per += 2 * w.Hq * w.D * 2
@@ -342,18 +345,16 @@ def measure_layered(dw, layers: int, reps: int, flush, peak: float) -> dict:
     back, each over its own cache (distinct memory, so nothing one layer
     reads is in L2 for the next), each launch free to start behind the
     previous one; L2 flushed before each group. Bytes / time of the group."""
-    from paged_kv_gqa_04_gb300 import _abi
     w = dw.w
-    caches = [(dw.k_cache, dw.v_cache)]
+    caches = [dw.caches()]
     for _ in range(layers - 1):
-        caches.append((dw.k_cache.clone(), dw.v_cache.clone()))
+        caches.append(tuple(c.clone() for c in dw.caches()))
     d = dw.decode_inputs
     outs = [(torch.empty_like(dw.out_partial), torch.empty_like(dw.lse_partial)) for _ in range(layers)]
 
     def group():
-        for (kc, vc), (op, lp) in zip(caches, outs):
-            _abi.paged_gqa_decode(d["q"], kc, vc, dw.block_tables, dw.seq_lens, w.softmax_scale, dw.num_splits,
-                                  op, lp, dw.k_scale, dw.v_scale, w.layout, dw.err)
+        for cs, (op, lp) in zip(caches, outs):
+            dw.decode_into(d["q"], cs, op, lp)
     stream = torch.cuda.current_stream()
     group()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
@@ -433,10 +434,17 @@ def oracle_step_timer(w, seqs, num_splits):
     def run() -> float:
         q = q0.copy()
         t0 = time.perf_counter()
-        oracle.rope_kv_write(q, k, v, pos, cs, st["k_cache"], st["v_cache"], slots, w.layout, w.style,
-                             w.k_scale, w.v_scale)
-        op, lp = oracle.paged_decode(q, st["k_cache"], st["v_cache"], bt, st["seq_lens"], w.softmax_scale,
-                                     num_splits, w.layout, w.k_scale, w.v_scale)
+        if w.cache_dtype == "nvfp4":
+            oracle.rope_kv_write_nvfp4(q, k, v, pos, cs, st["k_cache"], st["v_cache"], st["k_block_scale"],
+                                       st["v_block_scale"], slots, w.layout, w.style, w.k_scale, w.v_scale)
+            op, lp = oracle.paged_decode_nvfp4(q, st["k_cache"], st["v_cache"], st["k_block_scale"],
+                                               st["v_block_scale"], bt, st["seq_lens"], w.softmax_scale,
+                                               num_splits, w.layout, w.k_scale, w.v_scale)
+        else:
+            oracle.rope_kv_write(q, k, v, pos, cs, st["k_cache"], st["v_cache"], slots, w.layout, w.style,
+                                 w.k_scale, w.v_scale)
+            op, lp = oracle.paged_decode(q, st["k_cache"], st["v_cache"], bt, st["seq_lens"], w.softmax_scale,
+                                         num_splits, w.layout, w.k_scale, w.v_scale)
         oracle.lse_merge(op, lp)
         return time.perf_counter() - t0
     return run

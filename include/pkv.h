@@ -66,7 +66,9 @@ typedef enum {
 
 typedef enum { PKV_NHD = 0, PKV_HND = 1 } pkv_layout;
 typedef enum { PKV_ROPE_NEOX = 0, PKV_ROPE_INTERLEAVED = 1 } pkv_rope_style;
-typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1, PKV_F32 = 2, PKV_I32 = 3 } pkv_dtype;
+/* PKV_FP4_E2M1X2: one byte holding two E2M1 values, the even-indexed value
+ * in the low nibble (the value caches of the NVFP4 entry points). */
+typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1, PKV_F32 = 2, PKV_I32 = 3, PKV_FP4_E2M1X2 = 4 } pkv_dtype;
 
 /* Bits OR-ed into *err_flag by the kernels. */
 #define PKV_FLAG_SLOT_RANGE     0x01  /* slot_mapping entry >= num_pages * page_size        */
@@ -174,6 +176,75 @@ pkv_status pkv_paged_gqa_decode(const pkv_tensor* q, const pkv_tensor* k_cache, 
                                 int32_t* err_flag, pkv_stream_t stream);
 
 /*
+ * pkv_rope_kv_write_nvfp4 -- pkv_rope_kv_write into a 4-bit (NVFP4) cache.
+ * (mainarch, decode-attention section: 4-bit E2M1 KV with block scales,
+ *  dequantised in-kernel, with NVFP4 named as the open work. NVFP4 is the
+ *  form used here: E2M1 values, one E4M3 scale per 16 consecutive values of
+ *  a row, and a static float32 scale per tensor or per kv head.)
+ *
+ * RoPE and the rounding of every product and sum are those of
+ * pkv_rope_kv_write. Each (token, kv head) row y of rotated k, or of v, is
+ * then quantised block by block (16 values, blocks aligned to the row),
+ * with g the static scale of the head:
+ *   amax = max |y_i| over the block
+ *   s    = E4M3( f32(amax / f32(6 g)) )      saturating RNE, the block's
+ *                                            scale byte
+ *   e_i  = E2M1( f32(y_i / f32(g s)) )       saturating (to +-6) RNE, the
+ *                                            sign kept; every e_i = 0 when
+ *                                            s = 0
+ * where f32() is the correctly rounded float32 result. The stored value is
+ * y_i ~ g * s * e_i.
+ *
+ * k_cache,
+ * v_cache      NHD [num_pages, page_size, Hkv, D/2] or HND [num_pages, Hkv,
+ *              page_size, D/2], dtype PKV_FP4_E2M1X2 (values 2j and 2j+1 of
+ *              a row in byte j, low nibble first); innermost stride 1, other
+ *              strides multiples of 16 bytes, base 16-byte aligned.
+ * k_block_scale,
+ * v_block_scale  the same layout with D/16 in place of D/2, dtype
+ *              PKV_FP8_E4M3 (byte j = scale of values 16j..16j+15);
+ *              innermost stride 1.
+ * k_scale,
+ * v_scale      [1] or [Hkv] float32, positive, required.
+ * Every other argument, the supported sizes and the errors are those of
+ * pkv_rope_kv_write. The caches and scale caches must not alias one another
+ * or q, k, v.
+ */
+pkv_status pkv_rope_kv_write_nvfp4(const pkv_tensor* q, const pkv_tensor* k, const pkv_tensor* v,
+                                   const pkv_tensor* positions, const pkv_tensor* cos_sin,
+                                   const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                                   const pkv_tensor* k_block_scale, const pkv_tensor* v_block_scale,
+                                   const pkv_tensor* slot_mapping, const pkv_tensor* k_scale,
+                                   const pkv_tensor* v_scale, int32_t layout, int32_t rope_style,
+                                   int32_t* err_flag, pkv_stream_t stream);
+
+/*
+ * pkv_paged_gqa_decode_nvfp4 -- pkv_paged_gqa_decode over NVFP4 caches.
+ * (mainarch, decode-attention section: paged + GQA + FP4 KV in one kernel,
+ *  the block scales applied as the cache is read.)
+ *
+ * The same computation as pkv_paged_gqa_decode with cache values
+ *   K_t[d] = k_scale[kvh] * s_k(t, d/16) * e_k(t, d)
+ * (and likewise V), s the E4M3 block scale and e the E2M1 value.
+ *
+ * k_cache, v_cache, k_block_scale, v_block_scale  as for
+ *              pkv_rope_kv_write_nvfp4, HND layout only (NHD returns
+ *              PKV_ERR_UNSUPPORTED), page_size 16; the 16 x D/16 scale bytes
+ *              of one (page, kv head) must be contiguous (innermost two
+ *              strides 1 and D/16) and start on a 16-byte boundary (the
+ *              outer two strides multiples of 16 bytes, base 16-byte aligned).
+ * Every other argument, the supported sizes and the errors are those of
+ * pkv_paged_gqa_decode; the partials feed pkv_lse_merge unchanged.
+ */
+pkv_status pkv_paged_gqa_decode_nvfp4(const pkv_tensor* q, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                                      const pkv_tensor* k_block_scale, const pkv_tensor* v_block_scale,
+                                      const pkv_tensor* block_tables, const pkv_tensor* seq_lens,
+                                      float softmax_scale, int32_t num_splits, const pkv_tensor* out_partial,
+                                      const pkv_tensor* lse_partial, const pkv_tensor* k_scale,
+                                      const pkv_tensor* v_scale, int32_t layout, int32_t* err_flag,
+                                      pkv_stream_t stream);
+
+/*
  * pkv_lse_merge -- merge of the split partials.
  * (mainarch, decode-attention section: the combine of split-KV partials;
  *  Loom Kernels, "Attention" row: local split-K/LSE merge.)
@@ -199,8 +270,8 @@ pkv_status pkv_lse_merge(const pkv_tensor* out_partial, const pkv_tensor* lse_pa
  * "Local split-K paged decode".)
  *
  * B, Hkv: batch and kv heads; total_pages = sum over the batch of
- * ceil(seq_len/16); max_pages = the largest ceil(seq_len/16); cache_dtype a
- * pkv_dtype; sm_count the device's SM count. Models each split as one CTA
+ * ceil(seq_len/16); max_pages = the largest ceil(seq_len/16); cache_dtype the
+ * value cache's pkv_dtype (PKV_BF16, PKV_FP8_E4M3 or PKV_FP4_E2M1X2); sm_count the device's SM count. Models each split as one CTA
  * and returns the S in [1, 1024] with the lowest estimated time for
  * streaming the pages over the GPU's CTA slots plus the merge's extra
  * traffic and round trips.
@@ -279,7 +350,7 @@ const char* pkv_status_string(int32_t status);
 
 /* ABI version of this header (bumped on any signature change). */
 int32_t pkv_abi_version(void);
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

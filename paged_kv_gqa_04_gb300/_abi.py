@@ -34,10 +34,12 @@ _DTYPES = {
     torch.float32: 2,
     torch.int32: 3,
 }
+PKV_FP4_E2M1X2 = 4    # uint8 bytes of two E2M1 values (NVFP4 value caches)
+_CACHE_DTYPE = {"bf16": 0, "fp8": 1, "nvfp4": PKV_FP4_E2M1X2}
 
 EXPORTED = ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_choose_num_splits",
             "pkv_validate_indices", "pkv_status_string", "pkv_abi_version", "pkv_stream_read",
-            "pkv_validate_indices_static")
+            "pkv_validate_indices_static", "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4")
 
 
 class PkvTensor(ctypes.Structure):
@@ -67,6 +69,8 @@ def lib() -> ctypes.CDLL:
         i32 = ctypes.c_int32
         L.pkv_rope_kv_write.argtypes = [T, T, T, T, T, T, T, T, T, T, i32, i32, P, P]
         L.pkv_paged_gqa_decode.argtypes = [T, T, T, T, T, ctypes.c_float, i32, T, T, T, T, i32, P, P]
+        L.pkv_rope_kv_write_nvfp4.argtypes = [T, T, T, T, T, T, T, T, T, T, T, T, i32, i32, P, P]
+        L.pkv_paged_gqa_decode_nvfp4.argtypes = [T, T, T, T, T, T, T, ctypes.c_float, i32, T, T, T, T, i32, P, P]
         L.pkv_lse_merge.argtypes = [T, T, T, T, P]
         L.pkv_choose_num_splits.argtypes = [i32, i32, i32, i32, ctypes.c_int64, i32, i32, i32]
         L.pkv_validate_indices.argtypes = [T, T, T, ctypes.c_int64, T, P, P]
@@ -75,7 +79,8 @@ def lib() -> ctypes.CDLL:
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         for name in ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_validate_indices",
-                     "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read", "pkv_validate_indices_static"):
+                     "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read", "pkv_validate_indices_static",
+                     "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4"):
             getattr(L, name).restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -85,8 +90,9 @@ def status_string(status: int) -> str:
     return lib().pkv_status_string(int(status)).decode()
 
 
-def _desc(t: Optional[torch.Tensor]):
-    """Pointer to a descriptor of t (NULL for None)."""
+def _desc(t: Optional[torch.Tensor], dtype: Optional[int] = None):
+    """Pointer to a descriptor of t (NULL for None); `dtype` overrides the
+    pkv_dtype taken from t.dtype (uint8 NVFP4 value caches)."""
     if t is None:
         return None
     d = PkvTensor()
@@ -97,7 +103,7 @@ def _desc(t: Optional[torch.Tensor]):
     if t.numel() and not t.is_cuda:
         raise ValueError("the C ABI takes device tensors; copy host data to the GPU first")
     d.ptr = t.data_ptr() if t.numel() else None
-    d.dtype = _DTYPES[t.dtype]
+    d.dtype = _DTYPES[t.dtype] if dtype is None else dtype
     d.ndim = t.dim()
     for i, (n, s) in enumerate(zip(t.shape, t.stride())):
         d.shape[i] = n
@@ -141,6 +147,35 @@ def paged_gqa_decode(q, k_cache, v_cache, block_tables, seq_lens, softmax_scale:
         _ptr(err_flag), _stream(stream)))
 
 
+def _fp4(t):
+    if t is not None and t.dtype != torch.uint8:
+        raise TypeError("NVFP4 value caches are uint8 tensors of packed E2M1 pairs")
+    return _desc(t, PKV_FP4_E2M1X2)
+
+
+def rope_kv_write_nvfp4(q, k, v, positions, cos_sin, k_cache, v_cache, k_block_scale, v_block_scale,
+                        slot_mapping, k_scale, v_scale, layout: str = "HND", rope_style: str = "neox",
+                        err_flag=None, stream=None) -> None:
+    """pkv_rope_kv_write_nvfp4: as rope_kv_write into NVFP4 caches -- value
+    caches uint8 [.., D/2] (packed E2M1 pairs), block-scale caches uint8 or
+    float8_e4m3fn [.., D/16], static scales [1] or [Hkv] float32."""
+    _check("pkv_rope_kv_write_nvfp4", lib().pkv_rope_kv_write_nvfp4(
+        _desc(q), _desc(k), _desc(v), _desc(positions), _desc(cos_sin), _fp4(k_cache), _fp4(v_cache),
+        _desc(k_block_scale), _desc(v_block_scale), _desc(slot_mapping), _desc(k_scale), _desc(v_scale),
+        LAYOUTS[layout], STYLES[rope_style], _ptr(err_flag), _stream(stream)))
+
+
+def paged_gqa_decode_nvfp4(q, k_cache, v_cache, k_block_scale, v_block_scale, block_tables, seq_lens,
+                           softmax_scale: float, num_splits: int, out_partial, lse_partial, k_scale, v_scale,
+                           layout: str = "HND", err_flag=None, stream=None) -> None:
+    """pkv_paged_gqa_decode_nvfp4: paged GQA split-K decode over NVFP4
+    caches (HND) into out_partial [B,S,Hq,D] and lse_partial [B,S,Hq]."""
+    _check("pkv_paged_gqa_decode_nvfp4", lib().pkv_paged_gqa_decode_nvfp4(
+        _desc(q), _fp4(k_cache), _fp4(v_cache), _desc(k_block_scale), _desc(v_block_scale), _desc(block_tables),
+        _desc(seq_lens), float(softmax_scale), int(num_splits), _desc(out_partial), _desc(lse_partial),
+        _desc(k_scale), _desc(v_scale), LAYOUTS[layout], _ptr(err_flag), _stream(stream)))
+
+
 def lse_merge(out_partial, lse_partial, out, lse_out=None, stream=None) -> None:
     """LSE merge of the split partials into out [B,Hq,D] bf16 (pkv_lse_merge)."""
     _check("pkv_lse_merge", lib().pkv_lse_merge(_desc(out_partial), _desc(lse_partial), _desc(out),
@@ -151,7 +186,7 @@ def choose_num_splits(B: int, Hkv: int, Hq: int, D: int, total_pages: int, max_p
                       sm_count: int) -> int:
     """Split count from the library's heuristic (host only)."""
     return int(lib().pkv_choose_num_splits(B, Hkv, Hq, D, int(total_pages), max_pages,
-                                           1 if cache_dtype == "fp8" else 0, sm_count))
+                                           _CACHE_DTYPE[cache_dtype], sm_count))
 
 
 def validate_indices(block_tables, seq_lens, slot_mapping, num_pages: int, err_flag, slot_bitmap=None,

@@ -33,6 +33,16 @@
 // prmt, and Q and P are f16. Scales fold into the score scale (k_scale) and
 // the output (v_scale).
 //
+// NVFP4 caches (mainarch, decode-attention section: paged + GQA + 4-bit E2M1
+// KV with block scales in one kernel; NVFP4 form) use the FP8 path's
+// fragment mapping at half the bytes: a thread's 16-byte (K) or 8-byte (V)
+// share of a row is one or two whole 16-value blocks, so each f16x2 word
+// from cvt.rn.f16x2.e2m1x2 is multiplied (exactly) by its block's E4M3
+// scale, loaded with the page by a 16-byte-aligned bulk copy beside the
+// values. V pairs tokens by nibble: (a & 0x0F0F0F0F) | (b << 4 & 0xF0F0F0F0)
+// puts value d of tokens a and b in one byte. Rows past the sequence end get
+// a zero V scale (their nibbles are finite, so they contribute exactly 0).
+//
 // The tensor-core work is small (about 4*16*D flops per token and kv head
 // against 4*D bytes of bf16 K/V): the kernel is bound by HBM, and mma.sync
 // only keeps the ALU issue rate far from that bound. Scores and the softmax
@@ -63,14 +73,20 @@ constexpr int kWarps = PKV_DECODE_WARPS;
 constexpr int kRingBytes = PKV_DECODE_RING_BYTES;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-template <int D, bool FP8>
+template <int D, int KIND>
 struct Cfg {
-    static constexpr int E = FP8 ? 1 : 2;                  // cache element bytes
-    static constexpr int ROW = D * E;                      // bytes of one token row of one head
+    static constexpr bool F16 = KIND != kBf16;             // f16 mma operands (quantised caches)
+    static constexpr int ROW = KIND == kBf16 ? 2 * D : (KIND == kFp8 ? D : D / 2);  // bytes of one token row
+    static constexpr int E = KIND == kBf16 ? 2 : 1;        // bytes per tensor-map element
     static constexpr int BOXB = ROW >= 128 ? 128 : ROW;    // bytes per box row (swizzle span)
     static constexpr int NBOX = ROW / BOXB;                // boxes per page per tensor
     static constexpr int PAGE = kPageSize * ROW;           // bytes of one page of one head, K or V
-    static constexpr int SLOT = 2 * PAGE;                  // K + V
+    static constexpr int SROW = KIND == kFp4 ? D / 16 : 0; // block-scale bytes of one token row
+    static constexpr int SPAGE = kPageSize * SROW;
+    static constexpr int TX = 2 * PAGE + 2 * SPAGE;        // bytes landing per page
+    // K, V, then the K and V block scales; a slot keeps the swizzle span's
+    // alignment (8 rows of BOXB bytes)
+    static constexpr int SLOT = (TX + 8 * BOXB - 1) / (8 * BOXB) * (8 * BOXB);
     static constexpr int NSLOT = kRingBytes / SLOT < 2 ? 2 : (kRingBytes / SLOT > 8 ? 8 : kRingBytes / SLOT);
     static constexpr int RING = NSLOT * SLOT;              // per warp
     // Pages consumed per iteration. Two (one softmax update per 32 tokens)
@@ -80,33 +96,36 @@ struct Cfg {
     static constexpr int KS = D / 16;                      // k-steps of QK
     static constexpr int NT = D / 8;                       // n-tiles of PV
     static constexpr int SMEM = kWarps * RING + kWarps * NSLOT * 8 + 1024;  // + barriers + alignment
-    static_assert(BOXB == 128 || BOXB == 64, "swizzle span");
+    static_assert(BOXB == 128 || BOXB == 64 || BOXB == 32, "swizzle span");
     static_assert(RING >= (16 * (D + 8) + 32) * 4, "combine area must fit in a warp's ring");
 };
 
 // Byte offset of (row r, byte column col) in one page slice laid out by TMA
-// with a 128- or 64-byte swizzle (the 16-byte chunk index is XOR-ed with
-// address bits 7.. of the row start).
+// with a 128-, 64- or 32-byte swizzle (the 16-byte chunk index is XOR-ed
+// with address bits 7.. of the row start).
 template <int BOXB>
 __device__ __forceinline__ uint32_t swz(int r, int col) {
     if constexpr (BOXB == 128) {
         const int box = col >> 7;
         const int c = (col >> 4) & 7;
         return box * (kPageSize * 128) + r * 128 + ((c ^ (r & 7)) << 4) + (col & 15);
-    } else {
+    } else if constexpr (BOXB == 64) {
         const int c = (col >> 4) & 3;
         return r * 64 + ((c ^ ((r >> 1) & 3)) << 4) + (col & 15);
+    } else {
+        const int c = (col >> 4) & 1;
+        return r * 32 + ((c ^ ((r >> 2) & 1)) << 4) + (col & 15);
     }
 }
 
 __device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16_t>(w & 0xFFFFu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
 
-template <int D, bool FP8, bool TWO>
+template <int D, int KIND, bool TWO>
 __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         const DecodeArgs a, const int hnd) {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D, KIND>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t smem0 = smem_u32(smem);
@@ -182,7 +201,7 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     const uint64_t policy = l2_policy_evict_first();
     const int64_t num_pages = a.num_pages;
     float ks = 1.f, vs = 1.f;
-    if constexpr (FP8) {
+    if constexpr (KIND != kBf16) {
         ks = __ldg(a.k_scale + (a.n_scale == 1 ? 0 : kvh));
         vs = __ldg(a.v_scale + (a.n_scale == 1 ? 0 : kvh));
     }
@@ -204,7 +223,7 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
             mbar_arrive(bar);  // completes the phase with no bytes; the page is skipped
             return;
         }
-        mbar_arrive_expect_tx(bar, C::SLOT);
+        mbar_arrive_expect_tx(bar, C::TX);
         const uint32_t kdst = ring0 + slot * C::SLOT;
         const uint32_t vdst = kdst + C::PAGE;
         const int c1 = hnd ? 0 : kvh;
@@ -214,6 +233,11 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
             const int d0 = bx * (C::BOXB / C::E);
             tma_load_4d(kdst + bx * kPageSize * C::BOXB, &tmk, bar, d0, c1, c2, pid, policy);
             tma_load_4d(vdst + bx * kPageSize * C::BOXB, &tmv, bar, d0, c1, c2, pid, policy);
+        }
+        if constexpr (KIND == kFp4) {
+            bulk_load(kdst + 2 * C::PAGE, a.k_bs + pid * a.kbs_s0 + kvh * a.kbs_s1, C::SPAGE, bar, policy);
+            bulk_load(kdst + 2 * C::PAGE + C::SPAGE, a.v_bs + pid * a.vbs_s0 + kvh * a.vbs_s1, C::SPAGE, bar,
+                      policy);
         }
     };
 
@@ -235,7 +259,7 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
 #pragma unroll
         for (int j = 0; j < C::KS; ++j) {
             int dlo, dhi;
-            if constexpr (FP8) {
+            if constexpr (C::F16) {
                 dlo = (D / 4) * t + 4 * j;
                 dhi = dlo + 2;
             } else {
@@ -253,7 +277,7 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if constexpr (FP8)
+                if constexpr (C::F16)
                     qa[j][e] = pack_f16(bf16_lo(w[e]), bf16_hi(w[e]));
                 else
                     qa[j][e] = w[e];
@@ -274,7 +298,7 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     // S = Q K^T for the 16 tokens of the page at kb: sc[nt] holds tokens
     // 8nt + 2t, 8nt + 2t + 1 of rows g and g + 8.
     auto qk_page = [&](uint32_t kb, float (*sc)[4]) {
-        if constexpr (!FP8) {
+        if constexpr (KIND == kBf16) {
 #pragma unroll
             for (int jj = 0; jj < C::KS / 2; ++jj) {
 #pragma unroll
@@ -286,6 +310,40 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
                     mma16816<false>(sc[nt], qa[2 * jj][0], qa[2 * jj][1], qa[2 * jj][2], qa[2 * jj][3], b0, b1);
                     mma16816<false>(sc[nt], qa[2 * jj + 1][0], qa[2 * jj + 1][1], qa[2 * jj + 1][2],
                                     qa[2 * jj + 1][3], b2, b3);
+                }
+            }
+        } else if constexpr (KIND == kFp4) {
+            // thread t's share of row r: bytes [ (D/8)t, (D/8)(t+1) ), i.e.
+            // values [(D/4)t, (D/4)(t+1)) -- blocks 2t, 2t+1 (D = 128) or t
+            const uint32_t kbs = kb + 2 * C::PAGE;  // K block scales [16][D/16]
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int r = 8 * nt + g;
+                constexpr int NW = D / 32;          // words of E2M1 pairs per thread
+                uint32_t w[NW];
+                uint32_t sA, sB;                    // {s, s} of the first / second block
+                if constexpr (D == 128) {
+                    const uint4 x0 = lds128(kb + swz<C::BOXB>(r, 16 * t));
+                    w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
+                    const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint16_t>(lds16(kbs + r * C::SROW + 2 * t)));
+                    sA = prmt(s2, s2, 0x1010u);
+                    sB = prmt(s2, s2, 0x3232u);
+                } else {
+                    const uint2 x0 = lds64(kb + swz<C::BOXB>(r, 8 * t));
+                    w[0] = x0.x; w[1] = x0.y;
+                    const uint32_t s1 = lds8(kbs + r * C::SROW + t);
+                    sA = sB = e4m3x2_to_f16x2(static_cast<uint16_t>(s1 | (s1 << 8)));
+                }
+#pragma unroll
+                for (int wi = 0; wi < NW; ++wi) {
+                    uint32_t h[4];
+                    e2m1x8_to_f16x2(w[wi], h);
+                    const uint32_t sc2 = (D == 128 && wi >= 2) ? sB : sA;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) h[e] = hmul2(h[e], sc2);
+                    const int j = 2 * wi;
+                    mma16816<true>(sc[nt], qa[j][0], qa[j][1], qa[j][2], qa[j][3], h[0], h[1]);
+                    mma16816<true>(sc[nt], qa[j + 1][0], qa[j + 1][1], qa[j + 1][2], qa[j + 1][3], h[2], h[3]);
                 }
             }
         } else {
@@ -312,7 +370,7 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     // O += P V for the page at vb; tokens at or past `valid` contribute zero
     // (their V bytes may be anything, so they are zeroed, not only weighted 0).
     auto pv_page = [&](uint32_t vb, int valid, uint32_t pa0, uint32_t pa1, uint32_t pa2, uint32_t pa3) {
-        if constexpr (!FP8) {
+        if constexpr (KIND == kBf16) {
             uint32_t mk0 = 0xFFFFFFFFu, mk1 = 0xFFFFFFFFu;
             if (valid < kPageSize) {
                 mk0 = (2 * t < valid ? 0x0000FFFFu : 0u) | (2 * t + 1 < valid ? 0xFFFF0000u : 0u);
@@ -327,6 +385,48 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
                 ldsm_x4_t(vb + swz<C::BOXB>(r, col), b0, b1, b2, b3);
                 mma16816<false>(acc[2 * dp], pa0, pa1, pa2, pa3, b0 & mk0, b1 & mk1);
                 mma16816<false>(acc[2 * dp + 1], pa0, pa1, pa2, pa3, b2 & mk0, b3 & mk1);
+            }
+        } else if constexpr (KIND == kFp4) {
+            // thread g's share of each row: bytes [(D/16)g, (D/16)(g+1)), values
+            // d = (D/8)g + jn, jn < D/8 -- all in block g (D = 128) or g/2
+            constexpr int NWD = D / 64;  // words of E2M1 pairs per token row per thread
+            const uint32_t vbs = vb + C::PAGE + C::SPAGE;  // V block scales [16][D/16]
+            const int blk = D == 128 ? g : (g >> 1);
+            uint32_t va[4][NWD];
+            uint32_t sb4 = 0u;  // scale bytes of rows 2t, 2t+1, 2t+8, 2t+9
+            const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if constexpr (D == 128) {
+                    const uint2 xv = lds64(vb + swz<C::BOXB>(rows[q], 8 * g));
+                    va[q][0] = xv.x; va[q][1] = xv.y;
+                } else {
+                    va[q][0] = lds32(vb + swz<C::BOXB>(rows[q], 4 * g));
+                }
+                const uint32_t sbq = lds8(vbs + rows[q] * C::SROW + blk);
+                sb4 |= (rows[q] < valid ? sbq : 0u) << (8 * q);
+            }
+            const uint32_t s01 = e4m3x2_to_f16x2(lo16(sb4));  // {s(2t), s(2t+1)}
+            const uint32_t s89 = e4m3x2_to_f16x2(hi16(sb4));  // {s(2t+8), s(2t+9)}
+#pragma unroll
+            for (int wd = 0; wd < NWD; ++wd) {
+                // byte i of xe: value 2i of tokens 2t (low nibble) and 2t+1;
+                // xo: value 2i+1; ye / yo the same for tokens 2t+8, 2t+9
+                const uint32_t xe = (va[0][wd] & 0x0F0F0F0Fu) | ((va[1][wd] << 4) & 0xF0F0F0F0u);
+                const uint32_t xo = ((va[0][wd] >> 4) & 0x0F0F0F0Fu) | (va[1][wd] & 0xF0F0F0F0u);
+                const uint32_t ye = (va[2][wd] & 0x0F0F0F0Fu) | ((va[3][wd] << 4) & 0xF0F0F0F0u);
+                const uint32_t yo = ((va[2][wd] >> 4) & 0x0F0F0F0Fu) | (va[3][wd] & 0xF0F0F0F0u);
+                uint32_t he[4], ho[4], ge[4], go[4];
+                e2m1x8_to_f16x2(xe, he);
+                e2m1x8_to_f16x2(xo, ho);
+                e2m1x8_to_f16x2(ye, ge);
+                e2m1x8_to_f16x2(yo, go);
+#pragma unroll
+                for (int i2 = 0; i2 < 4; ++i2) {
+                    const int jn = 8 * wd + 2 * i2;
+                    mma16816<true>(acc[jn], pa0, pa1, pa2, pa3, hmul2(he[i2], s01), hmul2(ge[i2], s89));
+                    mma16816<true>(acc[jn + 1], pa0, pa1, pa2, pa3, hmul2(ho[i2], s01), hmul2(go[i2], s89));
+                }
             }
         } else {
             constexpr int NWD = D / 32;  // words of V bytes per token row per thread
@@ -468,7 +568,7 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
                 const float* p0r = pr[2 * j];
                 const float* p1r = pr[2 * j + 1];
                 uint32_t pa0, pa1 = 0u, pa2, pa3 = 0u;
-                if constexpr (FP8) {
+                if constexpr (C::F16) {
                     pa0 = pack_f16(p0r[0], p0r[1]);
                     pa2 = pack_f16(p1r[0], p1r[1]);
                     if constexpr (TWO) {
@@ -534,7 +634,7 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     }
 #pragma unroll
     for (int n = 0; n < C::NT; ++n) {
-        if constexpr (FP8) {
+        if constexpr (C::F16) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int d = (D / 8) * (2 * t + e) + n;
@@ -581,26 +681,36 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     }
 }
 
-template <int D, bool FP8, bool TWO>
+template <int D, int KIND, bool TWO>
 cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int hnd, cudaStream_t s) {
-    using C = Cfg<D, FP8>;
-    auto kern = paged_decode_kernel<D, FP8, TWO>;
+    using C = Cfg<D, KIND>;
+    auto kern = paged_decode_kernel<D, KIND, TWO>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid(a.num_splits, a.Hkv, a.B);
     return launch_dependent(kern, grid, dim3(kWarps * 32), C::SMEM, s, tk, tv, a, hnd);
 }
 
-template <int D, bool FP8>
+template <int D, int KIND>
 cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int hnd, cudaStream_t s) {
-    return a.G > 8 ? launch_t<D, FP8, true>(a, tk, tv, hnd, s) : launch_t<D, FP8, false>(a, tk, tv, hnd, s);
+    return a.G > 8 ? launch_t<D, KIND, true>(a, tk, tv, hnd, s) : launch_t<D, KIND, false>(a, tk, tv, hnd, s);
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int hnd, cudaStream_t s) {
+    switch (a.kind) {
+        case kBf16: return launch_g<D, kBf16>(a, tk, tv, hnd, s);
+        case kFp8: return launch_g<D, kFp8>(a, tk, tv, hnd, s);
+        case kFp4: return launch_g<D, kFp4>(a, tk, tv, hnd, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
-int decode_ctas_per_sm(int D, int fp8) {
+int decode_ctas_per_sm(int D, int kind) {
     (void)D;
-    (void)fp8;
+    (void)kind;
     return PKV_DECODE_MIN_CTAS;
 }
 
@@ -608,8 +718,8 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, cons
                                 cudaStream_t s) {
     if (a.B == 0) return cudaSuccess;
     const int hnd = a.layout == PKV_HND;
-    if (a.D == 128) return a.fp8 ? launch_g<128, true>(a, tk, tv, hnd, s) : launch_g<128, false>(a, tk, tv, hnd, s);
-    if (a.D == 64) return a.fp8 ? launch_g<64, true>(a, tk, tv, hnd, s) : launch_g<64, false>(a, tk, tv, hnd, s);
+    if (a.D == 128) return launch_d<128>(a, tk, tv, hnd, s);
+    if (a.D == 64) return launch_d<64>(a, tk, tv, hnd, s);
     return cudaErrorInvalidValue;
 }
 

@@ -25,6 +25,7 @@ int elem_bytes(int32_t dtype) {
         case PKV_FP8_E4M3: return 1;
         case PKV_F32: return 4;
         case PKV_I32: return 4;
+        case PKV_FP4_E2M1X2: return 1;
         default: return 0;
     }
 }
@@ -66,17 +67,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Tile map over a cache tensor [pages, a, b, D] (NHD: a = P, b = Hkv; HND:
-// a = Hkv, b = P). One box = 16 token rows of one kv head x (128 or 64
-// bytes of the head dim), swizzled to the same span.
+// Tile map over a cache tensor [pages, a, b, W] (NHD: a = P, b = Hkv; HND:
+// a = Hkv, b = P; W = D values, or D/2 bytes of E2M1 pairs). One box = 16
+// token rows of one kv head x (128, 64 or 32 bytes of the row), swizzled to
+// the same span.
 bool make_cache_map(CUtensorMap* m, const pkv_tensor& c, int32_t layout) {
     auto enc = encode_fn();
     if (!enc) return false;
     const int e = elem_bytes(c.dtype);
-    const int D = static_cast<int>(c.shape[3]);
-    const int row = D * e;
+    const int W = static_cast<int>(c.shape[3]);
+    const int row = W * e;
     const int boxb = row >= 128 ? 128 : row;
-    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(c.shape[2]),
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(c.shape[2]),
                           static_cast<cuuint64_t>(c.shape[1]), static_cast<cuuint64_t>(c.shape[0])};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(c.stride[2] * e), static_cast<cuuint64_t>(c.stride[1] * e),
                              static_cast<cuuint64_t>(c.stride[0] * e)};
@@ -86,32 +88,55 @@ bool make_cache_map(CUtensorMap* m, const pkv_tensor& c, int32_t layout) {
     box[2] = layout == PKV_HND ? 1 : kPageSize;
     box[3] = 1;
     cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapSwizzle swz = boxb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : (boxb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
     CUresult r = enc(m, c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
-                     c.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     boxb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     c.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-// Common checks of a cache pair. Returns PKV_OK and fills the dims.
+// Common checks of a cache pair. Returns PKV_OK and fills the dims. NVFP4
+// value caches (PKV_FP4_E2M1X2) hold D/2 bytes per row; the others D values.
 pkv_status check_caches(const pkv_tensor& kc, const pkv_tensor& vc, int32_t layout, int64_t* num_pages,
-                        int* P, int* Hkv, int* D) {
+                        int* P, int* Hkv, int* D, bool nvfp4 = false) {
     if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
     if (kc.ndim != 4 || vc.ndim != 4 || kc.dtype != vc.dtype) return PKV_ERR_INVALID_ARG;
-    if (kc.dtype != PKV_BF16 && kc.dtype != PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+    if (nvfp4 ? kc.dtype != PKV_FP4_E2M1X2 : (kc.dtype != PKV_BF16 && kc.dtype != PKV_FP8_E4M3))
+        return PKV_ERR_INVALID_ARG;
     for (int i = 0; i < 4; ++i)
         if (kc.shape[i] != vc.shape[i] || kc.shape[i] < 0) return PKV_ERR_INVALID_ARG;
     if (!kc.ptr || !vc.ptr) return PKV_ERR_INVALID_ARG;
     *num_pages = kc.shape[0];
     *P = static_cast<int>(layout == PKV_HND ? kc.shape[2] : kc.shape[1]);
     *Hkv = static_cast<int>(layout == PKV_HND ? kc.shape[1] : kc.shape[2]);
-    *D = static_cast<int>(kc.shape[3]);
+    *D = static_cast<int>(nvfp4 ? 2 * kc.shape[3] : kc.shape[3]);
     if (*num_pages < 1 || *P < 1 || *Hkv < 1) return PKV_ERR_INVALID_ARG;
     if (kc.stride[3] != 1 || vc.stride[3] != 1) return PKV_ERR_UNSUPPORTED;
     if (*D != 64 && *D != 128) return PKV_ERR_UNSUPPORTED;
     if (!strides_multiple(kc, 3, 16) || !strides_multiple(vc, 3, 16)) return PKV_ERR_UNSUPPORTED;
     if (!aligned(kc.ptr, 16) || !aligned(vc.ptr, 16)) return PKV_ERR_UNSUPPORTED;
     if (*num_pages > 0x7FFFFFFF / 16) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+// NVFP4 block-scale caches: E4M3 bytes, the value caches' layout with D/16
+// in the last dim, innermost stride 1. With `contiguous` (the decode's bulk
+// copies), the P x D/16 bytes of a (page, kv head) are contiguous and start
+// on 16-byte boundaries (HND only).
+pkv_status check_block_scales(const pkv_tensor& kc, const pkv_tensor& ks, const pkv_tensor& vs, int D,
+                              bool contiguous) {
+    for (const pkv_tensor* t : {&ks, &vs}) {
+        if (!t->ptr || t->ndim != 4 || t->dtype != PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+        for (int i = 0; i < 3; ++i)
+            if (t->shape[i] != kc.shape[i]) return PKV_ERR_INVALID_ARG;
+        if (t->shape[3] != D / 16) return PKV_ERR_INVALID_ARG;
+        if (t->stride[3] != 1) return PKV_ERR_UNSUPPORTED;
+        if (contiguous) {
+            if (t->stride[2] != D / 16 || !aligned(t->ptr, 16) || !strides_multiple(*t, 2, 16))
+                return PKV_ERR_UNSUPPORTED;
+        }
+    }
     return PKV_OK;
 }
 
@@ -147,10 +172,15 @@ const char* pkv_status_string(int32_t status) {
     }
 }
 
-pkv_status pkv_rope_kv_write(const pkv_tensor* q_p, const pkv_tensor* k_p, const pkv_tensor* v_p, const pkv_tensor* positions_p, const pkv_tensor* cos_sin_p,
-                             const pkv_tensor* k_cache_p, const pkv_tensor* v_cache_p, const pkv_tensor* slot_mapping_p, const pkv_tensor* k_scale_p,
-                             const pkv_tensor* v_scale_p, int32_t layout, int32_t rope_style, int32_t* err_flag,
-                             pkv_stream_t stream) {
+// The cache write for every cache format; kbs/vbs are the NVFP4 block-scale
+// caches (null otherwise).
+static pkv_status rope_kv_write_impl(const pkv_tensor* q_p, const pkv_tensor* k_p, const pkv_tensor* v_p,
+                                     const pkv_tensor* positions_p, const pkv_tensor* cos_sin_p,
+                                     const pkv_tensor* k_cache_p, const pkv_tensor* v_cache_p,
+                                     const pkv_tensor* kbs_p, const pkv_tensor* vbs_p,
+                                     const pkv_tensor* slot_mapping_p, const pkv_tensor* k_scale_p,
+                                     const pkv_tensor* v_scale_p, int32_t layout, int32_t rope_style,
+                                     int32_t* err_flag, pkv_stream_t stream, bool nvfp4) {
     const pkv_tensor& q = arg(q_p);
     const pkv_tensor& k = arg(k_p);
     const pkv_tensor& v = arg(v_p);
@@ -164,8 +194,12 @@ pkv_status pkv_rope_kv_write(const pkv_tensor* q_p, const pkv_tensor* k_p, const
     if (rope_style != PKV_ROPE_NEOX && rope_style != PKV_ROPE_INTERLEAVED) return PKV_ERR_INVALID_ARG;
     int64_t num_pages;
     int P, Hkv, D;
-    pkv_status st = check_caches(k_cache, v_cache, layout, &num_pages, &P, &Hkv, &D);
+    pkv_status st = check_caches(k_cache, v_cache, layout, &num_pages, &P, &Hkv, &D, nvfp4);
     if (st != PKV_OK) return st;
+    if (nvfp4) {
+        st = check_block_scales(k_cache, arg(kbs_p), arg(vbs_p), D, false);
+        if (st != PKV_OK) return st;
+    }
     if (!shape_ok(k, 3, PKV_BF16) || !shape_ok(v, 3, PKV_BF16)) return PKV_ERR_INVALID_ARG;
     const int64_t T = k.shape[0];
     if (k.shape[1] != Hkv || k.shape[2] != D || v.shape[0] != T || v.shape[1] != Hkv || v.shape[2] != D)
@@ -179,9 +213,9 @@ pkv_status pkv_rope_kv_write(const pkv_tensor* q_p, const pkv_tensor* k_p, const
     if (!shape_ok(positions, 1, PKV_I32) || !shape_ok(slot_mapping, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;
     if (positions.shape[0] != T || slot_mapping.shape[0] != T) return PKV_ERR_INVALID_ARG;
     if (!shape_ok(cos_sin, 2, PKV_F32) || cos_sin.shape[1] != D || cos_sin.shape[0] < 1) return PKV_ERR_INVALID_ARG;
-    const bool fp8 = k_cache.dtype == PKV_FP8_E4M3;
+    const int kind = nvfp4 ? pkv::kFp4 : (k_cache.dtype == PKV_FP8_E4M3 ? pkv::kFp8 : pkv::kBf16);
     int n_scale = 0;
-    if (fp8) {
+    if (kind != pkv::kBf16) {
         st = check_scales(k_scale, v_scale, Hkv, &n_scale);
         if (st != PKV_OK) return st;
     }
@@ -216,23 +250,56 @@ pkv_status pkv_rope_kv_write(const pkv_tensor* q_p, const pkv_tensor* k_p, const
     a.num_pages = num_pages;
     a.page_size = P;
     a.layout = layout;
-    a.k_scale = fp8 ? static_cast<const float*>(k_scale.ptr) : nullptr;
-    a.v_scale = fp8 ? static_cast<const float*>(v_scale.ptr) : nullptr;
+    a.k_scale = kind != pkv::kBf16 ? static_cast<const float*>(k_scale.ptr) : nullptr;
+    a.v_scale = kind != pkv::kBf16 ? static_cast<const float*>(v_scale.ptr) : nullptr;
     a.n_scale = n_scale;
+    if (nvfp4) {
+        a.k_bs = static_cast<uint8_t*>(arg(kbs_p).ptr);
+        a.v_bs = static_cast<uint8_t*>(arg(vbs_p).ptr);
+        for (int i = 0; i < 4; ++i) {
+            a.kbs_s[i] = arg(kbs_p).stride[i];
+            a.vbs_s[i] = arg(vbs_p).stride[i];
+        }
+    }
     a.T = T;
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.D = D;
     a.interleaved = rope_style == PKV_ROPE_INTERLEAVED;
-    a.fp8 = fp8;
+    a.kind = kind;
     a.err = err_flag;
     return cuda_status(pkv::launch_rope_kv_write(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-pkv_status pkv_paged_gqa_decode(const pkv_tensor* q_p, const pkv_tensor* k_cache_p, const pkv_tensor* v_cache_p, const pkv_tensor* block_tables_p,
-                                const pkv_tensor* seq_lens_p, float softmax_scale, int32_t num_splits, const pkv_tensor* out_partial_p,
-                                const pkv_tensor* lse_partial_p, const pkv_tensor* k_scale_p, const pkv_tensor* v_scale_p, int32_t layout,
-                                int32_t* err_flag, pkv_stream_t stream) {
+pkv_status pkv_rope_kv_write(const pkv_tensor* q, const pkv_tensor* k, const pkv_tensor* v,
+                             const pkv_tensor* positions, const pkv_tensor* cos_sin, const pkv_tensor* k_cache,
+                             const pkv_tensor* v_cache, const pkv_tensor* slot_mapping, const pkv_tensor* k_scale,
+                             const pkv_tensor* v_scale, int32_t layout, int32_t rope_style, int32_t* err_flag,
+                             pkv_stream_t stream) {
+    return rope_kv_write_impl(q, k, v, positions, cos_sin, k_cache, v_cache, nullptr, nullptr, slot_mapping,
+                              k_scale, v_scale, layout, rope_style, err_flag, stream, false);
+}
+
+pkv_status pkv_rope_kv_write_nvfp4(const pkv_tensor* q, const pkv_tensor* k, const pkv_tensor* v,
+                                   const pkv_tensor* positions, const pkv_tensor* cos_sin,
+                                   const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                                   const pkv_tensor* k_block_scale, const pkv_tensor* v_block_scale,
+                                   const pkv_tensor* slot_mapping, const pkv_tensor* k_scale,
+                                   const pkv_tensor* v_scale, int32_t layout, int32_t rope_style,
+                                   int32_t* err_flag, pkv_stream_t stream) {
+    return rope_kv_write_impl(q, k, v, positions, cos_sin, k_cache, v_cache, k_block_scale, v_block_scale,
+                              slot_mapping, k_scale, v_scale, layout, rope_style, err_flag, stream, true);
+}
+
+// The decode for every cache format; kbs/vbs are the NVFP4 block-scale
+// caches (null otherwise).
+static pkv_status paged_gqa_decode_impl(const pkv_tensor* q_p, const pkv_tensor* k_cache_p,
+                                        const pkv_tensor* v_cache_p, const pkv_tensor* kbs_p,
+                                        const pkv_tensor* vbs_p, const pkv_tensor* block_tables_p,
+                                        const pkv_tensor* seq_lens_p, float softmax_scale, int32_t num_splits,
+                                        const pkv_tensor* out_partial_p, const pkv_tensor* lse_partial_p,
+                                        const pkv_tensor* k_scale_p, const pkv_tensor* v_scale_p, int32_t layout,
+                                        int32_t* err_flag, pkv_stream_t stream, bool nvfp4) {
     const pkv_tensor& q = arg(q_p);
     const pkv_tensor& k_cache = arg(k_cache_p);
     const pkv_tensor& v_cache = arg(v_cache_p);
@@ -244,8 +311,12 @@ pkv_status pkv_paged_gqa_decode(const pkv_tensor* q_p, const pkv_tensor* k_cache
     const pkv_tensor& v_scale = arg(v_scale_p);
     int64_t num_pages;
     int P, Hkv, D;
-    pkv_status st = check_caches(k_cache, v_cache, layout, &num_pages, &P, &Hkv, &D);
+    pkv_status st = check_caches(k_cache, v_cache, layout, &num_pages, &P, &Hkv, &D, nvfp4);
     if (st != PKV_OK) return st;
+    if (nvfp4) {
+        st = check_block_scales(k_cache, arg(kbs_p), arg(vbs_p), D, true);
+        if (st != PKV_OK) return st;
+    }
     if (!shape_ok(q, 3, PKV_BF16) || q.shape[2] != D) return PKV_ERR_INVALID_ARG;
     const int64_t B = q.shape[0];
     const int64_t Hq = q.shape[1];
@@ -260,14 +331,15 @@ pkv_status pkv_paged_gqa_decode(const pkv_tensor* q_p, const pkv_tensor* k_cache
         lse_partial.shape[2] != Hq)
         return PKV_ERR_INVALID_ARG;
     if (!std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARG;
-    const bool fp8 = k_cache.dtype == PKV_FP8_E4M3;
+    const int kind = nvfp4 ? pkv::kFp4 : (k_cache.dtype == PKV_FP8_E4M3 ? pkv::kFp8 : pkv::kBf16);
     int n_scale = 0;
-    if (fp8) {
+    if (kind != pkv::kBf16) {
         st = check_scales(k_scale, v_scale, Hkv, &n_scale);
         if (st != PKV_OK) return st;
     }
     const int64_t G = Hq / Hkv;
     if (P != kPageSize) return PKV_ERR_UNSUPPORTED;
+    if (nvfp4 && layout != PKV_HND) return PKV_ERR_UNSUPPORTED;
     if (G > 16) return PKV_ERR_UNSUPPORTED;
     if (num_splits > 4096 || B > 65535 || Hkv > 65535) return PKV_ERR_UNSUPPORTED;
     if (B == 0) return PKV_OK;
@@ -293,9 +365,17 @@ pkv_status pkv_paged_gqa_decode(const pkv_tensor* q_p, const pkv_tensor* k_cache
     a.seq_lens = static_cast<const int32_t*>(seq_lens.ptr);
     a.num_pages = num_pages;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
-    a.k_scale = fp8 ? static_cast<const float*>(k_scale.ptr) : nullptr;
-    a.v_scale = fp8 ? static_cast<const float*>(v_scale.ptr) : nullptr;
+    a.k_scale = kind != pkv::kBf16 ? static_cast<const float*>(k_scale.ptr) : nullptr;
+    a.v_scale = kind != pkv::kBf16 ? static_cast<const float*>(v_scale.ptr) : nullptr;
     a.n_scale = n_scale;
+    if (nvfp4) {
+        a.k_bs = static_cast<const uint8_t*>(arg(kbs_p).ptr);
+        a.v_bs = static_cast<const uint8_t*>(arg(vbs_p).ptr);
+        a.kbs_s0 = arg(kbs_p).stride[0];
+        a.kbs_s1 = arg(kbs_p).stride[1];
+        a.vbs_s0 = arg(vbs_p).stride[0];
+        a.vbs_s1 = arg(vbs_p).stride[1];
+    }
     a.num_splits = num_splits;
     a.out_partial = static_cast<float*>(out_partial.ptr);
     a.op_s0 = out_partial.stride[0];
@@ -309,10 +389,32 @@ pkv_status pkv_paged_gqa_decode(const pkv_tensor* q_p, const pkv_tensor* k_cache
     a.Hkv = Hkv;
     a.D = D;
     a.G = static_cast<int32_t>(G);
-    a.fp8 = fp8;
+    a.kind = kind;
     a.layout = layout;
     a.err = err_flag;
     return cuda_status(pkv::launch_paged_decode(a, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_gqa_decode(const pkv_tensor* q, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                                const pkv_tensor* block_tables, const pkv_tensor* seq_lens, float softmax_scale,
+                                int32_t num_splits, const pkv_tensor* out_partial, const pkv_tensor* lse_partial,
+                                const pkv_tensor* k_scale, const pkv_tensor* v_scale, int32_t layout,
+                                int32_t* err_flag, pkv_stream_t stream) {
+    return paged_gqa_decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, seq_lens, softmax_scale,
+                                 num_splits, out_partial, lse_partial, k_scale, v_scale, layout, err_flag, stream,
+                                 false);
+}
+
+pkv_status pkv_paged_gqa_decode_nvfp4(const pkv_tensor* q, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                                      const pkv_tensor* k_block_scale, const pkv_tensor* v_block_scale,
+                                      const pkv_tensor* block_tables, const pkv_tensor* seq_lens,
+                                      float softmax_scale, int32_t num_splits, const pkv_tensor* out_partial,
+                                      const pkv_tensor* lse_partial, const pkv_tensor* k_scale,
+                                      const pkv_tensor* v_scale, int32_t layout, int32_t* err_flag,
+                                      pkv_stream_t stream) {
+    return paged_gqa_decode_impl(q, k_cache, v_cache, k_block_scale, v_block_scale, block_tables, seq_lens,
+                                 softmax_scale, num_splits, out_partial, lse_partial, k_scale, v_scale, layout,
+                                 err_flag, stream, true);
 }
 
 pkv_status pkv_lse_merge(const pkv_tensor* out_partial_p, const pkv_tensor* lse_partial_p, const pkv_tensor* out_p, const pkv_tensor* lse_out_p,
@@ -364,9 +466,11 @@ pkv_status pkv_lse_merge(const pkv_tensor* out_partial_p, const pkv_tensor* lse_
 int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int64_t total_pages,
                               int32_t max_pages, int32_t cache_dtype, int32_t sm_count) {
     if (B <= 0 || Hkv <= 0 || Hq <= 0 || D <= 0 || total_pages <= 0 || max_pages <= 0 || sm_count <= 0) return 1;
-    const int e = cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
-    const double page_bytes = 2.0 * kPageSize * D * e;              // K + V of one page, one kv head
-    const double slots = static_cast<double>(sm_count) * pkv::decode_ctas_per_sm(D, cache_dtype == PKV_FP8_E4M3);
+    const int kind = cache_dtype == PKV_FP4_E2M1X2 ? pkv::kFp4 : (cache_dtype == PKV_FP8_E4M3 ? pkv::kFp8 : pkv::kBf16);
+    // bytes of one token row of one head: values (+ NVFP4 block scales)
+    const double row = kind == pkv::kFp4 ? D / 2.0 + D / 16.0 : (kind == pkv::kFp8 ? D : 2.0 * D);
+    const double page_bytes = 2.0 * kPageSize * row;                // K + V of one page, one kv head
+    const double slots = static_cast<double>(sm_count) * pkv::decode_ctas_per_sm(D, kind);
     const double c0 = 32768.0 / page_bytes;                          // per-CTA start-up, in pages
     const double units = static_cast<double>(B) * Hkv;
     const double work = static_cast<double>(Hkv) * static_cast<double>(total_pages);

@@ -11,6 +11,10 @@ namespace pkv {
 
 constexpr int kPageSize = 16;  // tokens per page for the decode kernel
 
+// Cache formats: bf16 values, static-scale E4M3 bytes, or NVFP4 (packed
+// E2M1 pairs + one E4M3 block-scale byte per 16 values + a static scale).
+enum CacheKind : int { kBf16 = 0, kFp8 = 1, kFp4 = 2 };
+
 struct RopeArgs {
     uint16_t* q;               // bf16 bits, may be null
     int64_t q_s0, q_s1;        // element strides (token, head)
@@ -30,15 +34,19 @@ struct RopeArgs {
     int64_t num_pages;
     int32_t page_size;
     int32_t layout;            // pkv_layout
-    const float* k_scale;      // fp8 only
+    const float* k_scale;      // fp8 / nvfp4 only
     const float* v_scale;
     int32_t n_scale;           // 1 or Hkv
+    uint8_t* k_bs;             // nvfp4 block scales (E4M3 bytes), else null
+    uint8_t* v_bs;
+    int64_t kbs_s[4];          // byte strides of the 4 block-scale dims, tensor order
+    int64_t vbs_s[4];
     int64_t T;
     int32_t Hq;                // 0 when q is null
     int32_t Hkv;
     int32_t D;
     int32_t interleaved;
-    int32_t fp8;
+    int32_t kind;              // CacheKind
     int32_t* err;
 };
 
@@ -51,16 +59,20 @@ struct DecodeArgs {
     const int32_t* seq_lens;
     int64_t num_pages;
     float scale_log2;          // softmax_scale * log2(e)
-    const float* k_scale;      // fp8 only
+    const float* k_scale;      // fp8 / nvfp4 only
     const float* v_scale;
     int32_t n_scale;
+    const uint8_t* k_bs;       // nvfp4 block scales: the P x D/16 bytes of
+    const uint8_t* v_bs;       // (page, kv head) start at page*s0 + kvh*s1
+    int64_t kbs_s0, kbs_s1;    // (bytes)
+    int64_t vbs_s0, vbs_s1;
     int32_t num_splits;
     float* out_partial;
     int64_t op_s0, op_s1, op_s2;
     float* lse_partial;
     int64_t lp_s0, lp_s1;
     int32_t B, Hq, Hkv, D, G;
-    int32_t fp8;
+    int32_t kind;              // CacheKind
     int32_t layout;            // pkv_layout (selects the TMA coordinate order)
     int32_t* err;
 };
@@ -122,6 +134,6 @@ cudaError_t launch_stream_read(const void* buf, int64_t bytes, uint32_t* sink, i
 
 // Occupancy-related constants of the decode kernel, shared with the split
 // heuristic on the host.
-int decode_ctas_per_sm(int D, int fp8);
+int decode_ctas_per_sm(int D, int kind);
 
 }  // namespace pkv

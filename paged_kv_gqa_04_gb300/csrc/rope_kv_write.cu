@@ -23,6 +23,15 @@
 // reciprocal product when that provably gives the same byte, else from the
 // IEEE division), with the hardware's saturating round-to-nearest-even
 // E4M3 conversion.
+//
+// NVFP4 caches (mainarch, decode-attention section: 4-bit E2M1 KV with block
+// scales; NVFP4 form): a 16-value block of a row is the two 8-value chunks of
+// a lane pair (chunk c and c^1 are adjacent lanes), so the block's largest
+// magnitude takes one shuffle. Its E4M3 scale is the saturating RNE byte of
+// amax / (6 g), g the head's static scale; each value is the E2M1 code of the
+// correctly rounded quotient y / (g s), again from a reciprocal product unless
+// a value lies near an E2M1 rounding boundary. The lane with the even chunk
+// stores the scale of the low-half block, the odd lane that of the high half.
 #include <cuda_fp8.h>
 
 #include "pkv_internal.h"
@@ -96,6 +105,60 @@ __device__ __forceinline__ uint2 pack_e4m3x8(const Chunk8& c, float scale, float
     return make_uint2(w[0], w[1]);
 }
 
+// True when some float within four representable steps of z may have a
+// different E2M1 code than z: |z| in [0.234, 6] with the low 21 bits of its
+// pattern within 4 of zero -- every rounding boundary of E2M1 (0.25, 0.75,
+// 1.25, 1.75, 2.5, 3.5, 5) has those bits zero; so do the E2M1 values and
+// powers of two that the test also catches, harmlessly. Below 0.234 every
+// value gives a zero code, above 6 every value saturates.
+__device__ __forceinline__ bool e2m1_code_may_change(float z) {
+    const uint32_t m = __float_as_uint(z) & 0x7FFFFFFFu;
+    return m >= 0x3E700000u && m <= 0x40C00000u && ((m + 4u) & 0x1FFFFFu) <= 8u;
+}
+
+__device__ __forceinline__ float amax8(const Chunk8& c) {
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(c.v[j]));
+    return m;
+}
+
+// One 8-value half of an NVFP4 block whose largest magnitude is `amax`,
+// under the static scale g (six_g = RN(6 g)): returns the four bytes of
+// E2M1 pairs and the block's E4M3 scale byte. z = RN(y * RN(1/(g s))) is
+// within three representable steps of the correctly rounded quotient
+// y / (g s); when no value is near an E2M1 boundary (or the reciprocal could
+// leave the normal range) the codes of the products are those of the
+// quotients, else the quotients are computed.
+__device__ __forceinline__ uint32_t nvfp4_half(const Chunk8& c, float amax, float g, float six_g, uint32_t& sbyte) {
+    const uint32_t sb = __nv_cvt_float_to_fp8(__fdiv_rn(amax, six_g), __NV_SATFINITE, __NV_E4M3);
+    sbyte = sb;
+    const float s = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sb), __NV_E4M3)));
+    if (s == 0.f) return 0u;
+    const float denom = __fmul_rn(g, s);
+    float z[8];
+    bool near = !(denom >= 0x1p-100f && denom <= 0x1p100f);
+    if (!near) {
+        const float rcp = __frcp_rn(denom);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            z[j] = __fmul_rn(c.v[j], rcp);
+            near |= e2m1_code_may_change(z[j]);
+        }
+    }
+    if (near) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) z[j] = __fdiv_rn(c.v[j], denom);
+    }
+    return pack_e2m1x8(z);
+}
+
+__device__ __forceinline__ uint32_t lane_id() {
+    uint32_t l;
+    asm("mov.u32 %0, %%laneid;" : "=r"(l));
+    return l;
+}
+
 __device__ __forceinline__ void rot(float x1, float x2, float c, float s, float& y1, float& y2) {
     y1 = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s));
     y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
@@ -152,7 +215,7 @@ __device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float (
 // U tokens per thread: all of their loads (slot, position, the row's two
 // chunks, then the cos/sin rows) are issued before any token is processed,
 // so a thread keeps U times as many bytes in flight.
-template <int D, bool INTER, bool FP8, int U>
+template <int D, bool INTER, int KIND, int U>
 __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(const RopeArgs a) {
     constexpr int TPR = D / 16;  // threads per row
     // The decode kernel that usually follows may start its prologue now; it
@@ -206,10 +269,10 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
     }
 
     float scale = 1.f, rcp = 1.f;
-    if constexpr (FP8) {
+    if constexpr (KIND != kBf16) {
         if (!is_q) {
             scale = __ldg((is_k ? a.k_scale : a.v_scale) + (a.n_scale == 1 ? 0 : h));
-            rcp = __frcp_rn(scale);
+            rcp = KIND == kFp8 ? __frcp_rn(scale) : __fmul_rn(6.f, scale);  // nvfp4: RN(6 g)
         }
     }
 #pragma unroll
@@ -238,10 +301,30 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
         const int64_t* st = is_k ? a.kc_s : a.vc_s;
         const int64_t e = (a.layout == PKV_HND) ? page * st[0] + h * st[1] + off * st[2]
                                                 : page * st[0] + off * st[1] + h * st[2];
-        if constexpr (FP8) {
+        if constexpr (KIND == kFp8) {
             uint8_t* dst = static_cast<uint8_t*>(is_k ? a.k_cache : a.v_cache) + e;
             *reinterpret_cast<uint2*>(dst + 8 * c) = pack_e4m3x8(lo, scale, rcp);
             *reinterpret_cast<uint2*>(dst + D / 2 + 8 * c) = pack_e4m3x8(hi, scale, rcp);
+        } else if constexpr (KIND == kFp4) {
+            // both lanes of the pair (chunks c, c^1 of this row) are here
+            const unsigned pair = 3u << (lane_id() & 30u);
+            float am_lo = amax8(lo), am_hi = amax8(hi);
+            am_lo = fmaxf(am_lo, __shfl_xor_sync(pair, am_lo, 1));
+            am_hi = fmaxf(am_hi, __shfl_xor_sync(pair, am_hi, 1));
+            uint32_t s_lo, s_hi;
+            const uint32_t w_lo = nvfp4_half(lo, am_lo, scale, rcp, s_lo);
+            const uint32_t w_hi = nvfp4_half(hi, am_hi, scale, rcp, s_hi);
+            uint8_t* dst = static_cast<uint8_t*>(is_k ? a.k_cache : a.v_cache) + e;
+            *reinterpret_cast<uint32_t*>(dst + 4 * c) = w_lo;
+            *reinterpret_cast<uint32_t*>(dst + D / 4 + 4 * c) = w_hi;
+            const int64_t* bs = is_k ? a.kbs_s : a.vbs_s;
+            const int64_t eb = (a.layout == PKV_HND) ? page * bs[0] + h * bs[1] + off * bs[2]
+                                                     : page * bs[0] + off * bs[1] + h * bs[2];
+            uint8_t* bdst = (is_k ? a.k_bs : a.v_bs) + eb;
+            if (c & 1)
+                bdst[D / 32 + c / 2] = static_cast<uint8_t>(s_hi);
+            else
+                bdst[c / 2] = static_cast<uint8_t>(s_lo);
         } else {
             uint16_t* dst = static_cast<uint16_t*>(is_k ? a.k_cache : a.v_cache) + e;
             *reinterpret_cast<uint4*>(dst + 8 * c) = pack_bf16x8(lo);
@@ -250,7 +333,7 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
     }
 }
 
-template <int D, bool INTER, bool FP8>
+template <int D, bool INTER, int KIND>
 cudaError_t launch_t(const RopeArgs& a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
     const int per_tok = (a.Hq + 2 * a.Hkv) * (D / 16);  // work items of one token
@@ -258,23 +341,32 @@ cudaError_t launch_t(const RopeArgs& a, cudaStream_t s) {
     const int toks = per_tok >= 256 ? 1 : 256 / per_tok;  // tokens per CTA row of threads
     // Two tokens per thread when there are enough tokens to keep every SM
     // busy (cache fills of a bf16 cache); one for a decode step's few tokens
-    // and for FP8 caches (measured slower there: the quantiser's registers
-    // cost more occupancy than the second token's loads gain).
-    const bool two = !FP8 && a.T >= 8192 && per_tok * toks <= 512;
+    // and for quantised caches (measured slower for FP8: the quantiser's
+    // registers cost more occupancy than the second token's loads gain).
+    const bool two = KIND == kBf16 && a.T >= 8192 && per_tok * toks <= 512;
     const int64_t per_cta = static_cast<int64_t>(toks) * (two ? 2 : 1);
     const int64_t blocks = (a.T + per_cta - 1) / per_cta;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
     if (two)
-        rope_kv_write_kernel<D, INTER, FP8, 2><<<static_cast<unsigned>(blocks), dim3(per_tok, toks), 0, s>>>(a);
+        rope_kv_write_kernel<D, INTER, KIND, 2><<<static_cast<unsigned>(blocks), dim3(per_tok, toks), 0, s>>>(a);
     else
-        rope_kv_write_kernel<D, INTER, FP8, 1><<<static_cast<unsigned>(blocks), dim3(per_tok, toks), 0, s>>>(a);
+        rope_kv_write_kernel<D, INTER, KIND, 1><<<static_cast<unsigned>(blocks), dim3(per_tok, toks), 0, s>>>(a);
     return cudaGetLastError();
+}
+
+template <int D, bool INTER>
+cudaError_t launch_k(const RopeArgs& a, cudaStream_t s) {
+    switch (a.kind) {
+        case kBf16: return launch_t<D, INTER, kBf16>(a, s);
+        case kFp8: return launch_t<D, INTER, kFp8>(a, s);
+        case kFp4: return launch_t<D, INTER, kFp4>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <int D>
 cudaError_t launch_d(const RopeArgs& a, cudaStream_t s) {
-    if (a.interleaved) return a.fp8 ? launch_t<D, true, true>(a, s) : launch_t<D, true, false>(a, s);
-    return a.fp8 ? launch_t<D, false, true>(a, s) : launch_t<D, false, false>(a, s);
+    return a.interleaved ? launch_k<D, true>(a, s) : launch_k<D, false>(a, s);
 }
 
 }  // namespace

@@ -27,9 +27,13 @@ class DeviceWorkload:
         self.w = w
         self.device = torch.device(device)
         dev = self.device
-        cache_dtype = torch.uint8 if w.cache_dtype == "fp8" else torch.bfloat16
+        self.nvfp4 = w.cache_dtype == "nvfp4"
+        cache_dtype = torch.bfloat16 if w.cache_dtype == "bf16" else torch.uint8
         self.k_cache = torch.zeros(w.cache_shape(), dtype=cache_dtype, device=dev)
         self.v_cache = torch.zeros(w.cache_shape(), dtype=cache_dtype, device=dev)
+        # NVFP4 block scales (E4M3 bytes, one per 16 values)
+        self.k_block_scale = torch.zeros(w.scale_shape(), dtype=torch.uint8, device=dev) if self.nvfp4 else None
+        self.v_block_scale = torch.zeros(w.scale_shape(), dtype=torch.uint8, device=dev) if self.nvfp4 else None
         self.cos_sin = torch.from_numpy(w.cos_sin()).to(dev)
         self.block_tables = torch.from_numpy(w.block_tables).to(dev)
         self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
@@ -88,14 +92,36 @@ class DeviceWorkload:
     # ---- the three calls -------------------------------------------------------
     def write(self, q, k, v, positions, slot_mapping, stream=None) -> None:
         w = self.w
+        if self.nvfp4:
+            _abi.rope_kv_write_nvfp4(q, k, v, positions, self.cos_sin, self.k_cache, self.v_cache,
+                                     self.k_block_scale, self.v_block_scale, slot_mapping, self.k_scale,
+                                     self.v_scale, w.layout, w.style, self.err, stream)
+            return
         _abi.rope_kv_write(q, k, v, positions, self.cos_sin, self.k_cache, self.v_cache, slot_mapping,
                            self.k_scale, self.v_scale, w.layout, w.style, self.err, stream)
 
+    def caches(self) -> tuple:
+        """The cache tensors: (k, v), plus the block scales for NVFP4."""
+        if self.nvfp4:
+            return self.k_cache, self.v_cache, self.k_block_scale, self.v_block_scale
+        return self.k_cache, self.v_cache
+
     def decode(self, q, stream=None) -> None:
+        self.decode_into(q, self.caches(), self.out_partial, self.lse_partial, stream)
+
+    def decode_into(self, q, caches: tuple, out_partial, lse_partial, stream=None) -> None:
+        """The decode over the given caches (as returned by caches(), or
+        copies of them) into the given partial buffers."""
         w = self.w
-        _abi.paged_gqa_decode(q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens, w.softmax_scale,
-                              self.num_splits, self.out_partial, self.lse_partial, self.k_scale, self.v_scale,
-                              w.layout, self.err, stream)
+        if self.nvfp4:
+            kc, vc, kbs, vbs = caches
+            _abi.paged_gqa_decode_nvfp4(q, kc, vc, kbs, vbs, self.block_tables, self.seq_lens, w.softmax_scale,
+                                        self.num_splits, out_partial, lse_partial, self.k_scale, self.v_scale,
+                                        w.layout, self.err, stream)
+            return
+        kc, vc = caches
+        _abi.paged_gqa_decode(q, kc, vc, self.block_tables, self.seq_lens, w.softmax_scale, self.num_splits,
+                              out_partial, lse_partial, self.k_scale, self.v_scale, w.layout, self.err, stream)
 
     def merge(self, stream=None) -> None:
         _abi.lse_merge(self.out_partial, self.lse_partial, self.out, self.lse, stream)
@@ -121,7 +147,7 @@ class DeviceWorkload:
 
     # ---- host views -------------------------------------------------------------
     def cache_pages_u(self, cache: torch.Tensor, pages) -> np.ndarray:
-        """Raw bytes (uint16 for bf16, uint8 for fp8) of the given pages."""
+        """Raw bytes (uint16 for bf16, uint8 for fp8 / nvfp4) of the given pages."""
         idx = torch.as_tensor(np.asarray(pages, np.int64), device=self.device)
         sel = cache.index_select(0, idx).cpu()
         if sel.dtype == torch.bfloat16:

@@ -188,9 +188,14 @@ class Workload:
 
     @property
     def elem_bytes(self) -> float:
-        """Bytes per cached value (NVFP4: half a byte, plus one scale byte
-        per 16 values, counted by scale_shape)."""
+        """Bytes per cached value in the value cache (NVFP4: half a byte)."""
         return {"fp8": 1, "nvfp4": 0.5}.get(self.cache_dtype, 2)
+
+    @property
+    def cache_bytes_per_value(self) -> float:
+        """Value-cache bytes plus block-scale bytes per cached value (NVFP4:
+        1/2 + 1/16)."""
+        return self.elem_bytes + (1.0 / 16 if self.cache_dtype == "nvfp4" else 0.0)
 
     @property
     def pages_per_seq(self) -> np.ndarray:

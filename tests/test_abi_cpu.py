@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_abi_version() == 2
     for s in range(4):
         assert pkv.status_string(s)
     assert "invalid" in pkv.status_string(1)
@@ -47,7 +47,7 @@ def test_abi_version_and_status_strings(lib):
 def _t(shape, dtype, ptr=0x1000, strides=None):
     d = _abi.PkvTensor()
     d.ptr = ptr
-    d.dtype = {"bf16": 0, "fp8": 1, "f32": 2, "i32": 3}[dtype]
+    d.dtype = {"bf16": 0, "fp8": 1, "f32": 2, "i32": 3, "fp4": 4}[dtype]
     d.ndim = len(shape)
     if strides is None:
         strides, acc = [], 1
@@ -132,6 +132,60 @@ def test_decode_and_merge_reject_inconsistent_arguments(lib):
     assert m(_t((B, S, Hq, 96), "f32"), lp, _t((B, Hq, 96), "bf16"), NULL, None) == _abi.PKV_ERR_UNSUPPORTED
     assert m(op, lp, out, _t((B, Hq + 2), "f32"), None) == _abi.PKV_ERR_INVALID_ARG
     assert lib.pkv_validate_indices(bt, sl, NULL, 50, NULL, None, None) == _abi.PKV_ERR_INVALID_ARG
+
+
+def test_nvfp4_entry_points_reject_inconsistent_arguments(lib):
+    """Host validation of the NVFP4 write and decode: fake pointers, every
+    call returns before any CUDA work."""
+    T, B, Hq, Hkv, D, S, P = 4, 3, 12, 2, 128, 4, 50
+    kc = _t((P, Hkv, 16, D // 2), "fp4")
+    bs = _t((P, Hkv, 16, D // 16), "fp8")
+    g = _t((Hkv,), "f32")
+    w = dict(q=_t((T, Hq, D), "bf16"), k=_t((T, Hkv, D), "bf16"), v=_t((T, Hkv, D), "bf16"),
+             pos=_t((T,), "i32"), cs=_t((100, D), "f32"), kc=kc, vc=kc, kbs=bs, vbs=bs, slot=_t((T,), "i32"),
+             ks=g, vs=g)
+
+    def write(layout=1, **over):
+        a = dict(w, **over)
+        return lib.pkv_rope_kv_write_nvfp4(a["q"], a["k"], a["v"], a["pos"], a["cs"], a["kc"], a["vc"], a["kbs"],
+                                           a["vbs"], a["slot"], a["ks"], a["vs"], layout, 0, None, None)
+
+    assert write(kc=_t((P, Hkv, 16, D // 2), "fp8"), vc=_t((P, Hkv, 16, D // 2), "fp8")) == _abi.PKV_ERR_INVALID_ARG
+    # value caches of D/4 bytes describe D = 64: inconsistent with k, v and the scale caches
+    assert write(kc=_t((P, Hkv, 16, D // 4), "fp4"), vc=_t((P, Hkv, 16, D // 4), "fp4")) == _abi.PKV_ERR_INVALID_ARG
+    assert write(kc=_t((P, Hkv, 16, D), "fp4"), vc=_t((P, Hkv, 16, D), "fp4")) == _abi.PKV_ERR_UNSUPPORTED  # D = 256
+    assert write(kbs=_t((P, Hkv, 16, D // 8), "fp8")) == _abi.PKV_ERR_INVALID_ARG
+    assert write(vbs=_t((P, Hkv, 16, D // 16), "bf16")) == _abi.PKV_ERR_INVALID_ARG
+    assert write(kbs=NULL) == _abi.PKV_ERR_INVALID_ARG
+    assert write(ks=NULL, vs=NULL) == _abi.PKV_ERR_INVALID_ARG            # static scales are required
+    # the bf16/fp8 entry point does not take NVFP4 caches
+    assert lib.pkv_rope_kv_write(w["q"], w["k"], w["v"], w["pos"], w["cs"], kc, kc, w["slot"], g, g, 1, 0,
+                                 None, None) == _abi.PKV_ERR_INVALID_ARG
+    e = dict(q=_t((0, Hq, D), "bf16"), k=_t((0, Hkv, D), "bf16"), v=_t((0, Hkv, D), "bf16"),
+             pos=_t((0,), "i32"), slot=_t((0,), "i32"))
+    assert write(**e) == _abi.PKV_OK
+    assert write(layout=0, kc=_t((P, 16, Hkv, D // 2), "fp4"), vc=_t((P, 16, Hkv, D // 2), "fp4"),
+                 kbs=_t((P, 16, Hkv, D // 16), "fp8"), vbs=_t((P, 16, Hkv, D // 16), "fp8"), **e) == _abi.PKV_OK
+
+    d = dict(q=_t((B, Hq, D), "bf16"), kc=kc, vc=kc, kbs=bs, vbs=bs, bt=_t((B, 10), "i32"), sl=_t((B,), "i32"),
+             op=_t((B, S, Hq, D), "f32"), lp=_t((B, S, Hq), "f32"), ks=g, vs=g)
+
+    def dec(layout=1, **over):
+        a = dict(d, **over)
+        return lib.pkv_paged_gqa_decode_nvfp4(a["q"], a["kc"], a["vc"], a["kbs"], a["vbs"], a["bt"], a["sl"], 0.1, S,
+                                              a["op"], a["lp"], a["ks"], a["vs"], layout, None, None)
+
+    nhd = dict(kc=_t((P, 16, Hkv, D // 2), "fp4"), vc=_t((P, 16, Hkv, D // 2), "fp4"),
+               kbs=_t((P, 16, Hkv, D // 16), "fp8"), vbs=_t((P, 16, Hkv, D // 16), "fp8"))
+    assert dec(layout=0, **nhd) == _abi.PKV_ERR_UNSUPPORTED                 # HND only
+    # the scale bytes of one (page, head) must be contiguous and 16-byte aligned
+    strided = _t((P, Hkv, 16, D // 16), "fp8", strides=[Hkv * 16 * 16, 16 * 16, 16, 1])
+    assert dec(kbs=strided) == _abi.PKV_ERR_UNSUPPORTED
+    assert dec(vbs=_t((P, Hkv, 16, D // 16), "fp8", ptr=0x1008)) == _abi.PKV_ERR_UNSUPPORTED
+    assert dec(ks=NULL) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(q=_t((B, Hq, 64), "bf16")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(q=_t((0, Hq, D), "bf16"), bt=_t((0, 10), "i32"), sl=_t((0,), "i32"), op=_t((0, S, Hq, D), "f32"),
+               lp=_t((0, S, Hq), "f32")) == _abi.PKV_OK
 
 
 def test_split_heuristic(lib):

@@ -40,7 +40,10 @@ def _check(w, dw, seqs):
     for i, b in enumerate(seqs):
         assert np.array_equal(q[b], st["q_rot"][i]), f"q bytes of sequence {b}"
         n = int(w.pages_per_seq[b])
-        for gc, oc in ((dw.k_cache, st["k_cache"]), (dw.v_cache, st["v_cache"])):
+        pairs = [(dw.k_cache, st["k_cache"]), (dw.v_cache, st["v_cache"])]
+        if dw.nvfp4:
+            pairs += [(dw.k_block_scale, st["k_block_scale"]), (dw.v_block_scale, st["v_block_scale"])]
+        for gc, oc in pairs:
             got = dw.cache_pages_u(gc, w.block_tables[b, :n])
             assert np.array_equal(got, oc[st["block_tables"][i, :n]]), f"cache bytes of sequence {b}"
         assert_close_out(op[b], st["out_partial"][i], f"out_partial[{b}]")
@@ -69,7 +72,7 @@ def filled():
     cache.clear()
 
 
-@pytest.mark.parametrize("name", ["qwen", "longctx", "ragged", "fp8", "million"])
+@pytest.mark.parametrize("name", ["qwen", "longctx", "ragged", "fp8", "million", "fp4"])
 def test_full_size_sampled(filled, name):
     w, dw = filled(name)
     dw.decode_inputs["q"].copy_(dw.decode_inputs["q0"])

@@ -6,7 +6,8 @@ inputs, and compares: rotated q and every cache byte bit for bit; partial
 outputs, merged output and LSE within the tolerance of tests/_compare.py.
 Sizes span several pages per warp, ragged last pages, empty splits, block
 tables longer than one 32-entry batch per warp, both layouts, both RoPE
-styles, bf16 and FP8 caches, head dims 64 and 128 and groups of 1 to 16."""
+styles, bf16, FP8 and NVFP4 caches (NVFP4 block scales bit for bit too),
+head dims 64 and 128 and groups of 1 to 16."""
 import numpy as np
 import pytest
 import torch
@@ -38,6 +39,16 @@ CASES = [
     _case("mha_nhd_d128", (1,), seq_lens=[50], Hq=3, Hkv=3, D=128, layout="NHD"),
     _case("empty_and_short", (5,), seq_lens=[0, 1, 20], Hq=8, Hkv=2, D=128),
     _case("long_blocktable_batches", (1, 2), seq_lens=[4800, 4799], Hq=7, Hkv=1, D=128, rope_base=1e6),
+    _case("nvfp4_hnd_d128_g6_tails", (1, 3, 8), seq_lens=[1, 15, 16, 17, 31, 33, 100, 257], Hq=12, Hkv=2,
+          D=128, cache_dtype="nvfp4", rope_base=1e6),
+    _case("nvfp4_hnd_d64_g2_tensor_scale", (1, 2), seq_lens=[3, 70], Hq=4, Hkv=2, D=64, cache_dtype="nvfp4",
+          per_head_scale=False),
+    _case("nvfp4_hnd_d128_g12_interleaved", (2,), seq_lens=[33, 64], Hq=24, Hkv=2, D=128, cache_dtype="nvfp4",
+          style="interleaved", rope_base=5e5, outlier_p=0.05),
+    _case("nvfp4_hnd_d64_g16", (1, 3), seq_lens=[40, 9], Hq=16, Hkv=1, D=64, cache_dtype="nvfp4"),
+    _case("nvfp4_empty_and_short", (5,), seq_lens=[0, 1, 20], Hq=8, Hkv=2, D=128, cache_dtype="nvfp4"),
+    _case("nvfp4_long_blocktable_batches", (1, 2), seq_lens=[4800, 4799], Hq=8, Hkv=1, D=128,
+          cache_dtype="nvfp4", rope_base=1e6),
 ]
 
 
@@ -62,7 +73,10 @@ def run_and_compare(w, S, dw=None):
         n = int(w.pages_per_seq[b])
         if n == 0:
             continue
-        for gc, oc in ((dw.k_cache, st["k_cache"]), (dw.v_cache, st["v_cache"])):
+        pairs = [(dw.k_cache, st["k_cache"]), (dw.v_cache, st["v_cache"])]
+        if dw.nvfp4:
+            pairs += [(dw.k_block_scale, st["k_block_scale"]), (dw.v_block_scale, st["v_block_scale"])]
+        for gc, oc in pairs:
             got = dw.cache_pages_u(gc, w.block_tables[b, :n])
             assert np.array_equal(got, oc[st["block_tables"][b, :n]]), f"cache bytes of sequence {b}"
     assert_close_out(dw.out_partial.cpu().numpy(), st["out_partial"], "out_partial")
