@@ -2,51 +2,58 @@
 //
 // mainarch, decode-attention section: FlashDecoding-style split-KV online
 // softmax, paged KV through a block table with a shuffled layout, GQA that
-// reads each KV head once per group, FP8 KV dequantised in registers, and the
-// memory-bound rules measured there (wide loads, many pages in flight before
-// any cross-lane reduction, every buffer in device memory). Loom Kernels,
-// "Attention" row: paged MQA/GQA decode with local split-K and LSE merge.
+// reads each KV head once per group, FP8 and 4-bit KV dequantised in
+// registers, and the memory-bound rules measured there (wide loads, many
+// pages in flight before any cross-lane reduction, every buffer in device
+// memory). Loom Kernels, "Attention" row: paged MQA/GQA decode with local
+// split-K and LSE merge.
 //
 // Work decomposition. One CTA per (split s, kv head, sequence b) and four
 // warps per CTA; the split's pages are dealt round-robin to the warps. Each
-// warp runs its own ring of NSLOT page slots in shared memory: lane 0 issues
-// TMA tile loads (cp.async.bulk.tensor, 128- or 64-byte swizzle) of the K and
-// V rows of one page (16 tokens x D) into a slot and the slot's mbarrier
-// completes when the bytes land; the warp consumes slot i while the next
-// NSLOT-1 pages stream in, then refills the slot with page i + NSLOT. The
-// block-table entries are read 32 at a time, one batch ahead, so the page
-// id of every TMA issue is already in a register. Nothing waits across
+// warp runs its own ring of NSLOT page slots in shared memory: its lanes
+// issue TMA tile loads (cp.async.bulk.tensor, 128-, 64- or 32-byte swizzle)
+// of the K and V rows of one page (16 tokens x D) into a slot, one copy per
+// lane, and the slot's mbarrier completes when the bytes land; the warp
+// consumes slot i while the next NSLOT-1 pages stream in, then refills the
+// slot with page i + NSLOT.
+// The block-table entries are read 32 at a time, one batch ahead, so the
+// page id of every TMA issue is already in a register. Nothing waits across
 // warps until the final combine.
 //
-// Math per page (16 tokens). The G <= 16 query heads of the group form the
-// M = 16 rows of an mma.sync m16n8k16 tile (rows past G are zero), tokens
-// are N, the head dim is K:
-//   S[16 x 16] = Q[16 x D] . K^T      two n-tiles of 8 tokens, D/16 k-steps
-//   online softmax on S in registers (each thread holds rows g and g+8,
-//   token columns 2t, 2t+1; row max/sum need two quad shuffles)
-//   O[16 x D] += P[16 x 16] . V        D/8 n-tiles, one k-step of 16 tokens
-// bf16 caches feed ldmatrix (non-transposed for K, transposed for V) from
-// the swizzled slots. E4M3 caches are loaded with 16-byte shared loads and
-// converted to f16 in registers (cvt.rn.f16x2.e4m3x2, exact); the head-dim
-// index is permuted consistently between Q and K so that each thread's
-// bytes map straight onto its fragments, V's bytes are paired by token with
-// prmt, and Q and P are f16. Scales fold into the score scale (k_scale) and
-// the output (v_scale).
+// Math per page (16 tokens), with the cache on the M side of mma.sync
+// m16n8k16 and the query heads of the group on N (8 heads per n-tile, one
+// tile for G <= 8, two for G <= 16; heads past G are zero):
+//   S^T[16 tok x 8 h] = K[16 x D] . Q^T      D/16 k-steps
+//   online softmax on S^T in registers: a thread holds tokens g, g+8 of
+//   heads 2t, 2t+1; a head's max over the page is three xor-shuffles over
+//   the eight lanes g
+//   P^T as the B operand: the f16/bf16-packed S^T fragment of each 8-token
+//   half, transposed in registers with movmatrix
+//   O^T[16 d x 8 h] += V^T[16 x 16 tok] . P^T    D/16 m-tiles
+// With the cache as the A operand one mma covers 16 tokens (K) or 16
+// head-dim values (V) of all the group's heads: half the mma count of the
+// heads-as-M form for G <= 8, and half its accumulator and Q registers.
 //
-// NVFP4 caches (mainarch, decode-attention section: paged + GQA + 4-bit E2M1
-// KV with block scales in one kernel; NVFP4 form) use the FP8 path's
-// fragment mapping at half the bytes: a thread's 16-byte (K) or 8-byte (V)
-// share of a row is one or two whole 16-value blocks, so each f16x2 word
-// from cvt.rn.f16x2.e2m1x2 is multiplied (exactly) by its block's E4M3
-// scale, loaded with the page by a 16-byte-aligned bulk copy beside the
-// values. V pairs tokens by nibble: (a & 0x0F0F0F0F) | (b << 4 & 0xF0F0F0F0)
-// puts value d of tokens a and b in one byte. Rows past the sequence end get
-// a zero V scale (their nibbles are finite, so they contribute exactly 0).
+// bf16 caches feed ldmatrix (non-transposed for K, transposed for V) from
+// the swizzled slots. Quantised caches are loaded with 16/8-byte shared
+// loads and converted to f16 in registers: E4M3 with cvt.rn.f16x2.e4m3x2,
+// E2M1 with cvt.rn.f16x2.e2m1x2 followed by an f16x2 multiply by the block's
+// E4M3 scale (both exact). The head-dim index is permuted consistently
+// between Q and K so that each thread's bytes map straight onto its
+// fragments (thread t holds head-dim values [D/4 t, D/4 (t+1)) of K rows g
+// and g+8); V's bytes are paired by token, with prmt (E4M3) or a nibble
+// interleave (a & 0x0F0F0F0F) | (b << 4 & 0xF0F0F0F0) (E2M1), and thread g
+// owns head-dim values [D/8 g, D/8 (g+1)) of V. Q and P are then f16.
+// Static scales fold into the score scale (k_scale) and the output
+// (v_scale). NVFP4 block scales land with the page by a 16-byte-aligned
+// bulk copy beside the values (HND only); rows past the sequence end get a
+// zero V scale (their nibbles are finite, so they contribute exactly 0).
 //
 // The tensor-core work is small (about 4*16*D flops per token and kv head
-// against 4*D bytes of bf16 K/V): the kernel is bound by HBM, and mma.sync
-// only keeps the ALU issue rate far from that bound. Scores and the softmax
-// state are fp32; P enters the PV product as bf16 (bf16 caches) or f16 (FP8).
+// against 4*D bytes of bf16 K/V): the kernel is bound by HBM for bf16, and
+// by the dequantisation's ALU issue for the 1- and 1/2-byte formats, which
+// is why the register budget is sized for four CTAs per SM there. Scores
+// and the softmax state are fp32.
 //
 // Waits are bounded (about one second, then PKV_FLAG_WAIT_TIMEOUT is set,
 // copies still in flight are waited for with the same bound, and the CTA
@@ -57,21 +64,41 @@
 namespace pkv {
 namespace {
 
-// Launch shape: warps per CTA, shared-memory ring bytes per warp and the
-// CTAs per SM the register budget is sized for (tuned on GB300; see the
-// measurements recorded with the profiles).
+// Launch shape per cache format: shared-memory ring bytes per warp and the
+// CTAs per SM that registers and shared memory are sized for (tuned on
+// GB300; see the measurements recorded with the profiles).
 #ifndef PKV_DECODE_WARPS
 #define PKV_DECODE_WARPS 4
 #endif
-#ifndef PKV_DECODE_RING_BYTES
-#define PKV_DECODE_RING_BYTES 16384
+#ifndef PKV_DECODE_RING_BF16
+#define PKV_DECODE_RING_BF16 16384
 #endif
-#ifndef PKV_DECODE_MIN_CTAS
-#define PKV_DECODE_MIN_CTAS 3
+#ifndef PKV_DECODE_CTAS_BF16
+#define PKV_DECODE_CTAS_BF16 3
+#endif
+#ifndef PKV_DECODE_RING_FP8
+#define PKV_DECODE_RING_FP8 12288
+#endif
+#ifndef PKV_DECODE_CTAS_FP8
+#define PKV_DECODE_CTAS_FP8 4
+#endif
+#ifndef PKV_DECODE_RING_FP4
+#define PKV_DECODE_RING_FP4 12800
+#endif
+#ifndef PKV_DECODE_CTAS_FP4
+#define PKV_DECODE_CTAS_FP4 4
 #endif
 constexpr int kWarps = PKV_DECODE_WARPS;
-constexpr int kRingBytes = PKV_DECODE_RING_BYTES;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+constexpr int ring_bytes(int kind) {
+    return kind == kBf16 ? PKV_DECODE_RING_BF16 : (kind == kFp8 ? PKV_DECODE_RING_FP8 : PKV_DECODE_RING_FP4);
+}
+// Two head tiles (G > 8) need twice the accumulators: at most three CTAs.
+constexpr int ctas_per_sm(int kind, int nh) {
+    const int c = kind == kBf16 ? PKV_DECODE_CTAS_BF16 : (kind == kFp8 ? PKV_DECODE_CTAS_FP8 : PKV_DECODE_CTAS_FP4);
+    return nh == 2 && c > 3 ? 3 : c;
+}
 
 template <int D, int KIND>
 struct Cfg {
@@ -87,14 +114,10 @@ struct Cfg {
     // K, V, then the K and V block scales; a slot keeps the swizzle span's
     // alignment (8 rows of BOXB bytes)
     static constexpr int SLOT = (TX + 8 * BOXB - 1) / (8 * BOXB) * (8 * BOXB);
-    static constexpr int NSLOT = kRingBytes / SLOT < 2 ? 2 : (kRingBytes / SLOT > 8 ? 8 : kRingBytes / SLOT);
+    static constexpr int RB = ring_bytes(KIND);
+    static constexpr int NSLOT = RB / SLOT < 2 ? 2 : (RB / SLOT > 8 ? 8 : RB / SLOT);
     static constexpr int RING = NSLOT * SLOT;              // per warp
-    // Pages consumed per iteration. Two (one softmax update per 32 tokens)
-    // measured slower on GB300 for every ring size that fits: it halves the
-    // pages a warp keeps in flight while it computes.
-    static constexpr int PG = 1;
-    static constexpr int KS = D / 16;                      // k-steps of QK
-    static constexpr int NT = D / 8;                       // n-tiles of PV
+    static constexpr int KS = D / 16;                      // k-steps of K.Q^T = m-tiles of V^T.P^T
     static constexpr int SMEM = kWarps * RING + kWarps * NSLOT * 8 + 1024;  // + barriers + alignment
     static_assert(BOXB == 128 || BOXB == 64 || BOXB == 32, "swizzle span");
     static_assert(RING >= (16 * (D + 8) + 32) * 4, "combine area must fit in a warp's ring");
@@ -121,8 +144,8 @@ __device__ __forceinline__ uint32_t swz(int r, int col) {
 __device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16_t>(w & 0xFFFFu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
 
-template <int D, int KIND, bool TWO>
-__global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
+template <int D, int KIND, int NH>
+__global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(KIND, NH))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         const DecodeArgs a, const int hnd) {
     using C = Cfg<D, KIND>;
@@ -216,160 +239,166 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
         const int src = ((i >> 5) == cur_batch) ? cur : nxt;
         return __shfl_sync(0xffffffffu, src, i & 31);
     };
-    auto issue = [&](int i, int pid) {  // called by lane 0
-        const int slot = i % C::NSLOT;
+    // Start the copies of page `pid` into ring slot `slot`; called by the
+    // whole warp (pid is warp-uniform). Lane 0 posts the byte count, then
+    // each copy is issued by its own lane: lane 2 bx + v copies box bx of K
+    // (v = 0) or V (v = 1); NVFP4 scales come from the next two lanes.
+    constexpr int NCOPY = 2 * C::NBOX + (KIND == kFp4 ? 2 : 0);
+    auto issue = [&](int slot, int pid) {
         const uint32_t bar = bar0 + 8 * slot;
         if (pid < 0 || pid >= num_pages) {
-            mbar_arrive(bar);  // completes the phase with no bytes; the page is skipped
+            if (lane == 0) mbar_arrive(bar);  // completes the phase with no bytes; the page is skipped
             return;
         }
-        mbar_arrive_expect_tx(bar, C::TX);
+        if (lane == 0) mbar_arrive_expect_tx(bar, C::TX);
+        __syncwarp();
         const uint32_t kdst = ring0 + slot * C::SLOT;
-        const uint32_t vdst = kdst + C::PAGE;
-        const int c1 = hnd ? 0 : kvh;
-        const int c2 = hnd ? kvh : 0;
-#pragma unroll
-        for (int bx = 0; bx < C::NBOX; ++bx) {
-            const int d0 = bx * (C::BOXB / C::E);
-            tma_load_4d(kdst + bx * kPageSize * C::BOXB, &tmk, bar, d0, c1, c2, pid, policy);
-            tma_load_4d(vdst + bx * kPageSize * C::BOXB, &tmv, bar, d0, c1, c2, pid, policy);
-        }
-        if constexpr (KIND == kFp4) {
-            bulk_load(kdst + 2 * C::PAGE, a.k_bs + pid * a.kbs_s0 + kvh * a.kbs_s1, C::SPAGE, bar, policy);
-            bulk_load(kdst + 2 * C::PAGE + C::SPAGE, a.v_bs + pid * a.vbs_s0 + kvh * a.vbs_s1, C::SPAGE, bar,
-                      policy);
+        const int v = lane & 1;
+        if (lane < 2 * C::NBOX) {
+            const int bx = lane >> 1;
+            tma_load_4d(kdst + v * C::PAGE + bx * kPageSize * C::BOXB, v ? &tmv : &tmk, bar, bx * (C::BOXB / C::E),
+                        hnd ? 0 : kvh, hnd ? kvh : 0, pid, policy);
+        } else if (KIND == kFp4 && lane < NCOPY) {
+            const uint8_t* src = v ? a.v_bs + pid * a.vbs_s0 + kvh * a.vbs_s1 : a.k_bs + pid * a.kbs_s0 + kvh * a.kbs_s1;
+            bulk_load(kdst + 2 * C::PAGE + v * C::SPAGE, src, C::SPAGE, bar, policy);
         }
     };
 
     // prologue: fill the ring
     {
         const int n0 = min(C::NSLOT, nw);
-        for (int i = 0; i < n0; ++i) {
-            const int pid = page_id(i, 0);
-            if (lane == 0) issue(i, pid);
-        }
+        for (int i = 0; i < n0; ++i) issue(i, page_id(i, 0));
     }
 
-    // ---- Q fragments (A operand), loaded once -------------------------------
-    uint32_t qa[C::KS][4];
+    // ---- Q^T fragments (B operand), loaded once: head 8 ht + g ------------
+    // k-step kk, k-rows 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) are head-dim values
+    // 16 kk + 2t (+8) for bf16, and (D/4) t + 4 kk (+2) for the quantised
+    // formats (the order in which a thread's cache bytes hold them).
+    uint32_t qb[NH][C::KS][2];
     {
-        const uint16_t* qb = a.q + b * a.q_s0 + h0 * a.q_s1;
-        const bool rg = g < G;
-        const bool rg8 = TWO && (g + 8 < G);
+        const uint16_t* qbase = a.q + b * a.q_s0 + h0 * a.q_s1;
 #pragma unroll
-        for (int j = 0; j < C::KS; ++j) {
-            int dlo, dhi;
-            if constexpr (C::F16) {
-                dlo = (D / 4) * t + 4 * j;
-                dhi = dlo + 2;
-            } else {
-                dlo = 16 * j + 2 * t;
-                dhi = dlo + 8;
-            }
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
-            if (rg) {
-                w[0] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * a.q_s1 + dlo));
-                w[2] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * a.q_s1 + dhi));
-            }
-            if (rg8) {
-                w[1] = __ldg(reinterpret_cast<const uint32_t*>(qb + (g + 8) * a.q_s1 + dlo));
-                w[3] = __ldg(reinterpret_cast<const uint32_t*>(qb + (g + 8) * a.q_s1 + dhi));
-            }
+        for (int ht = 0; ht < NH; ++ht) {
+            const int h = 8 * ht + g;
+            const bool live = h < G;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if constexpr (C::F16)
-                    qa[j][e] = pack_f16(bf16_lo(w[e]), bf16_hi(w[e]));
-                else
-                    qa[j][e] = w[e];
+            for (int kk = 0; kk < C::KS; ++kk) {
+                const int dlo = C::F16 ? (D / 4) * t + 4 * kk : 16 * kk + 2 * t;
+                const int dhi = C::F16 ? dlo + 2 : dlo + 8;
+                uint32_t w0 = 0u, w1 = 0u;
+                if (live) {
+                    w0 = __ldg(reinterpret_cast<const uint32_t*>(qbase + h * a.q_s1 + dlo));
+                    w1 = __ldg(reinterpret_cast<const uint32_t*>(qbase + h * a.q_s1 + dhi));
+                }
+                if constexpr (C::F16) {
+                    qb[ht][kk][0] = pack_f16(bf16_lo(w0), bf16_hi(w0));
+                    qb[ht][kk][1] = pack_f16(bf16_lo(w1), bf16_hi(w1));
+                } else {
+                    qb[ht][kk][0] = w0;
+                    qb[ht][kk][1] = w1;
+                }
             }
         }
     }
 
     const float sl = a.scale_log2 * ks;
 
-    float acc[C::NT][4];
+    float acc[NH][C::KS][4];
 #pragma unroll
-    for (int n = 0; n < C::NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+    for (int ht = 0; ht < NH; ++ht)
+#pragma unroll
+        for (int md = 0; md < C::KS; ++md) acc[ht][md][0] = acc[ht][md][1] = acc[ht][md][2] = acc[ht][md][3] = 0.f;
+    float mx[NH][2], ls[NH][2];  // running max (log2 units) and partial sum of heads 8 ht + 2t + e
+#pragma unroll
+    for (int ht = 0; ht < NH; ++ht) mx[ht][0] = mx[ht][1] = -INFINITY, ls[ht][0] = ls[ht][1] = 0.f;
     bool ok = true;
     int bad_pages = 0;
     int i = 0;
+    int slot = 0;          // i % NSLOT
+    uint32_t phase = 0u;   // (i / NSLOT) & 1
 
-    // S = Q K^T for the 16 tokens of the page at kb: sc[nt] holds tokens
-    // 8nt + 2t, 8nt + 2t + 1 of rows g and g + 8.
+    // S^T = K Q^T for the 16 tokens of the page at kb: sc[ht] holds tokens
+    // g (e = 0, 1) and g + 8 (e = 2, 3) of heads 8 ht + 2t + (e & 1).
     auto qk_page = [&](uint32_t kb, float (*sc)[4]) {
         if constexpr (KIND == kBf16) {
 #pragma unroll
-            for (int jj = 0; jj < C::KS / 2; ++jj) {
+            for (int kk = 0; kk < C::KS; ++kk) {
+                const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int col = 2 * (16 * kk + 8 * (lane >> 4));
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kb + swz<C::BOXB>(r, col), a0, a1, a2, a3);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int r = 8 * nt + (lane & 7);
-                    const int col = 2 * (32 * jj + 8 * (lane >> 3));
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kb + swz<C::BOXB>(r, col), b0, b1, b2, b3);
-                    mma16816<false>(sc[nt], qa[2 * jj][0], qa[2 * jj][1], qa[2 * jj][2], qa[2 * jj][3], b0, b1);
-                    mma16816<false>(sc[nt], qa[2 * jj + 1][0], qa[2 * jj + 1][1], qa[2 * jj + 1][2],
-                                    qa[2 * jj + 1][3], b2, b3);
-                }
+                for (int ht = 0; ht < NH; ++ht) mma16816<false>(sc[ht], a0, a1, a2, a3, qb[ht][kk][0], qb[ht][kk][1]);
             }
-        } else if constexpr (KIND == kFp4) {
-            // thread t's share of row r: bytes [ (D/8)t, (D/8)(t+1) ), i.e.
-            // values [(D/4)t, (D/4)(t+1)) -- blocks 2t, 2t+1 (D = 128) or t
-            const uint32_t kbs = kb + 2 * C::PAGE;  // K block scales [16][D/16]
+        } else if constexpr (KIND == kFp8) {
+            // rows g and g + 8: bytes [(D/4) t, (D/4)(t + 1)), one word per k-step
+            uint32_t w[2][C::KS];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int r = 8 * nt + g;
-                constexpr int NW = D / 32;          // words of E2M1 pairs per thread
-                uint32_t w[NW];
-                uint32_t sA, sB;                    // {s, s} of the first / second block
-                if constexpr (D == 128) {
-                    const uint4 x0 = lds128(kb + swz<C::BOXB>(r, 16 * t));
-                    w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
-                    const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint16_t>(lds16(kbs + r * C::SROW + 2 * t)));
-                    sA = prmt(s2, s2, 0x1010u);
-                    sB = prmt(s2, s2, 0x3232u);
-                } else {
-                    const uint2 x0 = lds64(kb + swz<C::BOXB>(r, 8 * t));
-                    w[0] = x0.x; w[1] = x0.y;
-                    const uint32_t s1 = lds8(kbs + r * C::SROW + t);
-                    sA = sB = e4m3x2_to_f16x2(static_cast<uint16_t>(s1 | (s1 << 8)));
-                }
-#pragma unroll
-                for (int wi = 0; wi < NW; ++wi) {
-                    uint32_t h[4];
-                    e2m1x8_to_f16x2(w[wi], h);
-                    const uint32_t sc2 = (D == 128 && wi >= 2) ? sB : sA;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) h[e] = hmul2(h[e], sc2);
-                    const int j = 2 * wi;
-                    mma16816<true>(sc[nt], qa[j][0], qa[j][1], qa[j][2], qa[j][3], h[0], h[1]);
-                    mma16816<true>(sc[nt], qa[j + 1][0], qa[j + 1][1], qa[j + 1][2], qa[j + 1][3], h[2], h[3]);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int r = 8 * nt + g;
-                uint32_t w[C::KS];
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = g + 8 * hr;
                 if constexpr (D == 128) {
                     const uint4 x0 = lds128(kb + swz<C::BOXB>(r, 32 * t));
                     const uint4 x1 = lds128(kb + swz<C::BOXB>(r, 32 * t + 16));
-                    w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
-                    w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
+                    w[hr][0] = x0.x; w[hr][1] = x0.y; w[hr][2] = x0.z; w[hr][3] = x0.w;
+                    w[hr][4] = x1.x; w[hr][5] = x1.y; w[hr][6] = x1.z; w[hr][7] = x1.w;
                 } else {
                     const uint4 x0 = lds128(kb + swz<C::BOXB>(r, 16 * t));
-                    w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
+                    w[hr][0] = x0.x; w[hr][1] = x0.y; w[hr][2] = x0.z; w[hr][3] = x0.w;
                 }
+            }
 #pragma unroll
-                for (int j = 0; j < C::KS; ++j)
-                    mma16816<true>(sc[nt], qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(lo16(w[j])),
-                                   e4m3x2_to_f16x2(hi16(w[j])));
+            for (int kk = 0; kk < C::KS; ++kk) {
+                const uint32_t a0 = e4m3x2_to_f16x2(lo16(w[0][kk])), a1 = e4m3x2_to_f16x2(lo16(w[1][kk]));
+                const uint32_t a2 = e4m3x2_to_f16x2(hi16(w[0][kk])), a3 = e4m3x2_to_f16x2(hi16(w[1][kk]));
+#pragma unroll
+                for (int ht = 0; ht < NH; ++ht) mma16816<true>(sc[ht], a0, a1, a2, a3, qb[ht][kk][0], qb[ht][kk][1]);
+            }
+        } else {
+            // rows g and g + 8: bytes [(D/8) t, (D/8)(t + 1)), values
+            // [(D/4) t, (D/4)(t + 1)) -- blocks 2t, 2t+1 (D = 128) or t
+            constexpr int NW = D / 32;              // words of E2M1 pairs per row per thread
+            const uint32_t kbs = kb + 2 * C::PAGE;  // K block scales [16][D/16]
+            uint32_t w[2][NW], sA[2], sB[2];        // sA / sB: {s, s} of the first / second block
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = g + 8 * hr;
+                if constexpr (D == 128) {
+                    const uint4 x0 = lds128(kb + swz<C::BOXB>(r, 16 * t));
+                    w[hr][0] = x0.x; w[hr][1] = x0.y; w[hr][2] = x0.z; w[hr][3] = x0.w;
+                    const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint16_t>(lds16(kbs + r * C::SROW + 2 * t)));
+                    sA[hr] = prmt(s2, s2, 0x1010u);
+                    sB[hr] = prmt(s2, s2, 0x3232u);
+                } else {
+                    const uint2 x0 = lds64(kb + swz<C::BOXB>(r, 8 * t));
+                    w[hr][0] = x0.x; w[hr][1] = x0.y;
+                    const uint32_t s1 = lds8(kbs + r * C::SROW + t);
+                    sA[hr] = sB[hr] = e4m3x2_to_f16x2(static_cast<uint16_t>(s1 | (s1 << 8)));
+                }
+            }
+#pragma unroll
+            for (int wi = 0; wi < NW; ++wi) {
+                uint32_t ha[4], hb[4];
+                e2m1x8_to_f16x2(w[0][wi], ha);
+                e2m1x8_to_f16x2(w[1][wi], hb);
+                const bool second = D == 128 && wi >= 2;  // words 2, 3 hold block 2t + 1
+                const uint32_t fa = second ? sB[0] : sA[0];
+                const uint32_t fb = second ? sB[1] : sA[1];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int kk = 2 * wi + j;
+                    const uint32_t a0 = hmul2(ha[2 * j], fa), a2 = hmul2(ha[2 * j + 1], fa);
+                    const uint32_t a1 = hmul2(hb[2 * j], fb), a3 = hmul2(hb[2 * j + 1], fb);
+#pragma unroll
+                    for (int ht = 0; ht < NH; ++ht)
+                        mma16816<true>(sc[ht], a0, a1, a2, a3, qb[ht][kk][0], qb[ht][kk][1]);
+                }
             }
         }
     };
-    // O += P V for the page at vb; tokens at or past `valid` contribute zero
-    // (their V bytes may be anything, so they are zeroed, not only weighted 0).
-    auto pv_page = [&](uint32_t vb, int valid, uint32_t pa0, uint32_t pa1, uint32_t pa2, uint32_t pa3) {
+    // O^T += V^T P^T for the page at vb; tokens at or past `valid` contribute
+    // zero (their V bytes may be anything, so they are zeroed, not only
+    // weighted 0). pb[ht] = P^T fragments of head tile ht.
+    auto pv_page = [&](uint32_t vb, int valid, const uint32_t (*pb)[2]) {
         if constexpr (KIND == kBf16) {
             uint32_t mk0 = 0xFFFFFFFFu, mk1 = 0xFFFFFFFFu;
             if (valid < kPageSize) {
@@ -377,18 +406,57 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
                 mk1 = (2 * t + 8 < valid ? 0x0000FFFFu : 0u) | (2 * t + 9 < valid ? 0xFFFF0000u : 0u);
             }
 #pragma unroll
-            for (int dp = 0; dp < C::NT / 2; ++dp) {
+            for (int md = 0; md < C::KS; ++md) {
                 const int mi = lane >> 3;
-                const int r = 8 * (mi & 1) + (lane & 7);
-                const int col = 16 * (2 * dp + (mi >> 1));
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vb + swz<C::BOXB>(r, col), b0, b1, b2, b3);
-                mma16816<false>(acc[2 * dp], pa0, pa1, pa2, pa3, b0 & mk0, b1 & mk1);
-                mma16816<false>(acc[2 * dp + 1], pa0, pa1, pa2, pa3, b2 & mk0, b3 & mk1);
+                const int r = (lane & 7) + 8 * (mi >> 1);
+                const int col = 2 * (16 * md + 8 * (mi & 1));
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vb + swz<C::BOXB>(r, col), a0, a1, a2, a3);
+                a0 &= mk0;
+                a1 &= mk0;
+                a2 &= mk1;
+                a3 &= mk1;
+#pragma unroll
+                for (int ht = 0; ht < NH; ++ht) mma16816<false>(acc[ht][md], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);
             }
-        } else if constexpr (KIND == kFp4) {
-            // thread g's share of each row: bytes [(D/16)g, (D/16)(g+1)), values
-            // d = (D/8)g + jn, jn < D/8 -- all in block g (D = 128) or g/2
+        } else if constexpr (KIND == kFp8) {
+            constexpr int NWD = D / 32;  // words of V bytes per token row per thread
+            uint32_t va[4][NWD];
+            const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if constexpr (D == 128) {
+                    const uint4 xv = lds128(vb + swz<C::BOXB>(rows[q], 16 * g));
+                    va[q][0] = xv.x; va[q][1] = xv.y; va[q][2] = xv.z; va[q][3] = xv.w;
+                } else {
+                    const uint2 xv = lds64(vb + swz<C::BOXB>(rows[q], 8 * g));
+                    va[q][0] = xv.x; va[q][1] = xv.y;
+                }
+                if (rows[q] >= valid) {
+#pragma unroll
+                    for (int wd = 0; wd < NWD; ++wd) va[q][wd] = 0u;
+                }
+            }
+#pragma unroll
+            for (int wd = 0; wd < NWD; ++wd) {
+                // bytes {A d, B d, A d+1, B d+1}: tokens 2t / 2t+1 (p) and 2t+8 / 2t+9 (q)
+                const uint32_t pl = prmt(va[0][wd], va[1][wd], 0x5140u);
+                const uint32_t ph = prmt(va[0][wd], va[1][wd], 0x7362u);
+                const uint32_t ql = prmt(va[2][wd], va[3][wd], 0x5140u);
+                const uint32_t qh = prmt(va[2][wd], va[3][wd], 0x7362u);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t pw = j ? ph : pl, qw = j ? qh : ql;
+                    const uint32_t a0 = e4m3x2_to_f16x2(lo16(pw)), a1 = e4m3x2_to_f16x2(hi16(pw));
+                    const uint32_t a2 = e4m3x2_to_f16x2(lo16(qw)), a3 = e4m3x2_to_f16x2(hi16(qw));
+#pragma unroll
+                    for (int ht = 0; ht < NH; ++ht)
+                        mma16816<true>(acc[ht][2 * wd + j], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);
+                }
+            }
+        } else {
+            // thread g's share of each row: bytes [(D/16) g, (D/16)(g+1)),
+            // values (D/8) g + [0, D/8) -- all in block g (D = 128) or g/2
             constexpr int NWD = D / 64;  // words of E2M1 pairs per token row per thread
             const uint32_t vbs = vb + C::PAGE + C::SPAGE;  // V block scales [16][D/16]
             const int blk = D == 128 ? g : (g >> 1);
@@ -423,182 +491,104 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
                 e2m1x8_to_f16x2(yo, go);
 #pragma unroll
                 for (int i2 = 0; i2 < 4; ++i2) {
-                    const int jn = 8 * wd + 2 * i2;
-                    mma16816<true>(acc[jn], pa0, pa1, pa2, pa3, hmul2(he[i2], s01), hmul2(ge[i2], s89));
-                    mma16816<true>(acc[jn + 1], pa0, pa1, pa2, pa3, hmul2(ho[i2], s01), hmul2(go[i2], s89));
-                }
-            }
-        } else {
-            constexpr int NWD = D / 32;  // words of V bytes per token row per thread
-            uint32_t va[4][NWD];
-            const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+                    const uint32_t a0 = hmul2(he[i2], s01), a1 = hmul2(ho[i2], s01);
+                    const uint32_t a2 = hmul2(ge[i2], s89), a3 = hmul2(go[i2], s89);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if constexpr (D == 128) {
-                    const uint4 xv = lds128(vb + swz<C::BOXB>(rows[q], 16 * g));
-                    va[q][0] = xv.x; va[q][1] = xv.y; va[q][2] = xv.z; va[q][3] = xv.w;
-                } else {
-                    const uint2 xv = lds64(vb + swz<C::BOXB>(rows[q], 8 * g));
-                    va[q][0] = xv.x; va[q][1] = xv.y;
+                    for (int ht = 0; ht < NH; ++ht)
+                        mma16816<true>(acc[ht][4 * wd + i2], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);
                 }
-                if (rows[q] >= valid) {
-#pragma unroll
-                    for (int wd = 0; wd < NWD; ++wd) va[q][wd] = 0u;
-                }
-            }
-#pragma unroll
-            for (int wd = 0; wd < NWD; ++wd) {
-                const uint32_t pl = prmt(va[0][wd], va[1][wd], 0x5140u);
-                const uint32_t ph = prmt(va[0][wd], va[1][wd], 0x7362u);
-                const uint32_t ql = prmt(va[2][wd], va[3][wd], 0x5140u);
-                const uint32_t qh = prmt(va[2][wd], va[3][wd], 0x7362u);
-                mma16816<true>(acc[4 * wd + 0], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(lo16(pl)),
-                               e4m3x2_to_f16x2(lo16(ql)));
-                mma16816<true>(acc[4 * wd + 1], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(hi16(pl)),
-                               e4m3x2_to_f16x2(hi16(ql)));
-                mma16816<true>(acc[4 * wd + 2], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(lo16(ph)),
-                               e4m3x2_to_f16x2(lo16(qh)));
-                mma16816<true>(acc[4 * wd + 3], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(hi16(ph)),
-                               e4m3x2_to_f16x2(hi16(qh)));
             }
         }
     };
 
-    // Pages are consumed PG at a time; one softmax update covers all their
-    // tokens.
-    constexpr int PG = C::PG;
-    for (; i < nw; i += PG) {
+    for (; i < nw; ++i) {
         if (i > 0 && (i & 31) == 0) {
             cur = nxt;
             nxt = load_batch((i >> 5) + 1);
         }
-        bool landed = true;
-#pragma unroll
-        for (int j = 0; j < PG; ++j) {
-            const int ij = i + j;
-            if (ij < nw) landed &= mbar_wait_bounded(bar0 + 8 * (ij % C::NSLOT), (ij / C::NSLOT) & 1, kWaitLimitNs);
-        }
+        const bool landed = mbar_wait_bounded(bar0 + 8 * slot, phase, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, landed)) {
             ok = false;
             break;
         }
-        int valid[PG];
-        bool any = false;
+        const int pid = page_id(i, i >> 5);
+        const bool pid_ok = pid >= 0 && pid < num_pages;
+        if (!pid_ok) ++bad_pages;
+        const int p = p0 + warp + kWarps * i;
+        const int valid = pid_ok ? min(kPageSize, L - p * kPageSize) : 0;
+        if (valid > 0) {
+            const uint32_t kslot = ring0 + slot * C::SLOT;
+            float sc[NH][4];
 #pragma unroll
-        for (int j = 0; j < PG; ++j) {
-            const int ij = i + j;
-            const int pid = page_id(ij, i >> 5);
-            const bool pid_ok = pid >= 0 && pid < num_pages;
-            if (ij < nw && !pid_ok) ++bad_pages;
-            const int p = p0 + warp + kWarps * ij;
-            valid[j] = (ij < nw && pid_ok) ? min(kPageSize, L - p * kPageSize) : 0;
-            any |= valid[j] > 0;
-        }
-        if (any) {
-            float sc[2 * PG][4];
-#pragma unroll
-            for (int n = 0; n < 2 * PG; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-            for (int j = 0; j < PG; ++j)
-                if (valid[j] > 0) qk_page(ring0 + ((i + j) % C::NSLOT) * C::SLOT, &sc[2 * j]);
+            for (int ht = 0; ht < NH; ++ht) sc[ht][0] = sc[ht][1] = sc[ht][2] = sc[ht][3] = 0.f;
+            qk_page(kslot, sc);
 
             // ---- online softmax (log2 domain) -------------------------------
-            float x[2 * PG][4];
+            const bool v0 = g < valid, v1 = g + 8 < valid;
+            float pr[NH][4], al[NH][2];
+            bool moved = false;
 #pragma unroll
-            for (int n = 0; n < 2 * PG; ++n)
+            for (int ht = 0; ht < NH; ++ht) {
+                float x[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int tok = 8 * (n & 1) + 2 * t + (e & 1);
-                    x[n][e] = tok < valid[n >> 1] ? sc[n][e] * sl : -INFINITY;
-                }
-            float pmA = -INFINITY, pmB = -INFINITY;
+                for (int e = 0; e < 4; ++e) x[e] = ((e >> 1) ? v1 : v0) ? sc[ht][e] * sl : -INFINITY;
 #pragma unroll
-            for (int n = 0; n < 2 * PG; ++n) {
-                pmA = fmaxf(pmA, fmaxf(x[n][0], x[n][1]));
-                if constexpr (TWO) pmB = fmaxf(pmB, fmaxf(x[n][2], x[n][3]));
-            }
-            pmA = fmaxf(pmA, __shfl_xor_sync(0xffffffffu, pmA, 1));
-            pmA = fmaxf(pmA, __shfl_xor_sync(0xffffffffu, pmA, 2));
-            const float nA = fmaxf(mA, pmA);
-            const float alA = fast_exp2(mA - nA);
-            mA = nA;
-            float nB = 0.f, alB = 1.f;
-            if constexpr (TWO) {
-                pmB = fmaxf(pmB, __shfl_xor_sync(0xffffffffu, pmB, 1));
-                pmB = fmaxf(pmB, __shfl_xor_sync(0xffffffffu, pmB, 2));
-                nB = fmaxf(mB, pmB);
-                alB = fast_exp2(mB - nB);
-                mB = nB;
-            }
-            float pr[2 * PG][4];
-            float sA = 0.f, sB = 0.f;
-#pragma unroll
-            for (int n = 0; n < 2 * PG; ++n) {
-                pr[n][0] = fast_exp2(x[n][0] - nA);
-                pr[n][1] = fast_exp2(x[n][1] - nA);
-                sA += pr[n][0] + pr[n][1];
-                if constexpr (TWO) {
-                    pr[n][2] = fast_exp2(x[n][2] - nB);
-                    pr[n][3] = fast_exp2(x[n][3] - nB);
-                    sB += pr[n][2] + pr[n][3];
-                } else {
-                    pr[n][2] = pr[n][3] = 0.f;
+                for (int e = 0; e < 2; ++e) {
+                    float pm = fmaxf(x[e], x[2 + e]);
+                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+                    const float nm = fmaxf(mx[ht][e], pm);
+                    al[ht][e] = fast_exp2(mx[ht][e] - nm);
+                    moved |= al[ht][e] != 1.f;
+                    mx[ht][e] = nm;
+                    pr[ht][e] = fast_exp2(x[e] - nm);
+                    pr[ht][2 + e] = fast_exp2(x[2 + e] - nm);
+                    ls[ht][e] = ls[ht][e] * al[ht][e] + (pr[ht][e] + pr[ht][2 + e]);
                 }
             }
-            lA = lA * alA + sA;
-            if constexpr (TWO) lB = lB * alB + sB;
-            // rescale the accumulators only when some row's max moved (after
+            // rescale the accumulators only when some head's max moved (after
             // the first pages it rarely does)
-            if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
+            if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-                for (int n = 0; n < C::NT; ++n) {
-                    acc[n][0] *= alA;
-                    acc[n][1] *= alA;
-                    if constexpr (TWO) {
-                        acc[n][2] *= alB;
-                        acc[n][3] *= alB;
+                for (int ht = 0; ht < NH; ++ht)
+#pragma unroll
+                    for (int md = 0; md < C::KS; ++md) {
+                        acc[ht][md][0] *= al[ht][0];
+                        acc[ht][md][1] *= al[ht][1];
+                        acc[ht][md][2] *= al[ht][0];
+                        acc[ht][md][3] *= al[ht][1];
                     }
-                }
             }
-            // ---- O += P V, page by page (P as the A operand: rows g / g+8,
-            // tokens 2t.. and 8+2t.. of the page) -----------------------------
+            // ---- P^T fragments: pack S^T's 8-token halves, transpose ----------
+            uint32_t pb[NH][2];
 #pragma unroll
-            for (int j = 0; j < PG; ++j) {
-                if (valid[j] <= 0) continue;
-                const float* p0r = pr[2 * j];
-                const float* p1r = pr[2 * j + 1];
-                uint32_t pa0, pa1 = 0u, pa2, pa3 = 0u;
+            for (int ht = 0; ht < NH; ++ht) {
+                uint32_t x0, x1;
                 if constexpr (C::F16) {
-                    pa0 = pack_f16(p0r[0], p0r[1]);
-                    pa2 = pack_f16(p1r[0], p1r[1]);
-                    if constexpr (TWO) {
-                        pa1 = pack_f16(p0r[2], p0r[3]);
-                        pa3 = pack_f16(p1r[2], p1r[3]);
-                    }
+                    x0 = pack_f16(pr[ht][0], pr[ht][1]);
+                    x1 = pack_f16(pr[ht][2], pr[ht][3]);
                 } else {
-                    pa0 = pack_bf16(p0r[0], p0r[1]);
-                    pa2 = pack_bf16(p1r[0], p1r[1]);
-                    if constexpr (TWO) {
-                        pa1 = pack_bf16(p0r[2], p0r[3]);
-                        pa3 = pack_bf16(p1r[2], p1r[3]);
-                    }
+                    x0 = pack_bf16(pr[ht][0], pr[ht][1]);
+                    x1 = pack_bf16(pr[ht][2], pr[ht][3]);
                 }
-                pv_page(ring0 + ((i + j) % C::NSLOT) * C::SLOT + C::PAGE, valid[j], pa0, pa1, pa2, pa3);
+                pb[ht][0] = movmatrix_trans(x0);
+                pb[ht][1] = movmatrix_trans(x1);
             }
+            pv_page(kslot + C::PAGE, valid, pb);
         }
 
-        // ---- refill the consumed slots with pages i + NSLOT .. ----------------
+        // ---- refill the consumed slot with page i + NSLOT -------------------
         __syncwarp();
-#pragma unroll
-        for (int j = 0; j < PG; ++j) {
-            const int nx = i + j + C::NSLOT;
-            if (nx < nw) {
-                const int pid2 = page_id(nx, i >> 5);
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    issue(nx, pid2);
-                }
-            }
+        const int nx = i + C::NSLOT;
+        if (nx < nw) {
+            const int pid2 = page_id(nx, i >> 5);
+            fence_proxy_async_smem();  // this warp's reads of the slot before the copies' writes
+            issue(slot, pid2);
+        }
+        if (++slot == C::NSLOT) {
+            slot = 0;
+            phase ^= 1u;
         }
     }
 
@@ -613,40 +603,40 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     if (bad_pages && lane == 0) flag_error(a.err, PKV_FLAG_PAGE_RANGE);
 
     // ---- per-warp state -> shared memory (the warp's own ring) ----------------
-    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-    if constexpr (TWO) {
-        lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-        lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-    }
+#pragma unroll
+    for (int ht = 0; ht < NH; ++ht)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            ls[ht][e] += __shfl_xor_sync(0xffffffffu, ls[ht][e], 4);
+            ls[ht][e] += __shfl_xor_sync(0xffffffffu, ls[ht][e], 8);
+            ls[ht][e] += __shfl_xor_sync(0xffffffffu, ls[ht][e], 16);
+        }
     __syncwarp();
-    // [16][D + 8] partial sums (the 8-float pad makes the float2 stores of
-    // the eight row groups fall on distinct banks), then m[16], l[16]
+    // [16][D + 8] partial sums (the 8-float pad spreads the rows over the
+    // banks), then m[16], l[16]
     constexpr int CWS = D + 8;
     float* cw = reinterpret_cast<float*>(ring);
     float* cm = cw + 16 * CWS;
     float* cl = cm + 16;
-    if (t == 0) {
-        cm[g] = mA;
-        cl[g] = lA;
-        cm[g + 8] = TWO ? mB : -INFINITY;
-        cl[g + 8] = TWO ? lB : 0.f;
-    }
+    if (g == 0) {
 #pragma unroll
-    for (int n = 0; n < C::NT; ++n) {
-        if constexpr (C::F16) {
+        for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int d = (D / 8) * (2 * t + e) + n;
-                cw[g * CWS + d] = acc[n][e];
-                if constexpr (TWO) cw[(g + 8) * CWS + d] = acc[n][2 + e];
+                cm[8 * ht + 2 * t + e] = mx[ht][e];
+                cl[8 * ht + 2 * t + e] = ls[ht][e];
             }
-        } else {
-            const int d = 8 * n + 2 * t;
-            *reinterpret_cast<float2*>(cw + g * CWS + d) = make_float2(acc[n][0], acc[n][1]);
-            if constexpr (TWO) *reinterpret_cast<float2*>(cw + (g + 8) * CWS + d) = make_float2(acc[n][2], acc[n][3]);
-        }
     }
+#pragma unroll
+    for (int ht = 0; ht < NH; ++ht)
+#pragma unroll
+        for (int md = 0; md < C::KS; ++md)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int h = 8 * ht + 2 * t + (e & 1);
+                const int d = C::F16 ? (D / 8) * g + 2 * md + (e >> 1) : 16 * md + g + 8 * (e >> 1);
+                cw[h * CWS + d] = acc[ht][md][e];
+            }
     __syncthreads();
 
     // ---- combine the four warps ------------------------------------------------
@@ -681,10 +671,10 @@ __global__ void __launch_bounds__(kWarps * 32, PKV_DECODE_MIN_CTAS)
     }
 }
 
-template <int D, int KIND, bool TWO>
+template <int D, int KIND, int NH>
 cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int hnd, cudaStream_t s) {
     using C = Cfg<D, KIND>;
-    auto kern = paged_decode_kernel<D, KIND, TWO>;
+    auto kern = paged_decode_kernel<D, KIND, NH>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid(a.num_splits, a.Hkv, a.B);
@@ -693,7 +683,7 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
 
 template <int D, int KIND>
 cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int hnd, cudaStream_t s) {
-    return a.G > 8 ? launch_t<D, KIND, true>(a, tk, tv, hnd, s) : launch_t<D, KIND, false>(a, tk, tv, hnd, s);
+    return a.G > 8 ? launch_t<D, KIND, 2>(a, tk, tv, hnd, s) : launch_t<D, KIND, 1>(a, tk, tv, hnd, s);
 }
 
 template <int D>
@@ -708,10 +698,9 @@ cudaError_t launch_d(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
 
 }  // namespace
 
-int decode_ctas_per_sm(int D, int kind) {
+int decode_ctas_per_sm(int D, int kind, int G) {
     (void)D;
-    (void)kind;
-    return PKV_DECODE_MIN_CTAS;
+    return ctas_per_sm(kind, G > 8 ? 2 : 1);
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,

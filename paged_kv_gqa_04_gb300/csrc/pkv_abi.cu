@@ -470,7 +470,7 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
     // bytes of one token row of one head: values (+ NVFP4 block scales)
     const double row = kind == pkv::kFp4 ? D / 2.0 + D / 16.0 : (kind == pkv::kFp8 ? D : 2.0 * D);
     const double page_bytes = 2.0 * kPageSize * row;                // K + V of one page, one kv head
-    const double slots = static_cast<double>(sm_count) * pkv::decode_ctas_per_sm(D, kind);
+    const double slots = static_cast<double>(sm_count) * pkv::decode_ctas_per_sm(D, kind, (Hq + Hkv - 1) / Hkv);
     const double c0 = 32768.0 / page_bytes;                          // per-CTA start-up, in pages
     const double units = static_cast<double>(B) * Hkv;
     const double work = static_cast<double>(Hkv) * static_cast<double>(total_pages);

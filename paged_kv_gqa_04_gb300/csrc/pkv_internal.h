@@ -134,6 +134,6 @@ cudaError_t launch_stream_read(const void* buf, int64_t bytes, uint32_t* sink, i
 
 // Occupancy-related constants of the decode kernel, shared with the split
 // heuristic on the host.
-int decode_ctas_per_sm(int D, int kind);
+int decode_ctas_per_sm(int D, int kind, int G);
 
 }  // namespace pkv

@@ -42,19 +42,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns`
+// nanoseconds waiting for the phase (it resumes as soon as the phase
+// completes), so a waiting warp leaves the issue slots to the others.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 // Wait for the phase with the given parity to complete, giving up after
-// about `limit_ns` nanoseconds. Returns false on timeout.
+// about `limit_ns` nanoseconds. Returns false on timeout. Each retry
+// suspends the thread for at most 100 us, so the limit is checked at least
+// that often.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
         if (global_ns() - t0 > limit_ns) return false;
     }
 }
@@ -135,6 +150,15 @@ __device__ __forceinline__ uint32_t lds8(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held as an mma fragment (lane
+// 4r + c holds row r, columns 2c and 2c+1): returns the same fragment of
+// the transposed matrix.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
 }
 
 // D(16x8 f32) += A(16x16) * B(16x8), bf16 or f16 operands.
