@@ -80,6 +80,11 @@ def _L():
         lib.orc_rope_kv_write_nvfp4.restype = i64
         lib.orc_paged_decode_nvfp4.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, i64, i32, P, P, i32, P,
                                                i32, P, dbl, i32, P, P]
+        lib.orc_mla_cache_write.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, i64, P, P, i64, i32,
+                                            ctypes.c_float, P]
+        lib.orc_mla_cache_write.restype = i64
+        lib.orc_mla_decode.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, i64, ctypes.c_float, P, i32, P,
+                                       dbl, i32, P, P]
         _lib = lib
     return _lib
 
@@ -288,4 +293,41 @@ def paged_decode_nvfp4(q, k_cache, v_cache, k_block_scale, v_block_scale, block_
     _L().orc_paged_decode_nvfp4(B, Hq, Hkv, D, P, _p(q), _p(k_cache), _p(v_cache), _p(k_block_scale),
                                 _p(v_block_scale), num_pages, LAYOUT[layout], _p(ks), _p(vs), ks.size, _p(bt),
                                 bt.shape[1], _p(sl), float(softmax_scale), num_splits, _p(o), _p(l))
+    return o, l
+
+
+# ---- MLA (absorbed decode form) -----------------------------------------------
+def mla_cache_write(q_pe, ckv, kpe, positions, cos_sin, ckv_cache, kpe_cache, slot_mapping, ckv_scale: float,
+                    style: str = "interleaved") -> int:
+    """In place on numpy arrays: ckv_cache uint8 [pages, P, Dc] (E4M3),
+    kpe_cache uint16 [pages, P, Dr] (bf16 bits), q_pe [T, H, Dr] (or None)
+    rotated in place. ckv [T, Dc], kpe [T, Dr] bf16 bits."""
+    ckv = _c(ckv, np.uint16); kpe = _c(kpe, np.uint16)
+    T, Dc = ckv.shape
+    Dr = kpe.shape[1]
+    H = 0 if q_pe is None else q_pe.shape[1]
+    assert ckv_cache.dtype == np.uint8 and kpe_cache.dtype == np.uint16
+    assert ckv_cache.flags.c_contiguous and kpe_cache.flags.c_contiguous
+    if q_pe is not None:
+        assert q_pe.dtype == np.uint16 and q_pe.flags.c_contiguous
+    pos = _c(positions, np.int32); slot = _c(slot_mapping, np.int32)
+    cs = _c(cos_sin, np.float32)
+    return int(_L().orc_mla_cache_write(T, H, Dc, Dr, ckv_cache.shape[1], _p(q_pe), _p(ckv), _p(kpe), _p(pos),
+                                        _p(cs), cs.shape[0], _p(ckv_cache), _p(kpe_cache), ckv_cache.shape[0],
+                                        int(style == "interleaved"), float(ckv_scale), _p(slot)))
+
+
+def mla_decode(q_lat, q_pe, ckv_cache, kpe_cache, block_tables, seq_lens, softmax_scale: float, num_splits: int,
+               ckv_scale: float):
+    """(out_partial [B,S,H,Dc], lse_partial [B,S,H]) float64."""
+    q_lat = _c(q_lat, np.uint16); q_pe = _c(q_pe, np.uint16)
+    B, H, Dc = q_lat.shape
+    Dr = q_pe.shape[2]
+    num_pages, P, _ = ckv_cache.shape
+    bt = _c(block_tables, np.int32); sl = _c(seq_lens, np.int32)
+    o = np.empty((B, num_splits, H, Dc), np.float64)
+    l = np.empty((B, num_splits, H), np.float64)
+    _L().orc_mla_decode(B, H, Dc, Dr, P, _p(q_lat), _p(q_pe), _p(_c(ckv_cache, np.uint8)),
+                        _p(_c(kpe_cache, np.uint16)), num_pages, float(ckv_scale), _p(bt), bt.shape[1], _p(sl),
+                        float(softmax_scale), num_splits, _p(o), _p(l))
     return o, l

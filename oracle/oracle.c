@@ -517,6 +517,134 @@ void orc_paged_decode(int B, int Hq, int Hkv, int D, int page_size, const uint16
     free(o);
 }
 
+/* ---------------------------------------------------------------------- */
+/* Multi-head latent attention (MLA), absorbed decode form.                */
+/* mainarch, MLA decode section: the cache holds one compressed latent     */
+/* per token -- ckv, 512 values, stored as FP8 E4M3 -- beside a 64-value   */
+/* positional part kpe stored as BF16; the per-head projections are        */
+/* applied to the query before the cache is read (q_lat = the query        */
+/* already in latent space), so every head attends to the same cache rows: */
+/* per-head dot scores over [ckv | kpe], a local softmax with an exported  */
+/* LSE, softmax-weighted latent outputs (V = ckv), split-K over the        */
+/* sequence and a stage-2 merge of the partial records (orc_lse_merge).    */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * MLA cache write. For every token t with slot_mapping[t] >= 0 (slot =
+ * page * page_size + offset; ckv_cache [pages][P][Dc] bytes, kpe_cache
+ * [pages][P][Dr] bf16 bits):
+ *   ckv_cache[slot][d] = E4M3(f32(ckv[t][d] / ckv_scale))   saturating RNE,
+ *                        the rule of the FP8 KV write;
+ *   kpe_cache[slot]    = bf16(RoPE(kpe[t]))  RoPE of the Dr-value row with
+ *                        cos_sin row positions[t] (orc_rope_row_f32);
+ *   q_pe[t][h]         = bf16(RoPE(q_pe[t][h])) in place, when q_pe != NULL.
+ * Tokens whose slot is >= num_pages*page_size or whose position is outside
+ * [0, max_pos) are skipped (q_pe untouched) and counted in the return value.
+ */
+int64_t orc_mla_cache_write(int64_t T, int H, int Dc, int Dr, int page_size, uint16_t* q_pe,
+                            const uint16_t* ckv, const uint16_t* kpe, const int32_t* positions,
+                            const float* cos_sin, int64_t max_pos, uint8_t* ckv_cache, uint16_t* kpe_cache,
+                            int64_t num_pages, int interleaved, float ckv_scale, const int32_t* slot_mapping) {
+    int64_t bad = 0;
+    float* y = (float*)malloc(sizeof(float) * (size_t)Dr);
+    int64_t num_slots = num_pages * page_size;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        int64_t pos = positions[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots || pos < 0 || pos >= max_pos) { ++bad; continue; }
+        const float* cs = cos_sin + pos * Dr;
+        if (q_pe) {
+            for (int h = 0; h < H; ++h) {
+                uint16_t* row = q_pe + (t * H + h) * Dr;
+                orc_rope_row_f32(row, cs, y, Dr, interleaved);
+                for (int r = 0; r < Dr; ++r) row[r] = orc_bf16_rne(y[r]);
+            }
+        }
+        for (int d = 0; d < Dc; ++d) {
+            float z = orc_f32(orc_bf16_to_f64(ckv[t * Dc + d]) / (double)ckv_scale);
+            ckv_cache[slot * Dc + d] = orc_e4m3_sat_rne(z);
+        }
+        orc_rope_row_f32(kpe + t * Dr, cs, y, Dr, interleaved);
+        for (int r = 0; r < Dr; ++r) kpe_cache[slot * Dr + r] = orc_bf16_rne(y[r]);
+    }
+    free(y);
+    return bad;
+}
+
+/*
+ * MLA decode. For sequence b with L = seq_lens[b] tokens, split s covers the
+ * logical pages [s*pps, min((s+1)*pps, npages)), npages = ceil(L/P),
+ * pps = ceil(npages / S). For head h, over the split's tokens t:
+ *   score_t = softmax_scale * ( sum_d q_lat[b,h,d] * ckv_t[d]
+ *                             + sum_r q_pe[b,h,r]  * kpe_t[r] )
+ * with ckv_t[d] = E4M3 byte value * ckv_scale; then a plain two-pass softmax
+ * in float64: out_partial[b,s,h,:] = sum_t e^(score_t - m) ckv_t / l,
+ * lse_partial[b,s,h] = m + ln l (empty split: 0 and -inf). Pages whose
+ * block-table entry is outside [0, num_pages) are left out.
+ * q_lat [B][H][Dc], q_pe [B][H][Dr] bf16 bits; out_partial [B][S][H][Dc],
+ * lse_partial [B][S][H].
+ */
+void orc_mla_decode(int B, int H, int Dc, int Dr, int page_size, const uint16_t* q_lat, const uint16_t* q_pe,
+                    const uint8_t* ckv_cache, const uint16_t* kpe_cache, int64_t num_pages, float ckv_scale,
+                    const int32_t* block_tables, int max_pages, const int32_t* seq_lens, double softmax_scale,
+                    int num_splits, double* out_partial, double* lse_partial) {
+    double* ql = (double*)malloc(sizeof(double) * (size_t)Dc);
+    double* qr = (double*)malloc(sizeof(double) * (size_t)Dr);
+    double cs = (double)ckv_scale;
+    for (int b = 0; b < B; ++b) {
+        int64_t L = seq_lens[b];
+        if (L < 0) L = 0;
+        int64_t npages = (L + page_size - 1) / page_size;
+        if (npages > max_pages) npages = max_pages;
+        if (L > npages * page_size) L = npages * page_size;
+        int64_t pps = (npages + num_splits - 1) / num_splits;
+        int64_t cap = pps * page_size > 0 ? pps * page_size : 1;
+        double* sc = (double*)malloc(sizeof(double) * (size_t)cap);
+        int64_t* where = (int64_t*)malloc(sizeof(int64_t) * (size_t)cap);
+        for (int h = 0; h < H; ++h) {
+            for (int d = 0; d < Dc; ++d) ql[d] = orc_bf16_to_f64(q_lat[((int64_t)b * H + h) * Dc + d]);
+            for (int r = 0; r < Dr; ++r) qr[r] = orc_bf16_to_f64(q_pe[((int64_t)b * H + h) * Dr + r]);
+            for (int s = 0; s < num_splits; ++s) {
+                int64_t row = ((int64_t)b * num_splits + s) * H + h;
+                double* o = out_partial + row * Dc;
+                int64_t p0 = (int64_t)s * pps, p1 = p0 + pps;
+                if (p1 > npages) p1 = npages;
+                int64_t n = 0;
+                for (int64_t p = p0; p < p1; ++p) {
+                    int64_t page = block_tables[(int64_t)b * max_pages + p];
+                    if (page < 0 || page >= num_pages) continue;
+                    for (int off = 0; off < page_size; ++off) {
+                        if (p * page_size + off >= L) break;
+                        int64_t slot = page * page_size + off;
+                        double dot = 0.0;
+                        for (int d = 0; d < Dc; ++d) dot += ql[d] * (orc_e4m3_to_f64(ckv_cache[slot * Dc + d]) * cs);
+                        for (int r = 0; r < Dr; ++r) dot += qr[r] * orc_bf16_to_f64(kpe_cache[slot * Dr + r]);
+                        sc[n] = softmax_scale * dot;
+                        where[n] = slot;
+                        ++n;
+                    }
+                }
+                for (int d = 0; d < Dc; ++d) o[d] = 0.0;
+                if (n == 0) { lse_partial[row] = -INFINITY; continue; }
+                double m = sc[0];
+                for (int64_t i = 1; i < n; ++i) if (sc[i] > m) m = sc[i];
+                double l = 0.0;
+                for (int64_t i = 0; i < n; ++i) l += exp(sc[i] - m);
+                for (int64_t i = 0; i < n; ++i) {
+                    double w = exp(sc[i] - m) / l;
+                    for (int d = 0; d < Dc; ++d) o[d] += w * (orc_e4m3_to_f64(ckv_cache[where[i] * Dc + d]) * cs);
+                }
+                lse_partial[row] = m + log(l);
+            }
+        }
+        free(where);
+        free(sc);
+    }
+    free(qr);
+    free(ql);
+}
+
 /*
  * Merge of S partials of one row: M = max_s lse_s; w_s = exp(lse_s - M);
  * out = sum_s w_s o_s / sum_s w_s; lse = M + ln sum_s w_s. A row whose every

@@ -116,6 +116,17 @@ void orc_paged_decode_nvfp4(int B, int Hq, int Hkv, int D, int page_size, const 
                             const int32_t* seq_lens, double softmax_scale, int num_splits,
                             double* out_partial, double* lse_partial);
 
+/* MLA (absorbed decode form): latent cache ckv [pages][P][Dc] E4M3 bytes and
+ * kpe [pages][P][Dr] bf16 bits; see oracle.c. */
+int64_t orc_mla_cache_write(int64_t T, int H, int Dc, int Dr, int page_size, uint16_t* q_pe,
+                            const uint16_t* ckv, const uint16_t* kpe, const int32_t* positions,
+                            const float* cos_sin, int64_t max_pos, uint8_t* ckv_cache, uint16_t* kpe_cache,
+                            int64_t num_pages, int interleaved, float ckv_scale, const int32_t* slot_mapping);
+void orc_mla_decode(int B, int H, int Dc, int Dr, int page_size, const uint16_t* q_lat, const uint16_t* q_pe,
+                    const uint8_t* ckv_cache, const uint16_t* kpe_cache, int64_t num_pages, float ckv_scale,
+                    const int32_t* block_tables, int max_pages, const int32_t* seq_lens, double softmax_scale,
+                    int num_splits, double* out_partial, double* lse_partial);
+
 /* Merge: out_partial [B,S,Hq,D], lse_partial [B,S,Hq] -> out [B,Hq,D],
  * lse [B,Hq]. */
 void orc_lse_merge(int B, int S, int Hq, int D, const double* out_partial,

@@ -396,3 +396,144 @@ def custom_workload(name: str, seed: int, seq_lens, Hq: int, Hkv: int, D: int, l
         vs = (0.5 + uniform(stream_key(seed, "vscale"), n)).astype(np.float32)
     return Workload(name, seed, len(L), Hq, Hkv, D, layout, style, cache_dtype, rope_base, L, pool, bt,
                     ks, vs, k_mult=k_mult, outlier_p=outlier_p)
+
+
+# ---- multi-head latent attention (MLA) workloads ---------------------------------
+MLA_PAGE_SIZE = 64   # tokens per page of the latent cache (mainarch's MLA run: 51,200 tokens in 800 pages)
+MLA_DC = 512         # compressed latent (ckv) values per token
+MLA_DR = 64          # positional (kpe) values per token
+
+
+@dataclasses.dataclass
+class MlaWorkload:
+    """One MLA decode workload: B sequences, H query heads sharing one latent
+    cache of Dc-value ckv rows (FP8 E4M3, static per-tensor scale) and
+    Dr-value kpe rows (bf16), pages of page_size tokens."""
+    name: str
+    seed: int
+    B: int
+    H: int
+    seq_lens: np.ndarray            # int32 [B]
+    num_pages: int
+    block_tables: np.ndarray        # int32 [B, max_pages], -1 padded
+    ckv_scale: float                # float32-representable (the call takes a float32)
+    rope_base: float = 1e4
+    style: str = "interleaved"
+    Dc: int = MLA_DC
+    Dr: int = MLA_DR
+    page_size: int = MLA_PAGE_SIZE
+
+    @property
+    def softmax_scale(self) -> float:
+        # the query/key head width of the absorbed form: 128 no-position
+        # values (as in the per-head projections) + Dr positional values
+        return 1.0 / math.sqrt(128 + self.Dr)
+
+    @property
+    def pages_per_seq(self) -> np.ndarray:
+        return (self.seq_lens.astype(np.int64) + self.page_size - 1) // self.page_size
+
+    @property
+    def max_pos(self) -> int:
+        return int(self.seq_lens.max()) if self.B else 1
+
+    def cos_sin(self) -> np.ndarray:
+        return cos_sin_table(max(self.max_pos, 1), self.Dr, self.rope_base)
+
+    def seq_latent(self, b: int):
+        """bf16 bits of ckv [L, Dc] and kpe [L, Dr] (kpe before rotation) of
+        sequence b."""
+        L = int(self.seq_lens[b])
+        ckv = normal_f32(stream_key(self.seed, "ckv", b), L * self.Dc)
+        kpe = normal_f32(stream_key(self.seed, "kpe", b), L * self.Dr)
+        return f32_to_bf16_trunc(ckv).reshape(L, self.Dc), f32_to_bf16_trunc(kpe).reshape(L, self.Dr)
+
+    def seq_q(self, b: int):
+        """bf16 bits of the new token's q_lat [H, Dc] and q_pe [H, Dr] (q_pe
+        before rotation)."""
+        ql = normal_f32(stream_key(self.seed, "qlat", b), self.H * self.Dc)
+        qp = normal_f32(stream_key(self.seed, "qpe", b), self.H * self.Dr)
+        return f32_to_bf16_trunc(ql).reshape(self.H, self.Dc), f32_to_bf16_trunc(qp).reshape(self.H, self.Dr)
+
+    def slots(self, b: int, positions: np.ndarray) -> np.ndarray:
+        pos = np.asarray(positions, dtype=np.int64)
+        page = self.block_tables[b, pos // self.page_size].astype(np.int64)
+        return (page * self.page_size + pos % self.page_size).astype(np.int32)
+
+    def fill_batch(self, seqs=None):
+        """Context tokens 0..L-2 of each sequence as one cache-write call with
+        no q: dict(ckv [T,Dc], kpe [T,Dr] uint16, positions [T], slot_mapping [T])."""
+        seqs = range(self.B) if seqs is None else seqs
+        cs, ks, ps, ss = [], [], [], []
+        for b in seqs:
+            L = int(self.seq_lens[b])
+            if L <= 1:
+                continue
+            c, k = self.seq_latent(b)
+            pos = np.arange(L - 1, dtype=np.int32)
+            cs.append(c[:L - 1]); ks.append(k[:L - 1]); ps.append(pos); ss.append(self.slots(b, pos))
+        if not cs:
+            return dict(ckv=np.zeros((0, self.Dc), np.uint16), kpe=np.zeros((0, self.Dr), np.uint16),
+                        positions=np.zeros(0, np.int32), slot_mapping=np.zeros(0, np.int32))
+        return dict(ckv=np.concatenate(cs), kpe=np.concatenate(ks), positions=np.concatenate(ps),
+                    slot_mapping=np.concatenate(ss))
+
+    def decode_batch(self):
+        """The new token (position L-1) of every sequence: dict(q_lat [B,H,Dc],
+        q_pe [B,H,Dr], ckv [B,Dc], kpe [B,Dr], positions [B], slot_mapping [B])."""
+        ql = np.zeros((self.B, self.H, self.Dc), np.uint16)
+        qp = np.zeros((self.B, self.H, self.Dr), np.uint16)
+        ckv = np.zeros((self.B, self.Dc), np.uint16)
+        kpe = np.zeros((self.B, self.Dr), np.uint16)
+        pos = np.zeros(self.B, np.int32)
+        slot = np.full(self.B, -1, np.int32)
+        for b in range(self.B):
+            L = int(self.seq_lens[b])
+            ql[b], qp[b] = self.seq_q(b)
+            if L >= 1:
+                c, k = self.seq_latent(b)
+                ckv[b] = c[L - 1]; kpe[b] = k[L - 1]
+                pos[b] = L - 1
+                slot[b] = self.slots(b, np.array([L - 1]))[0]
+        return dict(q_lat=ql, q_pe=qp, ckv=ckv, kpe=kpe, positions=pos, slot_mapping=slot)
+
+
+def make_mla_workload(name: str, seed: Optional[int] = None) -> MlaWorkload:
+    """The MLA decode workloads (latent 512 FP8 + positional 64 bf16, pages of
+    64 tokens, interleaved RoPE base 1e4 on the positional part):
+
+    mla_tiny   B2, L {100, 300} (7 pages), 8 heads, an 11-page shuffled pool
+    mla        B1, L 51,200 (800 pages), 8 heads, 1024-page shuffled pool:
+               mainarch's MLA decode run (51,200 tokens across 800 pages,
+               8 heads)
+    mla_batch  B32, L ~ U[4096, 16384], 16 heads (a 128-head model over 8
+               GPUs), pool = the pages needed, shuffled
+    """
+    idx = {"mla_tiny": 0, "mla": 1, "mla_batch": 2}[name]
+    seed = 2000 + idx if seed is None else seed
+    cs = float(np.float32(0.01 + 0.04 * uniform(stream_key(seed, "ckvscale"), 1)[0]))  # a float32 input
+    if name == "mla_tiny":
+        L = np.array([100, 300], np.int32)
+        return MlaWorkload(name, seed, 2, 8, L, 11, _pool_tables(seed, L, 11, MLA_PAGE_SIZE), cs)
+    if name == "mla":
+        L = np.array([51200], np.int32)
+        return MlaWorkload(name, seed, 1, 8, L, 1024, _pool_tables(seed, L, 1024, MLA_PAGE_SIZE), cs)
+    L = _uniform_int(seed, "lens", 32, 4096, 16384)
+    pool = int(((L.astype(np.int64) + MLA_PAGE_SIZE - 1) // MLA_PAGE_SIZE).sum())
+    return MlaWorkload(name, seed, 32, 16, L, pool, _pool_tables(seed, L, pool, MLA_PAGE_SIZE), cs)
+
+
+MLA_WORKLOADS = ("mla_tiny", "mla", "mla_batch")
+
+
+def custom_mla_workload(name: str, seed: int, seq_lens, H: int, style: str = "interleaved",
+                        num_pages: Optional[int] = None, rope_base: float = 1e4,
+                        ckv_scale: Optional[float] = None) -> MlaWorkload:
+    """A small MLA workload of any batch and head count (edge cases)."""
+    L = np.asarray(seq_lens, np.int32)
+    need = int(((L.astype(np.int64) + MLA_PAGE_SIZE - 1) // MLA_PAGE_SIZE).sum())
+    pool = max(need, 1) if num_pages is None else num_pages
+    cs = float(np.float32(0.01 + 0.04 * uniform(stream_key(seed, "ckvscale"), 1)[0]) if ckv_scale is None
+               else np.float32(ckv_scale))
+    return MlaWorkload(name, seed, len(L), H, L, pool, _pool_tables(seed, L, pool, MLA_PAGE_SIZE), cs,
+                       rope_base=rope_base, style=style)

@@ -105,3 +105,50 @@ def nvfp4_values_f64(cache: np.ndarray, block_scale: np.ndarray) -> np.ndarray:
     vals = np.stack([lo, hi], axis=-1).reshape(cache.shape[:-1] + (2 * cache.shape[-1],))
     s = torch.from_numpy(np.ascontiguousarray(block_scale)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
     return vals * np.repeat(s, 16, axis=-1)
+
+
+def mla_oracle_step(w: synth.MlaWorkload, seqs=None, num_splits: int = 1):
+    """The oracle's MLA cache write (context, then the new token with q_pe)
+    and decode + merge for the given sequences, on a compact pool.
+
+    Returns dict(q_lat, q_pe_rot [n,H,*] uint16, ckv_cache [pool,P,Dc] uint8,
+    kpe_cache [pool,P,Dr] uint16, block_tables, seq_lens, out_partial,
+    lse_partial, out, lse)."""
+    seqs = list(range(w.B)) if seqs is None else list(seqs)
+    n = len(seqs)
+    P = w.page_size
+    npg = [int((int(w.seq_lens[b]) + P - 1) // P) for b in seqs]
+    width = max(1, max(npg) if npg else 1)
+    bt = np.full((n, width), -1, np.int32)
+    base = 0
+    for i, c in enumerate(npg):
+        bt[i, :c] = np.arange(base, base + c, dtype=np.int32)
+        base += c
+    pool = max(base, 1)
+    ckv_cache = np.zeros((pool, P, w.Dc), np.uint8)
+    kpe_cache = np.zeros((pool, P, w.Dr), np.uint16)
+    cs = w.cos_sin()
+    q_lat = np.zeros((n, w.H, w.Dc), np.uint16)
+    q_pe = np.zeros((n, w.H, w.Dr), np.uint16)
+    sl = np.array([int(w.seq_lens[b]) for b in seqs], np.int32)
+    for i, b in enumerate(seqs):
+        L = int(w.seq_lens[b])
+        ql, qp = w.seq_q(b)
+        q_lat[i] = ql
+        if L == 0:
+            q_pe[i] = qp
+            continue
+        ckv, kpe = w.seq_latent(b)
+        pos = np.arange(L, dtype=np.int32)
+        slots = (bt[i, pos // P].astype(np.int64) * P + pos % P).astype(np.int32)
+        if L > 1:
+            oracle.mla_cache_write(None, ckv[:L - 1], kpe[:L - 1], pos[:L - 1], cs, ckv_cache, kpe_cache,
+                                   slots[:L - 1], w.ckv_scale, w.style)
+        qpr = qp.reshape(1, w.H, w.Dr).copy()
+        oracle.mla_cache_write(qpr, ckv[L - 1:], kpe[L - 1:], pos[L - 1:], cs, ckv_cache, kpe_cache, slots[L - 1:],
+                               w.ckv_scale, w.style)
+        q_pe[i] = qpr[0]
+    op, lp = oracle.mla_decode(q_lat, q_pe, ckv_cache, kpe_cache, bt, sl, w.softmax_scale, num_splits, w.ckv_scale)
+    out, lse = oracle.lse_merge(op, lp)
+    return dict(q_lat=q_lat, q_pe_rot=q_pe, ckv_cache=ckv_cache, kpe_cache=kpe_cache, block_tables=bt,
+                seq_lens=sl, out_partial=op, lse_partial=lp, out=out, lse=lse)
