@@ -2,7 +2,9 @@
  * pkv.h -- C ABI of the paged-KV GQA decode step for NVIDIA GB300 (sm_103a).
  *
  * One decode step of transformer attention over a paged KV cache is three
- * calls on one CUDA stream:
+ * calls on one CUDA stream (for multi-head latent attention, the MLA pair
+ * pkv_mla_cache_write / pkv_paged_mla_decode takes the place of the first
+ * two):
  *
  *   pkv_rope_kv_write     rotate q and k of the new token(s) (NeoX or
  *                         interleaved RoPE) and write k and v into the paged
@@ -245,6 +247,87 @@ pkv_status pkv_paged_gqa_decode_nvfp4(const pkv_tensor* q, const pkv_tensor* k_c
                                       pkv_stream_t stream);
 
 /*
+ * pkv_mla_cache_write -- write of one or more tokens into a paged MLA
+ * latent cache (multi-head latent attention, absorbed decode form).
+ * (mainarch, MLA decode section: a paged latent cache holding FP8 E4M3 ckv
+ *  beside BF16 kpe; the cache becomes a 512-value compressed latent plus a
+ *  64-value positional part per token.)
+ *
+ * For every token t with slot_mapping[t] >= 0 (slot = page * P + offset):
+ *   ckv_cache[page, offset, d] = E4M3( f32(ckv[t, d] / ckv_scale) )
+ *       (correctly rounded quotient, saturating round-to-nearest-even, as
+ *       the FP8 KV write);
+ *   kpe_cache[page, offset, :] = bf16 RNE of RoPE(kpe[t, :]) and, when q_pe
+ *   is given, q_pe[t, h, :] = bf16 RNE of RoPE(q_pe[t, h, :]) in place:
+ *   the 64-value rotation of pkv_rope_kv_write (pairs (i, i+32) NeoX or
+ *   (2i, 2i+1) interleaved, cos_sin row positions[t], products and sums each
+ *   rounded to float32).
+ *
+ * q_pe         [T, H, 64] bf16, innermost stride 1, rows 16-byte aligned;
+ *              rotated IN PLACE; ptr may be NULL. 1 <= H <= 200.
+ * ckv          [T, 512] bf16 (the compressed latent), kpe [T, 64] bf16; read
+ *              only; innermost stride 1, rows 16-byte aligned.
+ * positions, slot_mapping  [T] int32, contiguous; slot < 0 skips the token.
+ * cos_sin      [max_pos, 64] float32, columns [0, 32) cos, [32, 64) sin.
+ * ckv_cache    [num_pages, P, 512] PKV_FP8_E4M3; kpe_cache [num_pages, P, 64]
+ *              PKV_BF16; innermost stride 1, other strides multiples of 16
+ *              bytes, bases 16-byte aligned. Any P >= 1 (the decode takes 64).
+ * ckv_scale    [1] float32, positive (static per-tensor scale).
+ * rope_style   pkv_rope_style.
+ * Errors: as pkv_rope_kv_write (PKV_FLAG_SLOT_RANGE, PKV_FLAG_POSITION_RANGE;
+ * that token is skipped, q_pe untouched).
+ */
+pkv_status pkv_mla_cache_write(const pkv_tensor* q_pe, const pkv_tensor* ckv, const pkv_tensor* kpe,
+                               const pkv_tensor* positions, const pkv_tensor* cos_sin,
+                               const pkv_tensor* ckv_cache, const pkv_tensor* kpe_cache,
+                               const pkv_tensor* slot_mapping, const pkv_tensor* ckv_scale, int32_t rope_style,
+                               int32_t* err_flag, pkv_stream_t stream);
+
+/*
+ * pkv_paged_mla_decode -- paged MLA split-K decode, absorbed form.
+ * (mainarch, MLA decode section: per-head dot scores, local softmax with
+ *  exported LSE, softmax-weighted output tiles, split-K across the sequence
+ *  with a stage-2 merge of the partial records.)
+ *
+ * Every query head h of sequence b attends to the same latent rows. For
+ * L = seq_lens[b], npages = ceil(L/64), split s covers logical pages
+ * [s*pps, min((s+1)*pps, npages)), pps = ceil(npages / num_splits):
+ *   score_t = softmax_scale * ( sum_d q_lat[b,h,d] * ckv_t[d]
+ *                             + sum_r q_pe[b,h,r]  * kpe_t[r] ),
+ *   ckv_t[d] = E4M3 value * ckv_scale,
+ *   out_partial[b,s,h,:] = sum_t exp(score_t - m) ckv_t / sum_t exp(score_t - m)
+ *   lse_partial[b,s,h]   = m + ln sum_t exp(score_t - m)
+ * (empty split: 0 and -inf). pkv_lse_merge with D = 512 merges the splits.
+ *
+ * q_lat        [B, H, 512] bf16: the query already projected into the latent
+ *              space; q_pe [B, H, 64] bf16, already rotated. Innermost stride
+ *              1, other strides even, base 4-byte aligned. 1 <= H <= 16.
+ * ckv_cache,
+ * kpe_cache    as for pkv_mla_cache_write with P = 64.
+ * block_tables [B, max_pages] int32 (64-token pages), seq_lens [B] int32.
+ * out_partial  [B, num_splits, H, 512] float32 (innermost stride 1, other
+ *              strides even, base 8-byte aligned); lse_partial
+ *              [B, num_splits, H] float32.
+ * ckv_scale    [1] float32.
+ * num_splits   >= 1, <= 4096 (see pkv_choose_num_splits_mla).
+ * Errors: as pkv_paged_gqa_decode.
+ */
+pkv_status pkv_paged_mla_decode(const pkv_tensor* q_lat, const pkv_tensor* q_pe, const pkv_tensor* ckv_cache,
+                                const pkv_tensor* kpe_cache, const pkv_tensor* block_tables,
+                                const pkv_tensor* seq_lens, float softmax_scale, int32_t num_splits,
+                                const pkv_tensor* out_partial, const pkv_tensor* lse_partial,
+                                const pkv_tensor* ckv_scale, int32_t* err_flag, pkv_stream_t stream);
+
+/*
+ * pkv_choose_num_splits_mla -- split count for pkv_paged_mla_decode (host
+ * only). B sequences, H heads, total_pages / max_pages in 64-token pages,
+ * sm_count the device's SM count. The cost model of pkv_choose_num_splits
+ * with the latent page (64 tokens x 640 bytes) and the MLA kernel's CTAs per
+ * SM. Returns a value in [1, 1024]; 1 for empty or invalid input.
+ */
+int32_t pkv_choose_num_splits_mla(int32_t B, int32_t H, int64_t total_pages, int32_t max_pages, int32_t sm_count);
+
+/*
  * pkv_lse_merge -- merge of the split partials.
  * (mainarch, decode-attention section: the combine of split-KV partials;
  *  Loom Kernels, "Attention" row: local split-K/LSE merge.)
@@ -258,7 +341,8 @@ pkv_status pkv_paged_gqa_decode_nvfp4(const pkv_tensor* q, const pkv_tensor* k_c
  * lse_partial  [B, S, Hq] float32, innermost stride 1.
  * out          [B, Hq, D] bf16, innermost stride 1.
  * lse_out      [B, Hq] float32; ptr may be NULL.
- * Supported: D in {64, 128}.
+ * Supported: D in {64, 128, 512} (512: the latent output of
+ * pkv_paged_mla_decode).
  */
 pkv_status pkv_lse_merge(const pkv_tensor* out_partial, const pkv_tensor* lse_partial, const pkv_tensor* out,
                          const pkv_tensor* lse_out, pkv_stream_t stream);
@@ -350,7 +434,7 @@ const char* pkv_status_string(int32_t status);
 
 /* ABI version of this header (bumped on any signature change). */
 int32_t pkv_abi_version(void);
-#define PKV_ABI_VERSION 2
+#define PKV_ABI_VERSION 3
 
 #ifdef __cplusplus
 }

@@ -39,7 +39,8 @@ _CACHE_DTYPE = {"bf16": 0, "fp8": 1, "nvfp4": PKV_FP4_E2M1X2}
 
 EXPORTED = ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_choose_num_splits",
             "pkv_validate_indices", "pkv_status_string", "pkv_abi_version", "pkv_stream_read",
-            "pkv_validate_indices_static", "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4")
+            "pkv_validate_indices_static", "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4",
+            "pkv_mla_cache_write", "pkv_paged_mla_decode", "pkv_choose_num_splits_mla")
 
 
 class PkvTensor(ctypes.Structure):
@@ -71,6 +72,9 @@ def lib() -> ctypes.CDLL:
         L.pkv_paged_gqa_decode.argtypes = [T, T, T, T, T, ctypes.c_float, i32, T, T, T, T, i32, P, P]
         L.pkv_rope_kv_write_nvfp4.argtypes = [T, T, T, T, T, T, T, T, T, T, T, T, i32, i32, P, P]
         L.pkv_paged_gqa_decode_nvfp4.argtypes = [T, T, T, T, T, T, T, ctypes.c_float, i32, T, T, T, T, i32, P, P]
+        L.pkv_mla_cache_write.argtypes = [T, T, T, T, T, T, T, T, T, i32, P, P]
+        L.pkv_paged_mla_decode.argtypes = [T, T, T, T, T, T, ctypes.c_float, i32, T, T, T, P, P]
+        L.pkv_choose_num_splits_mla.argtypes = [i32, i32, ctypes.c_int64, i32, i32]
         L.pkv_lse_merge.argtypes = [T, T, T, T, P]
         L.pkv_choose_num_splits.argtypes = [i32, i32, i32, i32, ctypes.c_int64, i32, i32, i32]
         L.pkv_validate_indices.argtypes = [T, T, T, ctypes.c_int64, T, P, P]
@@ -80,7 +84,8 @@ def lib() -> ctypes.CDLL:
         L.pkv_status_string.restype = ctypes.c_char_p
         for name in ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_validate_indices",
                      "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read", "pkv_validate_indices_static",
-                     "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4"):
+                     "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4", "pkv_mla_cache_write",
+                     "pkv_paged_mla_decode", "pkv_choose_num_splits_mla"):
             getattr(L, name).restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -174,6 +179,31 @@ def paged_gqa_decode_nvfp4(q, k_cache, v_cache, k_block_scale, v_block_scale, bl
         _desc(q), _fp4(k_cache), _fp4(v_cache), _desc(k_block_scale), _desc(v_block_scale), _desc(block_tables),
         _desc(seq_lens), float(softmax_scale), int(num_splits), _desc(out_partial), _desc(lse_partial),
         _desc(k_scale), _desc(v_scale), LAYOUTS[layout], _ptr(err_flag), _stream(stream)))
+
+
+def mla_cache_write(q_pe, ckv, kpe, positions, cos_sin, ckv_cache, kpe_cache, slot_mapping, ckv_scale,
+                    rope_style: str = "interleaved", err_flag=None, stream=None) -> None:
+    """pkv_mla_cache_write: ckv [T,512] bf16 -> E4M3 bytes of ckv_cache
+    [pages,P,512] (uint8 or float8_e4m3fn), RoPE(kpe [T,64]) -> kpe_cache
+    [pages,P,64] bf16, q_pe [T,H,64] (or None) rotated in place."""
+    _check("pkv_mla_cache_write", lib().pkv_mla_cache_write(
+        _desc(q_pe), _desc(ckv), _desc(kpe), _desc(positions), _desc(cos_sin), _desc(ckv_cache), _desc(kpe_cache),
+        _desc(slot_mapping), _desc(ckv_scale), STYLES[rope_style], _ptr(err_flag), _stream(stream)))
+
+
+def paged_mla_decode(q_lat, q_pe, ckv_cache, kpe_cache, block_tables, seq_lens, softmax_scale: float,
+                     num_splits: int, out_partial, lse_partial, ckv_scale, err_flag=None, stream=None) -> None:
+    """pkv_paged_mla_decode: q_lat [B,H,512], q_pe [B,H,64] over the latent
+    cache into out_partial [B,S,H,512] and lse_partial [B,S,H]."""
+    _check("pkv_paged_mla_decode", lib().pkv_paged_mla_decode(
+        _desc(q_lat), _desc(q_pe), _desc(ckv_cache), _desc(kpe_cache), _desc(block_tables), _desc(seq_lens),
+        float(softmax_scale), int(num_splits), _desc(out_partial), _desc(lse_partial), _desc(ckv_scale),
+        _ptr(err_flag), _stream(stream)))
+
+
+def choose_num_splits_mla(B: int, H: int, total_pages: int, max_pages: int, sm_count: int) -> int:
+    """Split count for the MLA decode from the library's heuristic (host only)."""
+    return int(lib().pkv_choose_num_splits_mla(B, H, int(total_pages), max_pages, sm_count))
 
 
 def lse_merge(out_partial, lse_partial, out, lse_out=None, stream=None) -> None:

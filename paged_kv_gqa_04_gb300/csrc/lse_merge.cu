@@ -17,7 +17,9 @@
 // again by their own LSE weights. The kernel is latency-bound (the partials
 // are a few MB): partial rows are loaded in batches of sixteen, the first
 // together with the LSE values and each next one while the previous batch is
-// summed.
+// summed. Rows wider than 128 columns (the 512-value latent output of MLA
+// decode) are cut into 128-column slices, each merged by its own warp (or
+// CTA) with the same LSE weights.
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
@@ -114,24 +116,35 @@ __device__ __forceinline__ void store_row(uint16_t* dst, const float (&o)[V]) {
     }
 }
 
-// Few splits (S <= 32): one warp per row, two rows per CTA.
+// Columns of a row one warp merges, and the slices a row is cut into.
+template <int D>
+struct Slice {
+    static constexpr int DW = D > 128 ? 128 : D;
+    static constexpr int N = D / DW;
+    static constexpr int V = DW / 32;  // columns per lane
+};
+
+// Few splits (S <= 32): one warp per row slice, two slices per CTA.
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs a) {
-    constexpr int V = D / 32;  // columns per lane
+    using SL = Slice<D>;
+    constexpr int V = SL::V;
     grid_dep_wait();           // the partials come from the preceding decode grid
     const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    if (row >= static_cast<int64_t>(a.B) * a.Hq) return;
+    const int64_t vrow = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    if (vrow >= static_cast<int64_t>(a.B) * a.Hq * SL::N) return;
+    const int64_t row = vrow / SL::N;
+    const int c0 = static_cast<int>(vrow % SL::N) * SL::DW + lane * V;
     const int b = static_cast<int>(row / a.Hq);
     const int h = static_cast<int>(row % a.Hq);
     float m, l, acc[V];
-    warp_merge<V, 16>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1, a.out_partial + b * a.op_s0 + h * a.op_s2 + lane * V,
+    warp_merge<V, 16>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1, a.out_partial + b * a.op_s0 + h * a.op_s2 + c0,
                       a.op_s1, 0, a.S, m, l, acc);
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] *= inv;
-    store_row<V>(a.out + b * a.o_s0 + h * a.o_s1 + lane * V, acc);
-    if (a.lse_out && lane == 0)
+    store_row<V>(a.out + b * a.o_s0 + h * a.o_s1 + c0, acc);
+    if (a.lse_out && c0 == 0)
         a.lse_out[b * a.lo_s0 + h * a.lo_s1] = (m == -INFINITY) ? -INFINITY : m + __logf(l);
 }
 
@@ -140,25 +153,28 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs 
 // W warp results are combined through shared memory by their own LSE weights.
 template <int D>
 __global__ void __launch_bounds__(512) lse_merge_tree_kernel(const MergeArgs a) {
-    constexpr int V = D / 32;
-    extern __shared__ float tree_smem[];  // W * D partial sums, then W maxima, W weight sums
+    using SL = Slice<D>;
+    constexpr int V = SL::V;
+    constexpr int DW = SL::DW;
+    extern __shared__ float tree_smem[];  // W * DW partial sums, then W maxima, W weight sums
     grid_dep_wait();
     const int W = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t row = blockIdx.x;
+    const int64_t row = blockIdx.x / SL::N;
+    const int c0 = static_cast<int>(blockIdx.x % SL::N) * DW;  // first column of this CTA's slice
     const int b = static_cast<int>(row / a.Hq);
     const int h = static_cast<int>(row % a.Hq);
     const int chunk = (a.S + W - 1) / W;
     const int s_lo = min(a.S, warp * chunk), s_hi = min(a.S, s_lo + chunk);
     float m, l, acc[V];
-    warp_merge<V, 8>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1, a.out_partial + b * a.op_s0 + h * a.op_s2 + lane * V,
-                     a.op_s1, s_lo, s_hi, m, l, acc);
+    warp_merge<V, 8>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1,
+                     a.out_partial + b * a.op_s0 + h * a.op_s2 + c0 + lane * V, a.op_s1, s_lo, s_hi, m, l, acc);
     float* sacc = tree_smem;
-    float* sm = tree_smem + W * D;
+    float* sm = tree_smem + W * DW;
     float* sl = sm + W;
 #pragma unroll
-    for (int i = 0; i < V; ++i) sacc[warp * D + lane * V + i] = acc[i];
+    for (int i = 0; i < V; ++i) sacc[warp * DW + lane * V + i] = acc[i];
     if (lane == 0) {
         sm[warp] = m;
         sl[warp] = l;
@@ -169,41 +185,46 @@ __global__ void __launch_bounds__(512) lse_merge_tree_kernel(const MergeArgs a) 
     float L = 0.f;
     for (int w = 0; w < W; ++w) L += (sm[w] == -INFINITY) ? 0.f : __expf(sm[w] - M) * sl[w];
     const float inv = (L > 0.f) ? 1.f / L : 0.f;
-    for (int d2 = threadIdx.x; d2 < D / 2; d2 += blockDim.x) {
+    for (int d2 = threadIdx.x; d2 < DW / 2; d2 += blockDim.x) {
         float o0 = 0.f, o1 = 0.f;
         for (int w = 0; w < W; ++w) {
             if (sm[w] == -INFINITY) continue;
             const float e = __expf(sm[w] - M);
-            o0 += e * sacc[w * D + 2 * d2];
-            o1 += e * sacc[w * D + 2 * d2 + 1];
+            o0 += e * sacc[w * DW + 2 * d2];
+            o1 += e * sacc[w * DW + 2 * d2 + 1];
         }
-        *reinterpret_cast<uint32_t*>(a.out + b * a.o_s0 + h * a.o_s1 + 2 * d2) = pack_bf16(o0 * inv, o1 * inv);
+        *reinterpret_cast<uint32_t*>(a.out + b * a.o_s0 + h * a.o_s1 + c0 + 2 * d2) = pack_bf16(o0 * inv, o1 * inv);
     }
-    if (a.lse_out && threadIdx.x == 0)
+    if (a.lse_out && c0 == 0 && threadIdx.x == 0)
         a.lse_out[b * a.lo_s0 + h * a.lo_s1] = (M == -INFINITY) ? -INFINITY : M + __logf(L);
+}
+
+template <int D>
+cudaError_t launch_d(const MergeArgs& a, cudaStream_t s) {
+    using SL = Slice<D>;
+    const int64_t rows = static_cast<int64_t>(a.B) * a.Hq * SL::N;  // row slices
+    if (a.S <= 32) {
+        const int64_t blocks = (rows + kWarps - 1) / kWarps;
+        if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+        return launch_dependent(lse_merge_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(kWarps * 32), 0, s, a);
+    }
+    if (rows > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    // one warp per 32 splits, 2..16 warps per row slice
+    const int W = a.S >= 16 * 32 ? 16 : (a.S + 31) / 32 < 2 ? 2 : (a.S + 31) / 32;
+    const size_t smem = static_cast<size_t>(W) * (SL::DW + 2) * sizeof(float);
+    return launch_dependent(lse_merge_tree_kernel<D>, dim3(static_cast<unsigned>(rows)), dim3(W * 32), smem, s, a);
 }
 
 }  // namespace
 
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s) {
-    const int64_t rows = static_cast<int64_t>(a.B) * a.Hq;
-    if (rows == 0) return cudaSuccess;
-    if (a.S <= 32) {
-        const int64_t blocks = (rows + kWarps - 1) / kWarps;
-        if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-        const dim3 grid(static_cast<unsigned>(blocks)), block(kWarps * 32);
-        if (a.D == 128) return launch_dependent(lse_merge_kernel<128>, grid, block, 0, s, a);
-        if (a.D == 64) return launch_dependent(lse_merge_kernel<64>, grid, block, 0, s, a);
-        return cudaErrorInvalidValue;
+    if (static_cast<int64_t>(a.B) * a.Hq == 0) return cudaSuccess;
+    switch (a.D) {
+        case 64: return launch_d<64>(a, s);
+        case 128: return launch_d<128>(a, s);
+        case 512: return launch_d<512>(a, s);
+        default: return cudaErrorInvalidValue;
     }
-    if (rows > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-    // one warp per 32 splits, 2..16 warps per row
-    const int W = a.S >= 16 * 32 ? 16 : (a.S + 31) / 32 < 2 ? 2 : (a.S + 31) / 32;
-    const size_t smem = static_cast<size_t>(W) * (a.D + 2) * sizeof(float);
-    const dim3 grid(static_cast<unsigned>(rows)), block(W * 32);
-    if (a.D == 128) return launch_dependent(lse_merge_tree_kernel<128>, grid, block, smem, s, a);
-    if (a.D == 64) return launch_dependent(lse_merge_tree_kernel<64>, grid, block, smem, s, a);
-    return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

@@ -96,6 +96,41 @@ bool make_cache_map(CUtensorMap* m, const pkv_tensor& c, int32_t layout) {
     return r == CUDA_SUCCESS;
 }
 
+// Tile map over an MLA cache [pages, P, W] (W = 512 E4M3 bytes of ckv or 64
+// bf16 values of kpe): one box = 32 token rows x 128 bytes, 128-byte swizzle.
+bool make_mla_map(CUtensorMap* m, const pkv_tensor& c) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const int e = elem_bytes(c.dtype);
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(c.shape[2]), static_cast<cuuint64_t>(c.shape[1]),
+                          static_cast<cuuint64_t>(c.shape[0])};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(c.stride[1] * e), static_cast<cuuint64_t>(c.stride[0] * e)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / e), 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                     c.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// An MLA latent cache pair: ckv [pages, P, 512] E4M3, kpe [pages, P, 64]
+// bf16; innermost stride 1, other strides multiples of 16 bytes, bases
+// 16-byte aligned.
+pkv_status check_mla_caches(const pkv_tensor& cc, const pkv_tensor& kc, int64_t* num_pages, int* P) {
+    if (!shape_ok(cc, 3, PKV_FP8_E4M3) || !shape_ok(kc, 3, PKV_BF16)) return PKV_ERR_INVALID_ARG;
+    if (cc.shape[2] != pkv::kMlaDc || kc.shape[2] != pkv::kMlaDr) return PKV_ERR_UNSUPPORTED;
+    if (cc.shape[0] != kc.shape[0] || cc.shape[1] != kc.shape[1]) return PKV_ERR_INVALID_ARG;
+    if (!cc.ptr || !kc.ptr) return PKV_ERR_INVALID_ARG;
+    *num_pages = cc.shape[0];
+    *P = static_cast<int>(cc.shape[1]);
+    if (*num_pages < 1 || *P < 1) return PKV_ERR_INVALID_ARG;
+    if (cc.stride[2] != 1 || kc.stride[2] != 1) return PKV_ERR_UNSUPPORTED;
+    if (!strides_multiple(cc, 2, 16) || !strides_multiple(kc, 2, 16)) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(cc.ptr, 16) || !aligned(kc.ptr, 16)) return PKV_ERR_UNSUPPORTED;
+    if (*num_pages > 0x7FFFFFFF / 64) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
 // Common checks of a cache pair. Returns PKV_OK and fills the dims. NVFP4
 // value caches (PKV_FP4_E2M1X2) hold D/2 bytes per row; the others D values.
 pkv_status check_caches(const pkv_tensor& kc, const pkv_tensor& vc, int32_t layout, int64_t* num_pages,
@@ -434,7 +469,7 @@ pkv_status pkv_lse_merge(const pkv_tensor* out_partial_p, const pkv_tensor* lse_
     if (lse_out.ptr && (!shape_ok(lse_out, 2, PKV_F32) || lse_out.shape[0] != B || lse_out.shape[1] != Hq))
         return PKV_ERR_INVALID_ARG;
     if (S < 1) return PKV_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128 && D != 512) return PKV_ERR_UNSUPPORTED;
     if (B * Hq == 0) return PKV_OK;
     if (!out_partial.ptr || !lse_partial.ptr || !out.ptr) return PKV_ERR_INVALID_ARG;
     if (out_partial.stride[3] != 1 || lse_partial.stride[2] != 1 || out.stride[2] != 1) return PKV_ERR_UNSUPPORTED;
@@ -461,6 +496,186 @@ pkv_status pkv_lse_merge(const pkv_tensor* out_partial_p, const pkv_tensor* lse_
     a.Hq = static_cast<int32_t>(Hq);
     a.D = static_cast<int32_t>(D);
     return cuda_status(pkv::launch_lse_merge(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_mla_cache_write(const pkv_tensor* q_pe_p, const pkv_tensor* ckv_p, const pkv_tensor* kpe_p,
+                               const pkv_tensor* positions_p, const pkv_tensor* cos_sin_p,
+                               const pkv_tensor* ckv_cache_p, const pkv_tensor* kpe_cache_p,
+                               const pkv_tensor* slot_mapping_p, const pkv_tensor* ckv_scale_p, int32_t rope_style,
+                               int32_t* err_flag, pkv_stream_t stream) {
+    const pkv_tensor& q_pe = arg(q_pe_p);
+    const pkv_tensor& ckv = arg(ckv_p);
+    const pkv_tensor& kpe = arg(kpe_p);
+    const pkv_tensor& positions = arg(positions_p);
+    const pkv_tensor& cos_sin = arg(cos_sin_p);
+    const pkv_tensor& ckv_cache = arg(ckv_cache_p);
+    const pkv_tensor& kpe_cache = arg(kpe_cache_p);
+    const pkv_tensor& slot_mapping = arg(slot_mapping_p);
+    const pkv_tensor& ckv_scale = arg(ckv_scale_p);
+    if (rope_style != PKV_ROPE_NEOX && rope_style != PKV_ROPE_INTERLEAVED) return PKV_ERR_INVALID_ARG;
+    int64_t num_pages;
+    int P;
+    pkv_status st = check_mla_caches(ckv_cache, kpe_cache, &num_pages, &P);
+    if (st != PKV_OK) return st;
+    if (!shape_ok(ckv, 2, PKV_BF16) || !shape_ok(kpe, 2, PKV_BF16)) return PKV_ERR_INVALID_ARG;
+    const int64_t T = ckv.shape[0];
+    if (ckv.shape[1] != pkv::kMlaDc || kpe.shape[0] != T || kpe.shape[1] != pkv::kMlaDr) return PKV_ERR_INVALID_ARG;
+    int H = 0;
+    if (q_pe.ptr) {
+        if (!shape_ok(q_pe, 3, PKV_BF16) || q_pe.shape[0] != T || q_pe.shape[2] != pkv::kMlaDr)
+            return PKV_ERR_INVALID_ARG;
+        if (q_pe.shape[1] < 1) return PKV_ERR_INVALID_ARG;
+        if (q_pe.shape[1] > 200) return PKV_ERR_UNSUPPORTED;  // one token's rows per CTA
+        H = static_cast<int>(q_pe.shape[1]);
+    }
+    if (!shape_ok(positions, 1, PKV_I32) || !shape_ok(slot_mapping, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;
+    if (positions.shape[0] != T || slot_mapping.shape[0] != T) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(cos_sin, 2, PKV_F32) || cos_sin.shape[1] != pkv::kMlaDr || cos_sin.shape[0] < 1)
+        return PKV_ERR_INVALID_ARG;
+    if (!ckv_scale.ptr || !shape_ok(ckv_scale, 1, PKV_F32) || ckv_scale.shape[0] != 1) return PKV_ERR_INVALID_ARG;
+    if (T == 0) return PKV_OK;
+    if (!ckv.ptr || !kpe.ptr || !positions.ptr || !slot_mapping.ptr || !cos_sin.ptr) return PKV_ERR_INVALID_ARG;
+    if (positions.stride[0] != 1 || slot_mapping.stride[0] != 1) return PKV_ERR_UNSUPPORTED;
+    if (!row16(ckv, 1) || !row16(kpe, 1) || (q_pe.ptr && !row16(q_pe, 2)) || !row16(cos_sin, 1))
+        return PKV_ERR_UNSUPPORTED;
+
+    pkv::MlaWriteArgs a{};
+    a.q_pe = static_cast<uint16_t*>(q_pe.ptr);
+    a.qp_s0 = q_pe.ptr ? q_pe.stride[0] : 0;
+    a.qp_s1 = q_pe.ptr ? q_pe.stride[1] : 0;
+    a.ckv = static_cast<const uint16_t*>(ckv.ptr);
+    a.ckv_s0 = ckv.stride[0];
+    a.kpe = static_cast<const uint16_t*>(kpe.ptr);
+    a.kpe_s0 = kpe.stride[0];
+    a.positions = static_cast<const int32_t*>(positions.ptr);
+    a.slots = static_cast<const int32_t*>(slot_mapping.ptr);
+    a.cos_sin = static_cast<const float*>(cos_sin.ptr);
+    a.cs_s0 = cos_sin.stride[0];
+    a.max_pos = cos_sin.shape[0];
+    a.ckv_cache = static_cast<uint8_t*>(ckv_cache.ptr);
+    a.cc_s0 = ckv_cache.stride[0];
+    a.cc_s1 = ckv_cache.stride[1];
+    a.kpe_cache = static_cast<uint16_t*>(kpe_cache.ptr);
+    a.kc_s0 = kpe_cache.stride[0];
+    a.kc_s1 = kpe_cache.stride[1];
+    a.num_pages = num_pages;
+    a.page_size = P;
+    a.ckv_scale = static_cast<const float*>(ckv_scale.ptr);
+    a.T = T;
+    a.H = H;
+    a.interleaved = rope_style == PKV_ROPE_INTERLEAVED;
+    a.err = err_flag;
+    return cuda_status(pkv::launch_mla_cache_write(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_mla_decode(const pkv_tensor* q_lat_p, const pkv_tensor* q_pe_p, const pkv_tensor* ckv_cache_p,
+                                const pkv_tensor* kpe_cache_p, const pkv_tensor* block_tables_p,
+                                const pkv_tensor* seq_lens_p, float softmax_scale, int32_t num_splits,
+                                const pkv_tensor* out_partial_p, const pkv_tensor* lse_partial_p,
+                                const pkv_tensor* ckv_scale_p, int32_t* err_flag, pkv_stream_t stream) {
+    const pkv_tensor& q_lat = arg(q_lat_p);
+    const pkv_tensor& q_pe = arg(q_pe_p);
+    const pkv_tensor& ckv_cache = arg(ckv_cache_p);
+    const pkv_tensor& kpe_cache = arg(kpe_cache_p);
+    const pkv_tensor& block_tables = arg(block_tables_p);
+    const pkv_tensor& seq_lens = arg(seq_lens_p);
+    const pkv_tensor& out_partial = arg(out_partial_p);
+    const pkv_tensor& lse_partial = arg(lse_partial_p);
+    const pkv_tensor& ckv_scale = arg(ckv_scale_p);
+    int64_t num_pages;
+    int P;
+    pkv_status st = check_mla_caches(ckv_cache, kpe_cache, &num_pages, &P);
+    if (st != PKV_OK) return st;
+    if (!shape_ok(q_lat, 3, PKV_BF16) || q_lat.shape[2] != pkv::kMlaDc) return PKV_ERR_INVALID_ARG;
+    const int64_t B = q_lat.shape[0];
+    const int64_t H = q_lat.shape[1];
+    if (!shape_ok(q_pe, 3, PKV_BF16) || q_pe.shape[0] != B || q_pe.shape[1] != H || q_pe.shape[2] != pkv::kMlaDr)
+        return PKV_ERR_INVALID_ARG;
+    if (H < 1 || num_splits < 1) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(block_tables, 2, PKV_I32) || block_tables.shape[0] != B) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(seq_lens, 1, PKV_I32) || seq_lens.shape[0] != B) return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(out_partial, 4, PKV_F32) || out_partial.shape[0] != B || out_partial.shape[1] != num_splits ||
+        out_partial.shape[2] != H || out_partial.shape[3] != pkv::kMlaDc)
+        return PKV_ERR_INVALID_ARG;
+    if (!shape_ok(lse_partial, 3, PKV_F32) || lse_partial.shape[0] != B || lse_partial.shape[1] != num_splits ||
+        lse_partial.shape[2] != H)
+        return PKV_ERR_INVALID_ARG;
+    if (!ckv_scale.ptr || !shape_ok(ckv_scale, 1, PKV_F32) || ckv_scale.shape[0] != 1) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARG;
+    if (P != pkv::kMlaPage) return PKV_ERR_UNSUPPORTED;
+    if (H > 16) return PKV_ERR_UNSUPPORTED;
+    if (num_splits > 4096 || B > 65535) return PKV_ERR_UNSUPPORTED;
+    if (B == 0) return PKV_OK;
+    if (!q_lat.ptr || !q_pe.ptr || !block_tables.ptr || !seq_lens.ptr || !out_partial.ptr || !lse_partial.ptr)
+        return PKV_ERR_INVALID_ARG;
+    const int64_t max_pages = block_tables.shape[1];
+    if (max_pages < 1) return PKV_ERR_INVALID_ARG;
+    if (max_pages > (int64_t{1} << 24)) return PKV_ERR_UNSUPPORTED;
+    for (const pkv_tensor* q : {&q_lat, &q_pe})
+        if (q->stride[2] != 1 || !aligned(q->ptr, 4) || (q->stride[0] % 2) || (q->stride[1] % 2))
+            return PKV_ERR_UNSUPPORTED;
+    if (block_tables.stride[1] != 1 || seq_lens.stride[0] != 1) return PKV_ERR_UNSUPPORTED;
+    if (out_partial.stride[3] != 1 || lse_partial.stride[2] != 1) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(out_partial.ptr, 8) || (out_partial.stride[0] % 2) || (out_partial.stride[1] % 2) ||
+        (out_partial.stride[2] % 2))
+        return PKV_ERR_UNSUPPORTED;
+
+    CUtensorMap tckv, tkpe;
+    if (!make_mla_map(&tckv, ckv_cache) || !make_mla_map(&tkpe, kpe_cache)) return PKV_ERR_CUDA;
+
+    pkv::MlaDecodeArgs a{};
+    a.q_lat = static_cast<const uint16_t*>(q_lat.ptr);
+    a.ql_s0 = q_lat.stride[0];
+    a.ql_s1 = q_lat.stride[1];
+    a.q_pe = static_cast<const uint16_t*>(q_pe.ptr);
+    a.qp_s0 = q_pe.stride[0];
+    a.qp_s1 = q_pe.stride[1];
+    a.block_tables = static_cast<const int32_t*>(block_tables.ptr);
+    a.bt_s0 = block_tables.stride[0];
+    a.max_pages = static_cast<int32_t>(max_pages);
+    a.seq_lens = static_cast<const int32_t*>(seq_lens.ptr);
+    a.num_pages = num_pages;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.ckv_scale = static_cast<const float*>(ckv_scale.ptr);
+    a.num_splits = num_splits;
+    a.out_partial = static_cast<float*>(out_partial.ptr);
+    a.op_s0 = out_partial.stride[0];
+    a.op_s1 = out_partial.stride[1];
+    a.op_s2 = out_partial.stride[2];
+    a.lse_partial = static_cast<float*>(lse_partial.ptr);
+    a.lp_s0 = lse_partial.stride[0];
+    a.lp_s1 = lse_partial.stride[1];
+    a.B = static_cast<int32_t>(B);
+    a.H = static_cast<int32_t>(H);
+    a.err = err_flag;
+    return cuda_status(pkv::launch_mla_decode(a, tckv, tkpe, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t pkv_choose_num_splits_mla(int32_t B, int32_t H, int64_t total_pages, int32_t max_pages, int32_t sm_count) {
+    if (B <= 0 || H <= 0 || total_pages <= 0 || max_pages <= 0 || sm_count <= 0) return 1;
+    const double page_bytes = static_cast<double>(pkv::kMlaPage) * (pkv::kMlaDc + 2 * pkv::kMlaDr);
+    const double slots = static_cast<double>(sm_count) * pkv::mla_decode_ctas_per_sm(H);
+    const double c0 = 32768.0 / page_bytes;     // per-CTA start-up, in pages
+    const double trip = 16384.0 / page_bytes;   // one memory round trip, in pages
+    const double work = static_cast<double>(total_pages);
+    int best = 1;
+    double best_cost = 1e300;
+    for (int S = 1; S <= 1024; ++S) {
+        if (S > max_pages) break;
+        const double ncta = static_cast<double>(B) * S;
+        const double longest = std::ceil(static_cast<double>(max_pages) / S) + c0;
+        const double total = work + ncta * c0;
+        double est = std::fmax(total / slots, longest);
+        if (ncta > slots) est = std::fmax(est, std::ceil(ncta / slots) * (total / ncta));
+        const double merge_bytes = 2.0 * B * S * static_cast<double>(H) * (pkv::kMlaDc + 1) * 4.0;
+        const double rounds = S <= 32 ? std::ceil(S / 16.0) : std::ceil(std::ceil(S / 16.0) / 16.0);
+        const double cost = est + merge_bytes / (page_bytes * slots) + trip * rounds;
+        if (cost < best_cost * (1.0 - 1e-9)) {
+            best_cost = cost;
+            best = S;
+        }
+    }
+    return best;
 }
 
 int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int64_t total_pages,

@@ -77,6 +77,58 @@ struct DecodeArgs {
     int32_t* err;
 };
 
+// Multi-head latent attention (absorbed decode form): every query head
+// attends to the same latent cache rows.
+constexpr int kMlaDc = 512;        // latent (ckv) values per token, E4M3 bytes
+constexpr int kMlaDr = 64;         // positional (kpe) values per token, bf16
+constexpr int kMlaPage = 64;       // tokens per page of the latent cache
+
+struct MlaDecodeArgs {
+    const uint16_t* q_lat;     // [B, H, 512] bf16 bits
+    int64_t ql_s0, ql_s1;
+    const uint16_t* q_pe;      // [B, H, 64] bf16 bits (rotated)
+    int64_t qp_s0, qp_s1;
+    const int32_t* block_tables;
+    int64_t bt_s0;
+    int32_t max_pages;
+    const int32_t* seq_lens;
+    int64_t num_pages;
+    float scale_log2;          // softmax_scale * log2(e)
+    const float* ckv_scale;    // [1]
+    int32_t num_splits;
+    float* out_partial;        // [B, S, H, 512]
+    int64_t op_s0, op_s1, op_s2;
+    float* lse_partial;        // [B, S, H]
+    int64_t lp_s0, lp_s1;
+    int32_t B, H;
+    int32_t* err;
+};
+
+struct MlaWriteArgs {
+    uint16_t* q_pe;            // [T, H, 64] bf16 bits, rotated in place; may be null
+    int64_t qp_s0, qp_s1;
+    const uint16_t* ckv;       // [T, 512]
+    int64_t ckv_s0;
+    const uint16_t* kpe;       // [T, 64]
+    int64_t kpe_s0;
+    const int32_t* positions;
+    const int32_t* slots;
+    const float* cos_sin;      // [max_pos, 64]
+    int64_t cs_s0;
+    int64_t max_pos;
+    uint8_t* ckv_cache;        // [pages, P, 512] E4M3 bytes
+    int64_t cc_s0, cc_s1;
+    uint16_t* kpe_cache;       // [pages, P, 64] bf16 bits
+    int64_t kc_s0, kc_s1;
+    int64_t num_pages;
+    int32_t page_size;
+    const float* ckv_scale;    // [1]
+    int64_t T;
+    int32_t H;                 // 0 when q_pe is null
+    int32_t interleaved;
+    int32_t* err;
+};
+
 struct MergeArgs {
     const float* out_partial;
     int64_t op_s0, op_s1, op_s2;
@@ -128,6 +180,10 @@ cudaError_t launch_rope_kv_write(const RopeArgs& a, cudaStream_t s);
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t s);
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s);
+cudaError_t launch_mla_decode(const MlaDecodeArgs& a, const CUtensorMap& tckv, const CUtensorMap& tkpe,
+                              cudaStream_t s);
+cudaError_t launch_mla_cache_write(const MlaWriteArgs& a, cudaStream_t s);
+int mla_decode_ctas_per_sm(int H);
 cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s);
 cudaError_t static_slot_bitmap(uint32_t** ptr, int64_t* words);
 cudaError_t launch_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int ctas, cudaStream_t s);

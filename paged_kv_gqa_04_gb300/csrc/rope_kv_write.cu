@@ -369,7 +369,69 @@ cudaError_t launch_d(const RopeArgs& a, cudaStream_t s) {
     return a.interleaved ? launch_k<D, true>(a, s) : launch_k<D, false>(a, s);
 }
 
+// MLA latent-cache write (mainarch, MLA decode section: FP8 E4M3 ckv beside
+// BF16 kpe). threadIdx.x of a token: [0, 64) the 8-value chunks of ckv
+// (E4M3 of the correctly rounded quotient by the scale, as the FP8 KV
+// write); [64, 68) kpe, chunks c and 32 + c as a D = 64 RoPE row; then four
+// threads per q_pe row, rotated in place. threadIdx.y and blockIdx.x: tokens.
+template <bool INTER>
+__global__ void __launch_bounds__(1024) mla_cache_write_kernel(const MlaWriteArgs a) {
+    grid_dep_launch();
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.y + threadIdx.y;
+    if (t >= a.T) return;
+    const int x = threadIdx.x;
+    const int32_t slot = __ldg(a.slots + t);
+    const int32_t pos = __ldg(a.positions + t);
+    if (slot < 0) return;
+    if (slot >= a.num_pages * a.page_size) {
+        if (x == 0) flag_error(a.err, PKV_FLAG_SLOT_RANGE);
+        return;
+    }
+    if (pos < 0 || pos >= a.max_pos) {
+        if (x == 0) flag_error(a.err, PKV_FLAG_POSITION_RANGE);
+        return;
+    }
+    const int64_t page = slot / a.page_size;
+    const int64_t off = slot - page * a.page_size;
+    if (x < kMlaDc / 8) {  // ckv chunk x
+        const float scale = __ldg(a.ckv_scale);
+        const Chunk8 v = unpack_bf16x8(*reinterpret_cast<const uint4*>(a.ckv + t * a.ckv_s0 + 8 * x));
+        *reinterpret_cast<uint2*>(a.ckv_cache + page * a.cc_s0 + off * a.cc_s1 + 8 * x) =
+            pack_e4m3x8(v, scale, __frcp_rn(scale));
+        return;
+    }
+    const int r = x - kMlaDc / 8;  // 0..3: kpe; 4..: q_pe rows
+    const int c = r & 3;
+    const int row = r >> 2;        // 0 = kpe, 1 + h = q_pe head h
+    if (row > a.H) return;
+    const uint16_t* src = row == 0 ? a.kpe + t * a.kpe_s0 : a.q_pe + t * a.qp_s0 + (row - 1) * a.qp_s1;
+    Chunk8 lo = unpack_bf16x8(*reinterpret_cast<const uint4*>(src + 8 * c));
+    Chunk8 hi = unpack_bf16x8(*reinterpret_cast<const uint4*>(src + kMlaDr / 2 + 8 * c));
+    float cv[8], sv[8];
+    load_cos_sin<kMlaDr, INTER>(a.cos_sin + pos * a.cs_s0, c, cv, sv);
+    rotate_row<INTER>(lo, hi, cv, sv);
+    uint16_t* dst = row == 0 ? a.kpe_cache + page * a.kc_s0 + off * a.kc_s1
+                             : a.q_pe + t * a.qp_s0 + (row - 1) * a.qp_s1;
+    *reinterpret_cast<uint4*>(dst + 8 * c) = pack_bf16x8(lo);
+    *reinterpret_cast<uint4*>(dst + kMlaDr / 2 + 8 * c) = pack_bf16x8(hi);
+}
+
 }  // namespace
+
+cudaError_t launch_mla_cache_write(const MlaWriteArgs& a, cudaStream_t s) {
+    if (a.T == 0) return cudaSuccess;
+    const int per_tok = kMlaDc / 8 + 4 * (1 + a.H);  // threads of one token
+    if (per_tok > 1024) return cudaErrorInvalidConfiguration;
+    const int toks = per_tok >= 256 ? 1 : 256 / per_tok;
+    const int64_t blocks = (a.T + toks - 1) / toks;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(per_tok, toks);
+    if (a.interleaved)
+        mla_cache_write_kernel<true><<<grid, block, 0, s>>>(a);
+    else
+        mla_cache_write_kernel<false><<<grid, block, 0, s>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_rope_kv_write(const RopeArgs& a, cudaStream_t s) {
     switch (a.D) {

@@ -23,6 +23,9 @@ def _u16_to_bf16(a: np.ndarray, device) -> torch.Tensor:
 class DeviceWorkload:
     """Caches, metadata and step buffers of one workload on one GPU."""
 
+    # the step's per-token inputs a host-to-device step copies ("q" = q0)
+    H2D_KEYS = ("q", "k", "v", "positions", "slot_mapping")
+
     def __init__(self, w: synth.Workload, device: str = "cuda", num_splits: Optional[int] = None):
         self.w = w
         self.device = torch.device(device)
@@ -165,9 +168,11 @@ class StepGraph:
     The graph holds the three C-ABI launches (the cache write; the decode and
     the merge as programmatic dependents, so each starts its prologue while
     its predecessor finishes). With ``host_io`` it also holds the step's
-    input copies from pinned host buffers (q, k, v, positions, slot_mapping,
-    block_tables, seq_lens) and the copies of out and lse back to pinned host
-    buffers; otherwise it starts by restoring the unrotated q on the device.
+    input copies from pinned host buffers (the workload's H2D_KEYS --
+    q, k, v, positions, slot_mapping, or the MLA step's q_pe, q_lat, ckv,
+    kpe, positions, slot_mapping -- then block_tables and seq_lens) and the
+    copies of out and lse back to pinned host buffers; otherwise it starts by
+    restoring the unrotated q (MLA: q_pe) on the device.
     """
 
     def __init__(self, dw: DeviceWorkload, host_io: bool = False):
@@ -175,8 +180,7 @@ class StepGraph:
         d = dw.decode_inputs
         self.host = None
         if host_io:
-            self.host = {k: d[k if k != "q" else "q0"].cpu().pin_memory()
-                         for k in ("q", "k", "v", "positions", "slot_mapping")}
+            self.host = {k: d[k if k != "q" else "q0"].cpu().pin_memory() for k in dw.H2D_KEYS}
             self.host["block_tables"] = dw.block_tables.cpu().pin_memory()
             self.host["seq_lens"] = dw.seq_lens.cpu().pin_memory()
             self.out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
@@ -193,8 +197,7 @@ class StepGraph:
         if h is None:
             d["q"].copy_(d["q0"])
         else:
-            d["q"].copy_(h["q"], non_blocking=True)
-            for key in ("k", "v", "positions", "slot_mapping"):
+            for key in self.dw.H2D_KEYS:
                 d[key].copy_(h[key], non_blocking=True)
             dw.block_tables.copy_(h["block_tables"], non_blocking=True)
             dw.seq_lens.copy_(h["seq_lens"], non_blocking=True)
@@ -215,3 +218,109 @@ class StepGraph:
 
     def replay(self) -> None:
         self.graph.replay()
+
+
+class MlaDeviceWorkload:
+    """Latent caches, metadata and step buffers of one MLA workload on one
+    GPU: the MLA cache write, the paged MLA decode and the D = 512 merge,
+    through the C ABI. decode_inputs["q"] is the working copy of q_pe (rotated
+    in place by the write), "q0" the unrotated one."""
+
+    H2D_KEYS = ("q", "q_lat", "ckv", "kpe", "positions", "slot_mapping")
+    nvfp4 = False
+
+    def __init__(self, w: synth.MlaWorkload, device: str = "cuda", num_splits: Optional[int] = None):
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        self.ckv_cache = torch.zeros((w.num_pages, w.page_size, w.Dc), dtype=torch.uint8, device=dev)
+        self.kpe_cache = torch.zeros((w.num_pages, w.page_size, w.Dr), dtype=torch.bfloat16, device=dev)
+        self.cos_sin = torch.from_numpy(w.cos_sin()).to(dev)
+        self.block_tables = torch.from_numpy(w.block_tables).to(dev)
+        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+        self.ckv_scale = torch.tensor([w.ckv_scale], dtype=torch.float32, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        if num_splits is None:
+            props = torch.cuda.get_device_properties(dev)
+            num_splits = _abi.choose_num_splits_mla(w.B, w.H, int(w.pages_per_seq.sum()),
+                                                    max(1, int(w.pages_per_seq.max()) if w.B else 1),
+                                                    props.multi_processor_count)
+        self.set_splits(num_splits)
+        self.out = torch.empty((w.B, w.H, w.Dc), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+        self.decode_inputs = None
+
+    def set_splits(self, num_splits: int) -> None:
+        w = self.w
+        self.num_splits = int(num_splits)
+        self.out_partial = torch.empty((w.B, self.num_splits, w.H, w.Dc), dtype=torch.float32, device=self.device)
+        self.lse_partial = torch.empty((w.B, self.num_splits, w.H), dtype=torch.float32, device=self.device)
+
+    def fill(self, max_tokens: int = 1 << 17) -> int:
+        """Context tokens 0..L-2 of every sequence through the library's MLA
+        cache write (no q_pe), in chunks of whole sequences."""
+        w = self.w
+        written = 0
+        b = 0
+        while b < w.B:
+            seqs = []
+            n = 0
+            while b < w.B and (not seqs or n + max(0, int(w.seq_lens[b]) - 1) <= max_tokens):
+                seqs.append(b)
+                n += max(0, int(w.seq_lens[b]) - 1)
+                b += 1
+            fb = w.fill_batch(seqs)
+            if len(fb["positions"]) == 0:
+                continue
+            self.write(None, _u16_to_bf16(fb["ckv"], self.device), _u16_to_bf16(fb["kpe"], self.device),
+                       torch.from_numpy(fb["positions"]).to(self.device),
+                       torch.from_numpy(fb["slot_mapping"]).to(self.device))
+            written += len(fb["positions"])
+        return written
+
+    def fill_inputs(self, seqs=None):
+        fb = self.w.fill_batch(seqs)
+        return dict(ckv=_u16_to_bf16(fb["ckv"], self.device), kpe=_u16_to_bf16(fb["kpe"], self.device),
+                    positions=torch.from_numpy(fb["positions"]).to(self.device),
+                    slot_mapping=torch.from_numpy(fb["slot_mapping"]).to(self.device))
+
+    def caches(self) -> tuple:
+        return self.ckv_cache, self.kpe_cache
+
+    def write(self, q_pe, ckv, kpe, positions, slot_mapping, stream=None) -> None:
+        _abi.mla_cache_write(q_pe, ckv, kpe, positions, self.cos_sin, self.ckv_cache, self.kpe_cache, slot_mapping,
+                             self.ckv_scale, self.w.style, self.err, stream)
+
+    def decode(self, q_pe, stream=None) -> None:
+        self.decode_into(q_pe, self.caches(), self.out_partial, self.lse_partial, stream)
+
+    def decode_into(self, q_pe, caches: tuple, out_partial, lse_partial, stream=None) -> None:
+        w = self.w
+        _abi.paged_mla_decode(self.decode_inputs["q_lat"], q_pe, caches[0], caches[1], self.block_tables,
+                              self.seq_lens, w.softmax_scale, self.num_splits, out_partial, lse_partial,
+                              self.ckv_scale, self.err, stream)
+
+    def merge(self, stream=None) -> None:
+        _abi.lse_merge(self.out_partial, self.lse_partial, self.out, self.lse, stream)
+
+    def upload_decode(self) -> dict:
+        db = self.w.decode_batch()
+        dev = self.device
+        d = dict(q0=_u16_to_bf16(db["q_pe"], dev), q_lat=_u16_to_bf16(db["q_lat"], dev),
+                 ckv=_u16_to_bf16(db["ckv"], dev), kpe=_u16_to_bf16(db["kpe"], dev),
+                 positions=torch.from_numpy(db["positions"]).to(dev),
+                 slot_mapping=torch.from_numpy(db["slot_mapping"]).to(dev))
+        d["q"] = d["q0"].clone()
+        self.decode_inputs = d
+        return d
+
+    def step(self, stream=None) -> None:
+        """One MLA decode step: cache write of the new token (q_pe rotated in
+        place), decode, merge."""
+        d = self.decode_inputs
+        self.write(d["q"], d["ckv"], d["kpe"], d["positions"], d["slot_mapping"], stream)
+        self.decode(d["q"], stream)
+        self.merge(stream)
+
+    cache_pages_u = DeviceWorkload.cache_pages_u
+    bf16_u16 = staticmethod(DeviceWorkload.bf16_u16)

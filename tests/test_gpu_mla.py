@@ -1,0 +1,118 @@
+"""GPU parity of the MLA decode step (latent-cache write, paged MLA decode,
+D = 512 merge) against the float64 oracle, through the C ABI.
+
+Compared: rotated q_pe and every ckv / kpe cache byte bit for bit; partial
+outputs, merged output and LSE within the tolerance of tests/_compare.py.
+Cases span ragged last pages and chunks (a page is two 32-token chunks),
+empty sequences and splits, 1 to 16 heads (one and two head tiles, counts
+that are not multiples of 8), both RoPE styles, split counts past 32 (the
+merge's tree path at D = 512), and the full-size workloads on sampled
+sequences."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_gqa_04_gb300 import _abi, harness, synth
+from tests._compare import assert_close_lse, assert_close_out, bf16_u16_to_f64
+from tests._pipeline import mla_oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(name, S_list, **kw):
+    return pytest.param(name, S_list, kw, id=name)
+
+
+CASES = [
+    _case("mla_tiny", (1, 2, 5)),
+    _case("ragged_h16_neox", (1, 3), seq_lens=[1, 31, 32, 33, 63, 64, 65, 200], H=16, style="neox"),
+    _case("h1", (1, 4), seq_lens=[130, 7], H=1),
+    _case("h5_h13", (2,), seq_lens=[100, 257], H=5),
+    _case("h13", (3,), seq_lens=[100, 257], H=13),
+    _case("empty_and_short", (4,), seq_lens=[0, 1, 2, 33], H=8),
+    _case("many_splits_tree_merge", (40, 64), seq_lens=[4100], H=8),
+]
+
+
+def _workload(name, kw):
+    return synth.make_mla_workload("mla_tiny") if name == "mla_tiny" else synth.custom_mla_workload(name, 303, **kw)
+
+
+def _compare(w, dw, st, seqs):
+    q = dw.bf16_u16(dw.decode_inputs["q"])
+    out = bf16_u16_to_f64(dw.bf16_u16(dw.out))
+    lse = dw.lse.cpu().numpy()
+    op = dw.out_partial.cpu().numpy()
+    lp = dw.lse_partial.cpu().numpy()
+    for i, b in enumerate(seqs):
+        assert np.array_equal(q[b], st["q_pe_rot"][i]), f"q_pe bytes of sequence {b}"
+        n = int(w.pages_per_seq[b])
+        if n:
+            for gc, oc in ((dw.ckv_cache, st["ckv_cache"]), (dw.kpe_cache, st["kpe_cache"])):
+                got = dw.cache_pages_u(gc, w.block_tables[b, :n])
+                want = oc[st["block_tables"][i, :n]]
+                # only the rows the sequence wrote are defined (a page's tail past L is not)
+                L = int(w.seq_lens[b])
+                got = got.reshape(n * w.page_size, -1)[:L]
+                want = want.reshape(n * w.page_size, -1)[:L]
+                assert np.array_equal(got, want), f"cache bytes of sequence {b}"
+        assert_close_out(op[b], st["out_partial"][i], f"out_partial[{b}]")
+        assert_close_lse(lp[b], st["lse_partial"][i], f"lse_partial[{b}]")
+        assert_close_out(out[b], st["out"][i], f"out[{b}]")
+        assert_close_lse(lse[b], st["lse"][i], f"lse[{b}]")
+    assert np.isfinite(out).all()
+    assert int(dw.err.item()) == 0
+
+
+@pytest.mark.parametrize("name,S_list,kw", CASES)
+def test_mla_step_parity(name, S_list, kw):
+    w = _workload(name, kw)
+    dw = harness.MlaDeviceWorkload(w, num_splits=S_list[0])
+    dw.fill()
+    dw.upload_decode()
+    for S in S_list:
+        dw.set_splits(S)
+        dw.decode_inputs["q"].copy_(dw.decode_inputs["q0"])
+        dw.err.zero_()
+        dw.step()
+        torch.cuda.synchronize()
+        _compare(w, dw, mla_oracle_step(w, num_splits=S), list(range(w.B)))
+
+
+@pytest.mark.parametrize("name", ["mla", "mla_batch"])
+def test_mla_full_size_sampled(name):
+    w = synth.make_mla_workload(name)
+    dw = harness.MlaDeviceWorkload(w)
+    dw.fill()
+    dw.upload_decode()
+    dw.step()
+    torch.cuda.synchronize()
+    L = w.seq_lens
+    seqs = sorted({int(np.argmax(L)), int(np.argmin(L)), int(w.B // 2)})
+    _compare(w, dw, mla_oracle_step(w, seqs=seqs, num_splits=dw.num_splits), seqs)
+
+
+def test_mla_bad_page_and_seq_len_are_flagged():
+    w = synth.custom_mla_workload("bad", 17, [200, 100], 8, num_pages=8)
+    dw = harness.MlaDeviceWorkload(w, num_splits=2)
+    dw.fill()
+    dw.upload_decode()
+    dw.step()
+    torch.cuda.synchronize()
+    assert int(dw.err.item()) == 0
+    bt = dw.block_tables.clone()
+    bt[0, 1] = w.num_pages + 3           # a page the first sequence needs
+    dw.block_tables.copy_(bt)
+    dw.err.zero_()
+    dw.decode(dw.decode_inputs["q"])
+    torch.cuda.synchronize()
+    assert int(dw.err.item()) == _abi.FLAG_PAGE_RANGE
+    dw.block_tables.copy_(torch.from_numpy(w.block_tables).cuda())
+    sl = dw.seq_lens.clone()
+    sl[1] = 64 * w.block_tables.shape[1] + 1
+    dw.seq_lens.copy_(sl)
+    dw.err.zero_()
+    dw.decode(dw.decode_inputs["q"])
+    torch.cuda.synchronize()
+    assert int(dw.err.item()) & _abi.FLAG_SEQ_LEN_RANGE
+    assert torch.isfinite(dw.out_partial).all()
