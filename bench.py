@@ -65,6 +65,9 @@ WORKLOAD_TEXT = {
                "65536-page shuffled pool",
     "fp4": "NVFP4 paged cache decode (E2M1 values + E4M3 scale per 16 + per-head static scale ~U[0.5,1.5]): "
            "B64, seq_lens ~U[2048,16384], 12 q / 2 kv heads, D128, HND",
+    "mla": "paged MLA decode (absorbed form; latent 512 E4M3 + positional 64 bf16 per token, 64-token pages): "
+           "B1, seq_len 51200 (800 pages), 8 heads -- mainarch's MLA run",
+    "mla_batch": "paged MLA decode (absorbed form, 64-token pages): B32, seq_lens ~U[4096,16384], 16 heads",
 }
 
 
@@ -76,7 +79,7 @@ def parse_args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="qwen", choices=sorted(WORKLOAD_TEXT))
     p.add_argument("--splits", type=int, default=0, help="num_splits (0 = the library's heuristic)")
-    p.add_argument("--also", default="longctx,ragged,fp8,million,fp4",
+    p.add_argument("--also", default="longctx,ragged,fp8,million,fp4,mla,mla_batch",
                    help="extra workloads whose decode roofline is reported under 'other_workloads' ('' = none)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -175,15 +178,27 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_kernel_source_hash() -> str:
-    src = open(os.path.join(ROOT, "paged_kv_gqa_04_gb300", "csrc", "paged_decode.cu"), "rb").read()
+def is_mla(name: str) -> bool:
+    return name.startswith("mla")
+
+
+def kernel_names(name: str) -> tuple:
+    """(cache write, decode, merge) entry points of a workload's step."""
+    if is_mla(name):
+        return "mla_cache_write", "paged_mla_decode", "lse_merge"
+    return "rope_kv_write", "paged_gqa_decode", "lse_merge"
+
+
+def decode_kernel_source_hash(name: str = "qwen") -> str:
+    f = "mla_decode.cu" if is_mla(name) else "paged_decode.cu"
+    src = open(os.path.join(ROOT, "paged_kv_gqa_04_gb300", "csrc", f), "rb").read()
     return hashlib.sha256(src).hexdigest()[:16]
 
 
 def ncu_traffic(workload: str):
     """DRAM bytes per decode launch from the committed ncu summary of this
     workload, if it was taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", f"paged_gqa_decode_{workload}.md")
+    p = os.path.join(ROOT, "profiles", f"{kernel_names(workload)[1]}_{workload}.md")
     try:
         txt = open(p).read()
     except OSError:
@@ -197,13 +212,19 @@ def ncu_traffic(workload: str):
                 t = float(line.split(":", 1)[1].strip())
             except ValueError:
                 t = None
-    return t if (h == decode_kernel_source_hash() and t) else None
+    return t if (h == decode_kernel_source_hash(workload) and t) else None
 
 
 # ---- byte counts ---------------------------------------------------------------------
 def decode_alg_bytes(w) -> float:
     """Q + K/V pages of every sequence (values and any block scales) +
-    block-table entries read + bf16 out."""
+    block-table entries read + bf16 out. MLA: q_lat + q_pe, the latent rows
+    (512 E4M3 + 64 bf16 per token), block-table entries, the 512-wide out."""
+    if hasattr(w, "Dc"):
+        q = w.B * w.H * (w.Dc + w.Dr) * 2
+        kv = float(w.seq_lens.astype(np.int64).sum()) * (w.Dc + 2 * w.Dr)
+        bt = float(w.pages_per_seq.sum()) * 4
+        return q + kv + bt + w.B * w.H * w.Dc * 2
     e = w.cache_bytes_per_value
     q = w.B * w.Hq * w.D * 2
     kv = float(w.seq_lens.astype(np.int64).sum()) * w.Hkv * w.D * 2 * e
@@ -213,6 +234,8 @@ def decode_alg_bytes(w) -> float:
 
 
 def partial_bytes(w, S) -> float:
+    if hasattr(w, "Dc"):
+        return 2.0 * w.B * S * w.H * (w.Dc + 1) * 4
     return 2.0 * w.B * S * w.Hq * (w.D + 1) * 4
 
 
@@ -220,7 +243,14 @@ def write_alg_bytes(w, T: int, with_q: bool, table_rows=None) -> float:
     """q read+write (if given) + k, v read + cache write + position and slot
     + one cos_sin row per token; with table_rows, the cos_sin rows are
     counted once per distinct position instead (rows shared by tokens at the
-    same position are read from L2, not HBM)."""
+    same position are read from L2, not HBM). MLA (no q): ckv and kpe read
+    (bf16), E4M3 ckv and bf16 kpe written, position and slot, one 64-value
+    cos_sin row."""
+    if hasattr(w, "Dc"):
+        assert not with_q
+        per = w.Dc * 2 + w.Dr * 2 + w.Dc + w.Dr * 2 + 8
+        rows = T if table_rows is None else table_rows
+        return float(T) * per + float(rows) * w.Dr * 4
     e = w.cache_bytes_per_value
     per = 2 * w.Hkv * w.D * 2 + 2 * w.Hkv * w.D * e + 8
     if with_q:
@@ -255,7 +285,7 @@ def time_steps(dw, steps: int, warmup: int, world: int, flush, per_kernel: bool)
         d["q"].copy_(d["q0"])
         e = ev[i]
         e[0].record(stream)
-        dw.write(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"])
+        dw.write_step()
         if per_kernel:
             e[1].record(stream)
         dw.decode(d["q"])
@@ -305,12 +335,12 @@ def time_fill(dw, reps: int, flush) -> dict:
     stream = torch.cuda.current_stream()
     for _ in range(2):
         flush.zero_()
-        dw.write(None, fi["k"], fi["v"], fi["positions"], fi["slot_mapping"])
+        dw.write_fill(fi)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     for a, b in ev:
         flush.zero_()
         a.record(stream)
-        dw.write(None, fi["k"], fi["v"], fi["positions"], fi["slot_mapping"])
+        dw.write_fill(fi)
         b.record(stream)
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
@@ -374,9 +404,9 @@ def measure_layered(dw, layers: int, reps: int, flush, peak: float) -> dict:
 def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -> dict:
     """Decode-kernel roofline of another workload (filled, then `reps`
     flushed launches)."""
-    from paged_kv_gqa_04_gb300 import harness, synth
-    w = synth.make_workload(name)
-    dw = harness.DeviceWorkload(w, num_splits=splits or None)
+    from paged_kv_gqa_04_gb300 import harness
+    dw = harness.make_device_workload(name, num_splits=splits or None)
+    w = dw.w
     dw.fill()
     d = dw.upload_decode()
     dw.step()
@@ -393,9 +423,9 @@ def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -
     rc = time_steps(dw, 20, 3, 1, flush, False)
     step = dict(chained_us=1e3 * statistics.mean(rc["step_ms"]),
                 tokens_per_s=w.B / (statistics.mean(rc["step_ms"]) * 1e-3),
-                separated_us={"rope_kv_write": 1e3 * statistics.mean(rs["write_ms"]),
-                              "paged_gqa_decode": 1e3 * statistics.mean(rs["decode_ms"]),
-                              "lse_merge": 1e3 * statistics.mean(rs["merge_ms"])})
+                separated_us=dict(zip(kernel_names(name), (1e3 * statistics.mean(rs["write_ms"]),
+                                                           1e3 * statistics.mean(rs["decode_ms"]),
+                                                           1e3 * statistics.mean(rs["merge_ms"])))))
     layered = measure_layered(dw, 4 if decode_alg_bytes(w) < 1e9 else 2, 5, flush, peak)
     fill = time_fill(dw, 5, flush)
     wb = write_alg_bytes(w, fill["T"], False)
@@ -418,7 +448,28 @@ def oracle_step_timer(w, seqs, num_splits):
     that runs one oracle decode step over them (new-token write with q,
     decode, merge) and returns its seconds."""
     import oracle
-    from tests._pipeline import oracle_step
+    from tests._pipeline import mla_oracle_step, oracle_step
+    if hasattr(w, "Dc"):  # MLA
+        st = mla_oracle_step(w, seqs=seqs, num_splits=num_splits)
+        db = w.decode_batch()
+        qp0 = db["q_pe"][seqs].copy()
+        ckv, kpe, pos = db["ckv"][seqs], db["kpe"][seqs], db["positions"][seqs]
+        P = w.page_size
+        bt = st["block_tables"]
+        slots = np.array([bt[i, p // P] * P + p % P if w.seq_lens[b] > 0 else -1
+                          for i, (b, p) in enumerate(zip(seqs, pos))], np.int32)
+        cs = w.cos_sin()
+
+        def run_mla() -> float:
+            qp = qp0.copy()
+            t0 = time.perf_counter()
+            oracle.mla_cache_write(qp, ckv, kpe, pos, cs, st["ckv_cache"], st["kpe_cache"], slots, w.ckv_scale,
+                                   w.style)
+            op, lp = oracle.mla_decode(st["q_lat"], qp, st["ckv_cache"], st["kpe_cache"], bt, st["seq_lens"],
+                                       w.softmax_scale, num_splits, w.ckv_scale)
+            oracle.lse_merge(op, lp)
+            return time.perf_counter() - t0
+        return run_mla
     st = oracle_step(w, seqs=seqs, num_splits=num_splits)
     db = w.decode_batch()
     q0 = db["q"][seqs].copy()
@@ -466,7 +517,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     from paged_kv_gqa_04_gb300 import synth
-    w = synth.make_workload(args.workload)
+    w = synth.make_mla_workload(args.workload) if is_mla(args.workload) else synth.make_workload(args.workload)
     S = args.splits or 1
     import oracle
     oracle.build()
@@ -507,8 +558,8 @@ def main():
     from paged_kv_gqa_04_gb300 import harness, synth
 
     peak, peak_kind = hbm_peak()
-    w = synth.make_workload(args.workload)
-    dw = harness.DeviceWorkload(w, num_splits=args.splits or None)
+    dw = harness.make_device_workload(args.workload, num_splits=args.splits or None)
+    w = dw.w
     dw.fill()
     dw.upload_decode()
     flush = flush_buffer()
@@ -561,8 +612,8 @@ def main():
                    "l2": "flushed before every timed step (512 MiB device write, outside the step's events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "step_us": {"step": 1e3 * statistics.mean(r["step_ms"]),
-                    "separated": {"rope_kv_write": 1e3 * statistics.mean(rk["write_ms"]),
-                                  "paged_gqa_decode": 1e3 * dec_ms,
+                    "separated": {kernel_names(args.workload)[0]: 1e3 * statistics.mean(rk["write_ms"]),
+                                  kernel_names(args.workload)[1]: 1e3 * dec_ms,
                                   "lse_merge": 1e3 * statistics.mean(rk["merge_ms"]),
                                   "step": 1e3 * statistics.mean(rk["step_ms"]),
                                   "note": "second K-step pass with an event between launches (no early "
@@ -575,7 +626,7 @@ def main():
                        "hbm_frac_table_rows_once": wbu / (fill["ms"] * 1e-3) / 1e9 / peak,
                        "note": "rope_kv_write_gbs counts one cos_sin row per token; hbm_frac_table_rows_once counts "
                                "each distinct position's row once"},
-        "roofline": {"kernel": "paged_gqa_decode", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": kernel_names(args.workload)[1], "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload),

@@ -209,8 +209,9 @@ cudaError_t launch_d(const MergeArgs& a, cudaStream_t s) {
         return launch_dependent(lse_merge_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(kWarps * 32), 0, s, a);
     }
     if (rows > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-    // one warp per 32 splits, 2..16 warps per row slice
-    const int W = a.S >= 16 * 32 ? 16 : (a.S + 31) / 32 < 2 ? 2 : (a.S + 31) / 32;
+    // 16 warps per row slice: each reads at most ceil(S / 16) partial rows,
+    // i.e. one or two batches of loads in sequence up to S = 256
+    const int W = 16;
     const size_t smem = static_cast<size_t>(W) * (SL::DW + 2) * sizeof(float);
     return launch_dependent(lse_merge_tree_kernel<D>, dim3(static_cast<unsigned>(rows)), dim3(W * 32), smem, s, a);
 }

@@ -20,15 +20,18 @@
 //            (mma.sync m16n8k16, the cache rows on M as in the GQA decode:
 //            E4M3 -> f16 for ckv, bf16 ldmatrix for kpe), written to shared
 //            memory;
-//   barrier  (one per chunk; it also frees the previous chunk's ring slot,
+//   barrier  (one per chunk; it also frees a consumed chunk's ring slot,
 //            which warp 0 refills);
 //   phase 2  every warp sums the four partials and runs the same online
 //            softmax (so their running max and sum agree exactly);
 //   phase 3  O_w^T[128 d x 8 h] += ckv^T[its 128 d x 32 tok] . P^T, the
 //            E4M3 bytes paired by token with prmt.
 // Each warp then writes its own 128 output columns: no cross-warp combine.
-// Up to 16 heads per CTA (two head tiles of 8); the partial-score exchange
-// is double-buffered by chunk parity.
+// The loop is software-pipelined: iteration c computes chunk c + 1's
+// partial scores (phase 1) and chunk c's softmax and output (phases 2, 3)
+// as two independent instruction streams, then meets the other warps at
+// the chunk's one barrier (the partial-score exchange is double-buffered by
+// chunk parity). Up to 16 heads per CTA (two head tiles of 8).
 //
 // Waits are bounded (about one second): a copy that never lands sets
 // PKV_FLAG_WAIT_TIMEOUT, the CTA stops at the same chunk (the barrier
@@ -175,180 +178,199 @@ __global__ void __launch_bounds__(kW * 32, 2)
 #pragma unroll
     for (int ht = 0; ht < NH; ++ht) mx[ht][0] = mx[ht][1] = -INFINITY, ls[ht][0] = ls[ht][1] = 0.f;
 
-    int bad = 0;
-    bool ok = true;
-    int c = 0;
-    int slot = 0;
-    uint32_t phase = 0u;
-    for (; c < nch; ++c) {
-        const bool landed = mbar_wait_bounded(bar0 + 8 * slot, phase, kWaitLimitNs);
+    // chunk c: ring slot c % kNSlot, barrier phase (c / kNSlot) & 1, its
+    // partial scores in parity buffer c & 1
+    auto valid_of = [&](int c) -> int {  // tokens of chunk c (0: its page id is out of range)
         const int pid = page_of(c);
-        const bool pid_ok = pid >= 0 && pid < num_pages;
-        const int valid = pid_ok ? min(kCh, ntok - c * kCh) : 0;
-        const uint32_t sb = ring0 + slot * kSlot;
+        return (pid >= 0 && pid < num_pages) ? min(kCh, ntok - c * kCh) : 0;
+    };
+
+    // ---- phase 1: partial scores of chunk c over this warp's columns -----------
+    auto phase1 = [&](int c) {
+        const uint32_t sb = ring0 + (c % kNSlot) * kSlot;
         const uint32_t ck = sb + warp * kBox;  // this warp's 128 ckv columns
         const uint32_t kp = sb + 4 * kBox;     // kpe box
         const uint32_t pw = part0 + (c & 1) * (kW * 2 * NH * 512);
-
-        // ---- phase 1: partial scores over this warp's columns ----------------
-        if (valid > 0) {
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                float sc[NH][4];
+        for (int mt = 0; mt < 2; ++mt) {
+            float sc[NH][4];
 #pragma unroll
-                for (int ht = 0; ht < NH; ++ht) sc[ht][0] = sc[ht][1] = sc[ht][2] = sc[ht][3] = 0.f;
-                uint32_t w[2][8];
+            for (int ht = 0; ht < NH; ++ht) sc[ht][0] = sc[ht][1] = sc[ht][2] = sc[ht][3] = 0.f;
+            uint32_t w[2][8];
 #pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int r = 16 * mt + g + 8 * hr;
-                    const uint4 x0 = lds128(ck + swz128(r, 32 * t));
-                    const uint4 x1 = lds128(ck + swz128(r, 32 * t + 16));
-                    w[hr][0] = x0.x; w[hr][1] = x0.y; w[hr][2] = x0.z; w[hr][3] = x0.w;
-                    w[hr][4] = x1.x; w[hr][5] = x1.y; w[hr][6] = x1.z; w[hr][7] = x1.w;
-                }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t a0 = e4m3x2_to_f16x2(lo16(w[0][kk])), a1 = e4m3x2_to_f16x2(lo16(w[1][kk]));
-                    const uint32_t a2 = e4m3x2_to_f16x2(hi16(w[0][kk])), a3 = e4m3x2_to_f16x2(hi16(w[1][kk]));
-#pragma unroll
-                    for (int ht = 0; ht < NH; ++ht)
-                        mma16816<true>(sc[ht], a0, a1, a2, a3, qb[ht][kk][0], qb[ht][kk][1]);
-                }
-#pragma unroll
-                for (int ht = 0; ht < NH; ++ht)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[ht][e] *= cks;  // the ckv part carries the latent scale
-                {
-                    const int r = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
-                    const int col = 2 * (16 * warp + 8 * (lane >> 4));
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kp + swz128(r, col), a0, a1, a2, a3);
-#pragma unroll
-                    for (int ht = 0; ht < NH; ++ht) mma16816<false>(sc[ht], a0, a1, a2, a3, qr[ht][0], qr[ht][1]);
-                }
-#pragma unroll
-                for (int ht = 0; ht < NH; ++ht)
-                    sts128(pw + ((warp * 2 * NH + mt * NH + ht) * 32 + lane) * 16, sc[ht][0], sc[ht][1], sc[ht][2],
-                           sc[ht][3]);
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = 16 * mt + g + 8 * hr;
+                const uint4 x0 = lds128(ck + swz128(r, 32 * t));
+                const uint4 x1 = lds128(ck + swz128(r, 32 * t + 16));
+                w[hr][0] = x0.x; w[hr][1] = x0.y; w[hr][2] = x0.z; w[hr][3] = x0.w;
+                w[hr][4] = x1.x; w[hr][5] = x1.y; w[hr][6] = x1.z; w[hr][7] = x1.w;
             }
-        }
-        // One barrier per chunk: the partials are complete, every warp is
-        // done with chunk c - 1 (its slot may be refilled), and all agree on
-        // whether the copies landed.
-        ok = __syncthreads_and(landed) != 0;
-        if (!ok) break;
-        if (!pid_ok && threadIdx.x == 0) ++bad;
-        if (warp == 0 && c >= 1 && c - 1 + kNSlot < nch) {
-            fence_proxy_async_smem();  // the CTA's reads of that slot before the copies' writes
-            issue(c - 1 + kNSlot);
-        }
-
-        if (valid > 0) {
-            // ---- phase 2: total scores, online softmax (log2 domain) ---------
-            float pr[2][NH][4];
-            float al[NH][2];
-            bool moved = false;
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t a0 = e4m3x2_to_f16x2(lo16(w[0][kk])), a1 = e4m3x2_to_f16x2(lo16(w[1][kk]));
+                const uint32_t a2 = e4m3x2_to_f16x2(hi16(w[0][kk])), a3 = e4m3x2_to_f16x2(hi16(w[1][kk]));
 #pragma unroll
-                for (int ht = 0; ht < NH; ++ht) {
-                    float4 tot = lds128f(pw + ((0 * 2 * NH + mt * NH + ht) * 32 + lane) * 16);
-#pragma unroll
-                    for (int w = 1; w < kW; ++w) {
-                        const float4 y = lds128f(pw + ((w * 2 * NH + mt * NH + ht) * 32 + lane) * 16);
-                        tot.x += y.x; tot.y += y.y; tot.z += y.z; tot.w += y.w;
-                    }
-                    const bool v0 = 16 * mt + g < valid, v1 = 16 * mt + g + 8 < valid;
-                    pr[mt][ht][0] = v0 ? tot.x * sl : -INFINITY;
-                    pr[mt][ht][1] = v0 ? tot.y * sl : -INFINITY;
-                    pr[mt][ht][2] = v1 ? tot.z * sl : -INFINITY;
-                    pr[mt][ht][3] = v1 ? tot.w * sl : -INFINITY;
-                }
+                for (int ht = 0; ht < NH; ++ht) mma16816<true>(sc[ht], a0, a1, a2, a3, qb[ht][kk][0], qb[ht][kk][1]);
+            }
 #pragma unroll
             for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float pm = fmaxf(fmaxf(pr[0][ht][e], pr[0][ht][2 + e]), fmaxf(pr[1][ht][e], pr[1][ht][2 + e]));
-                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-                    const float nm = fmaxf(mx[ht][e], pm);
-                    al[ht][e] = fast_exp2(mx[ht][e] - nm);
-                    moved |= al[ht][e] != 1.f;
-                    mx[ht][e] = nm;
-                    float sum = 0.f;
+                for (int e = 0; e < 4; ++e) sc[ht][e] *= cks;  // the ckv part carries the latent scale
+            {
+                const int r = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int col = 2 * (16 * warp + 8 * (lane >> 4));
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kp + swz128(r, col), a0, a1, a2, a3);
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        pr[mt][ht][e] = fast_exp2(pr[mt][ht][e] - nm);
-                        pr[mt][ht][2 + e] = fast_exp2(pr[mt][ht][2 + e] - nm);
-                        sum += pr[mt][ht][e] + pr[mt][ht][2 + e];
-                    }
-                    ls[ht][e] = ls[ht][e] * al[ht][e] + sum;
-                }
-            if (__any_sync(0xffffffffu, moved)) {
-#pragma unroll
-                for (int ht = 0; ht < NH; ++ht)
-#pragma unroll
-                    for (int md = 0; md < 8; ++md) {
-                        acc[ht][md][0] *= al[ht][0];
-                        acc[ht][md][1] *= al[ht][1];
-                        acc[ht][md][2] *= al[ht][0];
-                        acc[ht][md][3] *= al[ht][1];
-                    }
+                for (int ht = 0; ht < NH; ++ht) mma16816<false>(sc[ht], a0, a1, a2, a3, qr[ht][0], qr[ht][1]);
             }
+#pragma unroll
+            for (int ht = 0; ht < NH; ++ht)
+                sts128(pw + ((warp * 2 * NH + mt * NH + ht) * 32 + lane) * 16, sc[ht][0], sc[ht][1], sc[ht][2],
+                       sc[ht][3]);
+        }
+    };
 
-            // ---- phase 3: O^T += ckv^T P^T over this warp's 128 columns --------
+    // ---- phases 2 and 3 of chunk c: total scores and online softmax (every
+    // warp the same), then O^T += ckv^T P^T over this warp's 128 columns ------
+    auto phase23 = [&](int c, int valid) {
+        const uint32_t ck = ring0 + (c % kNSlot) * kSlot + warp * kBox;
+        const uint32_t pw = part0 + (c & 1) * (kW * 2 * NH * 512);
+        float pr[2][NH][4];
+        float al[NH][2];
+        bool moved = false;
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                uint32_t pb[NH][2];
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                for (int ht = 0; ht < NH; ++ht) {
-                    pb[ht][0] = movmatrix_trans(pack_f16(pr[kb][ht][0], pr[kb][ht][1]));
-                    pb[ht][1] = movmatrix_trans(pack_f16(pr[kb][ht][2], pr[kb][ht][3]));
+            for (int ht = 0; ht < NH; ++ht) {
+                float4 tot = lds128f(pw + ((0 * 2 * NH + mt * NH + ht) * 32 + lane) * 16);
+#pragma unroll
+                for (int w = 1; w < kW; ++w) {
+                    const float4 y = lds128f(pw + ((w * 2 * NH + mt * NH + ht) * 32 + lane) * 16);
+                    tot.x += y.x; tot.y += y.y; tot.z += y.z; tot.w += y.w;
                 }
-                // thread g: columns 128w + 16g .. +15 of tokens 16kb + 2t, 2t+1, 2t+8, 2t+9
-                uint32_t va[4][4];
-                const int rows[4] = {16 * kb + 2 * t, 16 * kb + 2 * t + 1, 16 * kb + 2 * t + 8, 16 * kb + 2 * t + 9};
+                const bool v0 = 16 * mt + g < valid, v1 = 16 * mt + g + 8 < valid;
+                pr[mt][ht][0] = v0 ? tot.x * sl : -INFINITY;
+                pr[mt][ht][1] = v0 ? tot.y * sl : -INFINITY;
+                pr[mt][ht][2] = v1 ? tot.z * sl : -INFINITY;
+                pr[mt][ht][3] = v1 ? tot.w * sl : -INFINITY;
+            }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 xv = lds128(ck + swz128(rows[q], 16 * g));
-                    const bool in = rows[q] < valid;  // bytes past the sequence end may be anything
-                    va[q][0] = in ? xv.x : 0u;
-                    va[q][1] = in ? xv.y : 0u;
-                    va[q][2] = in ? xv.z : 0u;
-                    va[q][3] = in ? xv.w : 0u;
+        for (int ht = 0; ht < NH; ++ht)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float pm = fmaxf(fmaxf(pr[0][ht][e], pr[0][ht][2 + e]), fmaxf(pr[1][ht][e], pr[1][ht][2 + e]));
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+                const float nm = fmaxf(mx[ht][e], pm);
+                al[ht][e] = fast_exp2(mx[ht][e] - nm);
+                moved |= al[ht][e] != 1.f;
+                mx[ht][e] = nm;
+                float sum = 0.f;
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    pr[mt][ht][e] = fast_exp2(pr[mt][ht][e] - nm);
+                    pr[mt][ht][2 + e] = fast_exp2(pr[mt][ht][2 + e] - nm);
+                    sum += pr[mt][ht][e] + pr[mt][ht][2 + e];
                 }
+                ls[ht][e] = ls[ht][e] * al[ht][e] + sum;
+            }
+        if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-                for (int wd = 0; wd < 4; ++wd) {
-                    const uint32_t pl = prmt(va[0][wd], va[1][wd], 0x5140u);
-                    const uint32_t ph = prmt(va[0][wd], va[1][wd], 0x7362u);
-                    const uint32_t ql = prmt(va[2][wd], va[3][wd], 0x5140u);
-                    const uint32_t qh = prmt(va[2][wd], va[3][wd], 0x7362u);
+            for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const uint32_t pwd = j ? ph : pl, qwd = j ? qh : ql;
-                        const uint32_t a0 = e4m3x2_to_f16x2(lo16(pwd)), a1 = e4m3x2_to_f16x2(hi16(pwd));
-                        const uint32_t a2 = e4m3x2_to_f16x2(lo16(qwd)), a3 = e4m3x2_to_f16x2(hi16(qwd));
+                for (int md = 0; md < 8; ++md) {
+                    acc[ht][md][0] *= al[ht][0];
+                    acc[ht][md][1] *= al[ht][1];
+                    acc[ht][md][2] *= al[ht][0];
+                    acc[ht][md][3] *= al[ht][1];
+                }
+        }
 #pragma unroll
-                        for (int ht = 0; ht < NH; ++ht)
-                            mma16816<true>(acc[ht][2 * wd + j], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);
-                    }
+        for (int kb = 0; kb < 2; ++kb) {
+            uint32_t pb[NH][2];
+#pragma unroll
+            for (int ht = 0; ht < NH; ++ht) {
+                pb[ht][0] = movmatrix_trans(pack_f16(pr[kb][ht][0], pr[kb][ht][1]));
+                pb[ht][1] = movmatrix_trans(pack_f16(pr[kb][ht][2], pr[kb][ht][3]));
+            }
+            // thread g: columns 128w + 16g .. +15 of tokens 16kb + 2t, 2t+1, 2t+8, 2t+9
+            uint32_t va[4][4];
+            const int rows[4] = {16 * kb + 2 * t, 16 * kb + 2 * t + 1, 16 * kb + 2 * t + 8, 16 * kb + 2 * t + 9};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 xv = lds128(ck + swz128(rows[q], 16 * g));
+                const bool in = rows[q] < valid;  // bytes past the sequence end may be anything
+                va[q][0] = in ? xv.x : 0u;
+                va[q][1] = in ? xv.y : 0u;
+                va[q][2] = in ? xv.z : 0u;
+                va[q][3] = in ? xv.w : 0u;
+            }
+#pragma unroll
+            for (int wd = 0; wd < 4; ++wd) {
+                const uint32_t pl = prmt(va[0][wd], va[1][wd], 0x5140u);
+                const uint32_t ph = prmt(va[0][wd], va[1][wd], 0x7362u);
+                const uint32_t ql = prmt(va[2][wd], va[3][wd], 0x5140u);
+                const uint32_t qh = prmt(va[2][wd], va[3][wd], 0x7362u);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t pwd = j ? ph : pl, qwd = j ? qh : ql;
+                    const uint32_t a0 = e4m3x2_to_f16x2(lo16(pwd)), a1 = e4m3x2_to_f16x2(hi16(pwd));
+                    const uint32_t a2 = e4m3x2_to_f16x2(lo16(qwd)), a3 = e4m3x2_to_f16x2(hi16(qwd));
+#pragma unroll
+                    for (int ht = 0; ht < NH; ++ht)
+                        mma16816<true>(acc[ht][2 * wd + j], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);
                 }
             }
         }
-        if (++slot == kNSlot) {
-            slot = 0;
-            phase ^= 1u;
+    };
+
+    // ---- software pipeline: chunk c + 1's partial scores are computed while
+    // chunk c's softmax and output accumulate; one barrier per chunk --------
+    int bad = 0;
+    int v_cur = valid_of(0);
+    bool landed = mbar_wait_bounded(bar0, 0u, kWaitLimitNs);
+    if (v_cur > 0) phase1(0);
+    if (v_cur == 0 && threadIdx.x == 0) ++bad;
+    bool ok = __syncthreads_and(landed) != 0;
+    int first_pending = 0;  // the oldest chunk whose copies may still be in flight
+    int c = 0;
+    if (ok) {
+        for (; c < nch; ++c) {
+            const int cn = c + 1;
+            landed = true;
+            int v_next = 0;
+            if (cn < nch) {
+                landed = mbar_wait_bounded(bar0 + 8 * (cn % kNSlot), (cn / kNSlot) & 1, kWaitLimitNs);
+                v_next = valid_of(cn);
+                if (v_next > 0) phase1(cn);
+            }
+            if (v_cur > 0) phase23(c, v_cur);
+            // the partials of chunk c + 1 are complete, every warp is done
+            // with chunk c (its slot may be refilled), and all agree on
+            // whether chunk c + 1's copies landed
+            ok = __syncthreads_and(landed) != 0;
+            if (!ok) {
+                first_pending = cn;
+                break;
+            }
+            if (cn < nch && v_next == 0 && threadIdx.x == 0) ++bad;
+            if (warp == 0 && c + kNSlot < nch) {
+                fence_proxy_async_smem();  // the CTA's reads of the slot before the copies' writes
+                issue(c + kNSlot);
+            }
+            v_cur = v_next;
         }
     }
 
     if (!ok) {
         // A copy never landed: record it, then wait (bounded) for the copies
-        // still in flight (chunks c .. c + kNSlot - 2) before exiting.
+        // still in flight before exiting.
         if (threadIdx.x == 0) flag_error(a.err, PKV_FLAG_WAIT_TIMEOUT);
         if (warp == 0) {
-            const int last = min(c + kNSlot - 1, nch);
-            for (int j = c; j < last; ++j)
+            const int last = min(c + kNSlot, nch);
+            for (int j = first_pending; j < last; ++j)
                 (void)mbar_wait_bounded(bar0 + 8 * (j % kNSlot), (j / kNSlot) & 1, kWaitLimitNs);
         }
         __syncthreads();

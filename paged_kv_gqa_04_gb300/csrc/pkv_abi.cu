@@ -668,7 +668,7 @@ int32_t pkv_choose_num_splits_mla(int32_t B, int32_t H, int64_t total_pages, int
         double est = std::fmax(total / slots, longest);
         if (ncta > slots) est = std::fmax(est, std::ceil(ncta / slots) * (total / ncta));
         const double merge_bytes = 2.0 * B * S * static_cast<double>(H) * (pkv::kMlaDc + 1) * 4.0;
-        const double rounds = S <= 32 ? std::ceil(S / 16.0) : std::ceil(std::ceil(S / 16.0) / 16.0);
+        const double rounds = S <= 32 ? std::ceil(S / 16.0) : std::ceil(std::ceil(S / 16.0) / 8.0);
         const double cost = est + merge_bytes / (page_bytes * slots) + trip * rounds;
         if (cost < best_cost * (1.0 - 1e-9)) {
             best_cost = cost;
@@ -701,9 +701,9 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
         // partial records written by the decode and read by the merge
         const double merge_bytes = 2.0 * B * S * static_cast<double>(Hq) * (D + 1) * 4.0;
         // the merge also pays about one memory round trip (~2 page times) per
-        // 16 partial rows one of its warps reads in sequence (up to 16 warps
-        // share a row beyond 32 splits)
-        const double rounds = S <= 32 ? std::ceil(S / 16.0) : std::ceil(std::ceil(S / 16.0) / 16.0);
+        // batch of partial rows one of its warps reads in sequence: 16 rows
+        // up to 32 splits, beyond that 16 warps share a row in batches of 8
+        const double rounds = S <= 32 ? std::ceil(S / 16.0) : std::ceil(std::ceil(S / 16.0) / 8.0);
         const double cost = est + merge_bytes / (page_bytes * slots) + 2.0 * rounds;
         if (cost < best_cost * (1.0 - 1e-9)) {
             best_cost = cost;

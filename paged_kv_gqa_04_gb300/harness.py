@@ -16,6 +16,14 @@ import torch
 from . import _abi, synth
 
 
+def make_device_workload(name: str, device: str = "cuda", num_splits: Optional[int] = None):
+    """The device workload of a named GQA (synth.WORKLOADS) or MLA
+    (synth.MLA_WORKLOADS) workload."""
+    if name in synth.MLA_WORKLOADS:
+        return MlaDeviceWorkload(synth.make_mla_workload(name), device, num_splits)
+    return DeviceWorkload(synth.make_workload(name), device, num_splits)
+
+
 def _u16_to_bf16(a: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
 
@@ -140,12 +148,20 @@ class DeviceWorkload:
         self.decode_inputs = d
         return d
 
+    def write_step(self, stream=None) -> None:
+        """The step's cache write: the new token of every sequence, with q."""
+        d = self.decode_inputs
+        self.write(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"], stream)
+
+    def write_fill(self, fi: dict, stream=None) -> None:
+        """A cache-fill call (no q) on inputs from fill_inputs()."""
+        self.write(None, fi["k"], fi["v"], fi["positions"], fi["slot_mapping"], stream)
+
     def step(self, stream=None) -> None:
         """One decode step on the current inputs: cache write of the new
         token (q rotated in place), decode, merge."""
-        d = self.decode_inputs
-        self.write(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"], stream)
-        self.decode(d["q"], stream)
+        self.write_step(stream)
+        self.decode(self.decode_inputs["q"], stream)
         self.merge(stream)
 
     # ---- host views -------------------------------------------------------------
@@ -314,12 +330,18 @@ class MlaDeviceWorkload:
         self.decode_inputs = d
         return d
 
+    def write_step(self, stream=None) -> None:
+        d = self.decode_inputs
+        self.write(d["q"], d["ckv"], d["kpe"], d["positions"], d["slot_mapping"], stream)
+
+    def write_fill(self, fi: dict, stream=None) -> None:
+        self.write(None, fi["ckv"], fi["kpe"], fi["positions"], fi["slot_mapping"], stream)
+
     def step(self, stream=None) -> None:
         """One MLA decode step: cache write of the new token (q_pe rotated in
         place), decode, merge."""
-        d = self.decode_inputs
-        self.write(d["q"], d["ckv"], d["kpe"], d["positions"], d["slot_mapping"], stream)
-        self.decode(d["q"], stream)
+        self.write_step(stream)
+        self.decode(self.decode_inputs["q"], stream)
         self.merge(stream)
 
     cache_pages_u = DeviceWorkload.cache_pages_u
