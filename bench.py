@@ -305,9 +305,10 @@ def time_steps(dw, steps: int, warmup: int, world: int, flush, per_kernel: bool)
 
 def time_e2e(dw, steps: int, warmup: int, world: int, flush) -> dict:
     """Through the binding with host buffers, one CUDA-graph submission per
-    step (harness.StepGraph): pinned-host -> device copies of the step's
-    inputs, the three C-ABI launches, device -> pinned-host copies of out and
-    lse; CUDA events around each replay."""
+    step (harness.StepGraph): one pinned-host -> device copy of the step's
+    packed inputs, the three C-ABI launches reading them in place, one
+    device -> pinned-host copy of the packed out and lse; CUDA events around
+    each replay."""
     from paged_kv_gqa_04_gb300 import harness
     g = harness.StepGraph(dw, host_io=True)
     stream = torch.cuda.current_stream()

@@ -183,24 +183,21 @@ class StepGraph:
 
     The graph holds the three C-ABI launches (the cache write; the decode and
     the merge as programmatic dependents, so each starts its prologue while
-    its predecessor finishes). With ``host_io`` it also holds the step's
-    input copies from pinned host buffers (the workload's H2D_KEYS --
-    q, k, v, positions, slot_mapping, or the MLA step's q_pe, q_lat, ckv,
-    kpe, positions, slot_mapping -- then block_tables and seq_lens) and the
-    copies of out and lse back to pinned host buffers; otherwise it starts by
-    restoring the unrotated q (MLA: q_pe) on the device.
+    its predecessor finishes). With ``host_io`` the step's inputs -- the
+    workload's H2D_KEYS (q, k, v, positions, slot_mapping, or the MLA step's
+    q_pe, q_lat, ckv, kpe, positions, slot_mapping), then block_tables and
+    seq_lens -- live in one packed device buffer (each tensor a 256-byte
+    aligned view the kernels read directly) filled by ONE copy from a pinned
+    host buffer of the same layout, and out and lse live in one packed device
+    buffer read back by ONE copy to pinned host memory. Without host_io the
+    graph starts by restoring the unrotated q (MLA: q_pe) on the device.
     """
 
-    def __init__(self, dw: DeviceWorkload, host_io: bool = False):
+    def __init__(self, dw, host_io: bool = False):
         self.dw = dw
-        d = dw.decode_inputs
-        self.host = None
+        self.host_io = host_io
         if host_io:
-            self.host = {k: d[k if k != "q" else "q0"].cpu().pin_memory() for k in dw.H2D_KEYS}
-            self.host["block_tables"] = dw.block_tables.cpu().pin_memory()
-            self.host["seq_lens"] = dw.seq_lens.cpu().pin_memory()
-            self.out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
-            self.lse_h = torch.empty(dw.lse.shape, dtype=dw.lse.dtype).pin_memory()
+            self._pack()
         self._body()  # run once outside the capture (first-call set-up)
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
@@ -208,29 +205,61 @@ class StepGraph:
             self._body()
         torch.cuda.synchronize()
 
+    @staticmethod
+    def _layout(tensors: dict) -> tuple:
+        offs, off = {}, 0
+        for k, t in tensors.items():
+            offs[k] = off
+            off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, off
+
+    @staticmethod
+    def _views(buf: torch.Tensor, tensors: dict, offs: dict) -> dict:
+        return {k: buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                for k, t in tensors.items()}
+
+    def _pack(self) -> None:
+        dw, d = self.dw, self.dw.decode_inputs
+        ins = {k: (d["q0"] if k == "q" else d[k]) for k in dw.H2D_KEYS}
+        ins["block_tables"] = dw.block_tables
+        ins["seq_lens"] = dw.seq_lens
+        offs, size = self._layout(ins)
+        self.dev_in = torch.zeros(size, dtype=torch.uint8, device=dw.device)
+        self.host_in = torch.zeros(size, dtype=torch.uint8).pin_memory()
+        hv = self._views(self.host_in, ins, offs)
+        for k, t in ins.items():
+            hv[k].copy_(t.cpu())
+        dv = self._views(self.dev_in, ins, offs)
+        for k in dw.H2D_KEYS:  # the step now reads its inputs from the packed buffer
+            d[k] = dv[k]
+        dw.block_tables = dv["block_tables"]
+        dw.seq_lens = dv["seq_lens"]
+        outs = {"out": dw.out, "lse": dw.lse}
+        offs, size = self._layout(outs)
+        self.dev_out = torch.zeros(size, dtype=torch.uint8, device=dw.device)
+        self.host_out = torch.zeros(size, dtype=torch.uint8).pin_memory()
+        ov = self._views(self.dev_out, outs, offs)
+        dw.out, dw.lse = ov["out"], ov["lse"]
+        hv = self._views(self.host_out, outs, offs)
+        self.out_h, self.lse_h = hv["out"], hv["lse"]
+
     def _body(self) -> None:
-        dw, d, h = self.dw, self.dw.decode_inputs, self.host
-        if h is None:
+        dw, d = self.dw, self.dw.decode_inputs
+        if not self.host_io:
             d["q"].copy_(d["q0"])
         else:
-            for key in self.dw.H2D_KEYS:
-                d[key].copy_(h[key], non_blocking=True)
-            dw.block_tables.copy_(h["block_tables"], non_blocking=True)
-            dw.seq_lens.copy_(h["seq_lens"], non_blocking=True)
+            self.dev_in.copy_(self.host_in, non_blocking=True)
         dw.step()
-        if h is not None:
-            self.out_h.copy_(dw.out, non_blocking=True)
-            self.lse_h.copy_(dw.lse, non_blocking=True)
+        if self.host_io:
+            self.host_out.copy_(self.dev_out, non_blocking=True)
 
     @property
     def h2d_bytes(self) -> int:
-        return 0 if self.host is None else sum(t.numel() * t.element_size() for t in self.host.values())
+        return self.host_in.numel() if self.host_io else 0
 
     @property
     def d2h_bytes(self) -> int:
-        if self.host is None:
-            return 0
-        return self.out_h.numel() * self.out_h.element_size() + self.lse_h.numel() * self.lse_h.element_size()
+        return self.host_out.numel() if self.host_io else 0
 
     def replay(self) -> None:
         self.graph.replay()
