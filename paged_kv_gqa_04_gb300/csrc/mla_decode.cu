@@ -44,15 +44,24 @@ namespace {
 
 constexpr int kW = 4;                   // warps per CTA
 constexpr int kCh = 32;                 // tokens per chunk
-constexpr int kNSlot = 4;               // ring slots
 constexpr int kBox = kCh * 128;         // bytes of one 32-row x 128-byte box
 constexpr int kSlot = 5 * kBox;         // four ckv boxes + one kpe box
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+#ifndef PKV_MLA_SLOTS_NH1
+#define PKV_MLA_SLOTS_NH1 4
+#endif
+#ifndef PKV_MLA_CTAS_NH1
+#define PKV_MLA_CTAS_NH1 2
+#endif
 
+// Up to 8 heads: PKV_MLA_CTAS_NH1 CTAs per SM with a PKV_MLA_SLOTS_NH1-slot
+// ring; 16 heads (twice the registers): 2 CTAs, 4 slots.
 template <int NH>
 struct MlaCfg {
+    static constexpr int NSLOT = NH == 1 ? PKV_MLA_SLOTS_NH1 : 4;  // ring slots
+    static constexpr int CTAS = NH == 1 ? PKV_MLA_CTAS_NH1 : 2;
     static constexpr int PART = 2 * kW * 2 * NH * 32 * 16;  // partial scores: [parity][warp][mt, ht][lane] float4
-    static constexpr int SMEM = kNSlot * kSlot + PART + kNSlot * 8 + 1024;
+    static constexpr int SMEM = NSLOT * kSlot + PART + NSLOT * 8 + 1024;
 };
 
 __device__ __forceinline__ uint32_t swz128(int r, int col) {
@@ -62,10 +71,11 @@ __device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16
 __device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
 
 template <int NH>
-__global__ void __launch_bounds__(kW * 32, 2)
+__global__ void __launch_bounds__(kW * 32, MlaCfg<NH>::CTAS)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tckv, const __grid_constant__ CUtensorMap tkpe,
                       const MlaDecodeArgs a) {
     using C = MlaCfg<NH>;
+    constexpr int kNSlot = C::NSLOT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t smem0 = smem_u32(smem);
@@ -413,10 +423,7 @@ cudaError_t launch_t(const MlaDecodeArgs& a, const CUtensorMap& tckv, const CUte
 
 }  // namespace
 
-int mla_decode_ctas_per_sm(int H) {
-    (void)H;
-    return 2;
-}
+int mla_decode_ctas_per_sm(int H) { return H > 8 ? MlaCfg<2>::CTAS : MlaCfg<1>::CTAS; }
 
 cudaError_t launch_mla_decode(const MlaDecodeArgs& a, const CUtensorMap& tckv, const CUtensorMap& tkpe,
                               cudaStream_t s) {

@@ -560,6 +560,9 @@ pkv_status pkv_mla_cache_write(const pkv_tensor* q_pe_p, const pkv_tensor* ckv_p
     a.kc_s1 = kpe_cache.stride[1];
     a.num_pages = num_pages;
     a.page_size = P;
+    a.page_shift = -1;
+    for (int sh = 0; sh < 31; ++sh)
+        if ((1 << sh) == P) a.page_shift = sh;
     a.ckv_scale = static_cast<const float*>(ckv_scale.ptr);
     a.T = T;
     a.H = H;

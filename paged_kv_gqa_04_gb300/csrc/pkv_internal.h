@@ -122,6 +122,7 @@ struct MlaWriteArgs {
     int64_t kc_s0, kc_s1;
     int64_t num_pages;
     int32_t page_size;
+    int32_t page_shift;        // log2(page_size) when it is a power of two, else -1
     const float* ckv_scale;    // [1]
     int64_t T;
     int32_t H;                 // 0 when q_pe is null

@@ -340,10 +340,10 @@ cudaError_t launch_t(const RopeArgs& a, cudaStream_t s) {
     if (per_tok > 1024) return cudaErrorInvalidConfiguration;
     const int toks = per_tok >= 256 ? 1 : 256 / per_tok;  // tokens per CTA row of threads
     // Two tokens per thread when there are enough tokens to keep every SM
-    // busy (cache fills of a bf16 cache); one for a decode step's few tokens
-    // and for quantised caches (measured slower for FP8: the quantiser's
-    // registers cost more occupancy than the second token's loads gain).
-    const bool two = KIND == kBf16 && a.T >= 8192 && per_tok * toks <= 512;
+    // busy (cache fills of bf16 and FP8 caches: twice the bytes in flight per
+    // thread); one for a decode step's few tokens and for NVFP4 (measured no
+    // faster there: its quantiser is bound by instruction issue).
+    const bool two = KIND != kFp4 && a.T >= 8192 && per_tok * toks <= 512;
     const int64_t per_cta = static_cast<int64_t>(toks) * (two ? 2 : 1);
     const int64_t blocks = (a.T + per_cta - 1) / per_cta;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
@@ -370,10 +370,11 @@ cudaError_t launch_d(const RopeArgs& a, cudaStream_t s) {
 }
 
 // MLA latent-cache write (mainarch, MLA decode section: FP8 E4M3 ckv beside
-// BF16 kpe). threadIdx.x of a token: [0, 64) the 8-value chunks of ckv
+// BF16 kpe). threadIdx.x of a token: [0, 32) the 16-value chunks of ckv
 // (E4M3 of the correctly rounded quotient by the scale, as the FP8 KV
-// write); [64, 68) kpe, chunks c and 32 + c as a D = 64 RoPE row; then four
-// threads per q_pe row, rotated in place. threadIdx.y and blockIdx.x: tokens.
+// write; 32-byte loads, 16-byte stores); [32, 36) kpe, chunks c and 32 + c
+// as a D = 64 RoPE row; then four threads per q_pe row, rotated in place.
+// threadIdx.y and blockIdx.x: tokens.
 template <bool INTER>
 __global__ void __launch_bounds__(1024) mla_cache_write_kernel(const MlaWriteArgs a) {
     grid_dep_launch();
@@ -391,18 +392,29 @@ __global__ void __launch_bounds__(1024) mla_cache_write_kernel(const MlaWriteArg
         if (x == 0) flag_error(a.err, PKV_FLAG_POSITION_RANGE);
         return;
     }
-    const int64_t page = slot / a.page_size;
-    const int64_t off = slot - page * a.page_size;
-    if (x < kMlaDc / 8) {  // ckv chunk x
+    int64_t page, off;
+    if (a.page_shift >= 0) {  // no division for power-of-two page sizes
+        page = slot >> a.page_shift;
+        off = slot & ((1 << a.page_shift) - 1);
+    } else {
+        page = slot / a.page_size;
+        off = slot - page * a.page_size;
+    }
+    if (x < kMlaDc / 16) {  // ckv values 16x .. 16x + 15
         const float scale = __ldg(a.ckv_scale);
-        const Chunk8 v = unpack_bf16x8(*reinterpret_cast<const uint4*>(a.ckv + t * a.ckv_s0 + 8 * x));
-        *reinterpret_cast<uint2*>(a.ckv_cache + page * a.cc_s0 + off * a.cc_s1 + 8 * x) =
-            pack_e4m3x8(v, scale, __frcp_rn(scale));
+        const float rcp = __frcp_rn(scale);
+        const uint16_t* src = a.ckv + t * a.ckv_s0 + 16 * x;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(src);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(src + 8);
+        const uint2 q0 = pack_e4m3x8(unpack_bf16x8(w0), scale, rcp);
+        const uint2 q1 = pack_e4m3x8(unpack_bf16x8(w1), scale, rcp);
+        *reinterpret_cast<uint4*>(a.ckv_cache + page * a.cc_s0 + off * a.cc_s1 + 16 * x) =
+            make_uint4(q0.x, q0.y, q1.x, q1.y);
         return;
     }
-    const int r = x - kMlaDc / 8;  // 0..3: kpe; 4..: q_pe rows
+    const int r = x - kMlaDc / 16;  // 0..3: kpe; 4..: q_pe rows
     const int c = r & 3;
-    const int row = r >> 2;        // 0 = kpe, 1 + h = q_pe head h
+    const int row = r >> 2;          // 0 = kpe, 1 + h = q_pe head h
     if (row > a.H) return;
     const uint16_t* src = row == 0 ? a.kpe + t * a.kpe_s0 : a.q_pe + t * a.qp_s0 + (row - 1) * a.qp_s1;
     Chunk8 lo = unpack_bf16x8(*reinterpret_cast<const uint4*>(src + 8 * c));
@@ -420,7 +432,7 @@ __global__ void __launch_bounds__(1024) mla_cache_write_kernel(const MlaWriteArg
 
 cudaError_t launch_mla_cache_write(const MlaWriteArgs& a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
-    const int per_tok = kMlaDc / 8 + 4 * (1 + a.H);  // threads of one token
+    const int per_tok = kMlaDc / 16 + 4 * (1 + a.H);  // threads of one token
     if (per_tok > 1024) return cudaErrorInvalidConfiguration;
     const int toks = per_tok >= 256 ? 1 : 256 / per_tok;
     const int64_t blocks = (a.T + toks - 1) / toks;
