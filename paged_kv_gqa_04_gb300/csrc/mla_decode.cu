@@ -1,5 +1,5 @@
 // mla_decode.cu -- paged multi-head latent attention (MLA) split-K decode
-// for sm_103a, absorbed form.
+// for sm_103a on the fifth-generation tensor cores (tcgen05), absorbed form.
 //
 // mainarch, MLA decode section: the cache holds one compressed latent per
 // token (ckv, 512 values, FP8 E4M3) beside a 64-value positional part (kpe,
@@ -9,84 +9,159 @@
 // softmax-weighted latent outputs (V = ckv), split-K over the sequence and a
 // stage-2 merge of the partial records (pkv_lse_merge with D = 512).
 //
-// Work decomposition. One CTA per (split, sequence); four warps. The split's
-// tokens stream through the CTA in chunks of 32 (half a 64-token page):
-// warp 0's lanes issue TMA tile loads of a chunk -- four 32-row x 128-byte
-// boxes of ckv and one 32-row x 128-byte box of kpe, 128-byte swizzle -- into
-// a 4-slot ring of 20 KB slots, each tracked by an mbarrier. Warp w owns the
-// latent columns [128w, 128w + 128) and the positional columns
-// [16w, 16w + 16):
-//   phase 1  partial scores S_w^T[32 tok x 8 h] over its columns
-//            (mma.sync m16n8k16, the cache rows on M as in the GQA decode:
-//            E4M3 -> f16 for ckv, bf16 ldmatrix for kpe), written to shared
-//            memory;
-//   barrier  (one per chunk; it also frees a consumed chunk's ring slot,
-//            which warp 0 refills);
-//   phase 2  every warp sums the four partials and runs the same online
-//            softmax (so their running max and sum agree exactly);
-//   phase 3  O_w^T[128 d x 8 h] += ckv^T[its 128 d x 32 tok] . P^T, the
-//            E4M3 bytes paired by token with prmt.
-// Each warp then writes its own 128 output columns: no cross-warp combine.
-// The loop is software-pipelined: iteration c computes chunk c + 1's
-// partial scores (phase 1) and chunk c's softmax and output (phases 2, 3)
-// as two independent instruction streams, then meets the other warps at
-// the chunk's one barrier (the partial-score exchange is double-buffered by
-// chunk parity). Up to 16 heads per CTA (two head tiles of 8).
+// The tensor cores read the E4M3 cache bytes as the copy engine lands them:
+// nothing is converted on the CUDA cores.
 //
-// Waits are bounded (about one second): a copy that never lands sets
-// PKV_FLAG_WAIT_TIMEOUT, the CTA stops at the same chunk (the barrier
-// agrees on it), waits (bounded) for its copies still in flight and exits.
+// Work decomposition. One CTA per (split, sequence), two CTAs per SM (106 KB
+// of shared memory, 256 tensor-memory columns each), six warps in three
+// roles. A split's tokens go through the CTA two pages (128 tokens, the MMA
+// M) at a time ("chunk"), one chunk in shared memory at a time; the two
+// CTAs of an SM overlap each other's waits.
+//
+//   warp 0, copies    TMA tile loads with 128-byte swizzle into the chunk
+//                     buffer: per page four 64-row x 128-byte boxes of ckv
+//                     (one per 128-value column block) and one of kpe; the
+//                     buffer holds ckv as [4 blocks][128 rows][128 B] and
+//                     kpe as [128 rows][128 B] (80 KB). The next two chunks
+//                     are prefetched into L2 (cp.async.bulk.prefetch), the
+//                     first ones before the wait on the preceding grid (a
+//                     prefetch reads through L2, which the preceding grid's
+//                     writes also go through).
+//   warp 1, MMA       the whole warp runs the issue loop; one elected lane
+//                     issues (elect.sync):
+//                       S^T[128 tok x 32]   = ckv . Q8^T    (kind::f8f6f4, E4M3 x E4M3, K = 512)
+//                       Spe^T[128 tok x 16] = kpe . q_pe^T  (kind::f16, bf16, K = 64)
+//                     then, once P is ready,
+//                       O^T[512 d x 48]    += ckv^T . P8^T  (E4M3 x E5M2, K = 128)
+//                     as four M = 128 MMAs per 32-token step: the buffer's
+//                     ckv bytes, read as an MN-major operand, are V^T.
+//                     O accumulates in tensor memory over the whole split.
+//   warps 2-5, softmax  (lane = token: warp w holds tokens 32(w%4) + 0..31)
+//                     scores from tensor memory, per-head chunk maxima
+//                     (redux.sync, a 4-warp exchange), P, its E5M2 terms to
+//                     shared memory, the running sums; the epilogue.
+//
+// Per chunk the steps are serial: copy -> S -> P -> P . V -> the buffer is
+// free for the next copy. So the next chunk's scores never overwrite S
+// before it was read, P is never rewritten before P . V read it, and O is
+// never scaled while P . V runs.
+//
+// The operands, in FP8:
+//   Q8: q_lat = 2^-k_h (t1 + t2) per head h, t1 = E4M3(2^k_h q),
+//       t2 = E4M3(2^k_h q - t1), 2^k_h the largest power of two with
+//       2^k_h max|q_h| <= 448. A bf16 value has 8 significant bits and t1 4,
+//       so the remainder fits t2 exactly: the pair is q itself unless
+//       2^k_h |q| < 2^-6 (E4M3's subnormal range, a remainder error of at
+//       most 2^-10 2^-k_h). Rows 0-15 of Q8 are the t1 of heads 0-15, rows
+//       16-31 the t2; S = 2^-k_h (S[:, h] + S[:, 16 + h]).
+//   P8: the weight P = 2^(s - m) (<= 2^8, see below) as 2^7 P rounded to
+//       f16, split into three E5M2 terms by truncation (E5M2 is the high
+//       byte of an f16): e1 = hi(x), e2 = hi(x - e1), e3 = E5M2(x - e1 - e2),
+//       both subtractions exact; the three hold about 10 significant bits
+//       (f16: 11). Rows 16t + h of P8 hold term t of head h; O is the sum of
+//       the three 16-column groups, times 2^-7.
+//
+// The online softmax keeps a reference maximum m per head that moves only
+// when a chunk's maximum exceeds it by more than 8 (so P <= 2^8 and 2^7 P
+// stays below E5M2's 57344); when it moves, the softmax warps scale O in
+// tensor memory (tcgen05.ld / st) and the running sums by 2^(m_old - m_new)
+// before handing P over. Tokens that take no part (past the sequence end,
+// or on a page whose id is out of range) get P = 0, and their ckv rows are
+// zeroed in shared memory before P . V reads them (a 0 weight times a NaN
+// byte would poison the sum).
+//
+// Every hand-off is an mbarrier (the copy engine's byte counts,
+// tcgen05.commit, warp arrivals). Tensor memory: S (48 columns) and O
+// (4 x 48 columns). Up to 16 heads; missing heads get zero queries and are
+// not written.
+//
+// Waits are bounded (about one second). A role that gives up sets
+// PKV_FLAG_WAIT_TIMEOUT and a CTA-wide abort flag that ends the other
+// roles' waits; the four softmax warps agree on stopping through their
+// barrier's AND; the copy and MMA roles wait (bounded) for their own
+// operations in flight; the CTA then frees its tensor memory and exits.
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kW = 4;                   // warps per CTA
-constexpr int kCh = 32;                 // tokens per chunk
-constexpr int kBox = kCh * 128;         // bytes of one 32-row x 128-byte box
-constexpr int kSlot = 5 * kBox;         // four ckv boxes + one kpe box
+constexpr int kT = 2 * kMlaPage;  // tokens per chunk (two pages), the MMA M
+constexpr int kN = 16;            // heads per CTA
+constexpr int kThreads = 192;
+constexpr int kCtasPerSm = 2;
+constexpr int kPrefetch = 2;      // chunks read into L2 ahead of the copy
+constexpr int kWarpCopy = 0, kWarpMma = 1, kWarpSm = 2;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-#ifndef PKV_MLA_SLOTS_NH1
-#define PKV_MLA_SLOTS_NH1 4
-#endif
-#ifndef PKV_MLA_CTAS_NH1
-#define PKV_MLA_CTAS_NH1 2
-#endif
 
-// Up to 8 heads: PKV_MLA_CTAS_NH1 CTAs per SM with a PKV_MLA_SLOTS_NH1-slot
-// ring; 16 heads (twice the registers): 2 CTAs, 4 slots.
-template <int NH>
-struct MlaCfg {
-    static constexpr int NSLOT = NH == 1 ? PKV_MLA_SLOTS_NH1 : 4;  // ring slots
-    static constexpr int CTAS = NH == 1 ? PKV_MLA_CTAS_NH1 : 2;
-    static constexpr int PART = 2 * kW * 2 * NH * 32 * 16;  // partial scores: [parity][warp][mt, ht][lane] float4
-    static constexpr int SMEM = NSLOT * kSlot + PART + NSLOT * 8 + 1024;
-};
+// shared memory, byte offsets from a 1024-byte-aligned base
+constexpr int kCkvBlock = kT * 128;               // one 128-value column block of a chunk
+constexpr int kPageRows = kMlaPage * 128;         // a page's rows in one block
+constexpr int kSlotCkv = 4 * kCkvBlock;
+constexpr int kSlotBytes = kSlotCkv + kT * 128;   // + kpe [128 rows][128 B]
+constexpr int kOffSlot = 0;
+constexpr int kOffQ = kOffSlot + kSlotBytes;         // Q8 E4M3 [4 blocks][32 rows][128 B]
+constexpr int kQBlock = 32 * 128;
+constexpr int kOffQp = kOffQ + 4 * kQBlock;           // q_pe bf16 [16 rows][128 B]
+constexpr int kOffP = kOffQp + kN * 128;              // P8 E5M2 [48 rows][128 B]
+constexpr int kPBytes = 48 * 128;
+constexpr int kRedBytes = 4 * kN * 4;                 // [4 warps][16 heads] floats
+constexpr int kOffMax = kOffP + kPBytes;              // per-warp chunk maxima
+constexpr int kOffSum = kOffMax + kRedBytes;          // per-warp sums
+constexpr int kOffQs = kOffSum + kRedBytes;           // [16] floats: ckv_scale 2^-k_h
+constexpr int kOffBar = kOffQs + kN * 4;
+enum : int { bFull = 0, bFree, bSFull, bPFull, bOFull, bQFull, kNumBars };
+constexpr int kOffMisc = kOffBar + 8 * kNumBars;      // tensor-memory base, abort flag
+constexpr int kSmem = kOffMisc + 16 + 1024;           // + alignment slack
+static_assert(kCtasPerSm * (kSmem + 1024) <= 233472, "shared memory per SM");
+static_assert(kSlotBytes % 1024 == 0 && kOffQ % 1024 == 0 && kOffQp % 1024 == 0 && kOffP % 1024 == 0 &&
+                  kPBytes % 1024 == 0,
+              "128-byte-swizzled tiles start on 1024-byte boundaries");
 
-__device__ __forceinline__ uint32_t swz128(int r, int col) {
-    return r * 128 + ((((col >> 4) & 7) ^ (r & 7)) << 4) + (col & 15);
+// tensor-memory columns
+constexpr uint32_t kTmemCols = 256;  // per CTA: two CTAs fill an SM's 512
+constexpr uint32_t kColS = 0;        // [S t1 | S t2 | Spe] (48)
+constexpr uint32_t kColO = 64;       // 4 blocks of 128 latent rows x [3 terms x 16 heads]
+constexpr float kRescaleLog2 = 8.f;  // P = 2^(s - m) <= 2^8
+constexpr float kPScale = 128.f;     // P8 holds 2^7 P
+
+constexpr uint32_t kIdescQk = umma_idesc(kT, 32, 0, 0, false, false);  // E4M3 x E4M3
+constexpr uint32_t kIdescPe = umma_idesc(kT, kN, 1, 1, false, false);  // bf16 x bf16
+constexpr uint32_t kIdescPv = umma_idesc(kT, 48, 0, 1, true, false);   // E4M3 (MN-major) x E5M2
+
+__device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return umma_desc_sw128(addr, 16, 1024); }
+
+// Wait for a phase; false after about a second or once another role has
+// given up.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
-__device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16_t>(w & 0xFFFFu); }
-__device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
 
-template <int NH>
-__global__ void __launch_bounds__(kW * 32, MlaCfg<NH>::CTAS)
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tckv, const __grid_constant__ CUtensorMap tkpe,
                       const MlaDecodeArgs a) {
-    using C = MlaCfg<NH>;
-    constexpr int kNSlot = C::NSLOT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t smem0 = smem_u32(smem);
-    const uint32_t ring0 = smem0;
-    const uint32_t part0 = smem0 + kNSlot * kSlot;
-    const uint32_t bar0 = part0 + C::PART;
+    const uint32_t s0 = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return s0 + kOffBar + 8 * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int g = lane >> 2;
-    const int t = lane & 3;
     const int s = blockIdx.x;
     const int b = blockIdx.y;
     const int H = a.H;
@@ -102,9 +177,10 @@ __global__ void __launch_bounds__(kW * 32, MlaCfg<NH>::CTAS)
     const int pps = (npages + a.num_splits - 1) / a.num_splits;
     const int p0 = s * pps;
     const int p1 = min(p0 + pps, npages);
-    const int tok0 = p0 * kMlaPage;                                 // first logical token of the split
+    const int npg = max(p1 - p0, 0);  // pages of the split
+    const int tok0 = p0 * kMlaPage;
     const int ntok = p1 > p0 ? min(L, p1 * kMlaPage) - tok0 : 0;
-    const int nch = (ntok + kCh - 1) / kCh;
+    const int nch = (ntok + kT - 1) / kT;
     float* outp = a.out_partial + b * a.op_s0 + s * a.op_s1;
     float* lsep = a.lse_partial + b * a.lp_s0 + s * a.lp_s1;
     if (nch == 0) {  // empty split: (0, -inf)
@@ -115,320 +191,432 @@ __global__ void __launch_bounds__(kW * 32, MlaCfg<NH>::CTAS)
         return;
     }
     const int32_t* bt = a.block_tables + b * a.bt_s0 + p0;
-    auto page_of = [&](int c) -> int { return __ldg(bt + (c >> 1)); };  // chunk c lies in page p0 + c/2
+    const int64_t num_pages = a.num_pages;
+    // page id of page pg of the split if it exists and is in range, else -1
+    auto page_id = [&](int pg) -> int {
+        if (pg >= npg) return -1;
+        const int pid = __ldg(bt + pg);
+        return (pid >= 0 && pid < num_pages) ? pid : -1;
+    };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNSlot; ++i) mbar_init(bar0 + 8 * i, 1);
+        mbar_init(bar(bFull), 1);
+        mbar_init(bar(bFree), 1);
+        mbar_init(bar(bSFull), 1);
+        mbar_init(bar(bPFull), 4);
+        mbar_init(bar(bOFull), 1);
+        mbar_init(bar(bQFull), 4);
+        *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tckv);
         tma_prefetch_desc(&tkpe);
     }
+    // At most two CTAs per SM (shared memory), each holding half of the
+    // tensor memory, so the allocation never waits for another CTA.
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
-    const uint64_t policy = l2_policy_evict_first();
-    const int64_t num_pages = a.num_pages;
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // Start reading the first chunks into L2 while the preceding grid may
+    // still run (a prefetch loads nothing into this CTA).
+    auto prefetch_chunk = [&](int c) {  // lanes 0-4: first page, 8-12: second
+        const int half = lane >> 3, j = lane & 7;
+        if (c < nch && half < 2 && j < 5) {
+            const int id = page_id(2 * c + half);
+            if (id >= 0) {
+                if (j < 4)
+                    tma_prefetch_3d(&tckv, 128 * j, 0, id);
+                else
+                    tma_prefetch_3d(&tkpe, 0, 0, id);
+            }
+        }
+    };
+    if (warp == kWarpCopy)
+        for (int c = 0; c <= kPrefetch; ++c) prefetch_chunk(c);
 
     // q and the cache may still be being written by the preceding grid.
     grid_dep_wait();
     grid_dep_launch();
 
-    // Start the copies of chunk c into its slot; called by warp 0 (pid uniform).
-    auto issue = [&](int c) {
-        const int slot = c % kNSlot;
-        const uint32_t bar = bar0 + 8 * slot;
-        const int pid = page_of(c);
-        if (pid < 0 || pid >= num_pages) {
-            if (lane == 0) mbar_arrive(bar);  // completes the phase with no bytes; the chunk is skipped
-            return;
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        flag_error(a.err, PKV_FLAG_WAIT_TIMEOUT);
+    };
+    // warp-uniform bounded wait; a failure stops the other roles too
+    auto warp_wait = [&](uint32_t bb, uint32_t par) -> bool {
+        const bool r = __all_sync(0xffffffffu, wait_or_abort(bb, par, abort_flag));
+        if (!r && lane == 0) give_up();
+        return r;
+    };
+
+    if (warp == kWarpCopy) {
+        // ======================= copies ===========================================
+        const uint64_t policy = l2_policy_evict_first();
+        int issued = 0;  // chunks whose copies were started
+        for (int c = 0; c < nch; ++c) {
+            if (c >= 1 && !warp_wait(bar(bFree), (c - 1) & 1)) break;  // chunk c - 1's P . V is done
+            const int pa = 2 * c, pb = 2 * c + 1;
+            const int ida = page_id(pa), idb = page_id(pb);
+            if (lane == 0 && (ida < 0 || (pb < npg && idb < 0))) flag_error(a.err, PKV_FLAG_PAGE_RANGE);
+            const uint32_t fb = bar(bFull);
+            const uint32_t bytes = (ida >= 0 ? 5 * kPageRows : 0) + (idb >= 0 ? 5 * kPageRows : 0);
+            if (lane == 0) {
+                if (bytes)
+                    mbar_arrive_expect_tx(fb, bytes);
+                else
+                    mbar_arrive(fb);  // nothing to load: the phase completes at once
+            }
+            __syncwarp();
+            const uint32_t sb = s0 + kOffSlot;
+            const int half = lane >> 3, j = lane & 7;  // lanes 0-4: first page, 8-12: second
+            const int id = half ? idb : ida;
+            if (half < 2 && id >= 0 && j < 5) {
+                if (j < 4)
+                    tma_load_3d(sb + j * kCkvBlock + half * kPageRows, &tckv, fb, 128 * j, 0, id, policy);
+                else
+                    tma_load_3d(sb + kSlotCkv + half * kPageRows, &tkpe, fb, 0, 0, id, policy);
+            }
+            if (c >= 1) prefetch_chunk(c + kPrefetch);
+            __syncwarp();
+            issued = c + 1;
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar, kSlot);
+        // The copies started land before the CTA may exit: wait (bounded)
+        // for the newest phase (at once on the normal path).
+        if (lane == 0 && issued > 0) (void)mbar_wait_bounded(bar(bFull), (issued - 1) & 1, kWaitLimitNs);
         __syncwarp();
-        const uint32_t dst = ring0 + slot * kSlot + lane * kBox;
-        const int row0 = (c & 1) * kCh;
-        if (lane < 4)
-            tma_load_3d(dst, &tckv, bar, 128 * lane, row0, pid, policy);
-        else if (lane == 4)
-            tma_load_3d(dst, &tkpe, bar, 0, row0, pid, policy);
-    };
-    if (warp == 0)
-        for (int c = 0; c < min(kNSlot, nch); ++c) issue(c);
-
-    // ---- Q^T fragments (B operands) for this warp's columns --------------------
-    // latent: k-step kk, k-rows 2t, 2t+1 (b0) / 2t+8, 2t+9 (b1) are columns
-    // 128w + 32t + 4kk (+0, +1 / +2, +3) -- the order of the thread's ckv
-    // bytes; positional: columns 16w + 2t (+8), natural order (ldmatrix).
-    uint32_t qb[NH][8][2], qr[NH][2];
+    } else if (warp == kWarpMma) {
+        // ======================= tensor-core issue ================================
+        int n_qk = 0, n_pv = 0;  // chunks whose MMAs were issued
+        auto qk = [&](int c) -> bool {
+            if (!warp_wait(bar(bFull), c & 1)) return false;
+            tc_fence_after();
+            const uint32_t sb = s0 + kOffSlot;
+            const uint32_t dS = tmem + kColS;
 #pragma unroll
-    for (int ht = 0; ht < NH; ++ht) {
-        const int h = 8 * ht + g;
-        const bool live = h < H;
-        const uint16_t* ql = a.q_lat + b * a.ql_s0 + h * a.ql_s1 + 128 * warp + 32 * t;
-        const uint16_t* qp = a.q_pe + b * a.qp_s0 + h * a.qp_s1 + 16 * warp + 2 * t;
+            for (int k = 0; k < kMlaDc / 32; ++k)
+                umma_f8_warp(dS, desc_k(sb + (k >> 2) * kCkvBlock + (k & 3) * 32),
+                             desc_k(s0 + kOffQ + (k >> 2) * kQBlock + (k & 3) * 32), kIdescQk, k > 0);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            uint32_t w0 = 0u, w1 = 0u;
-            if (live) {
-                w0 = __ldg(reinterpret_cast<const uint32_t*>(ql + 4 * kk));
-                w1 = __ldg(reinterpret_cast<const uint32_t*>(ql + 4 * kk + 2));
+            for (int k = 0; k < kMlaDr / 16; ++k)
+                umma_f16_warp(dS + 32, desc_k(sb + kSlotCkv + k * 32), desc_k(s0 + kOffQp + k * 32), kIdescPe, k > 0);
+            umma_commit_warp(bar(bSFull));
+            n_qk = c + 1;
+            return true;
+        };
+        auto pv = [&](int c) -> bool {
+            if (!warp_wait(bar(bPFull), c & 1)) return false;
+            tc_fence_after();
+            const uint32_t sb = s0 + kOffSlot;
+            const uint32_t pb = s0 + kOffP;
+#pragma unroll
+            for (int k = 0; k < kT / 32; ++k)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    umma_f8_warp(tmem + kColO + 48 * j, umma_desc_sw128(sb + j * kCkvBlock + k * 4096, kCkvBlock, 1024),
+                                 desc_k(pb + k * 32), kIdescPv, (c | k) != 0);
+            umma_commit_warp(bar(bOFull));
+            umma_commit_warp(bar(bFree));
+            n_pv = c + 1;
+            return true;
+        };
+        bool ok = warp_wait(bar(bQFull), 0);
+        for (int c = 0; c < nch && ok; ++c) ok = qk(c) && pv(c);
+        // Every commit's arrival lands before the CTA may exit: wait
+        // (bounded) for the newest phase of each barrier committed to.
+        if (lane == 0) {
+            if (n_qk > 0) (void)mbar_wait_bounded(bar(bSFull), (n_qk - 1) & 1, kWaitLimitNs);
+            if (n_pv > 0) {
+                (void)mbar_wait_bounded(bar(bOFull), (n_pv - 1) & 1, kWaitLimitNs);
+                (void)mbar_wait_bounded(bar(bFree), (n_pv - 1) & 1, kWaitLimitNs);
             }
-            qb[ht][kk][0] = pack_f16(bf16_lo(w0), bf16_hi(w0));
-            qb[ht][kk][1] = pack_f16(bf16_lo(w1), bf16_hi(w1));
         }
-        qr[ht][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qp)) : 0u;
-        qr[ht][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qp + 8)) : 0u;
+        __syncwarp();
+    } else {
+        // ======================= softmax, epilogue ================================
+        const int q = warp & 3;                    // tensor-memory lane quarter
+        const int i = threadIdx.x - kWarpSm * 32;  // 0..127
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const uint32_t qscale = s0 + kOffQs;
+        const float cks = __ldg(a.ckv_scale);
+        // ---- the queries as FP8 / bf16 B operands ----------------------------------
+        {
+            const int h = i >> 3, p = i & 7;  // head, 64-value part
+            const bool live = h < H;
+            const uint32_t* ql = reinterpret_cast<const uint32_t*>(a.q_lat + b * a.ql_s0 + h * a.ql_s1 + 64 * p);
+            float mx = 0.f;
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const uint32_t w2 = live ? __ldg(ql + k) : 0u;
+                mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w2)), fabsf(bf16_hi(w2))));
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            // 2^k with 2^k mx in (224, 448] (k = 0 for an all-zero head)
+            int k = 0;
+            if (mx > 0.f) {
+                const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
+                k = min(max(8 - e, -126), 126);
+                if (mx * __uint_as_float(static_cast<uint32_t>(k + 127) << 23) > 448.f) --k;
+            }
+            const float sc = __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+            if (p == 0) reinterpret_cast<float*>(smem + kOffQs)[h] = cks / sc;
+            // values 64p .. 64p + 63: block p / 2, 16-byte chunks 4 (p % 2) + 0..3
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t t1w[4], t2w[4];
+#pragma unroll
+                for (int m4 = 0; m4 < 4; ++m4) {
+                    uint32_t b1 = 0u, b2 = 0u;
+#pragma unroll
+                    for (int m2 = 0; m2 < 2; ++m2) {
+                        const uint32_t w2 = live ? __ldg(ql + 8 * ch + 2 * m4 + m2) : 0u;
+                        const float x0 = bf16_lo(w2) * sc, x1 = bf16_hi(w2) * sc;
+                        const uint32_t e1 = f32x2_to_e4m3x2(x1, x0);
+                        const uint32_t h1 = e4m3x2_to_f16x2(static_cast<uint16_t>(e1));
+                        const uint32_t e2 = f32x2_to_e4m3x2(x1 - f16_hi(h1), x0 - f16_lo(h1));
+                        b1 |= e1 << (16 * m2);
+                        b2 |= e2 << (16 * m2);
+                    }
+                    t1w[m4] = b1;
+                    t2w[m4] = b2;
+                }
+                const int blk = p >> 1, chunk = 4 * (p & 1) + ch;
+                sts128u(s0 + kOffQ + blk * kQBlock + h * 128 + ((chunk ^ (h & 7)) << 4), t1w[0], t1w[1], t1w[2],
+                        t1w[3]);
+                sts128u(s0 + kOffQ + blk * kQBlock + (16 + h) * 128 + ((chunk ^ ((16 + h) & 7)) << 4), t2w[0],
+                        t2w[1], t2w[2], t2w[3]);
+            }
+            const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q_pe + b * a.qp_s0 + h * a.qp_s1 + 8 * p);
+            uint32_t v[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) v[m] = live ? __ldg(qp + m) : 0u;
+            sts128u(s0 + kOffQp + h * 128 + ((p ^ (h & 7)) << 4), v[0], v[1], v[2], v[3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bQFull));
+        }
+        named_bar_and(1, 128, true);  // the q scales
+        float qs[kN];
+#pragma unroll
+        for (int h4 = 0; h4 < kN / 4; ++h4) {
+            const float4 y = lds128f(qscale + 16 * h4);
+            qs[4 * h4] = y.x;
+            qs[4 * h4 + 1] = y.y;
+            qs[4 * h4 + 2] = y.z;
+            qs[4 * h4 + 3] = y.w;
+        }
+        const float sl = a.scale_log2;
+        float m[kN], l[kN];  // reference maximum (log2 units), this thread's part of the sum
+#pragma unroll
+        for (int h = 0; h < kN; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+        }
+
+        const int tok = 32 * q + lane;  // token of the chunk = tensor-memory lane
+        // The four warps pass the same named barriers and decide whether to
+        // go on by the barrier's AND (a failed wait is carried into the next
+        // one), so all of them stop at the same chunk.
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+            const bool got = warp_wait(bar(bSFull), c & 1);
+            const bool live = page_id(2 * c + (tok >> 6)) >= 0 && tok < ntok - kT * c;
+            float sv[kN], cm[kN];
+            const uint32_t red = s0 + kOffMax;
+            if (got) {
+                tc_fence_after();
+                uint32_t r1[16], r2[16], rp[16];
+                const uint32_t ta = tmem + lane_base + kColS;
+                tmem_ld16(ta, r1);
+                tmem_ld16(ta + 16, r2);
+                tmem_ld16(ta + 32, rp);
+                tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < kN; ++h) {
+                    const float lat = __uint_as_float(r1[h]) + __uint_as_float(r2[h]);
+                    sv[h] = live ? fmaf(lat, qs[h], __uint_as_float(rp[h])) * sl : -INFINITY;
+                    cm[h] = sv[h];
+                }
+#pragma unroll
+                for (int h = 0; h < kN; ++h) cm[h] = warp_max(cm[h]);
+                if (lane == 0)
+#pragma unroll
+                    for (int h4 = 0; h4 < kN / 4; ++h4)
+                        sts128(red + (q * kN + 4 * h4) * 4, cm[4 * h4], cm[4 * h4 + 1], cm[4 * h4 + 2],
+                               cm[4 * h4 + 3]);
+            }
+            ok = named_bar_and(1, 128, got);
+            if (!ok) break;
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+#pragma unroll
+                for (int h4 = 0; h4 < kN / 4; ++h4) {
+                    const float4 y = lds128f(red + (w * kN + 4 * h4) * 4);
+                    if (w == 0) {
+                        cm[4 * h4] = y.x;
+                        cm[4 * h4 + 1] = y.y;
+                        cm[4 * h4 + 2] = y.z;
+                        cm[4 * h4 + 3] = y.w;
+                    } else {
+                        cm[4 * h4] = fmaxf(cm[4 * h4], y.x);
+                        cm[4 * h4 + 1] = fmaxf(cm[4 * h4 + 1], y.y);
+                        cm[4 * h4 + 2] = fmaxf(cm[4 * h4 + 2], y.z);
+                        cm[4 * h4 + 3] = fmaxf(cm[4 * h4 + 3], y.w);
+                    }
+                }
+            // New reference maxima (the same in every thread: the same values
+            // and operations). O holds the earlier chunks against the old
+            // ones; when a finite one moves, O must be scaled before P . V.
+            bool scale_o = false;
+#pragma unroll
+            for (int h = 0; h < kN; ++h) {
+                const bool move = cm[h] > m[h] + kRescaleLog2 || (m[h] == -INFINITY && cm[h] > -INFINITY);
+                cm[h] = move ? cm[h] : m[h];  // cm: the new reference
+                scale_o |= move && m[h] > -INFINITY;
+            }
+            // Chunk c - 1's P . V completed before chunk c's scores (its
+            // buffer was free first), so O holds every earlier chunk.
+            if (scale_o) {
+#pragma unroll 1
+                for (int j = 0; j < 12; ++j) {  // 4 blocks x 3 terms
+                    uint32_t r[16];
+                    const uint32_t ta = tmem + lane_base + kColO + 16 * j;
+                    tmem_ld16(ta, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int h = 0; h < kN; ++h)
+                        r[h] = __float_as_uint(__uint_as_float(r[h]) *
+                                               (m[h] == cm[h] ? 1.f : fast_exp2(m[h] - cm[h])));
+                    tmem_st16(ta, r);
+                }
+                tmem_wait_st();
+            }
+            const uint32_t sb = s0 + kOffSlot;
+            if (!live) {  // zero weight: make the ckv row exact zeros for P . V
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)  // rotated by token: 8 lanes, 8 bank groups
+                        sts128u(sb + blk * kCkvBlock + tok * 128 + (((ch + tok) & 7) << 4), 0u, 0u, 0u, 0u);
+            }
+            const uint32_t pb = s0 + kOffP;
+            const uint32_t colx = static_cast<uint32_t>((tok >> 4) << 4);  // the token's 16-byte chunk, unswizzled
+            if (__any_sync(0xffffffffu, scale_o)) {  // the same in every lane; rare after the first chunk
+#pragma unroll
+                for (int h = 0; h < kN; ++h) l[h] *= m[h] == cm[h] ? 1.f : fast_exp2(m[h] - cm[h]);  // 0 from -inf
+            }
+#pragma unroll
+            for (int h2 = 0; h2 < kN / 2; ++h2) {
+                float pw[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int h = 2 * h2 + e;
+                    const float p = cm[h] == -INFINITY ? 0.f : fast_exp2(sv[h] - cm[h]);
+                    l[h] += p;
+                    m[h] = cm[h];
+                    pw[e] = p * kPScale;
+                }
+                // three E5M2 terms of the pair (head 2 h2 in the low halves)
+                const uint32_t x = pack_f16(pw[0], pw[1]);
+                const uint32_t t1 = x & 0xFF00FF00u;
+                const uint32_t y = hsub2(x, t1);
+                const uint32_t t2 = y & 0xFF00FF00u;
+                const uint32_t t3 = f16x2_to_e5m2x2(hsub2(y, t2));
+                const uint32_t bytes[3][2] = {{(t1 >> 8) & 0xFFu, t1 >> 24},
+                                              {(t2 >> 8) & 0xFFu, t2 >> 24},
+                                              {t3 & 0xFFu, (t3 >> 8) & 0xFFu}};
+#pragma unroll
+                for (int t = 0; t < 3; ++t)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int row = 16 * t + 2 * h2 + e;
+                        sts8(pb + row * 128 + (colx ^ ((row & 7) << 4)) + (tok & 15), bytes[t][e]);
+                    }
+            }
+            fence_proxy_async_smem();  // P8 and zeroed rows before the tensor core reads them
+            tc_fence_before();         // S read and O scaled before the next MMAs
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bPFull));
+        }
+        const bool got_o = ok && warp_wait(bar(bOFull), (nch - 1) & 1);
+
+        // ---- epilogue: l over the tokens of the four warps ----------------------
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+            for (int h = 0; h < kN; ++h) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+        const uint32_t lred = s0 + kOffSum;
+        if (lane == 0)
+#pragma unroll
+            for (int h4 = 0; h4 < kN / 4; ++h4)
+                sts128(lred + (q * kN + 4 * h4) * 4, l[4 * h4], l[4 * h4 + 1], l[4 * h4 + 2], l[4 * h4 + 3]);
+        ok = named_bar_and(1, 128, got_o);
+        if (ok) {
+#pragma unroll
+            for (int h4 = 0; h4 < kN / 4; ++h4) {
+                float4 t = lds128f(lred + (4 * h4) * 4);
+#pragma unroll
+                for (int w = 1; w < 4; ++w) {
+                    const float4 y = lds128f(lred + (w * kN + 4 * h4) * 4);
+                    t.x += y.x;
+                    t.y += y.y;
+                    t.z += y.z;
+                    t.w += y.w;
+                }
+                l[4 * h4] = t.x;
+                l[4 * h4 + 1] = t.y;
+                l[4 * h4 + 2] = t.z;
+                l[4 * h4 + 3] = t.w;
+            }
+            float inv[kN];
+#pragma unroll
+            for (int h = 0; h < kN; ++h) inv[h] = l[h] > 0.f ? cks * __frcp_rn(kPScale * l[h]) : 0.f;
+            tc_fence_after();
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r0[16], r1[16], r2[16];
+                const uint32_t ta = tmem + lane_base + kColO + 48 * j;
+                tmem_ld16(ta, r0);
+                tmem_ld16(ta + 16, r1);
+                tmem_ld16(ta + 32, r2);
+                tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < kN; ++h)
+                    if (h < H)
+                        outp[h * a.op_s2 + 128 * j + 32 * q + lane] =
+                            (__uint_as_float(r0[h]) + __uint_as_float(r1[h]) + __uint_as_float(r2[h])) * inv[h];
+            }
+#pragma unroll
+            for (int h = 0; h < kN; ++h)
+                if (i == h && h < H)
+                    lsep[h] = l[h] > 0.f ? (m[h] + __log2f(l[h])) * 0.69314718055994530942f : -INFINITY;
+        }
     }
-    const float cks = __ldg(a.ckv_scale);
-    const float sl = a.scale_log2;
 
-    float acc[NH][8][4];
-#pragma unroll
-    for (int ht = 0; ht < NH; ++ht)
-#pragma unroll
-        for (int md = 0; md < 8; ++md) acc[ht][md][0] = acc[ht][md][1] = acc[ht][md][2] = acc[ht][md][3] = 0.f;
-    float mx[NH][2], ls[NH][2];  // running max (log2 units), partial sums of heads 8 ht + 2t + e
-#pragma unroll
-    for (int ht = 0; ht < NH; ++ht) mx[ht][0] = mx[ht][1] = -INFINITY, ls[ht][0] = ls[ht][1] = 0.f;
-
-    // chunk c: ring slot c % kNSlot, barrier phase (c / kNSlot) & 1, its
-    // partial scores in parity buffer c & 1
-    auto valid_of = [&](int c) -> int {  // tokens of chunk c (0: its page id is out of range)
-        const int pid = page_of(c);
-        return (pid >= 0 && pid < num_pages) ? min(kCh, ntok - c * kCh) : 0;
-    };
-
-    // ---- phase 1: partial scores of chunk c over this warp's columns -----------
-    auto phase1 = [&](int c) {
-        const uint32_t sb = ring0 + (c % kNSlot) * kSlot;
-        const uint32_t ck = sb + warp * kBox;  // this warp's 128 ckv columns
-        const uint32_t kp = sb + 4 * kBox;     // kpe box
-        const uint32_t pw = part0 + (c & 1) * (kW * 2 * NH * 512);
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            float sc[NH][4];
-#pragma unroll
-            for (int ht = 0; ht < NH; ++ht) sc[ht][0] = sc[ht][1] = sc[ht][2] = sc[ht][3] = 0.f;
-            uint32_t w[2][8];
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int r = 16 * mt + g + 8 * hr;
-                const uint4 x0 = lds128(ck + swz128(r, 32 * t));
-                const uint4 x1 = lds128(ck + swz128(r, 32 * t + 16));
-                w[hr][0] = x0.x; w[hr][1] = x0.y; w[hr][2] = x0.z; w[hr][3] = x0.w;
-                w[hr][4] = x1.x; w[hr][5] = x1.y; w[hr][6] = x1.z; w[hr][7] = x1.w;
-            }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t a0 = e4m3x2_to_f16x2(lo16(w[0][kk])), a1 = e4m3x2_to_f16x2(lo16(w[1][kk]));
-                const uint32_t a2 = e4m3x2_to_f16x2(hi16(w[0][kk])), a3 = e4m3x2_to_f16x2(hi16(w[1][kk]));
-#pragma unroll
-                for (int ht = 0; ht < NH; ++ht) mma16816<true>(sc[ht], a0, a1, a2, a3, qb[ht][kk][0], qb[ht][kk][1]);
-            }
-#pragma unroll
-            for (int ht = 0; ht < NH; ++ht)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sc[ht][e] *= cks;  // the ckv part carries the latent scale
-            {
-                const int r = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
-                const int col = 2 * (16 * warp + 8 * (lane >> 4));
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(kp + swz128(r, col), a0, a1, a2, a3);
-#pragma unroll
-                for (int ht = 0; ht < NH; ++ht) mma16816<false>(sc[ht], a0, a1, a2, a3, qr[ht][0], qr[ht][1]);
-            }
-#pragma unroll
-            for (int ht = 0; ht < NH; ++ht)
-                sts128(pw + ((warp * 2 * NH + mt * NH + ht) * 32 + lane) * 16, sc[ht][0], sc[ht][1], sc[ht][2],
-                       sc[ht][3]);
-        }
-    };
-
-    // ---- phases 2 and 3 of chunk c: total scores and online softmax (every
-    // warp the same), then O^T += ckv^T P^T over this warp's 128 columns ------
-    auto phase23 = [&](int c, int valid) {
-        const uint32_t ck = ring0 + (c % kNSlot) * kSlot + warp * kBox;
-        const uint32_t pw = part0 + (c & 1) * (kW * 2 * NH * 512);
-        float pr[2][NH][4];
-        float al[NH][2];
-        bool moved = false;
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int ht = 0; ht < NH; ++ht) {
-                float4 tot = lds128f(pw + ((0 * 2 * NH + mt * NH + ht) * 32 + lane) * 16);
-#pragma unroll
-                for (int w = 1; w < kW; ++w) {
-                    const float4 y = lds128f(pw + ((w * 2 * NH + mt * NH + ht) * 32 + lane) * 16);
-                    tot.x += y.x; tot.y += y.y; tot.z += y.z; tot.w += y.w;
-                }
-                const bool v0 = 16 * mt + g < valid, v1 = 16 * mt + g + 8 < valid;
-                pr[mt][ht][0] = v0 ? tot.x * sl : -INFINITY;
-                pr[mt][ht][1] = v0 ? tot.y * sl : -INFINITY;
-                pr[mt][ht][2] = v1 ? tot.z * sl : -INFINITY;
-                pr[mt][ht][3] = v1 ? tot.w * sl : -INFINITY;
-            }
-#pragma unroll
-        for (int ht = 0; ht < NH; ++ht)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float pm = fmaxf(fmaxf(pr[0][ht][e], pr[0][ht][2 + e]), fmaxf(pr[1][ht][e], pr[1][ht][2 + e]));
-                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-                const float nm = fmaxf(mx[ht][e], pm);
-                al[ht][e] = fast_exp2(mx[ht][e] - nm);
-                moved |= al[ht][e] != 1.f;
-                mx[ht][e] = nm;
-                float sum = 0.f;
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    pr[mt][ht][e] = fast_exp2(pr[mt][ht][e] - nm);
-                    pr[mt][ht][2 + e] = fast_exp2(pr[mt][ht][2 + e] - nm);
-                    sum += pr[mt][ht][e] + pr[mt][ht][2 + e];
-                }
-                ls[ht][e] = ls[ht][e] * al[ht][e] + sum;
-            }
-        if (__any_sync(0xffffffffu, moved)) {
-#pragma unroll
-            for (int ht = 0; ht < NH; ++ht)
-#pragma unroll
-                for (int md = 0; md < 8; ++md) {
-                    acc[ht][md][0] *= al[ht][0];
-                    acc[ht][md][1] *= al[ht][1];
-                    acc[ht][md][2] *= al[ht][0];
-                    acc[ht][md][3] *= al[ht][1];
-                }
-        }
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            uint32_t pb[NH][2];
-#pragma unroll
-            for (int ht = 0; ht < NH; ++ht) {
-                pb[ht][0] = movmatrix_trans(pack_f16(pr[kb][ht][0], pr[kb][ht][1]));
-                pb[ht][1] = movmatrix_trans(pack_f16(pr[kb][ht][2], pr[kb][ht][3]));
-            }
-            // thread g: columns 128w + 16g .. +15 of tokens 16kb + 2t, 2t+1, 2t+8, 2t+9
-            uint32_t va[4][4];
-            const int rows[4] = {16 * kb + 2 * t, 16 * kb + 2 * t + 1, 16 * kb + 2 * t + 8, 16 * kb + 2 * t + 9};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 xv = lds128(ck + swz128(rows[q], 16 * g));
-                const bool in = rows[q] < valid;  // bytes past the sequence end may be anything
-                va[q][0] = in ? xv.x : 0u;
-                va[q][1] = in ? xv.y : 0u;
-                va[q][2] = in ? xv.z : 0u;
-                va[q][3] = in ? xv.w : 0u;
-            }
-#pragma unroll
-            for (int wd = 0; wd < 4; ++wd) {
-                const uint32_t pl = prmt(va[0][wd], va[1][wd], 0x5140u);
-                const uint32_t ph = prmt(va[0][wd], va[1][wd], 0x7362u);
-                const uint32_t ql = prmt(va[2][wd], va[3][wd], 0x5140u);
-                const uint32_t qh = prmt(va[2][wd], va[3][wd], 0x7362u);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t pwd = j ? ph : pl, qwd = j ? qh : ql;
-                    const uint32_t a0 = e4m3x2_to_f16x2(lo16(pwd)), a1 = e4m3x2_to_f16x2(hi16(pwd));
-                    const uint32_t a2 = e4m3x2_to_f16x2(lo16(qwd)), a3 = e4m3x2_to_f16x2(hi16(qwd));
-#pragma unroll
-                    for (int ht = 0; ht < NH; ++ht)
-                        mma16816<true>(acc[ht][2 * wd + j], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);
-                }
-            }
-        }
-    };
-
-    // ---- software pipeline: chunk c + 1's partial scores are computed while
-    // chunk c's softmax and output accumulate; one barrier per chunk --------
-    int bad = 0;
-    int v_cur = valid_of(0);
-    bool landed = mbar_wait_bounded(bar0, 0u, kWaitLimitNs);
-    if (v_cur > 0) phase1(0);
-    if (v_cur == 0 && threadIdx.x == 0) ++bad;
-    bool ok = __syncthreads_and(landed) != 0;
-    int first_pending = 0;  // the oldest chunk whose copies may still be in flight
-    int c = 0;
-    if (ok) {
-        for (; c < nch; ++c) {
-            const int cn = c + 1;
-            landed = true;
-            int v_next = 0;
-            if (cn < nch) {
-                landed = mbar_wait_bounded(bar0 + 8 * (cn % kNSlot), (cn / kNSlot) & 1, kWaitLimitNs);
-                v_next = valid_of(cn);
-                if (v_next > 0) phase1(cn);
-            }
-            if (v_cur > 0) phase23(c, v_cur);
-            // the partials of chunk c + 1 are complete, every warp is done
-            // with chunk c (its slot may be refilled), and all agree on
-            // whether chunk c + 1's copies landed
-            ok = __syncthreads_and(landed) != 0;
-            if (!ok) {
-                first_pending = cn;
-                break;
-            }
-            if (cn < nch && v_next == 0 && threadIdx.x == 0) ++bad;
-            if (warp == 0 && c + kNSlot < nch) {
-                fence_proxy_async_smem();  // the CTA's reads of the slot before the copies' writes
-                issue(c + kNSlot);
-            }
-            v_cur = v_next;
-        }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
-
-    if (!ok) {
-        // A copy never landed: record it, then wait (bounded) for the copies
-        // still in flight before exiting.
-        if (threadIdx.x == 0) flag_error(a.err, PKV_FLAG_WAIT_TIMEOUT);
-        if (warp == 0) {
-            const int last = min(c + kNSlot, nch);
-            for (int j = first_pending; j < last; ++j)
-                (void)mbar_wait_bounded(bar0 + 8 * (j % kNSlot), (j / kNSlot) & 1, kWaitLimitNs);
-        }
-        __syncthreads();
-    }
-    if (bad) flag_error(a.err, PKV_FLAG_PAGE_RANGE);
-
-    // ---- epilogue: this warp's 128 columns of every head ------------------------
-#pragma unroll
-    for (int ht = 0; ht < NH; ++ht)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            ls[ht][e] += __shfl_xor_sync(0xffffffffu, ls[ht][e], 4);
-            ls[ht][e] += __shfl_xor_sync(0xffffffffu, ls[ht][e], 8);
-            ls[ht][e] += __shfl_xor_sync(0xffffffffu, ls[ht][e], 16);
-        }
-#pragma unroll
-    for (int ht = 0; ht < NH; ++ht)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int h = 8 * ht + 2 * t + e;
-            if (h >= H) continue;
-            const bool empty = !(ls[ht][e] > 0.f);
-            const float inv = empty ? 0.f : cks / ls[ht][e];
-            float* orow = outp + h * a.op_s2 + 128 * warp + 16 * g;
-#pragma unroll
-            for (int md = 0; md < 8; ++md)
-                *reinterpret_cast<float2*>(orow + 2 * md) = make_float2(acc[ht][md][e] * inv, acc[ht][md][2 + e] * inv);
-            if (warp == 0 && g == 0)
-                lsep[h] = empty ? -INFINITY : (mx[ht][e] + __log2f(ls[ht][e])) * 0.69314718055994530942f;
-        }
-}
-
-template <int NH>
-cudaError_t launch_t(const MlaDecodeArgs& a, const CUtensorMap& tckv, const CUtensorMap& tkpe, cudaStream_t s) {
-    auto kern = mla_decode_kernel<NH>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MlaCfg<NH>::SMEM);
-    if (e != cudaSuccess) return e;
-    return launch_dependent(kern, dim3(a.num_splits, a.B), dim3(kW * 32), MlaCfg<NH>::SMEM, s, tckv, tkpe, a);
 }
 
 }  // namespace
 
-int mla_decode_ctas_per_sm(int H) { return H > 8 ? MlaCfg<2>::CTAS : MlaCfg<1>::CTAS; }
+int mla_decode_ctas_per_sm(int) { return kCtasPerSm; }
 
 cudaError_t launch_mla_decode(const MlaDecodeArgs& a, const CUtensorMap& tckv, const CUtensorMap& tkpe,
                               cudaStream_t s) {
     if (a.B == 0) return cudaSuccess;
-    return a.H > 8 ? launch_t<2>(a, tckv, tkpe, s) : launch_t<1>(a, tckv, tkpe, s);
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(mla_decode_kernel, dim3(a.num_splits, a.B), dim3(kThreads), kSmem, s, tckv, tkpe, a);
 }
 
 }  // namespace pkv

@@ -97,7 +97,8 @@ bool make_cache_map(CUtensorMap* m, const pkv_tensor& c, int32_t layout) {
 }
 
 // Tile map over an MLA cache [pages, P, W] (W = 512 E4M3 bytes of ckv or 64
-// bf16 values of kpe): one box = 32 token rows x 128 bytes, 128-byte swizzle.
+// bf16 values of kpe): one box = the 64 token rows of a page x 128 bytes,
+// 128-byte swizzle.
 bool make_mla_map(CUtensorMap* m, const pkv_tensor& c) {
     auto enc = encode_fn();
     if (!enc) return false;
@@ -105,7 +106,7 @@ bool make_mla_map(CUtensorMap* m, const pkv_tensor& c) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(c.shape[2]), static_cast<cuuint64_t>(c.shape[1]),
                           static_cast<cuuint64_t>(c.shape[0])};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(c.stride[1] * e), static_cast<cuuint64_t>(c.stride[0] * e)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / e), 32, 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / e), static_cast<cuuint32_t>(pkv::kMlaPage), 1};  // one page
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
                      c.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
