@@ -12,21 +12,24 @@
 // The tensor cores read the E4M3 cache bytes as the copy engine lands them:
 // nothing is converted on the CUDA cores.
 //
-// Work decomposition. One CTA per (split, sequence), two CTAs per SM (106 KB
-// of shared memory, 256 tensor-memory columns each), six warps in three
-// roles. A split's tokens go through the CTA two pages (128 tokens, the MMA
-// M) at a time ("chunk"), one chunk in shared memory at a time; the two
-// CTAs of an SM overlap each other's waits.
+// Work decomposition. Persistent CTAs, two per SM (106 KB of shared memory,
+// 256 tensor-memory columns each), six warps in three roles. The work items
+// are the (sequence, split) pairs; CTA k takes items k, k + grid, k + 2 grid,
+// ... A split's tokens go through the CTA two pages (128 tokens, the MMA M)
+// at a time ("chunk"), one chunk in shared memory at a time; the copies run
+// on across items, so only a CTA's first chunk waits for a cold start, and
+// the two CTAs of an SM overlap each other's waits.
 //
 //   warp 0, copies    TMA tile loads with 128-byte swizzle into the chunk
 //                     buffer: per page four 64-row x 128-byte boxes of ckv
 //                     (one per 128-value column block) and one of kpe; the
 //                     buffer holds ckv as [4 blocks][128 rows][128 B] and
 //                     kpe as [128 rows][128 B] (80 KB). The next two chunks
-//                     are prefetched into L2 (cp.async.bulk.prefetch), the
-//                     first ones before the wait on the preceding grid (a
+//                     are prefetched into L2 (cp.async.bulk.prefetch): the
+//                     first chunk before the wait on the preceding grid (a
 //                     prefetch reads through L2, which the preceding grid's
-//                     writes also go through).
+//                     writes also go through), the read-ahead only once the
+//                     first chunk has landed.
 //   warp 1, MMA       the whole warp runs the issue loop; one elected lane
 //                     issues (elect.sync):
 //                       S^T[128 tok x 32]   = ckv . Q8^T    (kind::f8f6f4, E4M3 x E4M3, K = 512)
@@ -39,12 +42,15 @@
 //   warps 2-5, softmax  (lane = token: warp w holds tokens 32(w%4) + 0..31)
 //                     scores from tensor memory, per-head chunk maxima
 //                     (redux.sync, a 4-warp exchange), P, its E5M2 terms to
-//                     shared memory, the running sums; the epilogue.
+//                     shared memory, the running sums; per item the next
+//                     item's queries (so its scores overlap) and then the
+//                     epilogue; the (0, -inf) records of empty splits.
 //
 // Per chunk the steps are serial: copy -> S -> P -> P . V -> the buffer is
 // free for the next copy. So the next chunk's scores never overwrite S
-// before it was read, P is never rewritten before P . V read it, and O is
-// never scaled while P . V runs.
+// before it was read, P is never rewritten before P . V read it, O is never
+// scaled while P . V runs, and an item's first P . V (which starts O anew)
+// comes after the softmax warps read the previous item's O.
 //
 // The operands, in FP8:
 //   Q8: q_lat = 2^-k_h (t1 + t2) per head h, t1 = E4M3(2^k_h q),
@@ -80,6 +86,8 @@
 // roles' waits; the four softmax warps agree on stopping through their
 // barrier's AND; the copy and MMA roles wait (bounded) for their own
 // operations in flight; the CTA then frees its tensor memory and exits.
+#include <algorithm>
+
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
@@ -150,6 +158,64 @@ __device__ __forceinline__ float f16_hi(uint32_t w) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 
+// One work item: split s of sequence b (items are numbered b * S + s).
+struct Item {
+    int b, s;
+    int npg;              // pages of the split
+    int ntok;             // tokens of the split
+    int nch;              // chunks of the split
+    bool bad_len;         // seq_lens[b] outside [0, block-table width x page]
+    const int32_t* bt;    // the split's block-table entries
+};
+
+__device__ __forceinline__ Item item_of(const MlaDecodeArgs& a, int it) {
+    Item x;
+    x.b = it / a.num_splits;
+    x.s = it - x.b * a.num_splits;
+    const int L0 = __ldg(a.seq_lens + x.b);
+    const int cap = a.max_pages * kMlaPage;
+    x.bad_len = L0 < 0 || L0 > cap;
+    const int L = min(max(L0, 0), cap);
+    const int npages = (L + kMlaPage - 1) / kMlaPage;
+    const int pps = (npages + a.num_splits - 1) / a.num_splits;
+    const int p0 = x.s * pps;
+    const int p1 = min(p0 + pps, npages);
+    x.npg = max(p1 - p0, 0);
+    x.ntok = p1 > p0 ? min(L, p1 * kMlaPage) - p0 * kMlaPage : 0;
+    x.nch = (x.ntok + kT - 1) / kT;
+    x.bt = a.block_tables + x.b * a.bt_s0 + p0;
+    return x;
+}
+
+// page id of page pg of the item if it exists and is in range, else -1
+__device__ __forceinline__ int page_of(const Item& x, int pg, int64_t num_pages) {
+    if (pg >= x.npg) return -1;
+    const int pid = __ldg(x.bt + pg);
+    return (pid >= 0 && pid < num_pages) ? pid : -1;
+}
+
+// Position in this CTA's sequence of chunks: chunk c of its item `it`
+// (it >= n_items: past the end). Items without tokens are skipped.
+struct Cursor {
+    int it;
+    int c;
+    Item x;
+};
+__device__ __forceinline__ void settle(const MlaDecodeArgs& a, Cursor& u, int n_items) {
+    u.c = 0;
+    while (u.it < n_items) {
+        u.x = item_of(a, u.it);
+        if (u.x.nch > 0) return;
+        u.it += gridDim.x;
+    }
+}
+__device__ __forceinline__ void step(const MlaDecodeArgs& a, Cursor& u, int n_items) {
+    if (++u.c >= u.x.nch) {
+        u.it += gridDim.x;
+        settle(a, u, n_items);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tckv, const __grid_constant__ CUtensorMap tkpe,
                       const MlaDecodeArgs a) {
@@ -162,42 +228,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int s = blockIdx.x;
-    const int b = blockIdx.y;
     const int H = a.H;
-
-    // ---- this split's tokens ---------------------------------------------------
-    int L = __ldg(a.seq_lens + b);
-    const int cap = a.max_pages * kMlaPage;
-    if (L < 0 || L > cap) {
-        if (threadIdx.x == 0 && s == 0) flag_error(a.err, PKV_FLAG_SEQ_LEN_RANGE);
-        L = L < 0 ? 0 : cap;
-    }
-    const int npages = (L + kMlaPage - 1) / kMlaPage;
-    const int pps = (npages + a.num_splits - 1) / a.num_splits;
-    const int p0 = s * pps;
-    const int p1 = min(p0 + pps, npages);
-    const int npg = max(p1 - p0, 0);  // pages of the split
-    const int tok0 = p0 * kMlaPage;
-    const int ntok = p1 > p0 ? min(L, p1 * kMlaPage) - tok0 : 0;
-    const int nch = (ntok + kT - 1) / kT;
-    float* outp = a.out_partial + b * a.op_s0 + s * a.op_s1;
-    float* lsep = a.lse_partial + b * a.lp_s0 + s * a.lp_s1;
-    if (nch == 0) {  // empty split: (0, -inf)
-        grid_dep_wait();
-        grid_dep_launch();
-        for (int i = threadIdx.x; i < H * kMlaDc; i += blockDim.x) outp[(i / kMlaDc) * a.op_s2 + (i % kMlaDc)] = 0.f;
-        for (int i = threadIdx.x; i < H; i += blockDim.x) lsep[i] = -INFINITY;
-        return;
-    }
-    const int32_t* bt = a.block_tables + b * a.bt_s0 + p0;
+    const int n_items = a.B * a.num_splits;
     const int64_t num_pages = a.num_pages;
-    // page id of page pg of the split if it exists and is in range, else -1
-    auto page_id = [&](int pg) -> int {
-        if (pg >= npg) return -1;
-        const int pid = __ldg(bt + pg);
-        return (pid >= 0 && pid < num_pages) ? pid : -1;
-    };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(bFull), 1);
@@ -222,12 +255,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // Start reading the first chunks into L2 while the preceding grid may
-    // still run (a prefetch loads nothing into this CTA).
-    auto prefetch_chunk = [&](int c) {  // lanes 0-4: first page, 8-12: second
+    // L2 read-ahead of one chunk (lanes 0-4: its first page, 8-12: second)
+    auto prefetch_at = [&](const Cursor& u) {
         const int half = lane >> 3, j = lane & 7;
-        if (c < nch && half < 2 && j < 5) {
-            const int id = page_id(2 * c + half);
+        if (u.it < n_items && half < 2 && j < 5) {
+            const int id = page_of(u.x, 2 * u.c + half, num_pages);
             if (id >= 0) {
                 if (j < 4)
                     tma_prefetch_3d(&tckv, 128 * j, 0, id);
@@ -236,8 +268,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
         }
     };
-    if (warp == kWarpCopy)
-        for (int c = 0; c <= kPrefetch; ++c) prefetch_chunk(c);
+    // L2 read-ahead of the queries of item it (lane h < 16: q_lat row h,
+    // 16 + h: q_pe row h), for 16-byte aligned rows
+    auto prefetch_q = [&](int it) {
+        if (it >= n_items) return;
+        const int bq = it / a.num_splits;
+        const int h = lane & 15;
+        if (h < H) {
+            const void* r = lane < 16 ? static_cast<const void*>(a.q_lat + bq * a.ql_s0 + h * a.ql_s1)
+                                      : static_cast<const void*>(a.q_pe + bq * a.qp_s0 + h * a.qp_s1);
+            if ((reinterpret_cast<uintptr_t>(r) & 15) == 0) bulk_prefetch_l2(r, lane < 16 ? 2 * kMlaDc : 2 * kMlaDr);
+        }
+    };
+    // The first chunk and queries go into L2 while the preceding grid may
+    // still run (a prefetch loads nothing into this CTA; the index inputs
+    // are this call's own).
+    Cursor cur;
+    cur.it = blockIdx.x;
+    if (warp == kWarpCopy) {
+        settle(a, cur, n_items);
+        prefetch_at(cur);
+        prefetch_q(cur.it);
+    }
 
     // q and the cache may still be being written by the preceding grid.
     grid_dep_wait();
@@ -257,12 +309,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (warp == kWarpCopy) {
         // ======================= copies ===========================================
         const uint64_t policy = l2_policy_evict_first();
-        int issued = 0;  // chunks whose copies were started
-        for (int c = 0; c < nch; ++c) {
-            if (c >= 1 && !warp_wait(bar(bFree), (c - 1) & 1)) break;  // chunk c - 1's P . V is done
-            const int pa = 2 * c, pb = 2 * c + 1;
-            const int ida = page_id(pa), idb = page_id(pb);
-            if (lane == 0 && (ida < 0 || (pb < npg && idb < 0))) flag_error(a.err, PKV_FLAG_PAGE_RANGE);
+        Cursor pf = cur;  // the L2 read-ahead, kPrefetch chunks ahead of the copy
+        int g = 0, issued = 0;  // chunks of this CTA whose copies were started
+        for (; cur.it < n_items; step(a, cur, n_items), ++g) {
+            if (g >= 1 && !warp_wait(bar(bFree), (g - 1) & 1)) break;  // chunk g - 1's P . V is done
+            const int pa = 2 * cur.c, pb = pa + 1;
+            const int ida = page_of(cur.x, pa, num_pages), idb = page_of(cur.x, pb, num_pages);
+            if (lane == 0 && (ida < 0 || (pb < cur.x.npg && idb < 0))) flag_error(a.err, PKV_FLAG_PAGE_RANGE);
             const uint32_t fb = bar(bFull);
             const uint32_t bytes = (ida >= 0 ? 5 * kPageRows : 0) + (idb >= 0 ? 5 * kPageRows : 0);
             if (lane == 0) {
@@ -281,9 +334,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 else
                     tma_load_3d(sb + kSlotCkv + half * kPageRows, &tkpe, fb, 0, 0, id, policy);
             }
-            if (c >= 1) prefetch_chunk(c + kPrefetch);
             __syncwarp();
-            issued = c + 1;
+            issued = g + 1;
+            if (cur.c == 0) prefetch_q(cur.it + gridDim.x);  // the next item's queries
+            if (g == 0) {
+                // Every CTA's first chunk is requested before any read-ahead,
+                // so none waits behind the other CTAs' later chunks.
+                step(a, pf, n_items);
+                if (pf.it < n_items && !warp_wait(fb, 0)) break;
+                for (int k = 1; k <= kPrefetch; ++k) {
+                    prefetch_at(pf);
+                    if (k < kPrefetch) step(a, pf, n_items);
+                }
+            } else {
+                step(a, pf, n_items);
+                prefetch_at(pf);
+            }
         }
         // The copies started land before the CTA may exit: wait (bounded)
         // for the newest phase (at once on the normal path).
@@ -292,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     } else if (warp == kWarpMma) {
         // ======================= tensor-core issue ================================
         int n_qk = 0, n_pv = 0;  // chunks whose MMAs were issued
-        auto qk = [&](int c) -> bool {
-            if (!warp_wait(bar(bFull), c & 1)) return false;
+        auto qk = [&](int g) -> bool {
+            if (!warp_wait(bar(bFull), g & 1)) return false;
             tc_fence_after();
             const uint32_t sb = s0 + kOffSlot;
             const uint32_t dS = tmem + kColS;
@@ -305,11 +371,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int k = 0; k < kMlaDr / 16; ++k)
                 umma_f16_warp(dS + 32, desc_k(sb + kSlotCkv + k * 32), desc_k(s0 + kOffQp + k * 32), kIdescPe, k > 0);
             umma_commit_warp(bar(bSFull));
-            n_qk = c + 1;
+            n_qk = g + 1;
             return true;
         };
-        auto pv = [&](int c) -> bool {
-            if (!warp_wait(bar(bPFull), c & 1)) return false;
+        // P . V of chunk g, the item's chunk c (c = 0 starts the item's O;
+        // the item before has read its O by then: its epilogue precedes the
+        // softmax warps' P of this chunk)
+        auto pv = [&](int g, int c) -> bool {
+            if (!warp_wait(bar(bPFull), g & 1)) return false;
             tc_fence_after();
             const uint32_t sb = s0 + kOffSlot;
             const uint32_t pb = s0 + kOffP;
@@ -321,11 +390,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                  desc_k(pb + k * 32), kIdescPv, (c | k) != 0);
             umma_commit_warp(bar(bOFull));
             umma_commit_warp(bar(bFree));
-            n_pv = c + 1;
+            n_pv = g + 1;
             return true;
         };
-        bool ok = warp_wait(bar(bQFull), 0);
-        for (int c = 0; c < nch && ok; ++c) ok = qk(c) && pv(c);
+        bool ok = true;
+        int g = 0, n_ne = 0;  // chunks, items with tokens
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const Item x = item_of(a, it);
+            if (x.nch == 0) continue;
+            ok = warp_wait(bar(bQFull), n_ne & 1);  // the item's queries are staged
+            for (int c = 0; c < x.nch && ok; ++c, ++g) ok = qk(g) && pv(g, c);
+            ++n_ne;
+        }
         // Every commit's arrival lands before the CTA may exit: wait
         // (bounded) for the newest phase of each barrier committed to.
         if (lane == 0) {
@@ -341,19 +417,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int q = warp & 3;                    // tensor-memory lane quarter
         const int i = threadIdx.x - kWarpSm * 32;  // 0..127
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        const uint32_t qscale = s0 + kOffQs;
         const float cks = __ldg(a.ckv_scale);
-        // ---- the queries as FP8 / bf16 B operands ----------------------------------
-        {
+        const float sl = a.scale_log2;
+        // The item's queries as FP8 / bf16 B operands (Q8 is free: the last
+        // scores that read it are complete), then one arrival per warp.
+        auto stage_q = [&](const Item& x) {
             const int h = i >> 3, p = i & 7;  // head, 64-value part
             const bool live = h < H;
-            const uint32_t* ql = reinterpret_cast<const uint32_t*>(a.q_lat + b * a.ql_s0 + h * a.ql_s1 + 64 * p);
+            const uint32_t* ql = reinterpret_cast<const uint32_t*>(a.q_lat + x.b * a.ql_s0 + h * a.ql_s1 + 64 * p);
+            uint32_t w[32];  // the 64 values, loaded at once
+#pragma unroll
+            for (int k = 0; k < 32; ++k) w[k] = live ? __ldg(ql + k) : 0u;
             float mx = 0.f;
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
-                const uint32_t w2 = live ? __ldg(ql + k) : 0u;
-                mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w2)), fabsf(bf16_hi(w2))));
-            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
@@ -375,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     uint32_t b1 = 0u, b2 = 0u;
 #pragma unroll
                     for (int m2 = 0; m2 < 2; ++m2) {
-                        const uint32_t w2 = live ? __ldg(ql + 8 * ch + 2 * m4 + m2) : 0u;
+                        const uint32_t w2 = w[8 * ch + 2 * m4 + m2];
                         const float x0 = bf16_lo(w2) * sc, x1 = bf16_hi(w2) * sc;
                         const uint32_t e1 = f32x2_to_e4m3x2(x1, x0);
                         const uint32_t h1 = e4m3x2_to_f16x2(static_cast<uint16_t>(e1));
@@ -392,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 sts128u(s0 + kOffQ + blk * kQBlock + (16 + h) * 128 + ((chunk ^ ((16 + h) & 7)) << 4), t2w[0],
                         t2w[1], t2w[2], t2w[3]);
             }
-            const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q_pe + b * a.qp_s0 + h * a.qp_s1 + 8 * p);
+            const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q_pe + x.b * a.qp_s0 + h * a.qp_s1 + 8 * p);
             uint32_t v[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) v[m] = live ? __ldg(qp + m) : 0u;
@@ -400,183 +477,214 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bQFull));
-        }
-        named_bar_and(1, 128, true);  // the q scales
-        float qs[kN];
-#pragma unroll
-        for (int h4 = 0; h4 < kN / 4; ++h4) {
-            const float4 y = lds128f(qscale + 16 * h4);
-            qs[4 * h4] = y.x;
-            qs[4 * h4 + 1] = y.y;
-            qs[4 * h4 + 2] = y.z;
-            qs[4 * h4 + 3] = y.w;
-        }
-        const float sl = a.scale_log2;
-        float m[kN], l[kN];  // reference maximum (log2 units), this thread's part of the sum
-#pragma unroll
-        for (int h = 0; h < kN; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.f;
-        }
+        };
+        // every warp's part of the per-head scales (ckv_scale 2^-k_h) is written
+        auto load_qs = [&]() { named_bar_and(1, 128, true); };
+        // the first item with tokens from `it` on; splits without tokens on
+        // the way get their (0, -inf) records
+        auto next_item = [&](int it) -> int {
+            for (; it < n_items; it += gridDim.x) {
+                const Item y = item_of(a, it);
+                if (i == 0 && y.s == 0 && y.bad_len) flag_error(a.err, PKV_FLAG_SEQ_LEN_RANGE);
+                if (y.nch > 0) return it;
+                float* op = a.out_partial + y.b * a.op_s0 + y.s * a.op_s1;
+                for (int k = i; k < H * kMlaDc; k += 128) op[(k / kMlaDc) * a.op_s2 + (k % kMlaDc)] = 0.f;
+                if (i < H) a.lse_partial[y.b * a.lp_s0 + y.s * a.lp_s1 + i] = -INFINITY;
+            }
+            return it;
+        };
 
         const int tok = 32 * q + lane;  // token of the chunk = tensor-memory lane
         // The four warps pass the same named barriers and decide whether to
-        // go on by the barrier's AND (a failed wait is carried into the next
-        // one), so all of them stop at the same chunk.
+        // go on by the barrier's AND, so all of them stop at the same chunk.
         bool ok = true;
-        for (int c = 0; c < nch; ++c) {
-            const bool got = warp_wait(bar(bSFull), c & 1);
-            const bool live = page_id(2 * c + (tok >> 6)) >= 0 && tok < ntok - kT * c;
-            float sv[kN], cm[kN];
-            const uint32_t red = s0 + kOffMax;
-            if (got) {
-                tc_fence_after();
-                uint32_t r1[16], r2[16], rp[16];
-                const uint32_t ta = tmem + lane_base + kColS;
-                tmem_ld16(ta, r1);
-                tmem_ld16(ta + 16, r2);
-                tmem_ld16(ta + 32, rp);
-                tmem_wait_ld();
-#pragma unroll
-                for (int h = 0; h < kN; ++h) {
-                    const float lat = __uint_as_float(r1[h]) + __uint_as_float(r2[h]);
-                    sv[h] = live ? fmaf(lat, qs[h], __uint_as_float(rp[h])) * sl : -INFINITY;
-                    cm[h] = sv[h];
-                }
-#pragma unroll
-                for (int h = 0; h < kN; ++h) cm[h] = warp_max(cm[h]);
-                if (lane == 0)
-#pragma unroll
-                    for (int h4 = 0; h4 < kN / 4; ++h4)
-                        sts128(red + (q * kN + 4 * h4) * 4, cm[4 * h4], cm[4 * h4 + 1], cm[4 * h4 + 2],
-                               cm[4 * h4 + 3]);
-            }
-            ok = named_bar_and(1, 128, got);
-            if (!ok) break;
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-#pragma unroll
-                for (int h4 = 0; h4 < kN / 4; ++h4) {
-                    const float4 y = lds128f(red + (w * kN + 4 * h4) * 4);
-                    if (w == 0) {
-                        cm[4 * h4] = y.x;
-                        cm[4 * h4 + 1] = y.y;
-                        cm[4 * h4 + 2] = y.z;
-                        cm[4 * h4 + 3] = y.w;
-                    } else {
-                        cm[4 * h4] = fmaxf(cm[4 * h4], y.x);
-                        cm[4 * h4 + 1] = fmaxf(cm[4 * h4 + 1], y.y);
-                        cm[4 * h4 + 2] = fmaxf(cm[4 * h4 + 2], y.z);
-                        cm[4 * h4 + 3] = fmaxf(cm[4 * h4 + 3], y.w);
-                    }
-                }
-            // New reference maxima (the same in every thread: the same values
-            // and operations). O holds the earlier chunks against the old
-            // ones; when a finite one moves, O must be scaled before P . V.
-            bool scale_o = false;
+        int it = next_item(blockIdx.x);
+        Item x;
+        if (it < n_items) {
+            x = item_of(a, it);
+            stage_q(x);
+            load_qs();
+        }
+        int g = 0;  // chunks of this CTA
+        while (it < n_items && ok) {
+            float m[kN], l[kN];  // reference maximum (log2 units), this thread's part of the sum
 #pragma unroll
             for (int h = 0; h < kN; ++h) {
-                const bool move = cm[h] > m[h] + kRescaleLog2 || (m[h] == -INFINITY && cm[h] > -INFINITY);
-                cm[h] = move ? cm[h] : m[h];  // cm: the new reference
-                scale_o |= move && m[h] > -INFINITY;
+                m[h] = -INFINITY;
+                l[h] = 0.f;
             }
-            // Chunk c - 1's P . V completed before chunk c's scores (its
-            // buffer was free first), so O holds every earlier chunk.
-            if (scale_o) {
-#pragma unroll 1
-                for (int j = 0; j < 12; ++j) {  // 4 blocks x 3 terms
-                    uint32_t r[16];
-                    const uint32_t ta = tmem + lane_base + kColO + 16 * j;
-                    tmem_ld16(ta, r);
+            for (int c = 0; c < x.nch; ++c, ++g) {
+                const bool got = warp_wait(bar(bSFull), g & 1);
+                const bool live = page_of(x, 2 * c + (tok >> 6), num_pages) >= 0 && tok < x.ntok - kT * c;
+                float sv[kN], cm[kN];
+                const uint32_t red = s0 + kOffMax;
+                if (got) {
+                    tc_fence_after();
+                    uint32_t r1[16], r2[16], rp[16];
+                    const uint32_t ta = tmem + lane_base + kColS;
+                    tmem_ld16(ta, r1);
+                    tmem_ld16(ta + 16, r2);
+                    tmem_ld16(ta + 32, rp);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int h = 0; h < kN; ++h)
-                        r[h] = __float_as_uint(__uint_as_float(r[h]) *
-                                               (m[h] == cm[h] ? 1.f : fast_exp2(m[h] - cm[h])));
-                    tmem_st16(ta, r);
+                    for (int h4 = 0; h4 < kN / 4; ++h4) {
+                        const float4 qs = lds128f(s0 + kOffQs + 16 * h4);
+                        const float qv[4] = {qs.x, qs.y, qs.z, qs.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int h = 4 * h4 + e;
+                            const float lat = __uint_as_float(r1[h]) + __uint_as_float(r2[h]);
+                            sv[h] = live ? fmaf(lat, qv[e], __uint_as_float(rp[h])) * sl : -INFINITY;
+                            cm[h] = sv[h];
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < kN; ++h) cm[h] = warp_max(cm[h]);
+                    if (lane == 0)
+#pragma unroll
+                        for (int h4 = 0; h4 < kN / 4; ++h4)
+                            sts128(red + (q * kN + 4 * h4) * 4, cm[4 * h4], cm[4 * h4 + 1], cm[4 * h4 + 2],
+                                   cm[4 * h4 + 3]);
                 }
-                tmem_wait_st();
-            }
-            const uint32_t sb = s0 + kOffSlot;
-            if (!live) {  // zero weight: make the ckv row exact zeros for P . V
+                ok = named_bar_and(1, 128, got);
+                if (!ok) break;
 #pragma unroll
-                for (int blk = 0; blk < 4; ++blk)
+                for (int w = 0; w < 4; ++w)
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)  // rotated by token: 8 lanes, 8 bank groups
-                        sts128u(sb + blk * kCkvBlock + tok * 128 + (((ch + tok) & 7) << 4), 0u, 0u, 0u, 0u);
-            }
-            const uint32_t pb = s0 + kOffP;
-            const uint32_t colx = static_cast<uint32_t>((tok >> 4) << 4);  // the token's 16-byte chunk, unswizzled
-            if (__any_sync(0xffffffffu, scale_o)) {  // the same in every lane; rare after the first chunk
+                    for (int h4 = 0; h4 < kN / 4; ++h4) {
+                        const float4 y = lds128f(red + (w * kN + 4 * h4) * 4);
+                        if (w == 0) {
+                            cm[4 * h4] = y.x;
+                            cm[4 * h4 + 1] = y.y;
+                            cm[4 * h4 + 2] = y.z;
+                            cm[4 * h4 + 3] = y.w;
+                        } else {
+                            cm[4 * h4] = fmaxf(cm[4 * h4], y.x);
+                            cm[4 * h4 + 1] = fmaxf(cm[4 * h4 + 1], y.y);
+                            cm[4 * h4 + 2] = fmaxf(cm[4 * h4 + 2], y.z);
+                            cm[4 * h4 + 3] = fmaxf(cm[4 * h4 + 3], y.w);
+                        }
+                    }
+                // New reference maxima (the same in every thread: the same
+                // values and operations). O holds the item's earlier chunks
+                // against the old ones; when a finite one moves, O must be
+                // scaled before P . V.
+                bool scale_o = false;
 #pragma unroll
-                for (int h = 0; h < kN; ++h) l[h] *= m[h] == cm[h] ? 1.f : fast_exp2(m[h] - cm[h]);  // 0 from -inf
-            }
-#pragma unroll
-            for (int h2 = 0; h2 < kN / 2; ++h2) {
-                float pw[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int h = 2 * h2 + e;
-                    const float p = cm[h] == -INFINITY ? 0.f : fast_exp2(sv[h] - cm[h]);
-                    l[h] += p;
-                    m[h] = cm[h];
-                    pw[e] = p * kPScale;
+                for (int h = 0; h < kN; ++h) {
+                    const bool move = cm[h] > m[h] + kRescaleLog2 || (m[h] == -INFINITY && cm[h] > -INFINITY);
+                    cm[h] = move ? cm[h] : m[h];  // cm: the new reference
+                    scale_o |= move && m[h] > -INFINITY;
                 }
-                // three E5M2 terms of the pair (head 2 h2 in the low halves)
-                const uint32_t x = pack_f16(pw[0], pw[1]);
-                const uint32_t t1 = x & 0xFF00FF00u;
-                const uint32_t y = hsub2(x, t1);
-                const uint32_t t2 = y & 0xFF00FF00u;
-                const uint32_t t3 = f16x2_to_e5m2x2(hsub2(y, t2));
-                const uint32_t bytes[3][2] = {{(t1 >> 8) & 0xFFu, t1 >> 24},
-                                              {(t2 >> 8) & 0xFFu, t2 >> 24},
-                                              {t3 & 0xFFu, (t3 >> 8) & 0xFFu}};
+                // Chunk g - 1's P . V completed before chunk g's scores (the
+                // buffer was free first), so O holds every earlier chunk.
+                if (scale_o) {
+#pragma unroll 1
+                    for (int j = 0; j < 12; ++j) {  // 4 blocks x 3 terms
+                        uint32_t r[16];
+                        const uint32_t ta = tmem + lane_base + kColO + 16 * j;
+                        tmem_ld16(ta, r);
+                        tmem_wait_ld();
 #pragma unroll
-                for (int t = 0; t < 3; ++t)
+                        for (int h = 0; h < kN; ++h)
+                            r[h] = __float_as_uint(__uint_as_float(r[h]) *
+                                                   (m[h] == cm[h] ? 1.f : fast_exp2(m[h] - cm[h])));
+                        tmem_st16(ta, r);
+                    }
+                    tmem_wait_st();
+#pragma unroll
+                    for (int h = 0; h < kN; ++h) l[h] *= m[h] == cm[h] ? 1.f : fast_exp2(m[h] - cm[h]);
+                }
+                const uint32_t sb = s0 + kOffSlot;
+                if (!live) {  // zero weight: make the ckv row exact zeros for P . V
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)  // rotated by token: 8 lanes, 8 bank groups
+                            sts128u(sb + blk * kCkvBlock + tok * 128 + (((ch + tok) & 7) << 4), 0u, 0u, 0u, 0u);
+                }
+                const uint32_t pb = s0 + kOffP;
+                const uint32_t colx = static_cast<uint32_t>((tok >> 4) << 4);  // the token's 16-byte chunk, unswizzled
+#pragma unroll
+                for (int h2 = 0; h2 < kN / 2; ++h2) {
+                    float pw[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int row = 16 * t + 2 * h2 + e;
-                        sts8(pb + row * 128 + (colx ^ ((row & 7) << 4)) + (tok & 15), bytes[t][e]);
+                        const int h = 2 * h2 + e;
+                        const float p = cm[h] == -INFINITY ? 0.f : fast_exp2(sv[h] - cm[h]);
+                        l[h] += p;
+                        m[h] = cm[h];
+                        pw[e] = p * kPScale;
                     }
+                    // three E5M2 terms of the pair (head 2 h2 in the low halves)
+                    const uint32_t xw = pack_f16(pw[0], pw[1]);
+                    const uint32_t t1 = xw & 0xFF00FF00u;
+                    const uint32_t y = hsub2(xw, t1);
+                    const uint32_t t2 = y & 0xFF00FF00u;
+                    const uint32_t t3 = f16x2_to_e5m2x2(hsub2(y, t2));
+                    const uint32_t bytes[3][2] = {{(t1 >> 8) & 0xFFu, t1 >> 24},
+                                                  {(t2 >> 8) & 0xFFu, t2 >> 24},
+                                                  {t3 & 0xFFu, (t3 >> 8) & 0xFFu}};
+#pragma unroll
+                    for (int t = 0; t < 3; ++t)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int row = 16 * t + 2 * h2 + e;
+                            sts8(pb + row * 128 + (colx ^ ((row & 7) << 4)) + (tok & 15), bytes[t][e]);
+                        }
+                }
+                fence_proxy_async_smem();  // P8 and zeroed rows before the tensor core reads them
+                tc_fence_before();         // S read and O scaled before the next MMAs
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bPFull));
             }
-            fence_proxy_async_smem();  // P8 and zeroed rows before the tensor core reads them
-            tc_fence_before();         // S read and O scaled before the next MMAs
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bPFull));
-        }
-        const bool got_o = ok && warp_wait(bar(bOFull), (nch - 1) & 1);
-
-        // ---- epilogue: l over the tokens of the four warps ----------------------
+            if (!ok) break;
+            // The next item's queries first: its scores then overlap this
+            // item's epilogue (Q8 is free: this item's last scores are done).
+            const int nxt = next_item(it + gridDim.x);
+            Item y;
+            if (nxt < n_items) {
+                y = item_of(a, nxt);
+                stage_q(y);
+            }
+            // ---- epilogue: l over the tokens of the four warps, O / l ---------------
+            const bool got_o = warp_wait(bar(bOFull), (g - 1) & 1);  // the item's last P . V
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
+            for (int off = 16; off >= 1; off >>= 1)
 #pragma unroll
-            for (int h = 0; h < kN; ++h) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
-        const uint32_t lred = s0 + kOffSum;
-        if (lane == 0)
+                for (int h = 0; h < kN; ++h) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+            const uint32_t lred = s0 + kOffSum;
+            if (lane == 0)
 #pragma unroll
-            for (int h4 = 0; h4 < kN / 4; ++h4)
-                sts128(lred + (q * kN + 4 * h4) * 4, l[4 * h4], l[4 * h4 + 1], l[4 * h4 + 2], l[4 * h4 + 3]);
-        ok = named_bar_and(1, 128, got_o);
-        if (ok) {
+                for (int h4 = 0; h4 < kN / 4; ++h4)
+                    sts128(lred + (q * kN + 4 * h4) * 4, l[4 * h4], l[4 * h4 + 1], l[4 * h4 + 2], l[4 * h4 + 3]);
+            ok = named_bar_and(1, 128, got_o);
+            if (!ok) break;
 #pragma unroll
             for (int h4 = 0; h4 < kN / 4; ++h4) {
                 float4 t = lds128f(lred + (4 * h4) * 4);
 #pragma unroll
                 for (int w = 1; w < 4; ++w) {
-                    const float4 y = lds128f(lred + (w * kN + 4 * h4) * 4);
-                    t.x += y.x;
-                    t.y += y.y;
-                    t.z += y.z;
-                    t.w += y.w;
+                    const float4 v = lds128f(lred + (w * kN + 4 * h4) * 4);
+                    t.x += v.x;
+                    t.y += v.y;
+                    t.z += v.z;
+                    t.w += v.w;
                 }
                 l[4 * h4] = t.x;
                 l[4 * h4 + 1] = t.y;
                 l[4 * h4 + 2] = t.z;
                 l[4 * h4 + 3] = t.w;
             }
+#pragma unroll
+            for (int h = 0; h < kN; ++h)
+                if (i == h && h < H)
+                    a.lse_partial[x.b * a.lp_s0 + x.s * a.lp_s1 + h] =
+                        l[h] > 0.f ? (m[h] + __log2f(l[h])) * 0.69314718055994530942f : -INFINITY;
             float inv[kN];
 #pragma unroll
             for (int h = 0; h < kN; ++h) inv[h] = l[h] > 0.f ? cks * __frcp_rn(kPScale * l[h]) : 0.f;
+            float* outp = a.out_partial + x.b * a.op_s0 + x.s * a.op_s1;
             tc_fence_after();
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
@@ -592,10 +700,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         outp[h * a.op_s2 + 128 * j + 32 * q + lane] =
                             (__uint_as_float(r0[h]) + __uint_as_float(r1[h]) + __uint_as_float(r2[h])) * inv[h];
             }
-#pragma unroll
-            for (int h = 0; h < kN; ++h)
-                if (i == h && h < H)
-                    lsep[h] = l[h] > 0.f ? (m[h] + __log2f(l[h])) * 0.69314718055994530942f : -INFINITY;
+            // O is read (waited above) before this warp's next P hand-off,
+            // which is what lets the next item's P . V overwrite it.
+            tc_fence_before();
+            if (nxt < n_items) load_qs();
+            it = nxt;
+            x = y;
         }
     }
 
@@ -616,7 +726,14 @@ cudaError_t launch_mla_decode(const MlaDecodeArgs& a, const CUtensorMap& tckv, c
     if (a.B == 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(mla_decode_kernel, dim3(a.num_splits, a.B), dim3(kThreads), kSmem, s, tckv, tkpe, a);
+    int sms = 0;
+    e = device_sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    // persistent: at most two CTAs per SM, each taking items blockIdx.x,
+    // blockIdx.x + gridDim.x, ...
+    const int64_t items = static_cast<int64_t>(a.B) * a.num_splits;
+    const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(kCtasPerSm) * sms));
+    return launch_dependent(mla_decode_kernel, dim3(grid), dim3(kThreads), kSmem, s, tckv, tkpe, a);
 }
 
 }  // namespace pkv

@@ -10,6 +10,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "pkv.h"
@@ -193,6 +194,30 @@ bool row16(const pkv_tensor& t, int outer) {
 }
 
 }  // namespace
+
+namespace pkv {
+
+cudaError_t device_sm_count(int* n) {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) {
+        const int v = cached[dev].load(std::memory_order_relaxed);
+        if (v > 0) {
+            *n = v;
+            return cudaSuccess;
+        }
+    }
+    int v = 0;
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) cached[dev].store(v, std::memory_order_relaxed);
+    *n = v;
+    return cudaSuccess;
+}
+
+}  // namespace pkv
 
 extern "C" {
 

@@ -185,6 +185,8 @@ cudaError_t launch_mla_decode(const MlaDecodeArgs& a, const CUtensorMap& tckv, c
                               cudaStream_t s);
 cudaError_t launch_mla_cache_write(const MlaWriteArgs& a, cudaStream_t s);
 int mla_decode_ctas_per_sm(int H);
+// Number of SMs of the current device (cached per device).
+cudaError_t device_sm_count(int* n);
 cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s);
 cudaError_t static_slot_bitmap(uint32_t** ptr, int64_t* words);
 cudaError_t launch_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int ctas, cudaStream_t s);

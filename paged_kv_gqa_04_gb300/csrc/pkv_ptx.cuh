@@ -114,6 +114,12 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int c0, in
                  "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
+// Prefetch `bytes` (a multiple of 16) of global memory from a 16-byte
+// aligned address into L2 (no completion).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void sts128(uint32_t addr, float a, float b, float c, float d) {
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
