@@ -533,6 +533,46 @@ def cpu_baseline(w, num_splits, seconds: float) -> dict:
                       f"new-token cache write, decode, merge; float64, single thread; cache prepared untimed"}
 
 
+_ALLCORE_BARRIER = None
+
+
+def _allcore_init(barrier):
+    global _ALLCORE_BARRIER
+    _ALLCORE_BARRIER = barrier
+
+
+def _allcore_worker(job):
+    """One host process of the all-core oracle baseline: prepare its slice of
+    the batch (untimed), wait for the others, then time whole steps."""
+    name, seqs, num_splits, seconds = job
+    from paged_kv_gqa_04_gb300 import synth
+    w = synth.make_mla_workload(name) if is_mla(name) else synth.make_workload(name)
+    run = oracle_step_timer(w, seqs, num_splits)
+    _ALLCORE_BARRIER.wait()
+    total, n = 0.0, 0
+    while total < seconds or n == 0:
+        total += run()
+        n += 1
+    return len(seqs) * n / total
+
+
+def cpu_baseline_allcore(name, B, num_splits, seconds: float) -> dict:
+    """The oracle on every host core: one process per core (spawned: this
+    process has initialised CUDA), the batch's sequences dealt round-robin,
+    all timed over the same window; throughput = the sum of the processes'."""
+    import multiprocessing as mp
+    procs = max(1, min(os.cpu_count() or 1, B))
+    groups = [list(range(i, B, procs)) for i in range(procs)]
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(procs)
+    with ctx.Pool(procs, initializer=_allcore_init, initargs=(barrier,)) as pool:
+        rates = pool.map(_allcore_worker, [(name, g, num_splits, seconds) for g in groups])
+    return {"value": sum(rates), "unit": UNIT, "cores": procs, "kind": "oracle",
+            "sample": f"{procs} processes, each its round-robin share of the {B} sequences, {num_splits} splits, "
+                      f"whole oracle decode steps (new-token write, decode, merge) for about {seconds:g} s; "
+                      f"float64, one thread each"}
+
+
 def run_reference(args, world, rank):
     """Reference arm: the float64 oracle timed on the host cores."""
     if rank != 0:
@@ -620,9 +660,10 @@ def main():
         for name in [x for x in args.also.split(",") if x]:
             others[name] = measure_decode_only(name, 0, 20, flush, peak)
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, dw.num_splits, args.cpu_seconds)
+        cpu_all = cpu_baseline_allcore(args.workload, w.B, dw.num_splits, args.cpu_seconds)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -666,6 +707,8 @@ def main():
         line["other_workloads"] = others
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if cpu_all is not None:
+        line["cpu_baseline_all_cores"] = cpu_all
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
