@@ -300,8 +300,9 @@ pkv_status pkv_mla_cache_write(const pkv_tensor* q_pe, const pkv_tensor* ckv, co
  * (empty split: 0 and -inf). pkv_lse_merge with D = 512 merges the splits.
  * Arithmetic: the tensor cores read the E4M3 cache bytes as they are, with
  * q_lat as two E4M3 terms under a per-head power-of-two scale (exact for
- * every value within 2^14 of the head's largest magnitude) and the softmax
- * weights as three E5M2 terms (about 10 significant bits); sums in float32.
+ * every value within 2^9 of the head's largest magnitude) and the softmax
+ * weights as three E5M2 terms that sum exactly to their f16 rounding; sums
+ * in float32.
  *
  * q_lat        [B, H, 512] bf16: the query already projected into the latent
  *              space; q_pe [B, H, 64] bf16, already rotated. Innermost stride

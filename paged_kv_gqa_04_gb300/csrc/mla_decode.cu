@@ -55,17 +55,19 @@
 // The operands, in FP8:
 //   Q8: q_lat = 2^-k_h (t1 + t2) per head h, t1 = E4M3(2^k_h q),
 //       t2 = E4M3(2^k_h q - t1), 2^k_h the largest power of two with
-//       2^k_h max|q_h| <= 448. A bf16 value has 8 significant bits and t1 4,
-//       so the remainder fits t2 exactly: the pair is q itself unless
-//       2^k_h |q| < 2^-6 (E4M3's subnormal range, a remainder error of at
-//       most 2^-10 2^-k_h). Rows 0-15 of Q8 are the t1 of heads 0-15, rows
-//       16-31 the t2; S = 2^-k_h (S[:, h] + S[:, 16 + h]).
-//   P8: the weight P = 2^(s - m) (<= 2^8, see below) as 2^7 P rounded to
-//       f16, split into three E5M2 terms by truncation (E5M2 is the high
-//       byte of an f16): e1 = hi(x), e2 = hi(x - e1), e3 = E5M2(x - e1 - e2),
-//       both subtractions exact; the three hold about 10 significant bits
-//       (f16: 11). Rows 16t + h of P8 hold term t of head h; O is the sum of
-//       the three 16-column groups, times 2^-7.
+//       2^k_h max|q_h| <= 448. A bf16 value has 8 significant bits and t1
+//       keeps 4, so t2 holds the rest exactly wherever its last bit is not
+//       below E4M3's smallest step 2^-9: for 2^k_h |q| >= 2^-2, i.e. every
+//       value within 2^9 of the head's largest; below, the error is at most
+//       2^-10 2^-k_h. Rows 0-15 of Q8 are the t1 of heads 0-15, rows 16-31
+//       the t2; S = 2^-k_h (S[:, h] + S[:, 16 + h]).
+//   P8: the weight P = 2^(s - m) (<= 2^8, see below) as x = 2^7 P rounded
+//       to f16, split into three E5M2 terms each rounded to nearest:
+//       e1 = E5M2(x), e2 = E5M2(x - e1), e3 = E5M2(x - e1 - e2) (E5M2 is the
+//       high byte of an f16: the remainders are f16, exact). For x >= 2^-6
+//       the three sum to x exactly (the weight's error is the f16 rounding,
+//       2^-11 relative); below, within 2^-17. Rows 16t + h of P8 hold term t
+//       of head h; O is the sum of the three 16-column groups, times 2^-7.
 //
 // The online softmax keeps a reference maximum m per head that moves only
 // when a chunk's maximum exceeds it by more than 8 (so P <= 2^8 and 2^7 P
@@ -616,15 +618,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         m[h] = cm[h];
                         pw[e] = p * kPScale;
                     }
-                    // three E5M2 terms of the pair (head 2 h2 in the low halves)
+                    // three E5M2 terms of the pair (head 2 h2 in the low
+                    // halves), each rounded to nearest; an E5M2 byte is the
+                    // high byte of an f16, so the remainders are f16 and exact
                     const uint32_t xw = pack_f16(pw[0], pw[1]);
-                    const uint32_t t1 = xw & 0xFF00FF00u;
-                    const uint32_t y = hsub2(xw, t1);
-                    const uint32_t t2 = y & 0xFF00FF00u;
-                    const uint32_t t3 = f16x2_to_e5m2x2(hsub2(y, t2));
-                    const uint32_t bytes[3][2] = {{(t1 >> 8) & 0xFFu, t1 >> 24},
-                                                  {(t2 >> 8) & 0xFFu, t2 >> 24},
-                                                  {t3 & 0xFFu, (t3 >> 8) & 0xFFu}};
+                    const uint32_t e1 = f16x2_to_e5m2x2(xw);
+                    const uint32_t y = hsub2(xw, prmt(e1, 0u, 0x1404u));
+                    const uint32_t e2 = f16x2_to_e5m2x2(y);
+                    const uint32_t e3 = f16x2_to_e5m2x2(hsub2(y, prmt(e2, 0u, 0x1404u)));
+                    const uint32_t bytes[3][2] = {{e1 & 0xFFu, (e1 >> 8) & 0xFFu},
+                                                  {e2 & 0xFFu, (e2 >> 8) & 0xFFu},
+                                                  {e3 & 0xFFu, (e3 >> 8) & 0xFFu}};
 #pragma unroll
                     for (int t = 0; t < 3; ++t)
 #pragma unroll
