@@ -434,12 +434,26 @@ pkv_status pkv_validate_indices_static(const pkv_tensor* block_tables, const pkv
 pkv_status pkv_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int32_t ctas,
                            pkv_stream_t stream);
 
+/*
+ * pkv_selftest_bounded_wait -- self-test of the bounded in-kernel waits
+ * behind PKV_FLAG_WAIT_TIMEOUT (a diagnostic; not one of the decode step's
+ * calls). One CTA waits on mbarriers that nothing completes: one warp gives
+ * up after about limit_ns and ORs PKV_FLAG_WAIT_TIMEOUT into *err_flag; a
+ * second warp, with a limit 100 times longer, stops on the first one's
+ * abort signal. elapsed_ns[0] and [1] receive the two waiting times. The
+ * GPU context stays usable afterwards.
+ * limit_ns: 100,000 .. 10,000,000 (0.1 .. 10 ms); err_flag: device int32
+ * (the caller zeroes it); elapsed_ns: device memory of two uint64 words.
+ */
+pkv_status pkv_selftest_bounded_wait(int64_t limit_ns, int32_t* err_flag, uint64_t* elapsed_ns,
+                                     pkv_stream_t stream);
+
 /* Static description of a status code. */
 const char* pkv_status_string(int32_t status);
 
 /* ABI version of this header (bumped on any signature change). */
 int32_t pkv_abi_version(void);
-#define PKV_ABI_VERSION 3
+#define PKV_ABI_VERSION 4
 
 #ifdef __cplusplus
 }

@@ -40,7 +40,8 @@ _CACHE_DTYPE = {"bf16": 0, "fp8": 1, "nvfp4": PKV_FP4_E2M1X2}
 EXPORTED = ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_choose_num_splits",
             "pkv_validate_indices", "pkv_status_string", "pkv_abi_version", "pkv_stream_read",
             "pkv_validate_indices_static", "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4",
-            "pkv_mla_cache_write", "pkv_paged_mla_decode", "pkv_choose_num_splits_mla")
+            "pkv_mla_cache_write", "pkv_paged_mla_decode", "pkv_choose_num_splits_mla",
+            "pkv_selftest_bounded_wait")
 
 
 class PkvTensor(ctypes.Structure):
@@ -79,13 +80,14 @@ def lib() -> ctypes.CDLL:
         L.pkv_choose_num_splits.argtypes = [i32, i32, i32, i32, ctypes.c_int64, i32, i32, i32]
         L.pkv_validate_indices.argtypes = [T, T, T, ctypes.c_int64, T, P, P]
         L.pkv_stream_read.argtypes = [P, ctypes.c_int64, P, i32, P]
+        L.pkv_selftest_bounded_wait.argtypes = [ctypes.c_int64, P, P, P]
         L.pkv_validate_indices_static.argtypes = [T, T, T, ctypes.c_int64, P, P]
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         for name in ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_validate_indices",
                      "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read", "pkv_validate_indices_static",
                      "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4", "pkv_mla_cache_write",
-                     "pkv_paged_mla_decode", "pkv_choose_num_splits_mla"):
+                     "pkv_paged_mla_decode", "pkv_choose_num_splits_mla", "pkv_selftest_bounded_wait"):
             getattr(L, name).restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -239,6 +241,16 @@ def validate_indices_static(block_tables, seq_lens, slot_mapping, num_pages: int
     _check("pkv_validate_indices_static", lib().pkv_validate_indices_static(
         _desc(block_tables), _desc(seq_lens), _desc(slot_mapping), int(num_pages), _ptr(err_flag),
         _stream(stream)))
+
+
+def selftest_bounded_wait(limit_ns: int, err_flag: torch.Tensor, elapsed_ns: torch.Tensor, stream=None) -> None:
+    """Self-test of the bounded in-kernel waits (pkv_selftest_bounded_wait):
+    err_flag an int32 device word, elapsed_ns two int64 device words."""
+    if not (err_flag.is_cuda and err_flag.dtype == torch.int32 and elapsed_ns.is_cuda
+            and elapsed_ns.dtype == torch.int64 and elapsed_ns.numel() >= 2):
+        raise ValueError("int32 device flag and two int64 device words expected")
+    _check("pkv_selftest_bounded_wait",
+           lib().pkv_selftest_bounded_wait(int(limit_ns), err_flag.data_ptr(), elapsed_ns.data_ptr(), _stream(stream)))
 
 
 def stream_read(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:

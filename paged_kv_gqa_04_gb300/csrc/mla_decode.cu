@@ -144,13 +144,7 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return umma_desc_sw1
 // Wait for a phase; false after about a second or once another role has
 // given up.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
-        if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
+    return mbar_wait_or_abort(bar, parity, abort_flag, kWaitLimitNs);
 }
 
 __device__ __forceinline__ float f16_lo(uint32_t w) {

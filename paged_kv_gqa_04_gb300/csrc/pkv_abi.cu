@@ -823,6 +823,13 @@ pkv_status pkv_validate_indices_static(const pkv_tensor* block_tables_p, const p
     return cuda_status(pkv::launch_validate(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_selftest_bounded_wait(int64_t limit_ns, int32_t* err_flag, uint64_t* elapsed_ns,
+                                     pkv_stream_t stream) {
+    if (limit_ns < 100000 || limit_ns > 10000000 || !err_flag || !elapsed_ns) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_selftest_wait(static_cast<uint64_t>(limit_ns), err_flag, elapsed_ns,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int32_t ctas, pkv_stream_t stream) {
     if (bytes < 0 || bytes % 16 != 0 || ctas < 1 || ctas > 65535) return PKV_ERR_INVALID_ARG;
     if (bytes == 0) return PKV_OK;

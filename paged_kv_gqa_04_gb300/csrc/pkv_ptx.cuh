@@ -74,6 +74,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// As mbar_wait_bounded, but also gives up as soon as *abort_flag is set
+// (another part of the CTA has given up); each retry suspends for at most
+// 20 us, so both conditions are checked at least that often.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                                   uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Programmatic dependent launch: wait until the preceding grid in the
 // stream has completed and its writes are visible (a no-op when the kernel
 // was not launched as a programmatic dependent), and let the following grid

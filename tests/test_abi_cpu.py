@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pkv_abi_version() == 3
+    assert lib.pkv_abi_version() == 4
     for s in range(4):
         assert pkv.status_string(s)
     assert "invalid" in pkv.status_string(1)
@@ -211,3 +211,10 @@ def test_split_heuristic(lib):
     assert pkv.choose_num_splits(1, 1, 1, 128, 1, 1, "bf16", sms) == 1
     # never more splits than pages
     assert pkv.choose_num_splits(1, 1, 8, 128, 3, 3, "bf16", sms) <= 3
+
+
+def test_selftest_bounded_wait_rejects_bad_limits():
+    from paged_kv_gqa_04_gb300 import _abi
+    lib = _abi.lib()
+    for limit in (0, 99_999, 10_000_001):
+        assert lib.pkv_selftest_bounded_wait(limit, None, None, None) == _abi.PKV_ERR_INVALID_ARG
