@@ -119,7 +119,9 @@ constexpr int kRedBytes = 4 * kN * 4;                 // [4 warps][16 heads] flo
 constexpr int kOffMax = kOffP + kPBytes;              // per-warp chunk maxima
 constexpr int kOffSum = kOffMax + kRedBytes;          // per-warp sums
 constexpr int kOffQs = kOffSum + kRedBytes;           // [16] floats: ckv_scale 2^-k_h
-constexpr int kOffBar = kOffQs + kN * 4;
+constexpr int kSortMaxB = 64;                         // batches ordered by length up to this size
+constexpr int kOffOrder = kOffQs + kN * 4;            // [64] int16: sequences, longest first
+constexpr int kOffBar = kOffOrder + kSortMaxB * 2;
 enum : int { bFull = 0, bFree, bSFull, bPFull, bOFull, bQFull, kNumBars };
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;      // tensor-memory base, abort flag
 constexpr int kSmem = kOffMisc + 16 + 1024;           // + alignment slack
@@ -145,13 +147,6 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return umma_desc_sw1
 // given up.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
     return mbar_wait_or_abort(bar, parity, abort_flag, kWaitLimitNs);
-}
-
-__device__ __forceinline__ float f16_lo(uint32_t w) {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
-}
-__device__ __forceinline__ float f16_hi(uint32_t w) {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 
 // One work item: split s of sequence b (items are numbered b * S + s).
@@ -190,25 +185,42 @@ __device__ __forceinline__ int page_of(const Item& x, int pg, int64_t num_pages)
     return (pid >= 0 && pid < num_pages) ? pid : -1;
 }
 
-// Position in this CTA's sequence of chunks: chunk c of its item `it`
+// The CTA's j-th item (n_items past the end). Schedule positions are dealt
+// to the CTAs in rounds of gridDim.x. Without an order (batches above
+// kSortMaxB) position p is item p, so CTA k takes k, k + G, k + 2G, ...
+// With one, the positions walk the sequences longest first (each one's
+// splits in turn) and every other round is dealt in reverse, so a CTA that
+// drew one of the longest splits draws one of the shortest next.
+__device__ __forceinline__ int slot_item(const MlaDecodeArgs& a, const int16_t* order, int j, int n_items) {
+    const int G = gridDim.x, k = blockIdx.x;
+    const int64_t p = static_cast<int64_t>(j) * G + ((order != nullptr && (j & 1)) ? G - 1 - k : k);
+    if (p >= n_items) return n_items;  // only the last round is partial: nothing follows
+    if (order == nullptr) return static_cast<int>(p);
+    const int r = static_cast<int>(p) / a.num_splits;
+    return order[r] * a.num_splits + (static_cast<int>(p) - r * a.num_splits);
+}
+
+// Position in this CTA's sequence of chunks: chunk c of its j-th item `it`
 // (it >= n_items: past the end). Items without tokens are skipped.
 struct Cursor {
+    int j;
     int it;
     int c;
     Item x;
 };
-__device__ __forceinline__ void settle(const MlaDecodeArgs& a, Cursor& u, int n_items) {
+__device__ __forceinline__ void settle(const MlaDecodeArgs& a, const int16_t* order, Cursor& u, int n_items) {
     u.c = 0;
-    while (u.it < n_items) {
+    for (;; ++u.j) {
+        u.it = slot_item(a, order, u.j, n_items);
+        if (u.it >= n_items) return;
         u.x = item_of(a, u.it);
         if (u.x.nch > 0) return;
-        u.it += gridDim.x;
     }
 }
-__device__ __forceinline__ void step(const MlaDecodeArgs& a, Cursor& u, int n_items) {
+__device__ __forceinline__ void step(const MlaDecodeArgs& a, const int16_t* order, Cursor& u, int n_items) {
     if (++u.c >= u.x.nch) {
-        u.it += gridDim.x;
-        settle(a, u, n_items);
+        ++u.j;
+        settle(a, order, u, n_items);
     }
 }
 
@@ -246,10 +258,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    // The schedule order: sequences by page count, longest first, ties by
+    // index (index inputs only, read before the grid-dependency wait like
+    // the L2 read-ahead below).
+    int16_t* order_tab = reinterpret_cast<int16_t*>(smem + kOffOrder);
+    if (warp == kWarpCopy && a.B <= kSortMaxB) {
+        const int cap = a.max_pages * kMlaPage;
+        int key[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int b = lane + 32 * t;
+            key[t] = b < a.B ? (min(max(__ldg(a.seq_lens + b), 0), cap) + kMlaPage - 1) / kMlaPage : -1;
+        }
+        int rank[2] = {0, 0};
+        for (int b2 = 0; b2 < a.B; ++b2) {
+            const int kb = __shfl_sync(0xffffffffu, b2 < 32 ? key[0] : key[1], b2 & 31);
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                rank[t] += (kb > key[t] || (kb == key[t] && b2 < lane + 32 * t)) ? 1 : 0;
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+            if (lane + 32 * t < a.B) order_tab[rank[t]] = static_cast<int16_t>(lane + 32 * t);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int16_t* order = a.B <= kSortMaxB ? order_tab : nullptr;
 
     // L2 read-ahead of one chunk (lanes 0-4: its first page, 8-12: second)
     auto prefetch_at = [&](const Cursor& u) {
@@ -280,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // still run (a prefetch loads nothing into this CTA; the index inputs
     // are this call's own).
     Cursor cur;
-    cur.it = blockIdx.x;
+    cur.j = 0;
     if (warp == kWarpCopy) {
-        settle(a, cur, n_items);
+        settle(a, order, cur, n_items);
         prefetch_at(cur);
         prefetch_q(cur.it);
     }
@@ -307,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const uint64_t policy = l2_policy_evict_first();
         Cursor pf = cur;  // the L2 read-ahead, kPrefetch chunks ahead of the copy
         int g = 0, issued = 0;  // chunks of this CTA whose copies were started
-        for (; cur.it < n_items; step(a, cur, n_items), ++g) {
+        for (; cur.it < n_items; step(a, order, cur, n_items), ++g) {
             if (g >= 1 && !warp_wait(bar(bFree), (g - 1) & 1)) break;  // chunk g - 1's P . V is done
             const int pa = 2 * cur.c, pb = pa + 1;
             const int ida = page_of(cur.x, pa, num_pages), idb = page_of(cur.x, pb, num_pages);
@@ -332,18 +368,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
             __syncwarp();
             issued = g + 1;
-            if (cur.c == 0) prefetch_q(cur.it + gridDim.x);  // the next item's queries
+            if (cur.c == 0) prefetch_q(slot_item(a, order, cur.j + 1, n_items));  // the next item's queries
             if (g == 0) {
                 // Every CTA's first chunk is requested before any read-ahead,
                 // so none waits behind the other CTAs' later chunks.
-                step(a, pf, n_items);
+                step(a, order, pf, n_items);
                 if (pf.it < n_items && !warp_wait(fb, 0)) break;
                 for (int k = 1; k <= kPrefetch; ++k) {
                     prefetch_at(pf);
-                    if (k < kPrefetch) step(a, pf, n_items);
+                    if (k < kPrefetch) step(a, order, pf, n_items);
                 }
             } else {
-                step(a, pf, n_items);
+                step(a, order, pf, n_items);
                 prefetch_at(pf);
             }
         }
@@ -391,7 +427,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         };
         bool ok = true;
         int g = 0, n_ne = 0;  // chunks, items with tokens
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        for (int j = 0; ok; ++j) {
+            const int it = slot_item(a, order, j, n_items);
+            if (it >= n_items) break;
             const Item x = item_of(a, it);
             if (x.nch == 0) continue;
             ok = warp_wait(bar(bQFull), n_ne & 1);  // the item's queries are staged
@@ -417,84 +455,126 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const float sl = a.scale_log2;
         // The item's queries as FP8 / bf16 B operands (Q8 is free: the last
         // scores that read it are complete), then one arrival per warp.
+        // Warp q stages heads 4q .. 4q + 3; lane l holds latent values
+        // 8l .. 8l + 7 and 256 + 8l .. 256 + 8l + 7 of each, so every load
+        // reads whole 512-byte stretches of a row.
+        const bool ql_vec = ((reinterpret_cast<uintptr_t>(a.q_lat) | static_cast<uintptr_t>(a.ql_s0 * 2) |
+                              static_cast<uintptr_t>(a.ql_s1 * 2)) & 15) == 0;
+        const bool qp_vec = ((reinterpret_cast<uintptr_t>(a.q_pe) | static_cast<uintptr_t>(a.qp_s0 * 2) |
+                              static_cast<uintptr_t>(a.qp_s1 * 2)) & 15) == 0;
         auto stage_q = [&](const Item& x) {
-            const int h = i >> 3, p = i & 7;  // head, 64-value part
-            const bool live = h < H;
-            const uint32_t* ql = reinterpret_cast<const uint32_t*>(a.q_lat + x.b * a.ql_s0 + h * a.ql_s1 + 64 * p);
-            uint32_t w[32];  // the 64 values, loaded at once
+            uint4 w[4][2];  // [head][piece]: eight bf16 values each, all loads in flight at once
 #pragma unroll
-            for (int k = 0; k < 32; ++k) w[k] = live ? __ldg(ql + k) : 0u;
-            float mx = 0.f;
+            for (int hh = 0; hh < 4; ++hh) {
+                const int h = 4 * q + hh;
+                const uint16_t* row = a.q_lat + x.b * a.ql_s0 + h * a.ql_s1 + 8 * lane;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            // 2^k with 2^k mx in (224, 448] (k = 0 for an all-zero head)
-            int k = 0;
-            if (mx > 0.f) {
-                const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
-                k = min(max(8 - e, -126), 126);
-                if (mx * __uint_as_float(static_cast<uint32_t>(k + 127) << 23) > 448.f) --k;
+                for (int pc = 0; pc < 2; ++pc) {
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (h < H) {
+                        if (ql_vec) {
+                            v = ldg_nc128(row + 256 * pc);
+                        } else {
+                            const uint32_t* r32 = reinterpret_cast<const uint32_t*>(row + 256 * pc);
+                            v = make_uint4(__ldg(r32), __ldg(r32 + 1), __ldg(r32 + 2), __ldg(r32 + 3));
+                        }
+                    }
+                    w[hh][pc] = v;
+                }
             }
-            const float sc = __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
-            if (p == 0) reinterpret_cast<float*>(smem + kOffQs)[h] = cks / sc;
-            // values 64p .. 64p + 63: block p / 2, 16-byte chunks 4 (p % 2) + 0..3
+            {  // q_pe: lane l holds 16 bytes (part l % 8) of head 4q + l / 8
+                const int h = 4 * q + (lane >> 3), p = lane & 7;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (h < H) {
+                    const uint16_t* src = a.q_pe + x.b * a.qp_s0 + h * a.qp_s1 + 8 * p;
+                    if (qp_vec) {
+                        v = ldg_nc128(src);
+                    } else {
+                        const uint32_t* r32 = reinterpret_cast<const uint32_t*>(src);
+                        v = make_uint4(__ldg(r32), __ldg(r32 + 1), __ldg(r32 + 2), __ldg(r32 + 3));
+                    }
+                }
+                sts128u(s0 + kOffQp + h * 128 + ((p ^ (h & 7)) << 4), v.x, v.y, v.z, v.w);
+            }
+            float qsv[4];
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t t1w[4], t2w[4];
+            for (int hh = 0; hh < 4; ++hh) {
+                const int h = 4 * q + hh;
+                float mx = 0.f;
 #pragma unroll
-                for (int m4 = 0; m4 < 4; ++m4) {
-                    uint32_t b1 = 0u, b2 = 0u;
+                for (int pc = 0; pc < 2; ++pc) {
+                    const uint32_t u[4] = {w[hh][pc].x, w[hh][pc].y, w[hh][pc].z, w[hh][pc].w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(u[m])), fabsf(bf16_hi(u[m]))));
+                }
+                mx = warp_max(mx);
+                // 2^k with 2^k mx in (224, 448] (k = 0 for an all-zero head)
+                int k = 0;
+                if (mx > 0.f) {
+                    const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
+                    k = min(max(8 - e, -126), 126);
+                    if (mx * __uint_as_float(static_cast<uint32_t>(k + 127) << 23) > 448.f) --k;
+                }
+                const float sc = __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+                qsv[hh] = cks / sc;
+                // Two E4M3 terms through f16: every scaled value at or above
+                // 2^-17 is exact in f16 and those below round to zero in both
+                // terms either way, so the bytes are those of the exact split.
+#pragma unroll
+                for (int pc = 0; pc < 2; ++pc) {
+                    const uint32_t u[4] = {w[hh][pc].x, w[hh][pc].y, w[hh][pc].z, w[hh][pc].w};
+                    uint32_t t1[2], t2[2];
 #pragma unroll
                     for (int m2 = 0; m2 < 2; ++m2) {
-                        const uint32_t w2 = w[8 * ch + 2 * m4 + m2];
-                        const float x0 = bf16_lo(w2) * sc, x1 = bf16_hi(w2) * sc;
-                        const uint32_t e1 = f32x2_to_e4m3x2(x1, x0);
-                        const uint32_t h1 = e4m3x2_to_f16x2(static_cast<uint16_t>(e1));
-                        const uint32_t e2 = f32x2_to_e4m3x2(x1 - f16_hi(h1), x0 - f16_lo(h1));
-                        b1 |= e1 << (16 * m2);
-                        b2 |= e2 << (16 * m2);
-                    }
-                    t1w[m4] = b1;
-                    t2w[m4] = b2;
-                }
-                const int blk = p >> 1, chunk = 4 * (p & 1) + ch;
-                sts128u(s0 + kOffQ + blk * kQBlock + h * 128 + ((chunk ^ (h & 7)) << 4), t1w[0], t1w[1], t1w[2],
-                        t1w[3]);
-                sts128u(s0 + kOffQ + blk * kQBlock + (16 + h) * 128 + ((chunk ^ ((16 + h) & 7)) << 4), t2w[0],
-                        t2w[1], t2w[2], t2w[3]);
-            }
-            const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q_pe + x.b * a.qp_s0 + h * a.qp_s1 + 8 * p);
-            uint32_t v[4];
+                        uint32_t b1 = 0u, b2 = 0u;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) v[m] = live ? __ldg(qp + m) : 0u;
-            sts128u(s0 + kOffQp + h * 128 + ((p ^ (h & 7)) << 4), v[0], v[1], v[2], v[3]);
+                        for (int m = 0; m < 2; ++m) {
+                            const uint32_t xw = pack_f16(bf16_lo(u[2 * m2 + m]) * sc, bf16_hi(u[2 * m2 + m]) * sc);
+                            const uint32_t e1 = f16x2_to_e4m3x2(xw);
+                            const uint32_t e2 = f16x2_to_e4m3x2(hsub2(xw, e4m3x2_to_f16x2(static_cast<uint16_t>(e1))));
+                            b1 |= e1 << (16 * m);
+                            b2 |= e2 << (16 * m);
+                        }
+                        t1[m2] = b1;
+                        t2[m2] = b2;
+                    }
+                    // values 256 pc + 8 lane ..: block 2 pc + lane / 16, 16-byte
+                    // chunk (lane % 16) / 2, its half lane % 2
+                    const int blk = 2 * pc + (lane >> 4), chunk = (lane & 15) >> 1;
+                    const uint32_t base = s0 + kOffQ + blk * kQBlock + 8 * (lane & 1);
+                    sts64u(base + h * 128 + ((chunk ^ (h & 7)) << 4), t1[0], t1[1]);
+                    sts64u(base + (16 + h) * 128 + ((chunk ^ (h & 7)) << 4), t2[0], t2[1]);
+                }
+            }
+            if (lane == 0) sts128(s0 + kOffQs + 16 * q, qsv[0], qsv[1], qsv[2], qsv[3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bQFull));
         };
         // every warp's part of the per-head scales (ckv_scale 2^-k_h) is written
         auto load_qs = [&]() { named_bar_and(1, 128, true); };
-        // the first item with tokens from `it` on; splits without tokens on
-        // the way get their (0, -inf) records
-        auto next_item = [&](int it) -> int {
-            for (; it < n_items; it += gridDim.x) {
+        // the slot of the first item with tokens from slot j on (past the
+        // end if none); splits without tokens on the way get their
+        // (0, -inf) records
+        auto next_item = [&](int j) -> int {
+            for (;; ++j) {
+                const int it = slot_item(a, order, j, n_items);
+                if (it >= n_items) return j;
                 const Item y = item_of(a, it);
                 if (i == 0 && y.s == 0 && y.bad_len) flag_error(a.err, PKV_FLAG_SEQ_LEN_RANGE);
-                if (y.nch > 0) return it;
+                if (y.nch > 0) return j;
                 float* op = a.out_partial + y.b * a.op_s0 + y.s * a.op_s1;
                 for (int k = i; k < H * kMlaDc; k += 128) op[(k / kMlaDc) * a.op_s2 + (k % kMlaDc)] = 0.f;
                 if (i < H) a.lse_partial[y.b * a.lp_s0 + y.s * a.lp_s1 + i] = -INFINITY;
             }
-            return it;
         };
 
         const int tok = 32 * q + lane;  // token of the chunk = tensor-memory lane
         // The four warps pass the same named barriers and decide whether to
         // go on by the barrier's AND, so all of them stop at the same chunk.
         bool ok = true;
-        int it = next_item(blockIdx.x);
+        int js = next_item(0);  // schedule slot of the current item
+        int it = slot_item(a, order, js, n_items);
         Item x;
         if (it < n_items) {
             x = item_of(a, it);
@@ -639,7 +719,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (!ok) break;
             // The next item's queries first: its scores then overlap this
             // item's epilogue (Q8 is free: this item's last scores are done).
-            const int nxt = next_item(it + gridDim.x);
+            const int nj = next_item(js + 1);
+            const int nxt = slot_item(a, order, nj, n_items);
             Item y;
             if (nxt < n_items) {
                 y = item_of(a, nxt);
@@ -647,15 +728,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
             // ---- epilogue: l over the tokens of the four warps, O / l ---------------
             const bool got_o = warp_wait(bar(bOFull), (g - 1) & 1);  // the item's last P . V
+            // l over the warp's 32 tokens by recursive halving: each step
+            // hands half of the heads still held to the partner lane, so
+            // lanes 2k and 2k + 1 end with head 8 b4 + 4 b3 + 2 b2 + b1 of
+            // lane 2k (b_j: bit j of the lane).
+            float lr[kN / 2];
+            {
+                const bool u4 = lane & 16;
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
+                for (int j = 0; j < 8; ++j)
+                    lr[j] = (u4 ? l[j + 8] : l[j]) + __shfl_xor_sync(0xffffffffu, u4 ? l[j] : l[j + 8], 16);
+                const bool u3 = lane & 8;
 #pragma unroll
-                for (int h = 0; h < kN; ++h) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+                for (int j = 0; j < 4; ++j)
+                    lr[j] = (u3 ? lr[j + 4] : lr[j]) + __shfl_xor_sync(0xffffffffu, u3 ? lr[j] : lr[j + 4], 8);
+                const bool u2 = lane & 4;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    lr[j] = (u2 ? lr[j + 2] : lr[j]) + __shfl_xor_sync(0xffffffffu, u2 ? lr[j] : lr[j + 2], 4);
+                const bool u1 = lane & 2;
+                lr[0] = (u1 ? lr[1] : lr[0]) + __shfl_xor_sync(0xffffffffu, u1 ? lr[0] : lr[1], 2);
+                lr[0] += __shfl_xor_sync(0xffffffffu, lr[0], 1);
+            }
             const uint32_t lred = s0 + kOffSum;
-            if (lane == 0)
-#pragma unroll
-                for (int h4 = 0; h4 < kN / 4; ++h4)
-                    sts128(lred + (q * kN + 4 * h4) * 4, l[4 * h4], l[4 * h4 + 1], l[4 * h4 + 2], l[4 * h4 + 3]);
+            if ((lane & 1) == 0) {
+                const int hl = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(lred + (q * kN + hl) * 4), "f"(lr[0]) : "memory");
+            }
             ok = named_bar_and(1, 128, got_o);
             if (!ok) break;
 #pragma unroll
@@ -685,24 +784,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             float* outp = a.out_partial + x.b * a.op_s0 + x.s * a.op_s1;
             tc_fence_after();
 #pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r0[16], r1[16], r2[16];
-                const uint32_t ta = tmem + lane_base + kColO + 48 * j;
-                tmem_ld16(ta, r0);
-                tmem_ld16(ta + 16, r1);
-                tmem_ld16(ta + 32, r2);
+            for (int j2 = 0; j2 < 2; ++j2) {  // two 128-row blocks of O per tensor-memory wait
+                uint32_t r[6][16];
+                const uint32_t ta = tmem + lane_base + kColO + 96 * j2;
+#pragma unroll
+                for (int t = 0; t < 6; ++t) tmem_ld16(ta + 16 * t, r[t]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < kN; ++h)
-                    if (h < H)
-                        outp[h * a.op_s2 + 128 * j + 32 * q + lane] =
-                            (__uint_as_float(r0[h]) + __uint_as_float(r1[h]) + __uint_as_float(r2[h])) * inv[h];
+                for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                    for (int h = 0; h < kN; ++h)
+                        if (h < H)
+                            outp[h * a.op_s2 + 128 * (2 * j2 + jj) + 32 * q + lane] =
+                                (__uint_as_float(r[3 * jj][h]) + __uint_as_float(r[3 * jj + 1][h]) +
+                                 __uint_as_float(r[3 * jj + 2][h])) *
+                                inv[h];
             }
             // O is read (waited above) before this warp's next P hand-off,
             // which is what lets the next item's P . V overwrite it.
             tc_fence_before();
             if (nxt < n_items) load_qs();
             it = nxt;
+            js = nj;
             x = y;
         }
     }
@@ -727,8 +830,8 @@ cudaError_t launch_mla_decode(const MlaDecodeArgs& a, const CUtensorMap& tckv, c
     int sms = 0;
     e = device_sm_count(&sms);
     if (e != cudaSuccess) return e;
-    // persistent: at most two CTAs per SM, each taking items blockIdx.x,
-    // blockIdx.x + gridDim.x, ...
+    // persistent: at most two CTAs per SM, each taking one item of every
+    // round of gridDim.x schedule positions
     const int64_t items = static_cast<int64_t>(a.B) * a.num_splits;
     const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(kCtasPerSm) * sms));
     return launch_dependent(mla_decode_kernel, dim3(grid), dim3(kThreads), kSmem, s, tckv, tkpe, a);

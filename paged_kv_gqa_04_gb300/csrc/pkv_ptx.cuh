@@ -408,6 +408,15 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+__device__ __forceinline__ void sts64u(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+// 16 bytes from global memory through the read-only path (16-byte aligned).
+__device__ __forceinline__ uint4 ldg_nc128(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
 __device__ __forceinline__ void sts8(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -423,6 +432,13 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float hi, float lo) {
 __device__ __forceinline__ uint32_t f16x2_to_e5m2x2(uint32_t h) {
     uint16_t r;
     asm("cvt.rn.satfinite.e5m2x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    return r;
+}
+// f16x2 to two E4M3 bytes (high half -> high byte), round to nearest even,
+// saturating to +-448.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
     return r;
 }
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {

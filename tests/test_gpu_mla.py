@@ -116,3 +116,38 @@ def test_mla_bad_page_and_seq_len_are_flagged():
     torch.cuda.synchronize()
     assert int(dw.err.item()) & _abi.FLAG_SEQ_LEN_RANGE
     assert torch.isfinite(dw.out_partial).all()
+
+
+@pytest.mark.parametrize("pad_lat,pad_pe", [(2, 0), (0, 2), (2, 2)])
+def test_mla_padded_query_rows(pad_lat, pad_pe):
+    """Query rows padded by two elements are 4-byte but not 16-byte aligned,
+    which sends the kernel's query staging to its word-load path: the
+    partial outputs equal those of contiguous queries bit for bit (and the
+    oracle, checked on the contiguous run)."""
+    w = synth.custom_mla_workload("padded_q", 305, [300, 129, 64], 12)
+    dw = harness.MlaDeviceWorkload(w, num_splits=2)
+    dw.fill()
+    dw.upload_decode()
+    dw.step()
+    torch.cuda.synchronize()
+    _compare(w, dw, mla_oracle_step(w, num_splits=2), list(range(w.B)))
+    op0, lp0 = dw.out_partial.clone(), dw.lse_partial.clone()
+
+    def padded(t, pad):
+        if pad == 0:
+            return t
+        p = torch.zeros(*t.shape[:-1], t.shape[-1] + pad, dtype=t.dtype, device=t.device)
+        p[..., :t.shape[-1]] = t
+        return p[..., :t.shape[-1]]
+
+    ql, qp = dw.decode_inputs["q_lat"], dw.decode_inputs["q"]  # q_pe as rotated by the write
+    dw.decode_inputs["q_lat"] = padded(ql, pad_lat)
+    q_pe = padded(qp, pad_pe)
+    assert dw.decode_inputs["q_lat"].stride(1) % 8 == pad_lat % 8 and q_pe.stride(1) % 8 == pad_pe % 8
+    dw.out_partial.fill_(float("nan"))
+    dw.lse_partial.fill_(float("nan"))
+    dw.decode(q_pe)
+    torch.cuda.synchronize()
+    dw.decode_inputs["q_lat"] = ql
+    assert torch.equal(dw.out_partial, op0) and torch.equal(dw.lse_partial, lp0)
+    assert int(dw.err.item()) == 0
