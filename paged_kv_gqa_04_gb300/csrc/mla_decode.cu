@@ -224,6 +224,24 @@ __device__ __forceinline__ void step(const MlaDecodeArgs& a, const int16_t* orde
     }
 }
 
+// NH columns (one per head) of a warp's tensor-memory lanes: the heads the
+// softmax warps handle, 8 when H <= 8, else 16.
+template <int NH>
+__device__ __forceinline__ void tmem_ld_heads(uint32_t t, uint32_t (&r)[NH]) {
+    if constexpr (NH == 16)
+        tmem_ld16(t, r);
+    else
+        tmem_ld8(t, r);
+}
+template <int NH>
+__device__ __forceinline__ void tmem_st_heads(uint32_t t, const uint32_t (&r)[NH]) {
+    if constexpr (NH == 16)
+        tmem_st16(t, r);
+    else
+        tmem_st8(t, r);
+}
+
+template <int NH>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tckv, const __grid_constant__ CUtensorMap tkpe,
                       const MlaDecodeArgs a) {
@@ -573,6 +591,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // The four warps pass the same named barriers and decide whether to
         // go on by the barrier's AND, so all of them stop at the same chunk.
         bool ok = true;
+        if (NH < kN) {  // P8 rows of heads NH..15 are never written: P . V reads them as zeros
+            for (int k = i; k < kPBytes / 16; k += 128) sts128u(s0 + kOffP + 16 * k, 0u, 0u, 0u, 0u);
+        }
         int js = next_item(0);  // schedule slot of the current item
         int it = slot_item(a, order, js, n_items);
         Item x;
@@ -583,27 +604,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         int g = 0;  // chunks of this CTA
         while (it < n_items && ok) {
-            float m[kN], l[kN];  // reference maximum (log2 units), this thread's part of the sum
+            float m[NH], l[NH];  // reference maximum (log2 units), this thread's part of the sum
 #pragma unroll
-            for (int h = 0; h < kN; ++h) {
+            for (int h = 0; h < NH; ++h) {
                 m[h] = -INFINITY;
                 l[h] = 0.f;
             }
             for (int c = 0; c < x.nch; ++c, ++g) {
                 const bool got = warp_wait(bar(bSFull), g & 1);
                 const bool live = page_of(x, 2 * c + (tok >> 6), num_pages) >= 0 && tok < x.ntok - kT * c;
-                float sv[kN], cm[kN];
+                float sv[NH], cm[NH];
                 const uint32_t red = s0 + kOffMax;
                 if (got) {
                     tc_fence_after();
-                    uint32_t r1[16], r2[16], rp[16];
+                    uint32_t r1[NH], r2[NH], rp[NH];
                     const uint32_t ta = tmem + lane_base + kColS;
-                    tmem_ld16(ta, r1);
-                    tmem_ld16(ta + 16, r2);
-                    tmem_ld16(ta + 32, rp);
+                    tmem_ld_heads<NH>(ta, r1);
+                    tmem_ld_heads<NH>(ta + 16, r2);
+                    tmem_ld_heads<NH>(ta + 32, rp);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int h4 = 0; h4 < kN / 4; ++h4) {
+                    for (int h4 = 0; h4 < NH / 4; ++h4) {
                         const float4 qs = lds128f(s0 + kOffQs + 16 * h4);
                         const float qv[4] = {qs.x, qs.y, qs.z, qs.w};
 #pragma unroll
@@ -615,10 +636,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         }
                     }
 #pragma unroll
-                    for (int h = 0; h < kN; ++h) cm[h] = warp_max(cm[h]);
+                    for (int h = 0; h < NH; ++h) cm[h] = warp_max(cm[h]);
                     if (lane == 0)
 #pragma unroll
-                        for (int h4 = 0; h4 < kN / 4; ++h4)
+                        for (int h4 = 0; h4 < NH / 4; ++h4)
                             sts128(red + (q * kN + 4 * h4) * 4, cm[4 * h4], cm[4 * h4 + 1], cm[4 * h4 + 2],
                                    cm[4 * h4 + 3]);
                 }
@@ -627,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                 for (int w = 0; w < 4; ++w)
 #pragma unroll
-                    for (int h4 = 0; h4 < kN / 4; ++h4) {
+                    for (int h4 = 0; h4 < NH / 4; ++h4) {
                         const float4 y = lds128f(red + (w * kN + 4 * h4) * 4);
                         if (w == 0) {
                             cm[4 * h4] = y.x;
@@ -647,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 // scaled before P . V.
                 bool scale_o = false;
 #pragma unroll
-                for (int h = 0; h < kN; ++h) {
+                for (int h = 0; h < NH; ++h) {
                     const bool move = cm[h] > m[h] + kRescaleLog2 || (m[h] == -INFINITY && cm[h] > -INFINITY);
                     cm[h] = move ? cm[h] : m[h];  // cm: the new reference
                     scale_o |= move && m[h] > -INFINITY;
@@ -657,19 +678,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (scale_o) {
 #pragma unroll 1
                     for (int j = 0; j < 12; ++j) {  // 4 blocks x 3 terms
-                        uint32_t r[16];
+                        uint32_t r[NH];
                         const uint32_t ta = tmem + lane_base + kColO + 16 * j;
-                        tmem_ld16(ta, r);
+                        tmem_ld_heads<NH>(ta, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int h = 0; h < kN; ++h)
+                        for (int h = 0; h < NH; ++h)
                             r[h] = __float_as_uint(__uint_as_float(r[h]) *
                                                    (m[h] == cm[h] ? 1.f : fast_exp2(m[h] - cm[h])));
-                        tmem_st16(ta, r);
+                        tmem_st_heads<NH>(ta, r);
                     }
                     tmem_wait_st();
 #pragma unroll
-                    for (int h = 0; h < kN; ++h) l[h] *= m[h] == cm[h] ? 1.f : fast_exp2(m[h] - cm[h]);
+                    for (int h = 0; h < NH; ++h) l[h] *= m[h] == cm[h] ? 1.f : fast_exp2(m[h] - cm[h]);
                 }
                 const uint32_t sb = s0 + kOffSlot;
                 if (!live) {  // zero weight: make the ckv row exact zeros for P . V
@@ -682,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const uint32_t pb = s0 + kOffP;
                 const uint32_t colx = static_cast<uint32_t>((tok >> 4) << 4);  // the token's 16-byte chunk, unswizzled
 #pragma unroll
-                for (int h2 = 0; h2 < kN / 2; ++h2) {
+                for (int h2 = 0; h2 < NH / 2; ++h2) {
                     float pw[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -729,71 +750,68 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // ---- epilogue: l over the tokens of the four warps, O / l ---------------
             const bool got_o = warp_wait(bar(bOFull), (g - 1) & 1);  // the item's last P . V
             // l over the warp's 32 tokens by recursive halving: each step
-            // hands half of the heads still held to the partner lane, so
-            // lanes 2k and 2k + 1 end with head 8 b4 + 4 b3 + 2 b2 + b1 of
-            // lane 2k (b_j: bit j of the lane).
-            float lr[kN / 2];
-            {
-                const bool u4 = lane & 16;
+            // hands half of the heads still held to the partner lane (which
+            // keeps the upper half adds n/2 to its head), then the lanes left
+            // holding the same head add up; lane 32/NH k ends with head k'.
+            float lr[NH];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    lr[j] = (u4 ? l[j + 8] : l[j]) + __shfl_xor_sync(0xffffffffu, u4 ? l[j] : l[j + 8], 16);
-                const bool u3 = lane & 8;
+            for (int h = 0; h < NH; ++h) lr[h] = l[h];
+            int hl = 0;  // the head this lane ends with
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    lr[j] = (u3 ? lr[j + 4] : lr[j]) + __shfl_xor_sync(0xffffffffu, u3 ? lr[j] : lr[j + 4], 8);
-                const bool u2 = lane & 4;
+            for (int n = NH, off = 16; n > 1; n >>= 1, off >>= 1) {
+                const bool up = lane & off;
+                hl += up ? n / 2 : 0;
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    lr[j] = (u2 ? lr[j + 2] : lr[j]) + __shfl_xor_sync(0xffffffffu, u2 ? lr[j] : lr[j + 2], 4);
-                const bool u1 = lane & 2;
-                lr[0] = (u1 ? lr[1] : lr[0]) + __shfl_xor_sync(0xffffffffu, u1 ? lr[0] : lr[1], 2);
-                lr[0] += __shfl_xor_sync(0xffffffffu, lr[0], 1);
+                for (int j = 0; j < n / 2; ++j)
+                    lr[j] = (up ? lr[j + n / 2] : lr[j]) +
+                            __shfl_xor_sync(0xffffffffu, up ? lr[j] : lr[j + n / 2], off);
             }
+#pragma unroll
+            for (int off = 16 / NH; off >= 1; off >>= 1) lr[0] += __shfl_xor_sync(0xffffffffu, lr[0], off);
             const uint32_t lred = s0 + kOffSum;
-            if ((lane & 1) == 0) {
-                const int hl = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+            if ((lane & (32 / NH - 1)) == 0)
                 asm volatile("st.shared.f32 [%0], %1;" ::"r"(lred + (q * kN + hl) * 4), "f"(lr[0]) : "memory");
-            }
             ok = named_bar_and(1, 128, got_o);
             if (!ok) break;
+            // Thread h < NH: head h's l over the four warps, its LSE and
+            // ckv_scale / (2^7 l) into the (now free) chunk-maxima buffer.
+            const uint32_t ired = s0 + kOffMax;
+            if (i < NH) {
+                float lt = 0.f, mi = -INFINITY;
 #pragma unroll
-            for (int h4 = 0; h4 < kN / 4; ++h4) {
-                float4 t = lds128f(lred + (4 * h4) * 4);
+                for (int w = 0; w < 4; ++w) lt += __uint_as_float(lds32(lred + (w * kN + i) * 4));
 #pragma unroll
-                for (int w = 1; w < 4; ++w) {
-                    const float4 v = lds128f(lred + (w * kN + 4 * h4) * 4);
-                    t.x += v.x;
-                    t.y += v.y;
-                    t.z += v.z;
-                    t.w += v.w;
-                }
-                l[4 * h4] = t.x;
-                l[4 * h4 + 1] = t.y;
-                l[4 * h4 + 2] = t.z;
-                l[4 * h4 + 3] = t.w;
+                for (int h = 0; h < NH; ++h) mi = h == i ? m[h] : mi;
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(ired + i * 4),
+                             "f"(lt > 0.f ? cks * __frcp_rn(kPScale * lt) : 0.f)
+                             : "memory");
+                if (i < H)
+                    a.lse_partial[x.b * a.lp_s0 + x.s * a.lp_s1 + i] =
+                        lt > 0.f ? (mi + __log2f(lt)) * 0.69314718055994530942f : -INFINITY;
             }
+            named_bar_and(1, 128, true);
+            float inv[NH];
 #pragma unroll
-            for (int h = 0; h < kN; ++h)
-                if (i == h && h < H)
-                    a.lse_partial[x.b * a.lp_s0 + x.s * a.lp_s1 + h] =
-                        l[h] > 0.f ? (m[h] + __log2f(l[h])) * 0.69314718055994530942f : -INFINITY;
-            float inv[kN];
-#pragma unroll
-            for (int h = 0; h < kN; ++h) inv[h] = l[h] > 0.f ? cks * __frcp_rn(kPScale * l[h]) : 0.f;
+            for (int h4 = 0; h4 < NH / 4; ++h4) {
+                const float4 v = lds128f(ired + 16 * h4);
+                inv[4 * h4] = v.x;
+                inv[4 * h4 + 1] = v.y;
+                inv[4 * h4 + 2] = v.z;
+                inv[4 * h4 + 3] = v.w;
+            }
             float* outp = a.out_partial + x.b * a.op_s0 + x.s * a.op_s1;
             tc_fence_after();
 #pragma unroll 1
             for (int j2 = 0; j2 < 2; ++j2) {  // two 128-row blocks of O per tensor-memory wait
-                uint32_t r[6][16];
+                uint32_t r[6][NH];
                 const uint32_t ta = tmem + lane_base + kColO + 96 * j2;
 #pragma unroll
-                for (int t = 0; t < 6; ++t) tmem_ld16(ta + 16 * t, r[t]);
+                for (int t = 0; t < 6; ++t) tmem_ld_heads<NH>(ta + 16 * t, r[t]);
                 tmem_wait_ld();
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-                    for (int h = 0; h < kN; ++h)
+                    for (int h = 0; h < NH; ++h)
                         if (h < H)
                             outp[h * a.op_s2 + 128 * (2 * j2 + jj) + 32 * q + lane] =
                                 (__uint_as_float(r[3 * jj][h]) + __uint_as_float(r[3 * jj + 1][h]) +
@@ -825,7 +843,9 @@ int mla_decode_ctas_per_sm(int) { return kCtasPerSm; }
 cudaError_t launch_mla_decode(const MlaDecodeArgs& a, const CUtensorMap& tckv, const CUtensorMap& tkpe,
                               cudaStream_t s) {
     if (a.B == 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    // the softmax warps handle 8 heads when there are at most 8, else 16
+    auto kernel = a.H <= 8 ? mla_decode_kernel<8> : mla_decode_kernel<16>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = device_sm_count(&sms);
@@ -834,7 +854,7 @@ cudaError_t launch_mla_decode(const MlaDecodeArgs& a, const CUtensorMap& tckv, c
     // round of gridDim.x schedule positions
     const int64_t items = static_cast<int64_t>(a.B) * a.num_splits;
     const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(kCtasPerSm) * sms));
-    return launch_dependent(mla_decode_kernel, dim3(grid), dim3(kThreads), kSmem, s, tckv, tkpe, a);
+    return launch_dependent(kernel, dim3(grid), dim3(kThreads), kSmem, s, tckv, tkpe, a);
 }
 
 }  // namespace pkv
