@@ -361,9 +361,11 @@ pkv_status pkv_lse_merge(const pkv_tensor* out_partial, const pkv_tensor* lse_pa
  * B, Hkv: batch and kv heads; total_pages = sum over the batch of
  * ceil(seq_len/16); max_pages = the largest ceil(seq_len/16); cache_dtype the
  * value cache's pkv_dtype (PKV_BF16, PKV_FP8_E4M3 or PKV_FP4_E2M1X2); sm_count the device's SM count. Models each split as one CTA
- * and returns the S in [1, 1024] with the lowest estimated time for
- * streaming the pages over the GPU's CTA slots plus the merge's extra
- * traffic and round trips.
+ * (a fixed start-up plus a per-page streaming time, measured on GB300)
+ * and returns the S in [1, min(1024, max_pages)] with the lowest estimated
+ * step time: the larger of the HBM-bound streaming time (with the CTAs'
+ * start-up and, past one wave of CTAs, part of the longest split's excess)
+ * and the longest split's own time, plus the partial records' traffic.
  * Returns 1 for empty or invalid input.
  */
 int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int64_t total_pages,

@@ -715,25 +715,33 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
     const double row = kind == pkv::kFp4 ? D / 2.0 + D / 16.0 : (kind == pkv::kFp8 ? D : 2.0 * D);
     const double page_bytes = 2.0 * kPageSize * row;                // K + V of one page, one kv head
     const double slots = static_cast<double>(sm_count) * pkv::decode_ctas_per_sm(D, kind, (Hq + Hkv - 1) / Hkv);
-    const double c0 = 32768.0 / page_bytes;                          // per-CTA start-up, in pages
+    // GB300 constants, measured: a CTA spends ~3 us on start-up and its
+    // epilogue and streams a page in ~0.28 us per 8 KB (bf16) or ~0.55 us per
+    // 8 KB of its bytes (FP8 / NVFP4: bound by instruction issue); HBM moves
+    // ~7 bytes per ns.
+    const double t0 = 3.0;
+    const double tp = (kind == pkv::kBf16 ? 0.278 : 0.55) * page_bytes / 8192.0;
+    const double bw = 7.0e3;  // bytes per ns (x 1e3 per us below)
     const double units = static_cast<double>(B) * Hkv;
-    const double work = static_cast<double>(Hkv) * static_cast<double>(total_pages);
+    const double mean_pages = static_cast<double>(total_pages) / B;
+    const double stream0 = static_cast<double>(Hkv) * static_cast<double>(total_pages) * page_bytes / (bw * 1e3);
     int best = 1;
     double best_cost = 1e300;
     for (int S = 1; S <= 1024; ++S) {
         if (S > max_pages) break;
         const double ncta = units * S;
-        const double longest = std::ceil(static_cast<double>(max_pages) / S) + c0;
-        const double total = work + ncta * c0;
-        double est = std::fmax(total / slots, longest);
-        if (ncta > slots) est = std::fmax(est, std::ceil(ncta / slots) * (total / ncta));
+        const bool waves = ncta > slots;
+        const double t_mean = t0 + tp * mean_pages / S;                                // a mean CTA
+        const double t_max = t0 + tp * std::ceil(static_cast<double>(max_pages) / S);  // the longest split
+        // HBM time plus the CTAs' start-up where it does not overlap other
+        // CTAs' streaming, plus, past one wave, part of the longest split's
+        // excess (it may be dispatched last) ...
+        const double stream = stream0 + 0.25 * ncta * t0 / slots + (waves ? 0.5 * (t_max - t_mean) : 0.0);
+        // ... or the longest split itself (after a mean CTA's wait for a slot)
+        const double crit = t_max + (waves ? t_mean : 0.0);
         // partial records written by the decode and read by the merge
-        const double merge_bytes = 2.0 * B * S * static_cast<double>(Hq) * (D + 1) * 4.0;
-        // the merge also pays about one memory round trip (~2 page times) per
-        // batch of partial rows one of its warps reads in sequence: 16 rows
-        // up to 32 splits, beyond that 16 warps share a row in batches of 8
-        const double rounds = S <= 32 ? std::ceil(S / 16.0) : std::ceil(std::ceil(S / 16.0) / 8.0);
-        const double cost = est + merge_bytes / (page_bytes * slots) + 2.0 * rounds;
+        const double merge = 0.15 * 2.0 * B * S * static_cast<double>(Hq) * (D + 1) * 4.0 / 1e6;
+        const double cost = std::fmax(stream, crit) + merge;
         if (cost < best_cost * (1.0 - 1e-9)) {
             best_cost = cost;
             best = S;
