@@ -195,24 +195,28 @@ def decode_kernel_source_hash(name: str = "qwen") -> str:
     return hashlib.sha256(src).hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(workload: str, num_splits: int):
     """DRAM bytes per decode launch from the committed ncu summary of this
-    workload, if it was taken on the current kernel source (else None)."""
+    workload, if it was taken on the current kernel source and with the
+    same split count (else None)."""
     p = os.path.join(ROOT, "profiles", f"{kernel_names(workload)[1]}_{workload}.md")
     try:
         txt = open(p).read()
     except OSError:
         return None
-    h = t = None
+    h = t = s = None
     for line in txt.splitlines():
-        if line.startswith("kernel_source_sha256_16:"):
-            h = line.split(":", 1)[1].strip()
-        if line.startswith("dram_bytes_per_launch:"):
-            try:
-                t = float(line.split(":", 1)[1].strip())
-            except ValueError:
-                t = None
-    return t if (h == decode_kernel_source_hash(workload) and t) else None
+        key, _, val = line.partition(":")
+        try:
+            if key == "kernel_source_sha256_16":
+                h = val.strip()
+            elif key == "dram_bytes_per_launch":
+                t = float(val.strip())
+            elif key == "num_splits":
+                s = int(val.strip())
+        except ValueError:
+            return None
+    return t if (h == decode_kernel_source_hash(workload) and s == num_splits and t) else None
 
 
 # ---- byte counts ---------------------------------------------------------------------
@@ -692,7 +696,7 @@ def main():
         "roofline": {"kernel": kernel_names(args.workload)[1], "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload),
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload, dw.num_splits),
                      "alg_bytes_per_launch": alg, "partial_record_bytes": partial_bytes(w, dw.num_splits),
                      "stream_read_same_bytes_gbs": ceiling,
                      "stream_read_same_bytes_frac": ceiling / peak,
