@@ -326,9 +326,13 @@ pkv_status pkv_paged_mla_decode(const pkv_tensor* q_lat, const pkv_tensor* q_pe,
 /*
  * pkv_choose_num_splits_mla -- split count for pkv_paged_mla_decode (host
  * only). B sequences, H heads, total_pages / max_pages in 64-token pages,
- * sm_count the device's SM count. The cost model of pkv_choose_num_splits
- * with the latent page (64 tokens x 640 bytes) and the MLA kernel's CTAs per
- * SM. Returns a value in [1, 1024]; 1 for empty or invalid input.
+ * sm_count the device's SM count. Models the persistent decode (two CTAs
+ * per SM taking the (sequence, split) items): a fixed cost per item and a
+ * per-chunk time (128 tokens, two pages; higher when two CTAs share an SM)
+ * for the longest sequence and a mean other one, the larger of a CTA's share
+ * of the items, the largest item and the HBM time, plus the partial
+ * records. Returns a value in [1, min(1024, max_pages)]; 1 for empty or
+ * invalid input.
  */
 int32_t pkv_choose_num_splits_mla(int32_t B, int32_t H, int64_t total_pages, int32_t max_pages, int32_t sm_count);
 

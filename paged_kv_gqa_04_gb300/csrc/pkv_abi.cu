@@ -682,23 +682,41 @@ pkv_status pkv_paged_mla_decode(const pkv_tensor* q_lat_p, const pkv_tensor* q_p
 
 int32_t pkv_choose_num_splits_mla(int32_t B, int32_t H, int64_t total_pages, int32_t max_pages, int32_t sm_count) {
     if (B <= 0 || H <= 0 || total_pages <= 0 || max_pages <= 0 || sm_count <= 0) return 1;
-    const double page_bytes = static_cast<double>(pkv::kMlaPage) * (pkv::kMlaDc + 2 * pkv::kMlaDr);
-    const double slots = static_cast<double>(sm_count) * pkv::mla_decode_ctas_per_sm(H);
-    const double c0 = 32768.0 / page_bytes;     // per-CTA start-up, in pages
-    const double trip = 16384.0 / page_bytes;   // one memory round trip, in pages
-    const double work = static_cast<double>(total_pages);
+    const double sms = static_cast<double>(sm_count);
+    const double slots = sms * pkv::mla_decode_ctas_per_sm(H);
+    // GB300 constants, measured on the persistent decode: ~3 us per item
+    // (query staging, epilogue) and ~2 us per 128-token chunk a CTA streams
+    // alone, 60% more when two CTAs share every SM; the latent rows stream
+    // at ~5 bytes/ns; 0.1 us per MB of partial records.
+    const double e = 3.0, c = 2.0, share = 0.6, bw = 5.0e3;
+    const double mx = static_cast<double>(max_pages);
+    const double rest = B > 1 ? (static_cast<double>(total_pages) - mx) / (B - 1) : 0.0;  // a mean other sequence
+    const double hbm = static_cast<double>(total_pages) * pkv::kMlaPage * (pkv::kMlaDc + 2 * pkv::kMlaDr) / (bw * 1e3);
+    // items (splits with pages) and chunks of a sequence of n pages at S
+    // splits of ceil(n / S) pages, and the chunks of its largest item
+    auto split = [](double n, int S, double* items, double* chunks, double* cmax) {
+        *items = *chunks = *cmax = 0.0;
+        if (n <= 0.0) return;
+        const double pps = std::ceil(n / S);
+        const double full = std::floor(n / pps), r = n - full * pps;
+        *items = full + (r > 0.0 ? 1.0 : 0.0);
+        *chunks = full * std::ceil(pps / 2.0) + std::ceil(r / 2.0);
+        *cmax = std::ceil(pps / 2.0);
+    };
     int best = 1;
     double best_cost = 1e300;
     for (int S = 1; S <= 1024; ++S) {
         if (S > max_pages) break;
-        const double ncta = static_cast<double>(B) * S;
-        const double longest = std::ceil(static_cast<double>(max_pages) / S) + c0;
-        const double total = work + ncta * c0;
-        double est = std::fmax(total / slots, longest);
-        if (ncta > slots) est = std::fmax(est, std::ceil(ncta / slots) * (total / ncta));
-        const double merge_bytes = 2.0 * B * S * static_cast<double>(H) * (pkv::kMlaDc + 1) * 4.0;
-        const double rounds = S <= 32 ? std::ceil(S / 16.0) : std::ceil(std::ceil(S / 16.0) / 8.0);
-        const double cost = est + merge_bytes / (page_bytes * slots) + trip * rounds;
+        double i1, c1, cmax, ir, cr, unused;
+        split(mx, S, &i1, &c1, &cmax);
+        split(rest, S, &ir, &cr, &unused);
+        const double items = i1 + (B - 1) * ir, chunks = c1 + (B - 1) * cr;
+        const double busy = std::fmin(items, slots);
+        const double cc = c * (1.0 + share * std::fmax(0.0, busy - sms) / sms);
+        const double stream = (items * e + chunks * cc) / busy;  // a CTA's share of the items
+        const double crit = e + cc * cmax;                        // the largest item
+        const double merge = 0.1 * 2.0 * B * S * static_cast<double>(H) * (pkv::kMlaDc + 1) * 4.0 / 1e6;
+        const double cost = std::fmax(std::fmax(stream, crit), hbm) + merge;
         if (cost < best_cost * (1.0 - 1e-9)) {
             best_cost = cost;
             best = S;

@@ -218,6 +218,25 @@ def test_split_heuristic(lib):
     assert pkv.choose_num_splits(1, 1, 8, 128, 3, 3, "bf16", sms) <= 3
 
 
+def test_mla_split_heuristic(lib):
+    sms = 152
+
+    def choose(name):
+        w = synth.make_mla_workload(name)
+        return pkv.choose_num_splits_mla(w.B, w.H, int(w.pages_per_seq.sum()), int(w.pages_per_seq.max()), sms)
+
+    # one 800-page sequence: 4-page splits (two whole 128-token chunks each),
+    # one item per CTA (measured on GB300: 27.6 us per step against 29.8 at
+    # 5-page splits)
+    s1 = choose("mla")
+    assert 800 / 4 <= s1 < 800 / 3
+    # 32 sequences of 64-256 pages over 304 CTAs: about one long item per
+    # CTA (measured: 71.6 us per step at S = 12, 74.2 at 19, 80.9 at 8)
+    assert 10 <= choose("mla_batch") <= 16
+    assert pkv.choose_num_splits_mla(0, 8, 0, 0, sms) == 1
+    assert pkv.choose_num_splits_mla(1, 8, 3, 3, sms) <= 3
+
+
 def test_selftest_bounded_wait_rejects_bad_limits():
     from paged_kv_gqa_04_gb300 import _abi
     lib = _abi.lib()
