@@ -28,7 +28,8 @@ def _blocks(anchor: int, seed: int) -> np.ndarray:
     """uint16 [n, 16]: every finite bf16 pattern of magnitude <= the anchor's,
     15 to a block, the anchor at position (block index % 16)."""
     pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
-    vals = bf16_u16_to_f64(pats)
+    with np.errstate(invalid="ignore"):  # the NaN patterns (signalling ones raise "invalid"), filtered below
+        vals = bf16_u16_to_f64(pats)
     a = bf16_u16_to_f64(np.array([anchor], np.uint16))[0]
     sel = pats[np.isfinite(vals) & (np.abs(vals) <= a)]
     perm = np.argsort(synth.uniform(synth.stream_key(seed, "blk"), len(sel)))
