@@ -31,6 +31,10 @@ CASES = [
     _case("h13", (3,), seq_lens=[100, 257], H=13),
     _case("empty_and_short", (4,), seq_lens=[0, 1, 2, 33], H=8),
     _case("many_splits_tree_merge", (40, 64), seq_lens=[4100], H=8),
+    # the schedule: batches up to 64 are ordered by length (B > 32: two rank
+    # keys per lane, with ties and empty sequences), larger ones round-robin
+    _case("b40_length_order", (1, 3), seq_lens=[(37 * i) % 400 if i % 7 else 200 for i in range(40)], H=4),
+    _case("b70_round_robin", (2,), seq_lens=[(53 * i) % 300 for i in range(70)], H=2),
 ]
 
 
