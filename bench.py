@@ -331,8 +331,9 @@ def time_e2e(dw, steps: int, warmup: int, world: int, flush) -> dict:
     """Through the binding with host buffers, one CUDA-graph submission per
     step (harness.StepGraph): one pinned-host -> device copy of the step's
     packed inputs, the three C-ABI launches reading them in place, one
-    device -> pinned-host copy of the packed out and lse; CUDA events around
-    each replay."""
+    device -> pinned-host copy of the packed out and lse (both copies by
+    pkv_copy, the SMs reading / writing the pinned buffers); CUDA events
+    around each replay."""
     from paged_kv_gqa_04_gb300 import harness
     g = harness.StepGraph(dw, host_io=True)
     stream = torch.cuda.current_stream()

@@ -427,6 +427,26 @@ pkv_status pkv_validate_indices_static(const pkv_tensor* block_tables, const pkv
                                        pkv_stream_t stream);
 
 /*
+ * pkv_copy -- copy of `bytes` bytes from src to dst by the SMs, on `stream`
+ * (moves a decode step's inputs in and its results out; not one of the
+ * step's calls).
+ *
+ * dst, src     each device memory, managed memory, or host memory that CUDA
+ *              has page-locked and mapped at the same address (the pinned
+ *              allocations of cudaHostAlloc / cudaMallocHost under unified
+ *              addressing, which the SMs of a GB300 read and write over
+ *              NVLink-C2C); each must hold `bytes` bytes; the ranges must
+ *              not overlap. Any alignment (16-byte aligned pairs move in
+ *              16-byte words).
+ * Launched as a programmatic dependent: it waits for the preceding grid on
+ * the stream before reading src. Errors: bytes < 0, a NULL pointer or
+ * overlapping ranges give PKV_ERR_INVALID_ARG; a pointer the SMs cannot
+ * address (by cudaPointerGetAttributes) gives PKV_ERR_UNSUPPORTED, and
+ * nothing is launched. bytes == 0 launches nothing.
+ */
+pkv_status pkv_copy(void* dst, const void* src, int64_t bytes, pkv_stream_t stream);
+
+/*
  * pkv_stream_read -- streaming-read ceiling (a measurement helper; not one of
  * the decode step's calls). (mainarch, decode-attention section: a pure
  * device-memory streaming read is measured first and is the ceiling each
@@ -459,7 +479,7 @@ const char* pkv_status_string(int32_t status);
 
 /* ABI version of this header (bumped on any signature change). */
 int32_t pkv_abi_version(void);
-#define PKV_ABI_VERSION 4
+#define PKV_ABI_VERSION 5
 
 #ifdef __cplusplus
 }

@@ -41,7 +41,7 @@ EXPORTED = ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_c
             "pkv_validate_indices", "pkv_status_string", "pkv_abi_version", "pkv_stream_read",
             "pkv_validate_indices_static", "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4",
             "pkv_mla_cache_write", "pkv_paged_mla_decode", "pkv_choose_num_splits_mla",
-            "pkv_selftest_bounded_wait")
+            "pkv_selftest_bounded_wait", "pkv_copy")
 
 
 class PkvTensor(ctypes.Structure):
@@ -81,13 +81,14 @@ def lib() -> ctypes.CDLL:
         L.pkv_validate_indices.argtypes = [T, T, T, ctypes.c_int64, T, P, P]
         L.pkv_stream_read.argtypes = [P, ctypes.c_int64, P, i32, P]
         L.pkv_selftest_bounded_wait.argtypes = [ctypes.c_int64, P, P, P]
+        L.pkv_copy.argtypes = [P, P, ctypes.c_int64, P]
         L.pkv_validate_indices_static.argtypes = [T, T, T, ctypes.c_int64, P, P]
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         for name in ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_validate_indices",
                      "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read", "pkv_validate_indices_static",
                      "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4", "pkv_mla_cache_write",
-                     "pkv_paged_mla_decode", "pkv_choose_num_splits_mla", "pkv_selftest_bounded_wait"):
+                     "pkv_paged_mla_decode", "pkv_choose_num_splits_mla", "pkv_selftest_bounded_wait", "pkv_copy"):
             getattr(L, name).restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -251,6 +252,18 @@ def selftest_bounded_wait(limit_ns: int, err_flag: torch.Tensor, elapsed_ns: tor
         raise ValueError("int32 device flag and two int64 device words expected")
     _check("pkv_selftest_bounded_wait",
            lib().pkv_selftest_bounded_wait(int(limit_ns), err_flag.data_ptr(), elapsed_ns.data_ptr(), _stream(stream)))
+
+
+def copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    """pkv_copy: dst <- src byte for byte by the SMs; each a contiguous tensor
+    in device memory or in pinned host memory (e.g. from pin_memory()), the
+    same number of bytes."""
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy: dst and src must be contiguous")
+    n = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != n:
+        raise ValueError("copy: dst and src differ in size")
+    _check("pkv_copy", lib().pkv_copy(_ptr(dst), _ptr(src), n, _stream(stream)))
 
 
 def stream_read(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:

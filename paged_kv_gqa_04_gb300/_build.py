@@ -21,7 +21,7 @@ BUILD = os.path.join(ROOT, "_build", "pkv")
 LIB = os.path.join(HERE, "libpkv.so")
 
 SOURCES = ["pkv_abi.cu", "rope_kv_write.cu", "paged_decode.cu", "mla_decode.cu", "lse_merge.cu", "validate.cu",
-           "stream_read.cu", "selftest.cu"]
+           "stream_read.cu", "selftest.cu", "copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

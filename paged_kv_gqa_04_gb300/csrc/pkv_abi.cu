@@ -856,6 +856,35 @@ pkv_status pkv_selftest_bounded_wait(int64_t limit_ns, int32_t* err_flag, uint64
                                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// A pointer the SMs can address: device or managed memory, or host memory
+// page-locked by CUDA and mapped at the same address (unified addressing).
+static bool device_accessible(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    switch (at.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            return true;
+        case cudaMemoryTypeHost:
+            return at.devicePointer == p;
+        default:
+            return false;
+    }
+}
+
+pkv_status pkv_copy(void* dst, const void* src, int64_t bytes, pkv_stream_t stream) {
+    if (bytes < 0) return PKV_ERR_INVALID_ARG;
+    if (bytes == 0) return PKV_OK;
+    if (!dst || !src) return PKV_ERR_INVALID_ARG;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+    if (d < s + static_cast<uintptr_t>(bytes) && s < d + static_cast<uintptr_t>(bytes)) return PKV_ERR_INVALID_ARG;
+    if (!device_accessible(dst) || !device_accessible(src)) return PKV_ERR_UNSUPPORTED;
+    return cuda_status(pkv::launch_copy(dst, src, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int32_t ctas, pkv_stream_t stream) {
     if (bytes < 0 || bytes % 16 != 0 || ctas < 1 || ctas > 65535) return PKV_ERR_INVALID_ARG;
     if (bytes == 0) return PKV_OK;

@@ -190,6 +190,7 @@ cudaError_t device_sm_count(int* n);
 cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s);
 cudaError_t static_slot_bitmap(uint32_t** ptr, int64_t* words);
 cudaError_t launch_stream_read(const void* buf, int64_t bytes, uint32_t* sink, int ctas, cudaStream_t s);
+cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, int32_t* err, uint64_t* elapsed_ns, cudaStream_t s);
 
 // Occupancy-related constants of the decode kernel, shared with the split

@@ -189,7 +189,10 @@ class StepGraph:
     seq_lens -- live in one packed device buffer (each tensor a 256-byte
     aligned view the kernels read directly) filled by ONE copy from a pinned
     host buffer of the same layout, and out and lse live in one packed device
-    buffer read back by ONE copy to pinned host memory. Without host_io the
+    buffer read back by ONE copy to pinned host memory. Both copies are
+    pkv_copy launches (the SMs move the bytes over the host link; the
+    result's copy starts behind the merge as its programmatic dependent).
+    Without host_io the
     graph starts by restoring the unrotated q (MLA: q_pe) on the device.
     """
 
@@ -248,10 +251,10 @@ class StepGraph:
         if not self.host_io:
             d["q"].copy_(d["q0"])
         else:
-            self.dev_in.copy_(self.host_in, non_blocking=True)
+            _abi.copy(self.dev_in, self.host_in)  # pinned host -> device, by the SMs
         dw.step()
         if self.host_io:
-            self.host_out.copy_(self.dev_out, non_blocking=True)
+            _abi.copy(self.host_out, self.dev_out)  # device -> pinned host, behind the merge
 
     @property
     def h2d_bytes(self) -> int:

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pkv_abi_version() == 4
+    assert lib.pkv_abi_version() == 5
     for s in range(4):
         assert pkv.status_string(s)
     assert "invalid" in pkv.status_string(1)
@@ -235,6 +235,16 @@ def test_mla_split_heuristic(lib):
     assert 10 <= choose("mla_batch") <= 16
     assert pkv.choose_num_splits_mla(0, 8, 0, 0, sms) == 1
     assert pkv.choose_num_splits_mla(1, 8, 3, 3, sms) <= 3
+
+
+def test_copy_rejects_bad_arguments_before_any_cuda_call():
+    from paged_kv_gqa_04_gb300 import _abi
+    lib = _abi.lib()
+    assert lib.pkv_copy(0x2000, 0x1000, -1, None) == _abi.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy(None, 0x1000, 16, None) == _abi.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy(0x2000, None, 16, None) == _abi.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy(0x1008, 0x1000, 16, None) == _abi.PKV_ERR_INVALID_ARG  # overlapping ranges
+    assert lib.pkv_copy(None, None, 0, None) == _abi.PKV_OK                   # nothing to copy
 
 
 def test_selftest_bounded_wait_rejects_bad_limits():
