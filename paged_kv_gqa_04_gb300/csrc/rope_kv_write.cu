@@ -218,6 +218,10 @@ __device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float (
 template <int D, bool INTER, int KIND, int U>
 __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(const RopeArgs a) {
     constexpr int TPR = D / 16;  // threads per row
+    // Launched as a programmatic dependent: the inputs may come from the
+    // preceding grid (a copy of the step's inputs), and a preceding decode
+    // may still read the cache.
+    grid_dep_wait();
     // The decode kernel that usually follows may start its prologue now; it
     // waits for this grid's writes before it reads q or the cache.
     grid_dep_launch();
@@ -348,10 +352,10 @@ cudaError_t launch_t(const RopeArgs& a, cudaStream_t s) {
     const int64_t blocks = (a.T + per_cta - 1) / per_cta;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
     if (two)
-        rope_kv_write_kernel<D, INTER, KIND, 2><<<static_cast<unsigned>(blocks), dim3(per_tok, toks), 0, s>>>(a);
-    else
-        rope_kv_write_kernel<D, INTER, KIND, 1><<<static_cast<unsigned>(blocks), dim3(per_tok, toks), 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_dependent(rope_kv_write_kernel<D, INTER, KIND, 2>, dim3(static_cast<unsigned>(blocks)),
+                                dim3(per_tok, toks), 0, s, a);
+    return launch_dependent(rope_kv_write_kernel<D, INTER, KIND, 1>, dim3(static_cast<unsigned>(blocks)),
+                            dim3(per_tok, toks), 0, s, a);
 }
 
 template <int D, bool INTER>
@@ -377,6 +381,7 @@ cudaError_t launch_d(const RopeArgs& a, cudaStream_t s) {
 // threadIdx.y and blockIdx.x: tokens.
 template <bool INTER>
 __global__ void __launch_bounds__(1024) mla_cache_write_kernel(const MlaWriteArgs a) {
+    grid_dep_wait();  // as rope_kv_write_kernel: a programmatic dependent
     grid_dep_launch();
     const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.y + threadIdx.y;
     if (t >= a.T) return;
@@ -438,11 +443,8 @@ cudaError_t launch_mla_cache_write(const MlaWriteArgs& a, cudaStream_t s) {
     const int64_t blocks = (a.T + toks - 1) / toks;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(blocks)), block(per_tok, toks);
-    if (a.interleaved)
-        mla_cache_write_kernel<true><<<grid, block, 0, s>>>(a);
-    else
-        mla_cache_write_kernel<false><<<grid, block, 0, s>>>(a);
-    return cudaGetLastError();
+    if (a.interleaved) return launch_dependent(mla_cache_write_kernel<true>, grid, block, 0, s, a);
+    return launch_dependent(mla_cache_write_kernel<false>, grid, block, 0, s, a);
 }
 
 cudaError_t launch_rope_kv_write(const RopeArgs& a, cudaStream_t s) {
