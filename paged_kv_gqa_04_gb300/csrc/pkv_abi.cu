@@ -757,8 +757,10 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
         const double stream = stream0 + 0.25 * ncta * t0 / slots + (waves ? 0.5 * (t_max - t_mean) : 0.0);
         // ... or the longest split itself (after a mean CTA's wait for a slot)
         const double crit = t_max + (waves ? t_mean : 0.0);
-        // partial records written by the decode and read by the merge
-        const double merge = 0.15 * 2.0 * B * S * static_cast<double>(Hq) * (D + 1) * 4.0 / 1e6;
+        // partial records written by the decode and read by the merge, and
+        // past 32 splits the merge's two-level tree (measured ~2 us more
+        // per step than its one-warp-per-row form)
+        const double merge = 0.15 * 2.0 * B * S * static_cast<double>(Hq) * (D + 1) * 4.0 / 1e6 + (S > 32 ? 2.0 : 0.0);
         const double cost = std::fmax(stream, crit) + merge;
         if (cost < best_cost * (1.0 - 1e-9)) {
             best_cost = cost;
