@@ -12,14 +12,16 @@
 // writes bf16 (round to nearest even) out = sum w_s o_s / sum w_s and
 // lse = M + ln sum w_s. With more, the row is a two-level tree (mainarch,
 // decode-attention section: a parallel tree combine rather than one
-// workgroup grinding through the partials): up to 16 warps of one CTA each
-// merge a contiguous run of splits in parallel and their results are merged
-// again by their own LSE weights. The kernel is latency-bound (the partials
-// are a few MB): partial rows are loaded in batches of sixteen, the first
-// together with the LSE values and each next one while the previous batch is
-// summed. Rows wider than 128 columns (the 512-value latent output of MLA
-// decode) are cut into 128-column slices, each merged by its own warp (or
-// CTA) with the same LSE weights.
+// workgroup grinding through the partials): the 32 warps of one CTA each
+// merge a contiguous run of splits of a 64-column slice in parallel and
+// their results are merged again by their own LSE weights. The kernel is
+// latency-bound (the partials are a few MB): partial rows are loaded in
+// batches (sixteen for one warp per row, eight in the tree: one batch per
+// warp up to 256 splits), the first together with the LSE values and each
+// next one while the previous batch is summed. Rows wider than 128 columns
+// (the 512-value latent output of MLA decode) are cut into slices (128
+// columns for one warp per row, 64 in the tree), each merged with the same
+// LSE weights.
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
@@ -148,21 +150,26 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs 
         a.lse_out[b * a.lo_s0 + h * a.lo_s1] = (m == -INFINITY) ? -INFINITY : m + __logf(l);
 }
 
-// Many splits: a two-level tree. One CTA per row; each of its W warps
-// merges a contiguous chunk of the splits (all chunks in parallel), then the
-// W warp results are combined through shared memory by their own LSE weights.
+// Many splits: a two-level tree. One CTA per 64-column slice of a row; each
+// of its 32 warps merges a contiguous run of at most ceil(S / 32) splits
+// (one batch of loads up to S = 256), then the warp results are combined
+// through shared memory by their own LSE weights, each computed once.
+constexpr int kTreeWarps = 32;
+constexpr int kTreeCols = 64;
+
 template <int D>
-__global__ void __launch_bounds__(512) lse_merge_tree_kernel(const MergeArgs a) {
-    using SL = Slice<D>;
-    constexpr int V = SL::V;
-    constexpr int DW = SL::DW;
-    extern __shared__ float tree_smem[];  // W * DW partial sums, then W maxima, W weight sums
+__global__ void __launch_bounds__(kTreeWarps * 32) lse_merge_tree_kernel(const MergeArgs a) {
+    constexpr int DW = kTreeCols;
+    constexpr int NS = D / DW;  // slices per row
+    constexpr int V = DW / 32;  // columns per lane
+    constexpr int W = kTreeWarps;
+    // W * DW partial sums, then W maxima, W weight sums, W weights
+    extern __shared__ float tree_smem[];
     grid_dep_wait();
-    const int W = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t row = blockIdx.x / SL::N;
-    const int c0 = static_cast<int>(blockIdx.x % SL::N) * DW;  // first column of this CTA's slice
+    const int64_t row = blockIdx.x / NS;
+    const int c0 = static_cast<int>(blockIdx.x % NS) * DW;  // first column of this CTA's slice
     const int b = static_cast<int>(row / a.Hq);
     const int h = static_cast<int>(row % a.Hq);
     const int chunk = (a.S + W - 1) / W;
@@ -173,6 +180,7 @@ __global__ void __launch_bounds__(512) lse_merge_tree_kernel(const MergeArgs a) 
     float* sacc = tree_smem;
     float* sm = tree_smem + W * DW;
     float* sl = sm + W;
+    float* sw = sl + W;
 #pragma unroll
     for (int i = 0; i < V; ++i) sacc[warp * DW + lane * V + i] = acc[i];
     if (lane == 0) {
@@ -182,16 +190,16 @@ __global__ void __launch_bounds__(512) lse_merge_tree_kernel(const MergeArgs a) 
     __syncthreads();
     float M = -INFINITY;
     for (int w = 0; w < W; ++w) M = fmaxf(M, sm[w]);
+    if (threadIdx.x < W) sw[threadIdx.x] = (sm[threadIdx.x] == -INFINITY) ? 0.f : __expf(sm[threadIdx.x] - M);
+    __syncthreads();
     float L = 0.f;
-    for (int w = 0; w < W; ++w) L += (sm[w] == -INFINITY) ? 0.f : __expf(sm[w] - M) * sl[w];
+    for (int w = 0; w < W; ++w) L += sw[w] * sl[w];
     const float inv = (L > 0.f) ? 1.f / L : 0.f;
     for (int d2 = threadIdx.x; d2 < DW / 2; d2 += blockDim.x) {
         float o0 = 0.f, o1 = 0.f;
-        for (int w = 0; w < W; ++w) {
-            if (sm[w] == -INFINITY) continue;
-            const float e = __expf(sm[w] - M);
-            o0 += e * sacc[w * DW + 2 * d2];
-            o1 += e * sacc[w * DW + 2 * d2 + 1];
+        for (int w = 0; w < W; ++w) {  // an empty run's weight is 0 and its sums are 0
+            o0 += sw[w] * sacc[w * DW + 2 * d2];
+            o1 += sw[w] * sacc[w * DW + 2 * d2 + 1];
         }
         *reinterpret_cast<uint32_t*>(a.out + b * a.o_s0 + h * a.o_s1 + c0 + 2 * d2) = pack_bf16(o0 * inv, o1 * inv);
     }
@@ -208,12 +216,11 @@ cudaError_t launch_d(const MergeArgs& a, cudaStream_t s) {
         if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
         return launch_dependent(lse_merge_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(kWarps * 32), 0, s, a);
     }
-    if (rows > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-    // 16 warps per row slice: each reads at most ceil(S / 16) partial rows,
-    // i.e. one or two batches of loads in sequence up to S = 256
-    const int W = 16;
-    const size_t smem = static_cast<size_t>(W) * (SL::DW + 2) * sizeof(float);
-    return launch_dependent(lse_merge_tree_kernel<D>, dim3(static_cast<unsigned>(rows)), dim3(W * 32), smem, s, a);
+    const int64_t trows = static_cast<int64_t>(a.B) * a.Hq * (D / kTreeCols);  // 64-column row slices
+    if (trows > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    const size_t smem = static_cast<size_t>(kTreeWarps) * (kTreeCols + 3) * sizeof(float);
+    return launch_dependent(lse_merge_tree_kernel<D>, dim3(static_cast<unsigned>(trows)), dim3(kTreeWarps * 32), smem,
+                            s, a);
 }
 
 }  // namespace

@@ -190,7 +190,8 @@ def test_page_permutation_gives_identical_output():
                                  (128, 4096)])
 def test_lse_merge_random_partials(D, S):
     """Both merge forms: one warp per row (S <= 32) and the two-level tree
-    (S > 32, up to 16 warps per row)."""
+    (S > 32: 32 warps per 64-column slice; past 256 splits more than one
+    batch of loads per warp)."""
     B, Hq = (5, 6) if S <= 1000 else (2, 3)
     op = synth.normal_f32(synth.stream_key(40, "o"), B * S * Hq * D).reshape(B, S, Hq, D)
     lp = (synth.normal_f32(synth.stream_key(40, "l"), B * S * Hq) * 4).reshape(B, S, Hq)
