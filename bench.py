@@ -11,13 +11,15 @@ context token (written by the library's cache-write call before timing).
 
 Timing: W warm-up steps, then exactly K steps between a barrier and a device
 synchronise on each side. Before every timed step the L2 is flushed (a 512 MiB
-device write) and q is restored from its unrotated copy, both outside the
-step's CUDA events; per step, events on the launching stream bracket each of
-the three launches. Reported:
+device write, then a 512 MiB read so that the write-back of dirty lines also
+happens before the step) and q is restored from its unrotated copy, both
+outside the step's CUDA events. Events on the launching stream bracket each
+step (the launches chained as a program issues them); a second pass puts an
+event between the launches for each kernel's own time. Reported:
   value       tokens/s = B*K / sum of step times (inputs resident in HBM)
   e2e         the same through the Python binding with host buffers: every
               step copies its inputs from pinned host memory to the device and
-              its output (out, lse) back, inside the step's events
+              its output (out, lse) back (pkv_copy), inside the step's events
   roofline    of the decode kernel: algorithmic bytes (Q + K/V pages + block-
               table entries + output) / its mean event time, against the
               measured HBM copy bandwidth
@@ -290,7 +292,7 @@ def flush_buffer():
 
 def time_steps(dw, steps: int, warmup: int, world: int, flush, per_kernel: bool) -> dict:
     """Device-resident steps: per step flush L2 and restore q (both outside
-    the events), then the three launches. With per_kernel, events also
+    the events), then the step's three launches. With per_kernel, events also
     separate the launches (which stops the decode and merge kernels from
     starting early behind their predecessors); without, events bracket the
     step only."""

@@ -54,7 +54,7 @@ struct Vec<2> {
 // All loads of a batch of 16 partial rows are issued before any is used: the
 // first batch goes out with the first 32 LSE values, each later batch while
 // the previous one is summed. (16 rows per batch for a warp that merges a
-// whole row, 8 in the tree kernel, whose 16 warps share the register file.)
+// whole row, 8 in the tree kernel, whose 32 warps share the register file.)
 template <int V, int kBatch>
 __device__ __forceinline__ void warp_merge(const float* lse, int64_t lp_s1, const float* op, int64_t op_s1, int s_lo,
                                            int s_hi, float& m, float& l, float (&acc)[V]) {

@@ -9,13 +9,17 @@
 // softmax-weighted latent outputs (V = ckv), split-K over the sequence and a
 // stage-2 merge of the partial records (pkv_lse_merge with D = 512).
 //
-// The tensor cores read the E4M3 cache bytes as the copy engine lands them:
+// The tensor cores read the E4M3 cache bytes as the TMA copies land them:
 // nothing is converted on the CUDA cores.
 //
 // Work decomposition. Persistent CTAs, two per SM (106 KB of shared memory,
 // 256 tensor-memory columns each), six warps in three roles. The work items
-// are the (sequence, split) pairs; CTA k takes items k, k + grid, k + 2 grid,
-// ... A split's tokens go through the CTA two pages (128 tokens, the MMA M)
+// are the (sequence, split) pairs, dealt to the CTAs in rounds of `grid`
+// schedule positions: for batches up to 64 the positions walk the sequences
+// longest first and every other round runs in reverse (so a CTA that drew
+// one of the longest splits draws one of the shortest next); larger batches
+// go round-robin (CTA k takes items k, k + grid, ...). A split's tokens go
+// through the CTA two pages (128 tokens, the MMA M)
 // at a time ("chunk"), one chunk in shared memory at a time; the copies run
 // on across items, so only a CTA's first chunk waits for a cold start, and
 // the two CTAs of an SM overlap each other's waits.
@@ -78,7 +82,7 @@
 // zeroed in shared memory before P . V reads them (a 0 weight times a NaN
 // byte would poison the sum).
 //
-// Every hand-off is an mbarrier (the copy engine's byte counts,
+// Every hand-off is an mbarrier (the TMA copies' byte counts,
 // tcgen05.commit, warp arrivals). Tensor memory: S (48 columns) and O
 // (4 x 48 columns). Up to 16 heads; missing heads get zero queries and are
 // not written.
