@@ -28,8 +28,8 @@
 //                     buffer: per page four 64-row x 128-byte boxes of ckv
 //                     (one per 128-value column block) and one of kpe; the
 //                     buffer holds ckv as [4 blocks][128 rows][128 B] and
-//                     kpe as [128 rows][128 B] (80 KB). The next two chunks
-//                     are prefetched into L2 (cp.async.bulk.prefetch): the
+//                     kpe as [128 rows][128 B] (80 KB). The next chunk is
+//                     prefetched into L2 (cp.async.bulk.prefetch): the
 //                     first chunk before the wait on the preceding grid (a
 //                     prefetch reads through L2, which the preceding grid's
 //                     writes also go through), the read-ahead only once the
@@ -104,7 +104,7 @@ constexpr int kT = 2 * kMlaPage;  // tokens per chunk (two pages), the MMA M
 constexpr int kN = 16;            // heads per CTA
 constexpr int kThreads = 192;
 constexpr int kCtasPerSm = 2;
-constexpr int kPrefetch = 2;      // chunks read into L2 ahead of the copy
+constexpr int kPrefetch = 1;      // chunks read into L2 ahead of the copy (measured best of 0-3)
 constexpr int kWarpCopy = 0, kWarpMma = 1, kWarpSm = 2;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
