@@ -431,13 +431,13 @@ pkv_status pkv_validate_indices_static(const pkv_tensor* block_tables, const pkv
  * (moves a decode step's inputs in and its results out; not one of the
  * step's calls).
  *
- * dst, src     each device memory, managed memory, or host memory that CUDA
- *              has page-locked and mapped at the same address (the pinned
- *              allocations of cudaHostAlloc / cudaMallocHost under unified
- *              addressing, which the SMs of a GB300 read and write over
- *              NVLink-C2C); each must hold `bytes` bytes; the ranges must
- *              not overlap. Any alignment (16-byte aligned pairs move in
- *              16-byte words).
+ * dst, src     each device memory of the current device, managed memory,
+ *              or host memory that CUDA has page-locked and mapped at the
+ *              same address (the pinned allocations of cudaHostAlloc /
+ *              cudaMallocHost under unified addressing, which the SMs of a
+ *              GB300 read and write over NVLink-C2C); each must hold
+ *              `bytes` bytes; the ranges must not overlap. Any alignment
+ *              (16-byte aligned pairs move in 16-byte words).
  * Launched as a programmatic dependent: it waits for the preceding grid on
  * the stream before reading src. Errors: bytes < 0, a NULL pointer or
  * overlapping ranges give PKV_ERR_INVALID_ARG; a pointer the SMs cannot

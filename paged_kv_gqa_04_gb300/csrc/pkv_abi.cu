@@ -858,16 +858,20 @@ pkv_status pkv_selftest_bounded_wait(int64_t limit_ns, int32_t* err_flag, uint64
                                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
-// A pointer the SMs can address: device or managed memory, or host memory
-// page-locked by CUDA and mapped at the same address (unified addressing).
+// A pointer the SMs of the current device can address: its own device
+// memory, managed memory, or host memory page-locked by CUDA and mapped at
+// the same address (unified addressing). Another GPU's memory is refused
+// (it would need peer access).
 static bool device_accessible(const void* p) {
     cudaPointerAttributes at{};
-    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    int cur = -1;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess || cudaGetDevice(&cur) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
     }
     switch (at.type) {
         case cudaMemoryTypeDevice:
+            return at.device == cur;
         case cudaMemoryTypeManaged:
             return true;
         case cudaMemoryTypeHost:
