@@ -722,6 +722,21 @@ int32_t pkv_choose_num_splits_mla(int32_t B, int32_t H, int64_t total_pages, int
             best = S;
         }
     }
+    // More splits that only add empty ones (the same items, the longest
+    // split unchanged) up to the CTA slots: measured faster on one 800-page
+    // sequence (26.0 us per step at 254 splits against 27.0 at 200, both
+    // 200 four-page items), which the model above does not capture.
+    auto same_items = [&](int S1, int S2) {
+        double a1, b1, m1, a2, b2, m2, r1, q1, u1, r2, q2, u2;
+        split(mx, S1, &a1, &b1, &m1);
+        split(mx, S2, &a2, &b2, &m2);
+        split(rest, S1, &r1, &q1, &u1);
+        split(rest, S2, &r2, &q2, &u2);
+        return a1 == a2 && b1 == b2 && r1 == r2 && q1 == q2;
+    };
+    while (best < 1024 && best + 1 <= max_pages && static_cast<double>(B) * (best + 1) <= slots &&
+           same_items(best, best + 1))
+        ++best;
     return best;
 }
 
