@@ -19,10 +19,10 @@
 // longest first and every other round runs in reverse (so a CTA that drew
 // one of the longest splits draws one of the shortest next); larger batches
 // go round-robin (CTA k takes items k, k + grid, ...). A split's tokens go
-// through the CTA two pages (128 tokens, the MMA M)
-// at a time ("chunk"), one chunk in shared memory at a time; the copies run
-// on across items, so only a CTA's first chunk waits for a cold start, and
-// the two CTAs of an SM overlap each other's waits.
+// through the CTA two pages (128 tokens, the MMA M) at a time ("chunk"), one
+// chunk in shared memory at a time; the copies run on across items, so only
+// a CTA's first chunk waits for a cold start, and the two CTAs of an SM
+// overlap each other's waits.
 //
 //   warp 0, copies    TMA tile loads with 128-byte swizzle into the chunk
 //                     buffer: per page four 64-row x 128-byte boxes of ckv
@@ -49,6 +49,16 @@
 //                     shared memory, the running sums; per item the next
 //                     item's queries (so its scores overlap) and then the
 //                     epilogue; the (0, -inf) records of empty splits.
+//                     Query staging: warp q takes heads 4q .. 4q + 3 and
+//                     reads whole 512-byte stretches of each row. Epilogue:
+//                     l over the warp's tokens by recursive halving, one
+//                     thread per head forms ckv_scale / (2^7 l) and the LSE,
+//                     O is read from tensor memory two blocks per wait.
+//
+// The kernel has two instantiations by the heads its softmax warps handle:
+// NH = 8 when H <= 8 (scores, weights, rescale and epilogue on 8 of each
+// 16-column group; the P8 rows of heads 8-15 are zeroed once), else 16. The
+// MMA shapes keep 16 head slots either way.
 //
 // Per chunk the steps are serial: copy -> S -> P -> P . V -> the buffer is
 // free for the next copy. So the next chunk's scores never overwrite S
