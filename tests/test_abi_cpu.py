@@ -238,6 +238,21 @@ def test_mla_split_heuristic(lib):
     assert pkv.choose_num_splits_mla(1, 8, 3, 3, sms) <= 3
 
 
+def test_package_exports_resolve():
+    for name in pkv.__all__:
+        assert getattr(pkv, name) is not None, name
+
+
+def test_binding_copy_checks_its_tensors():
+    import torch
+    from paged_kv_gqa_04_gb300 import _abi
+    a = torch.zeros(8, 8, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        _abi.copy(a.t(), a)                               # not contiguous
+    with pytest.raises(ValueError):
+        _abi.copy(torch.zeros(63, dtype=torch.uint8), a)  # sizes differ
+
+
 def test_copy_rejects_bad_arguments_before_any_cuda_call():
     from paged_kv_gqa_04_gb300 import _abi
     lib = _abi.lib()
