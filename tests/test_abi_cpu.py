@@ -238,6 +238,27 @@ def test_mla_split_heuristic(lib):
     assert pkv.choose_num_splits_mla(1, 8, 3, 3, sms) <= 3
 
 
+def test_split_heuristics_stay_in_range_on_random_and_extreme_inputs():
+    rng = np.random.default_rng(7)
+    for _ in range(400):
+        B = int(rng.integers(1, 4096))
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.integers(1, 17))
+        D = int(rng.choice([64, 128]))
+        max_pages = int(rng.integers(1, 70000))
+        total = int(rng.integers(max_pages, max_pages * B + 1))
+        sms = int(rng.choice([1, 76, 132, 152, 160]))
+        for dt in ("bf16", "fp8", "nvfp4"):
+            S = pkv.choose_num_splits(B, Hkv, Hkv * G, D, total, max_pages, dt, sms)
+            assert 1 <= S <= min(1024, max_pages)
+            assert S == pkv.choose_num_splits(B, Hkv, Hkv * G, D, total, max_pages, dt, sms)  # deterministic
+        Sm = pkv.choose_num_splits_mla(B, int(rng.integers(1, 17)), total, max_pages, sms)
+        assert 1 <= Sm <= min(1024, max_pages)
+    # extreme but valid sizes
+    assert 1 <= pkv.choose_num_splits(65535, 64, 1024, 128, (1 << 40), 1 << 24, "bf16", 152) <= 1024
+    assert 1 <= pkv.choose_num_splits_mla(65535, 16, (1 << 40), 1 << 24, 152) <= 1024
+
+
 def test_package_exports_resolve():
     for name in pkv.__all__:
         assert getattr(pkv, name) is not None, name
