@@ -32,6 +32,15 @@
  *   - Streams. Every call only enqueues GPU work on `stream` (NULL = the
  *     legacy default stream) and returns; results are ready when that
  *     stream's work completes. Calls contain no host synchronisation.
+ *   - Ordering. The step's kernels (cache write, decode, merge, copy) are
+ *     launched as programmatic dependents, so one may start its prologue
+ *     while its predecessor on the stream finishes; each waits for that
+ *     predecessor (griddepcontrol.wait) before it reads anything another
+ *     grid may have written, and before it can finish. Calls on one stream
+ *     therefore see each other's results exactly as plain stream order
+ *     would give; only the decode and merge read index inputs (block
+ *     tables, seq_lens) before that wait, which the library's own kernels
+ *     never write.
  *   - Status. The return value reports argument validation and launch
  *     errors only: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED are returned
  *     before anything is launched; PKV_ERR_CUDA reports a launch failure
