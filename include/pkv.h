@@ -36,11 +36,11 @@
  *     launched as programmatic dependents, so one may start its prologue
  *     while its predecessor on the stream finishes; each waits for that
  *     predecessor (griddepcontrol.wait) before it reads anything another
- *     grid may have written, and before it can finish. Calls on one stream
- *     therefore see each other's results exactly as plain stream order
- *     would give; only the decode and merge read index inputs (block
- *     tables, seq_lens) before that wait, which the library's own kernels
- *     never write.
+ *     grid may have written, and before it can finish. Only the decodes read
+ *     index inputs (block tables, seq_lens) before that wait, and only the
+ *     cache writes and the decodes let their successor start early; neither
+ *     writes index inputs. Calls on one stream therefore see each other's
+ *     results exactly as plain stream order would give.
  *   - Status. The return value reports argument validation and launch
  *     errors only: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED are returned
  *     before anything is launched; PKV_ERR_CUDA reports a launch failure
@@ -448,7 +448,9 @@ pkv_status pkv_validate_indices_static(const pkv_tensor* block_tables, const pkv
  *              `bytes` bytes; the ranges must not overlap. Any alignment
  *              (16-byte aligned pairs move in 16-byte words).
  * Launched as a programmatic dependent: it waits for the preceding grid on
- * the stream before reading src. Errors: bytes < 0, a NULL pointer or
+ * the stream before reading src, and the next grid starts only once the
+ * copy has finished (so the copied bytes may be any later call's inputs,
+ * index inputs included). Errors: bytes < 0, a NULL pointer or
  * overlapping ranges give PKV_ERR_INVALID_ARG; a pointer the SMs cannot
  * address (by cudaPointerGetAttributes) gives PKV_ERR_UNSUPPORTED, and
  * nothing is launched. bytes == 0 launches nothing.

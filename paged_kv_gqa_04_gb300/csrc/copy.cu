@@ -3,7 +3,8 @@
 // directly over NVLink-C2C (unified addressing). For the few hundred KB a
 // decode step moves between host and device this avoids the copy engines'
 // set-up latency, and as a programmatic dependent the copy of a step's
-// result starts as soon as the kernel that wrote it has finished.
+// result is launched while the kernel that wrote it is still running (and
+// waits for it); the grid after the copy starts only once the copy is done.
 //
 // Each thread moves 16-byte words (both pointers 16-byte aligned) or single
 // bytes; the grid covers the buffer in one pass up to four CTAs per SM,
@@ -20,8 +21,10 @@ constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) copy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
                                                         int64_t bytes, int vec16) {
-    grid_dep_wait();  // the source may be written by the preceding grid
-    grid_dep_launch();
+    // The source may be written by the preceding grid. No early trigger: the
+    // next grid (a decode reads its block tables and seq_lens before its own
+    // wait) starts only once this copy has finished.
+    grid_dep_wait();
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * kThreads;
     int64_t done = 0;
