@@ -424,8 +424,13 @@ pkv_status pkv_validate_indices(const pkv_tensor* block_tables, const pkv_tensor
  * num_pages * 16 must not exceed PKV_STATIC_VALIDATE_MAX_SLOTS, else the call
  * returns PKV_ERR_UNSUPPORTED and launches nothing. The first call on a
  * device looks up the array's device address (once per device, with that
- * device current); make that first call before any stream capture. Every
- * call clears the bitmap on `stream` before using it, and all calls share
+ * device current); make that first call before any stream capture. If that
+ * lookup fails, the call returns PKV_ERR_CUDA and the next call on the device
+ * tries the lookup again; once it has succeeded it is not repeated. Every
+ * call clears the part of the bitmap its pool uses (num_pages * 16 bits) on
+ * `stream` before using it; bits an earlier call left above that part are
+ * never read, because slots past the pool are flagged as out of range
+ * before the bitmap is touched. All calls share
  * the one array: calls whose GPU work overlaps (on different streams, or
  * different host threads on one device) race on it and may report false or
  * missed duplicates. Calls ordered on one stream are safe.

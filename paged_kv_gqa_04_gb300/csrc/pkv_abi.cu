@@ -837,7 +837,8 @@ pkv_status pkv_validate_indices_static(const pkv_tensor* block_tables_p, const p
     if (!shape_ok(block_tables, 2, PKV_I32) || !shape_ok(seq_lens, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;
     if (seq_lens.shape[0] != block_tables.shape[0]) return PKV_ERR_INVALID_ARG;
     if (num_pages < 0) return PKV_ERR_INVALID_ARG;
-    if (num_pages * kPageSize > PKV_STATIC_VALIDATE_MAX_SLOTS) return PKV_ERR_UNSUPPORTED;
+    // compared before any product, so no num_pages can overflow the check
+    if (num_pages > PKV_STATIC_VALIDATE_MAX_SLOTS / kPageSize) return PKV_ERR_UNSUPPORTED;
     pkv::ValidateArgs a{};
     if (slot_mapping.ptr) {
         if (!shape_ok(slot_mapping, 1, PKV_I32)) return PKV_ERR_INVALID_ARG;

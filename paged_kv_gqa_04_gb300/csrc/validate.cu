@@ -64,24 +64,32 @@ static __device__ __align__(256) uint32_t g_static_slot_bitmap[PKV_STATIC_VALIDA
 
 }  // namespace
 
-// Device address of this device's copy of the static bitmap: looked up once
-// per device (with that device current) and then reused.
+// Device address of this device's copy of the static bitmap, looked up with
+// that device current. A successful lookup is kept and reused; a failed one
+// is not (the next call on that device tries again), so a lookup that fails
+// for a passing reason -- made during a stream capture, or before the device
+// was ready -- does not disable the entry point for the rest of the process.
 cudaError_t static_slot_bitmap(uint32_t** ptr, int64_t* words) {
     constexpr int kMaxDevices = 64;
     static uint32_t* addr[kMaxDevices] = {};
-    static cudaError_t status[kMaxDevices] = {};
-    static std::once_flag once[kMaxDevices];
+    static std::mutex lock[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::call_once(once[dev], [dev] {
-        void* p = nullptr;
-        status[dev] = cudaGetSymbolAddress(&p, g_static_slot_bitmap);
-        addr[dev] = static_cast<uint32_t*>(p);
-    });
-    if (status[dev] != cudaSuccess) return status[dev];
-    *ptr = addr[dev];
+    {
+        std::lock_guard<std::mutex> guard(lock[dev]);
+        if (addr[dev] == nullptr) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_static_slot_bitmap);
+            if (e != cudaSuccess) {
+                (void)cudaGetLastError();  // leave no sticky error behind for the caller's next launch
+                return e;
+            }
+            addr[dev] = static_cast<uint32_t*>(p);
+        }
+        *ptr = addr[dev];
+    }
     *words = PKV_STATIC_VALIDATE_MAX_SLOTS / 32;
     return cudaSuccess;
 }

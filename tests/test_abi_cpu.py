@@ -134,6 +134,31 @@ def test_decode_and_merge_reject_inconsistent_arguments(lib):
     assert lib.pkv_validate_indices(bt, sl, NULL, 50, NULL, None, None) == _abi.PKV_ERR_INVALID_ARG
 
 
+def test_validation_entry_points_reject_bad_arguments_before_any_cuda_call(lib):
+    """Host checks of both index-validation entry points; every call returns
+    before the static one looks up its device array or anything launches."""
+    B = 3
+    bt = _t((B, 10), "i32")
+    sl = _t((B,), "i32")
+    slots = _t((7,), "i32")
+    err = ctypes.c_void_p(0x2000)
+    st = lib.pkv_validate_indices_static
+    assert st(bt, sl, slots, 50, None, None) == _abi.PKV_ERR_INVALID_ARG              # no error word
+    assert st(bt, _t((B + 1,), "i32"), slots, 50, err, None) == _abi.PKV_ERR_INVALID_ARG
+    assert st(_t((B, 10), "f32"), sl, slots, 50, err, None) == _abi.PKV_ERR_INVALID_ARG
+    assert st(bt, sl, _t((7, 2), "i32"), 50, err, None) == _abi.PKV_ERR_INVALID_ARG
+    assert st(bt, sl, slots, -1, err, None) == _abi.PKV_ERR_INVALID_ARG
+    limit = (1 << 23) // 16
+    assert st(bt, sl, slots, limit + 1, err, None) == _abi.PKV_ERR_UNSUPPORTED
+    # pools whose slot count would overflow a 64-bit product are refused, not wrapped
+    for huge in ((1 << 59) + 1, (1 << 62), (1 << 63) - 1):
+        assert st(bt, sl, slots, huge, err, None) == _abi.PKV_ERR_UNSUPPORTED
+        assert lib.pkv_validate_indices(bt, sl, slots, huge, NULL, err, None) == _abi.PKV_ERR_UNSUPPORTED
+    al = lib.pkv_validate_indices
+    assert al(bt, sl, slots, -1, NULL, err, None) == _abi.PKV_ERR_INVALID_ARG
+    assert al(bt, sl, slots, 50, _t((10,), "i32"), err, None) == _abi.PKV_ERR_INVALID_ARG  # bitmap too small
+
+
 def test_nvfp4_entry_points_reject_inconsistent_arguments(lib):
     """Host validation of the NVFP4 write and decode: fake pointers, every
     call returns before any CUDA work."""

@@ -63,3 +63,24 @@ def test_static_validation_rejects_pools_beyond_its_bitmap():
     _abi.validate_indices_static(bt, sl, None, (1 << 23) // 16, err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+
+
+def test_bits_left_by_a_larger_pool_do_not_reach_a_smaller_one():
+    """Each call clears only the bits of its own pool. A call on a large pool
+    that leaves bits set (a duplicate), then a clean call on a small pool,
+    then a clean call on the large pool: the last two must report nothing,
+    and the allocating entry point must agree on each."""
+    big = synth.custom_workload("noalloc_big", 72, [3000, 1200, 40], 4, 2, 128, num_pages=4096)
+    small = synth.custom_workload("noalloc_small", 73, [20, 7], 4, 2, 128, num_pages=4)
+    bt_b, sl_b = torch.from_numpy(big.block_tables).cuda(), torch.from_numpy(big.seq_lens).cuda()
+    bt_s, sl_s = torch.from_numpy(small.block_tables).cuda(), torch.from_numpy(small.seq_lens).cuda()
+    hi = big.num_pages * 16 - 1  # slots far above the small pool's bits
+    dup = torch.tensor([hi, 5, hi - 40, hi, 60000], dtype=torch.int32, device="cuda")
+    a1, b1 = _both(bt_b, sl_b, dup, big.num_pages)
+    assert a1 == b1 == _abi.FLAG_DUPLICATE_SLOT
+    clean_small = torch.tensor([5, 6, 63, 0], dtype=torch.int32, device="cuda")
+    a2, b2 = _both(bt_s, sl_s, clean_small, small.num_pages)
+    assert a2 == b2 == 0
+    clean_big = torch.tensor([hi, 5, hi - 40, 60000], dtype=torch.int32, device="cuda")
+    a3, b3 = _both(bt_b, sl_b, clean_big, big.num_pages)
+    assert a3 == b3 == 0
