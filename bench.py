@@ -4,10 +4,13 @@ One step = the whole hot path over one batch: fused RoPE + paged-KV write of
 the new token (q rotated in place), paged GQA split-K decode, LSE merge --
 three launches of the library's kernels through the C ABI.
 
-Default workload: the Qwen2.5-1.5B-shaped decode (batch 32, seq_lens uniform
-in [512, 4096], 12 query / 2 kv heads, head dim 128, page size 16, HND, bf16
-cache, NeoX RoPE base 1e6, 12000-page shuffled pool). The cache holds every
-context token (written by the library's cache-write call before timing).
+Default workload: the ragged large-batch decode, the largest single-GPU
+configuration (batch 256, lognormal seq_lens with median 1024, sigma 1,
+clipped to [1, 8192]; 32 query / 8 kv heads, head dim 128, page size 16, NHD,
+bf16 cache, interleaved RoPE base 5e5, 1% of K rows scaled x8). The cache
+holds every context token (written by the library's cache-write call before
+timing). Every other configuration is measured the same way under
+'other_workloads'.
 
 Timing: W warm-up steps, then exactly K steps between a barrier and a device
 synchronise on each side. Before every timed step the L2 is flushed (a 512 MiB
@@ -17,14 +20,17 @@ outside the step's CUDA events. Events on the launching stream bracket each
 step (the launches chained as a program issues them); a second pass puts an
 event between the launches for each kernel's own time. Reported:
   value       tokens/s = B*K / sum of step times (inputs resident in HBM)
-  e2e         the same through the Python binding with host buffers: every
-              step copies its inputs from pinned host memory to the device and
-              its output (out, lse) back (pkv_copy), inside the step's events
+  e2e         the same through the binding with host buffers: every step
+              copies its inputs from pinned host memory to the device and its
+              output (out, lse) back (pkv_copy), inside the step's events
   roofline    of the decode kernel: algorithmic bytes (Q + K/V pages + block-
               table entries + output) / its mean event time, against the
               measured HBM copy bandwidth
-  cache_write GB/s of one cache-fill call over all context tokens
-  cpu_baseline the float64 oracle on the host, single thread
+  cache_fill  GB/s of one cache-fill call over all context tokens, counting
+              each distinct position's cos/sin row once
+  cpu_baseline the float64 oracle on the host, single thread and on every
+              core, over a sample of sequences at evenly spaced length
+              quantiles of the batch
 `--impl reference` times that oracle alone as the reference arm.
 Under torchrun with N > 1 every rank runs an independent replica (weak
 scaling, no collective on the data path); rank 0 prints the line.
@@ -79,12 +85,15 @@ def parse_args():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    p.add_argument("--workload", default="qwen", choices=sorted(WORKLOAD_TEXT))
+    p.add_argument("--workload", default="ragged", choices=sorted(WORKLOAD_TEXT))
     p.add_argument("--splits", type=int, default=0, help="num_splits (0 = the library's heuristic)")
-    p.add_argument("--also", default="longctx,ragged,fp8,million,fp4,mla,mla_batch",
-                   help="extra workloads whose decode roofline is reported under 'other_workloads' ('' = none)")
+    p.add_argument("--also", default="qwen,longctx,fp8,fp4,million,mla,mla_batch",
+                   help="other workloads measured the same way, reported under 'other_workloads' ('' = none)")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--cpu-seconds", type=float, default=8.0,
+                   help="seconds of oracle work per CPU-baseline leg of the headline workload")
+    p.add_argument("--cpu-seconds-other", type=float, default=3.0,
+                   help="seconds of oracle work per CPU-baseline leg of each other workload")
     p.add_argument("--clock-window", type=float, default=1.0,
                    help="seconds of untimed steps run under the clock sampler before the timed steps")
     p.add_argument("--no-e2e", action="store_true")
@@ -191,34 +200,86 @@ def kernel_names(name: str) -> tuple:
     return "rope_kv_write", "paged_gqa_decode", "lse_merge"
 
 
-def decode_kernel_source_hash(name: str = "qwen") -> str:
-    f = "mla_decode.cu" if is_mla(name) else "paged_decode.cu"
+def kernel_source_hash(kind: str, name: str = "ragged") -> str:
+    """First 16 hex digits of the SHA-256 of the source file that holds the
+    workload's decode ("decode") or cache-write ("write") kernel."""
+    if kind == "decode":
+        f = "mla_decode.cu" if is_mla(name) else "paged_decode.cu"
+    else:
+        f = "rope_kv_write.cu"
     src = open(os.path.join(ROOT, "paged_kv_gqa_04_gb300", "csrc", f), "rb").read()
     return hashlib.sha256(src).hexdigest()[:16]
+
+
+def decode_kernel_source_hash(name: str = "ragged") -> str:
+    return kernel_source_hash("decode", name)
+
+
+def _profile_fields(path: str) -> dict:
+    out = {}
+    try:
+        txt = open(path).read()
+    except OSError:
+        return out
+    for line in txt.splitlines():
+        key, sep, val = line.partition(":")
+        if sep and key and " " not in key.strip():
+            out[key.strip()] = val.strip()
+    return out
 
 
 def ncu_traffic(workload: str, num_splits: int):
     """DRAM bytes per decode launch from the committed ncu summary of this
     workload, if it was taken on the current kernel source and with the
     same split count (else None)."""
-    p = os.path.join(ROOT, "profiles", f"{kernel_names(workload)[1]}_{workload}.md")
+    f = _profile_fields(os.path.join(ROOT, "profiles", f"{kernel_names(workload)[1]}_{workload}.md"))
     try:
-        txt = open(p).read()
-    except OSError:
+        h, t, s = f["kernel_source_sha256_16"], float(f["dram_bytes_per_launch"]), int(f["num_splits"])
+    except (KeyError, ValueError):
         return None
-    h = t = s = None
-    for line in txt.splitlines():
-        key, _, val = line.partition(":")
-        try:
-            if key == "kernel_source_sha256_16":
-                h = val.strip()
-            elif key == "dram_bytes_per_launch":
-                t = float(val.strip())
-            elif key == "num_splits":
-                s = int(val.strip())
-        except ValueError:
-            return None
     return t if (h == decode_kernel_source_hash(workload) and s == num_splits and t) else None
+
+
+def ncu_fill_traffic(workload: str, tokens: int):
+    """DRAM bytes of the cache-fill launch over `tokens` tokens from the
+    committed ncu summary of this workload's fill, if it was taken on the
+    current kernel source and the same token count (else None)."""
+    f = _profile_fields(os.path.join(ROOT, "profiles", f"{kernel_names(workload)[0]}_fill_{workload}.md"))
+    try:
+        h, t, n = f["kernel_source_sha256_16"], float(f["dram_bytes_per_launch"]), int(f["tokens"])
+    except (KeyError, ValueError):
+        return None
+    return t if (h == kernel_source_hash("write", workload) and n == tokens and t) else None
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "Model name" and v.strip():
+                return v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            k, _, v = line.partition(":")
+            if k.strip() == "model name" and v.strip():
+                return v.strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+def stats(ms) -> dict:
+    """Mean, median, 10th / 90th percentile, min and max (microseconds) of a
+    list of millisecond timings."""
+    a = np.asarray(list(ms), dtype=np.float64) * 1e3
+    return {"mean": float(a.mean()), "median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "min": float(a.min()), "max": float(a.max()), "n": int(a.size)}
 
 
 # ---- byte counts ---------------------------------------------------------------------
@@ -355,9 +416,10 @@ def time_e2e(dw, steps: int, warmup: int, world: int, flush) -> dict:
     return dict(step_ms=[a.elapsed_time(b) for a, b in ev], h2d=g.h2d_bytes, d2h=g.d2h_bytes, B=dw.w.B)
 
 
-def time_fill(dw, reps: int, flush) -> dict:
-    """One cache-fill call (all context tokens, no q), timed alone."""
-    fi = dw.fill_inputs()
+def time_fill(dw, reps: int, flush, fi=None) -> dict:
+    """One cache-fill call (all context tokens, no q), timed alone. `fi` is
+    the fill call's device inputs (dw.fill_inputs()), made here if absent."""
+    fi = dw.fill_inputs() if fi is None else fi
     T = int(fi["positions"].numel())
     rows = int(torch.unique(fi["positions"]).numel())
     stream = torch.cuda.current_stream()
@@ -372,8 +434,16 @@ def time_fill(dw, reps: int, flush) -> dict:
         b.record(stream)
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
-    del fi
     return dict(T=T, rows=rows, ms=statistics.median(ms), ms_all=ms)
+
+
+def fill_cache(dw) -> dict:
+    """Write every context token into the cache with one cache-fill call and
+    return that call's device inputs (kept for timing the fill)."""
+    fi = dw.fill_inputs()
+    if int(fi["positions"].numel()):
+        dw.write_fill(fi)
+    return fi
 
 
 def stream_ceiling(nbytes: int, flush, reps: int = 20) -> float:
@@ -429,13 +499,16 @@ def measure_layered(dw, layers: int, reps: int, flush, peak: float) -> dict:
     return dict(layers=layers, us_per_layer=1e3 * ms / layers, gbs=gbs, frac=gbs / peak, layers_agree=ok)
 
 
-def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -> dict:
-    """Decode-kernel roofline of another workload (filled, then `reps`
-    flushed launches)."""
+def measure_workload(name: str, splits: int, reps: int, flush, peak: float, cpu_seconds: float,
+                     with_e2e: bool = True, with_cpu: bool = True) -> dict:
+    """Every figure of one workload: the decode kernel alone (`reps` flushed
+    launches), the chained and separated step, the step end to end with
+    host buffers, the cache-fill call, decode layered over distinct caches,
+    and the oracle on the host (single thread and all cores)."""
     from paged_kv_gqa_04_gb300 import harness
     dw = harness.make_device_workload(name, num_splits=splits or None)
     w = dw.w
-    dw.fill()
+    fi = fill_cache(dw)
     d = dw.upload_decode()
     dw.step()
     stream = torch.cuda.current_stream()
@@ -446,28 +519,52 @@ def measure_decode_only(name: str, splits: int, reps: int, flush, peak: float) -
         dw.decode(d["q"])
         b.record(stream)
     torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    rs = time_steps(dw, 20, 3, 1, flush, True)
-    rc = time_steps(dw, 20, 3, 1, flush, False)
-    step = dict(chained_us=1e3 * statistics.mean(rc["step_ms"]),
-                tokens_per_s=w.B / (statistics.mean(rc["step_ms"]) * 1e-3),
-                separated_us=dict(zip(kernel_names(name), (1e3 * statistics.mean(rs["write_ms"]),
-                                                           1e3 * statistics.mean(rs["decode_ms"]),
-                                                           1e3 * statistics.mean(rs["merge_ms"])))))
+    dec = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(dec)
+    rs = time_steps(dw, reps, 3, 1, flush, True)
+    rc = time_steps(dw, reps, 3, 1, flush, False)
+    names = kernel_names(name)
+    step = dict(tokens_per_s=w.B * len(rc["step_ms"]) / (sum(rc["step_ms"]) * 1e-3),
+                tokens_per_s_median_step=w.B / (statistics.median(rc["step_ms"]) * 1e-3),
+                chained_us=stats(rc["step_ms"]),
+                separated_us={names[0]: stats(rs["write_ms"]), names[1]: stats(rs["decode_ms"]),
+                              names[2]: stats(rs["merge_ms"])})
     layered = measure_layered(dw, 4 if decode_alg_bytes(w) < 1e9 else 2, 5, flush, peak)
-    fill = time_fill(dw, 5, flush)
-    wb = write_alg_bytes(w, fill["T"], False)
-    wbu = write_alg_bytes(w, fill["T"], False, fill["rows"])
+    fill = time_fill(dw, 5, flush, fi)
+    del fi
     alg = decode_alg_bytes(w)
-    r = dict(workload=WORKLOAD_TEXT[name], num_splits=dw.num_splits, decode_us=ms * 1e3,
+    r = dict(workload=WORKLOAD_TEXT[name], batch=w.B, context_tokens=int(w.seq_lens.sum()),
+             num_splits=dw.num_splits, decode_us=ms * 1e3, decode_us_stats=stats(dec),
              decode_gbs=alg / (ms * 1e-3) / 1e9, decode_frac=alg / (ms * 1e-3) / 1e9 / peak,
-             cache_write_gbs=wb / (fill["ms"] * 1e-3) / 1e9,
-             cache_write_frac=wb / (fill["ms"] * 1e-3) / 1e9 / peak,
-             cache_write_frac_table_rows_once=wbu / (fill["ms"] * 1e-3) / 1e9 / peak, err_flag=int(dw.err.item()),
-             stream_read_frac_same_bytes=stream_ceiling(alg, flush) / peak, layered=layered, step=step)
+             decode_traffic=ncu_traffic(name, dw.num_splits), decode_alg_bytes=alg,
+             stream_read_frac_same_bytes=stream_ceiling(alg, flush) / peak, layered=layered, step=step,
+             cache_fill=fill_figures(w, fill, peak, name), err_flag=int(dw.err.item()))
+    if with_e2e:
+        e = time_e2e(dw, reps, 3, 1, flush)
+        r["e2e"] = {"value": w.B * len(e["step_ms"]) / (sum(e["step_ms"]) * 1e-3), "unit": UNIT,
+                    "step_us": stats(e["step_ms"]), "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
     del dw
     torch.cuda.empty_cache()
+    if with_cpu:
+        r["cpu_baseline"] = cpu_baseline(w, r["num_splits"], cpu_seconds, max_seqs=8)
+        r["cpu_baseline_all_cores"] = cpu_baseline_allcore(name, w, r["num_splits"], cpu_seconds, max_seqs=8)
     return r
+
+
+def fill_figures(w, fill: dict, peak: float, name: str) -> dict:
+    """Figures of one cache-fill call. The headline fraction counts the
+    cos/sin row of each distinct position once (tokens at the same position
+    share the row, which is read from L2 after its first use); the
+    one-row-per-token figure is kept beside it. `dram_bytes` is the fill
+    launch's DRAM traffic from the committed ncu summary (null when that
+    summary is of another kernel source or token count)."""
+    wb = write_alg_bytes(w, fill["T"], False)
+    wbu = write_alg_bytes(w, fill["T"], False, fill["rows"])
+    s = fill["ms"] * 1e-3
+    return {"tokens": fill["T"], "distinct_positions": fill["rows"], "us": fill["ms"] * 1e3,
+            "us_stats": stats(fill["ms_all"]), "bytes": wbu, "gbs": wbu / s / 1e9, "hbm_frac": wbu / s / 1e9 / peak,
+            "bytes_one_row_per_token": wb, "hbm_frac_one_row_per_token": wb / s / 1e9 / peak,
+            "dram_bytes": ncu_fill_traffic(name, fill["T"])}
 
 
 # ---- CPU oracle -------------------------------------------------------------------------
@@ -529,15 +626,54 @@ def oracle_step_timer(w, seqs, num_splits):
     return run
 
 
-def cpu_baseline(w, num_splits, seconds: float) -> dict:
-    run = oracle_step_timer(w, list(range(w.B)), num_splits)
+def quantile_sample(w, n: int) -> list:
+    """n sequences of the batch at evenly spaced quantiles of its seq_len
+    distribution (sorted by length, the middle of each of n equal groups),
+    so the sample's mix of lengths is the batch's."""
+    n = max(1, min(int(n), w.B))
+    order = np.argsort(w.seq_lens, kind="stable")
+    return sorted(int(order[min(w.B - 1, int((i + 0.5) * w.B / n))]) for i in range(n))
+
+
+def seq_flops(w, b: int) -> float:
+    """Oracle arithmetic of one sequence's decode: scores and weighted sum,
+    two flops per product."""
+    if hasattr(w, "Dc"):
+        return 2.0 * float(w.seq_lens[b]) * w.H * (w.Dc + w.Dr + w.Dc)
+    return 2.0 * float(w.seq_lens[b]) * w.Hq * 2 * w.D
+
+
+def cpu_sample(w, max_seqs: int = 16, flop_budget: float = 2e9) -> list:
+    """The largest quantile sample of at most max_seqs sequences whose
+    oracle step stays within flop_budget (at least one sequence)."""
+    best = quantile_sample(w, 1)
+    for n in range(2, min(max_seqs, w.B) + 1):
+        cand = quantile_sample(w, n)
+        if sum(seq_flops(w, b) for b in cand) > flop_budget:
+            break
+        best = cand
+    return best
+
+
+def _sample_text(w, seqs) -> str:
+    L = w.seq_lens.astype(np.float64)
+    return (f"{len(seqs)} of {w.B} sequences at evenly spaced length quantiles (mean length "
+            f"{L[seqs].mean():.0f} vs the batch's {L.mean():.0f})")
+
+
+def cpu_baseline(w, num_splits, seconds: float, max_seqs: int = 16) -> dict:
+    """The oracle on one host thread: whole steps (new-token write with q,
+    decode, merge) over a quantile sample of the batch, repeated for about
+    `seconds`; tokens/s = sequences decoded per second."""
+    seqs = cpu_sample(w, max_seqs)
+    run = oracle_step_timer(w, seqs, num_splits)
     total, n = 0.0, 0
     while total < seconds or n == 0:
         total += run()
         n += 1
-    return {"value": w.B * n / total, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} oracle decode steps over the whole batch ({w.B} sequences, {num_splits} splits): "
-                      f"new-token cache write, decode, merge; float64, single thread; cache prepared untimed"}
+    return {"value": len(seqs) * n / total, "unit": UNIT, "cores": 1, "kind": "oracle", "cpu_model": cpu_model(),
+            "sample": f"{n} oracle decode steps over {_sample_text(w, seqs)}, {num_splits} splits: new-token "
+                      f"cache write, decode, merge; float64, single thread; cache prepared untimed"}
 
 
 _ALLCORE_BARRIER = None
@@ -549,8 +685,8 @@ def _allcore_init(barrier):
 
 
 def _allcore_worker(job):
-    """One host process of the all-core oracle baseline: prepare its slice of
-    the batch (untimed), wait for the others, then time whole steps."""
+    """One host process of the all-core oracle baseline: prepare the sample
+    (untimed), wait for the others, then time whole steps over it."""
     name, seqs, num_splits, seconds = job
     from paged_kv_gqa_04_gb300 import synth
     w = synth.make_mla_workload(name) if is_mla(name) else synth.make_workload(name)
@@ -563,20 +699,25 @@ def _allcore_worker(job):
     return len(seqs) * n / total
 
 
-def cpu_baseline_allcore(name, B, num_splits, seconds: float) -> dict:
+def cpu_baseline_allcore(name, w, num_splits, seconds: float, max_seqs: int = 16):
     """The oracle on every host core: one process per core (spawned: this
-    process has initialised CUDA), the batch's sequences dealt round-robin,
-    all timed over the same window; throughput = the sum of the processes'."""
+    process has initialised CUDA), each running whole steps over the same
+    quantile sample as the single-thread baseline, all timed over the same
+    window; throughput = the sum of the processes' (each keeps the batch's
+    mix of lengths). Null for a single-sequence batch, which the oracle
+    cannot spread over processes."""
     import multiprocessing as mp
-    procs = max(1, min(os.cpu_count() or 1, B))
-    groups = [list(range(i, B, procs)) for i in range(procs)]
+    if w.B < 2:
+        return None
+    seqs = cpu_sample(w, max_seqs)
+    procs = max(1, os.cpu_count() or 1)
     ctx = mp.get_context("spawn")
     barrier = ctx.Barrier(procs)
     with ctx.Pool(procs, initializer=_allcore_init, initargs=(barrier,)) as pool:
-        rates = pool.map(_allcore_worker, [(name, g, num_splits, seconds) for g in groups])
-    return {"value": sum(rates), "unit": UNIT, "cores": procs, "kind": "oracle",
-            "sample": f"{procs} processes, each its round-robin share of the {B} sequences, {num_splits} splits, "
-                      f"whole oracle decode steps (new-token write, decode, merge) for about {seconds:g} s; "
+        rates = pool.map(_allcore_worker, [(name, seqs, num_splits, seconds)] * procs)
+    return {"value": sum(rates), "unit": UNIT, "cores": procs, "kind": "oracle", "cpu_model": cpu_model(),
+            "sample": f"{procs} processes, each running whole oracle decode steps (new-token write, decode, "
+                      f"merge) over {_sample_text(w, seqs)}, {num_splits} splits, for about {seconds:g} s; "
                       f"float64, one thread each"}
 
 
@@ -590,26 +731,35 @@ def run_reference(args, world, rank):
     import oracle
     oracle.build()
     # size the per-step sample so that warm-up + timed steps take about a minute
-    probe = oracle_step_timer(w, [0], S)
-    t1 = probe()
+    probe_seqs = quantile_sample(w, 1)
+    t1 = oracle_step_timer(w, probe_seqs, S)()
     n = int(max(1, min(w.B, round(60.0 / max(1, args.steps + args.warmup) / max(t1, 1e-6)))))
-    seqs = list(range(n))
+    seqs = quantile_sample(w, n)
     run = oracle_step_timer(w, seqs, S)
     for _ in range(args.warmup):
         run()
     ts = [run() for _ in range(args.steps)]
     total = sum(ts)
-    value = n * args.steps / total
+    value = len(seqs) * args.steps / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "batch_sample": n, "num_splits": S},
-        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1,
-                         "sample": f"each step: the first {n} of {w.B} sequences (new-token write, decode, merge)"},
+        "config": workload_config(w, args.workload),
+        "batch_sample": len(seqs), "num_splits": S,
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1, "cpu_model": cpu_model(),
+                         "sample": f"each step: {_sample_text(w, seqs)} (new-token write, decode, merge)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def workload_config(w, name: str) -> dict:
+    """The line's `config`: the workload's description and sizes (the same
+    in both arms)."""
+    return {"workload": WORKLOAD_TEXT[name], "batch": w.B, "context_tokens": int(w.seq_lens.sum()),
+            "l2": "GPU arm: flushed before every timed step (512 MiB device write, then a 512 MiB read so "
+                  "the write's dirty lines are written back before the step; both outside the step's events)"}
 
 
 # ---- main -------------------------------------------------------------------------------
@@ -623,12 +773,12 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
     import __graft_entry__
     __graft_entry__.build()
-    from paged_kv_gqa_04_gb300 import harness, synth
+    from paged_kv_gqa_04_gb300 import harness
 
     peak, peak_kind = hbm_peak()
     dw = harness.make_device_workload(args.workload, num_splits=args.splits or None)
     w = dw.w
-    dw.fill()
+    fi = fill_cache(dw)
     dw.upload_decode()
     flush = flush_buffer()
     gpu_index = torch.cuda.current_device()
@@ -655,67 +805,67 @@ def main():
 
     e2e = None if args.no_e2e else time_e2e(dw, args.steps, max(3, args.warmup // 2), world, flush)
     e2e_s = max_over_ranks(sum(e2e["step_ms"]) * 1e-3, world) if e2e else None
-    fill = time_fill(dw, 10, flush)
-    wb = write_alg_bytes(w, fill["T"], False)
-    wbu = write_alg_bytes(w, fill["T"], False, fill["rows"])
-    write_gbs = wb / (fill["ms"] * 1e-3) / 1e9
+    fill = fill_figures(w, time_fill(dw, 10, flush, fi), peak, args.workload)
+    del fi
 
     ceiling = stream_ceiling(alg, flush)
-    layered = measure_layered(dw, 4, 10, flush, peak)
+    layered = measure_layered(dw, 4 if alg < 1e9 else 2, 10, flush, peak)
+    num_splits = dw.num_splits
+    del dw
+    torch.cuda.empty_cache()
     others = {}
     if args.also:
-        for name in [x for x in args.also.split(",") if x]:
-            others[name] = measure_decode_only(name, 0, 20, flush, peak)
+        for name in [x for x in args.also.split(",") if x and x != args.workload]:
+            others[name] = measure_workload(name, 0, 20, flush, peak, args.cpu_seconds_other,
+                                            with_e2e=not args.no_e2e,
+                                            with_cpu=rank == 0 and not args.no_cpu_baseline)
 
     cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, dw.num_splits, args.cpu_seconds)
-        cpu_all = cpu_baseline_allcore(args.workload, w.B, dw.num_splits, args.cpu_seconds)
+        cpu = cpu_baseline(w, num_splits, args.cpu_seconds)
+        cpu_all = cpu_baseline_allcore(args.workload, w, num_splits, args.cpu_seconds)
 
+    names = kernel_names(args.workload)
+    cfg = workload_config(w, args.workload)
+    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "batch": w.B, "num_splits": dw.num_splits,
-                   "context_tokens": int(w.seq_lens.sum()),
-                   "l2": "flushed before every timed step (512 MiB device write, then a 512 MiB read so the "
-                         "write's dirty lines are written back before the step; both outside the step's events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "step_us": {"step": 1e3 * statistics.mean(r["step_ms"]),
-                    "separated": {kernel_names(args.workload)[0]: 1e3 * statistics.mean(rk["write_ms"]),
-                                  kernel_names(args.workload)[1]: 1e3 * dec_ms,
-                                  "lse_merge": 1e3 * statistics.mean(rk["merge_ms"]),
-                                  "step": 1e3 * statistics.mean(rk["step_ms"]),
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if getattr(w, "cache_dtype", "bf16") == "bf16"
+        else w.cache_dtype, "data": "synthetic",
+        "config": cfg,
+        "num_splits": num_splits,
+        "step_us": {"chained": stats(r["step_ms"]),
+                    "separated": {names[0]: stats(rk["write_ms"]), names[1]: stats(rk["decode_ms"]),
+                                  names[2]: stats(rk["merge_ms"]), "step": stats(rk["step_ms"]),
                                   "note": "second K-step pass with an event between launches (no early "
                                           "start of decode/merge); the roofline uses its decode time"}},
         "decode_kv_read_gbs": achieved,
         "decode_hbm_frac": achieved / peak,
-        "rope_kv_write_gbs": write_gbs,
-        "rope_kv_write_hbm_frac": write_gbs / peak,
-        "cache_fill": {"tokens": fill["T"], "us": fill["ms"] * 1e3, "bytes": wb,
-                       "hbm_frac_table_rows_once": wbu / (fill["ms"] * 1e-3) / 1e9 / peak,
-                       "note": "rope_kv_write_gbs counts one cos_sin row per token; hbm_frac_table_rows_once counts "
-                               "each distinct position's row once"},
-        "roofline": {"kernel": kernel_names(args.workload)[1], "bound": "hbm", "achieved": achieved, "peak": peak,
+        "rope_kv_write_gbs": fill["gbs"],
+        "rope_kv_write_hbm_frac": fill["hbm_frac"],
+        "cache_fill": fill,
+        "roofline": {"kernel": names[1], "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload, dw.num_splits),
-                     "alg_bytes_per_launch": alg, "partial_record_bytes": partial_bytes(w, dw.num_splits),
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload, num_splits),
+                     "alg_bytes_per_launch": alg, "partial_record_bytes": partial_bytes(w, num_splits),
                      "stream_read_same_bytes_gbs": ceiling,
                      "stream_read_same_bytes_frac": ceiling / peak,
                      "layered": layered},
         "e2e": None if e2e is None else {"value": world * w.B * args.steps / e2e_s, "unit": UNIT,
-                                         "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+                                         "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                                         "step_us": stats(e2e["step_ms"])},
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "err_flag": err,
     }
-    if others:
-        line["other_workloads"] = others
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if cpu_all is not None:
         line["cpu_baseline_all_cores"] = cpu_all
+    if others:
+        line["other_workloads"] = others
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
