@@ -80,6 +80,10 @@ def _L():
         lib.orc_rope_kv_write_nvfp4.restype = i64
         lib.orc_paged_decode_nvfp4.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, i64, i32, P, P, i32, P,
                                                i32, P, dbl, i32, P, P]
+        lib.orc_paged_decode_splits.argtypes = [i32, i32, i32, i32, i32, P, P, P, i64, i32, i32, P, P, i32, P,
+                                                i32, P, dbl, i32, P, P, P]
+        lib.orc_paged_decode_nvfp4_splits.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, i64, i32, P, P, i32,
+                                                      P, i32, P, dbl, i32, P, P, P]
         lib.orc_mla_cache_write.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, i64, P, P, i64, i32,
                                             ctypes.c_float, P]
         lib.orc_mla_cache_write.restype = i64
@@ -201,8 +205,12 @@ def decode_head(b: int, h: int, Hq: int, q_row, k_cache, v_cache, block_tables, 
 
 
 def paged_decode(q, k_cache, v_cache, block_tables, seq_lens, softmax_scale: float, num_splits: int,
-                 layout: str, k_scale=None, v_scale=None):
-    """q [B,Hq,D] uint16 -> (out_partial [B,S,Hq,D], lse_partial [B,S,Hq]) float64."""
+                 layout: str, k_scale=None, v_scale=None, splits_per_seq=None):
+    """q [B,Hq,D] uint16 -> (out_partial [B,S,Hq,D], lse_partial [B,S,Hq]) float64.
+
+    splits_per_seq (int32 [B], optional): the number of splits each
+    sequence's pages are dealt into (clamped to [1, num_splits]); its
+    records past that count are empty. None = num_splits for every one."""
     q = _c(q, np.uint16)
     B, Hq, D = q.shape
     num_pages, Hkv, P, D2 = _cache_args(k_cache, layout)
@@ -211,12 +219,14 @@ def paged_decode(q, k_cache, v_cache, block_tables, seq_lens, softmax_scale: flo
     ks = None if k_scale is None else _c(k_scale, np.float32)
     vs = None if v_scale is None else _c(v_scale, np.float32)
     bt = _c(block_tables, np.int32); sl = _c(seq_lens, np.int32)
+    sp = None if splits_per_seq is None else _c(splits_per_seq, np.int32)
+    assert sp is None or sp.shape == (B,)
     o = np.empty((B, num_splits, Hq, D), np.float64)
     l = np.empty((B, num_splits, Hq), np.float64)
-    _L().orc_paged_decode(B, Hq, Hkv, D, P, _p(q), _p(_c(k_cache, k_cache.dtype)),
-                          _p(_c(v_cache, v_cache.dtype)), num_pages, LAYOUT[layout], int(fp8), _p(ks),
-                          _p(vs), 0 if ks is None else ks.size, _p(bt), bt.shape[1], _p(sl),
-                          float(softmax_scale), num_splits, _p(o), _p(l))
+    _L().orc_paged_decode_splits(B, Hq, Hkv, D, P, _p(q), _p(_c(k_cache, k_cache.dtype)),
+                                 _p(_c(v_cache, v_cache.dtype)), num_pages, LAYOUT[layout], int(fp8), _p(ks),
+                                 _p(vs), 0 if ks is None else ks.size, _p(bt), bt.shape[1], _p(sl),
+                                 float(softmax_scale), num_splits, _p(sp), _p(o), _p(l))
     return o, l
 
 
@@ -278,7 +288,7 @@ def rope_kv_write_nvfp4(q, k, v, positions, cos_sin, k_cache, v_cache, k_block_s
 
 
 def paged_decode_nvfp4(q, k_cache, v_cache, k_block_scale, v_block_scale, block_tables, seq_lens,
-                       softmax_scale: float, num_splits: int, layout: str, k_scale, v_scale):
+                       softmax_scale: float, num_splits: int, layout: str, k_scale, v_scale, splits_per_seq=None):
     """As paged_decode, for NVFP4 caches (value caches [.., D/2] bytes)."""
     q = _c(q, np.uint16)
     B, Hq, D = q.shape
@@ -288,11 +298,15 @@ def paged_decode_nvfp4(q, k_cache, v_cache, k_block_scale, v_block_scale, block_
         num_pages, P, Hkv, _ = k_cache.shape
     ks = _c(k_scale, np.float32); vs = _c(v_scale, np.float32)
     bt = _c(block_tables, np.int32); sl = _c(seq_lens, np.int32)
+    sp = None if splits_per_seq is None else _c(splits_per_seq, np.int32)
+    assert sp is None or sp.shape == (B,)
     o = np.empty((B, num_splits, Hq, D), np.float64)
     l = np.empty((B, num_splits, Hq), np.float64)
-    _L().orc_paged_decode_nvfp4(B, Hq, Hkv, D, P, _p(q), _p(k_cache), _p(v_cache), _p(k_block_scale),
-                                _p(v_block_scale), num_pages, LAYOUT[layout], _p(ks), _p(vs), ks.size, _p(bt),
-                                bt.shape[1], _p(sl), float(softmax_scale), num_splits, _p(o), _p(l))
+    _L().orc_paged_decode_nvfp4_splits(B, Hq, Hkv, D, P, _p(q), _p(_c(k_cache, np.uint8)),
+                                       _p(_c(v_cache, np.uint8)), _p(_c(k_block_scale, np.uint8)),
+                                       _p(_c(v_block_scale, np.uint8)), num_pages, LAYOUT[layout], _p(ks), _p(vs),
+                                       ks.size, _p(bt), bt.shape[1], _p(sl), float(softmax_scale), num_splits,
+                                       _p(sp), _p(o), _p(l))
     return o, l
 
 

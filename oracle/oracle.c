@@ -378,7 +378,10 @@ static double cache_value(const cache_view* c, int layout, int64_t page, int off
  * G = Hq / Hkv; the context is positions 0..L-1 (L = seq_lens[b], which
  * counts the new token); no mask, window, ALiBi or soft-cap. Split s covers
  * pages [s*pps, min((s+1)*pps, npages)) with npages = ceil(L/P) and
- * pps = ceil(npages / S). Each split is a plain two-pass softmax in float64:
+ * pps = ceil(npages / S_b), where S_b = seq_splits is the number of splits
+ * this sequence's pages are dealt into (the call's num_splits, or a count of
+ * its own per sequence, at most num_splits); records s >= S_b, and any
+ * split past the last page, are empty. Each split is a plain two-pass softmax in float64:
  * m = max score, l = sum exp(score - m), o = sum exp(score - m) * v / l,
  * lse = m + ln l; an empty split gives o = 0, lse = -inf. Scores are
  * softmax_scale * sum_d q_d * k_d with k = cache value * k_scale (FP8) and
@@ -389,7 +392,8 @@ static void decode_head_impl(int b, int h, int Hq, int Hkv, int D, int page_size
                              const cache_view* kc, const cache_view* vc, int64_t num_pages, int layout,
                              const float* k_scale, const float* v_scale, int n_scale,
                              const int32_t* block_tables, int max_pages, const int32_t* seq_lens,
-                             double softmax_scale, int num_splits, double* out_partial, double* lse_partial) {
+                             double softmax_scale, int num_splits, int seq_splits, double* out_partial,
+                             double* lse_partial) {
     int fp8 = kc->fmt != 0;  /* the static per-tensor / per-head scales apply */
     int G = Hq / Hkv;
     int kvh = h / G;
@@ -398,7 +402,7 @@ static void decode_head_impl(int b, int h, int Hq, int Hkv, int D, int page_size
     int64_t npages = (L + page_size - 1) / page_size;
     if (npages > max_pages) npages = max_pages;
     if (L > npages * page_size) L = npages * page_size;
-    int64_t pps = (npages + num_splits - 1) / num_splits;
+    int64_t pps = (npages + seq_splits - 1) / seq_splits;
     double ks = fp8 ? (double)scale_of(k_scale, n_scale, kvh) : 1.0;
     double vs = fp8 ? (double)scale_of(v_scale, n_scale, kvh) : 1.0;
     double* qd = (double*)malloc(sizeof(double) * (size_t)D);
@@ -454,7 +458,8 @@ void orc_decode_head(int b, int h, int Hq, int Hkv, int D, int page_size,
                      int num_splits, double* out_partial, double* lse_partial) {
     cache_view kc = {k_cache, NULL, fp8 ? 1 : 0}, vc = {v_cache, NULL, fp8 ? 1 : 0};
     decode_head_impl(b, h, Hq, Hkv, D, page_size, q_row, &kc, &vc, num_pages, layout, k_scale, v_scale, n_scale,
-                     block_tables, max_pages, seq_lens, softmax_scale, num_splits, out_partial, lse_partial);
+                     block_tables, max_pages, seq_lens, softmax_scale, num_splits, num_splits, out_partial,
+                     lse_partial);
 }
 
 /* NVFP4 caches: value k = g_k * s_block * E2M1 (and likewise v). */
@@ -466,7 +471,59 @@ void orc_decode_head_nvfp4(int b, int h, int Hq, int Hkv, int D, int page_size,
                            double softmax_scale, int num_splits, double* out_partial, double* lse_partial) {
     cache_view kc = {k_cache, k_block_scale, 2}, vc = {v_cache, v_block_scale, 2};
     decode_head_impl(b, h, Hq, Hkv, D, page_size, q_row, &kc, &vc, num_pages, layout, k_scale, v_scale, n_scale,
-                     block_tables, max_pages, seq_lens, softmax_scale, num_splits, out_partial, lse_partial);
+                     block_tables, max_pages, seq_lens, softmax_scale, num_splits, num_splits, out_partial,
+                     lse_partial);
+}
+
+/*
+ * The split count sequence b's pages are dealt into: splits_per_seq[b]
+ * (reading: a count below 1 is taken as 1 and one above num_splits as
+ * num_splits, the records the call has), or num_splits for every sequence
+ * when splits_per_seq is NULL.
+ */
+static int seq_split_count(const int32_t* splits_per_seq, int b, int num_splits) {
+    if (!splits_per_seq) return num_splits;
+    int sb = splits_per_seq[b];
+    if (sb < 1) sb = 1;
+    if (sb > num_splits) sb = num_splits;
+    return sb;
+}
+
+static void paged_decode_all(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
+                             const cache_view* kc, const cache_view* vc, int64_t num_pages, int layout,
+                             const float* k_scale, const float* v_scale, int n_scale,
+                             const int32_t* block_tables, int max_pages, const int32_t* seq_lens,
+                             double softmax_scale, int num_splits, const int32_t* splits_per_seq,
+                             double* out_partial, double* lse_partial) {
+    double* o = (double*)malloc(sizeof(double) * (size_t)num_splits * D);
+    double* l = (double*)malloc(sizeof(double) * (size_t)num_splits);
+    for (int b = 0; b < B; ++b) {
+        int sb = seq_split_count(splits_per_seq, b, num_splits);
+        for (int h = 0; h < Hq; ++h) {
+            decode_head_impl(b, h, Hq, Hkv, D, page_size, q + ((int64_t)b * Hq + h) * D, kc, vc, num_pages, layout,
+                             k_scale, v_scale, n_scale, block_tables, max_pages, seq_lens, softmax_scale, num_splits,
+                             sb, o, l);
+            for (int s = 0; s < num_splits; ++s) {
+                int64_t r = ((int64_t)b * num_splits + s) * Hq + h;
+                lse_partial[r] = l[s];
+                for (int d = 0; d < D; ++d) out_partial[r * D + d] = o[(int64_t)s * D + d];
+            }
+        }
+    }
+    free(l);
+    free(o);
+}
+
+void orc_paged_decode_nvfp4_splits(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
+                                   const uint8_t* k_cache, const uint8_t* v_cache, const uint8_t* k_block_scale,
+                                   const uint8_t* v_block_scale, int64_t num_pages, int layout, const float* k_scale,
+                                   const float* v_scale, int n_scale, const int32_t* block_tables, int max_pages,
+                                   const int32_t* seq_lens, double softmax_scale, int num_splits,
+                                   const int32_t* splits_per_seq, double* out_partial, double* lse_partial) {
+    cache_view kc = {k_cache, k_block_scale, 2}, vc = {v_cache, v_block_scale, 2};
+    paged_decode_all(B, Hq, Hkv, D, page_size, q, &kc, &vc, num_pages, layout, k_scale, v_scale, n_scale,
+                     block_tables, max_pages, seq_lens, softmax_scale, num_splits, splits_per_seq, out_partial,
+                     lse_partial);
 }
 
 void orc_paged_decode_nvfp4(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
@@ -475,22 +532,21 @@ void orc_paged_decode_nvfp4(int B, int Hq, int Hkv, int D, int page_size, const 
                             const float* v_scale, int n_scale, const int32_t* block_tables, int max_pages,
                             const int32_t* seq_lens, double softmax_scale, int num_splits,
                             double* out_partial, double* lse_partial) {
-    double* o = (double*)malloc(sizeof(double) * (size_t)num_splits * D);
-    double* l = (double*)malloc(sizeof(double) * (size_t)num_splits);
-    for (int b = 0; b < B; ++b) {
-        for (int h = 0; h < Hq; ++h) {
-            orc_decode_head_nvfp4(b, h, Hq, Hkv, D, page_size, q + ((int64_t)b * Hq + h) * D, k_cache, v_cache,
-                                  k_block_scale, v_block_scale, num_pages, layout, k_scale, v_scale, n_scale,
-                                  block_tables, max_pages, seq_lens, softmax_scale, num_splits, o, l);
-            for (int s = 0; s < num_splits; ++s) {
-                int64_t r = ((int64_t)b * num_splits + s) * Hq + h;
-                lse_partial[r] = l[s];
-                for (int d = 0; d < D; ++d) out_partial[r * D + d] = o[(int64_t)s * D + d];
-            }
-        }
-    }
-    free(l);
-    free(o);
+    orc_paged_decode_nvfp4_splits(B, Hq, Hkv, D, page_size, q, k_cache, v_cache, k_block_scale, v_block_scale,
+                                  num_pages, layout, k_scale, v_scale, n_scale, block_tables, max_pages, seq_lens,
+                                  softmax_scale, num_splits, NULL, out_partial, lse_partial);
+}
+
+void orc_paged_decode_splits(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
+                             const void* k_cache, const void* v_cache, int64_t num_pages, int layout,
+                             int fp8, const float* k_scale, const float* v_scale, int n_scale,
+                             const int32_t* block_tables, int max_pages, const int32_t* seq_lens,
+                             double softmax_scale, int num_splits, const int32_t* splits_per_seq,
+                             double* out_partial, double* lse_partial) {
+    cache_view kc = {k_cache, NULL, fp8 ? 1 : 0}, vc = {v_cache, NULL, fp8 ? 1 : 0};
+    paged_decode_all(B, Hq, Hkv, D, page_size, q, &kc, &vc, num_pages, layout, k_scale, v_scale, n_scale,
+                     block_tables, max_pages, seq_lens, softmax_scale, num_splits, splits_per_seq, out_partial,
+                     lse_partial);
 }
 
 void orc_paged_decode(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
@@ -499,22 +555,9 @@ void orc_paged_decode(int B, int Hq, int Hkv, int D, int page_size, const uint16
                       const int32_t* block_tables, int max_pages, const int32_t* seq_lens,
                       double softmax_scale, int num_splits, double* out_partial,
                       double* lse_partial) {
-    double* o = (double*)malloc(sizeof(double) * (size_t)num_splits * D);
-    double* l = (double*)malloc(sizeof(double) * (size_t)num_splits);
-    for (int b = 0; b < B; ++b) {
-        for (int h = 0; h < Hq; ++h) {
-            orc_decode_head(b, h, Hq, Hkv, D, page_size, q + ((int64_t)b * Hq + h) * D, k_cache, v_cache,
-                            num_pages, layout, fp8, k_scale, v_scale, n_scale, block_tables, max_pages,
-                            seq_lens, softmax_scale, num_splits, o, l);
-            for (int s = 0; s < num_splits; ++s) {
-                int64_t r = ((int64_t)b * num_splits + s) * Hq + h;
-                lse_partial[r] = l[s];
-                for (int d = 0; d < D; ++d) out_partial[r * D + d] = o[(int64_t)s * D + d];
-            }
-        }
-    }
-    free(l);
-    free(o);
+    orc_paged_decode_splits(B, Hq, Hkv, D, page_size, q, k_cache, v_cache, num_pages, layout, fp8, k_scale,
+                            v_scale, n_scale, block_tables, max_pages, seq_lens, softmax_scale, num_splits, NULL,
+                            out_partial, lse_partial);
 }
 
 /* ---------------------------------------------------------------------- */

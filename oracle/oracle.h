@@ -116,6 +116,23 @@ void orc_paged_decode_nvfp4(int B, int Hq, int Hkv, int D, int page_size, const 
                             const int32_t* seq_lens, double softmax_scale, int num_splits,
                             double* out_partial, double* lse_partial);
 
+/* The decodes above with a split count per sequence: sequence b's pages are
+ * dealt into splits_per_seq[b] splits (clamped to [1, num_splits]; NULL =
+ * num_splits for every sequence); the partial records keep num_splits slots
+ * per sequence, and the slots past a sequence's own splits are empty. */
+void orc_paged_decode_splits(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
+                             const void* k_cache, const void* v_cache, int64_t num_pages, int layout,
+                             int fp8, const float* k_scale, const float* v_scale, int n_scale,
+                             const int32_t* block_tables, int max_pages, const int32_t* seq_lens,
+                             double softmax_scale, int num_splits, const int32_t* splits_per_seq,
+                             double* out_partial, double* lse_partial);
+void orc_paged_decode_nvfp4_splits(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
+                                   const uint8_t* k_cache, const uint8_t* v_cache, const uint8_t* k_block_scale,
+                                   const uint8_t* v_block_scale, int64_t num_pages, int layout, const float* k_scale,
+                                   const float* v_scale, int n_scale, const int32_t* block_tables, int max_pages,
+                                   const int32_t* seq_lens, double softmax_scale, int num_splits,
+                                   const int32_t* splits_per_seq, double* out_partial, double* lse_partial);
+
 /* MLA (absorbed decode form): latent cache ckv [pages][P][Dc] E4M3 bytes and
  * kpe [pages][P][Dr] bf16 bits; see oracle.c. */
 int64_t orc_mla_cache_write(int64_t T, int H, int Dc, int Dr, int page_size, uint16_t* q_pe,

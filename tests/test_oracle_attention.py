@@ -205,3 +205,64 @@ def test_empty_sequence():
     st = oracle_step(w, num_splits=2)
     assert not st["out"][0].any() and np.all(st["lse"][0] == -np.inf)
     assert np.all(np.isfinite(st["out"][1]))
+
+
+# ---- a split count per sequence ------------------------------------------------------
+# Loom Kernels, "Evidence" table, row "Local split-K paged decode": the split
+# is local to each sequence. Reading: sequence b's pages are dealt into its
+# own count S_b of page-granular splits (at most the call's record count S);
+# its records past S_b are empty.
+
+def test_per_sequence_splits_merge_to_the_single_pass():
+    w = synth.custom_workload("vsplit", 21, [1, 16, 17, 200, 333, 64, 5], 8, 2, 128, style="interleaved")
+    st1 = oracle_step(w, num_splits=1)
+    S = 9
+    sp = np.array([1, 3, 9, 5, 9, 2, 4], np.int32)
+    op, lp = oracle.paged_decode(st1["q_rot"], st1["k_cache"], st1["v_cache"], st1["block_tables"],
+                                 st1["seq_lens"], w.softmax_scale, S, w.layout, splits_per_seq=sp)
+    out, lse = oracle.lse_merge(op, lp)
+    assert np.allclose(out, st1["out"], rtol=1e-12, atol=1e-13)
+    assert np.allclose(lse, st1["lse"], rtol=0, atol=1e-12)
+    # records past a sequence's own count are empty
+    for b, sb in enumerate(sp):
+        assert np.all(lp[b, sb:] == -np.inf) and not op[b, sb:].any()
+    # a count of S for every sequence is the uniform call, bit for bit
+    opu, lpu = oracle.paged_decode(st1["q_rot"], st1["k_cache"], st1["v_cache"], st1["block_tables"],
+                                   st1["seq_lens"], w.softmax_scale, S, w.layout)
+    opS, lpS = oracle.paged_decode(st1["q_rot"], st1["k_cache"], st1["v_cache"], st1["block_tables"],
+                                   st1["seq_lens"], w.softmax_scale, S, w.layout,
+                                   splits_per_seq=np.full(w.B, S, np.int32))
+    assert np.array_equal(opu, opS) and np.array_equal(lpu, lpS)
+
+
+def test_per_sequence_splits_partition_the_pages():
+    """Under equal scores (q = 0) a split's LSE is the log of its token
+    count. For every sequence the counts must: add up to L; be whole pages
+    except in the last non-empty split; fill a prefix of at most S_b
+    records; be equal except the last; and use the smallest equal page
+    count with which S_b splits cover the sequence."""
+    lens = [1, 15, 16, 17, 100, 160, 161, 333]
+    w = synth.custom_workload("vpart", 22, lens, 4, 2, 64)
+    st = oracle_step(w, num_splits=1)
+    q0 = np.zeros_like(st["q_rot"])
+    S = 7
+    for sp in (np.array([1, 2, 7, 3, 7, 4, 6, 5], np.int32), np.array([0, 9, -3, 100, 1, 7, 2, 3], np.int32)):
+        op, lp = oracle.paged_decode(q0, st["k_cache"], st["v_cache"], st["block_tables"], st["seq_lens"],
+                                     w.softmax_scale, S, w.layout, splits_per_seq=sp)
+        for b, L in enumerate(lens):
+            sb = min(max(int(sp[b]), 1), S)   # the stated clamp
+            counts = [round(math.exp(x)) if x != -np.inf else 0 for x in lp[b, :, 0]]
+            for x, c in zip(lp[b, :, 0], counts):
+                if c:
+                    assert x == pytest.approx(math.log(c), abs=1e-12)
+            assert sum(counts) == L
+            nz = [c for c in counts if c]
+            k = len(nz)
+            assert counts[:k] == nz and not any(counts[k:])          # a prefix of the records
+            assert k <= sb and k <= -(-L // 16)
+            assert all(c % 16 == 0 for c in nz[:-1])                # whole pages but the last
+            if k > 1:
+                p = nz[0] // 16                                     # pages per split
+                assert all(c == 16 * p for c in nz[:-1])
+                npages = -(-L // 16)
+                assert (p - 1) * sb < npages <= p * sb              # the smallest such count

@@ -243,6 +243,20 @@ def test_nvfp4_split_merge_equals_single_pass():
         assert np.allclose(lse, one["lse"], rtol=0, atol=1e-12)
 
 
+def test_nvfp4_per_sequence_splits_merge_to_the_single_pass():
+    w = synth.custom_workload("fp4v", 81, [1, 15, 16, 17, 200], 6, 2, 64, cache_dtype="nvfp4")
+    one = oracle_step(w, num_splits=1)
+    sp = np.array([1, 4, 2, 6, 3], np.int32)
+    op, lp = oracle.paged_decode_nvfp4(one["q_rot"], one["k_cache"], one["v_cache"], one["k_block_scale"],
+                                       one["v_block_scale"], one["block_tables"], one["seq_lens"],
+                                       w.softmax_scale, 6, w.layout, w.k_scale, w.v_scale, splits_per_seq=sp)
+    out, lse = oracle.lse_merge(op, lp)
+    assert np.allclose(out, one["out"], rtol=1e-12, atol=1e-13)
+    assert np.allclose(lse, one["lse"], rtol=0, atol=1e-12)
+    for b, sb in enumerate(sp):
+        assert np.all(lp[b, sb:] == -np.inf) and not op[b, sb:].any()
+
+
 def test_nvfp4_v_scale_enters_linearly():
     w = synth.custom_workload("fp4l", 80, [20, 45], 4, 2, 64, cache_dtype="nvfp4")
     st = oracle_step(w)
