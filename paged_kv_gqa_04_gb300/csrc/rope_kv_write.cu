@@ -64,56 +64,74 @@ __device__ __forceinline__ uint4 pack_bf16x8(const Chunk8& c) {
     return w;
 }
 
-// True when some float within six representable steps of z may round to a
-// different E4M3 byte than z: z is below the normal E4M3 range (|z| < 2^-6,
-// including zero), or the 20 bits below E4M3's mantissa are within 6 of the
-// midpoint pattern 0x80000, i.e. ((m + 0x80006) mod 2^20) <= 12. Anything
-// else (the E4M3 values themselves and the powers of two where binades
-// change lie far from midpoints; magnitudes of 448 and above all saturate
-// to 448, and the test only errs on the safe side there) keeps its byte.
-__device__ __forceinline__ bool e4m3_byte_may_change(float z) {
-    const uint32_t b = __float_as_uint(z);
-    return (b & 0x7FFFFFFFu) < 0x3C800000u || ((b + 0x80006u) & 0xFFFFFu) <= 12u;
+// Packed float32 product (sm_100+ f32x2 arithmetic): each lane is rounded
+// exactly as the scalar product would be, in one issue slot for two values.
+// Used only where no sum follows the product (the quantisers' scalings),
+// so there is nothing it could be contracted with.
+__device__ __forceinline__ void mul_rn_x2(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// Four E4M3 bytes (a -> byte 0 .. d -> byte 3), saturating round-to-nearest-even.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+        "mov.b32 %0, {l, h};\n\t}"
+        : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+
+// Per-scale constants of the FP8 quantiser: the reciprocal of the scale
+// nudged down and up by 2^-20 (relative), each rounded to float32.
+struct E4m3Rcp {
+    float lo, hi;
+    bool exact_only;  // a scale whose reciprocal could leave float32's normal range
+};
+__device__ __forceinline__ E4m3Rcp e4m3_rcp(float scale) {
+    E4m3Rcp r;
+    r.exact_only = !(scale >= 0x1p-100f && scale <= 0x1p100f);
+    const float rcp = __frcp_rn(scale);
+    r.lo = __fmul_rn(rcp, 1.0f - 0x1p-20f);
+    r.hi = __fmul_rn(rcp, 1.0f + 0x1p-20f);
+    return r;
 }
 
 // E4M3 bytes (low byte first) of the correctly rounded float32 quotients
-// y / scale, saturating, for the 8 values of a chunk. z = RN(y * r) with
-// r = RN(1 / scale) is within two units in the last place of y / scale, so
-// the correctly rounded quotient lies within five representable steps of z.
-// When no value of the chunk is near an E4M3 rounding boundary, the bytes of
-// the products are the bytes of the quotients and no division is needed;
-// otherwise (rare) the chunk is quantised from IEEE divisions.
-__device__ __forceinline__ uint2 pack_e4m3x8(const Chunk8& c, float scale, float rcp) {
-    float z[8];
-    bool near = false;
+// Q = RN(y / scale), saturating, for the 8 values of a chunk, without a
+// division in the common case. With r = RN(1/scale), r_lo = RN(r (1 - 2^-20))
+// and r_hi = RN(r (1 + 2^-20)), the products z_lo = RN(y r_lo) and
+// z_hi = RN(y r_hi) differ from y / scale by factors within
+// (1 - 2^-20)(1 +- 2^-24)^3 and (1 + 2^-20)(1 +- 2^-24)^3, while Q differs from
+// it by a factor within 1 +- 2^-24; so Q lies between z_lo and z_hi (values
+// so small that float32 rounds them absolutely are far below E4M3's smallest
+// step, where every one of the three gives the zero byte of the right
+// sign). E4M3 rounding is monotone, so when z_lo and z_hi give the same byte,
+// Q gives it too. When they differ -- Q is within about 2^-19 (relative) of
+// an E4M3 rounding boundary, about one value in 2^15 -- the chunk is
+// quantised from the IEEE divisions.
+__device__ __forceinline__ uint2 pack_e4m3x8(const Chunk8& c, float scale, const E4m3Rcp& r) {
+    float zl[8], zh[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        z[j] = __fmul_rn(c.v[j], rcp);
-        near |= e4m3_byte_may_change(z[j]);
+    for (int j = 0; j < 8; j += 2) {
+        mul_rn_x2(c.v[j], c.v[j + 1], r.lo, r.lo, zl[j], zl[j + 1]);
+        mul_rn_x2(c.v[j], c.v[j + 1], r.hi, r.hi, zh[j], zh[j + 1]);
     }
-    if (near) {
+    uint32_t w0 = e4m3x4(zl[0], zl[1], zl[2], zl[3]);
+    uint32_t w1 = e4m3x4(zl[4], zl[5], zl[6], zl[7]);
+    const uint32_t h0 = e4m3x4(zh[0], zh[1], zh[2], zh[3]);
+    const uint32_t h1 = e4m3x4(zh[4], zh[5], zh[6], zh[7]);
+    if ((w0 != h0) | (w1 != h1) | r.exact_only) {
+        float z[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) z[j] = __fdiv_rn(c.v[j], scale);
+        w0 = e4m3x4(z[0], z[1], z[2], z[3]);
+        w1 = e4m3x4(z[4], z[5], z[6], z[7]);
     }
-    uint32_t w[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t b0 = __nv_cvt_float2_to_fp8x2(make_float2(z[4 * h], z[4 * h + 1]), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t b1 = __nv_cvt_float2_to_fp8x2(make_float2(z[4 * h + 2], z[4 * h + 3]), __NV_SATFINITE, __NV_E4M3);
-        w[h] = b0 | (b1 << 16);
-    }
-    return make_uint2(w[0], w[1]);
-}
-
-// True when some float within four representable steps of z may have a
-// different E2M1 code than z: |z| in [0.234, 6] with the low 21 bits of its
-// pattern within 4 of zero -- every rounding boundary of E2M1 (0.25, 0.75,
-// 1.25, 1.75, 2.5, 3.5, 5) has those bits zero; so do the E2M1 values and
-// powers of two that the test also catches, harmlessly. Below 0.234 every
-// value gives a zero code, above 6 every value saturates.
-__device__ __forceinline__ bool e2m1_code_may_change(float z) {
-    const uint32_t m = __float_as_uint(z) & 0x7FFFFFFFu;
-    return m >= 0x3E700000u && m <= 0x40C00000u && ((m + 4u) & 0x1FFFFFu) <= 8u;
+    return make_uint2(w0, w1);
 }
 
 __device__ __forceinline__ float amax8(const Chunk8& c) {
@@ -123,33 +141,47 @@ __device__ __forceinline__ float amax8(const Chunk8& c) {
     return m;
 }
 
+// Bracketing reciprocals of a divisor d: RN(RN(1/d) (1 -+ 2^-20)). For any y,
+// RN(y * lo) and RN(y * hi) enclose the correctly rounded quotient RN(y / d)
+// (the argument of pack_e4m3x8), so a monotone rounding that gives both the
+// same code gives the quotient that code too. Divisors whose reciprocal could
+// leave float32's normal range are marked for the division path.
+__device__ __forceinline__ E4m3Rcp bracket_rcp(float d) { return e4m3_rcp(d); }
+
 // One 8-value half of an NVFP4 block whose largest magnitude is `amax`,
-// under the static scale g (six_g = RN(6 g)): returns the four bytes of
-// E2M1 pairs and the block's E4M3 scale byte. z = RN(y * RN(1/(g s))) is
-// within three representable steps of the correctly rounded quotient
-// y / (g s); when no value is near an E2M1 boundary (or the reciprocal could
-// leave the normal range) the codes of the products are those of the
-// quotients, else the quotients are computed.
-__device__ __forceinline__ uint32_t nvfp4_half(const Chunk8& c, float amax, float g, float six_g, uint32_t& sbyte) {
-    const uint32_t sb = __nv_cvt_float_to_fp8(__fdiv_rn(amax, six_g), __NV_SATFINITE, __NV_E4M3);
+// under the static scale g (six_g = RN(6 g), r6 = bracket_rcp(six_g)):
+// returns the four bytes of E2M1 pairs and the block's E4M3 scale byte,
+// which are those of the correctly rounded quotients amax / six_g and
+// y / RN(g s). Each is taken from the bracketing products when both
+// products give the same code, else (rarely) from the IEEE divisions.
+__device__ __forceinline__ uint32_t nvfp4_half(const Chunk8& c, float amax, float g, float six_g,
+                                               const E4m3Rcp& r6, uint32_t& sbyte) {
+    uint32_t sb;
+    {
+        uint16_t bl, bh;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(bl) : "f"(__fmul_rn(amax, r6.hi)), "f"(__fmul_rn(amax, r6.lo)));
+        bh = static_cast<uint16_t>(bl >> 8);
+        bl = static_cast<uint16_t>(bl & 0xFF);
+        sb = bl;
+        if (bl != bh || r6.exact_only)
+            sb = __nv_cvt_float_to_fp8(__fdiv_rn(amax, six_g), __NV_SATFINITE, __NV_E4M3);
+    }
     sbyte = sb;
     const float s = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sb), __NV_E4M3)));
     if (s == 0.f) return 0u;
     const float denom = __fmul_rn(g, s);
+    const E4m3Rcp r = bracket_rcp(denom);
+    float zl[8], zh[8];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        mul_rn_x2(c.v[j], c.v[j + 1], r.lo, r.lo, zl[j], zl[j + 1]);
+        mul_rn_x2(c.v[j], c.v[j + 1], r.hi, r.hi, zh[j], zh[j + 1]);
+    }
+    const uint32_t wl = pack_e2m1x8(zl);
+    if (wl == pack_e2m1x8(zh) && !r.exact_only) return wl;
     float z[8];
-    bool near = !(denom >= 0x1p-100f && denom <= 0x1p100f);
-    if (!near) {
-        const float rcp = __frcp_rn(denom);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            z[j] = __fmul_rn(c.v[j], rcp);
-            near |= e2m1_code_may_change(z[j]);
-        }
-    }
-    if (near) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) z[j] = __fdiv_rn(c.v[j], denom);
-    }
+    for (int j = 0; j < 8; ++j) z[j] = __fdiv_rn(c.v[j], denom);
     return pack_e2m1x8(z);
 }
 
@@ -157,11 +189,6 @@ __device__ __forceinline__ uint32_t lane_id() {
     uint32_t l;
     asm("mov.u32 %0, %%laneid;" : "=r"(l));
     return l;
-}
-
-__device__ __forceinline__ void rot(float x1, float x2, float c, float s, float& y1, float& y2) {
-    y1 = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s));
-    y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
 }
 
 // The cos and sin a thread needs for its two chunks, loaded as four 16-byte
@@ -188,6 +215,17 @@ __device__ __forceinline__ void load_cos_sin(const float* cs, int c, float (&cv)
     sv[4] = b1.x; sv[5] = b1.y; sv[6] = b1.z; sv[7] = b1.w;
 }
 
+__device__ __forceinline__ void rot(float x1, float x2, float c, float s, float& y1, float& y2) {
+    y1 = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s));
+    y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
+}
+
+// y1 = x1 c - x2 s, y2 = x2 c + x1 s for every pair of the row's two chunks,
+// each product and the sum / difference rounded on its own. Scalar
+// operations with explicit rounding: these are never contracted into a
+// fused multiply-add. (The packed f32x2 forms are not used here: the
+// compiler may contract a packed product with the packed sum that reads
+// it, which changes the rounding.)
 template <bool INTER>
 __device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float (&cv)[8], const float (&sv)[8]) {
     if constexpr (!INTER) {
@@ -272,11 +310,17 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
         if (is_q || is_k) load_cos_sin<D, INTER>(a.cos_sin + pos[u] * a.cs_s0, c, cv[u], sv[u]);
     }
 
-    float scale = 1.f, rcp = 1.f;
+    float scale = 1.f, six_g = 1.f;
+    E4m3Rcp r8{1.f, 1.f, false};  // FP8: brackets of 1/scale; NVFP4: of 1/RN(6 g)
     if constexpr (KIND != kBf16) {
         if (!is_q) {
             scale = __ldg((is_k ? a.k_scale : a.v_scale) + (a.n_scale == 1 ? 0 : h));
-            rcp = KIND == kFp8 ? __frcp_rn(scale) : __fmul_rn(6.f, scale);  // nvfp4: RN(6 g)
+            if constexpr (KIND == kFp8) {
+                r8 = e4m3_rcp(scale);
+            } else {
+                six_g = __fmul_rn(6.f, scale);
+                r8 = bracket_rcp(six_g);
+            }
         }
     }
 #pragma unroll
@@ -307,8 +351,8 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
                                                 : page * st[0] + off * st[1] + h * st[2];
         if constexpr (KIND == kFp8) {
             uint8_t* dst = static_cast<uint8_t*>(is_k ? a.k_cache : a.v_cache) + e;
-            *reinterpret_cast<uint2*>(dst + 8 * c) = pack_e4m3x8(lo, scale, rcp);
-            *reinterpret_cast<uint2*>(dst + D / 2 + 8 * c) = pack_e4m3x8(hi, scale, rcp);
+            *reinterpret_cast<uint2*>(dst + 8 * c) = pack_e4m3x8(lo, scale, r8);
+            *reinterpret_cast<uint2*>(dst + D / 2 + 8 * c) = pack_e4m3x8(hi, scale, r8);
         } else if constexpr (KIND == kFp4) {
             // both lanes of the pair (chunks c, c^1 of this row) are here
             const unsigned pair = 3u << (lane_id() & 30u);
@@ -316,8 +360,8 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
             am_lo = fmaxf(am_lo, __shfl_xor_sync(pair, am_lo, 1));
             am_hi = fmaxf(am_hi, __shfl_xor_sync(pair, am_hi, 1));
             uint32_t s_lo, s_hi;
-            const uint32_t w_lo = nvfp4_half(lo, am_lo, scale, rcp, s_lo);
-            const uint32_t w_hi = nvfp4_half(hi, am_hi, scale, rcp, s_hi);
+            const uint32_t w_lo = nvfp4_half(lo, am_lo, scale, six_g, r8, s_lo);
+            const uint32_t w_hi = nvfp4_half(hi, am_hi, scale, six_g, r8, s_hi);
             uint8_t* dst = static_cast<uint8_t*>(is_k ? a.k_cache : a.v_cache) + e;
             *reinterpret_cast<uint32_t*>(dst + 4 * c) = w_lo;
             *reinterpret_cast<uint32_t*>(dst + D / 4 + 4 * c) = w_hi;
@@ -407,12 +451,12 @@ __global__ void __launch_bounds__(1024) mla_cache_write_kernel(const MlaWriteArg
     }
     if (x < kMlaDc / 16) {  // ckv values 16x .. 16x + 15
         const float scale = __ldg(a.ckv_scale);
-        const float rcp = __frcp_rn(scale);
+        const E4m3Rcp r8 = e4m3_rcp(scale);
         const uint16_t* src = a.ckv + t * a.ckv_s0 + 16 * x;
         const uint4 w0 = *reinterpret_cast<const uint4*>(src);
         const uint4 w1 = *reinterpret_cast<const uint4*>(src + 8);
-        const uint2 q0 = pack_e4m3x8(unpack_bf16x8(w0), scale, rcp);
-        const uint2 q1 = pack_e4m3x8(unpack_bf16x8(w1), scale, rcp);
+        const uint2 q0 = pack_e4m3x8(unpack_bf16x8(w0), scale, r8);
+        const uint2 q1 = pack_e4m3x8(unpack_bf16x8(w1), scale, r8);
         *reinterpret_cast<uint4*>(a.ckv_cache + page * a.cc_s0 + off * a.cc_s1 + 16 * x) =
             make_uint4(q0.x, q0.y, q1.x, q1.y);
         return;
