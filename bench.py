@@ -86,7 +86,12 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="ragged", choices=sorted(WORKLOAD_TEXT))
-    p.add_argument("--splits", type=int, default=0, help="num_splits (0 = the library's heuristic)")
+    p.add_argument("--splits", type=int, default=0,
+                   help="one split count for every sequence (0 = the library's split plan, or its heuristic "
+                        "count with --split-mode uniform)")
+    p.add_argument("--split-mode", default="plan", choices=["plan", "uniform"],
+                   help="plan: a split count per sequence from pkv_plan_splits (GQA workloads); "
+                        "uniform: one count for the batch from pkv_choose_num_splits")
     p.add_argument("--also", default="qwen,longctx,fp8,fp4,million,mla,mla_batch",
                    help="other workloads measured the same way, reported under 'other_workloads' ('' = none)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -228,16 +233,20 @@ def _profile_fields(path: str) -> dict:
     return out
 
 
-def ncu_traffic(workload: str, num_splits: int):
+def ncu_traffic(workload: str, splits: dict):
     """DRAM bytes per decode launch from the committed ncu summary of this
-    workload, if it was taken on the current kernel source and with the
-    same split count (else None)."""
+    workload, if it was taken on the current kernel source with the same
+    split configuration (mode and record count; for a plan, also its item
+    count), else None."""
     f = _profile_fields(os.path.join(ROOT, "profiles", f"{kernel_names(workload)[1]}_{workload}.md"))
     try:
         h, t, s = f["kernel_source_sha256_16"], float(f["dram_bytes_per_launch"]), int(f["num_splits"])
+        mode = f.get("split_mode", "uniform")
+        items = int(f.get("plan_items", "0"))
     except (KeyError, ValueError):
         return None
-    return t if (h == decode_kernel_source_hash(workload) and s == num_splits and t) else None
+    same = mode == splits["mode"] and s == splits["records"] and (mode != "plan" or items == splits["items"])
+    return t if (h == decode_kernel_source_hash(workload) and same and t) else None
 
 
 def ncu_fill_traffic(workload: str, tokens: int):
@@ -499,14 +508,35 @@ def measure_layered(dw, layers: int, reps: int, flush, peak: float) -> dict:
     return dict(layers=layers, us_per_layer=1e3 * ms / layers, gbs=gbs, frac=gbs / peak, layers_agree=ok)
 
 
+def make_workload(name: str, splits: int, split_mode: str):
+    """The device workload with its split configuration: an explicit count,
+    else the library's split plan (GQA) or its heuristic count."""
+    from paged_kv_gqa_04_gb300 import harness
+    dw = harness.make_device_workload(name, num_splits=splits or None)
+    if not splits and split_mode == "plan" and not is_mla(name):
+        dw.set_plan()
+    return dw
+
+
+def split_desc(dw) -> dict:
+    """The split configuration of a workload, for the JSON line."""
+    if getattr(dw, "planned", False):
+        sp, work = dw.plan_host
+        pages = dw.w.pages_per_seq
+        pps = -(-pages // np.maximum(sp, 1))
+        return {"mode": "plan", "records": dw.num_splits, "items": int(len(work)),
+                "ctas": int(len(work)) * dw.w.Hkv, "splits_per_seq_min": int(sp.min()),
+                "splits_per_seq_max": int(sp.max()), "max_pages_per_split": int(pps.max())}
+    return {"mode": "uniform", "records": dw.num_splits}
+
+
 def measure_workload(name: str, splits: int, reps: int, flush, peak: float, cpu_seconds: float,
-                     with_e2e: bool = True, with_cpu: bool = True) -> dict:
+                     with_e2e: bool = True, with_cpu: bool = True, split_mode: str = "plan") -> dict:
     """Every figure of one workload: the decode kernel alone (`reps` flushed
     launches), the chained and separated step, the step end to end with
     host buffers, the cache-fill call, decode layered over distinct caches,
     and the oracle on the host (single thread and all cores)."""
-    from paged_kv_gqa_04_gb300 import harness
-    dw = harness.make_device_workload(name, num_splits=splits or None)
+    dw = make_workload(name, splits, split_mode)
     w = dw.w
     fi = fill_cache(dw)
     d = dw.upload_decode()
@@ -534,9 +564,9 @@ def measure_workload(name: str, splits: int, reps: int, flush, peak: float, cpu_
     del fi
     alg = decode_alg_bytes(w)
     r = dict(workload=WORKLOAD_TEXT[name], batch=w.B, context_tokens=int(w.seq_lens.sum()),
-             num_splits=dw.num_splits, decode_us=ms * 1e3, decode_us_stats=stats(dec),
+             num_splits=dw.num_splits, splits=split_desc(dw), decode_us=ms * 1e3, decode_us_stats=stats(dec),
              decode_gbs=alg / (ms * 1e-3) / 1e9, decode_frac=alg / (ms * 1e-3) / 1e9 / peak,
-             decode_traffic=ncu_traffic(name, dw.num_splits), decode_alg_bytes=alg,
+             decode_traffic=ncu_traffic(name, split_desc(dw)), decode_alg_bytes=alg,
              stream_read_frac_same_bytes=stream_ceiling(alg, flush) / peak, layered=layered, step=step,
              cache_fill=fill_figures(w, fill, peak, name), err_flag=int(dw.err.item()))
     if with_e2e:
@@ -773,10 +803,8 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
     import __graft_entry__
     __graft_entry__.build()
-    from paged_kv_gqa_04_gb300 import harness
-
     peak, peak_kind = hbm_peak()
-    dw = harness.make_device_workload(args.workload, num_splits=args.splits or None)
+    dw = make_workload(args.workload, args.splits, args.split_mode)
     w = dw.w
     fi = fill_cache(dw)
     dw.upload_decode()
@@ -811,6 +839,7 @@ def main():
     ceiling = stream_ceiling(alg, flush)
     layered = measure_layered(dw, 4 if alg < 1e9 else 2, 10, flush, peak)
     num_splits = dw.num_splits
+    splits = split_desc(dw)
     del dw
     torch.cuda.empty_cache()
     others = {}
@@ -818,7 +847,8 @@ def main():
         for name in [x for x in args.also.split(",") if x and x != args.workload]:
             others[name] = measure_workload(name, 0, 20, flush, peak, args.cpu_seconds_other,
                                             with_e2e=not args.no_e2e,
-                                            with_cpu=rank == 0 and not args.no_cpu_baseline)
+                                            with_cpu=rank == 0 and not args.no_cpu_baseline,
+                                            split_mode=args.split_mode)
 
     cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -835,6 +865,7 @@ def main():
         else w.cache_dtype, "data": "synthetic",
         "config": cfg,
         "num_splits": num_splits,
+        "splits": splits,
         "step_us": {"chained": stats(r["step_ms"]),
                     "separated": {names[0]: stats(rk["write_ms"]), names[1]: stats(rk["decode_ms"]),
                                   names[2]: stats(rk["merge_ms"]), "step": stats(rk["step_ms"]),
@@ -848,7 +879,7 @@ def main():
         "roofline": {"kernel": names[1], "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload, num_splits),
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(args.workload, splits),
                      "alg_bytes_per_launch": alg, "partial_record_bytes": partial_bytes(w, num_splits),
                      "stream_read_same_bytes_gbs": ceiling,
                      "stream_read_same_bytes_frac": ceiling / peak,

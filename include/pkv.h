@@ -88,6 +88,7 @@ typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1, PKV_F32 = 2, PKV_I32 = 3, PKV_FP4
 #define PKV_FLAG_SEQ_LEN_RANGE  0x08  /* seq_lens entry < 0 or > block-table width * 16      */
 #define PKV_FLAG_DUPLICATE_SLOT 0x10  /* two tokens of one call map to the same slot         */
 #define PKV_FLAG_WAIT_TIMEOUT   0x20  /* an in-kernel wait gave up after its time limit      */
+#define PKV_FLAG_PLAN_RANGE     0x40  /* a split plan entry outside the batch or its records */
 
 typedef struct {
     void*   ptr;        /* device address (NULL allowed only where stated) */
@@ -366,6 +367,95 @@ pkv_status pkv_lse_merge(const pkv_tensor* out_partial, const pkv_tensor* lse_pa
                          const pkv_tensor* lse_out, pkv_stream_t stream);
 
 /*
+ * Split plans: a split count of its own for every sequence.
+ * (Loom Kernels, "Evidence" table, row "Local split-K paged decode": the
+ *  split-K is local to each sequence; mainarch, decode-attention section:
+ *  split-KV over long contexts, then the combine.)
+ *
+ * With one split count for the whole batch, a batch of mixed lengths gives
+ * CTAs of very different sizes and the step waits for the longest. A plan
+ * deals sequence b's pages into S_b splits of its own, so that every CTA
+ * streams about the same number of pages: for sequence b (npages =
+ * ceil(L/16)), split s in [0, S_b) covers pages [s*pps, min((s+1)*pps,
+ * npages)), pps = ceil(npages / S_b) -- pkv_paged_gqa_decode's rule with
+ * S_b in place of num_splits. The partial records keep the layout
+ * [B, S, Hq, D] (S >= max S_b); sequence b writes records [0, S_b) and its
+ * records [S_b, S) are neither written nor read.
+ */
+
+/*
+ * pkv_plan_splits -- the host-side plan (no CUDA call).
+ *
+ * seq_lens       host [B] int32 (each clamped to [0, 16*max_pages], as the
+ *                decode does).
+ * Hkv, Hq, D, cache_dtype, sm_count  as for pkv_choose_num_splits
+ *                (cache_dtype PKV_BF16, PKV_FP8_E4M3 or PKV_FP4_E2M1X2).
+ * max_pages      the block-table width.
+ * max_splits     the largest S_b allowed, in [1, 4095] (the records the
+ *                caller will allocate at most).
+ * target_pages   pages per split to aim for; 0 = chosen by a cost model of
+ *                the decode on GB300 (per-CTA start-up, per-page streaming,
+ *                HBM time, partial records), the plan's counterpart of
+ *                pkv_choose_num_splits.
+ * splits_per_seq host [B] int32, out: S_b = min(max_splits,
+ *                ceil(npages / T)), at least 1, reduced to the splits that
+ *                hold pages when that keeps the same page ranges.
+ * num_records    out: max_b S_b, the S to allocate the partials with.
+ * work           host [work_capacity, 2] int32, out (may be NULL with
+ *                work_capacity 0 to size the plan): one (sequence, split)
+ *                item per CTA, item i = ((b << 12) | s, first page of the
+ *                split), ordered by decreasing page count (ties by b, s) so
+ *                the longest items are dispatched first.
+ * num_work       out: sum_b S_b, the number of items.
+ * Returns PKV_ERR_INVALID_ARG on inconsistent sizes or null outputs, or when
+ * work is given and work_capacity < num_work (the counts are still
+ * written); PKV_ERR_UNSUPPORTED for B > 2^19 or max_pages > 2^26.
+ */
+pkv_status pkv_plan_splits(const int32_t* seq_lens, int32_t B, int32_t Hkv, int32_t Hq, int32_t D,
+                           int32_t max_pages, int32_t cache_dtype, int32_t sm_count, int32_t max_splits,
+                           int32_t target_pages, int32_t* splits_per_seq, int32_t* num_records, int32_t* work,
+                           int64_t work_capacity, int64_t* num_work);
+
+/*
+ * pkv_paged_gqa_decode_planned -- pkv_paged_gqa_decode (or, with block
+ * scales, pkv_paged_gqa_decode_nvfp4) under a split plan: one CTA per work
+ * item and kv head.
+ *
+ * k_block_scale,
+ * v_block_scale  NULL (or ptr NULL) for bf16 / FP8 caches; the NVFP4 block-
+ *                scale caches for NVFP4 caches (HND only).
+ * splits_per_seq device [B] int32: the plan's S_b.
+ * work           device [W, 2] int32 (strides 2, 1; 8-byte aligned): the
+ *                plan's items. Every (b, s < S_b) should appear once; the
+ *                second word is only a hint for an early block-table read
+ *                (a plan made from other lengths stays correct, its page
+ *                ranges follow this call's seq_lens).
+ * out_partial    [B, S, Hq, D] float32 with S >= every S_b, S <= 4095.
+ * lse_partial    [B, S, Hq] float32.
+ * Every other argument is that of the uniform decode. The computation of
+ * each written record is that of pkv_paged_gqa_decode with S_b splits.
+ * Errors: besides the uniform decode's, an item whose sequence is outside
+ * [0, B) or whose split is >= S is skipped and S_b outside [1, S], or an
+ * item with s >= S_b, sets PKV_FLAG_PLAN_RANGE (S_b is clamped).
+ */
+pkv_status pkv_paged_gqa_decode_planned(const pkv_tensor* q, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                                        const pkv_tensor* k_block_scale, const pkv_tensor* v_block_scale,
+                                        const pkv_tensor* block_tables, const pkv_tensor* seq_lens,
+                                        float softmax_scale, const pkv_tensor* splits_per_seq,
+                                        const pkv_tensor* work, const pkv_tensor* out_partial,
+                                        const pkv_tensor* lse_partial, const pkv_tensor* k_scale,
+                                        const pkv_tensor* v_scale, int32_t layout, int32_t* err_flag,
+                                        pkv_stream_t stream);
+
+/*
+ * pkv_lse_merge_planned -- pkv_lse_merge of each sequence's own records
+ * [0, S_b) (S_b = splits_per_seq[b], device [B] int32, clamped to [1, S]).
+ */
+pkv_status pkv_lse_merge_planned(const pkv_tensor* out_partial, const pkv_tensor* lse_partial,
+                                 const pkv_tensor* splits_per_seq, const pkv_tensor* out, const pkv_tensor* lse_out,
+                                 pkv_stream_t stream);
+
+/*
  * pkv_choose_num_splits -- split count for pkv_paged_gqa_decode (host only,
  * no GPU work). (mainarch, MLA decode section: split-K of 64 vs 8 changes the
  * per-token time about threefold; Loom Kernels, "Evidence" table, row
@@ -495,7 +585,7 @@ const char* pkv_status_string(int32_t status);
 
 /* ABI version of this header (bumped on any signature change). */
 int32_t pkv_abi_version(void);
-#define PKV_ABI_VERSION 5
+#define PKV_ABI_VERSION 6
 
 #ifdef __cplusplus
 }

@@ -26,6 +26,7 @@ FLAG_PAGE_RANGE = 0x04
 FLAG_SEQ_LEN_RANGE = 0x08
 FLAG_DUPLICATE_SLOT = 0x10
 FLAG_WAIT_TIMEOUT = 0x20
+FLAG_PLAN_RANGE = 0x40
 
 _DTYPES = {
     torch.bfloat16: 0,
@@ -41,7 +42,8 @@ EXPORTED = ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_c
             "pkv_validate_indices", "pkv_status_string", "pkv_abi_version", "pkv_stream_read",
             "pkv_validate_indices_static", "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4",
             "pkv_mla_cache_write", "pkv_paged_mla_decode", "pkv_choose_num_splits_mla",
-            "pkv_selftest_bounded_wait", "pkv_copy")
+            "pkv_selftest_bounded_wait", "pkv_copy", "pkv_plan_splits", "pkv_paged_gqa_decode_planned",
+            "pkv_lse_merge_planned")
 
 
 class PkvTensor(ctypes.Structure):
@@ -83,12 +85,17 @@ def lib() -> ctypes.CDLL:
         L.pkv_selftest_bounded_wait.argtypes = [ctypes.c_int64, P, P, P]
         L.pkv_copy.argtypes = [P, P, ctypes.c_int64, P]
         L.pkv_validate_indices_static.argtypes = [T, T, T, ctypes.c_int64, P, P]
+        L.pkv_plan_splits.argtypes = [P, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P, P, ctypes.c_int64, P]
+        L.pkv_paged_gqa_decode_planned.argtypes = [T, T, T, T, T, T, T, ctypes.c_float, T, T, T, T, T, T, i32, P,
+                                                   P]
+        L.pkv_lse_merge_planned.argtypes = [T, T, T, T, T, P]
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         for name in ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_validate_indices",
                      "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read", "pkv_validate_indices_static",
                      "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4", "pkv_mla_cache_write",
-                     "pkv_paged_mla_decode", "pkv_choose_num_splits_mla", "pkv_selftest_bounded_wait", "pkv_copy"):
+                     "pkv_paged_mla_decode", "pkv_choose_num_splits_mla", "pkv_selftest_bounded_wait", "pkv_copy",
+                     "pkv_plan_splits", "pkv_paged_gqa_decode_planned", "pkv_lse_merge_planned"):
             getattr(L, name).restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -220,6 +227,45 @@ def choose_num_splits(B: int, Hkv: int, Hq: int, D: int, total_pages: int, max_p
     """Split count from the library's heuristic (host only)."""
     return int(lib().pkv_choose_num_splits(B, Hkv, Hq, D, int(total_pages), max_pages,
                                            _CACHE_DTYPE[cache_dtype], sm_count))
+
+
+def plan_splits(seq_lens, Hkv: int, Hq: int, D: int, max_pages: int, cache_dtype: str, sm_count: int,
+                max_splits: int = 4095, target_pages: int = 0):
+    """pkv_plan_splits (host only): (splits_per_seq int32 [B], num_records,
+    work int32 [W, 2]) for the planned decode and merge."""
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = int(sl.size)
+    sp = np.zeros(max(B, 1), np.int32)
+    nrec = ctypes.c_int32(0)
+    nwork = ctypes.c_int64(0)
+    f = lib().pkv_plan_splits
+    args = (sl.ctypes.data if B else None, B, Hkv, Hq, D, max_pages, _CACHE_DTYPE[cache_dtype], sm_count,
+            max_splits, target_pages, sp.ctypes.data)
+    _check("pkv_plan_splits", f(*args, ctypes.byref(nrec), None, 0, ctypes.byref(nwork)))
+    work = np.zeros((max(int(nwork.value), 1), 2), np.int32)
+    _check("pkv_plan_splits", f(*args, ctypes.byref(nrec), work.ctypes.data, int(nwork.value), ctypes.byref(nwork)))
+    return sp[:B], int(nrec.value), work[:int(nwork.value)]
+
+
+def paged_gqa_decode_planned(q, k_cache, v_cache, block_tables, seq_lens, softmax_scale: float, splits_per_seq,
+                             work, out_partial, lse_partial, k_scale=None, v_scale=None, layout: str = "HND",
+                             err_flag=None, stream=None, k_block_scale=None, v_block_scale=None) -> None:
+    """pkv_paged_gqa_decode_planned: the decode under a split plan (device
+    splits_per_seq [B] and work [W, 2] int32 from plan_splits); NVFP4 caches
+    when the block-scale caches are given."""
+    fp4 = k_block_scale is not None
+    kc, vc = (_fp4(k_cache), _fp4(v_cache)) if fp4 else (_desc(k_cache), _desc(v_cache))
+    _check("pkv_paged_gqa_decode_planned", lib().pkv_paged_gqa_decode_planned(
+        _desc(q), kc, vc, _desc(k_block_scale), _desc(v_block_scale), _desc(block_tables), _desc(seq_lens),
+        float(softmax_scale), _desc(splits_per_seq), _desc(work), _desc(out_partial), _desc(lse_partial),
+        _desc(k_scale), _desc(v_scale), LAYOUTS[layout], _ptr(err_flag), _stream(stream)))
+
+
+def lse_merge_planned(out_partial, lse_partial, splits_per_seq, out, lse_out=None, stream=None) -> None:
+    """pkv_lse_merge_planned: each sequence's own records [0, S_b)."""
+    _check("pkv_lse_merge_planned", lib().pkv_lse_merge_planned(
+        _desc(out_partial), _desc(lse_partial), _desc(splits_per_seq), _desc(out), _desc(lse_out), _stream(stream)))
 
 
 def validate_indices(block_tables, seq_lens, slot_mapping, num_pages: int, err_flag, slot_bitmap=None,

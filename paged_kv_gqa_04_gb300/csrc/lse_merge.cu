@@ -118,6 +118,14 @@ __device__ __forceinline__ void store_row(uint16_t* dst, const float (&o)[V]) {
     }
 }
 
+// The records merged for sequence b: its own split count under a split plan
+// (clamped to [1, S]; out-of-range counts were flagged by the decode), else
+// all S.
+__device__ __forceinline__ int records_of(const MergeArgs& a, int b) {
+    if (a.splits_per_seq == nullptr) return a.S;
+    return min(max(__ldg(a.splits_per_seq + b), 1), a.S);
+}
+
 // Columns of a row one warp merges, and the slices a row is cut into.
 template <int D>
 struct Slice {
@@ -141,7 +149,7 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs 
     const int h = static_cast<int>(row % a.Hq);
     float m, l, acc[V];
     warp_merge<V, 16>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1, a.out_partial + b * a.op_s0 + h * a.op_s2 + c0,
-                      a.op_s1, 0, a.S, m, l, acc);
+                      a.op_s1, 0, records_of(a, b), m, l, acc);
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] *= inv;
@@ -172,8 +180,9 @@ __global__ void __launch_bounds__(kTreeWarps * 32) lse_merge_tree_kernel(const M
     const int c0 = static_cast<int>(blockIdx.x % NS) * DW;  // first column of this CTA's slice
     const int b = static_cast<int>(row / a.Hq);
     const int h = static_cast<int>(row % a.Hq);
-    const int chunk = (a.S + W - 1) / W;
-    const int s_lo = min(a.S, warp * chunk), s_hi = min(a.S, s_lo + chunk);
+    const int S = records_of(a, b);
+    const int chunk = (S + W - 1) / W;
+    const int s_lo = min(S, warp * chunk), s_hi = min(S, s_lo + chunk);
     float m, l, acc[V];
     warp_merge<V, 8>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1,
                      a.out_partial + b * a.op_s0 + h * a.op_s2 + c0 + lane * V, a.op_s1, s_lo, s_hi, m, l, acc);

@@ -28,7 +28,8 @@
 //   heads 2t, 2t+1; a head's max over the page is three xor-shuffles over
 //   the eight lanes g
 //   P^T as the B operand: the f16/bf16-packed S^T fragment of each 8-token
-//   half, transposed in registers with movmatrix
+//   half, transposed in registers with movmatrix (bf16: two terms, the
+//   rounded weight and its rounded rest, each multiplied by V^T)
 //   O^T[16 d x 8 h] += V^T[16 x 16 tok] . P^T    D/16 m-tiles
 // With the cache as the A operand one mma covers 16 tokens (K) or 16
 // head-dim values (V) of all the group's heads: half the mma count of the
@@ -157,35 +158,61 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(KIND, NH))
     const int warp = threadIdx.x >> 5;
     const int g = lane >> 2;
     const int t = lane & 3;
-    const int s = blockIdx.x;
     const int kvh = blockIdx.y;
-    const int b = blockIdx.z;
     const int G = a.G;
     const int h0 = kvh * G;
+
+    // ---- which split of which sequence ----------------------------------------
+    // Uniform launch: split blockIdx.x of sequence blockIdx.z, every sequence
+    // in num_splits splits. Planned launch: work item blockIdx.x names the
+    // sequence and the split, and the sequence's own split count comes from
+    // splits_per_seq (clamped to [1, num_splits], the records there are).
+    int b, s, p0_guess;
+    if (a.work == nullptr) {
+        s = blockIdx.x;
+        b = blockIdx.z;
+        p0_guess = s * ((a.max_pages + a.num_splits - 1) / a.num_splits);
+    } else {
+        const int2 e = __ldg(reinterpret_cast<const int2*>(a.work) + blockIdx.x);
+        b = e.x >> 12;
+        s = e.x & 0xFFF;
+        p0_guess = min(max(e.y, -1), a.max_pages);  // a hint only: kept in range, checked below
+        if (b < 0 || b >= a.B || s >= a.num_splits) {  // an entry outside the batch or the records
+            if (threadIdx.x == 0 && kvh == 0) flag_error(a.err, PKV_FLAG_PLAN_RANGE);
+            grid_dep_wait();
+            grid_dep_launch();
+            return;
+        }
+    }
 
     // ---- sequence bounds and this split's page range -----------------------
     // The block-table entries this warp needs first depend on the split's
     // first page, which depends on seq_len. They are read at the same time as
-    // seq_len from the position a sequence of the full block-table width
-    // would start at; the guess is kept when it turns out right (always, for
-    // equal lengths) and re-read otherwise.
-    const int pps_guess = (a.max_pages + a.num_splits - 1) / a.num_splits;
-    const int p0_guess = s * pps_guess;
+    // seq_len from a guessed first page -- where a sequence of the full
+    // block-table width would start (uniform), or the plan's first page
+    // (planned); the guess is kept when it turns out right (always, for
+    // equal lengths or a plan made from these lengths) and re-read otherwise.
     const int32_t* bt_row = a.block_tables + b * a.bt_s0;
     auto guess_at = [&](int k) -> int {
         const int p = p0_guess + warp + kWarps * (k * 32 + lane);
-        return p < a.max_pages ? __ldg(bt_row + p) : -1;
+        return (p >= 0 && p < a.max_pages) ? __ldg(bt_row + p) : -1;  // a plan's hint may be anything
     };
     const int cur_guess = guess_at(0);
     const int nxt_guess = guess_at(1);
     int L = __ldg(a.seq_lens + b);
+    int S_b = a.num_splits;
+    if (a.splits_per_seq != nullptr) {
+        const int r = __ldg(a.splits_per_seq + b);
+        S_b = min(max(r, 1), a.num_splits);
+        if ((r != S_b || s >= S_b) && threadIdx.x == 0 && kvh == 0) flag_error(a.err, PKV_FLAG_PLAN_RANGE);
+    }
     const int cap = a.max_pages * kPageSize;
     if (L < 0 || L > cap) {
         if (threadIdx.x == 0 && s == 0 && kvh == 0) flag_error(a.err, PKV_FLAG_SEQ_LEN_RANGE);
         L = L < 0 ? 0 : cap;
     }
     const int npages = (L + kPageSize - 1) / kPageSize;
-    const int pps = (npages + a.num_splits - 1) / a.num_splits;
+    const int pps = (npages + S_b - 1) / S_b;
     const int p0 = s * pps;
     const int p1 = min(p0 + pps, npages);
     float* outp = a.out_partial + b * a.op_s0 + s * a.op_s1 + h0 * a.op_s2;
@@ -398,7 +425,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(KIND, NH))
     // O^T += V^T P^T for the page at vb; tokens at or past `valid` contribute
     // zero (their V bytes may be anything, so they are zeroed, not only
     // weighted 0). pb[ht] = P^T fragments of head tile ht.
-    auto pv_page = [&](uint32_t vb, int valid, const uint32_t (*pb)[2]) {
+    auto pv_page = [&](uint32_t vb, int valid, const uint32_t (*pb)[2], const uint32_t (*pl)[2]) {
         if constexpr (KIND == kBf16) {
             uint32_t mk0 = 0xFFFFFFFFu, mk1 = 0xFFFFFFFFu;
             if (valid < kPageSize) {
@@ -417,7 +444,10 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(KIND, NH))
                 a2 &= mk1;
                 a3 &= mk1;
 #pragma unroll
-                for (int ht = 0; ht < NH; ++ht) mma16816<false>(acc[ht][md], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);
+                for (int ht = 0; ht < NH; ++ht) {
+                    mma16816<false>(acc[ht][md], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);
+                    mma16816<false>(acc[ht][md], a0, a1, a2, a3, pl[ht][0], pl[ht][1]);
+                }
             }
         } else if constexpr (KIND == kFp8) {
             constexpr int NWD = D / 32;  // words of V bytes per token row per thread
@@ -561,7 +591,12 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(KIND, NH))
                     }
             }
             // ---- P^T fragments: pack S^T's 8-token halves, transpose ----------
-            uint32_t pb[NH][2];
+            // f16 weights keep 11 significant bits. bf16 keeps 8, too few
+            // where the weighted values cancel (a relative error of 2^-9 of
+            // each weight times |V|): bf16 weights are split into a rounded
+            // term and the rounded rest, P = P_hi + P_lo to 2^-17, and V^T
+            // meets both terms.
+            uint32_t pb[NH][2], pl[NH][2];
 #pragma unroll
             for (int ht = 0; ht < NH; ++ht) {
                 uint32_t x0, x1;
@@ -571,11 +606,15 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(KIND, NH))
                 } else {
                     x0 = pack_bf16(pr[ht][0], pr[ht][1]);
                     x1 = pack_bf16(pr[ht][2], pr[ht][3]);
+                    const uint32_t y0 = pack_bf16(pr[ht][0] - bf16_lo(x0), pr[ht][1] - bf16_hi(x0));
+                    const uint32_t y1 = pack_bf16(pr[ht][2] - bf16_lo(x1), pr[ht][3] - bf16_hi(x1));
+                    pl[ht][0] = movmatrix_trans(y0);
+                    pl[ht][1] = movmatrix_trans(y1);
                 }
                 pb[ht][0] = movmatrix_trans(x0);
                 pb[ht][1] = movmatrix_trans(x1);
             }
-            pv_page(kslot + C::PAGE, valid, pb);
+            pv_page(kslot + C::PAGE, valid, pb, pl);
         }
 
         // ---- refill the consumed slot with page i + NSLOT -------------------
@@ -677,7 +716,7 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
     auto kern = paged_decode_kernel<D, KIND, NH>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    const dim3 grid(a.num_splits, a.Hkv, a.B);
+    const dim3 grid = a.work ? dim3(static_cast<unsigned>(a.n_work), a.Hkv, 1) : dim3(a.num_splits, a.Hkv, a.B);
     return launch_dependent(kern, grid, dim3(kWarps * 32), C::SMEM, s, tk, tv, a, hnd);
 }
 
@@ -705,7 +744,7 @@ int decode_ctas_per_sm(int D, int kind, int G) {
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t s) {
-    if (a.B == 0) return cudaSuccess;
+    if (a.B == 0 || (a.work != nullptr && a.n_work == 0)) return cudaSuccess;
     const int hnd = a.layout == PKV_HND;
     if (a.D == 128) return launch_d<128>(a, tk, tv, hnd, s);
     if (a.D == 64) return launch_d<64>(a, tk, tv, hnd, s);

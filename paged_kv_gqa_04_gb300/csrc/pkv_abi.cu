@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <vector>
+#include <algorithm>
 #include <cstdint>
 #include <atomic>
 #include <mutex>
@@ -360,7 +362,9 @@ static pkv_status paged_gqa_decode_impl(const pkv_tensor* q_p, const pkv_tensor*
                                         const pkv_tensor* seq_lens_p, float softmax_scale, int32_t num_splits,
                                         const pkv_tensor* out_partial_p, const pkv_tensor* lse_partial_p,
                                         const pkv_tensor* k_scale_p, const pkv_tensor* v_scale_p, int32_t layout,
-                                        int32_t* err_flag, pkv_stream_t stream, bool nvfp4) {
+                                        int32_t* err_flag, pkv_stream_t stream, bool nvfp4,
+                                        const pkv_tensor* splits_per_seq_p = nullptr,
+                                        const pkv_tensor* work_p = nullptr) {
     const pkv_tensor& q = arg(q_p);
     const pkv_tensor& k_cache = arg(k_cache_p);
     const pkv_tensor& v_cache = arg(v_cache_p);
@@ -413,10 +417,29 @@ static pkv_status paged_gqa_decode_impl(const pkv_tensor* q_p, const pkv_tensor*
     if (block_tables.stride[1] != 1 || seq_lens.stride[0] != 1) return PKV_ERR_UNSUPPORTED;
     if (out_partial.stride[3] != 1 || lse_partial.stride[2] != 1) return PKV_ERR_UNSUPPORTED;
 
+    const bool planned = work_p != nullptr;
+    int64_t n_work = 0;
+    if (planned) {
+        const pkv_tensor& sp = arg(splits_per_seq_p);
+        const pkv_tensor& wk = arg(work_p);
+        if (!shape_ok(sp, 1, PKV_I32) || sp.shape[0] != B || !sp.ptr) return PKV_ERR_INVALID_ARG;
+        if (!shape_ok(wk, 2, PKV_I32) || wk.shape[1] != 2) return PKV_ERR_INVALID_ARG;
+        n_work = wk.shape[0];
+        if (n_work > 0 && !wk.ptr) return PKV_ERR_INVALID_ARG;
+        if (sp.stride[0] != 1 || wk.stride[1] != 1 || wk.stride[0] != 2 || !aligned(wk.ptr, 8))
+            return PKV_ERR_UNSUPPORTED;
+        if (n_work > 0x7FFFFFFF || num_splits > 4095 || B > (1 << 19)) return PKV_ERR_UNSUPPORTED;
+    }
+
     CUtensorMap tk, tv;
     if (!make_cache_map(&tk, k_cache, layout) || !make_cache_map(&tv, v_cache, layout)) return PKV_ERR_CUDA;
 
     pkv::DecodeArgs a{};
+    if (planned) {
+        a.splits_per_seq = static_cast<const int32_t*>(arg(splits_per_seq_p).ptr);
+        a.work = static_cast<const int32_t*>(arg(work_p).ptr);
+        a.n_work = n_work;
+    }
     a.q = static_cast<const uint16_t*>(q.ptr);
     a.q_s0 = q.stride[0];
     a.q_s1 = q.stride[1];
@@ -478,8 +501,28 @@ pkv_status pkv_paged_gqa_decode_nvfp4(const pkv_tensor* q, const pkv_tensor* k_c
                                  err_flag, stream, true);
 }
 
-pkv_status pkv_lse_merge(const pkv_tensor* out_partial_p, const pkv_tensor* lse_partial_p, const pkv_tensor* out_p, const pkv_tensor* lse_out_p,
-                         pkv_stream_t stream) {
+pkv_status pkv_paged_gqa_decode_planned(const pkv_tensor* q, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                                        const pkv_tensor* k_block_scale, const pkv_tensor* v_block_scale,
+                                        const pkv_tensor* block_tables, const pkv_tensor* seq_lens,
+                                        float softmax_scale, const pkv_tensor* splits_per_seq,
+                                        const pkv_tensor* work, const pkv_tensor* out_partial,
+                                        const pkv_tensor* lse_partial, const pkv_tensor* k_scale,
+                                        const pkv_tensor* v_scale, int32_t layout, int32_t* err_flag,
+                                        pkv_stream_t stream) {
+    if (!splits_per_seq || !work || !out_partial) return PKV_ERR_INVALID_ARG;
+    const bool nvfp4 = k_block_scale != nullptr && k_block_scale->ptr != nullptr;
+    const pkv_tensor& op = arg(out_partial);
+    if (op.ndim != 4) return PKV_ERR_INVALID_ARG;
+    if (op.shape[1] < 1 || op.shape[1] > 4095) return op.shape[1] < 1 ? PKV_ERR_INVALID_ARG : PKV_ERR_UNSUPPORTED;
+    return paged_gqa_decode_impl(q, k_cache, v_cache, nvfp4 ? k_block_scale : nullptr,
+                                 nvfp4 ? v_block_scale : nullptr, block_tables, seq_lens, softmax_scale,
+                                 static_cast<int32_t>(op.shape[1]), out_partial, lse_partial, k_scale, v_scale,
+                                 layout, err_flag, stream, nvfp4, splits_per_seq, work);
+}
+
+static pkv_status lse_merge_impl(const pkv_tensor* out_partial_p, const pkv_tensor* lse_partial_p,
+                                 const pkv_tensor* out_p, const pkv_tensor* lse_out_p, pkv_stream_t stream,
+                                 const pkv_tensor* splits_per_seq_p) {
     const pkv_tensor& out_partial = arg(out_partial_p);
     const pkv_tensor& lse_partial = arg(lse_partial_p);
     const pkv_tensor& out = arg(out_p);
@@ -502,8 +545,16 @@ pkv_status pkv_lse_merge(const pkv_tensor* out_partial_p, const pkv_tensor* lse_
     if (!aligned(out_partial.ptr, 16) || !strides_multiple(out_partial, 3, 16)) return PKV_ERR_UNSUPPORTED;
     if (!aligned(out.ptr, 8) || !strides_multiple(out, 2, 8)) return PKV_ERR_UNSUPPORTED;
     if (S > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+    const int32_t* spp = nullptr;
+    if (splits_per_seq_p) {
+        const pkv_tensor& sp = arg(splits_per_seq_p);
+        if (!shape_ok(sp, 1, PKV_I32) || sp.shape[0] != B || !sp.ptr) return PKV_ERR_INVALID_ARG;
+        if (sp.stride[0] != 1) return PKV_ERR_UNSUPPORTED;
+        spp = static_cast<const int32_t*>(sp.ptr);
+    }
 
     pkv::MergeArgs a{};
+    a.splits_per_seq = spp;
     a.out_partial = static_cast<const float*>(out_partial.ptr);
     a.op_s0 = out_partial.stride[0];
     a.op_s1 = out_partial.stride[1];
@@ -522,6 +573,18 @@ pkv_status pkv_lse_merge(const pkv_tensor* out_partial_p, const pkv_tensor* lse_
     a.Hq = static_cast<int32_t>(Hq);
     a.D = static_cast<int32_t>(D);
     return cuda_status(pkv::launch_lse_merge(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_lse_merge(const pkv_tensor* out_partial, const pkv_tensor* lse_partial, const pkv_tensor* out,
+                         const pkv_tensor* lse_out, pkv_stream_t stream) {
+    return lse_merge_impl(out_partial, lse_partial, out, lse_out, stream, nullptr);
+}
+
+pkv_status pkv_lse_merge_planned(const pkv_tensor* out_partial, const pkv_tensor* lse_partial,
+                                 const pkv_tensor* splits_per_seq, const pkv_tensor* out, const pkv_tensor* lse_out,
+                                 pkv_stream_t stream) {
+    if (!splits_per_seq) return PKV_ERR_INVALID_ARG;
+    return lse_merge_impl(out_partial, lse_partial, out, lse_out, stream, splits_per_seq);
 }
 
 pkv_status pkv_mla_cache_write(const pkv_tensor* q_pe_p, const pkv_tensor* ckv_p, const pkv_tensor* kpe_p,
@@ -783,6 +846,117 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
         }
     }
     return best;
+}
+
+// The split plan: a split count per sequence so that every CTA streams
+// about the same number of pages, and the work list of (sequence, split)
+// items, longest first. Host only; no CUDA call.
+pkv_status pkv_plan_splits(const int32_t* seq_lens, int32_t B, int32_t Hkv, int32_t Hq, int32_t D,
+                           int32_t max_pages, int32_t cache_dtype, int32_t sm_count, int32_t max_splits,
+                           int32_t target_pages, int32_t* splits_per_seq, int32_t* num_records, int32_t* work,
+                           int64_t work_capacity, int64_t* num_work) {
+    if (B < 0 || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || D < 1 || max_pages < 1 || sm_count < 1) return PKV_ERR_INVALID_ARG;
+    if (max_splits < 1 || max_splits > 4095 || target_pages < 0 || work_capacity < 0) return PKV_ERR_INVALID_ARG;
+    if (B > (1 << 19) || max_pages > (1 << 26)) return PKV_ERR_UNSUPPORTED;
+    if ((B > 0 && (!seq_lens || !splits_per_seq)) || !num_records || !num_work) return PKV_ERR_INVALID_ARG;
+    if (work_capacity > 0 && !work) return PKV_ERR_INVALID_ARG;
+    std::vector<int64_t> np(B);
+    int64_t max_np = 0, total = 0;
+    for (int b = 0; b < B; ++b) {
+        const int64_t L = std::min<int64_t>(std::max<int32_t>(seq_lens[b], 0), int64_t{16} * max_pages);
+        np[b] = (L + kPageSize - 1) / kPageSize;
+        max_np = std::max(max_np, np[b]);
+        total += np[b];
+    }
+    // the split count of a sequence of n pages under a target of T pages
+    // per split, reduced to the splits that hold pages (same page ranges)
+    auto count = [&](int64_t n, int64_t T) -> int64_t {
+        if (n <= 0) return 1;
+        int64_t S = std::min<int64_t>((n + T - 1) / T, max_splits);
+        const int64_t pps = (n + S - 1) / S;
+        const int64_t k = (n + pps - 1) / pps;
+        return ((n + k - 1) / k == pps) ? k : S;
+    };
+    int64_t T = target_pages;
+    if (T == 0) {
+        // When every sequence and kv head can have a CTA of its own within
+        // one wave, the plan fills that wave with items of nearly equal
+        // length, chosen with a model of the decode on GB300 (fitted to sweeps
+        // of the page target on the qwen, longctx, fp8 and fp4 workloads): a
+        // CTA spends ~3 us on start-up and its epilogue, then streams its
+        // page-heads at its share of HBM (~7 bytes/ns over the CTAs running
+        // at once), at most at the ~30 bytes/ns one CTA keeps in flight, or,
+        // for FP8 / NVFP4, at the ~0.36 us per page-head its dequantisation
+        // takes when that is slower; the step ends with the longest item.
+        // Past one wave (many short sequences) the uniform heuristic's
+        // longest split is the target: measured on the ragged workload, no
+        // other target did better by more than the run-to-run spread.
+        const int kind = cache_dtype == PKV_FP4_E2M1X2 ? pkv::kFp4 : (cache_dtype == PKV_FP8_E4M3 ? pkv::kFp8 : pkv::kBf16);
+        const double row = kind == pkv::kFp4 ? D / 2.0 + D / 16.0 : (kind == pkv::kFp8 ? D : 2.0 * D);
+        const double page_bytes = 2.0 * kPageSize * row;
+        const double slots = static_cast<double>(sm_count) * pkv::decode_ctas_per_sm(D, kind, Hq / Hkv);
+        const double t0 = 3.0, bw = 7.0e6, bw_cta = 2.95e4;  // us; bytes per us
+        const double tc = std::max(kind == pkv::kBf16 ? 0.0 : 0.36, page_bytes / bw_cta);
+        const int64_t top = std::max<int64_t>(max_np, 1);
+        if (static_cast<double>(B) * Hkv > slots) {
+            const int32_t S_u = pkv_choose_num_splits(B, Hkv, Hq, D, std::max<int64_t>(total, 1),
+                                                      static_cast<int32_t>(top), cache_dtype, sm_count);
+            T = (top + S_u - 1) / S_u;
+        } else {
+            double best_cost = 1e300;
+            int64_t best_T = top;
+            for (int64_t Tc = 1; Tc <= top; Tc = Tc < 64 ? Tc + 1 : std::max<int64_t>(Tc + 1, static_cast<int64_t>(Tc * 1.05))) {
+                double items = 0, p_max = 0;
+                int64_t recs = 1;
+                for (int b = 0; b < B; ++b) {
+                    const int64_t S = count(np[b], Tc);
+                    items += static_cast<double>(S);
+                    p_max = std::max(p_max, static_cast<double>(np[b] > 0 ? (np[b] + S - 1) / S : 0));
+                    recs = std::max(recs, S);
+                }
+                const double n = items * Hkv;  // CTAs
+                if (n > slots) continue;
+                const double cost = t0 + p_max * std::max(page_bytes * n / bw, tc) +
+                                    0.15 * 2.0 * items * static_cast<double>(Hq) * (D + 1) * 4.0 / 1e6 +
+                                    (recs > 32 ? 2.0 : 0.0);
+                if (cost < best_cost * (1.0 - 1e-9)) {
+                    best_cost = cost;
+                    best_T = Tc;
+                }
+            }
+            T = best_T;
+        }
+    }
+    int64_t n_items = 0;
+    int32_t recs = 1;
+    for (int b = 0; b < B; ++b) {
+        const int64_t S = count(np[b], T);
+        splits_per_seq[b] = static_cast<int32_t>(S);
+        recs = std::max<int32_t>(recs, static_cast<int32_t>(S));
+        n_items += S;
+    }
+    *num_records = recs;
+    *num_work = n_items;
+    if (!work) return PKV_OK;
+    if (work_capacity < n_items) return PKV_ERR_INVALID_ARG;
+    // items in order of decreasing pages, ties by sequence then split
+    struct It { int64_t pages; int32_t b, s, p0; };
+    std::vector<It> items;
+    items.reserve(static_cast<size_t>(n_items));
+    for (int b = 0; b < B; ++b) {
+        const int64_t S = splits_per_seq[b];
+        const int64_t pps = np[b] > 0 ? (np[b] + S - 1) / S : 0;
+        for (int64_t sp = 0; sp < S; ++sp) {
+            const int64_t p0 = std::min(sp * pps, np[b]);
+            items.push_back({std::min(pps, np[b] - p0), b, static_cast<int32_t>(sp), static_cast<int32_t>(p0)});
+        }
+    }
+    std::stable_sort(items.begin(), items.end(), [](const It& x, const It& y) { return x.pages > y.pages; });
+    for (int64_t i = 0; i < n_items; ++i) {
+        work[2 * i] = (items[i].b << 12) | items[i].s;
+        work[2 * i + 1] = items[i].p0;
+    }
+    return PKV_OK;
 }
 
 pkv_status pkv_validate_indices(const pkv_tensor* block_tables_p, const pkv_tensor* seq_lens_p, const pkv_tensor* slot_mapping_p,

@@ -47,6 +47,7 @@ struct RopeArgs {
     int32_t D;
     int32_t interleaved;
     int32_t kind;              // CacheKind
+    int32_t toks;              // tokens per group of a CTA (set by the launcher)
     int32_t* err;
 };
 
@@ -74,6 +75,13 @@ struct DecodeArgs {
     int32_t B, Hq, Hkv, D, G;
     int32_t kind;              // CacheKind
     int32_t layout;            // pkv_layout (selects the TMA coordinate order)
+    // Planned launches (a split count per sequence): work[2 i] = (b << 12) | s,
+    // work[2 i + 1] = the split's first page per the plan (a hint for the
+    // early block-table read); splits_per_seq[b] = the sequence's split count.
+    // Both null for a uniform launch (every sequence in num_splits splits).
+    const int32_t* work;
+    int64_t n_work;
+    const int32_t* splits_per_seq;
     int32_t* err;
 };
 
@@ -140,6 +148,7 @@ struct MergeArgs {
     float* lse_out;            // may be null
     int64_t lo_s0, lo_s1;
     int32_t B, S, Hq, D;
+    const int32_t* splits_per_seq;  // records merged per sequence (clamped to [1, S]); null = S
 };
 
 struct ValidateArgs {

@@ -6,8 +6,12 @@
 // separate q/k/v. microLLM-rocm, optimisation checkpoints: split-half RoPE
 // reading the projection layout and writing the attention layout directly.
 //
-// Mapping: a CTA is a 2-D block, x = the (row, chunk) items of one token and
-// y = tokens. Every (token, row) -- a q head, a k head or a v head -- is
+// Mapping: a CTA takes `toks` tokens at a time (U groups of them per thread).
+// Its threads are ordered by the kind of row first -- the q heads of all its
+// tokens, then their k heads, then their v heads -- and within a kind by
+// token, head and chunk, so a warp holds one kind of row only (the rotation
+// and the cos/sin loads of k rows are not spread over warps that also hold
+// v rows). Every (token, row) -- a q head, a k head or a v head -- is
 // handled by D/16 threads; thread c of a row owns the 8-element chunk starting at 8c
 // and the chunk starting at D/2 + 8c. Under NeoX these two chunks are exactly
 // the partners of one another's rotation pairs (i, i + D/2); under the
@@ -253,8 +257,12 @@ __device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float (
 // U tokens per thread: all of their loads (slot, position, the row's two
 // chunks, then the cos/sin rows) are issued before any token is processed,
 // so a thread keeps U times as many bytes in flight.
+#ifndef PKV_WRITE_FILL_MIN_CTAS
+#define PKV_WRITE_FILL_MIN_CTAS 3  // resident CTAs per SM the multi-token form is register-budgeted for
+#endif
 template <int D, bool INTER, int KIND, int U>
-__global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(const RopeArgs a) {
+__global__ void __launch_bounds__(U == 1 ? 1024 : 256, U == 1 ? 1 : (U == 2 ? PKV_WRITE_FILL_MIN_CTAS : 2))
+    rope_kv_write_kernel(const RopeArgs a) {
     constexpr int TPR = D / 16;  // threads per row
     // Launched as a programmatic dependent: the inputs may come from the
     // preceding grid (a copy of the step's inputs), and a preceding decode
@@ -263,15 +271,22 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
     // The decode kernel that usually follows may start its prologue now; it
     // waits for this grid's writes before it reads q or the cache.
     grid_dep_launch();
-    // threadIdx.x: the (row, chunk) work items of one token; threadIdx.y, u
-    // and blockIdx.x: tokens. No division is needed to find either.
-    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.y * U + threadIdx.y;
-    const int r = threadIdx.x;
-    const int row = r / TPR;
-    const int c = r % TPR;
-    const bool is_q = row < a.Hq;
-    const bool is_k = !is_q && row < a.Hq + a.Hkv;
-    const int h = is_q ? row : (is_k ? row - a.Hq : row - a.Hq - a.Hkv);
+    // threadIdx.x: [0, nq) the q rows of the CTA's `toks` tokens, then
+    // [nq, nq + nk) their k rows, then their v rows; within a kind, token
+    // tl, head h and chunk c (TPR threads per row, so a row's threads are
+    // consecutive lanes of one warp). u and blockIdx.x: groups of tokens.
+    const int toks = a.toks;
+    const int L = threadIdx.x;
+    const int nq = toks * a.Hq * TPR, nk = toks * a.Hkv * TPR;
+    const bool is_q = L < nq;
+    const bool is_k = !is_q && L < nq + nk;
+    const int j = is_q ? L : (is_k ? L - nq : L - nq - nk);
+    const int per = (is_q ? a.Hq : a.Hkv) * TPR;  // threads of one token's rows of this kind
+    const int tl = j / per;
+    const int h = (j - tl * per) / TPR;
+    const int c = j % TPR;
+    const bool lead = h == 0 && c == 0;  // flags a bad token once per kind
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * toks * U + tl;
     const int64_t num_slots = a.num_pages * a.page_size;
 
     // Reading the row of a skipped token stays inside the [T, heads, D] input.
@@ -280,7 +295,7 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
     bool live[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int64_t t = t0 + static_cast<int64_t>(u) * blockDim.y;
+        const int64_t t = t0 + static_cast<int64_t>(u) * toks;
         live[u] = t < a.T;
         if (!live[u]) continue;
         const uint16_t* src = is_q ? a.q + t * a.q_s0 + h * a.q_s1
@@ -298,12 +313,12 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
             continue;
         }
         if (slot[u] >= num_slots) {
-            if (r == 0) flag_error(a.err, PKV_FLAG_SLOT_RANGE);
+            if (lead) flag_error(a.err, PKV_FLAG_SLOT_RANGE);
             live[u] = false;
             continue;
         }
         if (pos[u] < 0 || pos[u] >= a.max_pos) {
-            if (r == 0) flag_error(a.err, PKV_FLAG_POSITION_RANGE);
+            if (lead) flag_error(a.err, PKV_FLAG_POSITION_RANGE);
             live[u] = false;
             continue;
         }
@@ -326,7 +341,7 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         if (!live[u]) continue;
-        const int64_t t = t0 + static_cast<int64_t>(u) * blockDim.y;
+        const int64_t t = t0 + static_cast<int64_t>(u) * toks;
         Chunk8 lo = unpack_bf16x8(wlo[u]);
         Chunk8 hi = unpack_bf16x8(whi[u]);
         if (is_q) {  // q head: rotate in place
@@ -381,25 +396,33 @@ __global__ void __launch_bounds__(U == 1 ? 1024 : 512) rope_kv_write_kernel(cons
     }
 }
 
+// Tokens per thread of a cache fill (measured on GB300; see the launcher).
+#ifndef PKV_WRITE_FILL_TOKENS
+#define PKV_WRITE_FILL_TOKENS 2
+#endif
+
 template <int D, bool INTER, int KIND>
 cudaError_t launch_t(const RopeArgs& a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
     const int per_tok = (a.Hq + 2 * a.Hkv) * (D / 16);  // work items of one token
     if (per_tok > 1024) return cudaErrorInvalidConfiguration;
-    const int toks = per_tok >= 256 ? 1 : 256 / per_tok;  // tokens per CTA row of threads
+    const int toks = per_tok >= 256 ? 1 : 256 / per_tok;  // tokens per group of the CTA
     // Two tokens per thread when there are enough tokens to keep every SM
     // busy (cache fills of bf16 and FP8 caches: twice the bytes in flight per
     // thread); one for a decode step's few tokens and for NVFP4 (measured no
     // faster there: its quantiser is bound by instruction issue).
-    const bool two = KIND != kFp4 && a.T >= 8192 && per_tok * toks <= 512;
-    const int64_t per_cta = static_cast<int64_t>(toks) * (two ? 2 : 1);
+    const bool two = KIND != kFp4 && a.T >= 8192 && per_tok * toks <= 256;
+    constexpr int UF = PKV_WRITE_FILL_TOKENS;
+    const int64_t per_cta = static_cast<int64_t>(toks) * (two ? UF : 1);
     const int64_t blocks = (a.T + per_cta - 1) / per_cta;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-    if (two)
-        return launch_dependent(rope_kv_write_kernel<D, INTER, KIND, 2>, dim3(static_cast<unsigned>(blocks)),
-                                dim3(per_tok, toks), 0, s, a);
-    return launch_dependent(rope_kv_write_kernel<D, INTER, KIND, 1>, dim3(static_cast<unsigned>(blocks)),
-                            dim3(per_tok, toks), 0, s, a);
+    RopeArgs b = a;
+    b.toks = toks;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(per_tok * toks);
+    if constexpr (KIND != kFp4) {
+        if (two) return launch_dependent(rope_kv_write_kernel<D, INTER, KIND, UF>, grid, block, 0, s, b);
+    }
+    return launch_dependent(rope_kv_write_kernel<D, INTER, KIND, 1>, grid, block, 0, s, b);
 }
 
 template <int D, bool INTER>

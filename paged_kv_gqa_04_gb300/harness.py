@@ -56,16 +56,37 @@ class DeviceWorkload:
             num_splits = _abi.choose_num_splits(w.B, w.Hkv, w.Hq, w.D, int(w.pages_per_seq.sum()),
                                                 max(1, int(w.pages_per_seq.max()) if w.B else 1), w.cache_dtype,
                                                 props.multi_processor_count)
+        self.splits_per_seq = None  # a split plan (set_plan), else one split count for the batch
+        self.work = None
         self.set_splits(num_splits)
         self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
         self.decode_inputs = None
 
     def set_splits(self, num_splits: int) -> None:
+        """One split count for every sequence (drops any split plan)."""
         w = self.w
+        self.splits_per_seq = self.work = None
         self.num_splits = int(num_splits)
         self.out_partial = torch.empty((w.B, self.num_splits, w.Hq, w.D), dtype=torch.float32, device=self.device)
         self.lse_partial = torch.empty((w.B, self.num_splits, w.Hq), dtype=torch.float32, device=self.device)
+
+    def set_plan(self, target_pages: int = 0, max_splits: int = 4095) -> None:
+        """A split count per sequence from the library's planner (host
+        seq_lens), uploaded with its work list; the partials get the plan's
+        record count."""
+        w = self.w
+        props = torch.cuda.get_device_properties(self.device)
+        sp, nrec, work = _abi.plan_splits(w.seq_lens, w.Hkv, w.Hq, w.D, max(1, w.max_pages), w.cache_dtype,
+                                          props.multi_processor_count, max_splits, target_pages)
+        self.set_splits(nrec)
+        self.plan_host = (sp, work)
+        self.splits_per_seq = torch.from_numpy(sp).to(self.device)
+        self.work = torch.from_numpy(np.ascontiguousarray(work)).to(self.device)
+
+    @property
+    def planned(self) -> bool:
+        return self.work is not None
 
     # ---- cache fill ----------------------------------------------------------
     def fill(self, max_tokens: int = 1 << 18) -> int:
@@ -124,6 +145,13 @@ class DeviceWorkload:
         """The decode over the given caches (as returned by caches(), or
         copies of them) into the given partial buffers."""
         w = self.w
+        if self.planned:
+            kbs, vbs = (caches[2], caches[3]) if self.nvfp4 else (None, None)
+            _abi.paged_gqa_decode_planned(q, caches[0], caches[1], self.block_tables, self.seq_lens,
+                                          w.softmax_scale, self.splits_per_seq, self.work, out_partial, lse_partial,
+                                          self.k_scale, self.v_scale, w.layout, self.err, stream,
+                                          k_block_scale=kbs, v_block_scale=vbs)
+            return
         if self.nvfp4:
             kc, vc, kbs, vbs = caches
             _abi.paged_gqa_decode_nvfp4(q, kc, vc, kbs, vbs, self.block_tables, self.seq_lens, w.softmax_scale,
@@ -135,6 +163,10 @@ class DeviceWorkload:
                               out_partial, lse_partial, self.k_scale, self.v_scale, w.layout, self.err, stream)
 
     def merge(self, stream=None) -> None:
+        if self.planned:
+            _abi.lse_merge_planned(self.out_partial, self.lse_partial, self.splits_per_seq, self.out, self.lse,
+                                   stream)
+            return
         _abi.lse_merge(self.out_partial, self.lse_partial, self.out, self.lse, stream)
 
     def upload_decode(self) -> dict:
@@ -226,6 +258,9 @@ class StepGraph:
         ins = {k: (d["q0"] if k == "q" else d[k]) for k in dw.H2D_KEYS}
         ins["block_tables"] = dw.block_tables
         ins["seq_lens"] = dw.seq_lens
+        if getattr(dw, "planned", False):  # a split plan is made per step on the host and travels with the inputs
+            ins["splits_per_seq"] = dw.splits_per_seq
+            ins["work"] = dw.work
         offs, size = self._layout(ins)
         self.dev_in = torch.zeros(size, dtype=torch.uint8, device=dw.device)
         self.host_in = torch.zeros(size, dtype=torch.uint8).pin_memory()
@@ -237,6 +272,9 @@ class StepGraph:
             d[k] = dv[k]
         dw.block_tables = dv["block_tables"]
         dw.seq_lens = dv["seq_lens"]
+        if getattr(dw, "planned", False):
+            dw.splits_per_seq = dv["splits_per_seq"]
+            dw.work = dv["work"]
         outs = {"out": dw.out, "lse": dw.lse}
         offs, size = self._layout(outs)
         self.dev_out = torch.zeros(size, dtype=torch.uint8, device=dw.device)

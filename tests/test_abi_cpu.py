@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pkv_abi_version() == 5
+    assert lib.pkv_abi_version() == 6
     for s in range(4):
         assert pkv.status_string(s)
     assert "invalid" in pkv.status_string(1)
@@ -314,3 +314,100 @@ def test_selftest_bounded_wait_rejects_bad_limits():
     lib = _abi.lib()
     for limit in (0, 99_999, 10_000_001):
         assert lib.pkv_selftest_bounded_wait(limit, None, None, None) == _abi.PKV_ERR_INVALID_ARG
+
+
+def _plan_pages(np_b, S):
+    """Pages of each split of a sequence of np_b pages dealt into S splits
+    (the decode's rule, written out for the test)."""
+    pps = -(-np_b // S) if np_b else 0
+    return [max(0, min(pps, np_b - s * pps)) for s in range(S)]
+
+
+@pytest.mark.parametrize("name", ["qwen", "ragged", "fp8", "fp4", "longctx", "million", "tiny"])
+def test_split_plan_covers_every_split_once_longest_first(lib, name):
+    w = synth.make_workload(name)
+    sp, nrec, work = _abi.plan_splits(w.seq_lens, w.Hkv, w.Hq, w.D, w.max_pages, w.cache_dtype, 152)
+    npg = w.pages_per_seq.astype(int)
+    assert sp.shape == (w.B,) and (sp >= 1).all() and nrec == int(sp.max())
+    items = [(int(e) >> 12, int(e) & 0xFFF, int(p0)) for e, p0 in work]
+    assert sorted((b, s) for b, s, _ in items) == [(b, s) for b in range(w.B) for s in range(int(sp[b]))]
+    pages = []
+    for b, s, p0 in items:
+        pp = _plan_pages(npg[b], int(sp[b]))
+        pps = pp[0]
+        assert p0 == min(s * pps, npg[b])                      # the hint is the split's first page
+        pages.append(pp[s])
+    assert all(x >= y for x, y in zip(pages, pages[1:]))      # longest first
+    for b in range(w.B):                                       # no empty split where pages exist
+        if npg[b]:
+            assert all(p > 0 for p in _plan_pages(npg[b], int(sp[b])))
+    # deterministic
+    sp2, nrec2, work2 = _abi.plan_splits(w.seq_lens, w.Hkv, w.Hq, w.D, w.max_pages, w.cache_dtype, 152)
+    assert np.array_equal(sp, sp2) and nrec == nrec2 and np.array_equal(work, work2)
+
+
+def test_split_plan_with_a_page_target(lib):
+    lens = np.array([0, 1, 16, 17, 160, 161, 1000, 4000, 33], np.int32)
+    npg = (lens.astype(int) + 15) // 16
+    for T in (1, 2, 3, 7, 16, 1000):
+        sp, nrec, work = _abi.plan_splits(lens, 2, 12, 128, 300, "bf16", 152, 4095, T)
+        for b in range(len(lens)):
+            pp = _plan_pages(npg[b], int(sp[b]))
+            assert max(pp) <= T                                 # no split above the target
+            if npg[b] > T:                                      # and no more splits than needed
+                assert int(sp[b]) == -(-npg[b] // T) or max(_plan_pages(npg[b], int(sp[b]) - 1)) > T
+        assert len(work) == int(sp.sum())
+    # a record cap binds: S_b <= max_splits, pages spread over the cap
+    sp, nrec, work = _abi.plan_splits(lens, 2, 12, 128, 300, "bf16", 152, 5, 1)
+    assert nrec == 5 and (sp <= 5).all() and int(sp[7]) == 5
+
+
+def test_split_plan_rejects_bad_arguments(lib):
+    f = lib.pkv_plan_splits
+    sl = np.array([10, 20], np.int32)
+    sp = np.zeros(2, np.int32)
+    nrec, nwork = ctypes.c_int32(0), ctypes.c_int64(0)
+
+    def call(B=2, Hkv=2, Hq=4, D=128, mp=4, dt=0, sms=152, ms=4095, T=0, work=None, cap=0, sl_p=True, sp_p=True):
+        return f(sl.ctypes.data if sl_p else None, B, Hkv, Hq, D, mp, dt, sms, ms, T, sp.ctypes.data if sp_p else None,
+                 ctypes.byref(nrec), work, cap, ctypes.byref(nwork))
+    assert call() == _abi.PKV_OK and nwork.value == int(sp.sum())
+    assert call(Hq=3) == _abi.PKV_ERR_INVALID_ARG
+    assert call(ms=0) == _abi.PKV_ERR_INVALID_ARG and call(ms=4096) == _abi.PKV_ERR_INVALID_ARG
+    assert call(T=-1) == _abi.PKV_ERR_INVALID_ARG
+    assert call(sl_p=False) == _abi.PKV_ERR_INVALID_ARG and call(sp_p=False) == _abi.PKV_ERR_INVALID_ARG
+    assert call(B=-1) == _abi.PKV_ERR_INVALID_ARG
+    small = np.zeros((1, 2), np.int32)
+    assert call(work=small.ctypes.data, cap=1) == _abi.PKV_ERR_INVALID_ARG   # capacity below the item count
+    assert nwork.value == int(sp.sum()) > 1                                  # the counts are still written
+    assert call(B=0, sl_p=False, sp_p=False) == _abi.PKV_OK and nwork.value == 0
+
+
+def test_planned_decode_and_merge_reject_inconsistent_arguments(lib):
+    B, Hq, Hkv, D, S = 3, 12, 2, 128, 4
+    q = _t((B, Hq, D), "bf16")
+    kc = _t((50, Hkv, 16, D), "bf16")
+    bt = _t((B, 10), "i32")
+    sl = _t((B,), "i32")
+    op = _t((B, S, Hq, D), "f32")
+    lp = _t((B, S, Hq), "f32")
+    sp = _t((B,), "i32")
+    wk = _t((7, 2), "i32")
+
+    def dec(**o):
+        a = dict(q=q, kc=kc, vc=kc, kbs=NULL, vbs=NULL, bt=bt, sl=sl, scale=0.1, sp=sp, wk=wk, op=op, lp=lp)
+        a.update(o)
+        return lib.pkv_paged_gqa_decode_planned(a["q"], a["kc"], a["vc"], a["kbs"], a["vbs"], a["bt"], a["sl"],
+                                                a["scale"], a["sp"], a["wk"], a["op"], a["lp"], NULL, NULL, 1, None,
+                                                None)
+    assert dec(sp=_t((B + 1,), "i32")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(wk=_t((7, 3), "i32")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(wk=_t((7,), "i32")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(sp=None) == _abi.PKV_ERR_INVALID_ARG and dec(wk=None) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(op=_t((B, 4096, Hq, D), "f32"), lp=_t((B, 4096, Hq), "f32")) == _abi.PKV_ERR_UNSUPPORTED
+    assert dec(lp=_t((B, S + 1, Hq), "f32")) == _abi.PKV_ERR_INVALID_ARG
+    out = _t((B, Hq, D), "bf16")
+    m = lib.pkv_lse_merge_planned
+    assert m(op, lp, None, out, NULL, None) == _abi.PKV_ERR_INVALID_ARG
+    assert m(op, lp, _t((B + 1,), "i32"), out, NULL, None) == _abi.PKV_ERR_INVALID_ARG
+    assert m(op, lp, _t((B,), "f32"), out, NULL, None) == _abi.PKV_ERR_INVALID_ARG
