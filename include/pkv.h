@@ -36,11 +36,12 @@
  *     launched as programmatic dependents, so one may start its prologue
  *     while its predecessor on the stream finishes; each waits for that
  *     predecessor (griddepcontrol.wait) before it reads anything another
- *     grid may have written, and before it can finish. Only the decodes read
- *     index inputs (block tables, seq_lens) before that wait, and only the
- *     cache writes and the decodes let their successor start early; neither
- *     writes index inputs. Calls on one stream therefore see each other's
- *     results exactly as plain stream order would give.
+ *     grid may have written, and before it can finish. Only the decodes
+ *     (block tables, seq_lens, a split plan) and the planned merge (the
+ *     plan's split counts) read index inputs before that wait, and only the
+ *     cache writes and the decodes let their successor start early; no
+ *     kernel writes index inputs. Calls on one stream therefore see each
+ *     other's results exactly as plain stream order would give.
  *   - Status. The return value reports argument validation and launch
  *     errors only: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED are returned
  *     before anything is launched; PKV_ERR_CUDA reports a launch failure

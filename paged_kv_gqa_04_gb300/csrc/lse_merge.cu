@@ -16,9 +16,10 @@
 // merge a contiguous run of splits of a 64-column slice in parallel and
 // their results are merged again by their own LSE weights. The kernel is
 // latency-bound (the partials are a few MB): partial rows are loaded in
-// batches (sixteen for one warp per row, eight in the tree: one batch per
-// warp up to 256 splits), the first together with the LSE values and each
-// next one while the previous batch is summed. Rows wider than 128 columns
+// batches (4 or 16 for one warp per row, by the call's record count;
+// eight in the tree: one batch per warp up to 256 splits), the first
+// together with the LSE values and each next one while the previous batch
+// is summed. Rows wider than 128 columns
 // (the 512-value latent output of MLA decode) are cut into slices (128
 // columns for one warp per row, 64 in the tree), each merged with the same
 // LSE weights.
@@ -55,9 +56,42 @@ struct Vec<2> {
 // first batch goes out with the first 32 LSE values, each later batch while
 // the previous one is summed. (16 rows per batch for a warp that merges a
 // whole row, 8 in the tree kernel, whose 32 warps share the register file.)
-template <int V, int kBatch>
+template <int V, int kBatch, bool kSingle = false>
 __device__ __forceinline__ void warp_merge(const float* lse, int64_t lp_s1, const float* op, int64_t op_s1, int s_lo,
                                            int s_hi, float& m, float& l, float (&acc)[V]) {
+    if constexpr (kSingle) {
+        // At most kBatch splits (the caller guarantees it; used for up to 4):
+        // every lane reads the same few LSE values (one broadcast
+        // transaction each) and forms the weights itself, no cross-lane
+        // step; one batch of partial rows.
+        using VT = typename Vec<V>::T;
+        const int n = s_hi - s_lo;
+        lse += s_lo * lp_s1;
+        op += s_lo * op_s1;
+        float lj[kBatch];
+        VT x[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            lj[j] = (j < n) ? __ldg(lse + j * lp_s1) : -INFINITY;
+            if (j < n) x[j] = __ldg(reinterpret_cast<const VT*>(op + j * op_s1));
+        }
+        m = lj[0];
+#pragma unroll
+        for (int j = 1; j < kBatch; ++j) m = fmaxf(m, lj[j]);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.f;
+        l = 0.f;
+        if (m == -INFINITY) return;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (j < n) {
+                const float w = __expf(lj[j] - m);
+                l += w;
+                Vec<V>::fma(acc, w, x[j]);
+            }
+        }
+        return;
+    }
     using VT = typename Vec<V>::T;
     const int lane = threadIdx.x & 31;
     const int n = s_hi - s_lo;
@@ -135,21 +169,28 @@ struct Slice {
 };
 
 // Few splits (S <= 32): one warp per row slice, two slices per CTA.
-template <int D>
+template <int D, int kBatch, bool kSingle>
 __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const MergeArgs a) {
     using SL = Slice<D>;
     constexpr int V = SL::V;
-    grid_dep_wait();           // the partials come from the preceding decode grid
     const int lane = threadIdx.x & 31;
     const int64_t vrow = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    if (vrow >= static_cast<int64_t>(a.B) * a.Hq * SL::N) return;
+    if (vrow >= static_cast<int64_t>(a.B) * a.Hq * SL::N) {
+        grid_dep_wait();
+        return;
+    }
     const int64_t row = vrow / SL::N;
     const int c0 = static_cast<int>(vrow % SL::N) * SL::DW + lane * V;
     const int b = static_cast<int>(row / a.Hq);
     const int h = static_cast<int>(row % a.Hq);
+    // The record count is an index input of the step (never written by the
+    // decode): read it while the decode may still run; the partials come
+    // from that decode grid, so they are read only after the wait.
+    const int S = records_of(a, b);
+    grid_dep_wait();
     float m, l, acc[V];
-    warp_merge<V, 16>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1, a.out_partial + b * a.op_s0 + h * a.op_s2 + c0,
-                      a.op_s1, 0, records_of(a, b), m, l, acc);
+    warp_merge<V, kBatch, kSingle>(a.lse_partial + b * a.lp_s0 + h, a.lp_s1,
+                                   a.out_partial + b * a.op_s0 + h * a.op_s2 + c0, a.op_s1, 0, S, m, l, acc);
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] *= inv;
@@ -173,14 +214,14 @@ __global__ void __launch_bounds__(kTreeWarps * 32) lse_merge_tree_kernel(const M
     constexpr int W = kTreeWarps;
     // W * DW partial sums, then W maxima, W weight sums, W weights
     extern __shared__ float tree_smem[];
-    grid_dep_wait();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t row = blockIdx.x / NS;
     const int c0 = static_cast<int>(blockIdx.x % NS) * DW;  // first column of this CTA's slice
     const int b = static_cast<int>(row / a.Hq);
     const int h = static_cast<int>(row % a.Hq);
-    const int S = records_of(a, b);
+    const int S = records_of(a, b);  // an index input: read before the wait, as above
+    grid_dep_wait();
     const int chunk = (S + W - 1) / W;
     const int s_lo = min(S, warp * chunk), s_hi = min(S, s_lo + chunk);
     float m, l, acc[V];
@@ -216,14 +257,28 @@ __global__ void __launch_bounds__(kTreeWarps * 32) lse_merge_tree_kernel(const M
         a.lse_out[b * a.lo_s0 + h * a.lo_s1] = (M == -INFINITY) ? -INFINITY : M + __logf(L);
 }
 
+// One warp per row slice. Up to four records, a batch of four rows read
+// with the LSE values by every lane (44 registers: the 8,192 rows of up to 4
+// records of the ragged workload fit one wave of warps; with the 16-row
+// batch, 164 registers per thread, they ran in about five waves, 11.0 us
+// per launch in ncu, caches cold). More records: the 16-row batch with the
+// weights shared by shuffles (measured faster there: one LSE load per lane
+// instead of one broadcast load per record).
+template <int D, int kBatch, bool kSingle>
+cudaError_t launch_rows(const MergeArgs& a, int64_t rows, cudaStream_t s) {
+    const int64_t blocks = (rows + kWarps - 1) / kWarps;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    return launch_dependent(lse_merge_kernel<D, kBatch, kSingle>, dim3(static_cast<unsigned>(blocks)),
+                            dim3(kWarps * 32), 0, s, a);
+}
+
 template <int D>
 cudaError_t launch_d(const MergeArgs& a, cudaStream_t s) {
     using SL = Slice<D>;
     const int64_t rows = static_cast<int64_t>(a.B) * a.Hq * SL::N;  // row slices
     if (a.S <= 32) {
-        const int64_t blocks = (rows + kWarps - 1) / kWarps;
-        if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-        return launch_dependent(lse_merge_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(kWarps * 32), 0, s, a);
+        if (a.S <= 4) return launch_rows<D, 4, true>(a, rows, s);
+        return launch_rows<D, 16, false>(a, rows, s);
     }
     const int64_t trows = static_cast<int64_t>(a.B) * a.Hq * (D / kTreeCols);  // 64-column row slices
     if (trows > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;

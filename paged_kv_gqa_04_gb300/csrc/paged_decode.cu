@@ -158,22 +158,24 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(KIND, NH))
     const int warp = threadIdx.x >> 5;
     const int g = lane >> 2;
     const int t = lane & 3;
-    const int kvh = blockIdx.y;
-    const int G = a.G;
-    const int h0 = kvh * G;
-
     // ---- which split of which sequence ----------------------------------------
-    // Uniform launch: split blockIdx.x of sequence blockIdx.z, every sequence
-    // in num_splits splits. Planned launch: work item blockIdx.x names the
-    // sequence and the split, and the sequence's own split count comes from
-    // splits_per_seq (clamped to [1, num_splits], the records there are).
-    int b, s, p0_guess;
+    // Uniform launch: split blockIdx.x of kv head blockIdx.y of sequence
+    // blockIdx.z, every sequence in num_splits splits. Planned launch (a
+    // 1-D grid): CTA x takes kv head x % Hkv of work item x / Hkv, so the
+    // hardware dispatches the items in the plan's order (longest first) with
+    // all kv heads of an item together; the item names the sequence and the
+    // split, and the sequence's own split count comes from splits_per_seq
+    // (clamped to [1, num_splits], the records there are).
+    int b, s, kvh, p0_guess;
     if (a.work == nullptr) {
         s = blockIdx.x;
+        kvh = blockIdx.y;
         b = blockIdx.z;
         p0_guess = s * ((a.max_pages + a.num_splits - 1) / a.num_splits);
     } else {
-        const int2 e = __ldg(reinterpret_cast<const int2*>(a.work) + blockIdx.x);
+        const int item = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.Hkv));
+        kvh = static_cast<int>(blockIdx.x - static_cast<unsigned>(item) * a.Hkv);
+        const int2 e = __ldg(reinterpret_cast<const int2*>(a.work) + item);
         b = e.x >> 12;
         s = e.x & 0xFFF;
         p0_guess = min(max(e.y, -1), a.max_pages);  // a hint only: kept in range, checked below
@@ -184,6 +186,8 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(KIND, NH))
             return;
         }
     }
+    const int G = a.G;
+    const int h0 = kvh * G;
 
     // ---- sequence bounds and this split's page range -----------------------
     // The block-table entries this warp needs first depend on the split's
@@ -716,7 +720,7 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
     auto kern = paged_decode_kernel<D, KIND, NH>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    const dim3 grid = a.work ? dim3(static_cast<unsigned>(a.n_work), a.Hkv, 1) : dim3(a.num_splits, a.Hkv, a.B);
+    const dim3 grid = a.work ? dim3(static_cast<unsigned>(a.n_work * a.Hkv)) : dim3(a.num_splits, a.Hkv, a.B);
     return launch_dependent(kern, grid, dim3(kWarps * 32), C::SMEM, s, tk, tv, a, hnd);
 }
 

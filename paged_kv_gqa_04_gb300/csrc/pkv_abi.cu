@@ -428,7 +428,7 @@ static pkv_status paged_gqa_decode_impl(const pkv_tensor* q_p, const pkv_tensor*
         if (n_work > 0 && !wk.ptr) return PKV_ERR_INVALID_ARG;
         if (sp.stride[0] != 1 || wk.stride[1] != 1 || wk.stride[0] != 2 || !aligned(wk.ptr, 8))
             return PKV_ERR_UNSUPPORTED;
-        if (n_work > 0x7FFFFFFF || num_splits > 4095 || B > (1 << 19)) return PKV_ERR_UNSUPPORTED;
+        if (n_work * Hkv > 0x7FFFFFFF || num_splits > 4095 || B > (1 << 19)) return PKV_ERR_UNSUPPORTED;
     }
 
     CUtensorMap tk, tv;

@@ -258,7 +258,7 @@ __device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float (
 // chunks, then the cos/sin rows) are issued before any token is processed,
 // so a thread keeps U times as many bytes in flight.
 #ifndef PKV_WRITE_FILL_MIN_CTAS
-#define PKV_WRITE_FILL_MIN_CTAS 3  // resident CTAs per SM the multi-token form is register-budgeted for
+#define PKV_WRITE_FILL_MIN_CTAS 4  // resident CTAs per SM the multi-token form is register-budgeted for
 #endif
 template <int D, bool INTER, int KIND, int U>
 __global__ void __launch_bounds__(U == 1 ? 1024 : 256, U == 1 ? 1 : (U == 2 ? PKV_WRITE_FILL_MIN_CTAS : 2))
@@ -409,8 +409,12 @@ cudaError_t launch_t(const RopeArgs& a, cudaStream_t s) {
     const int toks = per_tok >= 256 ? 1 : 256 / per_tok;  // tokens per group of the CTA
     // Two tokens per thread when there are enough tokens to keep every SM
     // busy (cache fills of bf16 and FP8 caches: twice the bytes in flight per
-    // thread); one for a decode step's few tokens and for NVFP4 (measured no
-    // faster there: its quantiser is bound by instruction issue).
+    // thread), with registers budgeted for four CTAs per SM (a few bytes of
+    // spill, but 32 warps to hide the loads: measured fills of the ragged,
+    // longctx and fp8 workloads 7%, 8% and 2% faster than at three CTAs,
+    // qwen 2% slower; three or four tokens per thread were slower); one for
+    // a decode step's few tokens and for NVFP4 (measured no faster there:
+    // its quantiser is bound by instruction issue).
     const bool two = KIND != kFp4 && a.T >= 8192 && per_tok * toks <= 256;
     constexpr int UF = PKV_WRITE_FILL_TOKENS;
     const int64_t per_cta = static_cast<int64_t>(toks) * (two ? UF : 1);

@@ -163,3 +163,43 @@ def test_bad_plan_entries_are_flagged_and_skipped():
     dw.step()
     torch.cuda.synchronize()
     assert int(dw.err.item()) & _abi.FLAG_PLAN_RANGE
+
+
+def test_planned_steps_back_to_back_and_as_graphs_match_one_step():
+    """Planned steps issued back to back, and the CUDA-graph forms of the
+    planned step (device inputs, and host inputs with the plan copied in
+    with them), give results bit-identical to one synchronised step."""
+    w = synth.custom_workload("b2bplan", 134, [700, 33, 1500, 250, 2], 12, 2, 128, rope_base=1e6)
+    dw = harness.DeviceWorkload(w)
+    dw.fill()
+    d = dw.upload_decode()
+    dw.set_plan(target_pages=9)
+    dw.step()
+    torch.cuda.synchronize()
+    nrec = dw.splits_per_seq.cpu().numpy()
+    ref_out, ref_lse = dw.bf16_u16(dw.out), dw.lse.cpu().numpy()
+    ref_op = [dw.out_partial[b, :int(nrec[b])].cpu().numpy() for b in range(w.B)]
+
+    def same():
+        assert np.array_equal(dw.bf16_u16(dw.out), ref_out)
+        assert np.array_equal(dw.lse.cpu().numpy(), ref_lse)
+        for b in range(w.B):
+            assert np.array_equal(dw.out_partial[b, :int(nrec[b])].cpu().numpy(), ref_op[b])
+
+    for _ in range(5):
+        d["q"].copy_(d["q0"])
+        dw.step()
+    torch.cuda.synchronize()
+    same()
+    g = harness.StepGraph(dw)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    same()
+    dw.out.zero_()
+    g2 = harness.StepGraph(dw, host_io=True)
+    g2.replay()
+    torch.cuda.synchronize()
+    same()
+    assert np.array_equal(g2.out_h.view(torch.int16).numpy().view(np.uint16), ref_out)
+    assert int(dw.err.item()) == 0
