@@ -89,6 +89,8 @@ def _L():
         lib.orc_mla_cache_write.restype = i64
         lib.orc_mla_decode.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, i64, ctypes.c_float, P, i32, P,
                                        dbl, i32, P, P]
+        lib.orc_mla_decode_splits.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, i64, ctypes.c_float, P, i32, P,
+                                              dbl, i32, P, P, P]
         _lib = lib
     return _lib
 
@@ -332,16 +334,19 @@ def mla_cache_write(q_pe, ckv, kpe, positions, cos_sin, ckv_cache, kpe_cache, sl
 
 
 def mla_decode(q_lat, q_pe, ckv_cache, kpe_cache, block_tables, seq_lens, softmax_scale: float, num_splits: int,
-               ckv_scale: float):
-    """(out_partial [B,S,H,Dc], lse_partial [B,S,H]) float64."""
+               ckv_scale: float, splits_per_seq=None):
+    """(out_partial [B,S,H,Dc], lse_partial [B,S,H]) float64. splits_per_seq
+    (int32 [B], optional): a split count per sequence, as for paged_decode."""
     q_lat = _c(q_lat, np.uint16); q_pe = _c(q_pe, np.uint16)
     B, H, Dc = q_lat.shape
     Dr = q_pe.shape[2]
     num_pages, P, _ = ckv_cache.shape
     bt = _c(block_tables, np.int32); sl = _c(seq_lens, np.int32)
+    sp = None if splits_per_seq is None else _c(splits_per_seq, np.int32)
+    assert sp is None or sp.shape == (B,)
     o = np.empty((B, num_splits, H, Dc), np.float64)
     l = np.empty((B, num_splits, H), np.float64)
-    _L().orc_mla_decode(B, H, Dc, Dr, P, _p(q_lat), _p(q_pe), _p(_c(ckv_cache, np.uint8)),
-                        _p(_c(kpe_cache, np.uint16)), num_pages, float(ckv_scale), _p(bt), bt.shape[1], _p(sl),
-                        float(softmax_scale), num_splits, _p(o), _p(l))
+    _L().orc_mla_decode_splits(B, H, Dc, Dr, P, _p(q_lat), _p(q_pe), _p(_c(ckv_cache, np.uint8)),
+                               _p(_c(kpe_cache, np.uint16)), num_pages, float(ckv_scale), _p(bt), bt.shape[1],
+                               _p(sl), float(softmax_scale), num_splits, _p(sp), _p(o), _p(l))
     return o, l

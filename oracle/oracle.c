@@ -374,6 +374,20 @@ static double cache_value(const cache_view* c, int layout, int64_t page, int off
 }
 
 /*
+ * The split count sequence b's pages are dealt into: splits_per_seq[b]
+ * (reading: a count below 1 is taken as 1 and one above num_splits as
+ * num_splits, the records the call has), or num_splits for every sequence
+ * when splits_per_seq is NULL.
+ */
+static int seq_split_count(const int32_t* splits_per_seq, int b, int num_splits) {
+    if (!splits_per_seq) return num_splits;
+    int sb = splits_per_seq[b];
+    if (sb < 1) sb = 1;
+    if (sb > num_splits) sb = num_splits;
+    return sb;
+}
+
+/*
  * One query head. Readings: query head h reads kv head floor(h / G) with
  * G = Hq / Hkv; the context is positions 0..L-1 (L = seq_lens[b], which
  * counts the new token); no mask, window, ALiBi or soft-cap. Split s covers
@@ -475,19 +489,6 @@ void orc_decode_head_nvfp4(int b, int h, int Hq, int Hkv, int D, int page_size,
                      lse_partial);
 }
 
-/*
- * The split count sequence b's pages are dealt into: splits_per_seq[b]
- * (reading: a count below 1 is taken as 1 and one above num_splits as
- * num_splits, the records the call has), or num_splits for every sequence
- * when splits_per_seq is NULL.
- */
-static int seq_split_count(const int32_t* splits_per_seq, int b, int num_splits) {
-    if (!splits_per_seq) return num_splits;
-    int sb = splits_per_seq[b];
-    if (sb < 1) sb = 1;
-    if (sb > num_splits) sb = num_splits;
-    return sb;
-}
 
 static void paged_decode_all(int B, int Hq, int Hkv, int D, int page_size, const uint16_t* q,
                              const cache_view* kc, const cache_view* vc, int64_t num_pages, int layout,
@@ -632,6 +633,20 @@ void orc_mla_decode(int B, int H, int Dc, int Dr, int page_size, const uint16_t*
                     const uint8_t* ckv_cache, const uint16_t* kpe_cache, int64_t num_pages, float ckv_scale,
                     const int32_t* block_tables, int max_pages, const int32_t* seq_lens, double softmax_scale,
                     int num_splits, double* out_partial, double* lse_partial) {
+    orc_mla_decode_splits(B, H, Dc, Dr, page_size, q_lat, q_pe, ckv_cache, kpe_cache, num_pages, ckv_scale,
+                          block_tables, max_pages, seq_lens, softmax_scale, num_splits, NULL, out_partial,
+                          lse_partial);
+}
+
+/* orc_mla_decode with a split count per sequence (reading: as for the GQA
+ * decode, sequence b's pages are dealt into splits_per_seq[b] splits,
+ * clamped to [1, num_splits], by the rule above; its records past that
+ * count are empty). NULL = num_splits for every sequence. */
+void orc_mla_decode_splits(int B, int H, int Dc, int Dr, int page_size, const uint16_t* q_lat, const uint16_t* q_pe,
+                           const uint8_t* ckv_cache, const uint16_t* kpe_cache, int64_t num_pages, float ckv_scale,
+                           const int32_t* block_tables, int max_pages, const int32_t* seq_lens, double softmax_scale,
+                           int num_splits, const int32_t* splits_per_seq, double* out_partial,
+                           double* lse_partial) {
     double* ql = (double*)malloc(sizeof(double) * (size_t)Dc);
     double* qr = (double*)malloc(sizeof(double) * (size_t)Dr);
     double cs = (double)ckv_scale;
@@ -641,7 +656,8 @@ void orc_mla_decode(int B, int H, int Dc, int Dr, int page_size, const uint16_t*
         int64_t npages = (L + page_size - 1) / page_size;
         if (npages > max_pages) npages = max_pages;
         if (L > npages * page_size) L = npages * page_size;
-        int64_t pps = (npages + num_splits - 1) / num_splits;
+        int64_t sb = seq_split_count(splits_per_seq, b, num_splits);
+        int64_t pps = (npages + sb - 1) / sb;
         int64_t cap = pps * page_size > 0 ? pps * page_size : 1;
         double* sc = (double*)malloc(sizeof(double) * (size_t)cap);
         int64_t* where = (int64_t*)malloc(sizeof(int64_t) * (size_t)cap);

@@ -143,6 +143,13 @@ void orc_mla_decode(int B, int H, int Dc, int Dr, int page_size, const uint16_t*
                     const uint8_t* ckv_cache, const uint16_t* kpe_cache, int64_t num_pages, float ckv_scale,
                     const int32_t* block_tables, int max_pages, const int32_t* seq_lens, double softmax_scale,
                     int num_splits, double* out_partial, double* lse_partial);
+/* orc_mla_decode with a split count per sequence (clamped to [1, num_splits];
+ * NULL = num_splits for every sequence); records past it are empty. */
+void orc_mla_decode_splits(int B, int H, int Dc, int Dr, int page_size, const uint16_t* q_lat, const uint16_t* q_pe,
+                           const uint8_t* ckv_cache, const uint16_t* kpe_cache, int64_t num_pages, float ckv_scale,
+                           const int32_t* block_tables, int max_pages, const int32_t* seq_lens, double softmax_scale,
+                           int num_splits, const int32_t* splits_per_seq, double* out_partial,
+                           double* lse_partial);
 
 /* Merge: out_partial [B,S,Hq,D], lse_partial [B,S,Hq] -> out [B,Hq,D],
  * lse [B,Hq]. */

@@ -86,6 +86,33 @@ def test_mla_split_merge_equals_single_pass(S):
     assert np.allclose(lse, one["lse"], rtol=0, atol=1e-12)
 
 
+def test_mla_per_sequence_splits_merge_to_the_single_pass_and_partition_the_pages():
+    """A split count per sequence (reading of the local split-K): merged, it
+    is the single pass; under equal scores (zero queries) a split's LSE is
+    the log of its token count, the counts fill a prefix of the sequence's
+    records, add up to its length and are whole 64-token pages but the last."""
+    lens = [1, 64, 65, 500, 130]
+    w = synth.custom_mla_workload("vsplit", 11, lens, 8)
+    one = mla_oracle_step(w, num_splits=1)
+    sp = np.array([1, 3, 2, 6, 0], np.int32)           # the last is clamped to 1
+    S = 6
+    args = (one["ckv_cache"], one["kpe_cache"], one["block_tables"], one["seq_lens"], w.softmax_scale, S,
+            w.ckv_scale)
+    op, lp = oracle.mla_decode(one["q_lat"], one["q_pe_rot"], *args, splits_per_seq=sp)
+    out, lse = oracle.lse_merge(op, lp)
+    assert np.allclose(out, one["out"], rtol=1e-12, atol=1e-13)
+    assert np.allclose(lse, one["lse"], rtol=0, atol=1e-12)
+    z_lat, z_pe = np.zeros_like(one["q_lat"]), np.zeros_like(one["q_pe_rot"])
+    _, lz = oracle.mla_decode(z_lat, z_pe, *args, splits_per_seq=sp)
+    for b, L in enumerate(lens):
+        sb = max(1, int(sp[b]))
+        counts = [round(np.exp(x)) if x != -np.inf else 0 for x in lz[b, :, 0]]
+        nz = [c for c in counts if c]
+        assert sum(counts) == L and counts[:len(nz)] == nz and len(nz) <= sb
+        assert all(c % 64 == 0 for c in nz[:-1])
+        assert np.all(lz[b, sb:] == -np.inf)
+
+
 def test_mla_page_permutation_invariance():
     w = synth.custom_mla_workload("perm", 9, [70, 200], 4)
     st = mla_oracle_step(w, num_splits=2)
