@@ -90,8 +90,8 @@ def parse_args():
                    help="one split count for every sequence (0 = the library's split plan, or its heuristic "
                         "count with --split-mode uniform)")
     p.add_argument("--split-mode", default="plan", choices=["plan", "uniform"],
-                   help="plan: a split count per sequence from pkv_plan_splits (GQA workloads); "
-                        "uniform: one count for the batch from pkv_choose_num_splits")
+                   help="plan: a split count per sequence from pkv_plan_splits (pkv_plan_splits_mla for MLA); "
+                        "uniform: one count for the batch from pkv_choose_num_splits (_mla)")
     p.add_argument("--also", default="qwen,longctx,fp8,fp4,million,mla,mla_batch",
                    help="other workloads measured the same way, reported under 'other_workloads' ('' = none)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -510,10 +510,11 @@ def measure_layered(dw, layers: int, reps: int, flush, peak: float) -> dict:
 
 def make_workload(name: str, splits: int, split_mode: str):
     """The device workload with its split configuration: an explicit count,
-    else the library's split plan (GQA) or its heuristic count."""
+    else the library's split plan (pkv_plan_splits, or pkv_plan_splits_mla
+    for an MLA workload) or, with split_mode "uniform", its heuristic count."""
     from paged_kv_gqa_04_gb300 import harness
     dw = harness.make_device_workload(name, num_splits=splits or None)
-    if not splits and split_mode == "plan" and not is_mla(name):
+    if not splits and split_mode == "plan":
         dw.set_plan()
     return dw
 
@@ -524,8 +525,10 @@ def split_desc(dw) -> dict:
         sp, work = dw.plan_host
         pages = dw.w.pages_per_seq
         pps = -(-pages // np.maximum(sp, 1))
+        # GQA: one CTA per (item, kv head); MLA: the items go to a persistent grid
+        ctas = int(len(work)) * dw.w.Hkv if hasattr(dw.w, "Hkv") else None
         return {"mode": "plan", "records": dw.num_splits, "items": int(len(work)),
-                "ctas": int(len(work)) * dw.w.Hkv, "splits_per_seq_min": int(sp.min()),
+                "ctas": ctas, "splits_per_seq_min": int(sp.min()),
                 "splits_per_seq_max": int(sp.max()), "max_pages_per_split": int(pps.max())}
     return {"mode": "uniform", "records": dw.num_splits}
 

@@ -449,6 +449,38 @@ pkv_status pkv_paged_gqa_decode_planned(const pkv_tensor* q, const pkv_tensor* k
                                         pkv_stream_t stream);
 
 /*
+ * pkv_plan_splits_mla -- the split plan of the MLA decode (host only; no CUDA
+ * call). The persistent MLA decode (two CTAs per SM) takes the plan's items
+ * in order; when every sequence can have a CTA of its own, the automatic
+ * plan (target_pages = 0) makes at most one item per CTA, all of nearly
+ * equal length: the smallest even page target (whole 128-token chunks)
+ * whose items fit the CTAs; past that, the longest split of
+ * pkv_choose_num_splits_mla. seq_lens counts tokens, pages are the cache's
+ * 64-token pages (max_pages = the block-table width); every other argument
+ * and output is that of pkv_plan_splits.
+ */
+pkv_status pkv_plan_splits_mla(const int32_t* seq_lens, int32_t B, int32_t H, int32_t max_pages, int32_t sm_count,
+                               int32_t max_splits, int32_t target_pages, int32_t* splits_per_seq,
+                               int32_t* num_records, int32_t* work, int64_t work_capacity, int64_t* num_work);
+
+/*
+ * pkv_paged_mla_decode_planned -- pkv_paged_mla_decode under a split plan
+ * (splits_per_seq device [B] int32, work device [W, 2] int32 with strides 2,
+ * 1, as for pkv_paged_gqa_decode_planned); out_partial [B, S, H, 512] and
+ * lse_partial [B, S, H] with S >= every S_b, S <= 4095. Each written record
+ * is that of pkv_paged_mla_decode with S_b splits; records [S_b, S) of
+ * sequence b are not written. Merge with pkv_lse_merge_planned (D = 512).
+ * Errors: besides pkv_paged_mla_decode's, items outside the batch or the
+ * records are skipped and set PKV_FLAG_PLAN_RANGE.
+ */
+pkv_status pkv_paged_mla_decode_planned(const pkv_tensor* q_lat, const pkv_tensor* q_pe, const pkv_tensor* ckv_cache,
+                                        const pkv_tensor* kpe_cache, const pkv_tensor* block_tables,
+                                        const pkv_tensor* seq_lens, float softmax_scale,
+                                        const pkv_tensor* splits_per_seq, const pkv_tensor* work,
+                                        const pkv_tensor* out_partial, const pkv_tensor* lse_partial,
+                                        const pkv_tensor* ckv_scale, int32_t* err_flag, pkv_stream_t stream);
+
+/*
  * pkv_lse_merge_planned -- pkv_lse_merge of each sequence's own records
  * [0, S_b) (S_b = splits_per_seq[b], device [B] int32, clamped to [1, S]).
  */
@@ -586,7 +618,7 @@ const char* pkv_status_string(int32_t status);
 
 /* ABI version of this header (bumped on any signature change). */
 int32_t pkv_abi_version(void);
-#define PKV_ABI_VERSION 6
+#define PKV_ABI_VERSION 7
 
 #ifdef __cplusplus
 }

@@ -43,7 +43,7 @@ EXPORTED = ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_c
             "pkv_validate_indices_static", "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4",
             "pkv_mla_cache_write", "pkv_paged_mla_decode", "pkv_choose_num_splits_mla",
             "pkv_selftest_bounded_wait", "pkv_copy", "pkv_plan_splits", "pkv_paged_gqa_decode_planned",
-            "pkv_lse_merge_planned")
+            "pkv_lse_merge_planned", "pkv_plan_splits_mla", "pkv_paged_mla_decode_planned")
 
 
 class PkvTensor(ctypes.Structure):
@@ -89,13 +89,16 @@ def lib() -> ctypes.CDLL:
         L.pkv_paged_gqa_decode_planned.argtypes = [T, T, T, T, T, T, T, ctypes.c_float, T, T, T, T, T, T, i32, P,
                                                    P]
         L.pkv_lse_merge_planned.argtypes = [T, T, T, T, T, P]
+        L.pkv_plan_splits_mla.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P, ctypes.c_int64, P]
+        L.pkv_paged_mla_decode_planned.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, T, T, P, P]
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         for name in ("pkv_rope_kv_write", "pkv_paged_gqa_decode", "pkv_lse_merge", "pkv_validate_indices",
                      "pkv_choose_num_splits", "pkv_abi_version", "pkv_stream_read", "pkv_validate_indices_static",
                      "pkv_rope_kv_write_nvfp4", "pkv_paged_gqa_decode_nvfp4", "pkv_mla_cache_write",
                      "pkv_paged_mla_decode", "pkv_choose_num_splits_mla", "pkv_selftest_bounded_wait", "pkv_copy",
-                     "pkv_plan_splits", "pkv_paged_gqa_decode_planned", "pkv_lse_merge_planned"):
+                     "pkv_plan_splits", "pkv_paged_gqa_decode_planned", "pkv_lse_merge_planned",
+                     "pkv_plan_splits_mla", "pkv_paged_mla_decode_planned"):
             getattr(L, name).restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -260,6 +263,34 @@ def paged_gqa_decode_planned(q, k_cache, v_cache, block_tables, seq_lens, softma
         _desc(q), kc, vc, _desc(k_block_scale), _desc(v_block_scale), _desc(block_tables), _desc(seq_lens),
         float(softmax_scale), _desc(splits_per_seq), _desc(work), _desc(out_partial), _desc(lse_partial),
         _desc(k_scale), _desc(v_scale), LAYOUTS[layout], _ptr(err_flag), _stream(stream)))
+
+
+def plan_splits_mla(seq_lens, H: int, max_pages: int, sm_count: int, max_splits: int = 4095, target_pages: int = 0):
+    """pkv_plan_splits_mla (host only): (splits_per_seq int32 [B],
+    num_records, work int32 [W, 2]) for the planned MLA decode."""
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = int(sl.size)
+    sp = np.zeros(max(B, 1), np.int32)
+    nrec = ctypes.c_int32(0)
+    nwork = ctypes.c_int64(0)
+    f = lib().pkv_plan_splits_mla
+    args = (sl.ctypes.data if B else None, B, H, max_pages, sm_count, max_splits, target_pages, sp.ctypes.data)
+    _check("pkv_plan_splits_mla", f(*args, ctypes.byref(nrec), None, 0, ctypes.byref(nwork)))
+    work = np.zeros((max(int(nwork.value), 1), 2), np.int32)
+    _check("pkv_plan_splits_mla", f(*args, ctypes.byref(nrec), work.ctypes.data, int(nwork.value),
+                                    ctypes.byref(nwork)))
+    return sp[:B], int(nrec.value), work[:int(nwork.value)]
+
+
+def paged_mla_decode_planned(q_lat, q_pe, ckv_cache, kpe_cache, block_tables, seq_lens, softmax_scale: float,
+                             splits_per_seq, work, out_partial, lse_partial, ckv_scale, err_flag=None,
+                             stream=None) -> None:
+    """pkv_paged_mla_decode_planned: the MLA decode under a split plan."""
+    _check("pkv_paged_mla_decode_planned", lib().pkv_paged_mla_decode_planned(
+        _desc(q_lat), _desc(q_pe), _desc(ckv_cache), _desc(kpe_cache), _desc(block_tables), _desc(seq_lens),
+        float(softmax_scale), _desc(splits_per_seq), _desc(work), _desc(out_partial), _desc(lse_partial),
+        _desc(ckv_scale), _ptr(err_flag), _stream(stream)))
 
 
 def lse_merge_planned(out_partial, lse_partial, splits_per_seq, out, lse_out=None, stream=None) -> None:

@@ -163,26 +163,45 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     return mbar_wait_or_abort(bar, parity, abort_flag, kWaitLimitNs);
 }
 
-// One work item: split s of sequence b (items are numbered b * S + s).
+// One work item: split s of sequence b (items are numbered b * S + s, or
+// are the entries of a split plan's work list).
 struct Item {
     int b, s;
     int npg;              // pages of the split
     int ntok;             // tokens of the split
     int nch;              // chunks of the split
     bool bad_len;         // seq_lens[b] outside [0, block-table width x page]
+    bool planless;        // a plan entry outside the batch or the records: no record, no work
     const int32_t* bt;    // the split's block-table entries
 };
 
 __device__ __forceinline__ Item item_of(const MlaDecodeArgs& a, int it) {
     Item x;
-    x.b = it / a.num_splits;
-    x.s = it - x.b * a.num_splits;
+    int S = a.num_splits;
+    x.planless = false;
+    if (a.work == nullptr) {
+        x.b = it / a.num_splits;
+        x.s = it - x.b * a.num_splits;
+    } else {
+        const int e = __ldg(a.work + 2 * it);
+        x.b = e >> 12;
+        x.s = e & 0xFFF;
+        if (x.b < 0 || x.b >= a.B || x.s >= a.num_splits) {
+            x.planless = true;
+            x.b = 0;
+            x.npg = x.ntok = x.nch = 0;
+            x.bad_len = false;
+            x.bt = a.block_tables;
+            return x;
+        }
+        S = min(max(__ldg(a.splits_per_seq + x.b), 1), a.num_splits);
+    }
     const int L0 = __ldg(a.seq_lens + x.b);
     const int cap = a.max_pages * kMlaPage;
     x.bad_len = L0 < 0 || L0 > cap;
     const int L = min(max(L0, 0), cap);
     const int npages = (L + kMlaPage - 1) / kMlaPage;
-    const int pps = (npages + a.num_splits - 1) / a.num_splits;
+    const int pps = (npages + S - 1) / S;
     const int p0 = x.s * pps;
     const int p1 = min(p0 + pps, npages);
     x.npg = max(p1 - p0, 0);
@@ -207,6 +226,7 @@ __device__ __forceinline__ int page_of(const Item& x, int pg, int64_t num_pages)
 // drew one of the longest splits draws one of the shortest next.
 __device__ __forceinline__ int slot_item(const MlaDecodeArgs& a, const int16_t* order, int j, int n_items) {
     const int G = gridDim.x, k = blockIdx.x;
+    if (a.work != nullptr) order = nullptr;  // a plan's items come in its own order
     const int64_t p = static_cast<int64_t>(j) * G + ((order != nullptr && (j & 1)) ? G - 1 - k : k);
     if (p >= n_items) return n_items;  // only the last round is partial: nothing follows
     if (order == nullptr) return static_cast<int>(p);
@@ -269,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int H = a.H;
-    const int n_items = a.B * a.num_splits;
+    const int n_items = a.work != nullptr ? static_cast<int>(a.n_work) : a.B * a.num_splits;
     const int64_t num_pages = a.num_pages;
 
     if (threadIdx.x == 0) {
@@ -294,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // index (index inputs only, read before the grid-dependency wait like
     // the L2 read-ahead below).
     int16_t* order_tab = reinterpret_cast<int16_t*>(smem + kOffOrder);
-    if (warp == kWarpCopy && a.B <= kSortMaxB) {
+    if (warp == kWarpCopy && a.B <= kSortMaxB && a.work == nullptr) {
         const int cap = a.max_pages * kMlaPage;
         int key[2];
 #pragma unroll
@@ -317,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int16_t* order = a.B <= kSortMaxB ? order_tab : nullptr;
+    const int16_t* order = (a.B <= kSortMaxB && a.work == nullptr) ? order_tab : nullptr;
 
     // L2 read-ahead of one chunk (lanes 0-4: its first page, 8-12: second)
     auto prefetch_at = [&](const Cursor& u) {
@@ -336,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // 16 + h: q_pe row h), for 16-byte aligned rows
     auto prefetch_q = [&](int it) {
         if (it >= n_items) return;
-        const int bq = it / a.num_splits;
+        const int bq = a.work != nullptr ? min(max(__ldg(a.work + 2 * it) >> 12, 0), a.B - 1) : it / a.num_splits;
         const int h = lane & 15;
         if (h < H) {
             const void* r = lane < 16 ? static_cast<const void*>(a.q_lat + bq * a.ql_s0 + h * a.ql_s1)
@@ -593,6 +613,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const int it = slot_item(a, order, j, n_items);
                 if (it >= n_items) return j;
                 const Item y = item_of(a, it);
+                if (i == 0 && y.planless) flag_error(a.err, PKV_FLAG_PLAN_RANGE);
+                if (y.planless) continue;
                 if (i == 0 && y.s == 0 && y.bad_len) flag_error(a.err, PKV_FLAG_SEQ_LEN_RANGE);
                 if (y.nch > 0) return j;
                 float* op = a.out_partial + y.b * a.op_s0 + y.s * a.op_s1;
@@ -866,7 +888,8 @@ cudaError_t launch_mla_decode(const MlaDecodeArgs& a, const CUtensorMap& tckv, c
     if (e != cudaSuccess) return e;
     // persistent: at most two CTAs per SM, each taking one item of every
     // round of gridDim.x schedule positions
-    const int64_t items = static_cast<int64_t>(a.B) * a.num_splits;
+    const int64_t items = a.work != nullptr ? a.n_work : static_cast<int64_t>(a.B) * a.num_splits;
+    if (items == 0) return cudaSuccess;
     const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(kCtasPerSm) * sms));
     return launch_dependent(kernel, dim3(grid), dim3(kThreads), kSmem, s, tckv, tkpe, a);
 }

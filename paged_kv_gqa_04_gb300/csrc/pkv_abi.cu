@@ -660,11 +660,14 @@ pkv_status pkv_mla_cache_write(const pkv_tensor* q_pe_p, const pkv_tensor* ckv_p
     return cuda_status(pkv::launch_mla_cache_write(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-pkv_status pkv_paged_mla_decode(const pkv_tensor* q_lat_p, const pkv_tensor* q_pe_p, const pkv_tensor* ckv_cache_p,
-                                const pkv_tensor* kpe_cache_p, const pkv_tensor* block_tables_p,
-                                const pkv_tensor* seq_lens_p, float softmax_scale, int32_t num_splits,
-                                const pkv_tensor* out_partial_p, const pkv_tensor* lse_partial_p,
-                                const pkv_tensor* ckv_scale_p, int32_t* err_flag, pkv_stream_t stream) {
+static pkv_status paged_mla_decode_impl(const pkv_tensor* q_lat_p, const pkv_tensor* q_pe_p,
+                                        const pkv_tensor* ckv_cache_p, const pkv_tensor* kpe_cache_p,
+                                        const pkv_tensor* block_tables_p, const pkv_tensor* seq_lens_p,
+                                        float softmax_scale, int32_t num_splits, const pkv_tensor* out_partial_p,
+                                        const pkv_tensor* lse_partial_p, const pkv_tensor* ckv_scale_p,
+                                        int32_t* err_flag, pkv_stream_t stream,
+                                        const pkv_tensor* splits_per_seq_p = nullptr,
+                                        const pkv_tensor* work_p = nullptr) {
     const pkv_tensor& q_lat = arg(q_lat_p);
     const pkv_tensor& q_pe = arg(q_pe_p);
     const pkv_tensor& ckv_cache = arg(ckv_cache_p);
@@ -712,10 +715,28 @@ pkv_status pkv_paged_mla_decode(const pkv_tensor* q_lat_p, const pkv_tensor* q_p
         (out_partial.stride[2] % 2))
         return PKV_ERR_UNSUPPORTED;
 
+    const bool planned = work_p != nullptr;
+    int64_t n_work = 0;
+    if (planned) {
+        const pkv_tensor& sp = arg(splits_per_seq_p);
+        const pkv_tensor& wk = arg(work_p);
+        if (!shape_ok(sp, 1, PKV_I32) || sp.shape[0] != B || !sp.ptr) return PKV_ERR_INVALID_ARG;
+        if (!shape_ok(wk, 2, PKV_I32) || wk.shape[1] != 2) return PKV_ERR_INVALID_ARG;
+        n_work = wk.shape[0];
+        if (n_work > 0 && !wk.ptr) return PKV_ERR_INVALID_ARG;
+        if (sp.stride[0] != 1 || wk.stride[1] != 1 || wk.stride[0] != 2) return PKV_ERR_UNSUPPORTED;
+        if (n_work > 0x7FFFFFFF || num_splits > 4095) return PKV_ERR_UNSUPPORTED;
+    }
+
     CUtensorMap tckv, tkpe;
     if (!make_mla_map(&tckv, ckv_cache) || !make_mla_map(&tkpe, kpe_cache)) return PKV_ERR_CUDA;
 
     pkv::MlaDecodeArgs a{};
+    if (planned) {
+        a.splits_per_seq = static_cast<const int32_t*>(arg(splits_per_seq_p).ptr);
+        a.work = static_cast<const int32_t*>(arg(work_p).ptr);
+        a.n_work = n_work;
+    }
     a.q_lat = static_cast<const uint16_t*>(q_lat.ptr);
     a.ql_s0 = q_lat.stride[0];
     a.ql_s1 = q_lat.stride[1];
@@ -741,6 +762,30 @@ pkv_status pkv_paged_mla_decode(const pkv_tensor* q_lat_p, const pkv_tensor* q_p
     a.H = static_cast<int32_t>(H);
     a.err = err_flag;
     return cuda_status(pkv::launch_mla_decode(a, tckv, tkpe, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_mla_decode(const pkv_tensor* q_lat, const pkv_tensor* q_pe, const pkv_tensor* ckv_cache,
+                                const pkv_tensor* kpe_cache, const pkv_tensor* block_tables,
+                                const pkv_tensor* seq_lens, float softmax_scale, int32_t num_splits,
+                                const pkv_tensor* out_partial, const pkv_tensor* lse_partial,
+                                const pkv_tensor* ckv_scale, int32_t* err_flag, pkv_stream_t stream) {
+    return paged_mla_decode_impl(q_lat, q_pe, ckv_cache, kpe_cache, block_tables, seq_lens, softmax_scale,
+                                 num_splits, out_partial, lse_partial, ckv_scale, err_flag, stream);
+}
+
+pkv_status pkv_paged_mla_decode_planned(const pkv_tensor* q_lat, const pkv_tensor* q_pe, const pkv_tensor* ckv_cache,
+                                        const pkv_tensor* kpe_cache, const pkv_tensor* block_tables,
+                                        const pkv_tensor* seq_lens, float softmax_scale,
+                                        const pkv_tensor* splits_per_seq, const pkv_tensor* work,
+                                        const pkv_tensor* out_partial, const pkv_tensor* lse_partial,
+                                        const pkv_tensor* ckv_scale, int32_t* err_flag, pkv_stream_t stream) {
+    if (!splits_per_seq || !work || !out_partial) return PKV_ERR_INVALID_ARG;
+    const pkv_tensor& op = arg(out_partial);
+    if (op.ndim != 4 || op.shape[1] < 1) return PKV_ERR_INVALID_ARG;
+    if (op.shape[1] > 4095) return PKV_ERR_UNSUPPORTED;
+    return paged_mla_decode_impl(q_lat, q_pe, ckv_cache, kpe_cache, block_tables, seq_lens, softmax_scale,
+                                 static_cast<int32_t>(op.shape[1]), out_partial, lse_partial, ckv_scale, err_flag,
+                                 stream, splits_per_seq, work);
 }
 
 int32_t pkv_choose_num_splits_mla(int32_t B, int32_t H, int64_t total_pages, int32_t max_pages, int32_t sm_count) {
@@ -848,6 +893,84 @@ int32_t pkv_choose_num_splits(int32_t B, int32_t Hkv, int32_t Hq, int32_t D, int
     return best;
 }
 
+namespace {
+
+// The split count of a sequence of n pages under a target of T pages per
+// split, at most max_splits, reduced to the splits that hold pages when that
+// keeps the same page ranges.
+int64_t plan_count(int64_t n, int64_t T, int max_splits) {
+    if (n <= 0) return 1;
+    const int64_t S = std::min<int64_t>((n + T - 1) / T, max_splits);
+    const int64_t pps = (n + S - 1) / S;
+    const int64_t k = (n + pps - 1) / pps;
+    return ((n + k - 1) / k == pps) ? k : S;
+}
+
+// Pages of each sequence (seq_lens clamped to [0, page * max_pages]).
+std::vector<int64_t> plan_pages(const int32_t* seq_lens, int32_t B, int64_t page, int32_t max_pages, int64_t* max_np,
+                                int64_t* total) {
+    std::vector<int64_t> np(B);
+    *max_np = 0;
+    *total = 0;
+    for (int b = 0; b < B; ++b) {
+        const int64_t L = std::min<int64_t>(std::max<int32_t>(seq_lens[b], 0), page * max_pages);
+        np[b] = (L + page - 1) / page;
+        *max_np = std::max(*max_np, np[b]);
+        *total += np[b];
+    }
+    return np;
+}
+
+// The plan's outputs for a page target T: split counts, record count and
+// the work list, items in order of decreasing page count (ties by sequence
+// then split).
+pkv_status plan_emit(const std::vector<int64_t>& np, int64_t T, int max_splits, int32_t* splits_per_seq,
+                     int32_t* num_records, int32_t* work, int64_t work_capacity, int64_t* num_work) {
+    const int B = static_cast<int>(np.size());
+    int64_t n_items = 0;
+    int32_t recs = 1;
+    for (int b = 0; b < B; ++b) {
+        const int64_t S = plan_count(np[b], T, max_splits);
+        splits_per_seq[b] = static_cast<int32_t>(S);
+        recs = std::max<int32_t>(recs, static_cast<int32_t>(S));
+        n_items += S;
+    }
+    *num_records = recs;
+    *num_work = n_items;
+    if (!work) return PKV_OK;
+    if (work_capacity < n_items) return PKV_ERR_INVALID_ARG;
+    struct It { int64_t pages; int32_t b, s, p0; };
+    std::vector<It> items;
+    items.reserve(static_cast<size_t>(n_items));
+    for (int b = 0; b < B; ++b) {
+        const int64_t S = splits_per_seq[b];
+        const int64_t pps = np[b] > 0 ? (np[b] + S - 1) / S : 0;
+        for (int64_t sp = 0; sp < S; ++sp) {
+            const int64_t p0 = std::min(sp * pps, np[b]);
+            items.push_back({std::min(pps, np[b] - p0), b, static_cast<int32_t>(sp), static_cast<int32_t>(p0)});
+        }
+    }
+    std::stable_sort(items.begin(), items.end(), [](const It& x, const It& y) { return x.pages > y.pages; });
+    for (int64_t i = 0; i < n_items; ++i) {
+        work[2 * i] = (items[i].b << 12) | items[i].s;
+        work[2 * i + 1] = items[i].p0;
+    }
+    return PKV_OK;
+}
+
+pkv_status plan_check(const int32_t* seq_lens, int32_t B, int32_t max_pages, int32_t sm_count, int32_t max_splits,
+                      int32_t target_pages, const int32_t* splits_per_seq, const int32_t* num_records,
+                      const int32_t* work, int64_t work_capacity, const int64_t* num_work) {
+    if (B < 0 || max_pages < 1 || sm_count < 1) return PKV_ERR_INVALID_ARG;
+    if (max_splits < 1 || max_splits > 4095 || target_pages < 0 || work_capacity < 0) return PKV_ERR_INVALID_ARG;
+    if (B > (1 << 19) || max_pages > (1 << 26)) return PKV_ERR_UNSUPPORTED;
+    if ((B > 0 && (!seq_lens || !splits_per_seq)) || !num_records || !num_work) return PKV_ERR_INVALID_ARG;
+    if (work_capacity > 0 && !work) return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
+}  // namespace
+
 // The split plan: a split count per sequence so that every CTA streams
 // about the same number of pages, and the work list of (sequence, split)
 // items, longest first. Host only; no CUDA call.
@@ -855,28 +978,12 @@ pkv_status pkv_plan_splits(const int32_t* seq_lens, int32_t B, int32_t Hkv, int3
                            int32_t max_pages, int32_t cache_dtype, int32_t sm_count, int32_t max_splits,
                            int32_t target_pages, int32_t* splits_per_seq, int32_t* num_records, int32_t* work,
                            int64_t work_capacity, int64_t* num_work) {
-    if (B < 0 || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || D < 1 || max_pages < 1 || sm_count < 1) return PKV_ERR_INVALID_ARG;
-    if (max_splits < 1 || max_splits > 4095 || target_pages < 0 || work_capacity < 0) return PKV_ERR_INVALID_ARG;
-    if (B > (1 << 19) || max_pages > (1 << 26)) return PKV_ERR_UNSUPPORTED;
-    if ((B > 0 && (!seq_lens || !splits_per_seq)) || !num_records || !num_work) return PKV_ERR_INVALID_ARG;
-    if (work_capacity > 0 && !work) return PKV_ERR_INVALID_ARG;
-    std::vector<int64_t> np(B);
+    if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || D < 1) return PKV_ERR_INVALID_ARG;
+    pkv_status st = plan_check(seq_lens, B, max_pages, sm_count, max_splits, target_pages, splits_per_seq,
+                               num_records, work, work_capacity, num_work);
+    if (st != PKV_OK) return st;
     int64_t max_np = 0, total = 0;
-    for (int b = 0; b < B; ++b) {
-        const int64_t L = std::min<int64_t>(std::max<int32_t>(seq_lens[b], 0), int64_t{16} * max_pages);
-        np[b] = (L + kPageSize - 1) / kPageSize;
-        max_np = std::max(max_np, np[b]);
-        total += np[b];
-    }
-    // the split count of a sequence of n pages under a target of T pages
-    // per split, reduced to the splits that hold pages (same page ranges)
-    auto count = [&](int64_t n, int64_t T) -> int64_t {
-        if (n <= 0) return 1;
-        int64_t S = std::min<int64_t>((n + T - 1) / T, max_splits);
-        const int64_t pps = (n + S - 1) / S;
-        const int64_t k = (n + pps - 1) / pps;
-        return ((n + k - 1) / k == pps) ? k : S;
-    };
+    const std::vector<int64_t> np = plan_pages(seq_lens, B, kPageSize, max_pages, &max_np, &total);
     int64_t T = target_pages;
     if (T == 0) {
         // When every sequence and kv head can have a CTA of its own within
@@ -909,7 +1016,7 @@ pkv_status pkv_plan_splits(const int32_t* seq_lens, int32_t B, int32_t Hkv, int3
                 double items = 0, p_max = 0;
                 int64_t recs = 1;
                 for (int b = 0; b < B; ++b) {
-                    const int64_t S = count(np[b], Tc);
+                    const int64_t S = plan_count(np[b], Tc, max_splits);
                     items += static_cast<double>(S);
                     p_max = std::max(p_max, static_cast<double>(np[b] > 0 ? (np[b] + S - 1) / S : 0));
                     recs = std::max(recs, S);
@@ -927,36 +1034,44 @@ pkv_status pkv_plan_splits(const int32_t* seq_lens, int32_t B, int32_t Hkv, int3
             T = best_T;
         }
     }
-    int64_t n_items = 0;
-    int32_t recs = 1;
-    for (int b = 0; b < B; ++b) {
-        const int64_t S = count(np[b], T);
-        splits_per_seq[b] = static_cast<int32_t>(S);
-        recs = std::max<int32_t>(recs, static_cast<int32_t>(S));
-        n_items += S;
-    }
-    *num_records = recs;
-    *num_work = n_items;
-    if (!work) return PKV_OK;
-    if (work_capacity < n_items) return PKV_ERR_INVALID_ARG;
-    // items in order of decreasing pages, ties by sequence then split
-    struct It { int64_t pages; int32_t b, s, p0; };
-    std::vector<It> items;
-    items.reserve(static_cast<size_t>(n_items));
-    for (int b = 0; b < B; ++b) {
-        const int64_t S = splits_per_seq[b];
-        const int64_t pps = np[b] > 0 ? (np[b] + S - 1) / S : 0;
-        for (int64_t sp = 0; sp < S; ++sp) {
-            const int64_t p0 = std::min(sp * pps, np[b]);
-            items.push_back({std::min(pps, np[b] - p0), b, static_cast<int32_t>(sp), static_cast<int32_t>(p0)});
+    return plan_emit(np, T, max_splits, splits_per_seq, num_records, work, work_capacity, num_work);
+}
+
+// The split plan of the MLA decode: persistent CTAs (two per SM) take the
+// items in the plan's order. When every sequence can have a CTA of its own,
+// the plan makes at most one item per CTA, of nearly equal length: the
+// smallest page target (whole 128-token chunks: an even page count) whose
+// items fit the CTAs; else the uniform heuristic's longest split. Host only.
+pkv_status pkv_plan_splits_mla(const int32_t* seq_lens, int32_t B, int32_t H, int32_t max_pages, int32_t sm_count,
+                               int32_t max_splits, int32_t target_pages, int32_t* splits_per_seq,
+                               int32_t* num_records, int32_t* work, int64_t work_capacity, int64_t* num_work) {
+    if (H < 1) return PKV_ERR_INVALID_ARG;
+    pkv_status st = plan_check(seq_lens, B, max_pages, sm_count, max_splits, target_pages, splits_per_seq,
+                               num_records, work, work_capacity, num_work);
+    if (st != PKV_OK) return st;
+    int64_t max_np = 0, total = 0;
+    const std::vector<int64_t> np = plan_pages(seq_lens, B, pkv::kMlaPage, max_pages, &max_np, &total);
+    int64_t T = target_pages;
+    if (T == 0) {
+        const int64_t ctas = static_cast<int64_t>(sm_count) * pkv::mla_decode_ctas_per_sm(H);
+        const int64_t top = std::max<int64_t>(max_np, 1);
+        if (static_cast<int64_t>(B) > ctas) {
+            const int32_t S_u = pkv_choose_num_splits_mla(B, H, std::max<int64_t>(total, 1), static_cast<int32_t>(top),
+                                                          sm_count);
+            T = (top + S_u - 1) / S_u;
+        } else {
+            T = top;
+            for (int64_t Tc = 2; Tc < top; Tc += 2) {
+                int64_t items = 0;
+                for (int b = 0; b < B && items <= ctas; ++b) items += plan_count(np[b], Tc, max_splits);
+                if (items <= ctas) {
+                    T = Tc;
+                    break;
+                }
+            }
         }
     }
-    std::stable_sort(items.begin(), items.end(), [](const It& x, const It& y) { return x.pages > y.pages; });
-    for (int64_t i = 0; i < n_items; ++i) {
-        work[2 * i] = (items[i].b << 12) | items[i].s;
-        work[2 * i + 1] = items[i].p0;
-    }
-    return PKV_OK;
+    return plan_emit(np, T, max_splits, splits_per_seq, num_records, work, work_capacity, num_work);
 }
 
 pkv_status pkv_validate_indices(const pkv_tensor* block_tables_p, const pkv_tensor* seq_lens_p, const pkv_tensor* slot_mapping_p,

@@ -109,6 +109,12 @@ struct MlaDecodeArgs {
     float* lse_partial;        // [B, S, H]
     int64_t lp_s0, lp_s1;
     int32_t B, H;
+    // A split plan (both null: every sequence in num_splits splits): item i
+    // = work[2 i] = (b << 12) | s in the plan's order, splits_per_seq[b] the
+    // sequence's split count.
+    const int32_t* work;
+    int64_t n_work;
+    const int32_t* splits_per_seq;
     int32_t* err;
 };
 

@@ -326,6 +326,7 @@ class MlaDeviceWorkload:
         self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
         self.ckv_scale = torch.tensor([w.ckv_scale], dtype=torch.float32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.splits_per_seq = self.work = None
         if num_splits is None:
             props = torch.cuda.get_device_properties(dev)
             num_splits = _abi.choose_num_splits_mla(w.B, w.H, int(w.pages_per_seq.sum()),
@@ -337,10 +338,28 @@ class MlaDeviceWorkload:
         self.decode_inputs = None
 
     def set_splits(self, num_splits: int) -> None:
+        """One split count for every sequence (drops any split plan)."""
         w = self.w
+        self.splits_per_seq = self.work = None
         self.num_splits = int(num_splits)
         self.out_partial = torch.empty((w.B, self.num_splits, w.H, w.Dc), dtype=torch.float32, device=self.device)
         self.lse_partial = torch.empty((w.B, self.num_splits, w.H), dtype=torch.float32, device=self.device)
+
+    def set_plan(self, target_pages: int = 0, max_splits: int = 4095) -> None:
+        """A split count per sequence from the library's MLA planner (host
+        seq_lens), uploaded with its work list."""
+        w = self.w
+        props = torch.cuda.get_device_properties(self.device)
+        sp, nrec, work = _abi.plan_splits_mla(w.seq_lens, w.H, max(1, int(w.block_tables.shape[1])),
+                                              props.multi_processor_count, max_splits, target_pages)
+        self.set_splits(nrec)
+        self.plan_host = (sp, work)
+        self.splits_per_seq = torch.from_numpy(sp).to(self.device)
+        self.work = torch.from_numpy(np.ascontiguousarray(work)).to(self.device)
+
+    @property
+    def planned(self) -> bool:
+        return self.work is not None
 
     def fill(self, max_tokens: int = 1 << 17) -> int:
         """Context tokens 0..L-2 of every sequence through the library's MLA
@@ -382,11 +401,20 @@ class MlaDeviceWorkload:
 
     def decode_into(self, q_pe, caches: tuple, out_partial, lse_partial, stream=None) -> None:
         w = self.w
+        if self.planned:
+            _abi.paged_mla_decode_planned(self.decode_inputs["q_lat"], q_pe, caches[0], caches[1], self.block_tables,
+                                          self.seq_lens, w.softmax_scale, self.splits_per_seq, self.work,
+                                          out_partial, lse_partial, self.ckv_scale, self.err, stream)
+            return
         _abi.paged_mla_decode(self.decode_inputs["q_lat"], q_pe, caches[0], caches[1], self.block_tables,
                               self.seq_lens, w.softmax_scale, self.num_splits, out_partial, lse_partial,
                               self.ckv_scale, self.err, stream)
 
     def merge(self, stream=None) -> None:
+        if self.planned:
+            _abi.lse_merge_planned(self.out_partial, self.lse_partial, self.splits_per_seq, self.out, self.lse,
+                                   stream)
+            return
         _abi.lse_merge(self.out_partial, self.lse_partial, self.out, self.lse, stream)
 
     def upload_decode(self) -> dict:

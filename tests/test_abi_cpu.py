@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pkv_abi_version() == 6
+    assert lib.pkv_abi_version() == 7
     for s in range(4):
         assert pkv.status_string(s)
     assert "invalid" in pkv.status_string(1)
@@ -411,3 +411,77 @@ def test_planned_decode_and_merge_reject_inconsistent_arguments(lib):
     assert m(op, lp, None, out, NULL, None) == _abi.PKV_ERR_INVALID_ARG
     assert m(op, lp, _t((B + 1,), "i32"), out, NULL, None) == _abi.PKV_ERR_INVALID_ARG
     assert m(op, lp, _t((B,), "f32"), out, NULL, None) == _abi.PKV_ERR_INVALID_ARG
+
+
+def _mla_plan_pages(np_b, S):
+    pps = -(-np_b // S) if np_b else 0
+    return [max(0, min(pps, np_b - s * pps)) for s in range(S)]
+
+
+@pytest.mark.parametrize("name", ["mla_tiny", "mla", "mla_batch"])
+def test_mla_split_plan_covers_every_split_once_longest_first(lib, name):
+    w = synth.make_mla_workload(name)
+    mp = int(w.block_tables.shape[1])
+    sp, nrec, work = _abi.plan_splits_mla(w.seq_lens, w.H, mp, 152)
+    npg = w.pages_per_seq.astype(int)
+    assert sp.shape == (w.B,) and (sp >= 1).all() and nrec == int(sp.max())
+    items = [(int(e) >> 12, int(e) & 0xFFF, int(p0)) for e, p0 in work]
+    assert sorted((b, s) for b, s, _ in items) == [(b, s) for b in range(w.B) for s in range(int(sp[b]))]
+    pages = [_mla_plan_pages(npg[b], int(sp[b]))[s] for b, s, _ in items]
+    assert all(x >= y for x, y in zip(pages, pages[1:]))
+    for b in range(w.B):
+        if npg[b]:
+            assert all(p > 0 for p in _mla_plan_pages(npg[b], int(sp[b])))
+    if len(work) <= 2 * 152:
+        # one item per CTA at most: the longest item is as short as an even page
+        # target allows (one target lower would need more items than CTAs)
+        T = max(pages)
+        T = T + (T & 1)
+        if T > 2:
+            n_lower = sum(-(-int(n) // (T - 2)) if n else 1 for n in npg)
+            assert n_lower > 2 * 152
+
+
+def test_mla_split_plan_with_a_page_target_and_bad_arguments(lib):
+    lens = np.array([0, 1, 64, 65, 640, 641, 9000, 33], np.int32)
+    npg = (lens.astype(int) + 63) // 64
+    for T in (1, 2, 4, 100):
+        sp, nrec, work = _abi.plan_splits_mla(lens, 16, 200, 152, 4095, T)
+        assert len(work) == int(sp.sum())
+        for b in range(len(lens)):
+            assert max(_mla_plan_pages(npg[b], int(sp[b]))) <= T
+    f = lib.pkv_plan_splits_mla
+    sp = np.zeros(len(lens), np.int32)
+    nrec, nwork = ctypes.c_int32(0), ctypes.c_int64(0)
+
+    def call(B=len(lens), H=16, mp=200, sms=152, ms=4095, T=0, work=None, cap=0):
+        return f(lens.ctypes.data, B, H, mp, sms, ms, T, sp.ctypes.data, ctypes.byref(nrec), work, cap,
+                 ctypes.byref(nwork))
+    assert call() == _abi.PKV_OK and nwork.value == int(sp.sum())
+    assert call(ms=0) == _abi.PKV_ERR_INVALID_ARG and call(ms=4096) == _abi.PKV_ERR_INVALID_ARG
+    assert call(T=-1) == _abi.PKV_ERR_INVALID_ARG and call(B=-1) == _abi.PKV_ERR_INVALID_ARG
+    small = np.zeros((1, 2), np.int32)
+    assert call(work=small.ctypes.data, cap=1) == _abi.PKV_ERR_INVALID_ARG
+
+
+def test_planned_mla_decode_rejects_inconsistent_arguments(lib):
+    B, H, S = 3, 16, 4
+    ql = _t((B, H, 512), "bf16")
+    qp = _t((B, H, 64), "bf16")
+    ckv = _t((50, 64, 512), "fp8")
+    kpe = _t((50, 64, 64), "bf16")
+    bt = _t((B, 10), "i32")
+    sl = _t((B,), "i32")
+    op = _t((B, S, H, 512), "f32")
+    lp = _t((B, S, H), "f32")
+    sc = _t((1,), "f32")
+
+    def dec(sp=_t((B,), "i32"), wk=_t((7, 2), "i32"), op=op, lp=lp):
+        return lib.pkv_paged_mla_decode_planned(ql, qp, ckv, kpe, bt, sl, 0.05, sp, wk, op, lp, sc, None, None)
+    assert dec(sp=_t((B + 1,), "i32")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(sp=_t((B,), "f32")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(wk=_t((7, 3), "i32")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(wk=_t((7,), "i32")) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(sp=None) == _abi.PKV_ERR_INVALID_ARG and dec(wk=None) == _abi.PKV_ERR_INVALID_ARG
+    assert dec(op=_t((B, 4096, H, 512), "f32"), lp=_t((B, 4096, H), "f32")) == _abi.PKV_ERR_UNSUPPORTED
+    assert dec(lp=_t((B, S + 1, H), "f32")) == _abi.PKV_ERR_INVALID_ARG

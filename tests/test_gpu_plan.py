@@ -203,3 +203,82 @@ def test_planned_steps_back_to_back_and_as_graphs_match_one_step():
     same()
     assert np.array_equal(g2.out_h.view(torch.int16).numpy().view(np.uint16), ref_out)
     assert int(dw.err.item()) == 0
+
+
+# ---- split plans of the MLA decode -----------------------------------------------------
+from tests._pipeline import mla_oracle_step  # noqa: E402
+
+MLA_CASES = [
+    pytest.param("mla_tiny", (0, 2, 4), {}, id="mla_tiny"),
+    pytest.param("ragged_h16", (0, 2, 6), dict(seq_lens=[1, 63, 64, 65, 200, 900, 0], H=16, style="neox"),
+                 id="ragged_h16"),
+    pytest.param("h5", (0, 4), dict(seq_lens=[100, 257, 1500], H=5), id="h5"),
+]
+
+
+def _check_mla_planned(w, dw, seqs=None):
+    seqs = list(range(w.B)) if seqs is None else list(seqs)
+    sp_all, _ = dw.plan_host
+    st = mla_oracle_step(w, seqs=seqs, num_splits=1)
+    sp = sp_all[seqs]
+    op, lp = oracle.mla_decode(st["q_lat"], st["q_pe_rot"], st["ckv_cache"], st["kpe_cache"], st["block_tables"],
+                               st["seq_lens"], w.softmax_scale, dw.num_splits, w.ckv_scale, splits_per_seq=sp)
+    out, lse = oracle.lse_merge(op, lp)
+    gop = dw.out_partial.cpu().numpy()
+    glp = dw.lse_partial.cpu().numpy()
+    for i, b in enumerate(seqs):
+        n = int(sp[i])
+        assert_close_out(gop[b, :n], op[i, :n], f"out_partial of sequence {b}")
+        assert_close_lse(glp[b, :n], lp[i, :n], f"lse_partial of sequence {b}")
+    assert_close_out(bf16_u16_to_f64(dw.bf16_u16(dw.out))[seqs], out, "out")
+    assert_close_lse(dw.lse.cpu().numpy()[seqs], lse, "lse")
+
+
+@pytest.mark.parametrize("name,targets,kw", MLA_CASES)
+def test_planned_mla_decode_parity(name, targets, kw):
+    w = synth.make_mla_workload("mla_tiny") if name == "mla_tiny" else synth.custom_mla_workload(name, 135, **kw)
+    dw = harness.MlaDeviceWorkload(w, num_splits=1)
+    dw.fill()
+    dw.upload_decode()
+    d = dw.decode_inputs
+    for T in targets:
+        dw.set_plan(target_pages=T)
+        sp, work = dw.plan_host
+        items = sorted((int(e) >> 12, int(e) & 0xFFF) for e in work[:, 0])
+        assert items == [(b, s) for b in range(w.B) for s in range(int(sp[b]))]
+        d["q"].copy_(d["q0"])
+        dw.err.zero_()
+        dw.step()
+        torch.cuda.synchronize()
+        assert int(dw.err.item()) == 0
+        _check_mla_planned(w, dw)
+
+
+def test_planned_mla_decode_full_size_sampled():
+    w = synth.make_mla_workload("mla_batch")
+    dw = harness.MlaDeviceWorkload(w)
+    dw.fill()
+    dw.upload_decode()
+    dw.set_plan()
+    dw.err.zero_()
+    dw.step()
+    torch.cuda.synchronize()
+    assert int(dw.err.item()) == 0
+    L = w.seq_lens
+    _check_mla_planned(w, dw, sorted({int(np.argmax(L)), int(np.argmin(L)), int(w.B // 2)}))
+
+
+def test_bad_mla_plan_entries_are_flagged_and_skipped():
+    w = synth.custom_mla_workload("badmla", 136, [300, 100], 4)
+    dw = harness.MlaDeviceWorkload(w, num_splits=1)
+    dw.fill()
+    dw.upload_decode()
+    dw.set_plan(target_pages=2)
+    sp, work = dw.plan_host
+    bad = np.concatenate([work, np.array([[(9 << 12) | 0, 0], [(1 << 12) | 4000, 0], [-7, 0]], np.int32)])
+    dw.work = torch.from_numpy(bad).cuda()
+    dw.err.zero_()
+    dw.step()
+    torch.cuda.synchronize()
+    assert int(dw.err.item()) == _abi.FLAG_PLAN_RANGE
+    _check_mla_planned(w, dw)
