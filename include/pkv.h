@@ -470,8 +470,9 @@ pkv_status pkv_plan_splits_mla(const int32_t* seq_lens, int32_t B, int32_t H, in
  * lse_partial [B, S, H] with S >= every S_b, S <= 4095. Each written record
  * is that of pkv_paged_mla_decode with S_b splits; records [S_b, S) of
  * sequence b are not written. Merge with pkv_lse_merge_planned (D = 512).
- * Errors: besides pkv_paged_mla_decode's, items outside the batch or the
- * records are skipped and set PKV_FLAG_PLAN_RANGE.
+ * Errors: besides pkv_paged_mla_decode's, an item whose sequence is outside
+ * [0, B) or whose split is >= S is skipped and S_b outside [1, S], or an
+ * item with s >= S_b, sets PKV_FLAG_PLAN_RANGE (S_b is clamped).
  */
 pkv_status pkv_paged_mla_decode_planned(const pkv_tensor* q_lat, const pkv_tensor* q_pe, const pkv_tensor* ckv_cache,
                                         const pkv_tensor* kpe_cache, const pkv_tensor* block_tables,

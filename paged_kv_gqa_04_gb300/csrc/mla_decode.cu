@@ -172,13 +172,14 @@ struct Item {
     int nch;              // chunks of the split
     bool bad_len;         // seq_lens[b] outside [0, block-table width x page]
     bool planless;        // a plan entry outside the batch or the records: no record, no work
+    bool plan_bad;        // S_b outside [1, records] (clamped) or s >= S_b (an empty record)
     const int32_t* bt;    // the split's block-table entries
 };
 
 __device__ __forceinline__ Item item_of(const MlaDecodeArgs& a, int it) {
     Item x;
     int S = a.num_splits;
-    x.planless = false;
+    x.planless = x.plan_bad = false;
     if (a.work == nullptr) {
         x.b = it / a.num_splits;
         x.s = it - x.b * a.num_splits;
@@ -194,7 +195,9 @@ __device__ __forceinline__ Item item_of(const MlaDecodeArgs& a, int it) {
             x.bt = a.block_tables;
             return x;
         }
-        S = min(max(__ldg(a.splits_per_seq + x.b), 1), a.num_splits);
+        const int r = __ldg(a.splits_per_seq + x.b);
+        S = min(max(r, 1), a.num_splits);
+        x.plan_bad = r != S || x.s >= S;
     }
     const int L0 = __ldg(a.seq_lens + x.b);
     const int cap = a.max_pages * kMlaPage;
@@ -613,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const int it = slot_item(a, order, j, n_items);
                 if (it >= n_items) return j;
                 const Item y = item_of(a, it);
-                if (i == 0 && y.planless) flag_error(a.err, PKV_FLAG_PLAN_RANGE);
+                if (i == 0 && (y.planless || y.plan_bad)) flag_error(a.err, PKV_FLAG_PLAN_RANGE);
                 if (y.planless) continue;
                 if (i == 0 && y.s == 0 && y.bad_len) flag_error(a.err, PKV_FLAG_SEQ_LEN_RANGE);
                 if (y.nch > 0) return j;

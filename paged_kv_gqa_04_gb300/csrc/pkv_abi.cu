@@ -1060,15 +1060,23 @@ pkv_status pkv_plan_splits_mla(const int32_t* seq_lens, int32_t B, int32_t H, in
                                                           sm_count);
             T = (top + S_u - 1) / S_u;
         } else {
-            T = top;
-            for (int64_t Tc = 2; Tc < top; Tc += 2) {
+            // The item count does not grow with the target: bisect over the
+            // even targets below the longest sequence (T = top gives B items).
+            auto fits = [&](int64_t Tc) {
                 int64_t items = 0;
                 for (int b = 0; b < B && items <= ctas; ++b) items += plan_count(np[b], Tc, max_splits);
-                if (items <= ctas) {
-                    T = Tc;
-                    break;
-                }
+                return items <= ctas;
+            };
+            int64_t lo = 1, hi = (top + 1) / 2;  // even targets 2 lo .. 2 hi; 2 hi >= top fits
+            if (fits(2)) hi = 1;
+            while (hi - lo > 1) {  // fits(2 hi) holds, fits(2 lo) does not
+                const int64_t mid = lo + (hi - lo) / 2;
+                if (fits(2 * mid))
+                    hi = mid;
+                else
+                    lo = mid;
             }
+            T = std::min<int64_t>(2 * hi, top);
         }
     }
     return plan_emit(np, T, max_splits, splits_per_seq, num_records, work, work_capacity, num_work);

@@ -282,3 +282,12 @@ def test_bad_mla_plan_entries_are_flagged_and_skipped():
     torch.cuda.synchronize()
     assert int(dw.err.item()) == _abi.FLAG_PLAN_RANGE
     _check_mla_planned(w, dw)
+    # a split count of 0 is taken as 1 (and flagged)
+    sp0 = sp.copy()
+    sp0[1] = 0
+    dw.splits_per_seq = torch.from_numpy(sp0).cuda()
+    dw.err.zero_()
+    dw.decode_inputs["q"].copy_(dw.decode_inputs["q0"])
+    dw.step()
+    torch.cuda.synchronize()
+    assert int(dw.err.item()) & _abi.FLAG_PLAN_RANGE
