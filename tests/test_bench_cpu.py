@@ -65,3 +65,10 @@ def test_byte_counts_of_the_roofline():
     per = 2 * Hkv * D * 2 + 2 * Hkv * D * 2 + 8
     assert bench.write_alg_bytes(w, T, False) == T * per + T * D * 4
     assert bench.write_alg_bytes(w, T, False, rows) == T * per + rows * D * 4
+
+
+def test_launch_mean_leaves_out_host_stalls_only():
+    m, out = bench.launch_mean([0.25, 0.26, 0.255, 61.3, 0.25])
+    assert out == 1 and abs(m - 0.25375) < 1e-12
+    m, out = bench.launch_mean([1.0, 1.9, 1.5])       # within twice the median: all kept
+    assert out == 0 and abs(m - 1.4666666666666666) < 1e-12
