@@ -498,7 +498,8 @@ def measure_layered(dw, layers: int, reps: int, flush, peak: float) -> dict:
     for _ in range(layers - 1):
         caches.append(tuple(c.clone() for c in dw.caches()))
     d = dw.decode_inputs
-    outs = [(torch.empty_like(dw.out_partial), torch.empty_like(dw.lse_partial)) for _ in range(layers)]
+    # zeroed, so that records a split plan leaves unwritten compare equal
+    outs = [(torch.zeros_like(dw.out_partial), torch.zeros_like(dw.lse_partial)) for _ in range(layers)]
 
     def group():
         for cs, (op, lp) in zip(caches, outs):
@@ -514,7 +515,7 @@ def measure_layered(dw, layers: int, reps: int, flush, peak: float) -> dict:
     torch.cuda.synchronize()
     ms = statistics.median(a.elapsed_time(b) for a, b in ev)
     gbs = layers * decode_alg_bytes(w) / (ms * 1e-3) / 1e9
-    ok = all(torch.equal(op, outs[0][0]) for op, _ in outs[1:])
+    ok = all(torch.equal(op, outs[0][0]) and torch.equal(lp, outs[0][1]) for op, lp in outs[1:])
     del caches, outs
     return dict(layers=layers, us_per_layer=1e3 * ms / layers, gbs=gbs, frac=gbs / peak, layers_agree=ok)
 
