@@ -776,9 +776,10 @@ def run_reference(args, world, rank):
     S = args.splits or 1
     import oracle
     oracle.build()
-    # size the per-step sample so that warm-up + timed steps take about a minute
-    probe_seqs = quantile_sample(w, 1)
-    t1 = oracle_step_timer(w, probe_seqs, S)()
+    # size the per-step sample so that warm-up + timed steps take about a
+    # minute, from the time per sequence of a probe at four length quantiles
+    probe_seqs = quantile_sample(w, min(4, w.B))
+    t1 = oracle_step_timer(w, probe_seqs, S)() / max(1, len(probe_seqs))
     n = int(max(1, min(w.B, round(60.0 / max(1, args.steps + args.warmup) / max(t1, 1e-6)))))
     seqs = quantile_sample(w, n)
     run = oracle_step_timer(w, seqs, S)
