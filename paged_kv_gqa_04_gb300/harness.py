@@ -361,7 +361,7 @@ class MlaDeviceWorkload:
     def planned(self) -> bool:
         return self.work is not None
 
-    def fill(self, max_tokens: int = 1 << 17) -> int:
+    def fill(self, max_tokens: int = 1 << 18) -> int:
         """Context tokens 0..L-2 of every sequence through the library's MLA
         cache write (no q_pe), in chunks of whole sequences."""
         w = self.w

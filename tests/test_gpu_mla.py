@@ -96,6 +96,30 @@ def test_mla_full_size_sampled(name):
     _compare(w, dw, mla_oracle_step(w, seqs=seqs, num_splits=dw.num_splits), seqs)
 
 
+def test_mla_fill_in_one_call_two_tokens_per_thread():
+    """One cache-write call over every context token of the mla_batch
+    workload (319,783 tokens: from 131,072 tokens on, the launcher gives each
+    thread two tokens) writes the oracle's bytes; sampled sequences include
+    the last one (the ragged end of the grid)."""
+    w = synth.make_mla_workload("mla_batch")
+    dw = harness.MlaDeviceWorkload(w)
+    fi = dw.fill_inputs()
+    assert int(fi["positions"].numel()) >= 131072
+    dw.err.zero_()
+    dw.write_fill(fi)
+    torch.cuda.synchronize()
+    assert int(dw.err.item()) == 0
+    L = w.seq_lens
+    seqs = sorted({0, int(w.B // 2), int(w.B - 1), int(np.argmax(L))})
+    st = mla_oracle_step(w, seqs=seqs, num_splits=1)
+    for i, b in enumerate(seqs):
+        n = int(w.pages_per_seq[b])
+        for gc, oc in ((dw.ckv_cache, st["ckv_cache"]), (dw.kpe_cache, st["kpe_cache"])):
+            got = dw.cache_pages_u(gc, w.block_tables[b, :n]).reshape(n * w.page_size, -1)[:int(L[b]) - 1]
+            want = oc[st["block_tables"][i, :n]].reshape(n * w.page_size, -1)[:int(L[b]) - 1]
+            assert np.array_equal(got, want), f"cache bytes of sequence {b}"
+
+
 def test_mla_bad_page_and_seq_len_are_flagged():
     w = synth.custom_mla_workload("bad", 17, [200, 100], 8, num_pages=8)
     dw = harness.MlaDeviceWorkload(w, num_splits=2)

@@ -254,8 +254,11 @@ def test_planned_mla_decode_parity(name, targets, kw):
         _check_mla_planned(w, dw)
 
 
-def test_planned_mla_decode_full_size_sampled():
-    w = synth.make_mla_workload("mla_batch")
+@pytest.mark.parametrize("name", ["mla", "mla_batch"])
+def test_planned_mla_decode_full_size_sampled(name):
+    """The automatic MLA plan on a full-size workload (mla: 200 records of
+    one sequence, merged by the two-level tree)."""
+    w = synth.make_mla_workload(name)
     dw = harness.MlaDeviceWorkload(w)
     dw.fill()
     dw.upload_decode()
