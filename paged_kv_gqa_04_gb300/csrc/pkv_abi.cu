@@ -898,11 +898,14 @@ namespace {
 // The split count of a sequence of n pages under a target of T pages per
 // split, at most max_splits, reduced to the splits that hold pages when that
 // keeps the same page ranges.
-int64_t plan_count(int64_t n, int64_t T, int max_splits) {
-    if (n <= 0) return 1;
-    const int64_t S = std::min<int64_t>((n + T - 1) / T, max_splits);
-    const int64_t pps = (n + S - 1) / S;
-    const int64_t k = (n + pps - 1) / pps;
+// Page counts and targets stay below 2^26 (the block-table width limit), so
+// the arithmetic is done in 32 bits. The count does not grow with T.
+int64_t plan_count(int64_t n64, int64_t T64, int max_splits) {
+    if (n64 <= 0) return 1;
+    const int32_t n = static_cast<int32_t>(n64), T = static_cast<int32_t>(std::min<int64_t>(T64, n64));
+    const int32_t S = std::min<int32_t>((n + T - 1) / T, max_splits);
+    const int32_t pps = (n + S - 1) / S;
+    const int32_t k = (n + pps - 1) / pps;
     return ((n + k - 1) / k == pps) ? k : S;
 }
 
@@ -1010,9 +1013,28 @@ pkv_status pkv_plan_splits(const int32_t* seq_lens, int32_t B, int32_t Hkv, int3
                                                       static_cast<int32_t>(top), cache_dtype, sm_count);
             T = (top + S_u - 1) / S_u;
         } else {
+            // The targets whose CTAs exceed one wave are skipped: the item
+            // count does not grow with the target, so the smallest target that
+            // fits is found by bisection and the search starts there.
+            const int64_t cap = static_cast<int64_t>(slots) / Hkv;
+            auto fits = [&](int64_t Tc) {
+                int64_t it = 0;
+                for (int b = 0; b < B && it <= cap; ++b) it += plan_count(np[b], Tc, max_splits);
+                return it <= cap;
+            };
+            int64_t lo = 0, hi = top;  // fits(top): B items, and B * Hkv <= slots here
+            while (hi - lo > 1) {
+                const int64_t mid = lo + (hi - lo) / 2;
+                if (fits(mid))
+                    hi = mid;
+                else
+                    lo = mid;
+            }
+            const int64_t T_fit = hi;
             double best_cost = 1e300;
             int64_t best_T = top;
             for (int64_t Tc = 1; Tc <= top; Tc = Tc < 64 ? Tc + 1 : std::max<int64_t>(Tc + 1, static_cast<int64_t>(Tc * 1.05))) {
+                if (Tc < T_fit) continue;
                 double items = 0, p_max = 0;
                 int64_t recs = 1;
                 for (int b = 0; b < B; ++b) {
