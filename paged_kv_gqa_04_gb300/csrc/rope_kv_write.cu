@@ -152,6 +152,24 @@ __device__ __forceinline__ float amax8(const Chunk8& c) {
 // leave float32's normal range are marked for the division path.
 __device__ __forceinline__ E4m3Rcp bracket_rcp(float d) { return e4m3_rcp(d); }
 
+// The same brackets from the hardware's approximate reciprocal r ~ 1/d
+// (rcp.approx.f32, documented within one unit in the last place; measured on
+// GB300 over every float32 in [2^-30, 2^30): relative error at most
+// 2^-23.27). With
+// |r d - 1| < 2^-22 the products RN(y RN(r (1 -+ 2^-20))) still differ from
+// y / d by factors within (1 -+ 2^-20)(1 +- 2^-22)(1 +- 2^-24)^2, i.e.
+// strictly beyond the 1 +- 2^-24 of RN(y / d) on each side, so they still
+// enclose it. Used for the per-block divisors of the NVFP4 quantiser.
+__device__ __forceinline__ E4m3Rcp bracket_rcp_approx(float d) {
+    E4m3Rcp r;
+    r.exact_only = !(d >= 0x1p-100f && d <= 0x1p100f);
+    float rcp;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(rcp) : "f"(d));
+    r.lo = __fmul_rn(rcp, 1.0f - 0x1p-20f);
+    r.hi = __fmul_rn(rcp, 1.0f + 0x1p-20f);
+    return r;
+}
+
 // One 8-value half of an NVFP4 block whose largest magnitude is `amax`,
 // under the static scale g (six_g = RN(6 g), r6 = bracket_rcp(six_g)):
 // returns the four bytes of E2M1 pairs and the block's E4M3 scale byte,
@@ -174,7 +192,7 @@ __device__ __forceinline__ uint32_t nvfp4_half(const Chunk8& c, float amax, floa
     const float s = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sb), __NV_E4M3)));
     if (s == 0.f) return 0u;
     const float denom = __fmul_rn(g, s);
-    const E4m3Rcp r = bracket_rcp(denom);
+    const E4m3Rcp r = bracket_rcp_approx(denom);
     float zl[8], zh[8];
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
