@@ -70,8 +70,8 @@ __device__ __forceinline__ uint4 pack_bf16x8(const Chunk8& c) {
 
 // Packed float32 product (sm_100+ f32x2 arithmetic): each lane is rounded
 // exactly as the scalar product would be, in one issue slot for two values.
-// Used only where no sum follows the product (the quantisers' scalings),
-// so there is nothing it could be contracted with.
+// Where a sum follows (the rotation), the sum is a scalar operation with
+// explicit rounding, which is never contracted with the product.
 __device__ __forceinline__ void mul_rn_x2(float a0, float a1, float b0, float b1, float& d0, float& d1) {
     asm("{\n\t.reg .b64 a, b, d;\n\t"
         "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
@@ -237,37 +237,42 @@ __device__ __forceinline__ void load_cos_sin(const float* cs, int c, float (&cv)
     sv[4] = b1.x; sv[5] = b1.y; sv[6] = b1.z; sv[7] = b1.w;
 }
 
-__device__ __forceinline__ void rot(float x1, float x2, float c, float s, float& y1, float& y2) {
-    y1 = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s));
-    y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
-}
-
 // y1 = x1 c - x2 s, y2 = x2 c + x1 s for every pair of the row's two chunks,
-// each product and the sum / difference rounded on its own. Scalar
-// operations with explicit rounding: these are never contracted into a
-// fused multiply-add. (The packed f32x2 forms are not used here: the
-// compiler may contract a packed product with the packed sum that reads
-// it, which changes the rounding.)
+// each product and the sum / difference rounded on its own, never fused:
+// the products are packed f32x2 multiplies (two per instruction, explicit
+// round-to-nearest), the sums and differences scalar operations with
+// explicit rounding. (A packed sum reading a packed product may be
+// contracted into a fused multiply-add by the compiler, which changes the
+// rounding; the scalar forms are not.)
 template <bool INTER>
 __device__ __forceinline__ void rotate_row(Chunk8& lo, Chunk8& hi, const float (&cv)[8], const float (&sv)[8]) {
     if constexpr (!INTER) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float y1, y2;
-            rot(lo.v[j], hi.v[j], cv[j], sv[j], y1, y2);
-            lo.v[j] = y1;
-            hi.v[j] = y2;
+        for (int j = 0; j < 8; j += 2) {
+            float lc0, lc1, hs0, hs1, hc0, hc1, ls0, ls1;
+            mul_rn_x2(lo.v[j], lo.v[j + 1], cv[j], cv[j + 1], lc0, lc1);
+            mul_rn_x2(hi.v[j], hi.v[j + 1], sv[j], sv[j + 1], hs0, hs1);
+            mul_rn_x2(hi.v[j], hi.v[j + 1], cv[j], cv[j + 1], hc0, hc1);
+            mul_rn_x2(lo.v[j], lo.v[j + 1], sv[j], sv[j + 1], ls0, ls1);
+            lo.v[j] = __fsub_rn(lc0, hs0);
+            lo.v[j + 1] = __fsub_rn(lc1, hs1);
+            hi.v[j] = __fadd_rn(hc0, ls0);
+            hi.v[j + 1] = __fadd_rn(hc1, ls1);
         }
     } else {
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            float y1, y2;
-            rot(lo.v[2 * m], lo.v[2 * m + 1], cv[m], sv[m], y1, y2);
-            lo.v[2 * m] = y1;
-            lo.v[2 * m + 1] = y2;
-            rot(hi.v[2 * m], hi.v[2 * m + 1], cv[4 + m], sv[4 + m], y1, y2);
-            hi.v[2 * m] = y1;
-            hi.v[2 * m + 1] = y2;
+            float p0, p1, q0, q1;
+            // lo pair (2m, 2m + 1) at frequency m
+            mul_rn_x2(lo.v[2 * m], lo.v[2 * m + 1], cv[m], cv[m], p0, p1);
+            mul_rn_x2(lo.v[2 * m + 1], lo.v[2 * m], sv[m], sv[m], q0, q1);
+            lo.v[2 * m] = __fsub_rn(p0, q0);
+            lo.v[2 * m + 1] = __fadd_rn(p1, q1);
+            // hi pair at frequency 4 + m
+            mul_rn_x2(hi.v[2 * m], hi.v[2 * m + 1], cv[4 + m], cv[4 + m], p0, p1);
+            mul_rn_x2(hi.v[2 * m + 1], hi.v[2 * m], sv[4 + m], sv[4 + m], q0, q1);
+            hi.v[2 * m] = __fsub_rn(p0, q0);
+            hi.v[2 * m + 1] = __fadd_rn(p1, q1);
         }
     }
 }
