@@ -527,7 +527,7 @@ def make_workload(name: str, splits: int, split_mode: str):
     from paged_kv_gqa_04_gb300 import harness
     dw = harness.make_device_workload(name, num_splits=splits or None)
     if not splits and split_mode == "plan":
-        dw.set_plan()
+        dw.set_plan(uniform_if_equal=True)  # a plan with one count for every sequence runs as the uniform launch
     return dw
 
 
@@ -542,6 +542,8 @@ def split_desc(dw) -> dict:
         return {"mode": "plan", "records": dw.num_splits, "items": int(len(work)),
                 "ctas": ctas, "splits_per_seq_min": int(sp.min()),
                 "splits_per_seq_max": int(sp.max()), "max_pages_per_split": int(pps.max())}
+    if getattr(dw, "uniform_from_plan", False):
+        return {"mode": "uniform", "records": dw.num_splits, "from_plan": True}
     return {"mode": "uniform", "records": dw.num_splits}
 
 

@@ -67,19 +67,25 @@ class DeviceWorkload:
         """One split count for every sequence (drops any split plan)."""
         w = self.w
         self.splits_per_seq = self.work = None
+        self.uniform_from_plan = False
         self.num_splits = int(num_splits)
         self.out_partial = torch.empty((w.B, self.num_splits, w.Hq, w.D), dtype=torch.float32, device=self.device)
         self.lse_partial = torch.empty((w.B, self.num_splits, w.Hq), dtype=torch.float32, device=self.device)
 
-    def set_plan(self, target_pages: int = 0, max_splits: int = 4095) -> None:
+    def set_plan(self, target_pages: int = 0, max_splits: int = 4095, uniform_if_equal: bool = False) -> None:
         """A split count per sequence from the library's planner (host
         seq_lens), uploaded with its work list; the partials get the plan's
-        record count."""
+        record count. With uniform_if_equal, a plan that gives every
+        sequence the same count runs as the uniform launch with that count
+        (the same records, without the work list's extra read)."""
         w = self.w
         props = torch.cuda.get_device_properties(self.device)
         sp, nrec, work = _abi.plan_splits(w.seq_lens, w.Hkv, w.Hq, w.D, max(1, w.max_pages), w.cache_dtype,
                                           props.multi_processor_count, max_splits, target_pages)
         self.set_splits(nrec)
+        if uniform_if_equal and w.B and bool((sp == nrec).all()):
+            self.uniform_from_plan = True
+            return
         self.plan_host = (sp, work)
         self.splits_per_seq = torch.from_numpy(sp).to(self.device)
         self.work = torch.from_numpy(np.ascontiguousarray(work)).to(self.device)
@@ -341,18 +347,23 @@ class MlaDeviceWorkload:
         """One split count for every sequence (drops any split plan)."""
         w = self.w
         self.splits_per_seq = self.work = None
+        self.uniform_from_plan = False
         self.num_splits = int(num_splits)
         self.out_partial = torch.empty((w.B, self.num_splits, w.H, w.Dc), dtype=torch.float32, device=self.device)
         self.lse_partial = torch.empty((w.B, self.num_splits, w.H), dtype=torch.float32, device=self.device)
 
-    def set_plan(self, target_pages: int = 0, max_splits: int = 4095) -> None:
+    def set_plan(self, target_pages: int = 0, max_splits: int = 4095, uniform_if_equal: bool = False) -> None:
         """A split count per sequence from the library's MLA planner (host
-        seq_lens), uploaded with its work list."""
+        seq_lens), uploaded with its work list (uniform_if_equal: as
+        DeviceWorkload.set_plan)."""
         w = self.w
         props = torch.cuda.get_device_properties(self.device)
         sp, nrec, work = _abi.plan_splits_mla(w.seq_lens, w.H, max(1, int(w.block_tables.shape[1])),
                                               props.multi_processor_count, max_splits, target_pages)
         self.set_splits(nrec)
+        if uniform_if_equal and w.B and bool((sp == nrec).all()):
+            self.uniform_from_plan = True
+            return
         self.plan_host = (sp, work)
         self.splits_per_seq = torch.from_numpy(sp).to(self.device)
         self.work = torch.from_numpy(np.ascontiguousarray(work)).to(self.device)
