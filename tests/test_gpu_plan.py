@@ -294,3 +294,33 @@ def test_bad_mla_plan_entries_are_flagged_and_skipped():
     dw.step()
     torch.cuda.synchronize()
     assert int(dw.err.item()) & _abi.FLAG_PLAN_RANGE
+
+
+def test_large_batch_of_short_sequences_uniform_and_planned():
+    """8,192 sequences of 0 to 80 tokens (grids of 8,192 x S x Hkv CTAs for
+    the uniform launch and a work list of about 8,000 items under a plan):
+    sampled sequences, including empty and one-token ones, against the
+    oracle in both forms."""
+    rng = np.random.default_rng(137)
+    lens = rng.integers(0, 81, 8192).astype(np.int32)
+    lens[:4] = [0, 1, 16, 17]
+    w = synth.custom_workload("bigbatch", 137, lens, 8, 2, 128)
+    dw = harness.DeviceWorkload(w, num_splits=2)
+    dw.fill()
+    d = dw.upload_decode()
+    seqs = sorted({0, 1, 2, 3, 4097, 8191, int(np.argmax(lens))})
+    dw.err.zero_()
+    dw.step()
+    torch.cuda.synchronize()
+    assert int(dw.err.item()) == 0
+    st = oracle_step(w, seqs=seqs, num_splits=2)
+    out = bf16_u16_to_f64(dw.bf16_u16(dw.out))
+    assert_close_out(out[seqs], st["out"], "out (uniform)")
+    assert_close_lse(dw.lse.cpu().numpy()[seqs], st["lse"], "lse (uniform)")
+    dw.set_plan(target_pages=2)
+    d["q"].copy_(d["q0"])
+    dw.err.zero_()
+    dw.step()
+    torch.cuda.synchronize()
+    assert int(dw.err.item()) == 0
+    _check_planned(w, dw, seqs)
